@@ -1,0 +1,71 @@
+// api.cu -- status reporting shared by every entry point of libcla.so.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "cla_internal.cuh"
+
+namespace cla {
+
+static thread_local char g_msg[512] = "";
+
+int fail(int status, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+void clear_error() { g_msg[0] = '\0'; }
+
+int check_launch(const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(CLA_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+    return CLA_OK;
+}
+
+}  // namespace cla
+
+extern "C" const char *cla_status_string(int status) {
+    switch (status) {
+        case CLA_OK: return "CLA_OK";
+        case CLA_ERR_INVALID_ARG: return "CLA_ERR_INVALID_ARG";
+        case CLA_ERR_UNSUPPORTED: return "CLA_ERR_UNSUPPORTED";
+        case CLA_ERR_CUDA: return "CLA_ERR_CUDA";
+        case CLA_ERR_TIMEOUT: return "CLA_ERR_TIMEOUT";
+        case CLA_ERR_WORKSPACE: return "CLA_ERR_WORKSPACE";
+        default: return "CLA_ERR_UNKNOWN";
+    }
+}
+
+extern "C" const char *cla_last_error_message(void) { return cla::g_msg; }
+
+namespace cla {
+namespace {
+// Waits on a header word that nothing sets: exercises the bounded wait.
+__global__ void selftest_wait_kernel(WsHeader *hdr) {
+    if (threadIdx.x == 0) (void)wait_flag(&hdr->pad[0], hdr, 99u);
+}
+}  // namespace
+}  // namespace cla
+
+extern "C" int cla_selftest_wait_timeout(void *ws, size_t ws_bytes, void *stream) {
+    cla::clear_error();
+    if (ws == nullptr || ws_bytes < sizeof(cla::WsHeader) || !cla::aligned16(ws))
+        return cla::fail(CLA_ERR_WORKSPACE, "cla_selftest_wait_timeout: need a 256-byte aligned workspace");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(cla::WsHeader), s), "cla_selftest_wait_timeout");
+    cla::selftest_wait_kernel<<<1, 32, 0, s>>>(static_cast<cla::WsHeader *>(ws));
+    return cla::check_launch("cla_selftest_wait_timeout");
+}
+
+extern "C" int cla_check_status(const void *ws, void *stream) {
+    if (ws == nullptr) return cla::fail(CLA_ERR_INVALID_ARG, "cla_check_status: ws is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cla::WsHeader hdr;
+    CLA_CUDA_TRY(cudaMemcpyAsync(&hdr, ws, sizeof(hdr), cudaMemcpyDeviceToHost, s), "cla_check_status: copy");
+    CLA_CUDA_TRY(cudaStreamSynchronize(s), "cla_check_status: synchronize");
+    if (hdr.error & cla::kErrTimeout)
+        return cla::fail(CLA_ERR_TIMEOUT, "a cross-block wait gave up (site %u)", hdr.where);
+    return CLA_OK;
+}

@@ -1,0 +1,79 @@
+// cla_internal.cuh -- shared host and device plumbing of libcla.so:
+// status reporting, the workspace header, and the release/acquire flag
+// protocol used by every cross-block carry (decoupled look-back).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/cla.h"
+
+namespace cla {
+
+// ----------------------------------------------------------------- host side
+// Records a one-line description for cla_last_error_message() and returns
+// the status unchanged.
+int fail(int status, const char *fmt, ...);
+int check_launch(const char *what);  // cudaGetLastError -> CLA_OK / CLA_ERR_CUDA
+void clear_error();
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned16_or_null(const void *p) { return p == nullptr || aligned16(p); }
+
+// Every workspace starts with this header.  It is cleared (with the flag
+// arrays that follow it) by one cudaMemsetAsync at the start of each call.
+struct WsHeader {
+    unsigned int ticket[8];   // per-kernel atomic tickets: block order of start
+    unsigned int error;       // nonzero: a bounded wait gave up
+    unsigned int where;       // which wait gave up (debug aid)
+    unsigned int pad[54];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+constexpr unsigned int kErrTimeout = 1u;
+
+// Bound on polls of one flag (each poll after the first few sleeps ~100 ns):
+// about a second before a block gives up, far beyond any legitimate wait.
+constexpr unsigned int kSpinLimit = 1u << 23;
+
+// ----------------------------------------------------------------- device side
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned int *p, unsigned int v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Loads that must observe another block's stores made visible by a release
+// on a flag we acquired: bypass L1 (data written by other SMs).
+__device__ __forceinline__ float4 ld_cg4(const float4 *p) { return __ldcg(p); }
+__device__ __forceinline__ float ld_cg(const float *p) { return __ldcg(p); }
+
+// Polls *flag until it is nonzero, at most kSpinLimit times.  On giving up
+// records kErrTimeout in the header and returns 0; callers then proceed
+// with a neutral value so that no other block waits on them forever.
+__device__ __forceinline__ unsigned int wait_flag(const unsigned int *flag, WsHeader *hdr,
+                                                  unsigned int where) {
+    for (unsigned int it = 0; it < kSpinLimit; ++it) {
+        unsigned int v = ld_acquire(flag);
+        if (v != 0u) return v;
+        if (it >= 8) __nanosleep(100);
+    }
+    atomicOr(&hdr->error, kErrTimeout);
+    atomicExch(&hdr->where, where);
+    return 0u;
+}
+
+}  // namespace cla
+
+#define CLA_CUDA_TRY(expr, what)                                                    \
+    do {                                                                            \
+        cudaError_t e_ = (expr);                                                    \
+        if (e_ != cudaSuccess)                                                      \
+            return ::cla::fail(CLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e_)); \
+    } while (0)

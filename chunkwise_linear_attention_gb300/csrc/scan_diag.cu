@@ -1,0 +1,522 @@
+// scan_diag.cu -- diagonal (vector-state) linear-recurrence scan, forward and
+// backward, for GB300 (sm_103a).
+//
+// "Parallel Scan" (zerotofrontier.app), "The scan for one number of state",
+// "A vectorized scan for diagonal states", "The backward pass is a scan in
+// reverse"; "Parallel Scan" (aiwiki), the tiling remark: load a chunk, scan
+// it on chip, carry one composed pair across the chunk boundary, never write
+// intermediate states.
+//
+// Work decomposition (one warp = one chunk tile of TC = 8*L steps x 16
+// channels):
+//   lane = (sub, cg): cg in 0..3 picks 4 adjacent channels (one float4),
+//   sub in 0..7 picks a run of L consecutive steps.  A warp load instruction
+//   touches 8 rows x 64 contiguous bytes; the 8 warps of a block cover 128
+//   adjacent channels, so every 128-byte line is consumed by one block.
+// Per tile:
+//   1. every lane loads its L rows of (a, b) into registers (16-byte loads);
+//   2. composes them sequentially into one pair (A, B) per channel;
+//   3. warp-shuffle Hillis-Steele over the 8 runs (3 rounds) gives each run's
+//      inclusive and exclusive prefix inside the chunk;
+//   4. the last run's lanes publish the chunk aggregate, then walk back over
+//      earlier chunks' published pairs (decoupled look-back) to obtain the
+//      state entering the chunk, and publish the inclusive state;
+//   5. every lane re-runs its L steps from its true starting state and
+//      writes h once.
+// HBM traffic is the algorithmic 12 B per element forward (read a, b; write
+// h) and 20 B backward (read a, h, dh; write da, db), plus 48 B per chunk
+// and 4 channels of look-back payload.
+#include "cla_internal.cuh"
+
+namespace cla {
+namespace {
+
+constexpr int kSub = 8;      // runs per chunk (lanes along time)
+constexpr int kCg = 4;       // lanes along channels
+constexpr int kWarps = 8;    // warps per block
+constexpr int kL = 8;        // steps per run
+constexpr int kTc = kSub * kL;  // steps per chunk
+
+template <int VEC>
+struct VecIO;
+
+template <>
+struct VecIO<4> {
+    static __device__ __forceinline__ void load(const float *p, float (&v)[4]) {
+        float4 x = __ldg(reinterpret_cast<const float4 *>(p));
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    }
+    static __device__ __forceinline__ void load_cs(const float *p, float (&v)[4]) {
+        float4 x = __ldcs(reinterpret_cast<const float4 *>(p));
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    }
+    static __device__ __forceinline__ void store(float *p, const float (&v)[4]) {
+        __stcs(reinterpret_cast<float4 *>(p), make_float4(v[0], v[1], v[2], v[3]));
+    }
+    static __device__ __forceinline__ void store_ws(float4 *p, const float (&v)[4]) {
+        __stcg(p, make_float4(v[0], v[1], v[2], v[3]));
+    }
+    static __device__ __forceinline__ void load_ws(const float4 *p, float (&v)[4]) {
+        float4 x = ld_cg4(p);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    }
+};
+
+template <>
+struct VecIO<1> {
+    static __device__ __forceinline__ void load(const float *p, float (&v)[1]) { v[0] = __ldg(p); }
+    static __device__ __forceinline__ void load_cs(const float *p, float (&v)[1]) { v[0] = __ldcs(p); }
+    static __device__ __forceinline__ void store(float *p, const float (&v)[1]) { __stcs(p, v[0]); }
+    static __device__ __forceinline__ void store_ws(float4 *p, const float (&v)[1]) {
+        __stcg(reinterpret_cast<float *>(p), v[0]);
+    }
+    static __device__ __forceinline__ void load_ws(const float4 *p, float (&v)[1]) {
+        v[0] = ld_cg(reinterpret_cast<const float *>(p));
+    }
+};
+
+struct ScanWs {
+    WsHeader *hdr;
+    unsigned int *flags;  // per (chunk, b, warp-column, cg): 0 none, 1 aggregate, 2 inclusive
+    float4 *aggA;         // product of the chunk's decays
+    float4 *aggB;         // the chunk's composed input
+    float4 *incl;         // state at the chunk's end (forward) / start (backward)
+};
+
+struct ScanGeom {
+    int B, D, n_chunks, n_cw, n_cblk;
+    long long T;
+};
+
+__host__ __device__ inline size_t scan_units(const ScanGeom &g) {
+    return (size_t)g.n_chunks * g.B * g.n_cw * kCg;
+}
+
+__device__ __forceinline__ size_t unit_index(const ScanGeom &g, int chunk, int b, int cw, int cg) {
+    return (((size_t)chunk * g.B + b) * g.n_cw + cw) * kCg + cg;
+}
+
+// ------------------------------------------------------------------ forward
+template <int VEC>
+__global__ void __launch_bounds__(kWarps * 32)
+scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
+                     const float *__restrict__ h0, float *__restrict__ h,
+                     float *__restrict__ hT, ScanGeom g, ScanWs ws) {
+    __shared__ unsigned int s_ticket;
+    if (threadIdx.x == 0) s_ticket = atomicAdd(&ws.hdr->ticket[0], 1u);
+    __syncthreads();
+    const unsigned int tk = s_ticket;
+    const int per_chunk = g.B * g.n_cblk;
+    const int chunk = (int)(tk / per_chunk);
+    const int rem = (int)(tk % per_chunk);
+    const int bi = rem / g.n_cblk;
+    const int cw = (rem % g.n_cblk) * kWarps + (threadIdx.x >> 5);
+    if (cw >= g.n_cw) return;  // whole warp idle: nobody waits on it
+    const int lane = threadIdx.x & 31;
+    const int sub = lane >> 2, cg = lane & 3;
+    const int c0 = cw * (kCg * VEC) + cg * VEC;
+    const bool cok = c0 < g.D;
+    const long long t_begin = (long long)chunk * kTc + sub * kL;
+
+    float av[kL][VEC], bv[kL][VEC];
+#pragma unroll
+    for (int i = 0; i < kL; ++i) {
+        const long long t = t_begin + i;
+        if (cok && t < g.T) {
+            const size_t idx = ((size_t)bi * g.T + t) * g.D + c0;
+            VecIO<VEC>::load_cs(a + idx, av[i]);
+            VecIO<VEC>::load_cs(b + idx, bv[i]);
+        } else {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) { av[i][v] = 1.f; bv[i][v] = 0.f; }
+        }
+    }
+    // 2. sequential composition of this lane's run
+    float A[VEC], Bc[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) { A[v] = 1.f; Bc[v] = 0.f; }
+#pragma unroll
+    for (int i = 0; i < kL; ++i)
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            Bc[v] = fmaf(av[i][v], Bc[v], bv[i][v]);
+            A[v] *= av[i][v];
+        }
+    // 3. Hillis-Steele across the 8 runs: combine with the run 1, 2, 4 to the left.
+#pragma unroll
+    for (int off = 1; off < kSub; off <<= 1) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            const float pa = __shfl_up_sync(0xffffffffu, A[v], off * kCg);
+            const float pb = __shfl_up_sync(0xffffffffu, Bc[v], off * kCg);
+            if (sub >= off) {  // (pa, pb) happened first
+                Bc[v] = fmaf(A[v], pb, Bc[v]);
+                A[v] *= pa;
+            }
+        }
+    }
+    float Aex[VEC], Bex[VEC];  // prefix of the runs before this one
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+        Aex[v] = __shfl_up_sync(0xffffffffu, A[v], kCg);
+        Bex[v] = __shfl_up_sync(0xffffffffu, Bc[v], kCg);
+        if (sub == 0) { Aex[v] = 1.f; Bex[v] = 0.f; }
+    }
+    // 4. decoupled look-back by the lanes holding the chunk aggregate
+    float carry[VEC];
+    if (sub == kSub - 1) {
+        const size_t u = unit_index(g, chunk, bi, cw, cg);
+        float hin[VEC];
+        if (chunk == 0) {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v)
+                hin[v] = (h0 != nullptr && cok) ? h0[(size_t)bi * g.D + c0 + v] : 0.f;
+        } else {
+            VecIO<VEC>::store_ws(ws.aggA + u, A);
+            VecIO<VEC>::store_ws(ws.aggB + u, Bc);
+            st_release(ws.flags + u, 1u);
+            float accA[VEC], accB[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) { accA[v] = 1.f; accB[v] = 0.f; }
+            int j = chunk - 1;
+            while (true) {
+                const size_t up = unit_index(g, j, bi, cw, cg);
+                const unsigned int f = wait_flag(ws.flags + up, ws.hdr, 1u);
+                if (f == 2u) {
+                    float s[VEC];
+                    VecIO<VEC>::load_ws(ws.incl + up, s);
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) hin[v] = fmaf(accA[v], s[v], accB[v]);
+                    break;
+                } else if (f == 1u) {
+                    float pa[VEC], pb[VEC];
+                    VecIO<VEC>::load_ws(ws.aggA + up, pa);
+                    VecIO<VEC>::load_ws(ws.aggB + up, pb);
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) {  // chunk j happened before acc
+                        accB[v] = fmaf(accA[v], pb[v], accB[v]);
+                        accA[v] *= pa[v];
+                    }
+                    if (--j < 0) {  // reached the sequence start: apply h0
+#pragma unroll
+                        for (int v = 0; v < VEC; ++v) {
+                            const float s0 = (h0 != nullptr && cok) ? h0[(size_t)bi * g.D + c0 + v] : 0.f;
+                            hin[v] = fmaf(accA[v], s0, accB[v]);
+                        }
+                        break;
+                    }
+                } else {  // gave up waiting: carry zero, the call reports CLA_ERR_TIMEOUT
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) hin[v] = 0.f;
+                    break;
+                }
+            }
+        }
+        float inc[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { inc[v] = fmaf(A[v], hin[v], Bc[v]); carry[v] = hin[v]; }
+        VecIO<VEC>::store_ws(ws.incl + u, inc);
+        st_release(ws.flags + u, 2u);
+    }
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) carry[v] = __shfl_sync(0xffffffffu, carry[v], (kSub - 1) * kCg + cg);
+    // 5. re-run this lane's steps from its true starting state; write h once
+    float hs[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) hs[v] = fmaf(Aex[v], carry[v], Bex[v]);
+#pragma unroll
+    for (int i = 0; i < kL; ++i) {
+        const long long t = t_begin + i;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) hs[v] = fmaf(av[i][v], hs[v], bv[i][v]);
+        if (cok && t < g.T) {
+            const size_t idx = ((size_t)bi * g.T + t) * g.D + c0;
+            VecIO<VEC>::store(h + idx, hs);
+            if (hT != nullptr && t == g.T - 1)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) hT[(size_t)bi * g.D + c0 + v] = hs[v];
+        }
+    }
+}
+
+// ------------------------------------------------------------------ backward
+// Reversed time: hbar_t = a'_t hbar_{t+1} + g_t with a'_t = a_{t+1}
+// (a'_{T-1} = 1 and g_{T-1} includes dhT), i.e. the forward scan on reversed
+// arrays with the decays shifted by one place.
+template <int VEC>
+__global__ void __launch_bounds__(kWarps * 32)
+scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0,
+                     const float *__restrict__ h, const float *__restrict__ dh,
+                     const float *__restrict__ dhT, float *__restrict__ da,
+                     float *__restrict__ db, float *__restrict__ dh0, ScanGeom g,
+                     ScanWs ws) {
+    __shared__ unsigned int s_ticket;
+    if (threadIdx.x == 0) s_ticket = atomicAdd(&ws.hdr->ticket[1], 1u);
+    __syncthreads();
+    const unsigned int tk = s_ticket;
+    const int per_chunk = g.B * g.n_cblk;
+    const int chunk = g.n_chunks - 1 - (int)(tk / per_chunk);
+    const int rem = (int)(tk % per_chunk);
+    const int bi = rem / g.n_cblk;
+    const int cw = (rem % g.n_cblk) * kWarps + (threadIdx.x >> 5);
+    if (cw >= g.n_cw) return;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane >> 2, cg = lane & 3;
+    const int c0 = cw * (kCg * VEC) + cg * VEC;
+    const bool cok = c0 < g.D;
+    const long long t_begin = (long long)chunk * kTc + sub * kL;
+
+    float ap[kL][VEC], gv[kL][VEC], hp[kL][VEC];
+#pragma unroll
+    for (int i = 0; i < kL; ++i) {
+        const long long t = t_begin + i;
+        if (cok && t < g.T) {
+            const size_t idx = ((size_t)bi * g.T + t) * g.D + c0;
+            VecIO<VEC>::load_cs(dh + idx, gv[i]);
+            if (t + 1 < g.T) {
+                VecIO<VEC>::load(a + idx + g.D, ap[i]);
+            } else {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    ap[i][v] = 1.f;
+                    if (dhT != nullptr) gv[i][v] += dhT[(size_t)bi * g.D + c0 + v];
+                }
+            }
+            if (t >= 1) {
+                VecIO<VEC>::load(h + idx - g.D, hp[i]);
+            } else {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) hp[i][v] = (h0 != nullptr) ? h0[(size_t)bi * g.D + c0 + v] : 0.f;
+            }
+        } else {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) { ap[i][v] = 1.f; gv[i][v] = 0.f; hp[i][v] = 0.f; }
+        }
+    }
+    // compose this lane's run from its last step down to its first
+    float A[VEC], Bc[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) { A[v] = 1.f; Bc[v] = 0.f; }
+#pragma unroll
+    for (int i = kL - 1; i >= 0; --i)
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            Bc[v] = fmaf(ap[i][v], Bc[v], gv[i][v]);
+            A[v] *= ap[i][v];
+        }
+    // Hillis-Steele over the runs toward the chunk's start (suffix direction)
+#pragma unroll
+    for (int off = 1; off < kSub; off <<= 1) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            const float pa = __shfl_down_sync(0xffffffffu, A[v], off * kCg);
+            const float pb = __shfl_down_sync(0xffffffffu, Bc[v], off * kCg);
+            if (sub + off < kSub) {  // the later run (pa, pb) applies first
+                Bc[v] = fmaf(A[v], pb, Bc[v]);
+                A[v] *= pa;
+            }
+        }
+    }
+    float Aex[VEC], Bex[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+        Aex[v] = __shfl_down_sync(0xffffffffu, A[v], kCg);
+        Bex[v] = __shfl_down_sync(0xffffffffu, Bc[v], kCg);
+        if (sub == kSub - 1) { Aex[v] = 1.f; Bex[v] = 0.f; }
+    }
+    float carry[VEC];
+    if (sub == 0) {
+        const size_t u = unit_index(g, chunk, bi, cw, cg);
+        float hin[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) hin[v] = 0.f;
+        if (chunk != g.n_chunks - 1) {
+            VecIO<VEC>::store_ws(ws.aggA + u, A);
+            VecIO<VEC>::store_ws(ws.aggB + u, Bc);
+            st_release(ws.flags + u, 1u);
+            float accA[VEC], accB[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) { accA[v] = 1.f; accB[v] = 0.f; }
+            int j = chunk + 1;
+            while (true) {
+                const size_t up = unit_index(g, j, bi, cw, cg);
+                const unsigned int f = wait_flag(ws.flags + up, ws.hdr, 2u);
+                if (f == 2u) {
+                    float s[VEC];
+                    VecIO<VEC>::load_ws(ws.incl + up, s);
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) hin[v] = fmaf(accA[v], s[v], accB[v]);
+                    break;
+                } else if (f == 1u) {
+                    float pa[VEC], pb[VEC];
+                    VecIO<VEC>::load_ws(ws.aggA + up, pa);
+                    VecIO<VEC>::load_ws(ws.aggB + up, pb);
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) {
+                        accB[v] = fmaf(accA[v], pb[v], accB[v]);
+                        accA[v] *= pa[v];
+                    }
+                    if (++j >= g.n_chunks) {
+#pragma unroll
+                        for (int v = 0; v < VEC; ++v) hin[v] = accB[v];
+                        break;
+                    }
+                } else {
+                    break;  // gave up waiting; reported as CLA_ERR_TIMEOUT
+                }
+            }
+        }
+        float inc[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { inc[v] = fmaf(A[v], hin[v], Bc[v]); carry[v] = hin[v]; }
+        VecIO<VEC>::store_ws(ws.incl + u, inc);
+        st_release(ws.flags + u, 2u);
+    }
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) carry[v] = __shfl_sync(0xffffffffu, carry[v], cg);
+    float hb[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) hb[v] = fmaf(Aex[v], carry[v], Bex[v]);
+#pragma unroll
+    for (int i = kL - 1; i >= 0; --i) {
+        const long long t = t_begin + i;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) hb[v] = fmaf(ap[i][v], hb[v], gv[i][v]);
+        if (cok && t < g.T) {
+            const size_t idx = ((size_t)bi * g.T + t) * g.D + c0;
+            float dav[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) dav[v] = hb[v] * hp[i][v];
+            VecIO<VEC>::store(db + idx, hb);
+            VecIO<VEC>::store(da + idx, dav);
+            if (dh0 != nullptr && t == 0) {
+                float a1[VEC];
+                VecIO<VEC>::load(a + idx, a1);
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) dh0[(size_t)bi * g.D + c0 + v] = a1[v] * hb[v];
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+struct Plan {
+    ScanGeom g;
+    int vec;
+    size_t flags_off, aggA_off, aggB_off, incl_off, total;
+};
+
+Plan make_plan(int64_t B, int64_t T, int64_t D, int vec) {
+    Plan p;
+    p.vec = vec;
+    p.g.B = (int)B;
+    p.g.D = (int)D;
+    p.g.T = T;
+    p.g.n_chunks = (int)((T + kTc - 1) / kTc);
+    const int per_warp = kCg * vec;
+    p.g.n_cw = (int)((D + per_warp - 1) / per_warp);
+    p.g.n_cblk = (p.g.n_cw + kWarps - 1) / kWarps;
+    const size_t units = scan_units(p.g);
+    p.flags_off = sizeof(WsHeader);
+    p.aggA_off = align_up(p.flags_off + units * sizeof(unsigned int), 256);
+    p.aggB_off = p.aggA_off + units * sizeof(float4);
+    p.incl_off = p.aggB_off + units * sizeof(float4);
+    p.total = p.incl_off + units * sizeof(float4);
+    return p;
+}
+
+ScanWs bind_ws(const Plan &p, void *ws) {
+    char *base = static_cast<char *>(ws);
+    ScanWs w;
+    w.hdr = reinterpret_cast<WsHeader *>(base);
+    w.flags = reinterpret_cast<unsigned int *>(base + p.flags_off);
+    w.aggA = reinterpret_cast<float4 *>(base + p.aggA_off);
+    w.aggB = reinterpret_cast<float4 *>(base + p.aggB_off);
+    w.incl = reinterpret_cast<float4 *>(base + p.incl_off);
+    return w;
+}
+
+int check_sizes(const char *fn, int64_t B, int64_t T, int64_t D) {
+    if (B < 0 || T < 0 || D < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (D > (1ll << 30) || B > (1ll << 24) || T > (1ll << 40))
+        return fail(CLA_ERR_UNSUPPORTED, "%s: size out of range", fn);
+    const int64_t n_chunks = (T + kTc - 1) / kTc;
+    const int64_t n_cblk = ((D + 15) / 16 + kWarps - 1) / kWarps;
+    if (n_chunks * B * ((D + 3) / 4 + kWarps - 1) >= (1ll << 31) || n_chunks * B * n_cblk >= (1ll << 31))
+        return fail(CLA_ERR_UNSUPPORTED, "%s: problem too large for one launch", fn);
+    return CLA_OK;
+}
+
+}  // namespace
+}  // namespace cla
+
+using namespace cla;
+
+extern "C" size_t cla_scan_diag_workspace_size(int64_t B, int64_t T, int64_t D) {
+    if (B < 0 || T < 0 || D < 0) return 0;
+    // the scalar-channel layout needs the most units; size for it
+    const Plan p1 = make_plan(B, T, D, 1);
+    const Plan p4 = make_plan(B, T, D, 4);
+    return p1.total > p4.total ? p1.total : p4.total;
+}
+
+extern "C" int cla_scan_diag_fwd(const float *a, const float *b, const float *h0, float *h,
+                                 float *hT, int64_t B, int64_t T, int64_t D, void *ws,
+                                 size_t ws_bytes, void *stream) {
+    clear_error();
+    const char *fn = "cla_scan_diag_fwd";
+    int st = check_sizes(fn, B, T, D);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (B == 0 || D == 0) return CLA_OK;
+    if (T == 0) {
+        if (hT) {
+            if (h0) CLA_CUDA_TRY(cudaMemcpyAsync(hT, h0, sizeof(float) * B * D, cudaMemcpyDeviceToDevice, s), fn);
+            else CLA_CUDA_TRY(cudaMemsetAsync(hT, 0, sizeof(float) * B * D, s), fn);
+        }
+        return CLA_OK;
+    }
+    if (!a || !b || !h) return fail(CLA_ERR_INVALID_ARG, "%s: a, b and h are required", fn);
+    if (!ws) return fail(CLA_ERR_WORKSPACE, "%s: workspace is NULL", fn);
+    if (!aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace not 16-byte aligned", fn);
+    const bool v4 = (D % 4 == 0) && aligned16(a) && aligned16(b) && aligned16(h);
+    const Plan p = make_plan(B, T, D, v4 ? 4 : 1);
+    if (ws_bytes < p.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, p.total);
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.aggA_off, s), fn);
+    const ScanWs w = bind_ws(p, ws);
+    const unsigned int grid = (unsigned int)((size_t)p.g.n_chunks * p.g.B * p.g.n_cblk);
+    if (v4) scan_diag_fwd_kernel<4><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);
+    else scan_diag_fwd_kernel<1><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);
+    return check_launch(fn);
+}
+
+extern "C" int cla_scan_diag_bwd(const float *a, const float *h0, const float *h,
+                                 const float *dh, const float *dhT, float *da, float *db,
+                                 float *dh0, int64_t B, int64_t T, int64_t D, void *ws,
+                                 size_t ws_bytes, void *stream) {
+    clear_error();
+    const char *fn = "cla_scan_diag_bwd";
+    int st = check_sizes(fn, B, T, D);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (B == 0 || D == 0) return CLA_OK;
+    if (T == 0) {  // h_T = h0: the gradient passes straight through
+        if (dh0) {
+            if (dhT) CLA_CUDA_TRY(cudaMemcpyAsync(dh0, dhT, sizeof(float) * B * D, cudaMemcpyDeviceToDevice, s), fn);
+            else CLA_CUDA_TRY(cudaMemsetAsync(dh0, 0, sizeof(float) * B * D, s), fn);
+        }
+        return CLA_OK;
+    }
+    if (!a || !h || !dh || !da || !db) return fail(CLA_ERR_INVALID_ARG, "%s: a, h, dh, da and db are required", fn);
+    if (!ws) return fail(CLA_ERR_WORKSPACE, "%s: workspace is NULL", fn);
+    if (!aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace not 16-byte aligned", fn);
+    const bool v4 = (D % 4 == 0) && aligned16(a) && aligned16(h) && aligned16(dh) && aligned16(da) && aligned16(db);
+    const Plan p = make_plan(B, T, D, v4 ? 4 : 1);
+    if (ws_bytes < p.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, p.total);
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.aggA_off, s), fn);
+    const ScanWs w = bind_ws(p, ws);
+    const unsigned int grid = (unsigned int)((size_t)p.g.n_chunks * p.g.B * p.g.n_cblk);
+    if (v4) scan_diag_bwd_kernel<4><<<grid, kWarps * 32, 0, s>>>(a, h0, h, dh, dhT, da, db, dh0, p.g, w);
+    else scan_diag_bwd_kernel<1><<<grid, kWarps * 32, 0, s>>>(a, h0, h, dh, dhT, da, db, dh0, p.g, w);
+    return check_launch(fn);
+}

@@ -1,0 +1,220 @@
+/*
+ * cla.h -- C ABI of libcla.so: linear-recurrence scans and chunkwise decayed
+ * linear attention, forward and backward, as hand-written CUDA for GB300
+ * (sm_103a).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  Inputs are
+ *    read, outputs are overwritten entirely; no pointer is retained after the
+ *    call returns.  The library never allocates or frees device memory and
+ *    never synchronises: it validates the arguments on the host, enqueues its
+ *    kernels (and small memsets of its workspace) on `stream` (a
+ *    cudaStream_t; NULL = the legacy default stream) and returns.
+ *  - Tensors are dense, row-major, with the innermost dimension last, and
+ *    16-byte aligned.  `bf16` arguments are bfloat16 bit patterns (uint16_t).
+ *  - Arguments marked [opt] may be NULL: an optional input then means zeros,
+ *    an optional output is not written.
+ *  - `ws`/`ws_bytes` is caller-owned scratch of at least the size returned by
+ *    the matching *_workspace_size() query (16-byte aligned).  Its contents
+ *    need not be initialised and are meaningless after the call.  Calls that
+ *    may run concurrently must use distinct workspaces.
+ *  - Errors: argument and shape errors are detected before anything is
+ *    enqueued and return CLA_ERR_INVALID_ARG / CLA_ERR_UNSUPPORTED /
+ *    CLA_ERR_WORKSPACE; a failed launch returns CLA_ERR_CUDA.  The kernels
+ *    never trap: a cross-block wait that exceeds its iteration bound records
+ *    a flag in the workspace and the block carries on; cla_check_status()
+ *    reports it as CLA_ERR_TIMEOUT.  cla_last_error_message() gives a
+ *    one-line description of the last failure on the calling host thread.
+ *
+ * Sources (page title and section):
+ *   "Parallel Scan" (zerotofrontier.app/ssm/parallel-scan)
+ *   "Lightning Attention-2" (arXiv 2401.04658, summary on paper-graph-ui)
+ *   "Parallel Scan" (aiwiki.thehackersbrain.dev/entries/parallel-scan)
+ */
+#ifndef CLA_H_
+#define CLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CLA_OK = 0,
+    CLA_ERR_INVALID_ARG = 1, /* null required pointer, negative size, misalignment */
+    CLA_ERR_UNSUPPORTED = 2, /* a size or head dimension this build has no kernel for */
+    CLA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    CLA_ERR_TIMEOUT = 4,     /* a bounded cross-block wait gave up (see cla_check_status) */
+    CLA_ERR_WORKSPACE = 5    /* ws is NULL, unaligned or smaller than required */
+} cla_status;
+
+/* Static, never-NULL name of a status code. */
+const char *cla_status_string(int status);
+
+/* Description of the last failing call on this host thread ("" if none). */
+const char *cla_last_error_message(void);
+
+/* Synchronises `stream`, then reports CLA_ERR_TIMEOUT if a kernel of the last
+ * call that used `ws` gave up a cross-block wait, CLA_ERR_CUDA if the stream
+ * holds an error, else CLA_OK.  `ws` must be the workspace of that call. */
+int cla_check_status(const void *ws, void *stream);
+
+/* Self-test of the failure path: launches one warp that polls a workspace
+ * word nothing ever sets.  Its bounded wait gives up after about a second,
+ * records the timeout in `ws` (>= 256 bytes) and returns; a following
+ * cla_check_status(ws, stream) then reports CLA_ERR_TIMEOUT.  No GPU fault,
+ * trap or hang is involved. */
+int cla_selftest_wait_timeout(void *ws, size_t ws_bytes, void *stream);
+
+/* ======================================================================== */
+/* Diagonal (vector-state) scan                                             */
+/* ======================================================================== */
+
+/* Bytes of workspace needed by cla_scan_diag_fwd / _bwd for [B, T, D]. */
+size_t cla_scan_diag_workspace_size(int64_t B, int64_t T, int64_t D);
+
+/* Forward: h_t = a_t * h_{t-1} + b_t elementwise over D channels, for
+ * t = 1..T, from h_0 = h0 ("Parallel Scan", "The scan for one number of
+ * state" and "A vectorized scan for diagonal states"; the initial state is
+ * folded into the first step, "Scans over vector and matrix states").
+ *   a, b   [B, T, D] fp32   decays and inputs
+ *   h0     [B, D]    fp32   [opt] initial state (NULL = 0)
+ *   h      [B, T, D] fp32   out: every state h_1..h_T
+ *   hT     [B, D]    fp32   [opt] out: h_T (h0 when T = 0)
+ * Each chunk of the sequence is composed inside one warp (a sequential run
+ * per lane, then Hillis-Steele across lanes) and one composed (a, b) pair per
+ * chunk and channel is carried across chunks by decoupled look-back; no
+ * intermediate pair reaches HBM beyond that one per chunk. */
+int cla_scan_diag_fwd(const float *a, const float *b, const float *h0, float *h,
+                      float *hT, int64_t B, int64_t T, int64_t D, void *ws,
+                      size_t ws_bytes, void *stream);
+
+/* Backward ("Parallel Scan", "The backward pass is a scan in reverse"): with
+ * direct gradients g_t = dh_t (plus dhT on h_T), the adjoint
+ * hbar_t = g_t + a_{t+1} hbar_{t+1} is the same scan on reversed time with
+ * the decays shifted by one; then db_t = hbar_t, da_t = hbar_t * h_{t-1},
+ * dh0 = a_1 * hbar_1.
+ *   a      [B, T, D] fp32   decays of the forward call
+ *   h0     [B, D]    fp32   [opt] initial state of the forward call
+ *   h      [B, T, D] fp32   states returned by the forward call
+ *   dh     [B, T, D] fp32   upstream gradient on every state
+ *   dhT    [B, D]    fp32   [opt] upstream gradient on the returned h_T
+ *   da, db [B, T, D] fp32   out
+ *   dh0    [B, D]    fp32   [opt] out */
+int cla_scan_diag_bwd(const float *a, const float *h0, const float *h,
+                      const float *dh, const float *dhT, float *da, float *db,
+                      float *dh0, int64_t B, int64_t T, int64_t D, void *ws,
+                      size_t ws_bytes, void *stream);
+
+/* ======================================================================== */
+/* Selective (Mamba-1 style) diagonal scan                                  */
+/* ======================================================================== */
+
+/* Time steps between the states saved by the forward for the backward. */
+#define CLA_SELECTIVE_CKPT_CHUNK 64
+
+/* Bytes of workspace for cla_selective_scan_fwd / _bwd. */
+size_t cla_selective_scan_workspace_size(int64_t B, int64_t T, int64_t D, int64_t N);
+
+/* Elements of the checkpoint tensor [B, ceil(T/64), D, N] (fp32). */
+size_t cla_selective_scan_ckpt_elems(int64_t B, int64_t T, int64_t D, int64_t N);
+
+/* Forward: per channel d and state entry n, h_{t,d,n} = a h_{t-1,d,n} + b with
+ * a = exp(delta_{t,d} A_{d,n}), b = delta_{t,d} Bm_t[n] x_{t,d}, and the read
+ * y_{t,d} = sum_n Cm_t[n] h_{t,d,n} ("Parallel Scan", "When a scan is the
+ * wrong tool": Mamba's selective decay; the (B, T, D, N) state never reaches
+ * HBM).
+ *   x      [B, T, D] bf16,  delta [B, T, D] fp32,  A [D, N] fp32
+ *   Bm, Cm [B, T, N] bf16,  h0 [B, D, N] fp32 [opt]
+ *   y      [B, T, D] fp32   out
+ *   hT     [B, D, N] fp32   [opt] out
+ *   ckpt   [B, ceil(T/64), D, N] fp32 [opt] out: the state entering every
+ *          64-step chunk, consumed by the backward
+ * N must be 16 in this build. */
+int cla_selective_scan_fwd(const uint16_t *x, const float *delta, const float *A,
+                           const uint16_t *Bm, const uint16_t *Cm, const float *h0,
+                           float *y, float *hT, float *ckpt, int64_t B, int64_t T,
+                           int64_t D, int64_t N, void *ws, size_t ws_bytes,
+                           void *stream);
+
+/* Backward: the adjoint of every (d, n) recurrence with direct gradient
+ * Cm_t[n] dy_{t,d}, recomputing the states from ckpt, then the chain rule
+ * through a and b:
+ *   dx_{t,d}     = sum_n hbar delta Bm_t[n]
+ *   ddelta_{t,d} = sum_n hbar (h_{t-1} a A_{d,n} + Bm_t[n] x_{t,d})
+ *   dA_{d,n}     = sum_{b,t} hbar h_{t-1} a delta
+ *   dB_t[n]      = sum_d hbar delta x,    dC_t[n] = sum_d dy h_t
+ *   dh0          = a_1 hbar_1
+ *   ckpt   as written by the forward with the same inputs
+ *   dy     [B, T, D] fp32;  dhT [B, D, N] fp32 [opt]
+ *   dx     [B, T, D] bf16 out;  ddelta [B, T, D] fp32 out
+ *   dA     [D, N] fp32 [opt] out;  dB, dC [B, T, N] fp32 out
+ *   dh0    [B, D, N] fp32 [opt] out
+ * Channel sums are reduced in a fixed order (no float atomics). */
+int cla_selective_scan_bwd(const uint16_t *x, const float *delta, const float *A,
+                           const uint16_t *Bm, const uint16_t *Cm, const float *h0,
+                           const float *ckpt, const float *dy, const float *dhT,
+                           uint16_t *dx, float *ddelta, float *dA, float *dB,
+                           float *dC, float *dh0, int64_t B, int64_t T, int64_t D,
+                           int64_t N, void *ws, size_t ws_bytes, void *stream);
+
+/* ======================================================================== */
+/* Chunkwise decayed linear attention (matrix state)                        */
+/* ======================================================================== */
+
+/* Bytes of workspace for cla_chunk_la_fwd / _bwd. */
+size_t cla_chunk_la_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                                   int64_t dim_v, int chunk);
+
+/* Forward of S_t = a_t S_{t-1} + k_t v_t^T (S is [dim_k, dim_v], rows indexed
+ * by keys), o_t = S_t^T q_t, with a_t = exp(log_decay_t), computed chunkwise
+ * ("Parallel Scan", "The chunkwise algorithm"; "Lightning Attention-2",
+ * eqs. 8 and 10 and Algorithm 1, with per-token decays):
+ *   O_[j] = (Q_[j] K_[j]^T . D) V_[j] + diag(lambda) Q_[j] S_[j-1]
+ *   S_[j] = alpha_j S_[j-1] + K_[j]^T diag(gamma) V_[j]
+ * D_rs = a_{t0+r:t0+s} (s <= r, unit diagonal), lambda_r = a_{t0+r:t0}
+ * (includes the first token's decay), gamma_s = a_{t0+Tc:t0+s}
+ * (gamma_Tc = 1); all from in-chunk sums of log_decay, never from long
+ * cumulative sums or ratios ("Long products without underflow").  A decay of
+ * exactly 0 (log_decay = -inf) is a reset and gives products of 0.
+ *   q, k       [B, H, T, dim_k] bf16
+ *   v          [B, H, T, dim_v] bf16
+ *   log_decay  [B, H, T] fp32
+ *   S0         [B, H, dim_k, dim_v] fp32 [opt]
+ *   o          [B, H, T, dim_v] bf16 out
+ *   ST         [B, H, dim_k, dim_v] fp32 [opt] out: S_T
+ * Supported: dim_k = dim_v in {64, 128}, chunk in {64, 128}; any T >= 0 (the
+ * last chunk may be shorter). */
+int cla_chunk_la_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const float *log_decay, const float *S0, uint16_t *o,
+                     float *ST, int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                     int64_t dim_v, int chunk, void *ws, size_t ws_bytes,
+                     void *stream);
+
+/* Backward ("Parallel Scan", "The backward pass of linear attention";
+ * "Lightning Attention-2", eqs. 15, 17, 19, 20 and Algorithm 2, with the
+ * decays above): a forward-order traversal rebuilds the chunk states and
+ * gives dQ; a reverse-order traversal carries the adjoint state dS and gives
+ * dK and dV; the decay gradient is the closed form
+ *   dlog_decay_u = sum_{t>=u} q_t.dq_t - sum_{s>=u} k_s.dk_s + <dST, S_T>
+ * (no per-token states), and dS0 is the adjoint state at t = 0.
+ *   dO         [B, H, T, dim_v] bf16   upstream gradient on o
+ *   dST        [B, H, dim_k, dim_v] fp32 [opt] upstream gradient on S_T
+ *   dq, dk     [B, H, T, dim_k] bf16 out;  dv [B, H, T, dim_v] bf16 out
+ *   dlog_decay [B, H, T] fp32 [opt] out;  dS0 [B, H, dim_k, dim_v] fp32 [opt] out
+ * Same support as the forward. */
+int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const float *log_decay, const float *S0, const uint16_t *dO,
+                     const float *dST, uint16_t *dq, uint16_t *dk, uint16_t *dv,
+                     float *dlog_decay, float *dS0, int64_t B, int64_t H,
+                     int64_t T, int64_t dim_k, int64_t dim_v, int chunk,
+                     void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CLA_H_ */
