@@ -191,7 +191,7 @@ def selective_scan_bwd(x, delta, A, Bm, Cm, h0, ckpt, dy, dhT=None, *, dx=None, 
     N = A.shape[1]
     dev = x.device
     f32, bf16 = torch.float32, torch.bfloat16
-    dx = _out(dx, (B, T, D), bf16, dev)
+    dx = _out(dx, (B, T, D), f32, dev)
     ddelta = _out(ddelta, (B, T, D), f32, dev)
     dA = _out(dA, (D, N), f32, dev) if (want_dA or dA is not None) else None
     dB = _out(dB, (B, T, N), f32, dev)
@@ -201,7 +201,7 @@ def selective_scan_bwd(x, delta, A, Bm, Cm, h0, ckpt, dy, dhT=None, *, dx=None, 
     _check("cla_selective_scan_bwd", lib().cla_selective_scan_bwd(
         _ptr(x, bf16, "x"), _ptr(delta, f32, "delta"), _ptr(A, f32, "A"), _ptr(Bm, bf16, "Bm"),
         _ptr(Cm, bf16, "Cm"), _ptr(h0, f32, "h0"), _ptr(ckpt, f32, "ckpt"), _ptr(dy, f32, "dy"),
-        _ptr(dhT, f32, "dhT"), _ptr(dx, bf16, "dx"), _ptr(ddelta, f32, "ddelta"), _ptr(dA, f32, "dA"),
+        _ptr(dhT, f32, "dhT"), _ptr(dx, f32, "dx"), _ptr(ddelta, f32, "ddelta"), _ptr(dA, f32, "dA"),
         _ptr(dB, f32, "dB"), _ptr(dC, f32, "dC"), _ptr(dh0, f32, "dh0"), B, T, D, N, _ptr(ws), ws.numel(),
         _stream(stream)))
     return dx, ddelta, dA, dB, dC, dh0
@@ -218,12 +218,12 @@ def chunk_la_fwd(q, k, v, log_decay, S0=None, *, chunk=64, o=None, ST=None, work
     dv = v.shape[-1]
     dev = q.device
     f32, bf16 = torch.float32, torch.bfloat16
-    o = _out(o, (B, H, T, dv), bf16, dev)
+    o = _out(o, (B, H, T, dv), f32, dev)
     ST = _out(ST, (B, H, dk, dv), f32, dev)
     ws = _ws(chunk_la_workspace_size(B, H, T, dk, dv, chunk), dev, workspace)
     _check("cla_chunk_la_fwd", lib().cla_chunk_la_fwd(
         _ptr(q, bf16, "q"), _ptr(k, bf16, "k"), _ptr(v, bf16, "v"), _ptr(log_decay, f32, "log_decay"),
-        _ptr(S0, f32, "S0"), _ptr(o, bf16, "o"), _ptr(ST, f32, "ST"), B, H, T, dk, dv, int(chunk),
+        _ptr(S0, f32, "S0"), _ptr(o, f32, "o"), _ptr(ST, f32, "ST"), B, H, T, dk, dv, int(chunk),
         _ptr(ws), ws.numel(), _stream(stream)))
     return o, ST
 
@@ -235,15 +235,15 @@ def chunk_la_bwd(q, k, v, log_decay, S0, dO, dST=None, *, chunk=64, dq=None, dk=
     dvv = v.shape[-1]
     dev = q.device
     f32, bf16 = torch.float32, torch.bfloat16
-    dq = _out(dq, (B, H, T, dkk), bf16, dev)
-    dk = _out(dk, (B, H, T, dkk), bf16, dev)
-    dv = _out(dv, (B, H, T, dvv), bf16, dev)
+    dq = _out(dq, (B, H, T, dkk), f32, dev)
+    dk = _out(dk, (B, H, T, dkk), f32, dev)
+    dv = _out(dv, (B, H, T, dvv), f32, dev)
     dlog_decay = _out(dlog_decay, (B, H, T), f32, dev)
     dS0 = _out(dS0, (B, H, dkk, dvv), f32, dev)
     ws = _ws(chunk_la_workspace_size(B, H, T, dkk, dvv, chunk), dev, workspace)
     _check("cla_chunk_la_bwd", lib().cla_chunk_la_bwd(
         _ptr(q, bf16, "q"), _ptr(k, bf16, "k"), _ptr(v, bf16, "v"), _ptr(log_decay, f32, "log_decay"),
-        _ptr(S0, f32, "S0"), _ptr(dO, bf16, "dO"), _ptr(dST, f32, "dST"), _ptr(dq, bf16, "dq"),
-        _ptr(dk, bf16, "dk"), _ptr(dv, bf16, "dv"), _ptr(dlog_decay, f32, "dlog_decay"),
+        _ptr(S0, f32, "S0"), _ptr(dO, bf16, "dO"), _ptr(dST, f32, "dST"), _ptr(dq, f32, "dq"),
+        _ptr(dk, f32, "dk"), _ptr(dv, f32, "dv"), _ptr(dlog_decay, f32, "dlog_decay"),
         _ptr(dS0, f32, "dS0"), B, H, T, dkk, dvv, int(chunk), _ptr(ws), ws.numel(), _stream(stream)))
     return dq, dk, dv, dlog_decay, dS0

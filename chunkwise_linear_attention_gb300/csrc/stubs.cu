@@ -12,19 +12,8 @@ extern "C" int cla_selective_scan_fwd(const uint16_t *, const float *, const flo
 }
 extern "C" int cla_selective_scan_bwd(const uint16_t *, const float *, const float *, const uint16_t *,
                                       const uint16_t *, const float *, const float *, const float *,
-                                      const float *, uint16_t *, float *, float *, float *, float *, float *,
+                                      const float *, float *, float *, float *, float *, float *, float *,
                                       int64_t, int64_t, int64_t, int64_t, void *, size_t, void *) {
     return fail(CLA_ERR_UNSUPPORTED, "cla_selective_scan_bwd: not built");
 }
-extern "C" size_t cla_chunk_la_workspace_size(int64_t, int64_t, int64_t, int64_t, int64_t, int) { return 256; }
-extern "C" int cla_chunk_la_fwd(const uint16_t *, const uint16_t *, const uint16_t *, const float *,
-                                const float *, uint16_t *, float *, int64_t, int64_t, int64_t, int64_t,
-                                int64_t, int, void *, size_t, void *) {
-    return fail(CLA_ERR_UNSUPPORTED, "cla_chunk_la_fwd: not built");
-}
-extern "C" int cla_chunk_la_bwd(const uint16_t *, const uint16_t *, const uint16_t *, const float *,
-                                const float *, const uint16_t *, const float *, uint16_t *, uint16_t *,
-                                uint16_t *, float *, float *, int64_t, int64_t, int64_t, int64_t, int64_t,
-                                int, void *, size_t, void *) {
-    return fail(CLA_ERR_UNSUPPORTED, "cla_chunk_la_bwd: not built");
-}
+

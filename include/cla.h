@@ -150,14 +150,14 @@ int cla_selective_scan_fwd(const uint16_t *x, const float *delta, const float *A
  *   dh0          = a_1 hbar_1
  *   ckpt   as written by the forward with the same inputs
  *   dy     [B, T, D] fp32;  dhT [B, D, N] fp32 [opt]
- *   dx     [B, T, D] bf16 out;  ddelta [B, T, D] fp32 out
+ *   dx     [B, T, D] fp32 out;  ddelta [B, T, D] fp32 out
  *   dA     [D, N] fp32 [opt] out;  dB, dC [B, T, N] fp32 out
  *   dh0    [B, D, N] fp32 [opt] out
  * Channel sums are reduced in a fixed order (no float atomics). */
 int cla_selective_scan_bwd(const uint16_t *x, const float *delta, const float *A,
                            const uint16_t *Bm, const uint16_t *Cm, const float *h0,
                            const float *ckpt, const float *dy, const float *dhT,
-                           uint16_t *dx, float *ddelta, float *dA, float *dB,
+                           float *dx, float *ddelta, float *dA, float *dB,
                            float *dC, float *dh0, int64_t B, int64_t T, int64_t D,
                            int64_t N, void *ws, size_t ws_bytes, void *stream);
 
@@ -184,12 +184,13 @@ size_t cla_chunk_la_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_
  *   v          [B, H, T, dim_v] bf16
  *   log_decay  [B, H, T] fp32
  *   S0         [B, H, dim_k, dim_v] fp32 [opt]
- *   o          [B, H, T, dim_v] bf16 out
+ *   o          [B, H, T, dim_v] fp32 out (the accumulation precision: bf16
+ *              rounding of the output alone would exceed the parity tolerance)
  *   ST         [B, H, dim_k, dim_v] fp32 [opt] out: S_T
  * Supported: dim_k = dim_v in {64, 128}, chunk in {64, 128}; any T >= 0 (the
  * last chunk may be shorter). */
 int cla_chunk_la_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                     const float *log_decay, const float *S0, uint16_t *o,
+                     const float *log_decay, const float *S0, float *o,
                      float *ST, int64_t B, int64_t H, int64_t T, int64_t dim_k,
                      int64_t dim_v, int chunk, void *ws, size_t ws_bytes,
                      void *stream);
@@ -203,12 +204,12 @@ int cla_chunk_la_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
  * (no per-token states), and dS0 is the adjoint state at t = 0.
  *   dO         [B, H, T, dim_v] bf16   upstream gradient on o
  *   dST        [B, H, dim_k, dim_v] fp32 [opt] upstream gradient on S_T
- *   dq, dk     [B, H, T, dim_k] bf16 out;  dv [B, H, T, dim_v] bf16 out
+ *   dq, dk     [B, H, T, dim_k] fp32 out;  dv [B, H, T, dim_v] fp32 out
  *   dlog_decay [B, H, T] fp32 [opt] out;  dS0 [B, H, dim_k, dim_v] fp32 [opt] out
  * Same support as the forward. */
 int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                      const float *log_decay, const float *S0, const uint16_t *dO,
-                     const float *dST, uint16_t *dq, uint16_t *dk, uint16_t *dv,
+                     const float *dST, float *dq, float *dk, float *dv,
                      float *dlog_decay, float *dS0, int64_t B, int64_t H,
                      int64_t T, int64_t dim_k, int64_t dim_v, int chunk,
                      void *ws, size_t ws_bytes, void *stream);

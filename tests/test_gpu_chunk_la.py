@@ -1,0 +1,113 @@
+"""Chunkwise decayed linear attention, forward and backward: GPU (through the
+C ABI) vs the oracle's per-token recurrence, with the bf16 tolerance
+(per output tensor, |x - r| / rms(r): max <= 2e-2, mean <= 5e-3)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._parity import assert_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cla():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import chunkwise_linear_attention_gb300 as m
+
+    m.lib()
+    return m
+
+
+def _dev(x):
+    return None if x is None else x.cuda()
+
+
+def _check(cla, inp, chunk, dST=None, heads=None, check_bwd=True):
+    t = {k: _dev(v) for k, v in inp.items()}
+    o, ST = cla.chunk_la_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], chunk=chunk)
+    if check_bwd:
+        g = cla.chunk_la_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"], _dev(dST), chunk=chunk)
+    torch.cuda.synchronize()
+    sel = (lambda x: x) if heads is None else (lambda x: None if x is None else x[:, heads])
+    ci = {k: sel(v) for k, v in inp.items()}
+    ro, rST = oracle.la_fwd(ci["q"], ci["k"], ci["v"], ci["log_a"], ci["S0"])
+    assert_bf16("o", sel(o), ro)
+    assert_bf16("S_T", sel(ST), rST)
+    if not check_bwd:
+        return
+    rdq, rdk, rdv, rdl, rdS0 = oracle.la_bwd(ci["q"], ci["k"], ci["v"], ci["log_a"], ci["S0"], ci["dO"], sel(dST))
+    for name, x, r in zip(("dq", "dk", "dv", "dlog_a", "dS0"), map(sel, g), (rdq, rdk, rdv, rdl, rdS0)):
+        assert_bf16(name, x, r)
+
+
+@pytest.mark.parametrize("B,H,T,d,chunk", [
+    (1, 2, 64, 64, 64), (1, 2, 300, 64, 64), (2, 1, 1, 64, 64), (1, 1, 1000, 64, 64),
+    (1, 1, 3000, 64, 64), (1, 2, 700, 64, 128), (1, 1, 2000, 128, 128), (1, 1, 500, 128, 64),
+    (2, 1, 129, 128, 128),
+])
+@pytest.mark.parametrize("with_state", [False, True])
+def test_chunk_la_small(cla, B, H, T, d, chunk, with_state):
+    inp = workloads.make("la_long", B=B, H=H, T=T, dk=d, dv=d)
+    dST = None
+    if not with_state:
+        inp["S0"] = None
+    else:
+        rng = np.random.default_rng(T + d)
+        dST = torch.from_numpy(rng.normal(0, 0.1, (B, H, d, d)).astype(np.float32))
+    _check(cla, inp, chunk, dST)
+
+
+def test_chunk_la_constant_decay_small(cla):
+    inp = workloads.make("la_const", B=1, H=16, T=777, dk=64, dv=64)
+    _check(cla, inp, 64)
+
+
+def test_chunk_la_resets(cla):
+    """log a = -inf (a reset) inside and at the start of chunks: products that
+    span it are 0, never NaN."""
+    inp = workloads.make("la_long", B=1, H=2, T=400, dk=64, dv=64)
+    la = inp["log_a"].clone()
+    for t in (0, 5, 64, 100, 255, 399):
+        la[0, 0, t] = -float("inf")
+    la[0, 1, 130] = -float("inf")
+    inp["log_a"] = la
+    t = {k: _dev(v) for k, v in inp.items()}
+    o, ST = cla.chunk_la_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], chunk=64)
+    dq, dk, dv, dl, dS0 = cla.chunk_la_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"], chunk=64)
+    torch.cuda.synchronize()
+    ro, rST = oracle.la_fwd(inp["q"], inp["k"], inp["v"], inp["log_a"], inp["S0"])
+    assert_bf16("o", o, ro)
+    assert_bf16("S_T", ST, rST)
+    rdq, rdk, rdv, rdl, rdS0 = oracle.la_bwd(inp["q"], inp["k"], inp["v"], inp["log_a"], inp["S0"], inp["dO"])
+    for name, x, r in (("dq", dq, rdq), ("dk", dk, rdk), ("dv", dv, rdv), ("dS0", dS0, rdS0)):
+        assert_bf16(name, x, r)
+    # dlog_a at a reset: the definition gives a_t <.,.> = 0 there
+    dl = dl.cpu().numpy()
+    assert np.all(np.isfinite(dl))
+    assert_bf16("dlog_a", dl, rdl)
+
+
+def test_chunk_la_empty(cla):
+    dev = torch.device("cuda")
+    z = torch.empty(1, 2, 0, 64, dtype=torch.bfloat16, device=dev)
+    S0 = torch.randn(1, 2, 64, 64, device=dev)
+    o, ST = cla.chunk_la_fwd(z, z, z, torch.empty(1, 2, 0, device=dev), S0)
+    torch.cuda.synchronize()
+    assert torch.equal(ST, S0)
+
+
+def test_chunk_la_constant_decay_workload_full(cla):
+    """4 x 16 x 8192, d = 64, chunk 64, every output element."""
+    inp = workloads.make("la_const")
+    _check(cla, inp, 64)
+
+
+def test_chunk_la_long_workload_sampled_heads(cla):
+    """1 x 32 x 65536, d = 128, chunk 128 on the GPU; heads 0 and 31 against
+    the oracle (heads are independent problems)."""
+    inp = workloads.make("la_long")
+    _check(cla, inp, 128, heads=[0, 31])
