@@ -51,6 +51,7 @@ def lib():
                 "cla_scan_diag_workspace_size": ([I64, I64, I64], SZ),
                 "cla_scan_diag_fwd": ([P, P, P, P, P, I64, I64, I64, P, SZ, P], INT),
                 "cla_scan_diag_bwd": ([P, P, P, P, P, P, P, P, I64, I64, I64, P, SZ, P], INT),
+                "cla_scan_diag_fwd_noalloc": ([P, P, P, P, P, I64, I64, I64, P], INT),
                 "cla_selective_scan_workspace_size": ([I64, I64, I64, I64], SZ),
                 "cla_selective_scan_ckpt_elems": ([I64, I64, I64, I64], SZ),
                 "cla_selective_scan_fwd": ([P] * 9 + [I64] * 4 + [P, SZ, P], INT),
@@ -137,6 +138,20 @@ def scan_diag_fwd(a, b, h0=None, *, h=None, hT=None, workspace=None, stream=None
     _check("cla_scan_diag_fwd", lib().cla_scan_diag_fwd(
         _ptr(a, f32, "a"), _ptr(b, f32, "b"), _ptr(h0, f32, "h0"), _ptr(h, f32, "h"), _ptr(hT, f32, "hT"),
         B, T, D, _ptr(ws), ws.numel(), _stream(stream)))
+    return h, hT
+
+
+def scan_diag_fwd_noalloc(a, b, h0=None, *, h=None, hT=None, stream=None):
+    """scan_diag_fwd without a workspace: the library's static scratch array
+    is used (limited size; overlapping calls race).  Returns (h, hT)."""
+    B, T, D = a.shape
+    dev = a.device
+    f32 = torch.float32
+    h = _out(h, (B, T, D), f32, dev)
+    hT = _out(hT, (B, D), f32, dev)
+    _check("cla_scan_diag_fwd_noalloc", lib().cla_scan_diag_fwd_noalloc(
+        _ptr(a, f32, "a"), _ptr(b, f32, "b"), _ptr(h0, f32, "h0"), _ptr(h, f32, "h"), _ptr(hT, f32, "hT"),
+        B, T, D, _stream(stream)))
     return h, hT
 
 

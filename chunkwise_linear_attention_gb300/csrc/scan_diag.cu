@@ -26,6 +26,8 @@
 // HBM traffic is the algorithmic 12 B per element forward (read a, b; write
 // h) and 20 B backward (read a, h, dh; write da, db), plus 48 B per chunk
 // and 4 channels of look-back payload.
+#include <mutex>
+
 #include "cla_internal.cuh"
 
 namespace cla {
@@ -518,5 +520,82 @@ extern "C" int cla_scan_diag_bwd(const float *a, const float *h0, const float *h
     const unsigned int grid = (unsigned int)((size_t)p.g.n_chunks * p.g.B * p.g.n_cblk);
     if (v4) scan_diag_bwd_kernel<4><<<grid, kWarps * 32, 0, s>>>(a, h0, h, dh, dhT, da, db, dh0, p.g, w);
     else scan_diag_bwd_kernel<1><<<grid, kWarps * 32, 0, s>>>(a, h0, h, dh, dhT, da, db, dh0, p.g, w);
+    return check_launch(fn);
+}
+
+// ------------------------------------------------------------------ no-allocation variant
+// Some callers cannot hand this library a workspace: a plugin inside a host
+// framework that owns every device allocation and exposes no scratch space, a
+// deployment whose device-memory footprint is fixed in advance, or a code
+// path where an allocation call (its latency or its implicit synchronisation)
+// is not allowed.  For them the forward diagonal scan can run with its
+// look-back scratch in a statically sized device array that is part of the
+// library image.  Each GPU that loads the library keeps this array for the
+// life of the process.
+
+namespace cla {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB per device
+static __device__ __align__(256) unsigned char g_scan_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the array, looked up once per device.  The name
+// g_scan_noalloc_scratch is only a host-side stand-in in host code and must
+// never be passed to a kernel directly.
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(void **out) {
+    int dev = -1;
+    CLA_CUDA_TRY(cudaGetDevice(&dev), "cla_scan_diag_fwd_noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(CLA_ERR_UNSUPPORTED, "cla_scan_diag_fwd_noalloc: device %d", dev);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_scan_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return fail(CLA_ERR_CUDA, "cla_scan_diag_fwd_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return CLA_OK;
+}
+
+}  // namespace
+}  // namespace cla
+
+extern "C" int cla_scan_diag_fwd_noalloc(const float *a, const float *b, const float *h0, float *h, float *hT,
+                                         int64_t B, int64_t T, int64_t D, void *stream) {
+    clear_error();
+    const char *fn = "cla_scan_diag_fwd_noalloc";
+    int st = check_sizes(fn, B, T, D);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (B == 0 || D == 0) return CLA_OK;
+    if (T == 0) {
+        if (hT) {
+            if (h0) CLA_CUDA_TRY(cudaMemcpyAsync(hT, h0, sizeof(float) * B * D, cudaMemcpyDeviceToDevice, s), fn);
+            else CLA_CUDA_TRY(cudaMemsetAsync(hT, 0, sizeof(float) * B * D, s), fn);
+        }
+        return CLA_OK;
+    }
+    if (!a || !b || !h) return fail(CLA_ERR_INVALID_ARG, "%s: a, b and h are required", fn);
+    const bool v4 = (D % 4 == 0) && aligned16(a) && aligned16(b) && aligned16(h);
+    const Plan p = make_plan(B, T, D, v4 ? 4 : 1);
+    if (p.total > kNoAllocScratchBytes)
+        return fail(CLA_ERR_UNSUPPORTED,
+                    "%s: this size needs %zu bytes of scratch but the static array holds %zu; "
+                    "use cla_scan_diag_fwd with a caller workspace",
+                    fn, p.total, kNoAllocScratchBytes);
+    void *ws = nullptr;
+    st = noalloc_scratch(&ws);
+    if (st) return st;
+    // tickets and flags must start at zero; the payload is always written before it is read
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.aggA_off, s), fn);
+    const ScanWs w = bind_ws(p, ws);
+    const unsigned int grid = (unsigned int)((size_t)p.g.n_chunks * p.g.B * p.g.n_cblk);
+    if (v4) scan_diag_fwd_kernel<4><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);
+    else scan_diag_fwd_kernel<1><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);
     return check_launch(fn);
 }

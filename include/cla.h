@@ -109,6 +109,34 @@ int cla_scan_diag_bwd(const float *a, const float *h0, const float *h,
                       float *dh0, int64_t B, int64_t T, int64_t D, void *ws,
                       size_t ws_bytes, void *stream);
 
+/* Forward diagonal scan for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a deployment variant of
+ * cla_scan_diag_fwd.  It is meant for code that may not (or cannot) hand the
+ * library a workspace: a plugin inside a framework that owns every device
+ * allocation and offers no scratch buffer, a deployment whose device-memory
+ * footprint is fixed ahead of time, or a path where an allocation call's
+ * latency or implicit synchronisation is not allowed.  Inputs, outputs and
+ * results are those of cla_scan_diag_fwd; the caller still passes every
+ * input and output buffer.
+ *  - Scratch: the look-back scratch lives in an 8 MiB array compiled into the
+ *    library (one per GPU that loads it, held until the process exits).  No
+ *    cudaMalloc, cudaFree or other allocating call is made.
+ *  - Limit: sizes whose scratch exceeds 8 MiB are rejected with
+ *    CLA_ERR_UNSUPPORTED and nothing is enqueued: about 40 million elements
+ *    of B*T*D when D is a multiple of 4 (8 x 4096 x 1024 fits), about 10
+ *    million otherwise.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array; the call clears what must start at
+ *    zero.  Calls that overlap on the GPU (other streams, other host threads)
+ *    race on it and must be serialised by the caller.
+ *  - There is no workspace to pass to cla_check_status(); a look-back wait
+ *    that gives up is not reported by this variant. */
+int cla_scan_diag_fwd_noalloc(const float *a, const float *b, const float *h0,
+                              float *h, float *hT, int64_t B, int64_t T,
+                              int64_t D, void *stream);
+
 /* ======================================================================== */
 /* Selective (Mamba-1 style) diagonal scan                                  */
 /* ======================================================================== */
