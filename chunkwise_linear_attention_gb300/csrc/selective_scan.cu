@@ -1,0 +1,705 @@
+// selective_scan.cu -- selective (Mamba-1 style) diagonal scan, forward and
+// backward, for GB300 (sm_103a).
+//
+// "Parallel Scan" (zerotofrontier.app), "Scans over vector and matrix states"
+// (a diagonal transition per channel), "When a scan is the wrong tool"
+// (Mamba's kernel: discretise on chip, keep the (B, T, D, N) state out of HBM,
+// recompute states in the backward pass) and "The backward pass is a scan in
+// reverse".
+//
+// Per channel d and state entry n: a = exp(delta A), b = delta B_t[n] x,
+// h_t = a h_{t-1} + b, y_t = sum_n C_t[n] h_t.  The decays and inputs are
+// formed in registers and never stored.
+//
+// Forward: one thread per channel holds all N = 16 state entries; a block owns
+// 128 channels x one 64-step chunk.  Phase 1 folds the chunk into one affine
+// pair per (channel, n) -- the product of the decays is exp(A sum delta), the
+// composed input is accumulated step by step -- and publishes it; decoupled
+// look-back over earlier chunks gives the state entering the chunk, which is
+// also saved as the backward's checkpoint; phase 2 re-runs the chunk and
+// writes y.
+//
+// Backward: two threads per channel (8 state entries each), blocks visit the
+// chunks last to first.  Pass A recomputes the chunk's states from the
+// checkpoint (keeping the state at every 8th step in shared memory) and folds
+// the adjoint recurrence hbar_t = C_t[n] dy_t + a_{t+1} hbar_{t+1} over the
+// chunk into one pair; look-back over later chunks gives hbar at the chunk's
+// end; pass B walks the 8-step sub-chunks backwards, recomputing their states
+// into registers, and forms dx, ddelta, dA, dB, dC, dh0.  Sums over channels
+// (dB, dC) and over batch and time (dA) are reduced in a fixed order: warp
+// transpose-reduce, per-block partials, then a small reduction kernel.
+#include <cuda_bf16.h>
+
+#include "cla_internal.cuh"
+
+namespace cla {
+namespace {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int kN = 16;        // state entries per channel
+constexpr int kTc = CLA_SELECTIVE_CKPT_CHUNK;  // 64 steps per chunk
+constexpr int kCh = 128;      // channels per block
+constexpr int kSubT = 8;      // backward sub-chunk length
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x on the FMA pipe, for the per-step decays a = exp(delta A).  Along a
+// channel with long memory (decays near 1) the error of every factor of a
+// product of many decays adds up, so the hardware approximation (about 2 ulp)
+// is not accurate enough there.  Method: split x = k + f with k = rint(x) and
+// |f| <= 1/2, evaluate 2^f = exp(f ln 2) by its Taylor series to degree 7
+// (coefficients (ln 2)^j / j!; the omitted terms are below 5.2e-9 relative),
+// and scale by 2^k by building the float with exponent field k + 127.
+// Results below 2^-126 are returned as 0 (a decay that small is 0 to fp32).
+__device__ __forceinline__ float exp2_fma(float x) {
+    x = fminf(x, 127.f);
+    const float k = rintf(x);
+    const float f = x - k;
+    float p = 1.5252733804059838e-05f;
+    p = fmaf(p, f, 1.5403530393381606e-04f);
+    p = fmaf(p, f, 1.3333558146428441e-03f);
+    p = fmaf(p, f, 9.618129107628477e-03f);
+    p = fmaf(p, f, 5.5504108664821576e-02f);
+    p = fmaf(p, f, 2.402265069591007e-01f);
+    p = fmaf(p, f, 6.931471805599453e-01f);
+    p = fmaf(p, f, 1.0f);
+    const int e = (int)k + 127;
+    const float scale = __int_as_float(max(e, 0) << 23);
+    return e > 0 ? p * scale : 0.f;
+}
+
+struct SelGeom {
+    int B, D, n_chunks, n_cblk;
+    long long T;
+};
+
+struct SelWs {
+    WsHeader *hdr;
+    unsigned int *flags;  // per unit (chunk, b, cblk)
+    float *agg;           // forward: [unit][17][128]; backward: [unit][32][128]
+    float *incl;          // [unit][16][128]
+    float *partB;         // [B][T][n_cblk][16]
+    float *partC;
+    float *partA;         // [B][n_chunks][D][16]
+};
+
+__device__ __forceinline__ size_t sel_unit(const SelGeom &g, int chunk, int b, int cblk) {
+    return ((size_t)chunk * g.B + b) * g.n_cblk + cblk;
+}
+
+// ------------------------------------------------------------------ forward
+struct SelFwdSmem {
+    float x[kTc][kCh];
+    float d[kTc][kCh];
+    float B[kTc][kN];
+    float C[kTc][kN];
+};
+
+__global__ void __launch_bounds__(kCh)
+sel_fwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, const float *__restrict__ A,
+               const bf16 *__restrict__ Bm, const bf16 *__restrict__ Cm, const float *__restrict__ h0,
+               float *__restrict__ y, float *__restrict__ hT, float *__restrict__ ckpt, SelGeom g, SelWs ws) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SelFwdSmem &sm = *reinterpret_cast<SelFwdSmem *>(smem_raw);
+    float(&s_x)[kTc][kCh] = sm.x;
+    float(&s_d)[kTc][kCh] = sm.d;
+    float(&s_B)[kTc][kN] = sm.B;
+    float(&s_C)[kTc][kN] = sm.C;
+    __shared__ unsigned int s_ticket, s_flag;
+
+    const int tid = threadIdx.x;
+    if (tid == 0) s_ticket = atomicAdd(&ws.hdr->ticket[0], 1u);
+    __syncthreads();
+    const unsigned int tk = s_ticket;
+    const int per_chunk = g.B * g.n_cblk;
+    const int chunk = (int)(tk / per_chunk);
+    const int bi = (int)(tk % per_chunk) / g.n_cblk;
+    const int cblk = (int)(tk % per_chunk) % g.n_cblk;
+    const int c = cblk * kCh + tid;
+    const bool cok = c < g.D;
+    const long long t0 = (long long)chunk * kTc;
+    const int L = (int)min((long long)kTc, g.T - t0);
+    const size_t unit = sel_unit(g, chunk, bi, cblk);
+
+    // stage the chunk: own channel column of x and delta, shared B_t and C_t rows
+#pragma unroll 8
+    for (int r = 0; r < kTc; ++r) {
+        const bool ok = cok && r < L;
+        const size_t idx = ((size_t)bi * g.T + t0 + r) * g.D + c;
+        s_x[r][tid] = ok ? __bfloat162float(x[idx]) : 0.f;
+        s_d[r][tid] = ok ? __ldcs(delta + idx) : 0.f;
+    }
+    for (int i = tid; i < kTc * kN; i += kCh) {
+        const int r = i / kN, n = i % kN;
+        const bool ok = r < L;
+        const size_t idx = ((size_t)bi * g.T + t0 + r) * kN + n;
+        s_B[r][n] = ok ? __bfloat162float(Bm[idx]) : 0.f;
+        s_C[r][n] = ok ? __bfloat162float(Cm[idx]) : 0.f;
+    }
+    __syncthreads();
+
+    float A2[kN];
+#pragma unroll
+    for (int n = 0; n < kN; ++n) A2[n] = cok ? A[(size_t)c * kN + n] * kLog2e : 0.f;
+
+    // phase 1: the chunk as one pair per n: (exp(A sum delta), Bagg)
+    float Bagg[kN];
+#pragma unroll
+    for (int n = 0; n < kN; ++n) Bagg[n] = 0.f;
+    float sumd = 0.f;
+    for (int r = 0; r < L; ++r) {
+        const float d = s_d[r][tid];
+        const float dx = d * s_x[r][tid];
+#pragma unroll
+        for (int n = 0; n < kN; ++n) Bagg[n] = fmaf(exp2_fma(d * A2[n]), Bagg[n], dx * s_B[r][n]);
+        sumd += d;
+    }
+
+    float hin[kN];
+    if (chunk == 0) {
+#pragma unroll
+        for (int n = 0; n < kN; ++n) hin[n] = (h0 != nullptr && cok) ? h0[((size_t)bi * g.D + c) * kN + n] : 0.f;
+    } else {
+        float *ag = ws.agg + unit * (17 * kCh);
+        __stcg(ag + tid, sumd);
+#pragma unroll
+        for (int n = 0; n < kN; ++n) __stcg(ag + (1 + n) * kCh + tid, Bagg[n]);
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release(ws.flags + unit, 1u);
+        float accS = 0.f, accB[kN];
+#pragma unroll
+        for (int n = 0; n < kN; ++n) accB[n] = 0.f;
+        int j = chunk - 1;
+        while (true) {
+            const size_t up = sel_unit(g, j, bi, cblk);
+            if (tid == 0) s_flag = wait_flag(ws.flags + up, ws.hdr, 20u);
+            __syncthreads();
+            const unsigned int f = s_flag;
+            __syncthreads();
+            if (f == 2u) {
+                const float *ic = ws.incl + up * (kN * kCh);
+#pragma unroll
+                for (int n = 0; n < kN; ++n) hin[n] = fmaf(exp2_fma(A2[n] * accS), ld_cg(ic + n * kCh + tid), accB[n]);
+                break;
+            } else if (f == 1u) {
+                const float *pa = ws.agg + up * (17 * kCh);
+#pragma unroll
+                for (int n = 0; n < kN; ++n) accB[n] = fmaf(exp2_fma(A2[n] * accS), ld_cg(pa + (1 + n) * kCh + tid), accB[n]);
+                accS += ld_cg(pa + tid);
+                if (--j < 0) {
+#pragma unroll
+                    for (int n = 0; n < kN; ++n) {
+                        const float s0 = (h0 != nullptr && cok) ? h0[((size_t)bi * g.D + c) * kN + n] : 0.f;
+                        hin[n] = fmaf(exp2_fma(A2[n] * accS), s0, accB[n]);
+                    }
+                    break;
+                }
+            } else {
+#pragma unroll
+                for (int n = 0; n < kN; ++n) hin[n] = 0.f;
+                break;
+            }
+        }
+    }
+    {
+        float *ic = ws.incl + unit * (kN * kCh);
+#pragma unroll
+        for (int n = 0; n < kN; ++n) __stcg(ic + n * kCh + tid, fmaf(exp2_fma(A2[n] * sumd), hin[n], Bagg[n]));
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release(ws.flags + unit, 2u);
+    }
+    if (ckpt != nullptr && cok) {
+        float4 *ck = reinterpret_cast<float4 *>(ckpt + (((size_t)bi * g.n_chunks + chunk) * g.D + c) * kN);
+#pragma unroll
+        for (int q = 0; q < kN / 4; ++q) ck[q] = make_float4(hin[4 * q], hin[4 * q + 1], hin[4 * q + 2], hin[4 * q + 3]);
+    }
+
+    // phase 2: re-run from the true incoming state; write y once
+    float h[kN];
+#pragma unroll
+    for (int n = 0; n < kN; ++n) h[n] = hin[n];
+    for (int r = 0; r < L; ++r) {
+        const float d = s_d[r][tid];
+        const float dx = d * s_x[r][tid];
+        float acc = 0.f;
+#pragma unroll
+        for (int n = 0; n < kN; ++n) {
+            h[n] = fmaf(exp2_fma(d * A2[n]), h[n], dx * s_B[r][n]);
+            acc = fmaf(s_C[r][n], h[n], acc);
+        }
+        if (cok) __stcs(y + ((size_t)bi * g.T + t0 + r) * g.D + c, acc);
+    }
+    if (hT != nullptr && cok && chunk == g.n_chunks - 1) {
+#pragma unroll
+        for (int n = 0; n < kN; ++n) hT[((size_t)bi * g.D + c) * kN + n] = h[n];
+    }
+}
+
+// ------------------------------------------------------------------ backward
+constexpr int kBwdThreads = 2 * kCh;  // two threads per channel, 8 state entries each
+constexpr int kNh = kN / 2;
+
+struct SelBwdSmem {
+    float x[kTc][kCh];
+    float d[kTc + 1][kCh];  // row kTc: delta of the next chunk's first step
+    float dy[kTc][kCh];
+    float Bs[kTc][kN];
+    float Cs[kTc][kN];
+    float bnd[kTc / kSubT][kBwdThreads][kNh];  // state before every 8th step
+    float red[kSubT][kBwdThreads / 32][2][kN];  // per-warp channel sums of dB, dC
+};
+
+// Sum of v[0..7] over the 16 lanes of this warp that share bit 0 of the lane
+// index; returns the total for entry 4*b4 + 2*b3 + b2 (bits of the lane).
+__device__ __forceinline__ float transpose_reduce8(float (&v)[kNh], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float w4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float send = b4 ? v[j] : v[j + 4];
+        const float keep = b4 ? v[j + 4] : v[j];
+        w4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    float w2[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float send = b3 ? w4[j] : w4[j + 2];
+        const float keep = b3 ? w4[j + 2] : w4[j];
+        w2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    const float send = b2 ? w2[0] : w2[1];
+    const float keep = b2 ? w2[1] : w2[0];
+    float w1 = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    w1 += __shfl_xor_sync(0xffffffffu, w1, 2);
+    return w1;
+}
+
+__global__ void __launch_bounds__(kBwdThreads)
+sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, const float *__restrict__ A,
+               const bf16 *__restrict__ Bm, const bf16 *__restrict__ Cm, const float *__restrict__ ckpt,
+               const float *__restrict__ dy, const float *__restrict__ dhT, float *__restrict__ dx,
+               float *__restrict__ ddelta, float *__restrict__ dh0, SelGeom g, SelWs ws) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SelBwdSmem &sm = *reinterpret_cast<SelBwdSmem *>(smem_raw);
+    __shared__ unsigned int s_ticket, s_flag;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_ticket = atomicAdd(&ws.hdr->ticket[1], 1u);
+    __syncthreads();
+    const unsigned int tk = s_ticket;
+    const int per_chunk = g.B * g.n_cblk;
+    const int chunk = g.n_chunks - 1 - (int)(tk / per_chunk);
+    const int bi = (int)(tk % per_chunk) / g.n_cblk;
+    const int cblk = (int)(tk % per_chunk) % g.n_cblk;
+    const int cl = tid >> 1, ng = tid & 1, n0 = ng * kNh;
+    const int c = cblk * kCh + cl;
+    const bool cok = c < g.D;
+    const long long t0 = (long long)chunk * kTc;
+    const int L = (int)min((long long)kTc, g.T - t0);
+    const bool last = chunk == g.n_chunks - 1;
+    const size_t unit = sel_unit(g, chunk, bi, cblk);
+
+    for (int i = tid; i < kTc * kCh; i += kBwdThreads) {
+        const int r = i / kCh, cc = i % kCh;
+        const int ch = cblk * kCh + cc;
+        const bool ok = ch < g.D && r < L;
+        const size_t idx = ((size_t)bi * g.T + t0 + r) * g.D + ch;
+        sm.x[r][cc] = ok ? __bfloat162float(x[idx]) : 0.f;
+        sm.d[r][cc] = ok ? delta[idx] : 0.f;
+        sm.dy[r][cc] = ok ? __ldcs(dy + idx) : 0.f;
+    }
+    for (int cc = tid; cc < kCh; cc += kBwdThreads) {
+        const int ch = cblk * kCh + cc;
+        sm.d[kTc][cc] = (!last && ch < g.D) ? delta[((size_t)bi * g.T + t0 + kTc) * g.D + ch] : 0.f;
+    }
+    for (int i = tid; i < kTc * kN; i += kBwdThreads) {
+        const int r = i / kN, n = i % kN;
+        const bool ok = r < L;
+        const size_t idx = ((size_t)bi * g.T + t0 + r) * kN + n;
+        sm.Bs[r][n] = ok ? __bfloat162float(Bm[idx]) : 0.f;
+        sm.Cs[r][n] = ok ? __bfloat162float(Cm[idx]) : 0.f;
+    }
+    __syncthreads();
+
+    float A2[kNh], Ar[kNh];
+#pragma unroll
+    for (int n = 0; n < kNh; ++n) {
+        Ar[n] = cok ? A[(size_t)c * kN + n0 + n] : 0.f;
+        A2[n] = Ar[n] * kLog2e;
+    }
+    // pass A: states (every 8th kept) and the adjoint pair of the chunk
+    float h[kNh], P[kNh], Bg[kNh];
+    {
+        const float *ck = ckpt + (((size_t)bi * g.n_chunks + chunk) * g.D + (cok ? c : 0)) * kN + n0;
+#pragma unroll
+        for (int n = 0; n < kNh; ++n) {
+            h[n] = cok ? ck[n] : 0.f;
+            P[n] = 1.f;
+            Bg[n] = 0.f;
+        }
+    }
+    for (int r = 0; r < L; ++r) {
+        if ((r % kSubT) == 0) {
+#pragma unroll
+            for (int n = 0; n < kNh; ++n) sm.bnd[r / kSubT][tid][n] = h[n];
+        }
+        const float d = sm.d[r][cl];
+        const float dxv = d * sm.x[r][cl];
+        const float gy = sm.dy[r][cl];
+#pragma unroll
+        for (int n = 0; n < kNh; ++n) {
+            const float a = exp2_fma(d * A2[n]);
+            if (r > 0) P[n] *= a;
+            Bg[n] = fmaf(P[n], sm.Cs[r][n0 + n] * gy, Bg[n]);
+            h[n] = fmaf(a, h[n], dxv * sm.Bs[r][n0 + n]);
+        }
+    }
+    float aend[kNh], Ag[kNh];
+#pragma unroll
+    for (int n = 0; n < kNh; ++n) {
+        aend[n] = last ? 1.f : exp2_fma(sm.d[kTc][cl] * A2[n]);
+        Ag[n] = P[n] * aend[n];
+    }
+    // look-back toward later chunks for hbar at the chunk's end
+    float hb[kNh];
+    if (last) {
+#pragma unroll
+        for (int n = 0; n < kNh; ++n) hb[n] = (dhT != nullptr && cok) ? dhT[((size_t)bi * g.D + c) * kN + n0 + n] : 0.f;
+    } else {
+        float *ag = ws.agg + unit * (32 * kCh);
+#pragma unroll
+        for (int n = 0; n < kNh; ++n) {
+            __stcg(ag + (n0 + n) * kCh + cl, Ag[n]);
+            __stcg(ag + (16 + n0 + n) * kCh + cl, Bg[n]);
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release(ws.flags + unit, 1u);
+        float accA[kNh], accB[kNh];
+#pragma unroll
+        for (int n = 0; n < kNh; ++n) { accA[n] = 1.f; accB[n] = 0.f; }
+        int j = chunk + 1;
+        while (true) {
+            const size_t up = sel_unit(g, j, bi, cblk);
+            if (tid == 0) s_flag = wait_flag(ws.flags + up, ws.hdr, 21u);
+            __syncthreads();
+            const unsigned int f = s_flag;
+            __syncthreads();
+            if (f == 2u) {
+                const float *ic = ws.incl + up * (kN * kCh);
+#pragma unroll
+                for (int n = 0; n < kNh; ++n) hb[n] = fmaf(accA[n], ld_cg(ic + (n0 + n) * kCh + cl), accB[n]);
+                break;
+            } else if (f == 1u) {
+                const float *pa = ws.agg + up * (32 * kCh);
+#pragma unroll
+                for (int n = 0; n < kNh; ++n) {
+                    accB[n] = fmaf(accA[n], ld_cg(pa + (16 + n0 + n) * kCh + cl), accB[n]);
+                    accA[n] *= ld_cg(pa + (n0 + n) * kCh + cl);
+                }
+                if (++j >= g.n_chunks) {
+#pragma unroll
+                    for (int n = 0; n < kNh; ++n) {
+                        const float s = (dhT != nullptr && cok) ? dhT[((size_t)bi * g.D + c) * kN + n0 + n] : 0.f;
+                        hb[n] = fmaf(accA[n], s, accB[n]);
+                    }
+                    break;
+                }
+            } else {
+#pragma unroll
+                for (int n = 0; n < kNh; ++n) hb[n] = 0.f;
+                break;
+            }
+        }
+    }
+    {
+        float *ic = ws.incl + unit * (kN * kCh);
+#pragma unroll
+        for (int n = 0; n < kNh; ++n) __stcg(ic + (n0 + n) * kCh + cl, fmaf(Ag[n], hb[n], Bg[n]));
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release(ws.flags + unit, 2u);
+    }
+
+    // pass B: sub-chunks from last to first
+    float anext[kNh], dA_acc[kNh];
+#pragma unroll
+    for (int n = 0; n < kNh; ++n) { anext[n] = aend[n]; dA_acc[n] = 0.f; }
+    const int nsub = (L + kSubT - 1) / kSubT;
+    for (int k = nsub - 1; k >= 0; --k) {
+        float hs[kSubT][kNh], hstart[kNh];
+#pragma unroll
+        for (int n = 0; n < kNh; ++n) {
+            hstart[n] = sm.bnd[k][tid][n];
+            h[n] = hstart[n];
+        }
+#pragma unroll
+        for (int i = 0; i < kSubT; ++i) {
+            const int r = k * kSubT + i;
+            const bool ok = r < L;
+            const float d = ok ? sm.d[r][cl] : 0.f;
+            const float dxv = d * (ok ? sm.x[r][cl] : 0.f);
+#pragma unroll
+            for (int n = 0; n < kNh; ++n) {
+                if (ok) h[n] = fmaf(exp2_fma(d * A2[n]), h[n], dxv * sm.Bs[r][n0 + n]);
+                hs[i][n] = h[n];
+            }
+        }
+#pragma unroll
+        for (int i = kSubT - 1; i >= 0; --i) {
+            const int r = k * kSubT + i;
+            float vB[kNh], vC[kNh];
+            if (r < L) {
+                const float d = sm.d[r][cl], xv = sm.x[r][cl], gy = sm.dy[r][cl];
+                float sx = 0.f, sd = 0.f;
+#pragma unroll
+                for (int n = 0; n < kNh; ++n) {
+                    const float Bn = sm.Bs[r][n0 + n], Cn = sm.Cs[r][n0 + n];
+                    hb[n] = fmaf(anext[n], hb[n], Cn * gy);
+                    const float a = exp2_fma(d * A2[n]);
+                    const float hp = (i > 0) ? hs[i - 1][n] : hstart[n];
+                    const float ga = hb[n] * hp * a;  // dL/da_t * a_t
+                    sx = fmaf(hb[n], Bn, sx);
+                    sd = fmaf(ga, Ar[n], fmaf(hb[n], Bn * xv, sd));
+                    dA_acc[n] = fmaf(ga, d, dA_acc[n]);
+                    vB[n] = hb[n] * d * xv;
+                    vC[n] = gy * hs[i][n];
+                    anext[n] = a;
+                }
+                sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+                sd += __shfl_xor_sync(0xffffffffu, sd, 1);
+                if (ng == 0 && cok) {
+                    const size_t idx = ((size_t)bi * g.T + t0 + r) * g.D + c;
+                    __stcs(dx + idx, sx * d);
+                    __stcs(ddelta + idx, sd);
+                }
+                if (r == 0 && chunk == 0 && dh0 != nullptr && cok) {
+#pragma unroll
+                    for (int n = 0; n < kNh; ++n) dh0[((size_t)bi * g.D + c) * kN + n0 + n] = anext[n] * hb[n];
+                }
+            } else {
+#pragma unroll
+                for (int n = 0; n < kNh; ++n) { vB[n] = 0.f; vC[n] = 0.f; }
+            }
+            if (!cok) {
+#pragma unroll
+                for (int n = 0; n < kNh; ++n) { vB[n] = 0.f; vC[n] = 0.f; }
+            }
+            // channel sums of this warp's 16 channels; lane keeps entry e of its half
+            const float sB = transpose_reduce8(vB, lane);
+            const float sC = transpose_reduce8(vC, lane);
+            if ((lane & 2) == 0) {
+                const int e = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+                sm.red[i][warp][0][n0 + e] = sB;
+                sm.red[i][warp][1][n0 + e] = sC;
+            }
+        }
+        __syncthreads();
+        // block partials over the 128 channels, in warp order
+        {
+            const int i = tid >> 5, w = tid & 31;  // 8 steps x (2 quantities x 16 entries)
+            const int q = w >> 4, n = w & 15;
+            const int r = k * kSubT + i;
+            if (r < L) {
+                float s = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < kBwdThreads / 32; ++ww) s += sm.red[i][ww][q][n];
+                float *dst = (q == 0 ? ws.partB : ws.partC);
+                dst[(((size_t)bi * g.T + t0 + r) * g.n_cblk + cblk) * kN + n] = s;
+            }
+        }
+        __syncthreads();
+    }
+    if (ws.partA != nullptr && cok) {
+        float *pa = ws.partA + (((size_t)bi * g.n_chunks + chunk) * g.D + c) * kN + n0;
+#pragma unroll
+        for (int n = 0; n < kNh; ++n) pa[n] = dA_acc[n];
+    }
+}
+
+// dB, dC: sums of the per-block partials, in block order.
+__global__ void sel_reduce_bc_kernel(const float *__restrict__ partB, const float *__restrict__ partC,
+                                     float *__restrict__ dB, float *__restrict__ dC, long long rows, int n_cblk) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // (b, t, n)
+    if (i >= rows * kN) return;
+    const long long row = i / kN;
+    const int n = (int)(i % kN);
+    float sb = 0.f, sc = 0.f;
+    for (int k = 0; k < n_cblk; ++k) {
+        sb += partB[(row * n_cblk + k) * kN + n];
+        sc += partC[(row * n_cblk + k) * kN + n];
+    }
+    dB[i] = sb;
+    dC[i] = sc;
+}
+
+// dA[d][n]: sum over batch rows and chunks, in that order.
+__global__ void sel_reduce_a_kernel(const float *__restrict__ partA, float *__restrict__ dA, int B, int n_chunks,
+                                    int D) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // (d, n)
+    if (i >= (long long)D * kN) return;
+    float s = 0.f;
+    for (int b = 0; b < B; ++b)
+        for (int j = 0; j < n_chunks; ++j) s += partA[((size_t)b * n_chunks + j) * D * kN + i];
+    dA[i] = s;
+}
+
+// ------------------------------------------------------------------ host side
+struct SelPlan {
+    SelGeom g;
+    size_t units;
+    size_t off_flags, off_agg, off_incl, off_pB, off_pC, off_pA, total;
+};
+
+SelPlan sel_plan(int64_t B, int64_t T, int64_t D) {
+    SelPlan p;
+    p.g.B = (int)B;
+    p.g.D = (int)D;
+    p.g.T = T;
+    p.g.n_chunks = (int)((T + kTc - 1) / kTc);
+    p.g.n_cblk = (int)((D + kCh - 1) / kCh);
+    p.units = (size_t)p.g.n_chunks * B * p.g.n_cblk;
+    p.off_flags = sizeof(WsHeader);
+    p.off_agg = align_up(p.off_flags + p.units * 4, 256);
+    p.off_incl = align_up(p.off_agg + p.units * 32 * kCh * 4, 256);
+    p.off_pB = align_up(p.off_incl + p.units * kN * kCh * 4, 256);
+    p.off_pC = align_up(p.off_pB + (size_t)B * T * p.g.n_cblk * kN * 4, 256);
+    p.off_pA = align_up(p.off_pC + (size_t)B * T * p.g.n_cblk * kN * 4, 256);
+    p.total = align_up(p.off_pA + (size_t)B * p.g.n_chunks * D * kN * 4, 256);
+    return p;
+}
+
+SelWs sel_bind(const SelPlan &p, void *ws) {
+    char *w = static_cast<char *>(ws);
+    SelWs s;
+    s.hdr = reinterpret_cast<WsHeader *>(w);
+    s.flags = reinterpret_cast<unsigned int *>(w + p.off_flags);
+    s.agg = reinterpret_cast<float *>(w + p.off_agg);
+    s.incl = reinterpret_cast<float *>(w + p.off_incl);
+    s.partB = reinterpret_cast<float *>(w + p.off_pB);
+    s.partC = reinterpret_cast<float *>(w + p.off_pC);
+    s.partA = reinterpret_cast<float *>(w + p.off_pA);
+    return s;
+}
+
+int sel_validate(const char *fn, int64_t B, int64_t T, int64_t D, int64_t N) {
+    if (B < 0 || T < 0 || D < 0 || N < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (N != kN) return fail(CLA_ERR_UNSUPPORTED, "%s: N must be %d (got %lld)", fn, kN, (long long)N);
+    if (D > (1 << 24) || B > (1 << 20) || T > (1ll << 36)) return fail(CLA_ERR_UNSUPPORTED, "%s: size out of range", fn);
+    const int64_t grid = ((T + kTc - 1) / kTc) * B * ((D + kCh - 1) / kCh);
+    if (grid >= (1ll << 31)) return fail(CLA_ERR_UNSUPPORTED, "%s: problem too large for one launch", fn);
+    return CLA_OK;
+}
+
+}  // namespace
+}  // namespace cla
+
+using namespace cla;
+
+extern "C" size_t cla_selective_scan_workspace_size(int64_t B, int64_t T, int64_t D, int64_t N) {
+    if (B < 0 || T < 0 || D < 0 || N != kN) return 0;
+    return sel_plan(B, T, D).total;
+}
+
+extern "C" size_t cla_selective_scan_ckpt_elems(int64_t B, int64_t T, int64_t D, int64_t N) {
+    if (B < 0 || T < 0 || D < 0 || N < 0) return 0;
+    return (size_t)B * (size_t)((T + kTc - 1) / kTc) * (size_t)D * (size_t)N;
+}
+
+extern "C" int cla_selective_scan_fwd(const uint16_t *x, const float *delta, const float *A, const uint16_t *Bm,
+                                      const uint16_t *Cm, const float *h0, float *y, float *hT, float *ckpt,
+                                      int64_t B, int64_t T, int64_t D, int64_t N, void *ws, size_t ws_bytes,
+                                      void *stream) {
+    clear_error();
+    const char *fn = "cla_selective_scan_fwd";
+    int st = sel_validate(fn, B, T, D, N);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (B == 0 || D == 0) return CLA_OK;
+    if (T == 0) {
+        if (hT) {
+            const size_t by = sizeof(float) * B * D * N;
+            if (h0) CLA_CUDA_TRY(cudaMemcpyAsync(hT, h0, by, cudaMemcpyDeviceToDevice, s), fn);
+            else CLA_CUDA_TRY(cudaMemsetAsync(hT, 0, by, s), fn);
+        }
+        return CLA_OK;
+    }
+    if (!x || !delta || !A || !Bm || !Cm || !y) return fail(CLA_ERR_INVALID_ARG, "%s: x, delta, A, Bm, Cm, y required", fn);
+    if (!aligned16_or_null(ckpt)) return fail(CLA_ERR_INVALID_ARG, "%s: ckpt must be 16-byte aligned", fn);
+    if (!ws || !aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace NULL or unaligned", fn);
+    const SelPlan p = sel_plan(B, T, D);
+    if (ws_bytes < p.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, p.total);
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.off_agg, s), fn);
+    const SelWs w = sel_bind(p, ws);
+    static bool configured = false;
+    if (!configured) {
+        CLA_CUDA_TRY(cudaFuncSetAttribute(sel_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)sizeof(SelFwdSmem)),
+                     fn);
+        configured = true;
+    }
+    const unsigned int grid = (unsigned int)((size_t)p.g.n_chunks * B * p.g.n_cblk);
+    sel_fwd_kernel<<<grid, kCh, sizeof(SelFwdSmem), s>>>(reinterpret_cast<const bf16 *>(x), delta, A, reinterpret_cast<const bf16 *>(Bm),
+                                        reinterpret_cast<const bf16 *>(Cm), h0, y, hT, ckpt, p.g, w);
+    return check_launch(fn);
+}
+
+extern "C" int cla_selective_scan_bwd(const uint16_t *x, const float *delta, const float *A, const uint16_t *Bm,
+                                      const uint16_t *Cm, const float *h0, const float *ckpt, const float *dy,
+                                      const float *dhT, float *dx, float *ddelta, float *dA, float *dB, float *dC,
+                                      float *dh0, int64_t B, int64_t T, int64_t D, int64_t N, void *ws,
+                                      size_t ws_bytes, void *stream) {
+    clear_error();
+    const char *fn = "cla_selective_scan_bwd";
+    int st = sel_validate(fn, B, T, D, N);
+    if (st) return st;
+    (void)h0;  // the checkpoints already contain the initial state
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (B == 0 || D == 0) {
+        if (dA && D > 0) CLA_CUDA_TRY(cudaMemsetAsync(dA, 0, sizeof(float) * D * N, s), fn);
+        return CLA_OK;
+    }
+    if (T == 0) {
+        if (dA) CLA_CUDA_TRY(cudaMemsetAsync(dA, 0, sizeof(float) * D * N, s), fn);
+        if (dh0) {
+            const size_t by = sizeof(float) * B * D * N;
+            if (dhT) CLA_CUDA_TRY(cudaMemcpyAsync(dh0, dhT, by, cudaMemcpyDeviceToDevice, s), fn);
+            else CLA_CUDA_TRY(cudaMemsetAsync(dh0, 0, by, s), fn);
+        }
+        return CLA_OK;
+    }
+    if (!x || !delta || !A || !Bm || !Cm || !ckpt || !dy || !dx || !ddelta || !dB || !dC)
+        return fail(CLA_ERR_INVALID_ARG, "%s: x, delta, A, Bm, Cm, ckpt, dy, dx, ddelta, dB, dC required", fn);
+    if (!ws || !aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace NULL or unaligned", fn);
+    const SelPlan p = sel_plan(B, T, D);
+    if (ws_bytes < p.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, p.total);
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.off_agg, s), fn);
+    SelWs w = sel_bind(p, ws);
+    if (!dA) w.partA = nullptr;
+    static bool configured = false;
+    if (!configured) {
+        CLA_CUDA_TRY(cudaFuncSetAttribute(sel_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)sizeof(SelBwdSmem)),
+                     fn);
+        configured = true;
+    }
+    const unsigned int grid = (unsigned int)((size_t)p.g.n_chunks * B * p.g.n_cblk);
+    sel_bwd_kernel<<<grid, kBwdThreads, sizeof(SelBwdSmem), s>>>(
+        reinterpret_cast<const bf16 *>(x), delta, A, reinterpret_cast<const bf16 *>(Bm),
+        reinterpret_cast<const bf16 *>(Cm), ckpt, dy, dhT, dx, ddelta, dh0, p.g, w);
+    st = check_launch(fn);
+    if (st) return st;
+    const long long rows = B * T;
+    sel_reduce_bc_kernel<<<(unsigned int)((rows * kN + 255) / 256), 256, 0, s>>>(w.partB, w.partC, dB, dC, rows,
+                                                                                p.g.n_cblk);
+    st = check_launch(fn);
+    if (st) return st;
+    if (dA) {
+        sel_reduce_a_kernel<<<(unsigned int)((D * kN + 255) / 256), 256, 0, s>>>(w.partA, dA, (int)B, p.g.n_chunks,
+                                                                               (int)D);
+        st = check_launch(fn);
+    }
+    return st;
+}
