@@ -24,8 +24,8 @@
 //   5. every lane re-runs its L steps from its true starting state and
 //      writes h once.
 // HBM traffic is the algorithmic 12 B per element forward (read a, b; write
-// h) and 20 B backward (read a, h, dh; write da, db), plus 48 B per chunk
-// and 4 channels of look-back payload.
+// h) and 20 B backward (read a, h, dh; write da, db), plus 24 B of look-back
+// payload per chunk and channel (about 0.4 B per element, L2-resident).
 #include <mutex>
 
 #include "cla_internal.cuh"
@@ -55,13 +55,6 @@ struct VecIO<4> {
     static __device__ __forceinline__ void store(float *p, const float (&v)[4]) {
         __stcs(reinterpret_cast<float4 *>(p), make_float4(v[0], v[1], v[2], v[3]));
     }
-    static __device__ __forceinline__ void store_ws(float4 *p, const float (&v)[4]) {
-        __stcg(p, make_float4(v[0], v[1], v[2], v[3]));
-    }
-    static __device__ __forceinline__ void load_ws(const float4 *p, float (&v)[4]) {
-        float4 x = ld_cg4(p);
-        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-    }
 };
 
 template <>
@@ -69,21 +62,83 @@ struct VecIO<1> {
     static __device__ __forceinline__ void load(const float *p, float (&v)[1]) { v[0] = __ldg(p); }
     static __device__ __forceinline__ void load_cs(const float *p, float (&v)[1]) { v[0] = __ldcs(p); }
     static __device__ __forceinline__ void store(float *p, const float (&v)[1]) { __stcs(p, v[0]); }
-    static __device__ __forceinline__ void store_ws(float4 *p, const float (&v)[1]) {
-        __stcg(reinterpret_cast<float *>(p), v[0]);
-    }
-    static __device__ __forceinline__ void load_ws(const float4 *p, float (&v)[1]) {
-        v[0] = ld_cg(reinterpret_cast<const float *>(p));
-    }
 };
 
+// Look-back payload: per (chunk, batch row, warp column, channel group) and
+// per channel, three 64-bit words -- the chunk's decay product A, its
+// composed input B, and the state at its far edge (inclusive) -- each holding
+// the float value in its low half and its status in its high half (0 not yet
+// written, 1 aggregate, 2 inclusive).  A word is written and read with one
+// relaxed 64-bit access, which is single-copy atomic, so a reader that sees
+// the status also sees the value: no memory fence is on the critical path.
 struct ScanWs {
     WsHeader *hdr;
-    unsigned int *flags;  // per (chunk, b, warp-column, cg): 0 none, 1 aggregate, 2 inclusive
-    float4 *aggA;         // product of the chunk's decays
-    float4 *aggB;         // the chunk's composed input
-    float4 *incl;         // state at the chunk's end (forward) / start (backward)
+    unsigned long long *words;  // [unit][3][4]
 };
+
+constexpr unsigned int kWordA = 0, kWordB = 1, kWordIncl = 2;
+
+__device__ __forceinline__ void pub_word(unsigned long long *p, float v, unsigned int status) {
+    const unsigned long long w = ((unsigned long long)status << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ unsigned long long peek_word(const unsigned long long *p) {
+    unsigned long long w;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+__device__ __forceinline__ unsigned int word_status(unsigned long long w) { return (unsigned int)(w >> 32); }
+__device__ __forceinline__ float word_value(unsigned long long w) { return __uint_as_float((unsigned int)w); }
+
+template <int VEC>
+__device__ __forceinline__ void publish(const ScanWs &ws, size_t u, unsigned int kind, const float (&v)[VEC],
+                                        unsigned int status) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) pub_word(ws.words + (u * 3 + kind) * 4 + i, v[i], status);
+}
+
+// One step of the look-back walk at unit `up`: returns 2 when the unit's
+// inclusive state was found (res = accA * incl + accB), 1 when its aggregate
+// was composed into (accA, accB), 0 when the bounded wait gave up.
+template <int VEC>
+__device__ __forceinline__ unsigned int look_at(const ScanWs &ws, size_t up, float (&accA)[VEC], float (&accB)[VEC],
+                                                float (&res)[VEC], unsigned int where) {
+    const unsigned long long *base = ws.words + up * 12;
+    for (unsigned int it = 0; it < kSpinLimit; ++it) {
+        unsigned long long wi[VEC];
+        bool all2 = true;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            wi[i] = peek_word(base + kWordIncl * 4 + i);
+            all2 = all2 && word_status(wi[i]) == 2u;
+        }
+        if (all2) {
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) res[i] = fmaf(accA[i], word_value(wi[i]), accB[i]);
+            return 2u;
+        }
+        unsigned long long wa[VEC], wb[VEC];
+        bool all1 = true;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            wa[i] = peek_word(base + kWordA * 4 + i);
+            wb[i] = peek_word(base + kWordB * 4 + i);
+            all1 = all1 && word_status(wa[i]) == 1u && word_status(wb[i]) == 1u;
+        }
+        if (all1) {
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) {  // the unit's chunk happened before acc
+                accB[i] = fmaf(accA[i], word_value(wb[i]), accB[i]);
+                accA[i] *= word_value(wa[i]);
+            }
+            return 1u;
+        }
+        if (it >= 8) __nanosleep(100);
+    }
+    atomicOr(&ws.hdr->error, kErrTimeout);
+    atomicExch(&ws.hdr->where, where);
+    return 0u;
+}
 
 struct ScanGeom {
     int B, D, n_chunks, n_cw, n_cblk;
@@ -100,7 +155,7 @@ __device__ __forceinline__ size_t unit_index(const ScanGeom &g, int chunk, int b
 
 // ------------------------------------------------------------------ forward
 template <int VEC>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 2)
 scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
                      const float *__restrict__ h0, float *__restrict__ h,
                      float *__restrict__ hT, ScanGeom g, ScanWs ws) {
@@ -174,42 +229,20 @@ scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
             for (int v = 0; v < VEC; ++v)
                 hin[v] = (h0 != nullptr && cok) ? h0[(size_t)bi * g.D + c0 + v] : 0.f;
         } else {
-            VecIO<VEC>::store_ws(ws.aggA + u, A);
-            VecIO<VEC>::store_ws(ws.aggB + u, Bc);
-            st_release(ws.flags + u, 1u);
+            publish<VEC>(ws, u, kWordA, A, 1u);
+            publish<VEC>(ws, u, kWordB, Bc, 1u);
             float accA[VEC], accB[VEC];
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) { accA[v] = 1.f; accB[v] = 0.f; }
-            int j = chunk - 1;
-            while (true) {
-                const size_t up = unit_index(g, j, bi, cw, cg);
-                const unsigned int f = wait_flag(ws.flags + up, ws.hdr, 1u);
-                if (f == 2u) {
-                    float s[VEC];
-                    VecIO<VEC>::load_ws(ws.incl + up, s);
+            for (int v = 0; v < VEC; ++v) { accA[v] = 1.f; accB[v] = 0.f; hin[v] = 0.f; }
+            for (int j = chunk - 1;; --j) {
+                const unsigned int f = look_at<VEC>(ws, unit_index(g, j, bi, cw, cg), accA, accB, hin, 1u);
+                if (f != 1u) break;  // inclusive found (or the wait gave up)
+                if (j == 0) {        // reached the sequence start: apply h0
 #pragma unroll
-                    for (int v = 0; v < VEC; ++v) hin[v] = fmaf(accA[v], s[v], accB[v]);
-                    break;
-                } else if (f == 1u) {
-                    float pa[VEC], pb[VEC];
-                    VecIO<VEC>::load_ws(ws.aggA + up, pa);
-                    VecIO<VEC>::load_ws(ws.aggB + up, pb);
-#pragma unroll
-                    for (int v = 0; v < VEC; ++v) {  // chunk j happened before acc
-                        accB[v] = fmaf(accA[v], pb[v], accB[v]);
-                        accA[v] *= pa[v];
+                    for (int v = 0; v < VEC; ++v) {
+                        const float s0 = (h0 != nullptr && cok) ? h0[(size_t)bi * g.D + c0 + v] : 0.f;
+                        hin[v] = fmaf(accA[v], s0, accB[v]);
                     }
-                    if (--j < 0) {  // reached the sequence start: apply h0
-#pragma unroll
-                        for (int v = 0; v < VEC; ++v) {
-                            const float s0 = (h0 != nullptr && cok) ? h0[(size_t)bi * g.D + c0 + v] : 0.f;
-                            hin[v] = fmaf(accA[v], s0, accB[v]);
-                        }
-                        break;
-                    }
-                } else {  // gave up waiting: carry zero, the call reports CLA_ERR_TIMEOUT
-#pragma unroll
-                    for (int v = 0; v < VEC; ++v) hin[v] = 0.f;
                     break;
                 }
             }
@@ -217,8 +250,7 @@ scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
         float inc[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { inc[v] = fmaf(A[v], hin[v], Bc[v]); carry[v] = hin[v]; }
-        VecIO<VEC>::store_ws(ws.incl + u, inc);
-        st_release(ws.flags + u, 2u);
+        publish<VEC>(ws, u, kWordIncl, inc, 2u);
     }
 #pragma unroll
     for (int v = 0; v < VEC; ++v) carry[v] = __shfl_sync(0xffffffffu, carry[v], (kSub - 1) * kCg + cg);
@@ -246,7 +278,7 @@ scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
 // (a'_{T-1} = 1 and g_{T-1} includes dhT), i.e. the forward scan on reversed
 // arrays with the decays shifted by one place.
 template <int VEC>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 2)
 scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0,
                      const float *__restrict__ h, const float *__restrict__ dh,
                      const float *__restrict__ dhT, float *__restrict__ da,
@@ -268,7 +300,24 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0,
     const bool cok = c0 < g.D;
     const long long t_begin = (long long)chunk * kTc + sub * kL;
 
-    float ap[kL][VEC], gv[kL][VEC], hp[kL][VEC];
+    // h_{t-1} is only needed in the last pass: stage it in shared memory now
+    // (asynchronously, holding no registers) so its latency overlaps the rest.
+    __shared__ __align__(16) float s_hp[kL][kWarps * 32][VEC];
+#pragma unroll
+    for (int i = 0; i < kL; ++i) {
+        const long long t = t_begin + i;
+        const bool ok = cok && t >= 1 && t < g.T;
+        const float *src = h + (ok ? ((size_t)bi * g.T + t - 1) * g.D + c0 : 0);
+        const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(&s_hp[i][threadIdx.x][0]));
+        if (VEC == 4)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(ok ? 16u : 0u)
+                         : "memory");
+        else
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(ok ? 4u : 0u)
+                         : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+    float ap[kL][VEC], gv[kL][VEC];
 #pragma unroll
     for (int i = 0; i < kL; ++i) {
         const long long t = t_begin + i;
@@ -284,15 +333,9 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0,
                     if (dhT != nullptr) gv[i][v] += dhT[(size_t)bi * g.D + c0 + v];
                 }
             }
-            if (t >= 1) {
-                VecIO<VEC>::load(h + idx - g.D, hp[i]);
-            } else {
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) hp[i][v] = (h0 != nullptr) ? h0[(size_t)bi * g.D + c0 + v] : 0.f;
-            }
         } else {
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) { ap[i][v] = 1.f; gv[i][v] = 0.f; hp[i][v] = 0.f; }
+            for (int v = 0; v < VEC; ++v) { ap[i][v] = 1.f; gv[i][v] = 0.f; }
         }
     }
     // compose this lane's run from its last step down to its first
@@ -333,49 +376,29 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0,
 #pragma unroll
         for (int v = 0; v < VEC; ++v) hin[v] = 0.f;
         if (chunk != g.n_chunks - 1) {
-            VecIO<VEC>::store_ws(ws.aggA + u, A);
-            VecIO<VEC>::store_ws(ws.aggB + u, Bc);
-            st_release(ws.flags + u, 1u);
+            publish<VEC>(ws, u, kWordA, A, 1u);
+            publish<VEC>(ws, u, kWordB, Bc, 1u);
             float accA[VEC], accB[VEC];
 #pragma unroll
             for (int v = 0; v < VEC; ++v) { accA[v] = 1.f; accB[v] = 0.f; }
-            int j = chunk + 1;
-            while (true) {
-                const size_t up = unit_index(g, j, bi, cw, cg);
-                const unsigned int f = wait_flag(ws.flags + up, ws.hdr, 2u);
-                if (f == 2u) {
-                    float s[VEC];
-                    VecIO<VEC>::load_ws(ws.incl + up, s);
+            for (int j = chunk + 1;; ++j) {
+                const unsigned int f = look_at<VEC>(ws, unit_index(g, j, bi, cw, cg), accA, accB, hin, 2u);
+                if (f != 1u) break;
+                if (j == g.n_chunks - 1) {  // past the sequence end: nothing more flows in
 #pragma unroll
-                    for (int v = 0; v < VEC; ++v) hin[v] = fmaf(accA[v], s[v], accB[v]);
+                    for (int v = 0; v < VEC; ++v) hin[v] = accB[v];
                     break;
-                } else if (f == 1u) {
-                    float pa[VEC], pb[VEC];
-                    VecIO<VEC>::load_ws(ws.aggA + up, pa);
-                    VecIO<VEC>::load_ws(ws.aggB + up, pb);
-#pragma unroll
-                    for (int v = 0; v < VEC; ++v) {
-                        accB[v] = fmaf(accA[v], pb[v], accB[v]);
-                        accA[v] *= pa[v];
-                    }
-                    if (++j >= g.n_chunks) {
-#pragma unroll
-                        for (int v = 0; v < VEC; ++v) hin[v] = accB[v];
-                        break;
-                    }
-                } else {
-                    break;  // gave up waiting; reported as CLA_ERR_TIMEOUT
                 }
             }
         }
         float inc[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { inc[v] = fmaf(A[v], hin[v], Bc[v]); carry[v] = hin[v]; }
-        VecIO<VEC>::store_ws(ws.incl + u, inc);
-        st_release(ws.flags + u, 2u);
+        publish<VEC>(ws, u, kWordIncl, inc, 2u);
     }
 #pragma unroll
     for (int v = 0; v < VEC; ++v) carry[v] = __shfl_sync(0xffffffffu, carry[v], cg);
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");  // own copies of h_{t-1}
     float hb[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) hb[v] = fmaf(Aex[v], carry[v], Bex[v]);
@@ -386,9 +409,17 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0,
         for (int v = 0; v < VEC; ++v) hb[v] = fmaf(ap[i][v], hb[v], gv[i][v]);
         if (cok && t < g.T) {
             const size_t idx = ((size_t)bi * g.T + t) * g.D + c0;
+            float hp[VEC];  // h_{t-1}
+            if (t >= 1) {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) hp[v] = s_hp[i][threadIdx.x][v];
+            } else {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) hp[v] = (h0 != nullptr) ? h0[(size_t)bi * g.D + c0 + v] : 0.f;
+            }
             float dav[VEC];
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) dav[v] = hb[v] * hp[i][v];
+            for (int v = 0; v < VEC; ++v) dav[v] = hb[v] * hp[v];
             VecIO<VEC>::store(db + idx, hb);
             VecIO<VEC>::store(da + idx, dav);
             if (dh0 != nullptr && t == 0) {
@@ -405,7 +436,7 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0,
 struct Plan {
     ScanGeom g;
     int vec;
-    size_t flags_off, aggA_off, aggB_off, incl_off, total;
+    size_t words_off, total;
 };
 
 Plan make_plan(int64_t B, int64_t T, int64_t D, int vec) {
@@ -418,12 +449,8 @@ Plan make_plan(int64_t B, int64_t T, int64_t D, int vec) {
     const int per_warp = kCg * vec;
     p.g.n_cw = (int)((D + per_warp - 1) / per_warp);
     p.g.n_cblk = (p.g.n_cw + kWarps - 1) / kWarps;
-    const size_t units = scan_units(p.g);
-    p.flags_off = sizeof(WsHeader);
-    p.aggA_off = align_up(p.flags_off + units * sizeof(unsigned int), 256);
-    p.aggB_off = p.aggA_off + units * sizeof(float4);
-    p.incl_off = p.aggB_off + units * sizeof(float4);
-    p.total = p.incl_off + units * sizeof(float4);
+    p.words_off = sizeof(WsHeader);
+    p.total = p.words_off + scan_units(p.g) * 12 * sizeof(unsigned long long);
     return p;
 }
 
@@ -431,10 +458,7 @@ ScanWs bind_ws(const Plan &p, void *ws) {
     char *base = static_cast<char *>(ws);
     ScanWs w;
     w.hdr = reinterpret_cast<WsHeader *>(base);
-    w.flags = reinterpret_cast<unsigned int *>(base + p.flags_off);
-    w.aggA = reinterpret_cast<float4 *>(base + p.aggA_off);
-    w.aggB = reinterpret_cast<float4 *>(base + p.aggB_off);
-    w.incl = reinterpret_cast<float4 *>(base + p.incl_off);
+    w.words = reinterpret_cast<unsigned long long *>(base + p.words_off);
     return w;
 }
 
@@ -484,7 +508,7 @@ extern "C" int cla_scan_diag_fwd(const float *a, const float *b, const float *h0
     const bool v4 = (D % 4 == 0) && aligned16(a) && aligned16(b) && aligned16(h);
     const Plan p = make_plan(B, T, D, v4 ? 4 : 1);
     if (ws_bytes < p.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, p.total);
-    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.aggA_off, s), fn);
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.total, s), fn);
     const ScanWs w = bind_ws(p, ws);
     const unsigned int grid = (unsigned int)((size_t)p.g.n_chunks * p.g.B * p.g.n_cblk);
     if (v4) scan_diag_fwd_kernel<4><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);
@@ -515,7 +539,7 @@ extern "C" int cla_scan_diag_bwd(const float *a, const float *h0, const float *h
     const bool v4 = (D % 4 == 0) && aligned16(a) && aligned16(h) && aligned16(dh) && aligned16(da) && aligned16(db);
     const Plan p = make_plan(B, T, D, v4 ? 4 : 1);
     if (ws_bytes < p.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, p.total);
-    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.aggA_off, s), fn);
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.total, s), fn);
     const ScanWs w = bind_ws(p, ws);
     const unsigned int grid = (unsigned int)((size_t)p.g.n_chunks * p.g.B * p.g.n_cblk);
     if (v4) scan_diag_bwd_kernel<4><<<grid, kWarps * 32, 0, s>>>(a, h0, h, dh, dhT, da, db, dh0, p.g, w);
@@ -536,7 +560,7 @@ extern "C" int cla_scan_diag_bwd(const float *a, const float *h0, const float *h
 namespace cla {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB per device
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
 static __device__ __align__(256) unsigned char g_scan_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of the array, looked up once per device.  The name
@@ -592,7 +616,7 @@ extern "C" int cla_scan_diag_fwd_noalloc(const float *a, const float *b, const f
     st = noalloc_scratch(&ws);
     if (st) return st;
     // tickets and flags must start at zero; the payload is always written before it is read
-    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.aggA_off, s), fn);
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.total, s), fn);
     const ScanWs w = bind_ws(p, ws);
     const unsigned int grid = (unsigned int)((size_t)p.g.n_chunks * p.g.B * p.g.n_cblk);
     if (v4) scan_diag_fwd_kernel<4><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);

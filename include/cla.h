@@ -118,12 +118,12 @@ int cla_scan_diag_bwd(const float *a, const float *h0, const float *h,
  * latency or implicit synchronisation is not allowed.  Inputs, outputs and
  * results are those of cla_scan_diag_fwd; the caller still passes every
  * input and output buffer.
- *  - Scratch: the look-back scratch lives in an 8 MiB array compiled into the
+ *  - Scratch: the look-back scratch lives in a 16 MiB array compiled into the
  *    library (one per GPU that loads it, held until the process exits).  No
  *    cudaMalloc, cudaFree or other allocating call is made.
- *  - Limit: sizes whose scratch exceeds 8 MiB are rejected with
- *    CLA_ERR_UNSUPPORTED and nothing is enqueued: about 40 million elements
- *    of B*T*D when D is a multiple of 4 (8 x 4096 x 1024 fits), about 10
+ *  - Limit: sizes whose scratch exceeds 16 MiB are rejected with
+ *    CLA_ERR_UNSUPPORTED and nothing is enqueued: about 44 million elements
+ *    of B*T*D when D is a multiple of 4 (8 x 4096 x 1024 fits), about 11
  *    million otherwise.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
