@@ -812,6 +812,19 @@ LaArgs base_args(const LaPlan &pl, void *ws, int64_t BH, int64_t T) {
 }  // namespace
 }  // namespace cla
 
+#include "chunk_la_tc.cuh"
+
+namespace cla {
+namespace {
+// The tensor-core kernel needs at least one full chunk per head (its tile
+// boxes are one chunk tall); shorter sequences use the mma.sync kernel.
+int run_pass(int DX, int TC, bool REV, const LaArgs &a, cudaStream_t s, unsigned int grid) {
+    if (a.T >= TC && tensor_map_encoder() != nullptr) return launch_tc_pass(DX, TC, REV, a, s, grid);
+    return launch_pass(DX, TC, REV, a, s, grid);
+}
+}  // namespace
+}  // namespace cla
+
 using namespace cla;
 
 extern "C" size_t cla_chunk_la_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
@@ -859,7 +872,7 @@ extern "C" int cla_chunk_la_fwd(const uint16_t *q, const uint16_t *k, const uint
     a.nzb = (int)(dim_v / 64);
     a.ticket_slot = 0;
     const unsigned int grid = (unsigned int)((size_t)pl.n_seg * BH * a.nzb);
-    return launch_pass((int)dim_k, chunk, false, a, s, grid);
+    return run_pass((int)dim_k, chunk, false, a, s, grid);
 }
 
 extern "C" int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
@@ -913,7 +926,7 @@ extern "C" int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint
     a.nzb = (int)(dim_k / 64);
     a.ticket_slot = 0;
     unsigned int grid = (unsigned int)((size_t)pl.n_seg * BH * a.nzb);
-    st = launch_pass((int)dim_v, chunk, false, a, s, grid);
+    st = run_pass((int)dim_v, chunk, false, a, s, grid);
     if (st) return st;
 
     // pass 2 (reverse order): dV = [(Q K^T) . D]^T dO + diag(gamma) K dS, carrying dS
@@ -932,7 +945,7 @@ extern "C" int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint
     a.nzb = (int)(dim_v / 64);
     a.ticket_slot = 1;
     grid = (unsigned int)((size_t)pl.n_seg * BH * a.nzb);
-    st = launch_pass((int)dim_k, chunk, true, a, s, grid);
+    st = run_pass((int)dim_k, chunk, true, a, s, grid);
     if (st) return st;
 
     // pass 3 (reverse order): dK = [(dO V^T) . D]^T Q + diag(gamma) V dS^T, carrying dS^T
@@ -951,7 +964,7 @@ extern "C" int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint
     a.nzb = (int)(dim_k / 64);
     a.ticket_slot = 2;
     grid = (unsigned int)((size_t)pl.n_seg * BH * a.nzb);
-    st = launch_pass((int)dim_v, chunk, true, a, s, grid);
+    st = run_pass((int)dim_v, chunk, true, a, s, grid);
     if (st) return st;
 
     // decay gradient: suffix sums of q.dq - k.dk plus <dS_T, S_T>

@@ -1,0 +1,770 @@
+// chunk_la_tc.cuh -- the chunk kernel of chunk_la.cu on Blackwell's fifth-
+// generation tensor cores: TMA tile loads and stores, tcgen05.mma with the
+// accumulators in tensor memory (TMEM).  Included by chunk_la.cu (shares its
+// LaArgs, decay helpers and workspace layout); computes exactly the products
+// documented there:
+//     P       = X Y^T                     (M = Tc, N = Tc, K = DX)   smem x smem
+//     O_inter = X S_hi + X S_lo           (M = Tc, N = 64, K = DX)   smem x smem
+//     dS      = Y^T Zs_hi + Y^T Zs_lo     (M = DX, N = 64, K = Tc)   smem x smem
+//     O_intra = P_hi Z + P_lo Z           (M = Tc, N = 64, K = Tc)   tmem x smem
+// where Zs = diag(w_state) Z and P is masked and decayed in registers between
+// the first and the last product, split into two bf16 parts and written back
+// to TMEM as the A operand.  OUT = O_intra + diag(w_out) O_inter, State =
+// alpha State + dS.  One warp quarter of TMEM lanes belongs to each of the 4
+// warps; the thread whose lane holds row r of an M-row accumulator owns that
+// row (M = 128: lane = row; M = 64: rows 16w..16w+15 sit in lanes
+// 32w..32w+15).
+//
+// Operand layouts in shared memory use the 128-byte swizzle (8 rows of 128
+// bytes per 1024-byte atom, 16-byte chunks XOR-ed with the row's low 3 bits),
+// as TMA writes them: X, Y as K-major A/B operands (blocks of 64 columns),
+// Y as the MN-major A operand of dS, Z and S as MN-major B operands, Zs as
+// a K-major B operand written by the threads.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+namespace cla {
+namespace {
+
+// ----------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// Bounded wait for the phase with parity `ph` to complete; returns false on giving up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t ph) {
+    for (uint32_t it = 0; it < (1u << 24); ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(bar), "r"(ph)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;  // descriptor version of this architecture
+    d |= 2ull << 61;  // 128-byte swizzle
+    return d;
+}
+// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+            d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%"
+        "19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// byte offset of element (row, col < 64) of a 128-byte-swizzled tile
+__device__ __forceinline__ uint32_t sw128(int row, int col) {
+    return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((((col >> 3) ^ (row & 7)) & 7) << 4) + (col & 7) * 2);
+}
+
+// ----------------------------------------------------------------- configuration
+template <int DX, int TC>
+struct TcCfg {
+    static constexpr int NT = 128;
+    static constexpr int KBX = DX / 64;  // 64-column blocks of X and Y
+    static constexpr int KBT = TC / 64;  // 64-token blocks of Zs
+    // TMEM columns
+    static constexpr uint32_t C_P = 0;                         // P (fp32, Tc columns); later P_hi/P_lo
+    static constexpr uint32_t C_R = TC;                        // Tc = 128: first half's P_hi/P_lo
+    static constexpr uint32_t C_OI = (TC == 128) ? 192 : 64;  // O_inter
+    static constexpr uint32_t C_OA = C_OI + 64;                // O_intra
+    static constexpr uint32_t C_DS = C_OA + 64;                // dS
+    static constexpr uint32_t TMEM_COLS = (C_DS + 64 <= 256) ? 256 : 512;
+    // shared memory (offsets from a 1024-aligned base)
+    static constexpr int X_BYTES = KBX * TC * 128;
+    static constexpr int Z_BYTES = TC * 128;
+    static constexpr int S_BYTES = DX * 128;       // one bf16 part of State (MN-major)
+    static constexpr int ZS_BYTES = KBT * 64 * 128;  // one bf16 part of Zs (K-major)
+    static constexpr int OFF_X = 0;
+    static constexpr int OFF_Y0 = OFF_X + X_BYTES;
+    static constexpr int OFF_Y1 = OFF_Y0 + X_BYTES;
+    static constexpr int OFF_Z0 = OFF_Y1 + X_BYTES;
+    static constexpr int OFF_Z1 = OFF_Z0 + Z_BYTES;
+    static constexpr int OFF_W = OFF_Z1 + Z_BYTES;
+    static constexpr int OFF_SH = OFF_W + Z_BYTES;
+    static constexpr int OFF_SL = OFF_SH + S_BYTES;
+    static constexpr int OFF_ZSH = OFF_SL + S_BYTES;  // Zs_hi, Zs_lo; later the fp32 OUT staging tile
+    static constexpr int OFF_ZSL = OFF_ZSH + ZS_BYTES;
+    static constexpr int OFF_DEC = OFF_ZSL + ZS_BYTES;
+    static constexpr int DEC_BYTES = 4 * TC * 4;
+    static constexpr int OFF_BAR = OFF_DEC + DEC_BYTES;
+    static constexpr int SMEM = OFF_BAR + 128 + 1024;  // + alignment slack
+    static_assert(2 * ZS_BYTES == TC * 64 * 4, "OUT staging (fp32 Tc x 64) fits the Zs buffers");
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+struct TcMaps {
+    CUtensorMap x, y, z, w, out;
+};
+
+template <int DX, int TC, bool REV>
+__global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ TcMaps maps, const LaArgs p) {
+    using C = TcCfg<DX, TC>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    __shared__ uint32_t s_tmem;
+    __shared__ unsigned int s_ticket, s_flag;
+    __shared__ float s_alpha, s_palpha;
+    __shared__ float s_red[4];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // barriers: 0 X, 1 YZ0, 2 YZ1, 3 W, 4 P, 5 S, 6 O
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+
+    // TMEM first (before taking a ticket, so every ticket holder owns its TMEM)
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(C::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        tc_fence_before();
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 7; ++i) mbar_init(bar(i), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_ticket = atomicAdd(&p.hdr->ticket[p.ticket_slot], 1u);
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const unsigned int tk = s_ticket;
+    const int per_seg = p.BH * p.nzb;
+    const int sidx = (int)(tk / per_seg);
+    const int bh = (int)(tk % per_seg) / p.nzb;
+    const int zb = (int)(tk % per_seg) % p.nzb;
+    const int seg = REV ? (p.n_seg - 1 - sidx) : sidx;
+    const int c_begin = seg * p.seg_chunks;
+    const int c_end = min(c_begin + p.seg_chunks, p.n_chunks);
+    const int nc = c_end - c_begin;
+    const size_t unit = ((size_t)seg * p.BH + bh) * p.nzb + zb;
+    auto chunk_at = [&](int i) { return REV ? (c_end - 1 - i) : (c_begin + i); };
+
+    // rows owned by this thread (-1: none) for M = Tc and M = DX accumulators
+    const int prow = (TC == 128) ? tid : (lane < 16 ? warp * 16 + lane : -1);
+    const int srow = (DX == 128) ? tid : (lane < 16 ? warp * 16 + lane : -1);
+    const uint32_t tlane = (uint32_t)(warp * 32) << 16;
+
+    float *cl = reinterpret_cast<float *>(smem + C::OFF_DEC);
+    int *zr = reinterpret_cast<int *>(cl + TC);
+    float *wout = reinterpret_cast<float *>(zr + TC);
+    float *wst = wout + TC;
+    const float *Lb = p.ell + (size_t)bh * p.T;
+    const bool has_w = p.W != nullptr;
+    bool timed_out = false;
+
+    // ---------------------------------------------------------------- producer (thread 0)
+    auto issue_x = [&](int chunk) {
+        mbar_expect_tx(bar(0), (uint32_t)C::X_BYTES);
+        for (int kb = 0; kb < C::KBX; ++kb)
+            tma_load_3d(sbase + C::OFF_X + kb * TC * 128, &maps.x, kb * 64, chunk * TC, bh, bar(0));
+    };
+    auto issue_yz = [&](int b, int chunk) {
+        mbar_expect_tx(bar(1 + b), (uint32_t)(C::X_BYTES + C::Z_BYTES));
+        const uint32_t oy = b ? C::OFF_Y1 : C::OFF_Y0, oz = b ? C::OFF_Z1 : C::OFF_Z0;
+        for (int kb = 0; kb < C::KBX; ++kb)
+            tma_load_3d(sbase + oy + kb * TC * 128, &maps.y, kb * 64, chunk * TC, bh, bar(1 + b));
+        tma_load_3d(sbase + oz, &maps.z, zb * 64, chunk * TC, bh, bar(1 + b));
+    };
+    auto issue_w = [&](int chunk) {
+        mbar_expect_tx(bar(3), (uint32_t)C::Z_BYTES);
+        tma_load_3d(sbase + C::OFF_W, &maps.w, zb * 64, chunk * TC, bh, bar(3));
+    };
+    uint32_t ph[7] = {0, 0, 0, 0, 0, 0, 0};
+    auto wait = [&](int i) {
+        if (!mbar_wait(bar(i), ph[i])) timed_out = true;
+        ph[i] ^= 1u;
+    };
+
+    // ---------------------------------------------------------------- in-chunk decays
+    auto decays = [&](int chunk) {
+        if (warp == 0) {
+            constexpr int PER = TC / 32;
+            const long long t0 = (long long)chunk * TC;
+            float v[PER];
+            int zz[PER];
+            float run = 0.f;
+            int lastz = -1;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int r = lane * PER + k;
+                const float l = (t0 + r < p.T) ? __ldg(Lb + t0 + r) : 0.f;
+                const bool reset = (l == -INFINITY);
+                run += reset ? 0.f : l * kLog2e;
+                if (reset) lastz = r;
+                v[k] = run;
+                zz[k] = lastz;
+            }
+            float tot = run;
+            int zt = lastz;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, tot, off);
+                const int oz = __shfl_up_sync(0xffffffffu, zt, off);
+                if (lane >= off) {
+                    tot += o;
+                    zt = max(zt, oz);
+                }
+            }
+            float ex = __shfl_up_sync(0xffffffffu, tot, 1);
+            int zex = __shfl_up_sync(0xffffffffu, zt, 1);
+            if (lane == 0) {
+                ex = 0.f;
+                zex = -1;
+            }
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                cl[lane * PER + k] = v[k] + ex;
+                zr[lane * PER + k] = max(zz[k], zex);
+            }
+            __syncwarp();
+            const float cL = cl[TC - 1];
+            const int zL = zr[TC - 1];
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int r = lane * PER + k;
+                const float lam = zr[r] >= 0 ? 0.f : ex2(cl[r]);
+                const float gam = zL > r ? 0.f : ex2(cL - cl[r]);
+                wout[r] = REV ? gam : lam;
+                wst[r] = REV ? lam : gam;
+            }
+            if (lane == 0) s_alpha = zL >= 0 ? 0.f : ex2(cL);
+        }
+    };
+
+    // Zs = diag(w_state) Z as two bf16 parts, K-major [64 rows n][Tc tokens k]
+    auto write_zs = [&](int b) {
+        const uint8_t *zt = smem + (b ? C::OFF_Z1 : C::OFF_Z0);
+        for (int r = tid; r < TC; r += C::NT) {
+            const float w = wst[r];
+            const int kb = r >> 6, kc = r & 63;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 q = *reinterpret_cast<const uint4 *>(zt + sw128(r, c * 8));
+                const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const float2 f = unpack_bf16(words[h]);
+                    const float x0 = f.x * w, x1 = f.y * w;
+                    const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+                    const __nv_bfloat16 l0 = __float2bfloat16_rn(x0 - __bfloat162float(h0));
+                    const __nv_bfloat16 l1 = __float2bfloat16_rn(x1 - __bfloat162float(h1));
+                    const int n = c * 8 + h * 2;
+                    const uint32_t o0 = kb * 64 * 128 + sw128(n, kc), o1 = kb * 64 * 128 + sw128(n + 1, kc);
+                    *reinterpret_cast<__nv_bfloat16 *>(smem + C::OFF_ZSH + o0) = h0;
+                    *reinterpret_cast<__nv_bfloat16 *>(smem + C::OFF_ZSH + o1) = h1;
+                    *reinterpret_cast<__nv_bfloat16 *>(smem + C::OFF_ZSL + o0) = l0;
+                    *reinterpret_cast<__nv_bfloat16 *>(smem + C::OFF_ZSL + o1) = l1;
+                }
+            }
+        }
+    };
+
+    // tensor-core products (issued by thread 0)
+    auto issue_state_mma = [&](int b) {
+        const uint32_t oy = b ? C::OFF_Y1 : C::OFF_Y0;
+        constexpr uint32_t id = idesc_bf16(DX, 64, 1, 0);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            const uint32_t ozs = part ? C::OFF_ZSL : C::OFF_ZSH;
+#pragma unroll
+            for (int kk = 0; kk < TC / 16; ++kk) {
+                const uint64_t a = smem_desc(sbase + oy + kk * 2048, TC * 128, 1024);
+                const uint64_t bd = smem_desc(sbase + ozs + (kk >> 2) * 64 * 128 + (kk & 3) * 32, 16, 1024);
+                mma_ss(tmem + C::C_DS, a, bd, id, (part | kk) ? 1u : 0u);
+            }
+        }
+    };
+    auto issue_p_and_inter = [&](int b) {
+        const uint32_t oy = b ? C::OFF_Y1 : C::OFF_Y0;
+        constexpr uint32_t idp = idesc_bf16(TC, TC, 0, 0);
+#pragma unroll
+        for (int kk = 0; kk < DX / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * TC * 128 + (kk & 3) * 32;
+            mma_ss(tmem + C::C_P, smem_desc(sbase + C::OFF_X + off, 16, 1024), smem_desc(sbase + oy + off, 16, 1024),
+                   idp, kk ? 1u : 0u);
+        }
+        constexpr uint32_t ido = idesc_bf16(TC, 64, 0, 1);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            const uint32_t os = part ? C::OFF_SL : C::OFF_SH;
+#pragma unroll
+            for (int kk = 0; kk < DX / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * TC * 128 + (kk & 3) * 32;
+                mma_ss(tmem + C::C_OI, smem_desc(sbase + C::OFF_X + off, 16, 1024),
+                       smem_desc(sbase + os + kk * 2048, 8192, 1024), ido, (part | kk) ? 1u : 0u);
+            }
+        }
+    };
+    auto issue_intra = [&](int b) {
+        const uint32_t oz = b ? C::OFF_Z1 : C::OFF_Z0;
+        constexpr uint32_t id = idesc_bf16(TC, 64, 0, 1);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+            for (int kk = 0; kk < TC / 16; ++kk) {
+                uint32_t acol;
+                if (TC == 128) acol = (kk < 4 ? C::C_R + kk * 8 : C::C_P + (kk - 4) * 8) + part * 32;
+                else acol = C::C_P + kk * 8 + part * 32;
+                mma_ts(tmem + C::C_OA, tmem + acol, smem_desc(sbase + oz + kk * 2048, 8192, 1024), id,
+                       (part | kk) ? 1u : 0u);
+            }
+        }
+    };
+
+    // State rows in registers (fp32); this thread owns row srow of the [DX][64] slab.
+    float S[64];
+#pragma unroll
+    for (int c = 0; c < 64; ++c) S[c] = 0.f;
+
+    // dS row -> State = alpha State + dS
+    auto state_accumulate = [&](float alpha) {
+        uint32_t r[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            tmem_ld32(tmem + tlane + C::C_DS + h * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) S[h * 32 + j] = fmaf(alpha, S[h * 32 + j], __uint_as_float(r[j]));
+        }
+    };
+    // State as two bf16 parts, MN-major [DX rows k][64 n] (row srow)
+    auto write_s_smem = [&]() {
+        if (srow < 0) return;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const float x0 = S[c * 8 + 2 * h], x1 = S[c * 8 + 2 * h + 1];
+                hi[h] = pack_bf16(x0, x1);
+                const float2 fh = unpack_bf16(hi[h]);
+                lo[h] = pack_bf16(x0 - fh.x, x1 - fh.y);
+            }
+            const uint32_t off = sw128(srow, c * 8);
+            *reinterpret_cast<uint4 *>(smem + C::OFF_SH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(smem + C::OFF_SL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+    };
+
+    // ================================================================ phase 1
+    float alpha_seg = 1.f;
+    if (tid == 0) {
+        issue_yz(0, chunk_at(0));
+        if (nc > 1) issue_yz(1, chunk_at(1));
+    }
+    for (int i = 0; i < nc; ++i) {
+        const int b = i & 1;
+        wait(1 + b);
+        decays(chunk_at(i));
+        __syncthreads();
+        const float alpha = s_alpha;
+        alpha_seg *= alpha;
+        write_zs(b);
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            issue_state_mma(b);
+            mma_commit(bar(5));
+        }
+        wait(5);
+        tc_fence_after();
+        state_accumulate(alpha);
+        tc_fence_before();
+        __syncthreads();  // Y, Z of buffer b, Zs and the dS columns are free
+        if (tid == 0 && i + 2 < nc) issue_yz(b, chunk_at(i + 2));
+    }
+
+    // ================================================================ look-back
+    const bool first = REV ? (seg == p.n_seg - 1) : (seg == 0);
+    float4 *agg4 = p.agg + unit * (size_t)(DX * 16);
+    float4 *inc4 = p.incl + unit * (size_t)(DX * 16);
+    auto load_state0 = [&](float (&dst)[64], float scale, bool add) {
+        if (srow < 0) return;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+            float v = 0.f;
+            if (p.state0 != nullptr) {
+                const int col = zb * 64 + c;
+                v = p.trans0 ? p.state0[((size_t)bh * p.DZ + col) * DX + srow]
+                             : p.state0[((size_t)bh * DX + srow) * p.DZ + col];
+            }
+            dst[c] = add ? fmaf(scale, v, dst[c]) : v;
+        }
+    };
+    float Sin[64];
+#pragma unroll
+    for (int c = 0; c < 64; ++c) Sin[c] = 0.f;
+    if (first) {
+        load_state0(Sin, 1.f, false);
+    } else {
+        if (srow >= 0) {
+#pragma unroll
+            for (int c4 = 0; c4 < 16; ++c4)
+                __stcg(agg4 + c4 * DX + srow, make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]));
+        }
+        if (tid == 0) p.alpha_ws[unit] = alpha_seg;
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release(p.flags + unit, 1u);
+        float accA = 1.f;
+        int j = REV ? seg + 1 : seg - 1;
+        while (true) {
+            const size_t up = ((size_t)j * p.BH + bh) * p.nzb + zb;
+            if (tid == 0) {
+                const unsigned int f = wait_flag(p.flags + up, p.hdr, 30u + (unsigned)p.ticket_slot);
+                s_flag = f;
+                if (f == 1u) s_palpha = ld_cg(p.alpha_ws + up);
+            }
+            __syncthreads();
+            const unsigned int f = s_flag;
+            const float pa = s_palpha;
+            __syncthreads();
+            if (f == 2u || f == 1u) {
+                const float4 *src = (f == 2u ? p.incl : p.agg) + up * (size_t)(DX * 16);
+                if (srow >= 0) {
+#pragma unroll
+                    for (int c4 = 0; c4 < 16; ++c4) {
+                        const float4 v = ld_cg4(src + c4 * DX + srow);
+                        Sin[4 * c4] = fmaf(accA, v.x, Sin[4 * c4]);
+                        Sin[4 * c4 + 1] = fmaf(accA, v.y, Sin[4 * c4 + 1]);
+                        Sin[4 * c4 + 2] = fmaf(accA, v.z, Sin[4 * c4 + 2]);
+                        Sin[4 * c4 + 3] = fmaf(accA, v.w, Sin[4 * c4 + 3]);
+                    }
+                }
+                if (f == 2u) break;
+                accA *= pa;
+                j = REV ? j + 1 : j - 1;
+                if (j < 0 || j >= p.n_seg) {
+                    load_state0(Sin, accA, true);
+                    break;
+                }
+            } else {
+                break;
+            }
+        }
+    }
+    if (srow >= 0) {
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4)
+            __stcg(inc4 + c4 * DX + srow,
+                   make_float4(fmaf(alpha_seg, Sin[4 * c4], S[4 * c4]), fmaf(alpha_seg, Sin[4 * c4 + 1], S[4 * c4 + 1]),
+                               fmaf(alpha_seg, Sin[4 * c4 + 2], S[4 * c4 + 2]),
+                               fmaf(alpha_seg, Sin[4 * c4 + 3], S[4 * c4 + 3])));
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) st_release(p.flags + unit, 2u);
+
+    // ================================================================ phase 2
+#pragma unroll
+    for (int c = 0; c < 64; ++c) S[c] = Sin[c];
+    write_s_smem();
+    fence_async_smem();
+    if (tid == 0) {
+        issue_yz(0, chunk_at(0));
+        if (nc > 1) issue_yz(1, chunk_at(1));
+        issue_x(chunk_at(0));
+        if (has_w) issue_w(chunk_at(0));
+    }
+    __syncthreads();
+    for (int i = 0; i < nc; ++i) {
+        const int b = i & 1;
+        const int chunk = chunk_at(i);
+        const long long t0 = (long long)chunk * TC;
+        wait(1 + b);
+        wait(0);
+        if (tid == 0) tma_store_wait_read();  // the previous OUT tile has left the Zs buffers
+        decays(chunk);
+        __syncthreads();
+        const float alpha = s_alpha;
+        if (tid == 0) {
+            tc_fence_after();
+            issue_p_and_inter(b);
+            mma_commit(bar(4));
+        }
+        write_zs(b);
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            issue_state_mma(b);
+            mma_commit(bar(5));
+        }
+        // ---- mask and decay P (row prow), split into bf16 parts, back into TMEM
+        wait(4);
+        tc_fence_after();
+        if (tid == 0 && i + 1 < nc) issue_x(chunk_at(i + 1));  // X is free once P and X.S are done
+        {
+            const int r = prow < 0 ? 0 : prow;
+            const float clr = cl[r];
+            const int zrr = zr[r];
+            auto mask_piece = [&](const uint32_t (&pr)[32], int s0, uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float x[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int s = s0 + 2 * j + e;
+                        float m;
+                        if (!REV) m = (s <= r && zrr <= s) ? ex2(clr - cl[s]) : 0.f;
+                        else m = (s >= r && zr[s] <= r) ? ex2(cl[s] - clr) : 0.f;
+                        x[e] = __uint_as_float(pr[2 * j + e]) * m;
+                    }
+                    hi[j] = pack_bf16(x[0], x[1]);
+                    const float2 fh = unpack_bf16(hi[j]);
+                    lo[j] = pack_bf16(x[0] - fh.x, x[1] - fh.y);
+                }
+            };
+            if (TC == 64) {
+                uint32_t pa[32], pb[32], hi[16], lo[16], hi2[16], lo2[16];
+                tmem_ld32(tmem + tlane + C::C_P, pa);
+                tmem_ld32(tmem + tlane + C::C_P + 32, pb);
+                tmem_ld_wait();
+                mask_piece(pa, 0, hi, lo);
+                mask_piece(pb, 32, hi2, lo2);
+                tmem_st16(tmem + tlane + C::C_P + 0, hi);
+                tmem_st16(tmem + tlane + C::C_P + 16, hi2);
+                tmem_st16(tmem + tlane + C::C_P + 32, lo);
+                tmem_st16(tmem + tlane + C::C_P + 48, lo2);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t pr[32], hi[16], lo[16];
+                    tmem_ld32(tmem + tlane + C::C_P + q * 32, pr);
+                    tmem_ld_wait();
+                    mask_piece(pr, q * 32, hi, lo);
+                    // tokens 0..63 -> region R, tokens 64..127 -> the (already read) first half of P
+                    const uint32_t base = (q < 2) ? C::C_R : C::C_P;
+                    tmem_st16(tmem + tlane + base + (q & 1) * 16, hi);
+                    tmem_st16(tmem + tlane + base + 32 + (q & 1) * 16, lo);
+                }
+            }
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            issue_intra(b);
+            mma_commit(bar(6));
+        }
+        // ---- State = alpha State + dS; its bf16 parts for the next chunk (X.S of this chunk is done)
+        wait(5);
+        tc_fence_after();
+        state_accumulate(alpha);
+        write_s_smem();
+        fence_async_smem();
+        // ---- OUT = O_intra + w_out O_inter
+        wait(6);
+        tc_fence_after();
+        if (has_w) wait(3);
+        {
+            float *stage = reinterpret_cast<float *>(smem + C::OFF_ZSH);  // [Tc][64] fp32
+            const int r = prow < 0 ? 0 : prow;
+            const float wr = wout[r];
+            float dot = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t oa[32], oi[32];
+                tmem_ld32(tmem + tlane + C::C_OA + h * 32, oa);
+                tmem_ld32(tmem + tlane + C::C_OI + h * 32, oi);
+                tmem_ld_wait();
+                float o[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = fmaf(wr, __uint_as_float(oi[j]), __uint_as_float(oa[j]));
+                if (has_w && prow >= 0) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 q = *reinterpret_cast<const uint4 *>(smem + C::OFF_W + sw128(r, h * 32 + c * 8));
+                        const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = unpack_bf16(words[e]);
+                            dot = fmaf(o[c * 8 + 2 * e], f.x, fmaf(o[c * 8 + 2 * e + 1], f.y, dot));
+                        }
+                    }
+                }
+                if (prow >= 0) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int cc = (c + r) & 7;  // rotate 16-byte chunks across rows
+                        *reinterpret_cast<float4 *>(stage + (size_t)r * 64 + h * 32 + cc * 4) =
+                            make_float4(o[cc * 4], o[cc * 4 + 1], o[cc * 4 + 2], o[cc * 4 + 3]);
+                    }
+                }
+            }
+            if (has_w && prow >= 0 && t0 + prow < p.T) p.wdot[((size_t)zb * p.BH + bh) * p.T + t0 + prow] = dot;
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tma_store_3d(&maps.out, zb * 64, (int)t0, bh, sbase + C::OFF_ZSH);
+            if (i + 2 < nc) issue_yz(b, chunk_at(i + 2));
+            if (has_w && i + 1 < nc) issue_w(chunk_at(i + 1));
+        }
+    }
+    if (tid == 0) tma_store_wait_all();
+
+    // ================================================================ final state
+    const bool last = REV ? (seg == 0) : (seg == p.n_seg - 1);
+    if (last && p.fs_mode == 1 && srow >= 0) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) p.fs_out[((size_t)bh * DX + srow) * p.DZ + zb * 64 + c] = S[c];
+    } else if (last && p.fs_mode == 2) {
+        float acc = 0.f;
+        if (p.fs_dot != nullptr && srow >= 0) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+                acc = fmaf(S[c], p.fs_dot[((size_t)bh * p.DZ + zb * 64 + c) * DX + srow], acc);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) s_red[warp] = acc;
+        __syncthreads();
+        if (tid == 0) p.fs_partial[(size_t)zb * p.BH + bh] = s_red[0] + s_red[1] + s_red[2] + s_red[3];
+    }
+    if (timed_out) {
+        atomicOr(&p.hdr->error, kErrTimeout);
+        atomicExch(&p.hdr->where, 40u + (unsigned)p.ticket_slot);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
+}
+
+// ----------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 3-D map over [BH][T][cols] with a {64, rows, 1} box.
+bool make_map(CUtensorMap *m, const void *base, bool bf16, int cols, long long T, int BH, int rows, bool swizzle) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const size_t es = bf16 ? 2 : 4;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * es, (cuuint64_t)cols * es * (cuuint64_t)T};
+    cuuint32_t box[3] = {64u, (cuuint32_t)rows, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int DX, int TC, bool REV>
+int launch_tc_variant(const LaArgs &a, cudaStream_t s, unsigned int grid) {
+    using C = TcCfg<DX, TC>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e =
+            cudaFuncSetAttribute(la_tc_kernel<DX, TC, REV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return fail(CLA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        configured = true;
+    }
+    TcMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    bool ok = make_map(&maps.x, a.X, true, DX, a.T, a.BH, TC, true) &&
+              make_map(&maps.y, a.Y, true, DX, a.T, a.BH, TC, true) &&
+              make_map(&maps.z, a.Z, true, a.DZ, a.T, a.BH, TC, true) &&
+              make_map(&maps.out, a.out, false, a.DZ, a.T, a.BH, TC, false);
+    if (ok && a.W != nullptr) ok = make_map(&maps.w, a.W, true, a.DZ, a.T, a.BH, TC, true);
+    if (!ok) return fail(CLA_ERR_CUDA, "chunk_la: tensor map encoding failed");
+    la_tc_kernel<DX, TC, REV><<<grid, C::NT, C::SMEM, s>>>(maps, a);
+    return check_launch("la_tc_kernel");
+}
+
+int launch_tc_pass(int DX, int TC, bool REV, const LaArgs &a, cudaStream_t s, unsigned int grid) {
+#define CLA_TC_CASE(dx, tc)                                                           \
+    if (DX == dx && TC == tc)                                                         \
+        return REV ? launch_tc_variant<dx, tc, true>(a, s, grid) : launch_tc_variant<dx, tc, false>(a, s, grid);
+    CLA_TC_CASE(64, 64)
+    CLA_TC_CASE(64, 128)
+    CLA_TC_CASE(128, 64)
+    CLA_TC_CASE(128, 128)
+#undef CLA_TC_CASE
+    return fail(CLA_ERR_UNSUPPORTED, "chunk_la: no tensor-core kernel for head dim %d and chunk %d", DX, TC);
+}
+
+}  // namespace
+}  // namespace cla
