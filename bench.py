@@ -248,8 +248,8 @@ def _time_calls(torch, fn, flush, iters):
     return statistics.median(ts)
 
 
-def bench_scan_small(torch, cla, workloads, dev, flush, peaks, iters=20):
-    inp = workloads.make("scan_small")
+def bench_scan_small(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
+    inp = workloads.make("scan_small", **(shape or {}))
     a, b = inp["a"].to(dev), inp["b"].to(dev)
     B, T, D = a.shape
     ws = torch.empty(cla.scan_diag_workspace_size(B, T, D), dtype=torch.uint8, device=dev)
@@ -260,8 +260,8 @@ def bench_scan_small(torch, cla, workloads, dev, flush, peaks, iters=20):
             "GBps": round(by / ms / 1e6, 1), "frac_hbm": round(by / ms / 1e6 / peaks["hbm_gbs"], 4)}
 
 
-def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=5):
-    inp = workloads.make(name)
+def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=5, shape=None):
+    inp = workloads.make(name, **(shape or {}))
     t = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     B, H, T, d = t["q"].shape
     ws = torch.empty(cla.chunk_la_workspace_size(B, H, T, d, d, chunk), dtype=torch.uint8, device=dev)
@@ -298,8 +298,8 @@ def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=5):
     return res
 
 
-def bench_selective(torch, cla, workloads, dev, flush, peaks, iters=5):
-    inp = workloads.make("selective")
+def bench_selective(torch, cla, workloads, dev, flush, peaks, iters=5, shape=None):
+    inp = workloads.make("selective", **(shape or {}))
     t = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     B, T, D = t["x"].shape
     N = t["A"].shape[1]
@@ -396,6 +396,10 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--only", default=None,
+                    choices=["scan_small", "selective", "la_const", "la_long", "la_long_chunk64"],
+                    help="time one workload only (forward and backward), e.g. for profiling")
+    ap.add_argument("--shape", default="", help="shape overrides for --only, e.g. H=32,T=4096")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -421,6 +425,17 @@ def main():
 
     cla.lib()
     peaks, peak_kind = load_peaks()
+    if args.only:
+        shape = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in args.shape.split(",") if kv}
+        flush = Flusher(torch, dev)
+        it = max(1, args.steps)
+        fns = {"scan_small": lambda: bench_scan_small(torch, cla, workloads, dev, flush, peaks, it, shape),
+               "selective": lambda: bench_selective(torch, cla, workloads, dev, flush, peaks, it, shape),
+               "la_const": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_const", 64, it, shape),
+               "la_long": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 128, it, shape),
+               "la_long_chunk64": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 64, it, shape)}
+        print(json.dumps({"only": args.only, "shape": shape, "result": fns[args.only]()}), flush=True)
+        return 0
 
     sampler = ClockSampler(local_rank) if rank == 0 else None
     head = bench_scan(torch, cla, workloads, dev, args.steps, args.warmup, dist_on)

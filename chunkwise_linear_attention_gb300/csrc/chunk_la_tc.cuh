@@ -13,7 +13,7 @@
 // alpha State + dS.  One warp quarter of TMEM lanes belongs to each of the 4
 // warps; the thread whose lane holds row r of an M-row accumulator owns that
 // row (M = 128: lane = row; M = 64: rows 16w..16w+15 sit in lanes
-// 32w..32w+15).
+// 32w..32w+15); warps w and w + 4 share lane quarter w and split the columns.
 //
 // Operand layouts in shared memory use the 128-byte swizzle (8 rows of 128
 // bytes per 1024-byte atom, 16-byte chunks XOR-ed with the row's low 3 bits),
@@ -126,20 +126,20 @@ __device__ __forceinline__ uint32_t sw128(int row, int col) {
 // ----------------------------------------------------------------- configuration
 template <int DX, int TC>
 struct TcCfg {
-    static constexpr int NT = 128;
+    static constexpr int NT = 256;       // 8 warps: warps w and w + 4 share TMEM lane quarter w
     static constexpr int KBX = DX / 64;  // 64-column blocks of X and Y
     static constexpr int KBT = TC / 64;  // 64-token blocks of Zs
-    // TMEM columns
-    static constexpr uint32_t C_P = 0;                         // P (fp32, Tc columns); later P_hi/P_lo
-    static constexpr uint32_t C_R = TC;                        // Tc = 128: first half's P_hi/P_lo
-    static constexpr uint32_t C_OI = (TC == 128) ? 192 : 64;  // O_inter
-    static constexpr uint32_t C_OA = C_OI + 64;                // O_intra
-    static constexpr uint32_t C_DS = C_OA + 64;                // dS
-    static constexpr uint32_t TMEM_COLS = (C_DS + 64 <= 256) ? 256 : 512;
+    // TMEM columns.  P (fp32, Tc columns) is overwritten in place, 32 tokens
+    // at a time, by its bf16 high part (16 columns) and low part (16 columns).
+    static constexpr uint32_t C_P = 0;
+    static constexpr uint32_t C_OI = TC;        // O_inter
+    static constexpr uint32_t C_OA = TC + 64;   // O_intra
+    static constexpr uint32_t C_DS = TC + 128;  // dS
+    static constexpr uint32_t TMEM_COLS = (TC + 192 <= 256) ? 256 : 512;
     // shared memory (offsets from a 1024-aligned base)
     static constexpr int X_BYTES = KBX * TC * 128;
     static constexpr int Z_BYTES = TC * 128;
-    static constexpr int S_BYTES = DX * 128;       // one bf16 part of State (MN-major)
+    static constexpr int S_BYTES = DX * 128;         // one bf16 part of State (MN-major)
     static constexpr int ZS_BYTES = KBT * 64 * 128;  // one bf16 part of Zs (K-major)
     static constexpr int OFF_X = 0;
     static constexpr int OFF_Y0 = OFF_X + X_BYTES;
@@ -152,7 +152,7 @@ struct TcCfg {
     static constexpr int OFF_ZSH = OFF_SL + S_BYTES;  // Zs_hi, Zs_lo; later the fp32 OUT staging tile
     static constexpr int OFF_ZSL = OFF_ZSH + ZS_BYTES;
     static constexpr int OFF_DEC = OFF_ZSL + ZS_BYTES;
-    static constexpr int DEC_BYTES = 4 * TC * 4;
+    static constexpr int DEC_BYTES = 6 * TC * 4;  // cl, zr, w_out, w_state, two half-row dot products
     static constexpr int OFF_BAR = OFF_DEC + DEC_BYTES;
     static constexpr int SMEM = OFF_BAR + 128 + 1024;  // + alignment slack
     static_assert(2 * ZS_BYTES == TC * 64 * 4, "OUT staging (fp32 Tc x 64) fits the Zs buffers");
@@ -163,8 +163,19 @@ struct TcMaps {
     CUtensorMap x, y, z, w, out;
 };
 
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 template <int DX, int TC, bool REV>
-__global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ TcMaps maps, const LaArgs p) {
+__global__ void __launch_bounds__(256, 1) la_tc_kernel(const __grid_constant__ TcMaps maps, const LaArgs p) {
     using C = TcCfg<DX, TC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -172,9 +183,11 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
     __shared__ uint32_t s_tmem;
     __shared__ unsigned int s_ticket, s_flag;
     __shared__ float s_alpha, s_palpha;
-    __shared__ float s_red[4];
+    __shared__ float s_red[8];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q = warp & 3;   // TMEM lane quarter
+    const int hf = warp >> 2; // which half of the columns this warp handles
     // barriers: 0 X, 1 YZ0, 2 YZ1, 3 W, 4 P, 5 S, 6 O
     const uint32_t bar0 = sbase + C::OFF_BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -206,15 +219,16 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
     const size_t unit = ((size_t)seg * p.BH + bh) * p.nzb + zb;
     auto chunk_at = [&](int i) { return REV ? (c_end - 1 - i) : (c_begin + i); };
 
-    // rows owned by this thread (-1: none) for M = Tc and M = DX accumulators
-    const int prow = (TC == 128) ? tid : (lane < 16 ? warp * 16 + lane : -1);
-    const int srow = (DX == 128) ? tid : (lane < 16 ? warp * 16 + lane : -1);
-    const uint32_t tlane = (uint32_t)(warp * 32) << 16;
+    // rows owned (-1: none) for M = Tc and M = DX accumulators; this warp owns columns [32 hf, 32 hf + 32)
+    const int prow = (TC == 128) ? q * 32 + lane : (lane < 16 ? q * 16 + lane : -1);
+    const int srow = (DX == 128) ? q * 32 + lane : (lane < 16 ? q * 16 + lane : -1);
+    const uint32_t tlane = (uint32_t)(q * 32) << 16;
 
     float *cl = reinterpret_cast<float *>(smem + C::OFF_DEC);
     int *zr = reinterpret_cast<int *>(cl + TC);
     float *wout = reinterpret_cast<float *>(zr + TC);
     float *wst = wout + TC;
+    float *dotp = wst + TC;  // [2][Tc] half-row dot products
     const float *Lb = p.ell + (size_t)bh * p.T;
     const bool has_w = p.W != nullptr;
     bool timed_out = false;
@@ -298,31 +312,35 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
         }
     };
 
-    // Zs = diag(w_state) Z as two bf16 parts, K-major [64 rows n][Tc tokens k]
+    // Zs = diag(w_state) Z as two bf16 parts, K-major [64 rows n][Tc tokens]:
+    // 8x8 blocks of Z are read transposed (ldmatrix.trans), scaled per token,
+    // split, and written (stmatrix) into the transposed tile.
     auto write_zs = [&](int b) {
-        const uint8_t *zt = smem + (b ? C::OFF_Z1 : C::OFF_Z0);
-        for (int r = tid; r < TC; r += C::NT) {
-            const float w = wst[r];
-            const int kb = r >> 6, kc = r & 63;
+        const uint32_t zt = sbase + (b ? C::OFF_Z1 : C::OFF_Z0);
+        constexpr int NBLK = (TC / 8) * 8;  // 8x8 blocks (token block, n block)
+        const int j = lane & 7, blk_in = lane >> 3;
+        for (int g4 = warp; g4 < NBLK / 4; g4 += C::NT / 32) {
+            // four blocks per instruction: token blocks tb, n block nb = 4 * (g4 % 2) + blk_in
+            const int tb = g4 >> 1, nb = 4 * (g4 & 1) + blk_in;
+            uint32_t r[4];
+            ldsm_x4_trans(zt + sw128(tb * 8 + j, nb * 8), r);
+            // this thread's elements: n = nb'*8 + lane/4 of block i, tokens tb*8 + 2*(lane%4) + {0, 1}
+            const int t = tb * 8 + 2 * (lane & 3);
+            const float w0 = wst[t], w1 = wst[t + 1];
+            uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 q = *reinterpret_cast<const uint4 *>(zt + sw128(r, c * 8));
-                const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const float2 f = unpack_bf16(words[h]);
-                    const float x0 = f.x * w, x1 = f.y * w;
-                    const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                    const __nv_bfloat16 l0 = __float2bfloat16_rn(x0 - __bfloat162float(h0));
-                    const __nv_bfloat16 l1 = __float2bfloat16_rn(x1 - __bfloat162float(h1));
-                    const int n = c * 8 + h * 2;
-                    const uint32_t o0 = kb * 64 * 128 + sw128(n, kc), o1 = kb * 64 * 128 + sw128(n + 1, kc);
-                    *reinterpret_cast<__nv_bfloat16 *>(smem + C::OFF_ZSH + o0) = h0;
-                    *reinterpret_cast<__nv_bfloat16 *>(smem + C::OFF_ZSH + o1) = h1;
-                    *reinterpret_cast<__nv_bfloat16 *>(smem + C::OFF_ZSL + o0) = l0;
-                    *reinterpret_cast<__nv_bfloat16 *>(smem + C::OFF_ZSL + o1) = l1;
-                }
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = unpack_bf16(r[i]);
+                const float x0 = f.x * w0, x1 = f.y * w1;
+                hi[i] = pack_bf16(x0, x1);
+                const float2 fh = unpack_bf16(hi[i]);
+                lo[i] = pack_bf16(x0 - fh.x, x1 - fh.y);
             }
+            // target rows n = nb_i * 8 + j (block i from lane group), 16-byte chunk of tokens tb*8..tb*8+7
+            const int nrow = (4 * (g4 & 1) + blk_in) * 8 + j;
+            const uint32_t off = (uint32_t)((tb * 8) >> 6) * 64 * 128 + sw128(nrow, (tb * 8) & 63);
+            stsm_x4(sbase + C::OFF_ZSH + off, hi);
+            stsm_x4(sbase + C::OFF_ZSL + off, lo);
         }
     };
 
@@ -369,36 +387,29 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
             for (int kk = 0; kk < TC / 16; ++kk) {
-                uint32_t acol;
-                if (TC == 128) acol = (kk < 4 ? C::C_R + kk * 8 : C::C_P + (kk - 4) * 8) + part * 32;
-                else acol = C::C_P + kk * 8 + part * 32;
+                // tokens 16kk.. lie in piece kk/2: high part at its columns 0..15, low part at 16..31
+                const uint32_t acol = C::C_P + (uint32_t)(kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
                 mma_ts(tmem + C::C_OA, tmem + acol, smem_desc(sbase + oz + kk * 2048, 8192, 1024), id,
                        (part | kk) ? 1u : 0u);
             }
         }
     };
 
-    // State rows in registers (fp32); this thread owns row srow of the [DX][64] slab.
-    float S[64];
+    // State row srow, columns [32 hf, 32 hf + 32), in registers (fp32)
+    float S[32];
 #pragma unroll
-    for (int c = 0; c < 64; ++c) S[c] = 0.f;
-
-    // dS row -> State = alpha State + dS
+    for (int c = 0; c < 32; ++c) S[c] = 0.f;
     auto state_accumulate = [&](float alpha) {
         uint32_t r[32];
+        tmem_ld32(tmem + tlane + C::C_DS + hf * 32, r);
+        tmem_ld_wait();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            tmem_ld32(tmem + tlane + C::C_DS + h * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) S[h * 32 + j] = fmaf(alpha, S[h * 32 + j], __uint_as_float(r[j]));
-        }
+        for (int j = 0; j < 32; ++j) S[j] = fmaf(alpha, S[j], __uint_as_float(r[j]));
     };
-    // State as two bf16 parts, MN-major [DX rows k][64 n] (row srow)
     auto write_s_smem = [&]() {
         if (srow < 0) return;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -407,7 +418,7 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
                 const float2 fh = unpack_bf16(hi[h]);
                 lo[h] = pack_bf16(x0 - fh.x, x1 - fh.y);
             }
-            const uint32_t off = sw128(srow, c * 8);
+            const uint32_t off = sw128(srow, hf * 32 + c * 8);
             *reinterpret_cast<uint4 *>(smem + C::OFF_SH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             *reinterpret_cast<uint4 *>(smem + C::OFF_SL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
@@ -446,29 +457,30 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
     const bool first = REV ? (seg == p.n_seg - 1) : (seg == 0);
     float4 *agg4 = p.agg + unit * (size_t)(DX * 16);
     float4 *inc4 = p.incl + unit * (size_t)(DX * 16);
-    auto load_state0 = [&](float (&dst)[64], float scale, bool add) {
+    auto load_state0 = [&](float (&dst)[32], float scale, bool add) {
         if (srow < 0) return;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < 32; ++c) {
             float v = 0.f;
             if (p.state0 != nullptr) {
-                const int col = zb * 64 + c;
+                const int col = zb * 64 + hf * 32 + c;
                 v = p.trans0 ? p.state0[((size_t)bh * p.DZ + col) * DX + srow]
                              : p.state0[((size_t)bh * DX + srow) * p.DZ + col];
             }
             dst[c] = add ? fmaf(scale, v, dst[c]) : v;
         }
     };
-    float Sin[64];
+    float Sin[32];
 #pragma unroll
-    for (int c = 0; c < 64; ++c) Sin[c] = 0.f;
+    for (int c = 0; c < 32; ++c) Sin[c] = 0.f;
     if (first) {
         load_state0(Sin, 1.f, false);
     } else {
         if (srow >= 0) {
 #pragma unroll
-            for (int c4 = 0; c4 < 16; ++c4)
-                __stcg(agg4 + c4 * DX + srow, make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]));
+            for (int c4 = 0; c4 < 8; ++c4)
+                __stcg(agg4 + (hf * 8 + c4) * DX + srow,
+                       make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]));
         }
         if (tid == 0) p.alpha_ws[unit] = alpha_seg;
         __threadfence();
@@ -491,8 +503,8 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
                 const float4 *src = (f == 2u ? p.incl : p.agg) + up * (size_t)(DX * 16);
                 if (srow >= 0) {
 #pragma unroll
-                    for (int c4 = 0; c4 < 16; ++c4) {
-                        const float4 v = ld_cg4(src + c4 * DX + srow);
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 v = ld_cg4(src + (hf * 8 + c4) * DX + srow);
                         Sin[4 * c4] = fmaf(accA, v.x, Sin[4 * c4]);
                         Sin[4 * c4 + 1] = fmaf(accA, v.y, Sin[4 * c4 + 1]);
                         Sin[4 * c4 + 2] = fmaf(accA, v.z, Sin[4 * c4 + 2]);
@@ -513,8 +525,8 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
     }
     if (srow >= 0) {
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4)
-            __stcg(inc4 + c4 * DX + srow,
+        for (int c4 = 0; c4 < 8; ++c4)
+            __stcg(inc4 + (hf * 8 + c4) * DX + srow,
                    make_float4(fmaf(alpha_seg, Sin[4 * c4], S[4 * c4]), fmaf(alpha_seg, Sin[4 * c4 + 1], S[4 * c4 + 1]),
                                fmaf(alpha_seg, Sin[4 * c4 + 2], S[4 * c4 + 2]),
                                fmaf(alpha_seg, Sin[4 * c4 + 3], S[4 * c4 + 3])));
@@ -525,7 +537,7 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
 
     // ================================================================ phase 2
 #pragma unroll
-    for (int c = 0; c < 64; ++c) S[c] = Sin[c];
+    for (int c = 0; c < 32; ++c) S[c] = Sin[c];
     write_s_smem();
     fence_async_smem();
     if (tid == 0) {
@@ -558,7 +570,7 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
             issue_state_mma(b);
             mma_commit(bar(5));
         }
-        // ---- mask and decay P (row prow), split into bf16 parts, back into TMEM
+        // ---- mask and decay P, split into bf16 parts, back into TMEM in place
         wait(4);
         tc_fence_after();
         if (tid == 0 && i + 1 < nc) issue_x(chunk_at(i + 1));  // X is free once P and X.S are done
@@ -566,46 +578,40 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
             const int r = prow < 0 ? 0 : prow;
             const float clr = cl[r];
             const int zrr = zr[r];
-            auto mask_piece = [&](const uint32_t (&pr)[32], int s0, uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+            const int rmin = (TC == 128) ? q * 32 : q * 16, rmax = (TC == 128) ? q * 32 + 31 : q * 16 + 15;
+            constexpr int PIECES = TC / 64;  // pieces of 32 tokens per warp
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    float x[2];
+            for (int pc = 0; pc < PIECES; ++pc) {
+                const int piece = hf * PIECES + pc;
+                const int s0 = piece * 32;
+                const uint32_t col = C::C_P + (uint32_t)s0;
+                uint32_t hi[16], lo[16];
+                const bool all_masked = REV ? (s0 + 31 < rmin) : (s0 > rmax);  // warp-uniform
+                if (all_masked) {
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int s = s0 + 2 * j + e;
-                        float m;
-                        if (!REV) m = (s <= r && zrr <= s) ? ex2(clr - cl[s]) : 0.f;
-                        else m = (s >= r && zr[s] <= r) ? ex2(cl[s] - clr) : 0.f;
-                        x[e] = __uint_as_float(pr[2 * j + e]) * m;
-                    }
-                    hi[j] = pack_bf16(x[0], x[1]);
-                    const float2 fh = unpack_bf16(hi[j]);
-                    lo[j] = pack_bf16(x[0] - fh.x, x[1] - fh.y);
-                }
-            };
-            if (TC == 64) {
-                uint32_t pa[32], pb[32], hi[16], lo[16], hi2[16], lo2[16];
-                tmem_ld32(tmem + tlane + C::C_P, pa);
-                tmem_ld32(tmem + tlane + C::C_P + 32, pb);
-                tmem_ld_wait();
-                mask_piece(pa, 0, hi, lo);
-                mask_piece(pb, 32, hi2, lo2);
-                tmem_st16(tmem + tlane + C::C_P + 0, hi);
-                tmem_st16(tmem + tlane + C::C_P + 16, hi2);
-                tmem_st16(tmem + tlane + C::C_P + 32, lo);
-                tmem_st16(tmem + tlane + C::C_P + 48, lo2);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t pr[32], hi[16], lo[16];
-                    tmem_ld32(tmem + tlane + C::C_P + q * 32, pr);
+                    for (int jj = 0; jj < 16; ++jj) { hi[jj] = 0u; lo[jj] = 0u; }
+                } else {
+                    uint32_t pr[32];
+                    tmem_ld32(tmem + tlane + col, pr);
                     tmem_ld_wait();
-                    mask_piece(pr, q * 32, hi, lo);
-                    // tokens 0..63 -> region R, tokens 64..127 -> the (already read) first half of P
-                    const uint32_t base = (q < 2) ? C::C_R : C::C_P;
-                    tmem_st16(tmem + tlane + base + (q & 1) * 16, hi);
-                    tmem_st16(tmem + tlane + base + 32 + (q & 1) * 16, lo);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        float x[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int s = s0 + 2 * jj + e;
+                            float m;
+                            if (!REV) m = (s <= r && zrr <= s) ? ex2(clr - cl[s]) : 0.f;
+                            else m = (s >= r && zr[s] <= r) ? ex2(cl[s] - clr) : 0.f;
+                            x[e] = __uint_as_float(pr[2 * jj + e]) * m;
+                        }
+                        hi[jj] = pack_bf16(x[0], x[1]);
+                        const float2 fh = unpack_bf16(hi[jj]);
+                        lo[jj] = pack_bf16(x[0] - fh.x, x[1] - fh.y);
+                    }
                 }
+                tmem_st16(tmem + tlane + col, hi);
+                tmem_st16(tmem + tlane + col + 16, lo);
             }
             tmem_st_wait();
         }
@@ -622,7 +628,7 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
         state_accumulate(alpha);
         write_s_smem();
         fence_async_smem();
-        // ---- OUT = O_intra + w_out O_inter
+        // ---- OUT = O_intra + w_out O_inter (this warp: columns [32 hf, 32 hf + 32))
         wait(6);
         tc_fence_after();
         if (has_w) wait(3);
@@ -630,42 +636,41 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
             float *stage = reinterpret_cast<float *>(smem + C::OFF_ZSH);  // [Tc][64] fp32
             const int r = prow < 0 ? 0 : prow;
             const float wr = wout[r];
-            float dot = 0.f;
+            uint32_t oa[32], oi[32];
+            tmem_ld32(tmem + tlane + C::C_OA + hf * 32, oa);
+            tmem_ld32(tmem + tlane + C::C_OI + hf * 32, oi);
+            tmem_ld_wait();
+            float o[32];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t oa[32], oi[32];
-                tmem_ld32(tmem + tlane + C::C_OA + h * 32, oa);
-                tmem_ld32(tmem + tlane + C::C_OI + h * 32, oi);
-                tmem_ld_wait();
-                float o[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] = fmaf(wr, __uint_as_float(oi[j]), __uint_as_float(oa[j]));
-                if (has_w && prow >= 0) {
+            for (int jj = 0; jj < 32; ++jj) o[jj] = fmaf(wr, __uint_as_float(oi[jj]), __uint_as_float(oa[jj]));
+            if (prow >= 0) {
+                if (has_w) {
+                    float dot = 0.f;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const uint4 q = *reinterpret_cast<const uint4 *>(smem + C::OFF_W + sw128(r, h * 32 + c * 8));
-                        const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+                        const uint4 qq = *reinterpret_cast<const uint4 *>(smem + C::OFF_W + sw128(r, hf * 32 + c * 8));
+                        const uint32_t words[4] = {qq.x, qq.y, qq.z, qq.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float2 f = unpack_bf16(words[e]);
                             dot = fmaf(o[c * 8 + 2 * e], f.x, fmaf(o[c * 8 + 2 * e + 1], f.y, dot));
                         }
                     }
+                    dotp[hf * TC + r] = dot;
                 }
-                if (prow >= 0) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const int cc = (c + r) & 7;  // rotate 16-byte chunks across rows
-                        *reinterpret_cast<float4 *>(stage + (size_t)r * 64 + h * 32 + cc * 4) =
-                            make_float4(o[cc * 4], o[cc * 4 + 1], o[cc * 4 + 2], o[cc * 4 + 3]);
-                    }
+                for (int c = 0; c < 8; ++c) {
+                    const int cc = (c + r) & 7;  // rotate 16-byte chunks across rows
+                    *reinterpret_cast<float4 *>(stage + (size_t)r * 64 + hf * 32 + cc * 4) =
+                        make_float4(o[cc * 4], o[cc * 4 + 1], o[cc * 4 + 2], o[cc * 4 + 3]);
                 }
             }
-            if (has_w && prow >= 0 && t0 + prow < p.T) p.wdot[((size_t)zb * p.BH + bh) * p.T + t0 + prow] = dot;
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        if (has_w && hf == 0 && prow >= 0 && t0 + prow < p.T)
+            p.wdot[((size_t)zb * p.BH + bh) * p.T + t0 + prow] = dotp[prow] + dotp[TC + prow];
         if (tid == 0) {
             tma_store_3d(&maps.out, zb * 64, (int)t0, bh, sbase + C::OFF_ZSH);
             if (i + 2 < nc) issue_yz(b, chunk_at(i + 2));
@@ -678,19 +683,23 @@ __global__ void __launch_bounds__(128, 1) la_tc_kernel(const __grid_constant__ T
     const bool last = REV ? (seg == 0) : (seg == p.n_seg - 1);
     if (last && p.fs_mode == 1 && srow >= 0) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) p.fs_out[((size_t)bh * DX + srow) * p.DZ + zb * 64 + c] = S[c];
+        for (int c = 0; c < 32; ++c) p.fs_out[((size_t)bh * DX + srow) * p.DZ + zb * 64 + hf * 32 + c] = S[c];
     } else if (last && p.fs_mode == 2) {
         float acc = 0.f;
         if (p.fs_dot != nullptr && srow >= 0) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
-                acc = fmaf(S[c], p.fs_dot[((size_t)bh * p.DZ + zb * 64 + c) * DX + srow], acc);
+            for (int c = 0; c < 32; ++c)
+                acc = fmaf(S[c], p.fs_dot[((size_t)bh * p.DZ + zb * 64 + hf * 32 + c) * DX + srow], acc);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (lane == 0) s_red[warp] = acc;
         __syncthreads();
-        if (tid == 0) p.fs_partial[(size_t)zb * p.BH + bh] = s_red[0] + s_red[1] + s_red[2] + s_red[3];
+        if (tid == 0) {
+            float t = 0.f;
+            for (int w = 0; w < 8; ++w) t += s_red[w];
+            p.fs_partial[(size_t)zb * p.BH + bh] = t;
+        }
     }
     if (timed_out) {
         atomicOr(&p.hdr->error, kErrTimeout);
