@@ -1,6 +1,6 @@
 // chunk_la_tc.cuh -- the chunk kernel of chunk_la.cu on Blackwell's fifth-
-// generation tensor cores: TMA tile loads and stores, tcgen05.mma with the
-// accumulators in tensor memory (TMEM).  Included by chunk_la.cu (shares its
+// generation tensor cores: TMA tile loads, tcgen05.mma with the accumulators
+// in tensor memory (TMEM).  Included by chunk_la.cu (shares its
 // LaArgs, decay helpers and workspace layout); computes exactly the products
 // documented there:
 //     P       = X Y^T                     (M = Tc, N = Tc, K = DX)   smem x smem
@@ -10,10 +10,19 @@
 // where Zs = diag(w_state) Z and P is masked and decayed in registers between
 // the first and the last product, split into two bf16 parts and written back
 // to TMEM as the A operand.  OUT = O_intra + diag(w_out) O_inter, State =
-// alpha State + dS.  One warp quarter of TMEM lanes belongs to each of the 4
-// warps; the thread whose lane holds row r of an M-row accumulator owns that
-// row (M = 128: lane = row; M = 64: rows 16w..16w+15 sit in lanes
-// 32w..32w+15); warps w and w + 4 share lane quarter w and split the columns.
+// alpha State + dS.
+//
+// Warp roles.  Warp 8 (the producer) issues every TMA load and, from one
+// lane, every MMA, so the tensor pipe works ahead of the elementwise stages
+// (the next chunk's P is formed while this chunk's output is written).
+// Warps 0..7 (the math warps) do the elementwise work: decays, Zs, masking,
+// the State recurrence and the output epilogue, which goes from registers
+// straight to global memory.  They hand work to the producer through named
+// barriers and learn of finished MMAs and loads through mbarriers.  A math
+// warp w reads TMEM lane quarter w & 3 (the lanes a warp may access are fixed
+// by its rank within its warpgroup); warps w and w + 4 split the columns.
+// The thread whose lane holds row r of an M-row accumulator owns that row
+// (M = 128: lane = row; M = 64: rows 16q..16q+15 sit in lanes 32q..32q+15).
 //
 // Operand layouts in shared memory use the 128-byte swizzle (8 rows of 128
 // bytes per 1024-byte atom, 16-byte chunks XOR-ed with the row's low 3 bits),
@@ -53,15 +62,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z, uint32_t src) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y), "r"(z), "r"(src)
-                 : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -126,7 +126,7 @@ __device__ __forceinline__ uint32_t sw128(int row, int col) {
 // ----------------------------------------------------------------- configuration
 template <int DX, int TC>
 struct TcCfg {
-    static constexpr int NT = 256;       // 8 warps: warps w and w + 4 share TMEM lane quarter w
+    static constexpr int NT = 288;       // 8 math warps (w and w + 4 share TMEM lane quarter w) + 1 producer warp
     static constexpr int KBX = DX / 64;  // 64-column blocks of X and Y
     static constexpr int KBT = TC / 64;  // 64-token blocks of Zs
     // TMEM columns.  P (fp32, Tc columns) is overwritten in place, 32 tokens
@@ -149,18 +149,17 @@ struct TcCfg {
     static constexpr int OFF_W = OFF_Z1 + Z_BYTES;
     static constexpr int OFF_SH = OFF_W + Z_BYTES;
     static constexpr int OFF_SL = OFF_SH + S_BYTES;
-    static constexpr int OFF_ZSH = OFF_SL + S_BYTES;  // Zs_hi, Zs_lo; later the fp32 OUT staging tile
+    static constexpr int OFF_ZSH = OFF_SL + S_BYTES;  // Zs_hi, Zs_lo
     static constexpr int OFF_ZSL = OFF_ZSH + ZS_BYTES;
     static constexpr int OFF_DEC = OFF_ZSL + ZS_BYTES;
     static constexpr int DEC_BYTES = 6 * TC * 4;  // cl, zr, w_out, w_state, two half-row dot products
     static constexpr int OFF_BAR = OFF_DEC + DEC_BYTES;
-    static constexpr int SMEM = OFF_BAR + 128 + 1024;  // + alignment slack
-    static_assert(2 * ZS_BYTES == TC * 64 * 4, "OUT staging (fp32 Tc x 64) fits the Zs buffers");
+    static constexpr int SMEM = OFF_BAR + 128 + 1024;  // 8 mbarriers + alignment slack
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
 struct TcMaps {
-    CUtensorMap x, y, z, w, out;
+    CUtensorMap x, y, z, w;
 };
 
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
@@ -174,8 +173,21 @@ __device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
                  : "memory");
 }
 
+// Named barriers between the 8 math warps and the producer warp.
+constexpr int kBarMath = 1;   // the 256 math threads
+constexpr int kBarZs = 2;     // math: Zs written          -> producer may issue dS
+constexpr int kBarPmask = 3;  // math: P masked and split  -> producer may issue O_intra
+constexpr int kBarDone = 4;   // math: chunk finished      -> producer may issue the next O_inter
+constexpr int kMathThreads = 256;
+constexpr int kAllThreads = 288;
+
+__device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 template <int DX, int TC, bool REV>
-__global__ void __launch_bounds__(256, 1) la_tc_kernel(const __grid_constant__ TcMaps maps, const LaArgs p) {
+__global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_constant__ TcMaps maps, const LaArgs p) {
     using C = TcCfg<DX, TC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -186,9 +198,10 @@ __global__ void __launch_bounds__(256, 1) la_tc_kernel(const __grid_constant__ T
     __shared__ float s_red[8];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp & 3;   // TMEM lane quarter
-    const int hf = warp >> 2; // which half of the columns this warp handles
-    // barriers: 0 X, 1 YZ0, 2 YZ1, 3 W, 4 P, 5 S, 6 O
+    const bool producer = (warp == 8);
+    const int q = warp & 3;    // TMEM lane quarter (math warps)
+    const int hf = warp >> 2;  // which half of the columns this math warp handles
+    // mbarriers: 0 X, 1 YZ0, 2 YZ1, 3 W, 4 P, 5 dS, 6 O_intra, 7 O_inter
     const uint32_t bar0 = sbase + C::OFF_BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
@@ -200,7 +213,7 @@ __global__ void __launch_bounds__(256, 1) la_tc_kernel(const __grid_constant__ T
         tc_fence_before();
     }
     if (tid == 0) {
-        for (int i = 0; i < 7; ++i) mbar_init(bar(i), 1);
+        for (int i = 0; i < 8; ++i) mbar_init(bar(i), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_ticket = atomicAdd(&p.hdr->ticket[p.ticket_slot], 1u);
     }
@@ -218,487 +231,524 @@ __global__ void __launch_bounds__(256, 1) la_tc_kernel(const __grid_constant__ T
     const int nc = c_end - c_begin;
     const size_t unit = ((size_t)seg * p.BH + bh) * p.nzb + zb;
     auto chunk_at = [&](int i) { return REV ? (c_end - 1 - i) : (c_begin + i); };
-
-    // rows owned (-1: none) for M = Tc and M = DX accumulators; this warp owns columns [32 hf, 32 hf + 32)
-    const int prow = (TC == 128) ? q * 32 + lane : (lane < 16 ? q * 16 + lane : -1);
-    const int srow = (DX == 128) ? q * 32 + lane : (lane < 16 ? q * 16 + lane : -1);
-    const uint32_t tlane = (uint32_t)(q * 32) << 16;
-
-    float *cl = reinterpret_cast<float *>(smem + C::OFF_DEC);
-    int *zr = reinterpret_cast<int *>(cl + TC);
-    float *wout = reinterpret_cast<float *>(zr + TC);
-    float *wst = wout + TC;
-    float *dotp = wst + TC;  // [2][Tc] half-row dot products
-    const float *Lb = p.ell + (size_t)bh * p.T;
     const bool has_w = p.W != nullptr;
     bool timed_out = false;
-
-    // ---------------------------------------------------------------- producer (thread 0)
-    auto issue_x = [&](int chunk) {
-        mbar_expect_tx(bar(0), (uint32_t)C::X_BYTES);
-        for (int kb = 0; kb < C::KBX; ++kb)
-            tma_load_3d(sbase + C::OFF_X + kb * TC * 128, &maps.x, kb * 64, chunk * TC, bh, bar(0));
-    };
-    auto issue_yz = [&](int b, int chunk) {
-        mbar_expect_tx(bar(1 + b), (uint32_t)(C::X_BYTES + C::Z_BYTES));
-        const uint32_t oy = b ? C::OFF_Y1 : C::OFF_Y0, oz = b ? C::OFF_Z1 : C::OFF_Z0;
-        for (int kb = 0; kb < C::KBX; ++kb)
-            tma_load_3d(sbase + oy + kb * TC * 128, &maps.y, kb * 64, chunk * TC, bh, bar(1 + b));
-        tma_load_3d(sbase + oz, &maps.z, zb * 64, chunk * TC, bh, bar(1 + b));
-    };
-    auto issue_w = [&](int chunk) {
-        mbar_expect_tx(bar(3), (uint32_t)C::Z_BYTES);
-        tma_load_3d(sbase + C::OFF_W, &maps.w, zb * 64, chunk * TC, bh, bar(3));
-    };
-    uint32_t ph[7] = {0, 0, 0, 0, 0, 0, 0};
+    uint32_t ph[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     auto wait = [&](int i) {
         if (!mbar_wait(bar(i), ph[i])) timed_out = true;
         ph[i] ^= 1u;
     };
 
-    // ---------------------------------------------------------------- in-chunk decays
-    auto decays = [&](int chunk) {
-        if (warp == 0) {
-            constexpr int PER = TC / 32;
-            const long long t0 = (long long)chunk * TC;
-            float v[PER];
-            int zz[PER];
-            float run = 0.f;
-            int lastz = -1;
+    if (producer) {
+        // ============================================================ producer warp
+        const bool leader = (lane == 0);
+        auto issue_x = [&](int chunk) {
+            mbar_expect_tx(bar(0), (uint32_t)C::X_BYTES);
+            for (int kb = 0; kb < C::KBX; ++kb)
+                tma_load_3d(sbase + C::OFF_X + kb * TC * 128, &maps.x, kb * 64, chunk * TC, bh, bar(0));
+        };
+        auto issue_yz = [&](int b, int chunk) {
+            mbar_expect_tx(bar(1 + b), (uint32_t)(C::X_BYTES + C::Z_BYTES));
+            const uint32_t oy = b ? C::OFF_Y1 : C::OFF_Y0, oz = b ? C::OFF_Z1 : C::OFF_Z0;
+            for (int kb = 0; kb < C::KBX; ++kb)
+                tma_load_3d(sbase + oy + kb * TC * 128, &maps.y, kb * 64, chunk * TC, bh, bar(1 + b));
+            tma_load_3d(sbase + oz, &maps.z, zb * 64, chunk * TC, bh, bar(1 + b));
+        };
+        auto issue_w = [&](int chunk) {
+            mbar_expect_tx(bar(3), (uint32_t)C::Z_BYTES);
+            tma_load_3d(sbase + C::OFF_W, &maps.w, zb * 64, chunk * TC, bh, bar(3));
+        };
+        auto issue_state_mma = [&](int b) {
+            const uint32_t oy = b ? C::OFF_Y1 : C::OFF_Y0;
+            constexpr uint32_t id = idesc_bf16(DX, 64, 1, 0);
 #pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const int r = lane * PER + k;
-                const float l = (t0 + r < p.T) ? __ldg(Lb + t0 + r) : 0.f;
-                const bool reset = (l == -INFINITY);
-                run += reset ? 0.f : l * kLog2e;
-                if (reset) lastz = r;
-                v[k] = run;
-                zz[k] = lastz;
-            }
-            float tot = run;
-            int zt = lastz;
+            for (int part = 0; part < 2; ++part) {
+                const uint32_t ozs = part ? C::OFF_ZSL : C::OFF_ZSH;
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float o = __shfl_up_sync(0xffffffffu, tot, off);
-                const int oz = __shfl_up_sync(0xffffffffu, zt, off);
-                if (lane >= off) {
-                    tot += o;
-                    zt = max(zt, oz);
+                for (int kk = 0; kk < TC / 16; ++kk) {
+                    const uint64_t a = smem_desc(sbase + oy + kk * 2048, TC * 128, 1024);
+                    const uint64_t bd = smem_desc(sbase + ozs + (kk >> 2) * 64 * 128 + (kk & 3) * 32, 16, 1024);
+                    mma_ss(tmem + C::C_DS, a, bd, id, (part | kk) ? 1u : 0u);
                 }
             }
-            float ex = __shfl_up_sync(0xffffffffu, tot, 1);
-            int zex = __shfl_up_sync(0xffffffffu, zt, 1);
-            if (lane == 0) {
-                ex = 0.f;
-                zex = -1;
-            }
-#pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                cl[lane * PER + k] = v[k] + ex;
-                zr[lane * PER + k] = max(zz[k], zex);
-            }
-            __syncwarp();
-            const float cL = cl[TC - 1];
-            const int zL = zr[TC - 1];
-#pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const int r = lane * PER + k;
-                const float lam = zr[r] >= 0 ? 0.f : ex2(cl[r]);
-                const float gam = zL > r ? 0.f : ex2(cL - cl[r]);
-                wout[r] = REV ? gam : lam;
-                wst[r] = REV ? lam : gam;
-            }
-            if (lane == 0) s_alpha = zL >= 0 ? 0.f : ex2(cL);
-        }
-    };
-
-    // Zs = diag(w_state) Z as two bf16 parts, K-major [64 rows n][Tc tokens]:
-    // 8x8 blocks of Z are read transposed (ldmatrix.trans), scaled per token,
-    // split, and written (stmatrix) into the transposed tile.
-    auto write_zs = [&](int b) {
-        const uint32_t zt = sbase + (b ? C::OFF_Z1 : C::OFF_Z0);
-        constexpr int NBLK = (TC / 8) * 8;  // 8x8 blocks (token block, n block)
-        const int j = lane & 7, blk_in = lane >> 3;
-        for (int g4 = warp; g4 < NBLK / 4; g4 += C::NT / 32) {
-            // four blocks per instruction: token blocks tb, n block nb = 4 * (g4 % 2) + blk_in
-            const int tb = g4 >> 1, nb = 4 * (g4 & 1) + blk_in;
-            uint32_t r[4];
-            ldsm_x4_trans(zt + sw128(tb * 8 + j, nb * 8), r);
-            // this thread's elements: n = nb'*8 + lane/4 of block i, tokens tb*8 + 2*(lane%4) + {0, 1}
-            const int t = tb * 8 + 2 * (lane & 3);
-            const float w0 = wst[t], w1 = wst[t + 1];
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 f = unpack_bf16(r[i]);
-                const float x0 = f.x * w0, x1 = f.y * w1;
-                hi[i] = pack_bf16(x0, x1);
-                const float2 fh = unpack_bf16(hi[i]);
-                lo[i] = pack_bf16(x0 - fh.x, x1 - fh.y);
-            }
-            // target rows n = nb_i * 8 + j (block i from lane group), 16-byte chunk of tokens tb*8..tb*8+7
-            const int nrow = (4 * (g4 & 1) + blk_in) * 8 + j;
-            const uint32_t off = (uint32_t)((tb * 8) >> 6) * 64 * 128 + sw128(nrow, (tb * 8) & 63);
-            stsm_x4(sbase + C::OFF_ZSH + off, hi);
-            stsm_x4(sbase + C::OFF_ZSL + off, lo);
-        }
-    };
-
-    // tensor-core products (issued by thread 0)
-    auto issue_state_mma = [&](int b) {
-        const uint32_t oy = b ? C::OFF_Y1 : C::OFF_Y0;
-        constexpr uint32_t id = idesc_bf16(DX, 64, 1, 0);
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            const uint32_t ozs = part ? C::OFF_ZSL : C::OFF_ZSH;
-#pragma unroll
-            for (int kk = 0; kk < TC / 16; ++kk) {
-                const uint64_t a = smem_desc(sbase + oy + kk * 2048, TC * 128, 1024);
-                const uint64_t bd = smem_desc(sbase + ozs + (kk >> 2) * 64 * 128 + (kk & 3) * 32, 16, 1024);
-                mma_ss(tmem + C::C_DS, a, bd, id, (part | kk) ? 1u : 0u);
-            }
-        }
-    };
-    auto issue_p_and_inter = [&](int b) {
-        const uint32_t oy = b ? C::OFF_Y1 : C::OFF_Y0;
-        constexpr uint32_t idp = idesc_bf16(TC, TC, 0, 0);
-#pragma unroll
-        for (int kk = 0; kk < DX / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * TC * 128 + (kk & 3) * 32;
-            mma_ss(tmem + C::C_P, smem_desc(sbase + C::OFF_X + off, 16, 1024), smem_desc(sbase + oy + off, 16, 1024),
-                   idp, kk ? 1u : 0u);
-        }
-        constexpr uint32_t ido = idesc_bf16(TC, 64, 0, 1);
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            const uint32_t os = part ? C::OFF_SL : C::OFF_SH;
+        };
+        auto issue_p = [&](int b) {
+            const uint32_t oy = b ? C::OFF_Y1 : C::OFF_Y0;
+            constexpr uint32_t idp = idesc_bf16(TC, TC, 0, 0);
 #pragma unroll
             for (int kk = 0; kk < DX / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * TC * 128 + (kk & 3) * 32;
-                mma_ss(tmem + C::C_OI, smem_desc(sbase + C::OFF_X + off, 16, 1024),
-                       smem_desc(sbase + os + kk * 2048, 8192, 1024), ido, (part | kk) ? 1u : 0u);
+                mma_ss(tmem + C::C_P, smem_desc(sbase + C::OFF_X + off, 16, 1024),
+                       smem_desc(sbase + oy + off, 16, 1024), idp, kk ? 1u : 0u);
             }
-        }
-    };
-    auto issue_intra = [&](int b) {
-        const uint32_t oz = b ? C::OFF_Z1 : C::OFF_Z0;
-        constexpr uint32_t id = idesc_bf16(TC, 64, 0, 1);
+        };
+        auto issue_inter = [&]() {
+            constexpr uint32_t ido = idesc_bf16(TC, 64, 0, 1);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
+            for (int part = 0; part < 2; ++part) {
+                const uint32_t os = part ? C::OFF_SL : C::OFF_SH;
 #pragma unroll
-            for (int kk = 0; kk < TC / 16; ++kk) {
-                // tokens 16kk.. lie in piece kk/2: high part at its columns 0..15, low part at 16..31
-                const uint32_t acol = C::C_P + (uint32_t)(kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
-                mma_ts(tmem + C::C_OA, tmem + acol, smem_desc(sbase + oz + kk * 2048, 8192, 1024), id,
-                       (part | kk) ? 1u : 0u);
+                for (int kk = 0; kk < DX / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * TC * 128 + (kk & 3) * 32;
+                    mma_ss(tmem + C::C_OI, smem_desc(sbase + C::OFF_X + off, 16, 1024),
+                           smem_desc(sbase + os + kk * 2048, 8192, 1024), ido, (part | kk) ? 1u : 0u);
+                }
             }
-        }
-    };
-
-    // State row srow, columns [32 hf, 32 hf + 32), in registers (fp32)
-    float S[32];
+        };
+        auto issue_intra = [&](int b) {
+            const uint32_t oz = b ? C::OFF_Z1 : C::OFF_Z0;
+            constexpr uint32_t id = idesc_bf16(TC, 64, 0, 1);
 #pragma unroll
-    for (int c = 0; c < 32; ++c) S[c] = 0.f;
-    auto state_accumulate = [&](float alpha) {
-        uint32_t r[32];
-        tmem_ld32(tmem + tlane + C::C_DS + hf * 32, r);
-        tmem_ld_wait();
+            for (int part = 0; part < 2; ++part) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) S[j] = fmaf(alpha, S[j], __uint_as_float(r[j]));
-    };
-    auto write_s_smem = [&]() {
-        if (srow < 0) return;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const float x0 = S[c * 8 + 2 * h], x1 = S[c * 8 + 2 * h + 1];
-                hi[h] = pack_bf16(x0, x1);
-                const float2 fh = unpack_bf16(hi[h]);
-                lo[h] = pack_bf16(x0 - fh.x, x1 - fh.y);
+                for (int kk = 0; kk < TC / 16; ++kk) {
+                    // tokens 16kk.. lie in piece kk/2: high part at its columns 0..15, low part at 16..31
+                    const uint32_t acol = C::C_P + (uint32_t)(kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
+                    mma_ts(tmem + C::C_OA, tmem + acol, smem_desc(sbase + oz + kk * 2048, 8192, 1024), id,
+                           (part | kk) ? 1u : 0u);
+                }
             }
-            const uint32_t off = sw128(srow, hf * 32 + c * 8);
-            *reinterpret_cast<uint4 *>(smem + C::OFF_SH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4 *>(smem + C::OFF_SL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        };
+        // ---- phase 1: dS per chunk
+        if (leader) {
+            issue_yz(0, chunk_at(0));
+            if (nc > 1) issue_yz(1, chunk_at(1));
         }
-    };
-
-    // ================================================================ phase 1
-    float alpha_seg = 1.f;
-    if (tid == 0) {
-        issue_yz(0, chunk_at(0));
-        if (nc > 1) issue_yz(1, chunk_at(1));
-    }
-    for (int i = 0; i < nc; ++i) {
-        const int b = i & 1;
-        wait(1 + b);
-        decays(chunk_at(i));
-        __syncthreads();
-        const float alpha = s_alpha;
-        alpha_seg *= alpha;
-        write_zs(b);
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            issue_state_mma(b);
-            mma_commit(bar(5));
-        }
-        wait(5);
-        tc_fence_after();
-        state_accumulate(alpha);
-        tc_fence_before();
-        __syncthreads();  // Y, Z of buffer b, Zs and the dS columns are free
-        if (tid == 0 && i + 2 < nc) issue_yz(b, chunk_at(i + 2));
-    }
-
-    // ================================================================ look-back
-    const bool first = REV ? (seg == p.n_seg - 1) : (seg == 0);
-    float4 *agg4 = p.agg + unit * (size_t)(DX * 16);
-    float4 *inc4 = p.incl + unit * (size_t)(DX * 16);
-    auto load_state0 = [&](float (&dst)[32], float scale, bool add) {
-        if (srow < 0) return;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            float v = 0.f;
-            if (p.state0 != nullptr) {
-                const int col = zb * 64 + hf * 32 + c;
-                v = p.trans0 ? p.state0[((size_t)bh * p.DZ + col) * DX + srow]
-                             : p.state0[((size_t)bh * DX + srow) * p.DZ + col];
+        for (int i = 0; i < nc; ++i) {
+            const int b = i & 1;
+            wait(1 + b);
+            bar_sync(kBarZs, kAllThreads);
+            if (leader) {
+                tc_fence_after();
+                issue_state_mma(b);
+                mma_commit(bar(5));
             }
-            dst[c] = add ? fmaf(scale, v, dst[c]) : v;
+            __syncwarp();
+            wait(5);
+            if (leader && i + 2 < nc) issue_yz(b, chunk_at(i + 2));
         }
-    };
-    float Sin[32];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) Sin[c] = 0.f;
-    if (first) {
-        load_state0(Sin, 1.f, false);
+        // ---- phase 2 loads start while the math warps look back
+        if (leader) {
+            issue_yz(0, chunk_at(0));
+            if (nc > 1) issue_yz(1, chunk_at(1));
+            issue_x(chunk_at(0));
+            if (has_w) issue_w(chunk_at(0));
+        }
+        for (int i = 0; i < nc; ++i) {
+            const int b = i & 1;
+            wait(1 + b);
+            wait(0);
+            if (leader) {
+                tc_fence_after();
+                issue_p(b);
+                mma_commit(bar(4));
+            }
+            __syncwarp();
+            bar_sync(kBarDone, kAllThreads);  // previous chunk finished; State's bf16 parts written
+            if (leader) {
+                tc_fence_after();
+                issue_inter();
+                mma_commit(bar(7));
+                if (has_w && i > 0) issue_w(chunk_at(i));
+            }
+            __syncwarp();
+            bar_sync(kBarZs, kAllThreads);
+            if (leader) {
+                tc_fence_after();
+                issue_state_mma(b);
+                mma_commit(bar(5));
+            }
+            __syncwarp();
+            wait(7);  // P and O_inter done: X is free
+            if (leader && i + 1 < nc) issue_x(chunk_at(i + 1));
+            bar_sync(kBarPmask, kAllThreads);
+            if (leader) {
+                tc_fence_after();
+                issue_intra(b);
+                mma_commit(bar(6));
+            }
+            __syncwarp();
+            wait(6);
+            wait(5);
+            if (leader && i + 2 < nc) issue_yz(b, chunk_at(i + 2));
+        }
+        bar_sync(kBarDone, kAllThreads);  // the last chunk's arrival
     } else {
+        // ============================================================ math warps
+        const int mtid = tid;  // 0..255
+        const int prow = (TC == 128) ? q * 32 + lane : (lane < 16 ? q * 16 + lane : -1);
+        const int srow = (DX == 128) ? q * 32 + lane : (lane < 16 ? q * 16 + lane : -1);
+        const uint32_t tlane = (uint32_t)(q * 32) << 16;
+        float *cl = reinterpret_cast<float *>(smem + C::OFF_DEC);
+        int *zr = reinterpret_cast<int *>(cl + TC);
+        float *wout = reinterpret_cast<float *>(zr + TC);
+        float *wst = wout + TC;
+        float *dotp = wst + TC;  // [2][Tc] half-row dot products
+        const float *Lb = p.ell + (size_t)bh * p.T;
+
+        // Warp 0 computes a chunk's decays from log-decays it loaded one chunk
+        // earlier (load_ell), so the global load latency is off the critical path.
+        constexpr int PER = TC / 32;
+        float ell_pre[PER];
+        auto load_ell = [&](int chunk) {
+            if (warp == 0) {
+                const long long t0 = (long long)chunk * TC;
+#pragma unroll
+                for (int k = 0; k < PER; ++k) {
+                    const long long t = t0 + lane * PER + k;
+                    ell_pre[k] = (t < p.T) ? __ldg(Lb + t) : 0.f;
+                }
+            }
+        };
+        auto decays = [&](int next_chunk) {
+            if (warp == 0) {
+                float v[PER];
+                int zz[PER];
+                float run = 0.f;
+                int lastz = -1;
+#pragma unroll
+                for (int k = 0; k < PER; ++k) {
+                    const int r = lane * PER + k;
+                    const float l = ell_pre[k];
+                    const bool reset = (l == -INFINITY);
+                    run += reset ? 0.f : l * kLog2e;
+                    if (reset) lastz = r;
+                    v[k] = run;
+                    zz[k] = lastz;
+                }
+                float tot = run;
+                int zt = lastz;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_up_sync(0xffffffffu, tot, off);
+                    const int oz = __shfl_up_sync(0xffffffffu, zt, off);
+                    if (lane >= off) {
+                        tot += o;
+                        zt = max(zt, oz);
+                    }
+                }
+                float ex = __shfl_up_sync(0xffffffffu, tot, 1);
+                int zex = __shfl_up_sync(0xffffffffu, zt, 1);
+                if (lane == 0) {
+                    ex = 0.f;
+                    zex = -1;
+                }
+#pragma unroll
+                for (int k = 0; k < PER; ++k) {
+                    cl[lane * PER + k] = v[k] + ex;
+                    zr[lane * PER + k] = max(zz[k], zex);
+                }
+                __syncwarp();
+                const float cL = cl[TC - 1];
+                const int zL = zr[TC - 1];
+#pragma unroll
+                for (int k = 0; k < PER; ++k) {
+                    const int r = lane * PER + k;
+                    const float lam = zr[r] >= 0 ? 0.f : ex2(cl[r]);
+                    const float gam = zL > r ? 0.f : ex2(cL - cl[r]);
+                    wout[r] = REV ? gam : lam;
+                    wst[r] = REV ? lam : gam;
+                }
+                if (lane == 0) s_alpha = zL >= 0 ? 0.f : ex2(cL);
+                if (next_chunk >= 0) load_ell(next_chunk);
+            }
+        };
+        // Zs = diag(w_state) Z as two bf16 parts, K-major [64 rows n][Tc tokens]: 8x8 blocks of
+        // Z read transposed (ldmatrix.trans), scaled per token, split, written with stmatrix.
+        auto write_zs = [&](int b) {
+            const uint32_t zt = sbase + (b ? C::OFF_Z1 : C::OFF_Z0);
+            constexpr int NBLK = (TC / 8) * 8;
+            const int j = lane & 7, blk_in = lane >> 3;
+            for (int g4 = warp; g4 < NBLK / 4; g4 += 8) {
+                const int tb = g4 >> 1;
+                uint32_t r[4];
+                ldsm_x4_trans(zt + sw128(tb * 8 + j, (4 * (g4 & 1) + blk_in) * 8), r);
+                const int t = tb * 8 + 2 * (lane & 3);
+                const float w0 = wst[t], w1 = wst[t + 1];
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = unpack_bf16(r[i]);
+                    const float x0 = f.x * w0, x1 = f.y * w1;
+                    hi[i] = pack_bf16(x0, x1);
+                    const float2 fh = unpack_bf16(hi[i]);
+                    lo[i] = pack_bf16(x0 - fh.x, x1 - fh.y);
+                }
+                const int nrow = (4 * (g4 & 1) + blk_in) * 8 + j;
+                const uint32_t off = (uint32_t)((tb * 8) >> 6) * 64 * 128 + sw128(nrow, (tb * 8) & 63);
+                stsm_x4(sbase + C::OFF_ZSH + off, hi);
+                stsm_x4(sbase + C::OFF_ZSL + off, lo);
+            }
+        };
+        float S[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) S[c] = 0.f;
+        auto state_accumulate = [&](float alpha) {
+            uint32_t r[32];
+            tmem_ld32(tmem + tlane + C::C_DS + hf * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) S[jj] = fmaf(alpha, S[jj], __uint_as_float(r[jj]));
+        };
+        auto write_s_smem = [&]() {
+            if (srow < 0) return;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const float x0 = S[c * 8 + 2 * h], x1 = S[c * 8 + 2 * h + 1];
+                    hi[h] = pack_bf16(x0, x1);
+                    const float2 fh = unpack_bf16(hi[h]);
+                    lo[h] = pack_bf16(x0 - fh.x, x1 - fh.y);
+                }
+                const uint32_t off = sw128(srow, hf * 32 + c * 8);
+                *reinterpret_cast<uint4 *>(smem + C::OFF_SH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(smem + C::OFF_SL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        };
+
+        // ---- phase 1
+        float alpha_seg = 1.f;
+        load_ell(chunk_at(0));
+        for (int i = 0; i < nc; ++i) {
+            const int b = i & 1;
+            wait(1 + b);
+            decays(chunk_at(i + 1 < nc ? i + 1 : 0));  // phase 2 starts again at chunk_at(0)
+            bar_sync(kBarMath, kMathThreads);
+            const float alpha = s_alpha;
+            alpha_seg *= alpha;
+            write_zs(b);
+            fence_async_smem();
+            bar_arrive(kBarZs, kAllThreads);
+            wait(5);
+            tc_fence_after();
+            state_accumulate(alpha);
+            tc_fence_before();
+        }
+
+        // ---- look-back
+        const bool first = REV ? (seg == p.n_seg - 1) : (seg == 0);
+        float4 *agg4 = p.agg + unit * (size_t)(DX * 16);
+        float4 *inc4 = p.incl + unit * (size_t)(DX * 16);
+        auto load_state0 = [&](float (&dst)[32], float scale, bool add) {
+            if (srow < 0) return;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                float v = 0.f;
+                if (p.state0 != nullptr) {
+                    const int col = zb * 64 + hf * 32 + c;
+                    v = p.trans0 ? p.state0[((size_t)bh * p.DZ + col) * DX + srow]
+                                 : p.state0[((size_t)bh * DX + srow) * p.DZ + col];
+                }
+                dst[c] = add ? fmaf(scale, v, dst[c]) : v;
+            }
+        };
+        float Sin[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) Sin[c] = 0.f;
+        if (first) {
+            load_state0(Sin, 1.f, false);
+        } else {
+            if (srow >= 0) {
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4)
+                    __stcg(agg4 + (hf * 8 + c4) * DX + srow,
+                           make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]));
+            }
+            if (mtid == 0) p.alpha_ws[unit] = alpha_seg;
+            __threadfence();
+            bar_sync(kBarMath, kMathThreads);
+            if (mtid == 0) st_release(p.flags + unit, 1u);
+            float accA = 1.f;
+            int j = REV ? seg + 1 : seg - 1;
+            while (true) {
+                const size_t up = ((size_t)j * p.BH + bh) * p.nzb + zb;
+                if (mtid == 0) {
+                    const unsigned int f = wait_flag(p.flags + up, p.hdr, 30u + (unsigned)p.ticket_slot);
+                    s_flag = f;
+                    if (f == 1u) s_palpha = ld_cg(p.alpha_ws + up);
+                }
+                bar_sync(kBarMath, kMathThreads);
+                const unsigned int f = s_flag;
+                const float pa = s_palpha;
+                bar_sync(kBarMath, kMathThreads);
+                if (f == 2u || f == 1u) {
+                    const float4 *src = (f == 2u ? p.incl : p.agg) + up * (size_t)(DX * 16);
+                    if (srow >= 0) {
+#pragma unroll
+                        for (int c4 = 0; c4 < 8; ++c4) {
+                            const float4 v = ld_cg4(src + (hf * 8 + c4) * DX + srow);
+                            Sin[4 * c4] = fmaf(accA, v.x, Sin[4 * c4]);
+                            Sin[4 * c4 + 1] = fmaf(accA, v.y, Sin[4 * c4 + 1]);
+                            Sin[4 * c4 + 2] = fmaf(accA, v.z, Sin[4 * c4 + 2]);
+                            Sin[4 * c4 + 3] = fmaf(accA, v.w, Sin[4 * c4 + 3]);
+                        }
+                    }
+                    if (f == 2u) break;
+                    accA *= pa;
+                    j = REV ? j + 1 : j - 1;
+                    if (j < 0 || j >= p.n_seg) {
+                        load_state0(Sin, accA, true);
+                        break;
+                    }
+                } else {
+                    break;
+                }
+            }
+        }
         if (srow >= 0) {
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4)
-                __stcg(agg4 + (hf * 8 + c4) * DX + srow,
-                       make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]));
+                __stcg(inc4 + (hf * 8 + c4) * DX + srow,
+                       make_float4(fmaf(alpha_seg, Sin[4 * c4], S[4 * c4]),
+                                   fmaf(alpha_seg, Sin[4 * c4 + 1], S[4 * c4 + 1]),
+                                   fmaf(alpha_seg, Sin[4 * c4 + 2], S[4 * c4 + 2]),
+                                   fmaf(alpha_seg, Sin[4 * c4 + 3], S[4 * c4 + 3])));
         }
-        if (tid == 0) p.alpha_ws[unit] = alpha_seg;
         __threadfence();
-        __syncthreads();
-        if (tid == 0) st_release(p.flags + unit, 1u);
-        float accA = 1.f;
-        int j = REV ? seg + 1 : seg - 1;
-        while (true) {
-            const size_t up = ((size_t)j * p.BH + bh) * p.nzb + zb;
-            if (tid == 0) {
-                const unsigned int f = wait_flag(p.flags + up, p.hdr, 30u + (unsigned)p.ticket_slot);
-                s_flag = f;
-                if (f == 1u) s_palpha = ld_cg(p.alpha_ws + up);
-            }
-            __syncthreads();
-            const unsigned int f = s_flag;
-            const float pa = s_palpha;
-            __syncthreads();
-            if (f == 2u || f == 1u) {
-                const float4 *src = (f == 2u ? p.incl : p.agg) + up * (size_t)(DX * 16);
-                if (srow >= 0) {
-#pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
-                        const float4 v = ld_cg4(src + (hf * 8 + c4) * DX + srow);
-                        Sin[4 * c4] = fmaf(accA, v.x, Sin[4 * c4]);
-                        Sin[4 * c4 + 1] = fmaf(accA, v.y, Sin[4 * c4 + 1]);
-                        Sin[4 * c4 + 2] = fmaf(accA, v.z, Sin[4 * c4 + 2]);
-                        Sin[4 * c4 + 3] = fmaf(accA, v.w, Sin[4 * c4 + 3]);
-                    }
-                }
-                if (f == 2u) break;
-                accA *= pa;
-                j = REV ? j + 1 : j - 1;
-                if (j < 0 || j >= p.n_seg) {
-                    load_state0(Sin, accA, true);
-                    break;
-                }
-            } else {
-                break;
-            }
-        }
-    }
-    if (srow >= 0) {
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4)
-            __stcg(inc4 + (hf * 8 + c4) * DX + srow,
-                   make_float4(fmaf(alpha_seg, Sin[4 * c4], S[4 * c4]), fmaf(alpha_seg, Sin[4 * c4 + 1], S[4 * c4 + 1]),
-                               fmaf(alpha_seg, Sin[4 * c4 + 2], S[4 * c4 + 2]),
-                               fmaf(alpha_seg, Sin[4 * c4 + 3], S[4 * c4 + 3])));
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) st_release(p.flags + unit, 2u);
+        bar_sync(kBarMath, kMathThreads);
+        if (mtid == 0) st_release(p.flags + unit, 2u);
 
-    // ================================================================ phase 2
+        // ---- phase 2
 #pragma unroll
-    for (int c = 0; c < 32; ++c) S[c] = Sin[c];
-    write_s_smem();
-    fence_async_smem();
-    if (tid == 0) {
-        issue_yz(0, chunk_at(0));
-        if (nc > 1) issue_yz(1, chunk_at(1));
-        issue_x(chunk_at(0));
-        if (has_w) issue_w(chunk_at(0));
-    }
-    __syncthreads();
-    for (int i = 0; i < nc; ++i) {
-        const int b = i & 1;
-        const int chunk = chunk_at(i);
-        const long long t0 = (long long)chunk * TC;
-        wait(1 + b);
-        wait(0);
-        if (tid == 0) tma_store_wait_read();  // the previous OUT tile has left the Zs buffers
-        decays(chunk);
-        __syncthreads();
-        const float alpha = s_alpha;
-        if (tid == 0) {
-            tc_fence_after();
-            issue_p_and_inter(b);
-            mma_commit(bar(4));
-        }
-        write_zs(b);
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            issue_state_mma(b);
-            mma_commit(bar(5));
-        }
-        // ---- mask and decay P, split into bf16 parts, back into TMEM in place
-        wait(4);
-        tc_fence_after();
-        if (tid == 0 && i + 1 < nc) issue_x(chunk_at(i + 1));  // X is free once P and X.S are done
-        {
-            const int r = prow < 0 ? 0 : prow;
-            const float clr = cl[r];
-            const int zrr = zr[r];
-            const int rmin = (TC == 128) ? q * 32 : q * 16, rmax = (TC == 128) ? q * 32 + 31 : q * 16 + 15;
-            constexpr int PIECES = TC / 64;  // pieces of 32 tokens per warp
-#pragma unroll
-            for (int pc = 0; pc < PIECES; ++pc) {
-                const int piece = hf * PIECES + pc;
-                const int s0 = piece * 32;
-                const uint32_t col = C::C_P + (uint32_t)s0;
-                uint32_t hi[16], lo[16];
-                const bool all_masked = REV ? (s0 + 31 < rmin) : (s0 > rmax);  // warp-uniform
-                if (all_masked) {
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) { hi[jj] = 0u; lo[jj] = 0u; }
-                } else {
-                    uint32_t pr[32];
-                    tmem_ld32(tmem + tlane + col, pr);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        float x[2];
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int s = s0 + 2 * jj + e;
-                            float m;
-                            if (!REV) m = (s <= r && zrr <= s) ? ex2(clr - cl[s]) : 0.f;
-                            else m = (s >= r && zr[s] <= r) ? ex2(cl[s] - clr) : 0.f;
-                            x[e] = __uint_as_float(pr[2 * jj + e]) * m;
-                        }
-                        hi[jj] = pack_bf16(x[0], x[1]);
-                        const float2 fh = unpack_bf16(hi[jj]);
-                        lo[jj] = pack_bf16(x[0] - fh.x, x[1] - fh.y);
-                    }
-                }
-                tmem_st16(tmem + tlane + col, hi);
-                tmem_st16(tmem + tlane + col + 16, lo);
-            }
-            tmem_st_wait();
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            issue_intra(b);
-            mma_commit(bar(6));
-        }
-        // ---- State = alpha State + dS; its bf16 parts for the next chunk (X.S of this chunk is done)
-        wait(5);
-        tc_fence_after();
-        state_accumulate(alpha);
+        for (int c = 0; c < 32; ++c) S[c] = Sin[c];
         write_s_smem();
         fence_async_smem();
-        // ---- OUT = O_intra + w_out O_inter (this warp: columns [32 hf, 32 hf + 32))
-        wait(6);
-        tc_fence_after();
-        if (has_w) wait(3);
-        {
-            float *stage = reinterpret_cast<float *>(smem + C::OFF_ZSH);  // [Tc][64] fp32
-            const int r = prow < 0 ? 0 : prow;
-            const float wr = wout[r];
-            uint32_t oa[32], oi[32];
-            tmem_ld32(tmem + tlane + C::C_OA + hf * 32, oa);
-            tmem_ld32(tmem + tlane + C::C_OI + hf * 32, oi);
-            tmem_ld_wait();
-            float o[32];
+        bar_arrive(kBarDone, kAllThreads);  // State's bf16 parts for chunk 0
+        for (int i = 0; i < nc; ++i) {
+            const int b = i & 1;
+            const int chunk = chunk_at(i);
+            const long long t0 = (long long)chunk * TC;
+            wait(1 + b);
+            decays(i + 1 < nc ? chunk_at(i + 1) : -1);
+            bar_sync(kBarMath, kMathThreads);
+            const float alpha = s_alpha;
+            write_zs(b);
+            fence_async_smem();
+            bar_arrive(kBarZs, kAllThreads);
+            // ---- mask and decay P, split into bf16 parts, back into TMEM in place
+            wait(4);
+            tc_fence_after();
+            {
+                const int r = prow < 0 ? 0 : prow;
+                const float clr = cl[r];
+                const int zrr = zr[r];
+                const int rmin = (TC == 128) ? q * 32 : q * 16, rmax = (TC == 128) ? q * 32 + 31 : q * 16 + 15;
+                constexpr int PIECES = TC / 64;  // pieces of 32 tokens per warp
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) o[jj] = fmaf(wr, __uint_as_float(oi[jj]), __uint_as_float(oa[jj]));
-            if (prow >= 0) {
-                if (has_w) {
-                    float dot = 0.f;
+                for (int pc = 0; pc < PIECES; ++pc) {
+                    const int piece = hf * PIECES + pc;
+                    const int s0 = piece * 32;
+                    const uint32_t col = C::C_P + (uint32_t)s0;
+                    uint32_t hi[16], lo[16];
+                    const bool all_masked = REV ? (s0 + 31 < rmin) : (s0 > rmax);  // warp-uniform
+                    if (all_masked) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint4 qq = *reinterpret_cast<const uint4 *>(smem + C::OFF_W + sw128(r, hf * 32 + c * 8));
-                        const uint32_t words[4] = {qq.x, qq.y, qq.z, qq.w};
+                        for (int jj = 0; jj < 16; ++jj) {
+                            hi[jj] = 0u;
+                            lo[jj] = 0u;
+                        }
+                    } else {
+                        uint32_t pr[32];
+                        tmem_ld32(tmem + tlane + col, pr);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = unpack_bf16(words[e]);
-                            dot = fmaf(o[c * 8 + 2 * e], f.x, fmaf(o[c * 8 + 2 * e + 1], f.y, dot));
+                        for (int jj = 0; jj < 16; ++jj) {
+                            float x[2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int s = s0 + 2 * jj + e;
+                                float m;
+                                if (!REV) m = (s <= r && zrr <= s) ? ex2(clr - cl[s]) : 0.f;
+                                else m = (s >= r && zr[s] <= r) ? ex2(cl[s] - clr) : 0.f;
+                                x[e] = __uint_as_float(pr[2 * jj + e]) * m;
+                            }
+                            hi[jj] = pack_bf16(x[0], x[1]);
+                            const float2 fh = unpack_bf16(hi[jj]);
+                            lo[jj] = pack_bf16(x[0] - fh.x, x[1] - fh.y);
                         }
                     }
-                    dotp[hf * TC + r] = dot;
+                    tmem_st16(tmem + tlane + col, hi);
+                    tmem_st16(tmem + tlane + col + 16, lo);
                 }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            bar_arrive(kBarPmask, kAllThreads);
+            // ---- State = alpha State + dS
+            wait(5);
+            tc_fence_after();
+            state_accumulate(alpha);
+            // ---- OUT = O_intra + w_out O_inter (this warp: columns [32 hf, 32 hf + 32)), straight to HBM
+            wait(7);
+            wait(6);
+            tc_fence_after();
+            if (has_w) wait(3);
+            {
+                const int r = prow < 0 ? 0 : prow;
+                const float wr = wout[r];
+                uint32_t oa[32], oi[32];
+                tmem_ld32(tmem + tlane + C::C_OA + hf * 32, oa);
+                tmem_ld32(tmem + tlane + C::C_OI + hf * 32, oi);
+                tmem_ld_wait();
+                float o[32];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int cc = (c + r) & 7;  // rotate 16-byte chunks across rows
-                    *reinterpret_cast<float4 *>(stage + (size_t)r * 64 + hf * 32 + cc * 4) =
-                        make_float4(o[cc * 4], o[cc * 4 + 1], o[cc * 4 + 2], o[cc * 4 + 3]);
+                for (int jj = 0; jj < 32; ++jj) o[jj] = fmaf(wr, __uint_as_float(oi[jj]), __uint_as_float(oa[jj]));
+                if (prow >= 0 && t0 + prow < p.T) {
+                    if (has_w) {
+                        float dot = 0.f;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 qq =
+                                *reinterpret_cast<const uint4 *>(smem + C::OFF_W + sw128(r, hf * 32 + c * 8));
+                            const uint32_t words[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = unpack_bf16(words[e]);
+                                dot = fmaf(o[c * 8 + 2 * e], f.x, fmaf(o[c * 8 + 2 * e + 1], f.y, dot));
+                            }
+                        }
+                        dotp[hf * TC + r] = dot;
+                    }
+                    float4 *dst = reinterpret_cast<float4 *>(p.out + ((size_t)bh * p.T + t0 + prow) * p.DZ + zb * 64 +
+                                                             hf * 32);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        __stcs(dst + c, make_float4(o[c * 4], o[c * 4 + 1], o[c * 4 + 2], o[c * 4 + 3]));
                 }
             }
+            // State's bf16 parts for the next chunk (this chunk's O_inter has consumed them)
+            write_s_smem();
+            fence_async_smem();
+            tc_fence_before();
+            bar_sync(kBarMath, kMathThreads);
+            if (has_w && hf == 0 && prow >= 0 && t0 + prow < p.T)
+                p.wdot[((size_t)zb * p.BH + bh) * p.T + t0 + prow] = dotp[prow] + dotp[TC + prow];
+            bar_arrive(kBarDone, kAllThreads);
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (has_w && hf == 0 && prow >= 0 && t0 + prow < p.T)
-            p.wdot[((size_t)zb * p.BH + bh) * p.T + t0 + prow] = dotp[prow] + dotp[TC + prow];
-        if (tid == 0) {
-            tma_store_3d(&maps.out, zb * 64, (int)t0, bh, sbase + C::OFF_ZSH);
-            if (i + 2 < nc) issue_yz(b, chunk_at(i + 2));
-            if (has_w && i + 1 < nc) issue_w(chunk_at(i + 1));
-        }
-    }
-    if (tid == 0) tma_store_wait_all();
 
-    // ================================================================ final state
-    const bool last = REV ? (seg == 0) : (seg == p.n_seg - 1);
-    if (last && p.fs_mode == 1 && srow >= 0) {
+        // ---- final state of the sequence
+        const bool last = REV ? (seg == 0) : (seg == p.n_seg - 1);
+        if (last && p.fs_mode == 1 && srow >= 0) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) p.fs_out[((size_t)bh * DX + srow) * p.DZ + zb * 64 + hf * 32 + c] = S[c];
-    } else if (last && p.fs_mode == 2) {
-        float acc = 0.f;
-        if (p.fs_dot != nullptr && srow >= 0) {
+            for (int c = 0; c < 32; ++c) p.fs_out[((size_t)bh * DX + srow) * p.DZ + zb * 64 + hf * 32 + c] = S[c];
+        } else if (last && p.fs_mode == 2) {
+            float acc = 0.f;
+            if (p.fs_dot != nullptr && srow >= 0) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-                acc = fmaf(S[c], p.fs_dot[((size_t)bh * p.DZ + zb * 64 + hf * 32 + c) * DX + srow], acc);
-        }
+                for (int c = 0; c < 32; ++c)
+                    acc = fmaf(S[c], p.fs_dot[((size_t)bh * p.DZ + zb * 64 + hf * 32 + c) * DX + srow], acc);
+            }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) s_red[warp] = acc;
-        __syncthreads();
-        if (tid == 0) {
-            float t = 0.f;
-            for (int w = 0; w < 8; ++w) t += s_red[w];
-            p.fs_partial[(size_t)zb * p.BH + bh] = t;
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (lane == 0) s_red[warp] = acc;
+            bar_sync(kBarMath, kMathThreads);
+            if (mtid == 0) {
+                float t = 0.f;
+                for (int w = 0; w < 8; ++w) t += s_red[w];
+                p.fs_partial[(size_t)zb * p.BH + bh] = t;
+            }
         }
     }
     if (timed_out) {
@@ -725,18 +775,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 3-D map over [BH][T][cols] with a {64, rows, 1} box.
-bool make_map(CUtensorMap *m, const void *base, bool bf16, int cols, long long T, int BH, int rows, bool swizzle) {
+// 3-D map over a bf16 [BH][T][cols] array with a {64, rows, 1} box.
+bool make_map(CUtensorMap *m, const void *base, int cols, long long T, int BH, int rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    const size_t es = bf16 ? 2 : 4;
+    const size_t es = 2;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)T, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)cols * es, (cuuint64_t)cols * es * (cuuint64_t)T};
     cuuint32_t box[3] = {64u, (cuuint32_t)rows, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
-                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -753,11 +802,10 @@ int launch_tc_variant(const LaArgs &a, cudaStream_t s, unsigned int grid) {
     }
     TcMaps maps;
     memset(&maps, 0, sizeof(maps));
-    bool ok = make_map(&maps.x, a.X, true, DX, a.T, a.BH, TC, true) &&
-              make_map(&maps.y, a.Y, true, DX, a.T, a.BH, TC, true) &&
-              make_map(&maps.z, a.Z, true, a.DZ, a.T, a.BH, TC, true) &&
-              make_map(&maps.out, a.out, false, a.DZ, a.T, a.BH, TC, false);
-    if (ok && a.W != nullptr) ok = make_map(&maps.w, a.W, true, a.DZ, a.T, a.BH, TC, true);
+    bool ok = make_map(&maps.x, a.X, DX, a.T, a.BH, TC) &&
+              make_map(&maps.y, a.Y, DX, a.T, a.BH, TC) &&
+              make_map(&maps.z, a.Z, a.DZ, a.T, a.BH, TC);
+    if (ok && a.W != nullptr) ok = make_map(&maps.w, a.W, a.DZ, a.T, a.BH, TC);
     if (!ok) return fail(CLA_ERR_CUDA, "chunk_la: tensor map encoding failed");
     la_tc_kernel<DX, TC, REV><<<grid, C::NT, C::SMEM, s>>>(maps, a);
     return check_launch("la_tc_kernel");
