@@ -50,7 +50,12 @@ namespace {
 typedef __nv_bfloat16 bf16;
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kSegChunks = 8;  // chunks per segment (one block)
+// Chunks per segment (one block): the largest of kSegChoices that still
+// leaves at least kMinBlocks blocks (several waves on a 152-SM part), so the
+// fixed cost of a block's look-back is spread over as many chunks as the
+// grid's size allows; the smallest choice otherwise.
+constexpr int kSegChoices[3] = {32, 16, 8};
+constexpr long long kMinBlocks = 2048;
 
 // ----------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -738,11 +743,18 @@ LaPlan la_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chun
     p.TC = chunk;
     p.DXmax = (int)(dk > dv ? dk : dv);
     p.n_chunks = (int)((T + chunk - 1) / chunk);
-    p.seg_chunks = kSegChunks;
-    p.n_seg = (p.n_chunks + p.seg_chunks - 1) / p.seg_chunks;
-    if (p.n_seg < 1) p.n_seg = 1;
     p.nzb_max = (int)((dk > dv ? dk : dv) / 64);
     const size_t BH = (size_t)B * H;
+    p.seg_chunks = kSegChoices[2];
+    for (int c : kSegChoices) {
+        const long long nseg = (p.n_chunks + c - 1) / c;
+        if (nseg * (long long)BH * p.nzb_max >= kMinBlocks) {
+            p.seg_chunks = c;
+            break;
+        }
+    }
+    p.n_seg = (p.n_chunks + p.seg_chunks - 1) / p.seg_chunks;
+    if (p.n_seg < 1) p.n_seg = 1;
     p.units = (size_t)p.n_seg * BH * p.nzb_max;
     const size_t state_floats = (size_t)p.DXmax * 64;
     p.off_flags = sizeof(WsHeader);

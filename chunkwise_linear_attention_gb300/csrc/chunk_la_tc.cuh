@@ -62,6 +62,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -108,6 +120,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+// 8 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
@@ -135,7 +164,10 @@ struct TcCfg {
     static constexpr uint32_t C_OI = TC;        // O_inter
     static constexpr uint32_t C_OA = TC + 64;   // O_intra
     static constexpr uint32_t C_DS = TC + 128;  // dS
-    static constexpr uint32_t TMEM_COLS = (TC + 192 <= 256) ? 256 : 512;
+    // masked, decayed P as the bf16 A operand of O_intra: per 32-token piece,
+    // the high part in its first 16 columns and the low part in the next 16
+    static constexpr uint32_t C_PB = TC + 192;
+    static constexpr uint32_t TMEM_COLS = (2 * TC + 192 <= 256) ? 256 : 512;
     // shared memory (offsets from a 1024-aligned base)
     static constexpr int X_BYTES = KBX * TC * 128;
     static constexpr int Z_BYTES = TC * 128;
@@ -149,17 +181,23 @@ struct TcCfg {
     static constexpr int OFF_W = OFF_Z1 + Z_BYTES;
     static constexpr int OFF_SH = OFF_W + Z_BYTES;
     static constexpr int OFF_SL = OFF_SH + S_BYTES;
-    static constexpr int OFF_ZSH = OFF_SL + S_BYTES;  // Zs_hi, Zs_lo
+    // Zs_hi, Zs_lo; after the chunk's dS product, the fp32 output tile (two
+    // 128-byte-swizzled halves of Tc rows x 32 columns) for the TMA store
+    static constexpr int OFF_ZSH = OFF_SL + S_BYTES;
     static constexpr int OFF_ZSL = OFF_ZSH + ZS_BYTES;
     static constexpr int OFF_DEC = OFF_ZSL + ZS_BYTES;
-    static constexpr int DEC_BYTES = 6 * TC * 4;  // cl, zr, w_out, w_state, two half-row dot products
+    // decays, two buffers (chunk sequence number parity) of cl, zr, w_out,
+    // w_state, g [Tc] and alpha; then the two half-row dot products [2][Tc]
+    static constexpr int DEC_STRIDE = 5 * TC + 4;  // floats per buffer
+    static constexpr int DEC_BYTES = (2 * DEC_STRIDE + 2 * TC) * 4;
     static constexpr int OFF_BAR = OFF_DEC + DEC_BYTES;
-    static constexpr int SMEM = OFF_BAR + 128 + 1024;  // 8 mbarriers + alignment slack
+    static constexpr int SMEM = OFF_BAR + 128 + 1024;  // 10 mbarriers + alignment slack
+    static_assert(2 * ZS_BYTES == TC * 64 * 4, "the output tile fits the Zs buffers");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
 struct TcMaps {
-    CUtensorMap x, y, z, w;
+    CUtensorMap x, y, z, w, out;
 };
 
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
@@ -194,14 +232,12 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
     const uint32_t sbase = smem_u32(smem);
     __shared__ uint32_t s_tmem;
     __shared__ unsigned int s_ticket, s_flag;
-    __shared__ float s_alpha, s_palpha;
+    __shared__ float s_palpha;
     __shared__ float s_red[8];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool producer = (warp == 8);
-    const int q = warp & 3;    // TMEM lane quarter (math warps)
-    const int hf = warp >> 2;  // which half of the columns this math warp handles
-    // mbarriers: 0 X, 1 YZ0, 2 YZ1, 3 W, 4 P, 5 dS, 6 O_intra, 7 O_inter
+    // mbarriers: 0 X, 1 YZ0, 2 YZ1, 3 W, 4 P, 5 dS, 6 O_intra, 7 O_inter, 8-9 decay buffers
     const uint32_t bar0 = sbase + C::OFF_BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
@@ -214,6 +250,8 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
     }
     if (tid == 0) {
         for (int i = 0; i < 8; ++i) mbar_init(bar(i), 1);
+        mbar_init(bar(8), 32);
+        mbar_init(bar(9), 32);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_ticket = atomicAdd(&p.hdr->ticket[p.ticket_slot], 1u);
     }
@@ -238,10 +276,92 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
         if (!mbar_wait(bar(i), ph[i])) timed_out = true;
         ph[i] ^= 1u;
     };
+    // Decays are computed once per chunk visit.  Visits are numbered 0..2nc-1
+    // (phase 1, then phase 2); visit n uses decay buffer n & 1, whose mbarrier
+    // completes one phase per use, so its parity for visit n is (n >> 1) & 1.
+    float *dec = reinterpret_cast<float *>(smem + C::OFF_DEC);
+    auto dbuf = [&](int n) { return dec + (n & 1) * C::DEC_STRIDE; };
+    float *dotp = dec + 2 * C::DEC_STRIDE;  // [2][Tc] half-row dot products
 
     if (producer) {
         // ============================================================ producer warp
         const bool leader = (lane == 0);
+        const float *Lb = p.ell + (size_t)bh * p.T;
+        // decays of visit n, by the whole warp: cl_r = in-chunk sum of log2 a up to r (resets
+        // skipped), zr_r = last reset at or before r, w_out / w_state, the column factors g of
+        // the off-diagonal score pieces, and alpha = the chunk's total decay
+        constexpr int PER = TC / 32;
+        float ell_pre[PER];  // log-decays of the next visit, loaded one visit ahead
+        auto load_ell = [&](int n) {
+            const long long t0 = (long long)chunk_at(n < nc ? n : n - nc) * TC;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const long long t = t0 + lane * PER + k;
+                ell_pre[k] = (t < p.T) ? __ldg(Lb + t) : 0.f;
+            }
+        };
+        auto compute_decays = [&](int n) {
+            float *cl = dbuf(n);
+            int *zr = reinterpret_cast<int *>(cl + TC);
+            float *wout = cl + 2 * TC, *wst = cl + 3 * TC, *gcol = cl + 4 * TC;
+            float v[PER];
+            int zz[PER];
+            float run = 0.f;
+            int lastz = -1;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int r = lane * PER + k;
+                const float l = ell_pre[k];
+                const bool reset = (l == -INFINITY);
+                run += reset ? 0.f : l * kLog2e;
+                if (reset) lastz = r;
+                v[k] = run;
+                zz[k] = lastz;
+            }
+            float tot = run;
+            int zt = lastz;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, tot, off);
+                const int oz = __shfl_up_sync(0xffffffffu, zt, off);
+                if (lane >= off) {
+                    tot += o;
+                    zt = max(zt, oz);
+                }
+            }
+            float ex = __shfl_up_sync(0xffffffffu, tot, 1);
+            int zex = __shfl_up_sync(0xffffffffu, zt, 1);
+            if (lane == 0) {
+                ex = 0.f;
+                zex = -1;
+            }
+            const float cL = __shfl_sync(0xffffffffu, tot, 31);
+            const int zL = __shfl_sync(0xffffffffu, zt, 31);
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                v[k] += ex;
+                zz[k] = max(zz[k], zex);
+                cl[lane * PER + k] = v[k];
+                zr[lane * PER + k] = zz[k];
+            }
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int r = lane * PER + k;
+                const float lam = zz[k] >= 0 ? 0.f : ex2(v[k]);
+                const float gam = zL > r ? 0.f : ex2(cL - v[k]);
+                wout[r] = REV ? gam : lam;
+                wst[r] = REV ? lam : gam;
+                // D_rs = 2^(cl_r - cl_s) over a 32-token piece of s that row r lies past
+                // (forward: every s < r; reversed: every s > r) splits as
+                // 2^(cl_r - cl_e) * 2^(cl_e - cl_s), e the piece's token nearest r.
+                // With log-decays <= 0, cl is nonincreasing and both factors are <= 1.
+                gcol[r] = REV ? ex2(v[k] - cl[r & ~31]) : ex2(cl[r | 31] - v[k]);
+            }
+            if (lane == 0) cl[5 * TC] = zL >= 0 ? 0.f : ex2(cL);
+            mbar_arrive(bar(8 + (n & 1)));  // all 32 lanes: release of this lane's writes
+            if (n + 1 < 2 * nc) load_ell(n + 1);
+        };
         auto issue_x = [&](int chunk) {
             mbar_expect_tx(bar(0), (uint32_t)C::X_BYTES);
             for (int kb = 0; kb < C::KBX; ++kb)
@@ -303,7 +423,7 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
 #pragma unroll
                 for (int kk = 0; kk < TC / 16; ++kk) {
                     // tokens 16kk.. lie in piece kk/2: high part at its columns 0..15, low part at 16..31
-                    const uint32_t acol = C::C_P + (uint32_t)(kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
+                    const uint32_t acol = C::C_PB + (uint32_t)(kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
                     mma_ts(tmem + C::C_OA, tmem + acol, smem_desc(sbase + oz + kk * 2048, 8192, 1024), id,
                            (part | kk) ? 1u : 0u);
                 }
@@ -314,6 +434,9 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
             issue_yz(0, chunk_at(0));
             if (nc > 1) issue_yz(1, chunk_at(1));
         }
+        load_ell(0);
+        compute_decays(0);
+        compute_decays(1);  // visit 1 is phase 2's first chunk when nc == 1
         for (int i = 0; i < nc; ++i) {
             const int b = i & 1;
             wait(1 + b);
@@ -324,26 +447,27 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
                 mma_commit(bar(5));
             }
             __syncwarp();
+            if (i + 2 <= nc) compute_decays(i + 2);  // buffer i & 1: visit i's readers are past Zs
             wait(5);
             if (leader && i + 2 < nc) issue_yz(b, chunk_at(i + 2));
         }
-        // ---- phase 2 loads start while the math warps look back
+        // ---- phase 2 loads and the first scores while the math warps look back
         if (leader) {
             issue_yz(0, chunk_at(0));
             if (nc > 1) issue_yz(1, chunk_at(1));
             issue_x(chunk_at(0));
             if (has_w) issue_w(chunk_at(0));
         }
+        wait(1);
+        wait(0);
+        if (leader) {
+            tc_fence_after();
+            issue_p(0);
+            mma_commit(bar(4));
+        }
+        __syncwarp();
         for (int i = 0; i < nc; ++i) {
             const int b = i & 1;
-            wait(1 + b);
-            wait(0);
-            if (leader) {
-                tc_fence_after();
-                issue_p(b);
-                mma_commit(bar(4));
-            }
-            __syncwarp();
             bar_sync(kBarDone, kAllThreads);  // previous chunk finished; State's bf16 parts written
             if (leader) {
                 tc_fence_after();
@@ -361,13 +485,25 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
             __syncwarp();
             wait(7);  // P and O_inter done: X is free
             if (leader && i + 1 < nc) issue_x(chunk_at(i + 1));
-            bar_sync(kBarPmask, kAllThreads);
+            __syncwarp();
+            if (i + 1 < nc) compute_decays(nc + i + 1);  // its buffer's last readers finished chunk i - 1
+            bar_sync(kBarPmask, kAllThreads);  // masked P written, P read
             if (leader) {
                 tc_fence_after();
                 issue_intra(b);
                 mma_commit(bar(6));
             }
             __syncwarp();
+            if (i + 1 < nc) {
+                wait(1 + (b ^ 1));
+                wait(0);
+                if (leader) {
+                    tc_fence_after();
+                    issue_p(b ^ 1);
+                    mma_commit(bar(4));
+                }
+                __syncwarp();
+            }
             wait(6);
             wait(5);
             if (leader && i + 2 < nc) issue_yz(b, chunk_at(i + 2));
@@ -375,91 +511,25 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
         bar_sync(kBarDone, kAllThreads);  // the last chunk's arrival
     } else {
         // ============================================================ math warps
-        const int mtid = tid;  // 0..255
+        const int q = warp & 3;    // TMEM lane quarter
+        const int hf = warp >> 2;  // which half of the columns this warp handles
+        const int mtid = tid;      // 0..255
         const int prow = (TC == 128) ? q * 32 + lane : (lane < 16 ? q * 16 + lane : -1);
         const int srow = (DX == 128) ? q * 32 + lane : (lane < 16 ? q * 16 + lane : -1);
         const uint32_t tlane = (uint32_t)(q * 32) << 16;
-        float *cl = reinterpret_cast<float *>(smem + C::OFF_DEC);
-        int *zr = reinterpret_cast<int *>(cl + TC);
-        float *wout = reinterpret_cast<float *>(zr + TC);
-        float *wst = wout + TC;
-        float *dotp = wst + TC;  // [2][Tc] half-row dot products
-        const float *Lb = p.ell + (size_t)bh * p.T;
+        auto wait_dec = [&](int n) {
+            if (!mbar_wait(bar(8 + (n & 1)), (uint32_t)((n >> 1) & 1))) timed_out = true;
+        };
 
-        // Warp 0 computes a chunk's decays from log-decays it loaded one chunk
-        // earlier (load_ell), so the global load latency is off the critical path.
-        constexpr int PER = TC / 32;
-        float ell_pre[PER];
-        auto load_ell = [&](int chunk) {
-            if (warp == 0) {
-                const long long t0 = (long long)chunk * TC;
-#pragma unroll
-                for (int k = 0; k < PER; ++k) {
-                    const long long t = t0 + lane * PER + k;
-                    ell_pre[k] = (t < p.T) ? __ldg(Lb + t) : 0.f;
-                }
-            }
-        };
-        auto decays = [&](int next_chunk) {
-            if (warp == 0) {
-                float v[PER];
-                int zz[PER];
-                float run = 0.f;
-                int lastz = -1;
-#pragma unroll
-                for (int k = 0; k < PER; ++k) {
-                    const int r = lane * PER + k;
-                    const float l = ell_pre[k];
-                    const bool reset = (l == -INFINITY);
-                    run += reset ? 0.f : l * kLog2e;
-                    if (reset) lastz = r;
-                    v[k] = run;
-                    zz[k] = lastz;
-                }
-                float tot = run;
-                int zt = lastz;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float o = __shfl_up_sync(0xffffffffu, tot, off);
-                    const int oz = __shfl_up_sync(0xffffffffu, zt, off);
-                    if (lane >= off) {
-                        tot += o;
-                        zt = max(zt, oz);
-                    }
-                }
-                float ex = __shfl_up_sync(0xffffffffu, tot, 1);
-                int zex = __shfl_up_sync(0xffffffffu, zt, 1);
-                if (lane == 0) {
-                    ex = 0.f;
-                    zex = -1;
-                }
-#pragma unroll
-                for (int k = 0; k < PER; ++k) {
-                    cl[lane * PER + k] = v[k] + ex;
-                    zr[lane * PER + k] = max(zz[k], zex);
-                }
-                __syncwarp();
-                const float cL = cl[TC - 1];
-                const int zL = zr[TC - 1];
-#pragma unroll
-                for (int k = 0; k < PER; ++k) {
-                    const int r = lane * PER + k;
-                    const float lam = zr[r] >= 0 ? 0.f : ex2(cl[r]);
-                    const float gam = zL > r ? 0.f : ex2(cL - cl[r]);
-                    wout[r] = REV ? gam : lam;
-                    wst[r] = REV ? lam : gam;
-                }
-                if (lane == 0) s_alpha = zL >= 0 ? 0.f : ex2(cL);
-                if (next_chunk >= 0) load_ell(next_chunk);
-            }
-        };
         // Zs = diag(w_state) Z as two bf16 parts, K-major [64 rows n][Tc tokens]: 8x8 blocks of
         // Z read transposed (ldmatrix.trans), scaled per token, split, written with stmatrix.
-        auto write_zs = [&](int b) {
+        auto write_zs = [&](int b, const float *wst) {
             const uint32_t zt = sbase + (b ? C::OFF_Z1 : C::OFF_Z0);
             constexpr int NBLK = (TC / 8) * 8;
             const int j = lane & 7, blk_in = lane >> 3;
-            for (int g4 = warp; g4 < NBLK / 4; g4 += 8) {
+#pragma unroll
+            for (int it = 0; it < NBLK / 32; ++it) {
+                const int g4 = warp + 8 * it;
                 const int tb = g4 >> 1;
                 uint32_t r[4];
                 ldsm_x4_trans(zt + sw128(tb * 8 + j, (4 * (g4 & 1) + blk_in) * 8), r);
@@ -510,15 +580,14 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
 
         // ---- phase 1
         float alpha_seg = 1.f;
-        load_ell(chunk_at(0));
         for (int i = 0; i < nc; ++i) {
             const int b = i & 1;
             wait(1 + b);
-            decays(chunk_at(i + 1 < nc ? i + 1 : 0));  // phase 2 starts again at chunk_at(0)
-            bar_sync(kBarMath, kMathThreads);
-            const float alpha = s_alpha;
+            wait_dec(i);
+            const float *dv = dbuf(i);
+            const float alpha = dv[5 * TC];
             alpha_seg *= alpha;
-            write_zs(b);
+            write_zs(b, dv + 3 * TC);
             fence_async_smem();
             bar_arrive(kBarZs, kAllThreads);
             wait(5);
@@ -618,59 +687,76 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
         bar_arrive(kBarDone, kAllThreads);  // State's bf16 parts for chunk 0
         for (int i = 0; i < nc; ++i) {
             const int b = i & 1;
-            const int chunk = chunk_at(i);
-            const long long t0 = (long long)chunk * TC;
+            const long long t0 = (long long)chunk_at(i) * TC;
+            const float *cl = dbuf(nc + i);
+            const int *zr = reinterpret_cast<const int *>(cl + TC);
+            const float *wout = cl + 2 * TC, *wst = cl + 3 * TC, *gcol = cl + 4 * TC;
             wait(1 + b);
-            decays(i + 1 < nc ? chunk_at(i + 1) : -1);
+            wait_dec(nc + i);
+            const float alpha = cl[5 * TC];
+            if (mtid == 0) tma_store_wait_read();  // the previous chunk's output tile has been read
             bar_sync(kBarMath, kMathThreads);
-            const float alpha = s_alpha;
-            write_zs(b);
+            write_zs(b, wst);
             fence_async_smem();
             bar_arrive(kBarZs, kAllThreads);
-            // ---- mask and decay P, split into bf16 parts, back into TMEM in place
+            // ---- mask and decay P (fp32, TMEM) into its bf16 parts (TMEM)
             wait(4);
             tc_fence_after();
             {
                 const int r = prow < 0 ? 0 : prow;
                 const float clr = cl[r];
                 const int zrr = zr[r];
-                const int rmin = (TC == 128) ? q * 32 : q * 16, rmax = (TC == 128) ? q * 32 + 31 : q * 16 + 15;
+                // the 32-token piece holding this warp's rows; other pieces are either fully
+                // masked or lie entirely on the unmasked side of every row (off-diagonal)
+                const int rpiece = ((TC == 128) ? q * 32 : q * 16) >> 5;
                 constexpr int PIECES = TC / 64;  // pieces of 32 tokens per warp
+                auto store_parts = [&](int s0, float (&x)[32]) {
 #pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t hi[8], lo[8];
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const float x0 = x[16 * h + 2 * jj], x1 = x[16 * h + 2 * jj + 1];
+                            hi[jj] = pack_bf16(x0, x1);
+                            const float2 fh = unpack_bf16(hi[jj]);
+                            lo[jj] = pack_bf16(x0 - fh.x, x1 - fh.y);
+                        }
+                        tmem_st8(tmem + tlane + C::C_PB + (uint32_t)(s0 + 8 * h), hi);
+                        tmem_st8(tmem + tlane + C::C_PB + (uint32_t)(s0 + 16 + 8 * h), lo);
+                    }
+                };
+#pragma unroll 1
                 for (int pc = 0; pc < PIECES; ++pc) {
                     const int piece = hf * PIECES + pc;
                     const int s0 = piece * 32;
-                    const uint32_t col = C::C_P + (uint32_t)s0;
-                    uint32_t hi[16], lo[16];
-                    const bool all_masked = REV ? (s0 + 31 < rmin) : (s0 > rmax);  // warp-uniform
-                    if (all_masked) {
+                    float x[32];
+                    if (REV ? (piece < rpiece) : (piece > rpiece)) {  // fully masked (warp-uniform)
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            hi[jj] = 0u;
-                            lo[jj] = 0u;
-                        }
+                        for (int e = 0; e < 32; ++e) x[e] = 0.f;
                     } else {
                         uint32_t pr[32];
-                        tmem_ld32(tmem + tlane + col, pr);
+                        tmem_ld32(tmem + tlane + C::C_P + (uint32_t)s0, pr);
                         tmem_ld_wait();
+                        if (piece != rpiece) {
+                            // off-diagonal: row factor times column factor
+                            const float f = REV ? ex2(cl[s0] - clr) : ex2(clr - cl[s0 + 31]);
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            float x[2];
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int s = s0 + 2 * jj + e;
-                                float m;
-                                if (!REV) m = (s <= r && zrr <= s) ? ex2(clr - cl[s]) : 0.f;
-                                else m = (s >= r && zr[s] <= r) ? ex2(cl[s] - clr) : 0.f;
-                                x[e] = __uint_as_float(pr[2 * jj + e]) * m;
+                            for (int e = 0; e < 32; ++e) {
+                                const int s = s0 + e;
+                                const bool keep = REV ? (zr[s] <= r) : (zrr <= s);
+                                x[e] = keep ? __uint_as_float(pr[e]) * (f * gcol[s]) : 0.f;
                             }
-                            hi[jj] = pack_bf16(x[0], x[1]);
-                            const float2 fh = unpack_bf16(hi[jj]);
-                            lo[jj] = pack_bf16(x[0] - fh.x, x[1] - fh.y);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const int s = s0 + e;
+                                const bool keep = REV ? (s >= r && zr[s] <= r) : (s <= r && zrr <= s);
+                                const float m = ex2(REV ? cl[s] - clr : clr - cl[s]);
+                                x[e] = keep ? __uint_as_float(pr[e]) * m : 0.f;
+                            }
                         }
                     }
-                    tmem_st16(tmem + tlane + col, hi);
-                    tmem_st16(tmem + tlane + col + 16, lo);
+                    store_parts(s0, x);
                 }
                 tmem_st_wait();
             }
@@ -680,7 +766,8 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
             wait(5);
             tc_fence_after();
             state_accumulate(alpha);
-            // ---- OUT = O_intra + w_out O_inter (this warp: columns [32 hf, 32 hf + 32)), straight to HBM
+            // ---- OUT = O_intra + w_out O_inter (this warp: columns [32 hf, 32 hf + 32)), staged in the
+            // 128-byte-swizzled output tile, written by a TMA store
             wait(7);
             wait(6);
             tc_fence_after();
@@ -695,27 +782,26 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
                 float o[32];
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) o[jj] = fmaf(wr, __uint_as_float(oi[jj]), __uint_as_float(oa[jj]));
-                if (prow >= 0 && t0 + prow < p.T) {
-                    if (has_w) {
-                        float dot = 0.f;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint4 qq =
-                                *reinterpret_cast<const uint4 *>(smem + C::OFF_W + sw128(r, hf * 32 + c * 8));
-                            const uint32_t words[4] = {qq.x, qq.y, qq.z, qq.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = unpack_bf16(words[e]);
-                                dot = fmaf(o[c * 8 + 2 * e], f.x, fmaf(o[c * 8 + 2 * e + 1], f.y, dot));
-                            }
-                        }
-                        dotp[hf * TC + r] = dot;
-                    }
-                    float4 *dst = reinterpret_cast<float4 *>(p.out + ((size_t)bh * p.T + t0 + prow) * p.DZ + zb * 64 +
-                                                             hf * 32);
+                if (prow >= 0) {
+                    const uint32_t row = sbase + C::OFF_ZSH + (uint32_t)(hf * TC * 128 + prow * 128);
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        __stcs(dst + c, make_float4(o[c * 4], o[c * 4 + 1], o[c * 4 + 2], o[c * 4 + 3]));
+                        st_shared_v4(row + (uint32_t)((c ^ (prow & 7)) << 4), o[c * 4], o[c * 4 + 1], o[c * 4 + 2],
+                                     o[c * 4 + 3]);
+                }
+                if (has_w && prow >= 0 && t0 + prow < p.T) {
+                    float dot = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 qq = *reinterpret_cast<const uint4 *>(smem + C::OFF_W + sw128(r, hf * 32 + c * 8));
+                        const uint32_t words[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 fw = unpack_bf16(words[e]);
+                            dot = fmaf(o[c * 8 + 2 * e], fw.x, fmaf(o[c * 8 + 2 * e + 1], fw.y, dot));
+                        }
+                    }
+                    dotp[hf * TC + r] = dot;
                 }
             }
             // State's bf16 parts for the next chunk (this chunk's O_inter has consumed them)
@@ -723,10 +809,18 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
             fence_async_smem();
             tc_fence_before();
             bar_sync(kBarMath, kMathThreads);
+            if (mtid == 0) {
+                // rows past T are clipped by the store; the Zs buffers are rewritten only after
+                // the store has read them (tma_store_wait_read before the next chunk's Zs)
+                tma_store_3d(&maps.out, zb * 64, (int)t0, bh, sbase + C::OFF_ZSH);
+                tma_store_3d(&maps.out, zb * 64 + 32, (int)t0, bh, sbase + C::OFF_ZSH + TC * 128);
+                tma_store_commit();
+            }
             if (has_w && hf == 0 && prow >= 0 && t0 + prow < p.T)
                 p.wdot[((size_t)zb * p.BH + bh) * p.T + t0 + prow] = dotp[prow] + dotp[TC + prow];
             bar_arrive(kBarDone, kAllThreads);
         }
+        if (mtid == 0) tma_store_wait_all();
 
         // ---- final state of the sequence
         const bool last = REV ? (seg == 0) : (seg == p.n_seg - 1);
@@ -775,16 +869,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 3-D map over a bf16 [BH][T][cols] array with a {64, rows, 1} box.
-bool make_map(CUtensorMap *m, const void *base, int cols, long long T, int BH, int rows) {
+// 3-D map over a [BH][T][cols] array with 128-byte-swizzled boxes of 128-byte rows:
+// {64, rows, 1} for bf16 operands, {32, rows, 1} for the fp32 output.
+bool make_map(CUtensorMap *m, const void *base, int cols, long long T, int BH, int rows, bool bf16 = true) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    const size_t es = 2;
+    const size_t es = bf16 ? 2 : 4;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)T, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)cols * es, (cuuint64_t)cols * es * (cuuint64_t)T};
-    cuuint32_t box[3] = {64u, (cuuint32_t)rows, 1u};
+    cuuint32_t box[3] = {bf16 ? 64u : 32u, (cuuint32_t)rows, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -804,7 +899,8 @@ int launch_tc_variant(const LaArgs &a, cudaStream_t s, unsigned int grid) {
     memset(&maps, 0, sizeof(maps));
     bool ok = make_map(&maps.x, a.X, DX, a.T, a.BH, TC) &&
               make_map(&maps.y, a.Y, DX, a.T, a.BH, TC) &&
-              make_map(&maps.z, a.Z, a.DZ, a.T, a.BH, TC);
+              make_map(&maps.z, a.Z, a.DZ, a.T, a.BH, TC) &&
+              make_map(&maps.out, a.out, a.DZ, a.T, a.BH, TC, false);
     if (ok && a.W != nullptr) ok = make_map(&maps.w, a.W, a.DZ, a.T, a.BH, TC);
     if (!ok) return fail(CLA_ERR_CUDA, "chunk_la: tensor map encoding failed");
     la_tc_kernel<DX, TC, REV><<<grid, C::NT, C::SMEM, s>>>(maps, a);
