@@ -91,21 +91,28 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, 
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// Warp-wide forms: every lane of the warp executes them with the same
+// operands (so the compiler keeps those in uniform registers); one elected
+// lane issues.
+__device__ __forceinline__ void mma_ss_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "{\n .reg .pred p, e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
-            d),
+        "{\n .reg .pred p, e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+__device__ __forceinline__ void mma_commit_w(uint32_t bar) {
+    asm volatile(
+        "{\n .reg .pred e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
+        : "memory");
 }
 // 32 consecutive 32-bit TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -155,24 +162,26 @@ __device__ __forceinline__ uint32_t sw128(int row, int col) {
 // ----------------------------------------------------------------- configuration
 template <int DX, int TC>
 struct TcCfg {
-    static constexpr int NT = 288;       // 8 math warps (w and w + 4 share TMEM lane quarter w) + 1 producer warp
+    static constexpr int NT = 320;  // 8 math warps (w and w + 4 share TMEM lane quarter w), producer, decay warp
     static constexpr int KBX = DX / 64;  // 64-column blocks of X and Y
     static constexpr int KBT = TC / 64;  // 64-token blocks of Zs
-    // TMEM columns.  P (fp32, Tc columns) is overwritten in place, 32 tokens
-    // at a time, by its bf16 high part (16 columns) and low part (16 columns).
+    // TMEM columns: P (fp32), the accumulators, and the masked P as bf16 parts.
     static constexpr uint32_t C_P = 0;
     static constexpr uint32_t C_OI = TC;        // O_inter
     static constexpr uint32_t C_OA = TC + 64;   // O_intra
-    static constexpr uint32_t C_DS = TC + 128;  // dS
+    static constexpr uint32_t C_DS = TC + 128;  // dS: Y^T Zs_hi in 64 columns, then Y^T Zs_lo in 64
     // masked, decayed P as the bf16 A operand of O_intra: per 32-token piece,
     // the high part in its first 16 columns and the low part in the next 16
-    static constexpr uint32_t C_PB = TC + 192;
-    static constexpr uint32_t TMEM_COLS = (2 * TC + 192 <= 256) ? 256 : 512;
+    static constexpr uint32_t C_PB = TC + 256;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(C_PB + TC <= TMEM_COLS, "tensor memory budget");
     // shared memory (offsets from a 1024-aligned base)
     static constexpr int X_BYTES = KBX * TC * 128;
     static constexpr int Z_BYTES = TC * 128;
     static constexpr int S_BYTES = DX * 128;         // one bf16 part of State (MN-major)
-    static constexpr int ZS_BYTES = KBT * 64 * 128;  // one bf16 part of Zs (K-major)
+    // Zs as the K-major B operand of dS, N = 128: per 64-token block, rows
+    // 0..63 hold Zs_hi and rows 64..127 Zs_lo (16 KB per block)
+    static constexpr int ZS_BYTES = KBT * 128 * 128;
     static constexpr int OFF_X = 0;
     static constexpr int OFF_Y0 = OFF_X + X_BYTES;
     static constexpr int OFF_Y1 = OFF_Y0 + X_BYTES;
@@ -181,18 +190,17 @@ struct TcCfg {
     static constexpr int OFF_W = OFF_Z1 + Z_BYTES;
     static constexpr int OFF_SH = OFF_W + Z_BYTES;
     static constexpr int OFF_SL = OFF_SH + S_BYTES;
-    // Zs_hi, Zs_lo; after the chunk's dS product, the fp32 output tile (two
+    // Zs; after the chunk's dS product, the fp32 output tile (two
     // 128-byte-swizzled halves of Tc rows x 32 columns) for the TMA store
-    static constexpr int OFF_ZSH = OFF_SL + S_BYTES;
-    static constexpr int OFF_ZSL = OFF_ZSH + ZS_BYTES;
-    static constexpr int OFF_DEC = OFF_ZSL + ZS_BYTES;
+    static constexpr int OFF_ZS = OFF_SL + S_BYTES;
+    static constexpr int OFF_DEC = OFF_ZS + ZS_BYTES;
     // decays, two buffers (chunk sequence number parity) of cl, zr, w_out,
     // w_state, g [Tc] and alpha; then the two half-row dot products [2][Tc]
     static constexpr int DEC_STRIDE = 5 * TC + 4;  // floats per buffer
     static constexpr int DEC_BYTES = (2 * DEC_STRIDE + 2 * TC) * 4;
     static constexpr int OFF_BAR = OFF_DEC + DEC_BYTES;
-    static constexpr int SMEM = OFF_BAR + 128 + 1024;  // 10 mbarriers + alignment slack
-    static_assert(2 * ZS_BYTES == TC * 64 * 4, "the output tile fits the Zs buffers");
+    static constexpr int SMEM = OFF_BAR + 128 + 1024;  // 12 mbarriers + alignment slack
+    static_assert(ZS_BYTES == TC * 64 * 4, "the output tile fits the Zs buffer");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
@@ -217,7 +225,8 @@ constexpr int kBarZs = 2;     // math: Zs written          -> producer may issue
 constexpr int kBarPmask = 3;  // math: P masked and split  -> producer may issue O_intra
 constexpr int kBarDone = 4;   // math: chunk finished      -> producer may issue the next O_inter
 constexpr int kMathThreads = 256;
-constexpr int kAllThreads = 288;
+constexpr int kAllThreads = 288;    // math warps + producer: the named-barrier count
+constexpr int kBlockThreads = 320;  // + the decay warp
 
 __device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void bar_arrive(int id, int n) {
@@ -225,7 +234,7 @@ __device__ __forceinline__ void bar_arrive(int id, int n) {
 }
 
 template <int DX, int TC, bool REV>
-__global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_constant__ TcMaps maps, const LaArgs p) {
+__global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_constant__ TcMaps maps, const LaArgs p) {
     using C = TcCfg<DX, TC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -238,6 +247,7 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool producer = (warp == 8);
     // mbarriers: 0 X, 1 YZ0, 2 YZ1, 3 W, 4 P, 5 dS, 6 O_intra, 7 O_inter, 8-9 decay buffers
+    // full (the decay warp's 32 lanes arrive), 10-11 decay buffers empty (one arrival per math warp)
     const uint32_t bar0 = sbase + C::OFF_BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
@@ -252,6 +262,8 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
         for (int i = 0; i < 8; ++i) mbar_init(bar(i), 1);
         mbar_init(bar(8), 32);
         mbar_init(bar(9), 32);
+        mbar_init(bar(10), 8);
+        mbar_init(bar(11), 8);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_ticket = atomicAdd(&p.hdr->ticket[p.ticket_slot], 1u);
     }
@@ -276,9 +288,10 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
         if (!mbar_wait(bar(i), ph[i])) timed_out = true;
         ph[i] ^= 1u;
     };
-    // Decays are computed once per chunk visit.  Visits are numbered 0..2nc-1
-    // (phase 1, then phase 2); visit n uses decay buffer n & 1, whose mbarrier
-    // completes one phase per use, so its parity for visit n is (n >> 1) & 1.
+    // Decays are computed once per chunk visit, by the decay warp.  Visits are
+    // numbered 0..2nc-1 (phase 1, then phase 2); visit n uses decay buffer
+    // n & 1, whose full and empty mbarriers complete one phase per use: visit
+    // n is use n >> 1 of its buffer.
     float *dec = reinterpret_cast<float *>(smem + C::OFF_DEC);
     auto dbuf = [&](int n) { return dec + (n & 1) * C::DEC_STRIDE; };
     float *dotp = dec + 2 * C::DEC_STRIDE;  // [2][Tc] half-row dot products
@@ -286,6 +299,132 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
     if (producer) {
         // ============================================================ producer warp
         const bool leader = (lane == 0);
+        auto issue_x = [&](int chunk) {
+            mbar_expect_tx(bar(0), (uint32_t)C::X_BYTES);
+            for (int kb = 0; kb < C::KBX; ++kb)
+                tma_load_3d(sbase + C::OFF_X + kb * TC * 128, &maps.x, kb * 64, chunk * TC, bh, bar(0));
+        };
+        auto issue_yz = [&](int b, int chunk) {
+            mbar_expect_tx(bar(1 + b), (uint32_t)(C::X_BYTES + C::Z_BYTES));
+            const uint32_t oy = b ? C::OFF_Y1 : C::OFF_Y0, oz = b ? C::OFF_Z1 : C::OFF_Z0;
+            for (int kb = 0; kb < C::KBX; ++kb)
+                tma_load_3d(sbase + oy + kb * TC * 128, &maps.y, kb * 64, chunk * TC, bh, bar(1 + b));
+            tma_load_3d(sbase + oz, &maps.z, zb * 64, chunk * TC, bh, bar(1 + b));
+        };
+        auto issue_w = [&](int chunk) {
+            mbar_expect_tx(bar(3), (uint32_t)C::Z_BYTES);
+            tma_load_3d(sbase + C::OFF_W, &maps.w, zb * 64, chunk * TC, bh, bar(3));
+        };
+        // Descriptors of every operand tile, built once; a K step adds a constant
+        // byte offset (>> 4) to the start-address field.
+        const uint64_t dX = smem_desc(sbase + C::OFF_X, 16, 1024);                  // K-major
+        const uint64_t dY[2] = {smem_desc(sbase + C::OFF_Y0, 16, 1024), smem_desc(sbase + C::OFF_Y1, 16, 1024)};
+        const uint64_t dYt[2] = {smem_desc(sbase + C::OFF_Y0, TC * 128, 1024),     // MN-major (Y^T)
+                                 smem_desc(sbase + C::OFF_Y1, TC * 128, 1024)};
+        const uint64_t dZ[2] = {smem_desc(sbase + C::OFF_Z0, 8192, 1024),          // MN-major
+                                smem_desc(sbase + C::OFF_Z1, 8192, 1024)};
+        const uint64_t dS[2] = {smem_desc(sbase + C::OFF_SH, 8192, 1024), smem_desc(sbase + C::OFF_SL, 8192, 1024)};
+        const uint64_t dZs = smem_desc(sbase + C::OFF_ZS, 16, 1024);               // K-major, 128 rows
+        auto issue_state_mma = [&](int b) {
+            // dS = Y^T [Zs_hi | Zs_lo]  (M = DX, N = 128, K = Tc)
+            constexpr uint32_t id = idesc_bf16(DX, 128, 1, 0);
+            const uint64_t a0 = dYt[b];
+#pragma unroll
+            for (int kk = 0; kk < TC / 16; ++kk)
+                mma_ss_w(tmem + C::C_DS, a0 + (uint64_t)(kk * 2048 / 16),
+                         dZs + (uint64_t)(((kk >> 2) * 128 * 128 + (kk & 3) * 32) / 16), id, kk ? 1u : 0u);
+        };
+        auto issue_p = [&](int b) {
+            constexpr uint32_t idp = idesc_bf16(TC, TC, 0, 0);
+            const uint64_t b0 = dY[b];
+#pragma unroll
+            for (int kk = 0; kk < DX / 16; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * TC * 128 + (kk & 3) * 32) / 16);
+                mma_ss_w(tmem + C::C_P, dX + off, b0 + off, idp, kk ? 1u : 0u);
+            }
+        };
+        auto issue_inter = [&]() {
+            constexpr uint32_t ido = idesc_bf16(TC, 64, 0, 1);
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                for (int kk = 0; kk < DX / 16; ++kk)
+                    mma_ss_w(tmem + C::C_OI, dX + (uint64_t)(((kk >> 2) * TC * 128 + (kk & 3) * 32) / 16),
+                             dS[part] + (uint64_t)(kk * 2048 / 16), ido, (part | kk) ? 1u : 0u);
+            }
+        };
+        auto issue_intra = [&](int b) {
+            constexpr uint32_t id = idesc_bf16(TC, 64, 0, 1);
+            const uint64_t b0 = dZ[b];
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                for (int kk = 0; kk < TC / 16; ++kk) {
+                    // tokens 16kk.. lie in piece kk/2: high part at its columns 0..15, low part at 16..31
+                    const uint32_t acol = C::C_PB + (uint32_t)(kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
+                    mma_ts_w(tmem + C::C_OA, tmem + acol, b0 + (uint64_t)(kk * 2048 / 16), id, (part | kk) ? 1u : 0u);
+                }
+            }
+        };
+        // ---- phase 1: dS per chunk
+        if (leader) {
+            issue_yz(0, chunk_at(0));
+            if (nc > 1) issue_yz(1, chunk_at(1));
+        }
+        for (int i = 0; i < nc; ++i) {
+            const int b = i & 1;
+            wait(1 + b);
+            bar_sync(kBarZs, kAllThreads);
+            tc_fence_after();
+            issue_state_mma(b);
+            mma_commit_w(bar(5));
+            wait(5);
+            if (leader && i + 2 < nc) issue_yz(b, chunk_at(i + 2));
+        }
+        // ---- phase 2 loads and the first scores while the math warps look back
+        if (leader) {
+            issue_yz(0, chunk_at(0));
+            if (nc > 1) issue_yz(1, chunk_at(1));
+            issue_x(chunk_at(0));
+            if (has_w) issue_w(chunk_at(0));
+        }
+        wait(1);
+        wait(0);
+        tc_fence_after();
+        issue_p(0);
+        mma_commit_w(bar(4));
+        for (int i = 0; i < nc; ++i) {
+            const int b = i & 1;
+            bar_sync(kBarDone, kAllThreads);  // previous chunk finished; State's bf16 parts written
+            tc_fence_after();
+            issue_inter();
+            mma_commit_w(bar(7));
+            if (leader && has_w && i > 0) issue_w(chunk_at(i));
+            __syncwarp();
+            bar_sync(kBarZs, kAllThreads);
+            tc_fence_after();
+            issue_state_mma(b);
+            mma_commit_w(bar(5));
+            wait(7);  // P and O_inter done: X is free
+            if (leader && i + 1 < nc) issue_x(chunk_at(i + 1));
+            bar_sync(kBarPmask, kAllThreads);  // masked P written, P read
+            tc_fence_after();
+            issue_intra(b);
+            mma_commit_w(bar(6));
+            if (i + 1 < nc) {
+                wait(1 + (b ^ 1));
+                wait(0);
+                tc_fence_after();
+                issue_p(b ^ 1);
+                mma_commit_w(bar(4));
+            }
+            wait(6);
+            wait(5);
+            if (leader && i + 2 < nc) issue_yz(b, chunk_at(i + 2));
+        }
+        bar_sync(kBarDone, kAllThreads);  // the last chunk's arrival
+    } else if (warp == 9) {
+        // ============================================================ decay warp
         const float *Lb = p.ell + (size_t)bh * p.T;
         // decays of visit n, by the whole warp: cl_r = in-chunk sum of log2 a up to r (resets
         // skipped), zr_r = last reset at or before r, w_out / w_state, the column factors g of
@@ -360,155 +499,14 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
             }
             if (lane == 0) cl[5 * TC] = zL >= 0 ? 0.f : ex2(cL);
             mbar_arrive(bar(8 + (n & 1)));  // all 32 lanes: release of this lane's writes
-            if (n + 1 < 2 * nc) load_ell(n + 1);
         };
-        auto issue_x = [&](int chunk) {
-            mbar_expect_tx(bar(0), (uint32_t)C::X_BYTES);
-            for (int kb = 0; kb < C::KBX; ++kb)
-                tma_load_3d(sbase + C::OFF_X + kb * TC * 128, &maps.x, kb * 64, chunk * TC, bh, bar(0));
-        };
-        auto issue_yz = [&](int b, int chunk) {
-            mbar_expect_tx(bar(1 + b), (uint32_t)(C::X_BYTES + C::Z_BYTES));
-            const uint32_t oy = b ? C::OFF_Y1 : C::OFF_Y0, oz = b ? C::OFF_Z1 : C::OFF_Z0;
-            for (int kb = 0; kb < C::KBX; ++kb)
-                tma_load_3d(sbase + oy + kb * TC * 128, &maps.y, kb * 64, chunk * TC, bh, bar(1 + b));
-            tma_load_3d(sbase + oz, &maps.z, zb * 64, chunk * TC, bh, bar(1 + b));
-        };
-        auto issue_w = [&](int chunk) {
-            mbar_expect_tx(bar(3), (uint32_t)C::Z_BYTES);
-            tma_load_3d(sbase + C::OFF_W, &maps.w, zb * 64, chunk * TC, bh, bar(3));
-        };
-        auto issue_state_mma = [&](int b) {
-            const uint32_t oy = b ? C::OFF_Y1 : C::OFF_Y0;
-            constexpr uint32_t id = idesc_bf16(DX, 64, 1, 0);
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                const uint32_t ozs = part ? C::OFF_ZSL : C::OFF_ZSH;
-#pragma unroll
-                for (int kk = 0; kk < TC / 16; ++kk) {
-                    const uint64_t a = smem_desc(sbase + oy + kk * 2048, TC * 128, 1024);
-                    const uint64_t bd = smem_desc(sbase + ozs + (kk >> 2) * 64 * 128 + (kk & 3) * 32, 16, 1024);
-                    mma_ss(tmem + C::C_DS, a, bd, id, (part | kk) ? 1u : 0u);
-                }
-            }
-        };
-        auto issue_p = [&](int b) {
-            const uint32_t oy = b ? C::OFF_Y1 : C::OFF_Y0;
-            constexpr uint32_t idp = idesc_bf16(TC, TC, 0, 0);
-#pragma unroll
-            for (int kk = 0; kk < DX / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * TC * 128 + (kk & 3) * 32;
-                mma_ss(tmem + C::C_P, smem_desc(sbase + C::OFF_X + off, 16, 1024),
-                       smem_desc(sbase + oy + off, 16, 1024), idp, kk ? 1u : 0u);
-            }
-        };
-        auto issue_inter = [&]() {
-            constexpr uint32_t ido = idesc_bf16(TC, 64, 0, 1);
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                const uint32_t os = part ? C::OFF_SL : C::OFF_SH;
-#pragma unroll
-                for (int kk = 0; kk < DX / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * TC * 128 + (kk & 3) * 32;
-                    mma_ss(tmem + C::C_OI, smem_desc(sbase + C::OFF_X + off, 16, 1024),
-                           smem_desc(sbase + os + kk * 2048, 8192, 1024), ido, (part | kk) ? 1u : 0u);
-                }
-            }
-        };
-        auto issue_intra = [&](int b) {
-            const uint32_t oz = b ? C::OFF_Z1 : C::OFF_Z0;
-            constexpr uint32_t id = idesc_bf16(TC, 64, 0, 1);
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                for (int kk = 0; kk < TC / 16; ++kk) {
-                    // tokens 16kk.. lie in piece kk/2: high part at its columns 0..15, low part at 16..31
-                    const uint32_t acol = C::C_PB + (uint32_t)(kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
-                    mma_ts(tmem + C::C_OA, tmem + acol, smem_desc(sbase + oz + kk * 2048, 8192, 1024), id,
-                           (part | kk) ? 1u : 0u);
-                }
-            }
-        };
-        // ---- phase 1: dS per chunk
-        if (leader) {
-            issue_yz(0, chunk_at(0));
-            if (nc > 1) issue_yz(1, chunk_at(1));
-        }
         load_ell(0);
-        compute_decays(0);
-        compute_decays(1);  // visit 1 is phase 2's first chunk when nc == 1
-        for (int i = 0; i < nc; ++i) {
-            const int b = i & 1;
-            wait(1 + b);
-            bar_sync(kBarZs, kAllThreads);
-            if (leader) {
-                tc_fence_after();
-                issue_state_mma(b);
-                mma_commit(bar(5));
-            }
-            __syncwarp();
-            if (i + 2 <= nc) compute_decays(i + 2);  // buffer i & 1: visit i's readers are past Zs
-            wait(5);
-            if (leader && i + 2 < nc) issue_yz(b, chunk_at(i + 2));
+        for (int n = 0; n < 2 * nc; ++n) {
+            const int use = n >> 1;
+            if (use > 0 && !mbar_wait(bar(10 + (n & 1)), (uint32_t)((use - 1) & 1))) timed_out = true;
+            compute_decays(n);
+            if (n + 1 < 2 * nc) load_ell(n + 1);
         }
-        // ---- phase 2 loads and the first scores while the math warps look back
-        if (leader) {
-            issue_yz(0, chunk_at(0));
-            if (nc > 1) issue_yz(1, chunk_at(1));
-            issue_x(chunk_at(0));
-            if (has_w) issue_w(chunk_at(0));
-        }
-        wait(1);
-        wait(0);
-        if (leader) {
-            tc_fence_after();
-            issue_p(0);
-            mma_commit(bar(4));
-        }
-        __syncwarp();
-        for (int i = 0; i < nc; ++i) {
-            const int b = i & 1;
-            bar_sync(kBarDone, kAllThreads);  // previous chunk finished; State's bf16 parts written
-            if (leader) {
-                tc_fence_after();
-                issue_inter();
-                mma_commit(bar(7));
-                if (has_w && i > 0) issue_w(chunk_at(i));
-            }
-            __syncwarp();
-            bar_sync(kBarZs, kAllThreads);
-            if (leader) {
-                tc_fence_after();
-                issue_state_mma(b);
-                mma_commit(bar(5));
-            }
-            __syncwarp();
-            wait(7);  // P and O_inter done: X is free
-            if (leader && i + 1 < nc) issue_x(chunk_at(i + 1));
-            __syncwarp();
-            if (i + 1 < nc) compute_decays(nc + i + 1);  // its buffer's last readers finished chunk i - 1
-            bar_sync(kBarPmask, kAllThreads);  // masked P written, P read
-            if (leader) {
-                tc_fence_after();
-                issue_intra(b);
-                mma_commit(bar(6));
-            }
-            __syncwarp();
-            if (i + 1 < nc) {
-                wait(1 + (b ^ 1));
-                wait(0);
-                if (leader) {
-                    tc_fence_after();
-                    issue_p(b ^ 1);
-                    mma_commit(bar(4));
-                }
-                __syncwarp();
-            }
-            wait(6);
-            wait(5);
-            if (leader && i + 2 < nc) issue_yz(b, chunk_at(i + 2));
-        }
-        bar_sync(kBarDone, kAllThreads);  // the last chunk's arrival
     } else {
         // ============================================================ math warps
         const int q = warp & 3;    // TMEM lane quarter
@@ -545,20 +543,22 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
                     lo[i] = pack_bf16(x0 - fh.x, x1 - fh.y);
                 }
                 const int nrow = (4 * (g4 & 1) + blk_in) * 8 + j;
-                const uint32_t off = (uint32_t)((tb * 8) >> 6) * 64 * 128 + sw128(nrow, (tb * 8) & 63);
-                stsm_x4(sbase + C::OFF_ZSH + off, hi);
-                stsm_x4(sbase + C::OFF_ZSL + off, lo);
+                const uint32_t off = (uint32_t)((tb * 8) >> 6) * 128 * 128 + sw128(nrow, (tb * 8) & 63);
+                stsm_x4(sbase + C::OFF_ZS + off, hi);
+                stsm_x4(sbase + C::OFF_ZS + off + 64 * 128, lo);
             }
         };
         float S[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) S[c] = 0.f;
         auto state_accumulate = [&](float alpha) {
-            uint32_t r[32];
-            tmem_ld32(tmem + tlane + C::C_DS + hf * 32, r);
+            uint32_t rh[32], rl[32];
+            tmem_ld32(tmem + tlane + C::C_DS + hf * 32, rh);
+            tmem_ld32(tmem + tlane + C::C_DS + 64 + hf * 32, rl);
             tmem_ld_wait();
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) S[jj] = fmaf(alpha, S[jj], __uint_as_float(r[jj]));
+            for (int jj = 0; jj < 32; ++jj)
+                S[jj] = fmaf(alpha, S[jj], __uint_as_float(rh[jj]) + __uint_as_float(rl[jj]));
         };
         auto write_s_smem = [&]() {
             if (srow < 0) return;
@@ -588,6 +588,8 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
             const float alpha = dv[5 * TC];
             alpha_seg *= alpha;
             write_zs(b, dv + 3 * TC);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(10 + (i & 1)));  // this warp is done with visit i's decays
             fence_async_smem();
             bar_arrive(kBarZs, kAllThreads);
             wait(5);
@@ -602,16 +604,32 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
         float4 *inc4 = p.incl + unit * (size_t)(DX * 16);
         auto load_state0 = [&](float (&dst)[32], float scale, bool add) {
             if (srow < 0) return;
+            float v[32];
+            const int col0 = zb * 64 + hf * 32;
+            if (p.state0 == nullptr) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                float v = 0.f;
-                if (p.state0 != nullptr) {
-                    const int col = zb * 64 + hf * 32 + c;
-                    v = p.trans0 ? p.state0[((size_t)bh * p.DZ + col) * DX + srow]
-                                 : p.state0[((size_t)bh * DX + srow) * p.DZ + col];
+                for (int c = 0; c < 32; ++c) v[c] = 0.f;
+            } else if (p.trans0) {  // [DZ][DX]: lanes read consecutive rows
+#pragma unroll
+                for (int c = 0; c < 32; ++c) v[c] = __ldg(p.state0 + ((size_t)bh * p.DZ + col0 + c) * DX + srow);
+            } else {  // [DX][DZ]: this thread's 32 columns are contiguous
+                const float *src = p.state0 + ((size_t)bh * DX + srow) * p.DZ + col0;
+                if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 f = __ldg(reinterpret_cast<const float4 *>(src) + c4);
+                        v[4 * c4] = f.x;
+                        v[4 * c4 + 1] = f.y;
+                        v[4 * c4 + 2] = f.z;
+                        v[4 * c4 + 3] = f.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) v[c] = __ldg(src + c);
                 }
-                dst[c] = add ? fmaf(scale, v, dst[c]) : v;
             }
+#pragma unroll
+            for (int c = 0; c < 32; ++c) dst[c] = add ? fmaf(scale, v[c], dst[c]) : v[c];
         };
         float Sin[32];
 #pragma unroll
@@ -626,9 +644,12 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
                            make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]));
             }
             if (mtid == 0) p.alpha_ws[unit] = alpha_seg;
-            __threadfence();
             bar_sync(kBarMath, kMathThreads);
-            if (mtid == 0) st_release(p.flags + unit, 1u);
+            // the barrier orders every math thread's stores before thread 0's fence (cumulativity)
+            if (mtid == 0) {
+                __threadfence();
+                st_release(p.flags + unit, 1u);
+            }
             float accA = 1.f;
             int j = REV ? seg + 1 : seg - 1;
             while (true) {
@@ -675,9 +696,11 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
                                    fmaf(alpha_seg, Sin[4 * c4 + 2], S[4 * c4 + 2]),
                                    fmaf(alpha_seg, Sin[4 * c4 + 3], S[4 * c4 + 3])));
         }
-        __threadfence();
         bar_sync(kBarMath, kMathThreads);
-        if (mtid == 0) st_release(p.flags + unit, 2u);
+        if (mtid == 0) {
+            __threadfence();
+            st_release(p.flags + unit, 2u);
+        }
 
         // ---- phase 2
 #pragma unroll
@@ -783,7 +806,7 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) o[jj] = fmaf(wr, __uint_as_float(oi[jj]), __uint_as_float(oa[jj]));
                 if (prow >= 0) {
-                    const uint32_t row = sbase + C::OFF_ZSH + (uint32_t)(hf * TC * 128 + prow * 128);
+                    const uint32_t row = sbase + C::OFF_ZS + (uint32_t)(hf * TC * 128 + prow * 128);
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         st_shared_v4(row + (uint32_t)((c ^ (prow & 7)) << 4), o[c * 4], o[c * 4 + 1], o[c * 4 + 2],
@@ -804,6 +827,8 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
                     dotp[hf * TC + r] = dot;
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(10 + ((nc + i) & 1)));  // done with this visit's decays
             // State's bf16 parts for the next chunk (this chunk's O_inter has consumed them)
             write_s_smem();
             fence_async_smem();
@@ -812,8 +837,8 @@ __global__ void __launch_bounds__(kAllThreads, 1) la_tc_kernel(const __grid_cons
             if (mtid == 0) {
                 // rows past T are clipped by the store; the Zs buffers are rewritten only after
                 // the store has read them (tma_store_wait_read before the next chunk's Zs)
-                tma_store_3d(&maps.out, zb * 64, (int)t0, bh, sbase + C::OFF_ZSH);
-                tma_store_3d(&maps.out, zb * 64 + 32, (int)t0, bh, sbase + C::OFF_ZSH + TC * 128);
+                tma_store_3d(&maps.out, zb * 64, (int)t0, bh, sbase + C::OFF_ZS);
+                tma_store_3d(&maps.out, zb * 64 + 32, (int)t0, bh, sbase + C::OFF_ZS + TC * 128);
                 tma_store_commit();
             }
             if (has_w && hf == 0 && prow >= 0 && t0 + prow < p.T)

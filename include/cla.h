@@ -207,7 +207,10 @@ size_t cla_chunk_la_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_
  * (includes the first token's decay), gamma_s = a_{t0+Tc:t0+s}
  * (gamma_Tc = 1); all from in-chunk sums of log_decay, never from long
  * cumulative sums or ratios ("Long products without underflow").  A decay of
- * exactly 0 (log_decay = -inf) is a reset and gives products of 0.
+ * exactly 0 (log_decay = -inf) is a reset and gives products of 0.  Decays
+ * are gates in [0, 1], i.e. log_decay <= 0; larger values are computed as
+ * given, but a product over up to 32 consecutive tokens beyond 2^127
+ * overflows.
  *   q, k       [B, H, T, dim_k] bf16
  *   v          [B, H, T, dim_v] bf16
  *   log_decay  [B, H, T] fp32
