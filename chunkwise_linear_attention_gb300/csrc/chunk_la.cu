@@ -690,44 +690,106 @@ __global__ void __launch_bounds__(TC * 2) la_chunk_kernel(const LaArgs p) {
     }
 }
 
-// dlog_a_u = sum_{t >= u} (sum_zb qdq - sum_zb kdk)_t + sum_zb <dS_T, S_T> partials.
-// One block per (b, h); each thread owns a contiguous run of tokens.
-__global__ void __launch_bounds__(1024) la_dlog_finalize_kernel(const float *__restrict__ qdq,
-                                                               const float *__restrict__ kdk,
-                                                               const float *__restrict__ fsp, float *__restrict__ dlog,
-                                                               int nzb, int BH, long long T) {
-    __shared__ float s_part[32];
-    const int bh = blockIdx.x;
+// dlog_a_u = sum_{t >= u} (sum_zb qdq - sum_zb kdk)_t + sum_zb <dS_T, S_T> partials,
+// as a reverse scan over tiles of kFinTile tokens: la_dlog_tile_sums_kernel
+// reduces each tile, la_dlog_finalize_kernel scans a tile and adds the sum of
+// every later tile and the final-state term.  Both grids are tiles x B*H
+// blocks, block = bh * tiles + tile;
+// every sum runs in a fixed order, so results do not depend on scheduling.
+constexpr int kFinThreads = 256;
+constexpr int kFinPer = 8;  // consecutive tokens per thread in the scan
+constexpr int kFinTile = kFinThreads * kFinPer;
+
+__device__ __forceinline__ float dlog_delta(const float *__restrict__ qdq, const float *__restrict__ kdk, int nzb,
+                                            int BH, int bh, long long T, long long t) {
+    float d = 0.f;
+    for (int z = 0; z < nzb; ++z) {
+        d += qdq[((size_t)z * BH + bh) * T + t];
+        d -= kdk[((size_t)z * BH + bh) * T + t];
+    }
+    return d;
+}
+
+__global__ void __launch_bounds__(kFinThreads) la_dlog_tile_sums_kernel(const float *__restrict__ qdq,
+                                                                        const float *__restrict__ kdk,
+                                                                        float *__restrict__ tsum, int nzb, int BH,
+                                                                        long long T, int n_tiles) {
+    __shared__ float s_w[kFinThreads / 32];
+    const int tile = (int)(blockIdx.x % (unsigned)n_tiles), bh = (int)(blockIdx.x / (unsigned)n_tiles);
+    const int tid = threadIdx.x;
+    const long long t0 = (long long)tile * kFinTile;
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < kFinPer; ++k) {
+        const long long t = t0 + k * kFinThreads + tid;
+        if (t < T) acc += dlog_delta(qdq, kdk, nzb, BH, bh, T, t);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if ((tid & 31) == 0) s_w[tid >> 5] = acc;
+    __syncthreads();
+    if (tid == 0) {
+        float t = 0.f;
+        for (int w = 0; w < kFinThreads / 32; ++w) t += s_w[w];
+        tsum[(size_t)bh * n_tiles + tile] = t;
+    }
+}
+
+__global__ void __launch_bounds__(kFinThreads) la_dlog_finalize_kernel(
+    const float *__restrict__ qdq, const float *__restrict__ kdk, const float *__restrict__ fsp,
+    const float *__restrict__ tsum, float *__restrict__ dlog, int nzb, int BH, long long T, int n_tiles) {
+    // tile staged with one pad word per 8, so both the coalesced pass (consecutive
+    // threads, consecutive tokens) and the per-thread pass (8 consecutive tokens) are conflict-free
+    __shared__ float sh[kFinTile + kFinTile / kFinPer];
+    __shared__ float s_w[kFinThreads / 32];
+    __shared__ float s_off;
+    const int tile = (int)(blockIdx.x % (unsigned)n_tiles), bh = (int)(blockIdx.x / (unsigned)n_tiles);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long long per = (T + blockDim.x - 1) / blockDim.x;
-    const long long ta = tid * per, tb = min(T, ta + per);
-    auto delta = [&](long long t) {
-        float d = 0.f;
-        for (int z = 0; z < nzb; ++z) {
-            d += qdq[((size_t)z * BH + bh) * T + t];
-            d -= kdk[((size_t)z * BH + bh) * T + t];
+    const long long t0 = (long long)tile * kFinTile;
+#pragma unroll
+    for (int k = 0; k < kFinPer; ++k) {
+        const int e = k * kFinThreads + tid;
+        const long long t = t0 + e;
+        sh[e + e / kFinPer] = (t < T) ? dlog_delta(qdq, kdk, nzb, BH, bh, T, t) : 0.f;
+    }
+    if (warp == 0) {  // offset of this tile: every later tile plus the final-state term
+        float o = 0.f;
+        for (int j = tile + 1 + lane; j < n_tiles; j += 32) o += tsum[(size_t)bh * n_tiles + j];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) o += __shfl_xor_sync(0xffffffffu, o, off);
+        if (lane == 0) {
+            float tail = 0.f;
+            for (int z = 0; z < nzb; ++z) tail += fsp[(size_t)z * BH + bh];
+            s_off = o + tail;
         }
-        return d;
-    };
-    float local = 0.f;
-    for (long long t = ta; t < tb; ++t) local += delta(t);
-    // exclusive suffix sum of `local` over threads (threads after this one)
-    float incl = local;
+    }
+    __syncthreads();
+    float v[kFinPer];
+    float run = 0.f;
+#pragma unroll
+    for (int j = kFinPer - 1; j >= 0; --j) {
+        run += sh[tid * (kFinPer + 1) + j];
+        v[j] = run;
+    }
+    // exclusive suffix sum of the thread totals (threads after this one)
+    float incl = run;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const float o = __shfl_down_sync(0xffffffffu, incl, off);
         if (lane + off < 32) incl += o;
     }
-    if (lane == 0) s_part[warp] = incl;  // warp total
+    if (lane == 0) s_w[warp] = incl;
     __syncthreads();
-    float after = 0.f;
-    for (int w = warp + 1; w < (int)(blockDim.x >> 5); ++w) after += s_part[w];
-    float tail = 0.f;
-    for (int z = 0; z < nzb; ++z) tail += fsp[(size_t)z * BH + bh];
-    float run = after + (incl - local) + tail;
-    for (long long t = tb - 1; t >= ta; --t) {
-        run += delta(t);
-        dlog[(size_t)bh * T + t] = run;
+    float after = s_off + (incl - run);
+    for (int w = warp + 1; w < kFinThreads / 32; ++w) after += s_w[w];
+#pragma unroll
+    for (int j = 0; j < kFinPer; ++j) sh[tid * (kFinPer + 1) + j] = v[j] + after;
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kFinPer; ++k) {
+        const int e = k * kFinThreads + tid;
+        const long long t = t0 + e;
+        if (t < T) dlog[(size_t)bh * T + t] = sh[e + e / kFinPer];
     }
 }
 
@@ -735,7 +797,8 @@ __global__ void __launch_bounds__(1024) la_dlog_finalize_kernel(const float *__r
 struct LaPlan {
     int TC, DXmax, n_chunks, seg_chunks, n_seg, nzb_max;
     size_t units;
-    size_t off_flags, off_alpha, off_agg, off_incl, off_qdq, off_kdk, off_fsp, total;
+    size_t off_flags, off_alpha, off_agg, off_incl, off_qdq, off_kdk, off_fsp, off_tsum, total;
+    int fin_tiles;
 };
 
 LaPlan la_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chunk) {
@@ -764,7 +827,10 @@ LaPlan la_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chun
     p.off_qdq = align_up(p.off_incl + p.units * state_floats * 4, 256);
     p.off_kdk = align_up(p.off_qdq + (size_t)p.nzb_max * BH * T * 4, 256);
     p.off_fsp = align_up(p.off_kdk + (size_t)p.nzb_max * BH * T * 4, 256);
-    p.total = align_up(p.off_fsp + (size_t)p.nzb_max * BH * 4, 256);
+    p.off_tsum = align_up(p.off_fsp + (size_t)p.nzb_max * BH * 4, 256);
+    p.fin_tiles = (int)((T + kFinTile - 1) / kFinTile);
+    if (p.fin_tiles < 1) p.fin_tiles = 1;
+    p.total = align_up(p.off_tsum + (size_t)p.fin_tiles * BH * 4, 256);
     return p;
 }
 
@@ -981,8 +1047,14 @@ extern "C" int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint
 
     // decay gradient: suffix sums of q.dq - k.dk plus <dS_T, S_T>
     if (dlog_decay) {
-        la_dlog_finalize_kernel<<<(unsigned int)BH, 1024, 0, s>>>(qdq, kdk, fsp, dlog_decay, (int)(dim_k / 64),
-                                                                  (int)BH, T);
+        float *tsum = reinterpret_cast<float *>(w + pl.off_tsum);
+        const unsigned int fgrid = (unsigned int)((size_t)pl.fin_tiles * BH);
+        la_dlog_tile_sums_kernel<<<fgrid, kFinThreads, 0, s>>>(qdq, kdk, tsum, (int)(dim_k / 64), (int)BH, T,
+                                                               pl.fin_tiles);
+        st = check_launch("la_dlog_tile_sums_kernel");
+        if (st) return st;
+        la_dlog_finalize_kernel<<<fgrid, kFinThreads, 0, s>>>(qdq, kdk, fsp, tsum, dlog_decay, (int)(dim_k / 64),
+                                                              (int)BH, T, pl.fin_tiles);
         st = check_launch("la_dlog_finalize_kernel");
     }
     return st;
