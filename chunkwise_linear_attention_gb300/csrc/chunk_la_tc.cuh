@@ -703,10 +703,29 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
         }
 
         // ---- phase 2
+        // the 32-token piece holding this warp's rows; other pieces are either fully masked
+        // (the same ones for every chunk: their bf16 parts are zeroed here, once) or lie
+        // entirely on the unmasked side of every row (off-diagonal)
+        const int rpiece = ((TC == 128) ? q * 32 : q * 16) >> 5;
+        constexpr int PIECES = TC / 64;  // pieces of 32 tokens per warp
+        auto piece_masked = [&](int piece) { return REV ? (piece < rpiece) : (piece > rpiece); };
+        {
+            const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int pc = 0; pc < PIECES; ++pc) {
+                const int piece = hf * PIECES + pc;
+                if (piece_masked(piece)) {
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) tmem_st8(tmem + tlane + C::C_PB + (uint32_t)(piece * 32 + 8 * c8), zero);
+                }
+            }
+            tmem_st_wait();
+        }
 #pragma unroll
         for (int c = 0; c < 32; ++c) S[c] = Sin[c];
         write_s_smem();
         fence_async_smem();
+        tc_fence_before();
         bar_arrive(kBarDone, kAllThreads);  // State's bf16 parts for chunk 0
         for (int i = 0; i < nc; ++i) {
             const int b = i & 1;
@@ -729,10 +748,6 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                 const int r = prow < 0 ? 0 : prow;
                 const float clr = cl[r];
                 const int zrr = zr[r];
-                // the 32-token piece holding this warp's rows; other pieces are either fully
-                // masked or lie entirely on the unmasked side of every row (off-diagonal)
-                const int rpiece = ((TC == 128) ? q * 32 : q * 16) >> 5;
-                constexpr int PIECES = TC / 64;  // pieces of 32 tokens per warp
                 auto store_parts = [&](int s0, float (&x)[32]) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -751,32 +766,46 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
 #pragma unroll 1
                 for (int pc = 0; pc < PIECES; ++pc) {
                     const int piece = hf * PIECES + pc;
+                    if (piece_masked(piece)) continue;  // zeroed before phase 2 (warp-uniform)
                     const int s0 = piece * 32;
                     float x[32];
-                    if (REV ? (piece < rpiece) : (piece > rpiece)) {  // fully masked (warp-uniform)
+                    uint32_t pr[32];
+                    tmem_ld32(tmem + tlane + C::C_P + (uint32_t)s0, pr);
+                    // the piece's per-token values, as 16-byte broadcast loads (same address in every lane)
+                    float cs[32];
+                    int zs[32];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) x[e] = 0.f;
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 g = *reinterpret_cast<const float4 *>((piece != rpiece ? gcol : cl) + s0 + 4 * c4);
+                        cs[4 * c4] = g.x;
+                        cs[4 * c4 + 1] = g.y;
+                        cs[4 * c4 + 2] = g.z;
+                        cs[4 * c4 + 3] = g.w;
+                        if (REV) {
+                            const int4 zv = *reinterpret_cast<const int4 *>(zr + s0 + 4 * c4);
+                            zs[4 * c4] = zv.x;
+                            zs[4 * c4 + 1] = zv.y;
+                            zs[4 * c4 + 2] = zv.z;
+                            zs[4 * c4 + 3] = zv.w;
+                        }
+                    }
+                    tmem_ld_wait();
+                    if (piece != rpiece) {
+                        // off-diagonal: row factor times column factor
+                        const float f = REV ? ex2(cl[s0] - clr) : ex2(clr - cl[s0 + 31]);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int s = s0 + e;
+                            const bool keep = REV ? (zs[e] <= r) : (zrr <= s);
+                            x[e] = keep ? __uint_as_float(pr[e]) * (f * cs[e]) : 0.f;
+                        }
                     } else {
-                        uint32_t pr[32];
-                        tmem_ld32(tmem + tlane + C::C_P + (uint32_t)s0, pr);
-                        tmem_ld_wait();
-                        if (piece != rpiece) {
-                            // off-diagonal: row factor times column factor
-                            const float f = REV ? ex2(cl[s0] - clr) : ex2(clr - cl[s0 + 31]);
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) {
-                                const int s = s0 + e;
-                                const bool keep = REV ? (zr[s] <= r) : (zrr <= s);
-                                x[e] = keep ? __uint_as_float(pr[e]) * (f * gcol[s]) : 0.f;
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) {
-                                const int s = s0 + e;
-                                const bool keep = REV ? (s >= r && zr[s] <= r) : (s <= r && zrr <= s);
-                                const float m = ex2(REV ? cl[s] - clr : clr - cl[s]);
-                                x[e] = keep ? __uint_as_float(pr[e]) * m : 0.f;
-                            }
+                        for (int e = 0; e < 32; ++e) {
+                            const int s = s0 + e;
+                            const bool keep = REV ? (s >= r && zs[e] <= r) : (s <= r && zrr <= s);
+                            const float m = ex2(REV ? cs[e] - clr : clr - cs[e]);
+                            x[e] = keep ? __uint_as_float(pr[e]) * m : 0.f;
                         }
                     }
                     store_parts(s0, x);
