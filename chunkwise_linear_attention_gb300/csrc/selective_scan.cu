@@ -51,9 +51,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 // (coefficients (ln 2)^j / j!; the omitted terms are below 5.2e-9 relative),
 // and scale by 2^k by building the float with exponent field k + 127.
 // Results below 2^-126 are returned as 0 (a decay that small is 0 to fp32).
+// k is rounded to nearest-even by adding and removing 1.5 * 2^23 (exact for
+// |x| <= 2^22, which the clamp ensures), and the low bits of x + 1.5 * 2^23
+// are k itself, so the exponent field is one shift-add of them.
 __device__ __forceinline__ float exp2_fma(float x) {
-    x = fminf(x, 127.f);
-    const float k = rintf(x);
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    x = fminf(fmaxf(x, -127.f), 127.f);
+    const float km = x + kMagic;
+    const float k = km - kMagic;
     const float f = x - k;
     float p = 1.5252733804059838e-05f;
     p = fmaf(p, f, 1.5403530393381606e-04f);
@@ -63,9 +68,9 @@ __device__ __forceinline__ float exp2_fma(float x) {
     p = fmaf(p, f, 2.402265069591007e-01f);
     p = fmaf(p, f, 6.931471805599453e-01f);
     p = fmaf(p, f, 1.0f);
-    const int e = (int)k + 127;
-    const float scale = __int_as_float(max(e, 0) << 23);
-    return e > 0 ? p * scale : 0.f;
+    // k + 127 in [0, 254]; 0 gives the float 0 (results below 2^-126 are 0)
+    const int e = (__float_as_int(km) - __float_as_int(kMagic)) + 127;
+    return p * __int_as_float(e << 23);
 }
 
 struct SelGeom {
@@ -89,7 +94,7 @@ __device__ __forceinline__ size_t sel_unit(const SelGeom &g, int chunk, int b, i
 
 // ------------------------------------------------------------------ forward
 struct SelFwdSmem {
-    float x[kTc][kCh];
+    bf16 x[kTc][kCh];
     float d[kTc][kCh];
     float B[kTc][kN];
     float C[kTc][kN];
@@ -101,7 +106,7 @@ sel_fwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
                float *__restrict__ y, float *__restrict__ hT, float *__restrict__ ckpt, SelGeom g, SelWs ws) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SelFwdSmem &sm = *reinterpret_cast<SelFwdSmem *>(smem_raw);
-    float(&s_x)[kTc][kCh] = sm.x;
+    bf16(&s_x)[kTc][kCh] = sm.x;
     float(&s_d)[kTc][kCh] = sm.d;
     float(&s_B)[kTc][kN] = sm.B;
     float(&s_C)[kTc][kN] = sm.C;
@@ -126,7 +131,7 @@ sel_fwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
     for (int r = 0; r < kTc; ++r) {
         const bool ok = cok && r < L;
         const size_t idx = ((size_t)bi * g.T + t0 + r) * g.D + c;
-        s_x[r][tid] = ok ? __bfloat162float(x[idx]) : 0.f;
+        s_x[r][tid] = ok ? x[idx] : __float2bfloat16(0.f);
         s_d[r][tid] = ok ? __ldcs(delta + idx) : 0.f;
     }
     for (int i = tid; i < kTc * kN; i += kCh) {
@@ -149,7 +154,7 @@ sel_fwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
     float sumd = 0.f;
     for (int r = 0; r < L; ++r) {
         const float d = s_d[r][tid];
-        const float dx = d * s_x[r][tid];
+        const float dx = d * __bfloat162float(s_x[r][tid]);
 #pragma unroll
         for (int n = 0; n < kN; ++n) Bagg[n] = fmaf(exp2_fma(d * A2[n]), Bagg[n], dx * s_B[r][n]);
         sumd += d;
@@ -222,7 +227,7 @@ sel_fwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
     for (int n = 0; n < kN; ++n) h[n] = hin[n];
     for (int r = 0; r < L; ++r) {
         const float d = s_d[r][tid];
-        const float dx = d * s_x[r][tid];
+        const float dx = d * __bfloat162float(s_x[r][tid]);
         float acc = 0.f;
 #pragma unroll
         for (int n = 0; n < kN; ++n) {
@@ -429,7 +434,7 @@ sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
     for (int n = 0; n < kNh; ++n) { anext[n] = aend[n]; dA_acc[n] = 0.f; }
     const int nsub = (L + kSubT - 1) / kSubT;
     for (int k = nsub - 1; k >= 0; --k) {
-        float hs[kSubT][kNh], hstart[kNh];
+        float hs[kSubT][kNh], as[kSubT][kNh], hstart[kNh];
 #pragma unroll
         for (int n = 0; n < kNh; ++n) {
             hstart[n] = sm.bnd[k][tid][n];
@@ -443,7 +448,8 @@ sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
             const float dxv = d * (ok ? sm.x[r][cl] : 0.f);
 #pragma unroll
             for (int n = 0; n < kNh; ++n) {
-                if (ok) h[n] = fmaf(exp2_fma(d * A2[n]), h[n], dxv * sm.Bs[r][n0 + n]);
+                as[i][n] = exp2_fma(d * A2[n]);
+                if (ok) h[n] = fmaf(as[i][n], h[n], dxv * sm.Bs[r][n0 + n]);
                 hs[i][n] = h[n];
             }
         }
@@ -458,7 +464,7 @@ sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
                 for (int n = 0; n < kNh; ++n) {
                     const float Bn = sm.Bs[r][n0 + n], Cn = sm.Cs[r][n0 + n];
                     hb[n] = fmaf(anext[n], hb[n], Cn * gy);
-                    const float a = exp2_fma(d * A2[n]);
+                    const float a = as[i][n];
                     const float hp = (i > 0) ? hs[i - 1][n] : hstart[n];
                     const float ga = hb[n] * hp * a;  // dL/da_t * a_t
                     sx = fmaf(hb[n], Bn, sx);
