@@ -73,6 +73,30 @@ __device__ __forceinline__ float exp2_fma(float x) {
     return p * __int_as_float(e << 23);
 }
 
+// The same 2^x on two arguments at once: the paired FP32 instructions
+// (add / mul / fma on float2) round each lane exactly as the scalar ones, so
+// the results equal exp2_fma's; the instruction count is about halved.
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+    constexpr float kMagic = 12582912.0f;
+    x.x = fminf(fmaxf(x.x, -127.f), 127.f);
+    x.y = fminf(fmaxf(x.y, -127.f), 127.f);
+    const float2 km = __fadd2_rn(x, make_float2(kMagic, kMagic));
+    const float2 k = __fadd2_rn(km, make_float2(-kMagic, -kMagic));
+    const float2 f = __ffma2_rn(k, make_float2(-1.f, -1.f), x);  // x - k, exact
+    float2 p = make_float2(1.5252733804059838e-05f, 1.5252733804059838e-05f);
+    p = __ffma2_rn(p, f, make_float2(1.5403530393381606e-04f, 1.5403530393381606e-04f));
+    p = __ffma2_rn(p, f, make_float2(1.3333558146428441e-03f, 1.3333558146428441e-03f));
+    p = __ffma2_rn(p, f, make_float2(9.618129107628477e-03f, 9.618129107628477e-03f));
+    p = __ffma2_rn(p, f, make_float2(5.5504108664821576e-02f, 5.5504108664821576e-02f));
+    p = __ffma2_rn(p, f, make_float2(2.402265069591007e-01f, 2.402265069591007e-01f));
+    p = __ffma2_rn(p, f, make_float2(6.931471805599453e-01f, 6.931471805599453e-01f));
+    p = __ffma2_rn(p, f, make_float2(1.0f, 1.0f));
+    const int ex = (__float_as_int(km.x) - __float_as_int(kMagic)) + 127;
+    const int ey = (__float_as_int(km.y) - __float_as_int(kMagic)) + 127;
+    return __fmul2_rn(p, make_float2(__int_as_float(ex << 23), __int_as_float(ey << 23)));
+}
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
 struct SelGeom {
     int B, D, n_chunks, n_cblk;
     long long T;
@@ -143,21 +167,34 @@ sel_fwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
     }
     __syncthreads();
 
+    // state entries in pairs (n = 2j, 2j + 1) for the paired FP32 instructions
+    constexpr int kJ = kN / 2;
     float A2[kN];
 #pragma unroll
     for (int n = 0; n < kN; ++n) A2[n] = cok ? A[(size_t)c * kN + n] * kLog2e : 0.f;
+    float2 A2p[kJ];
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) A2p[j] = make_float2(A2[2 * j], A2[2 * j + 1]);
 
     // phase 1: the chunk as one pair per n: (exp(A sum delta), Bagg)
-    float Bagg[kN];
+    float2 Baggp[kJ];
 #pragma unroll
-    for (int n = 0; n < kN; ++n) Bagg[n] = 0.f;
+    for (int j = 0; j < kJ; ++j) Baggp[j] = f2(0.f);
     float sumd = 0.f;
     for (int r = 0; r < L; ++r) {
         const float d = s_d[r][tid];
         const float dx = d * __bfloat162float(s_x[r][tid]);
+        const float2 *Br = reinterpret_cast<const float2 *>(s_B[r]);
 #pragma unroll
-        for (int n = 0; n < kN; ++n) Bagg[n] = fmaf(exp2_fma(d * A2[n]), Bagg[n], dx * s_B[r][n]);
+        for (int j = 0; j < kJ; ++j)
+            Baggp[j] = __ffma2_rn(exp2_fma2(__fmul2_rn(f2(d), A2p[j])), Baggp[j], __fmul2_rn(f2(dx), Br[j]));
         sumd += d;
+    }
+    float Bagg[kN];
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+        Bagg[2 * j] = Baggp[j].x;
+        Bagg[2 * j + 1] = Baggp[j].y;
     }
 
     float hin[kN];
@@ -222,23 +259,28 @@ sel_fwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
     }
 
     // phase 2: re-run from the true incoming state; write y once
-    float h[kN];
+    float2 hp[kJ];
 #pragma unroll
-    for (int n = 0; n < kN; ++n) h[n] = hin[n];
+    for (int j = 0; j < kJ; ++j) hp[j] = make_float2(hin[2 * j], hin[2 * j + 1]);
     for (int r = 0; r < L; ++r) {
         const float d = s_d[r][tid];
         const float dx = d * __bfloat162float(s_x[r][tid]);
-        float acc = 0.f;
+        const float2 *Br = reinterpret_cast<const float2 *>(s_B[r]);
+        const float2 *Cr = reinterpret_cast<const float2 *>(s_C[r]);
+        float2 acc = f2(0.f);  // even and odd entries summed separately, then added
 #pragma unroll
-        for (int n = 0; n < kN; ++n) {
-            h[n] = fmaf(exp2_fma(d * A2[n]), h[n], dx * s_B[r][n]);
-            acc = fmaf(s_C[r][n], h[n], acc);
+        for (int j = 0; j < kJ; ++j) {
+            hp[j] = __ffma2_rn(exp2_fma2(__fmul2_rn(f2(d), A2p[j])), hp[j], __fmul2_rn(f2(dx), Br[j]));
+            acc = __ffma2_rn(Cr[j], hp[j], acc);
         }
-        if (cok) __stcs(y + ((size_t)bi * g.T + t0 + r) * g.D + c, acc);
+        if (cok) __stcs(y + ((size_t)bi * g.T + t0 + r) * g.D + c, acc.x + acc.y);
     }
     if (hT != nullptr && cok && chunk == g.n_chunks - 1) {
 #pragma unroll
-        for (int n = 0; n < kN; ++n) hT[((size_t)bi * g.D + c) * kN + n] = h[n];
+        for (int j = 0; j < kJ; ++j) {
+            hT[((size_t)bi * g.D + c) * kN + 2 * j] = hp[j].x;
+            hT[((size_t)bi * g.D + c) * kN + 2 * j + 1] = hp[j].y;
+        }
     }
 }
 
@@ -334,31 +376,52 @@ sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
         Ar[n] = cok ? A[(size_t)c * kN + n0 + n] : 0.f;
         A2[n] = Ar[n] * kLog2e;
     }
+    // state entries in pairs (n0 + 2j, n0 + 2j + 1) for the paired FP32 instructions
+    constexpr int kJh = kNh / 2;
+    float2 A2p[kJh], Arp[kJh];
+#pragma unroll
+    for (int j = 0; j < kJh; ++j) {
+        A2p[j] = make_float2(A2[2 * j], A2[2 * j + 1]);
+        Arp[j] = make_float2(Ar[2 * j], Ar[2 * j + 1]);
+    }
     // pass A: states (every 8th kept) and the adjoint pair of the chunk
     float h[kNh], P[kNh], Bg[kNh];
     {
         const float *ck = ckpt + (((size_t)bi * g.n_chunks + chunk) * g.D + (cok ? c : 0)) * kN + n0;
+        float2 hq[kJh], Pq[kJh], Bq[kJh];
 #pragma unroll
-        for (int n = 0; n < kNh; ++n) {
-            h[n] = cok ? ck[n] : 0.f;
-            P[n] = 1.f;
-            Bg[n] = 0.f;
+        for (int j = 0; j < kJh; ++j) {
+            hq[j] = cok ? make_float2(ck[2 * j], ck[2 * j + 1]) : f2(0.f);
+            Pq[j] = f2(1.f);
+            Bq[j] = f2(0.f);
         }
-    }
-    for (int r = 0; r < L; ++r) {
-        if ((r % kSubT) == 0) {
+        for (int r = 0; r < L; ++r) {
+            if ((r % kSubT) == 0) {
+                float2 *bd = reinterpret_cast<float2 *>(sm.bnd[r / kSubT][tid]);
 #pragma unroll
-            for (int n = 0; n < kNh; ++n) sm.bnd[r / kSubT][tid][n] = h[n];
+                for (int j = 0; j < kJh; ++j) bd[j] = hq[j];
+            }
+            const float d = sm.d[r][cl];
+            const float dxv = d * sm.x[r][cl];
+            const float gy = sm.dy[r][cl];
+            const float2 *Cr = reinterpret_cast<const float2 *>(&sm.Cs[r][n0]);
+            const float2 *Br = reinterpret_cast<const float2 *>(&sm.Bs[r][n0]);
+#pragma unroll
+            for (int j = 0; j < kJh; ++j) {
+                const float2 a = exp2_fma2(__fmul2_rn(f2(d), A2p[j]));
+                if (r > 0) Pq[j] = __fmul2_rn(Pq[j], a);
+                Bq[j] = __ffma2_rn(Pq[j], __fmul2_rn(Cr[j], f2(gy)), Bq[j]);
+                hq[j] = __ffma2_rn(a, hq[j], __fmul2_rn(f2(dxv), Br[j]));
+            }
         }
-        const float d = sm.d[r][cl];
-        const float dxv = d * sm.x[r][cl];
-        const float gy = sm.dy[r][cl];
 #pragma unroll
-        for (int n = 0; n < kNh; ++n) {
-            const float a = exp2_fma(d * A2[n]);
-            if (r > 0) P[n] *= a;
-            Bg[n] = fmaf(P[n], sm.Cs[r][n0 + n] * gy, Bg[n]);
-            h[n] = fmaf(a, h[n], dxv * sm.Bs[r][n0 + n]);
+        for (int j = 0; j < kJh; ++j) {
+            h[2 * j] = hq[j].x;
+            h[2 * j + 1] = hq[j].y;
+            P[2 * j] = Pq[j].x;
+            P[2 * j + 1] = Pq[j].y;
+            Bg[2 * j] = Bq[j].x;
+            Bg[2 * j + 1] = Bq[j].y;
         }
     }
     float aend[kNh], Ag[kNh];
@@ -429,16 +492,23 @@ sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
     }
 
     // pass B: sub-chunks from last to first
-    float anext[kNh], dA_acc[kNh];
+    float2 anext[kJh], dA_acc[kJh], hbq[kJh];
 #pragma unroll
-    for (int n = 0; n < kNh; ++n) { anext[n] = aend[n]; dA_acc[n] = 0.f; }
+    for (int j = 0; j < kJh; ++j) {
+        anext[j] = make_float2(aend[2 * j], aend[2 * j + 1]);
+        dA_acc[j] = f2(0.f);
+        hbq[j] = make_float2(hb[2 * j], hb[2 * j + 1]);
+    }
     const int nsub = (L + kSubT - 1) / kSubT;
     for (int k = nsub - 1; k >= 0; --k) {
-        float hs[kSubT][kNh], as[kSubT][kNh], hstart[kNh];
+        float2 hs[kSubT][kJh], as[kSubT][kJh], hstart[kJh], hq[kJh];
+        {
+            const float2 *bd = reinterpret_cast<const float2 *>(sm.bnd[k][tid]);
 #pragma unroll
-        for (int n = 0; n < kNh; ++n) {
-            hstart[n] = sm.bnd[k][tid][n];
-            h[n] = hstart[n];
+            for (int j = 0; j < kJh; ++j) {
+                hstart[j] = bd[j];
+                hq[j] = hstart[j];
+            }
         }
 #pragma unroll
         for (int i = 0; i < kSubT; ++i) {
@@ -446,11 +516,12 @@ sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
             const bool ok = r < L;
             const float d = ok ? sm.d[r][cl] : 0.f;
             const float dxv = d * (ok ? sm.x[r][cl] : 0.f);
+            const float2 *Br = reinterpret_cast<const float2 *>(&sm.Bs[ok ? r : 0][n0]);
 #pragma unroll
-            for (int n = 0; n < kNh; ++n) {
-                as[i][n] = exp2_fma(d * A2[n]);
-                if (ok) h[n] = fmaf(as[i][n], h[n], dxv * sm.Bs[r][n0 + n]);
-                hs[i][n] = h[n];
+            for (int j = 0; j < kJh; ++j) {
+                as[i][j] = exp2_fma2(__fmul2_rn(f2(d), A2p[j]));
+                if (ok) hq[j] = __ffma2_rn(as[i][j], hq[j], __fmul2_rn(f2(dxv), Br[j]));
+                hs[i][j] = hq[j];
             }
         }
 #pragma unroll
@@ -459,21 +530,28 @@ sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
             float vB[kNh], vC[kNh];
             if (r < L) {
                 const float d = sm.d[r][cl], xv = sm.x[r][cl], gy = sm.dy[r][cl];
-                float sx = 0.f, sd = 0.f;
+                const float2 *Br = reinterpret_cast<const float2 *>(&sm.Bs[r][n0]);
+                const float2 *Cr = reinterpret_cast<const float2 *>(&sm.Cs[r][n0]);
+                float2 sx2 = f2(0.f), sd2 = f2(0.f);  // even and odd entries, added at the end
 #pragma unroll
-                for (int n = 0; n < kNh; ++n) {
-                    const float Bn = sm.Bs[r][n0 + n], Cn = sm.Cs[r][n0 + n];
-                    hb[n] = fmaf(anext[n], hb[n], Cn * gy);
-                    const float a = as[i][n];
-                    const float hp = (i > 0) ? hs[i - 1][n] : hstart[n];
-                    const float ga = hb[n] * hp * a;  // dL/da_t * a_t
-                    sx = fmaf(hb[n], Bn, sx);
-                    sd = fmaf(ga, Ar[n], fmaf(hb[n], Bn * xv, sd));
-                    dA_acc[n] = fmaf(ga, d, dA_acc[n]);
-                    vB[n] = hb[n] * d * xv;
-                    vC[n] = gy * hs[i][n];
-                    anext[n] = a;
+                for (int j = 0; j < kJh; ++j) {
+                    const float2 Bn = Br[j], Cn = Cr[j];
+                    hbq[j] = __ffma2_rn(anext[j], hbq[j], __fmul2_rn(Cn, f2(gy)));
+                    const float2 a = as[i][j];
+                    const float2 hp = (i > 0) ? hs[i - 1][j] : hstart[j];
+                    const float2 ga = __fmul2_rn(__fmul2_rn(hbq[j], hp), a);  // dL/da_t * a_t
+                    sx2 = __ffma2_rn(hbq[j], Bn, sx2);
+                    sd2 = __ffma2_rn(ga, Arp[j], __ffma2_rn(hbq[j], __fmul2_rn(Bn, f2(xv)), sd2));
+                    dA_acc[j] = __ffma2_rn(ga, f2(d), dA_acc[j]);
+                    const float2 vb = __fmul2_rn(__fmul2_rn(hbq[j], f2(d)), f2(xv));
+                    const float2 vc = __fmul2_rn(f2(gy), hs[i][j]);
+                    vB[2 * j] = vb.x;
+                    vB[2 * j + 1] = vb.y;
+                    vC[2 * j] = vc.x;
+                    vC[2 * j + 1] = vc.y;
+                    anext[j] = a;
                 }
+                float sx = sx2.x + sx2.y, sd = sd2.x + sd2.y;
                 sx += __shfl_xor_sync(0xffffffffu, sx, 1);
                 sd += __shfl_xor_sync(0xffffffffu, sd, 1);
                 if (ng == 0 && cok) {
@@ -483,7 +561,11 @@ sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
                 }
                 if (r == 0 && chunk == 0 && dh0 != nullptr && cok) {
 #pragma unroll
-                    for (int n = 0; n < kNh; ++n) dh0[((size_t)bi * g.D + c) * kN + n0 + n] = anext[n] * hb[n];
+                    for (int j = 0; j < kJh; ++j) {
+                        const float2 v = __fmul2_rn(anext[j], hbq[j]);
+                        dh0[((size_t)bi * g.D + c) * kN + n0 + 2 * j] = v.x;
+                        dh0[((size_t)bi * g.D + c) * kN + n0 + 2 * j + 1] = v.y;
+                    }
                 }
             } else {
 #pragma unroll
@@ -521,7 +603,10 @@ sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
     if (ws.partA != nullptr && cok) {
         float *pa = ws.partA + (((size_t)bi * g.n_chunks + chunk) * g.D + c) * kN + n0;
 #pragma unroll
-        for (int n = 0; n < kNh; ++n) pa[n] = dA_acc[n];
+        for (int j = 0; j < kJh; ++j) {
+            pa[2 * j] = dA_acc[j].x;
+            pa[2 * j + 1] = dA_acc[j].y;
+        }
     }
 }
 
