@@ -143,7 +143,8 @@ def _sync_all(torch, dist_on):
         import torch.distributed as dist
 
         dist.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def _max_over_ranks(torch, x, dist_on):
@@ -154,6 +155,12 @@ def _max_over_ranks(torch, x, dist_on):
     t = torch.tensor([x], dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_throughput(world, bytes_per_step, slowest_step_ms):
+    """Whole-job GB/s of `world` independent replicas, each moving
+    `bytes_per_step` per step, timed by the slowest rank (weak scaling)."""
+    return world * bytes_per_step / (slowest_step_ms / 1e3) / 1e9
 
 
 # ------------------------------------------------------------------ headline: diagonal scan
@@ -446,7 +453,7 @@ def main():
     fwd_ms = _max_over_ranks(torch, head["fwd_ms"], dist_on)
     e2e_ms = _max_over_ranks(torch, head["e2e_ms"], dist_on)
     bytes_step = head["bytes_fwd"] + head["bytes_bwd"]
-    value = world * bytes_step / (step_ms / 1e3) / 1e9
+    value = replica_throughput(world, bytes_step, step_ms)
 
     extra = {}
     if not args.headline_only and rank == 0:
@@ -503,7 +510,7 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": round(world * bytes_step / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(replica_throughput(world, bytes_step, e2e_ms), 1), "unit": "GB/s",
                 "h2d_bytes_per_step": head["h2d_bytes"], "d2h_bytes_per_step": head["d2h_bytes"]},
         "gpu_launches": head["launches"],
         "clocks": clocks,
