@@ -557,8 +557,13 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
             tmem_ld32(tmem + tlane + C::C_DS + 64 + hf * 32, rl);
             tmem_ld_wait();
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-                S[jj] = fmaf(alpha, S[jj], __uint_as_float(rh[jj]) + __uint_as_float(rl[jj]));
+            for (int jj = 0; jj < 16; ++jj) {
+                const float2 d = __fadd2_rn(make_float2(__uint_as_float(rh[2 * jj]), __uint_as_float(rh[2 * jj + 1])),
+                                            make_float2(__uint_as_float(rl[2 * jj]), __uint_as_float(rl[2 * jj + 1])));
+                const float2 v = __ffma2_rn(make_float2(alpha, alpha), make_float2(S[2 * jj], S[2 * jj + 1]), d);
+                S[2 * jj] = v.x;
+                S[2 * jj + 1] = v.y;
+            }
         };
         auto write_s_smem = [&]() {
             if (srow < 0) return;
@@ -748,16 +753,16 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                 const int r = prow < 0 ? 0 : prow;
                 const float clr = cl[r];
                 const int zrr = zr[r];
-                auto store_parts = [&](int s0, float (&x)[32]) {
+                auto store_parts = [&](int s0, float2 (&x)[16]) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint32_t hi[8], lo[8];
 #pragma unroll
                         for (int jj = 0; jj < 8; ++jj) {
-                            const float x0 = x[16 * h + 2 * jj], x1 = x[16 * h + 2 * jj + 1];
-                            hi[jj] = pack_bf16(x0, x1);
-                            const float2 fh = unpack_bf16(hi[jj]);
-                            lo[jj] = pack_bf16(x0 - fh.x, x1 - fh.y);
+                            const float2 v = x[8 * h + jj];
+                            hi[jj] = pack_bf16(v.x, v.y);
+                            const float2 r2 = __ffma2_rn(unpack_bf16(hi[jj]), make_float2(-1.f, -1.f), v);  // v - hi, exact
+                            lo[jj] = pack_bf16(r2.x, r2.y);
                         }
                         tmem_st8(tmem + tlane + C::C_PB + (uint32_t)(s0 + 8 * h), hi);
                         tmem_st8(tmem + tlane + C::C_PB + (uint32_t)(s0 + 16 + 8 * h), lo);
@@ -768,7 +773,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                     const int piece = hf * PIECES + pc;
                     if (piece_masked(piece)) continue;  // zeroed before phase 2 (warp-uniform)
                     const int s0 = piece * 32;
-                    float x[32];
+                    float2 x[16];
                     uint32_t pr[32];
                     tmem_ld32(tmem + tlane + C::C_P + (uint32_t)s0, pr);
                     // the piece's per-token values, as 16-byte broadcast loads (same address in every lane)
@@ -790,22 +795,36 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                         }
                     }
                     tmem_ld_wait();
+                    auto pv = [&](int j) { return make_float2(__uint_as_float(pr[2 * j]), __uint_as_float(pr[2 * j + 1])); };
                     if (piece != rpiece) {
-                        // off-diagonal: row factor times column factor
+                        // off-diagonal: row factor times column factor; without a reset between
+                        // the piece and the row (zr is nondecreasing) every product is kept
                         const float f = REV ? ex2(cl[s0] - clr) : ex2(clr - cl[s0 + 31]);
+                        const float2 ff = make_float2(f, f);
+                        const bool all_keep = REV ? (zs[31] <= r) : (zrr <= s0);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int s = s0 + e;
-                            const bool keep = REV ? (zs[e] <= r) : (zrr <= s);
-                            x[e] = keep ? __uint_as_float(pr[e]) * (f * cs[e]) : 0.f;
+                        for (int j = 0; j < 16; ++j) {
+                            float2 v = __fmul2_rn(pv(j), __fmul2_rn(ff, make_float2(cs[2 * j], cs[2 * j + 1])));
+                            if (!all_keep) {
+                                const int sa = s0 + 2 * j;
+                                if (!(REV ? (zs[2 * j] <= r) : (zrr <= sa))) v.x = 0.f;
+                                if (!(REV ? (zs[2 * j + 1] <= r) : (zrr <= sa + 1))) v.y = 0.f;
+                            }
+                            x[j] = v;
                         }
                     } else {
+                        const float2 cc = make_float2(clr, clr);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int s = s0 + e;
-                            const bool keep = REV ? (s >= r && zs[e] <= r) : (s <= r && zrr <= s);
-                            const float m = ex2(REV ? cs[e] - clr : clr - cs[e]);
-                            x[e] = keep ? __uint_as_float(pr[e]) * m : 0.f;
+                        for (int j = 0; j < 16; ++j) {
+                            // decay exponent: cl_r - cl_s forward, cl_s - cl_r reversed
+                            const float2 cs2 = make_float2(cs[2 * j], cs[2 * j + 1]);
+                            const float2 arg = REV ? __ffma2_rn(cc, make_float2(-1.f, -1.f), cs2)
+                                                   : __ffma2_rn(cs2, make_float2(-1.f, -1.f), cc);
+                            float2 v = __fmul2_rn(pv(j), make_float2(ex2(arg.x), ex2(arg.y)));
+                            const int sa = s0 + 2 * j;
+                            if (!(REV ? (sa >= r && zs[2 * j] <= r) : (sa <= r && zrr <= sa))) v.x = 0.f;
+                            if (!(REV ? (sa + 1 >= r && zs[2 * j + 1] <= r) : (sa + 1 <= r && zrr <= sa + 1))) v.y = 0.f;
+                            x[j] = v;
                         }
                     }
                     store_parts(s0, x);
@@ -833,7 +852,13 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                 tmem_ld_wait();
                 float o[32];
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) o[jj] = fmaf(wr, __uint_as_float(oi[jj]), __uint_as_float(oa[jj]));
+                for (int jj = 0; jj < 16; ++jj) {
+                    const float2 v = __ffma2_rn(make_float2(wr, wr),
+                                                make_float2(__uint_as_float(oi[2 * jj]), __uint_as_float(oi[2 * jj + 1])),
+                                                make_float2(__uint_as_float(oa[2 * jj]), __uint_as_float(oa[2 * jj + 1])));
+                    o[2 * jj] = v.x;
+                    o[2 * jj + 1] = v.y;
+                }
                 if (prow >= 0) {
                     const uint32_t row = sbase + C::OFF_ZS + (uint32_t)(hf * TC * 128 + prow * 128);
 #pragma unroll
