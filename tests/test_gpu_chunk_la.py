@@ -111,3 +111,35 @@ def test_chunk_la_long_workload_sampled_heads(cla):
     the oracle (heads are independent problems)."""
     inp = workloads.make("la_long")
     _check(cla, inp, 128, heads=[0, 31])
+
+
+@pytest.mark.parametrize("d,chunk", [(128, 128), (64, 128), (128, 64)])
+def test_chunk_la_resets_across_pieces(cla, d, chunk):
+    """Resets at and next to the 32-token piece boundaries inside a chunk (the
+    off-diagonal pieces' decays are formed as row x column factors, which a
+    reset between piece and row must zero), in both traversal directions."""
+    inp = workloads.make("la_long", B=1, H=2, T=700, dk=d, dv=d)
+    la = inp["log_a"].clone()
+    for t in (31, 32, 33, 63, 95, 96, 127, 128, 200, 330, 511, 512, 699):
+        la[0, 0, t] = -float("inf")
+    for t in (17, 150, 401):
+        la[0, 1, t] = -float("inf")
+    inp["log_a"] = la
+    _check(cla, inp, chunk, dST=torch.from_numpy(np.random.default_rng(5).normal(0, 0.1, (1, 2, d, d)).astype(np.float32)))
+
+
+@pytest.mark.parametrize("d,chunk", [(128, 128), (64, 64)])
+def test_chunk_la_strong_decay(cla, d, chunk):
+    """Decays far from 1 (log a in [-8, -2]): products over a chunk underflow to
+    0 in fp32; every term must stay finite and match the recurrence."""
+    inp = workloads.make("la_long", B=1, H=2, T=600, dk=d, dv=d)
+    rng = np.random.default_rng(11)
+    inp["log_a"] = torch.from_numpy(-rng.uniform(2.0, 8.0, (1, 2, 600)).astype(np.float32))
+    _check(cla, inp, chunk)
+
+
+def test_chunk_la_long_workload_chunk64_sampled_heads(cla):
+    """1 x 32 x 65536, d = 128, chunk 64 (segments of 32 chunks) on the GPU;
+    heads 5 and 20 against the oracle."""
+    inp = workloads.make("la_long")
+    _check(cla, inp, 64, heads=[5, 20])
