@@ -741,7 +741,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
             wait(1 + b);
             wait_dec(nc + i);
             const float alpha = cl[5 * TC];
-            if (mtid == 0) tma_store_wait_read();  // the previous chunk's output tile has been read
+            if (lane == 0) tma_store_wait_read();  // this warp's rows of the previous output tile were read
             bar_sync(kBarMath, kMathThreads);
             write_zs(b, wst);
             fence_async_smem();
@@ -838,7 +838,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
             tc_fence_after();
             state_accumulate(alpha);
             // ---- OUT = O_intra + w_out O_inter (this warp: columns [32 hf, 32 hf + 32)), staged in the
-            // 128-byte-swizzled output tile, written by a TMA store
+            // 128-byte-swizzled output tile; each warp stores its own rows with a TMA store
             wait(7);
             wait(6);
             tc_fence_after();
@@ -866,6 +866,16 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                         st_shared_v4(row + (uint32_t)((c ^ (prow & 7)) << 4), o[c * 4], o[c * 4 + 1], o[c * 4 + 2],
                                      o[c * 4 + 3]);
                 }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    // rows past T are clipped by the store; the Zs buffer is rewritten only after
+                    // every warp's store has read its rows (the wait before the next chunk's Zs)
+                    constexpr int WROWS = (TC == 128) ? 32 : 16;
+                    tma_store_3d(&maps.out, zb * 64 + hf * 32, (int)t0 + q * WROWS, bh,
+                                 sbase + C::OFF_ZS + (uint32_t)(hf * TC * 128 + q * WROWS * 128));
+                    tma_store_commit();
+                }
                 if (has_w && prow >= 0 && t0 + prow < p.T) {
                     float dot = 0.f;
 #pragma unroll
@@ -887,19 +897,14 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
             write_s_smem();
             fence_async_smem();
             tc_fence_before();
-            bar_sync(kBarMath, kMathThreads);
-            if (mtid == 0) {
-                // rows past T are clipped by the store; the Zs buffers are rewritten only after
-                // the store has read them (tma_store_wait_read before the next chunk's Zs)
-                tma_store_3d(&maps.out, zb * 64, (int)t0, bh, sbase + C::OFF_ZS);
-                tma_store_3d(&maps.out, zb * 64 + 32, (int)t0, bh, sbase + C::OFF_ZS + TC * 128);
-                tma_store_commit();
+            if (has_w) {
+                bar_sync(kBarMath, kMathThreads);
+                if (hf == 0 && prow >= 0 && t0 + prow < p.T)
+                    p.wdot[((size_t)zb * p.BH + bh) * p.T + t0 + prow] = dotp[prow] + dotp[TC + prow];
             }
-            if (has_w && hf == 0 && prow >= 0 && t0 + prow < p.T)
-                p.wdot[((size_t)zb * p.BH + bh) * p.T + t0 + prow] = dotp[prow] + dotp[TC + prow];
             bar_arrive(kBarDone, kAllThreads);
         }
-        if (mtid == 0) tma_store_wait_all();
+        if (lane == 0) tma_store_wait_all();
 
         // ---- final state of the sequence
         const bool last = REV ? (seg == 0) : (seg == p.n_seg - 1);
@@ -979,7 +984,7 @@ int launch_tc_variant(const LaArgs &a, cudaStream_t s, unsigned int grid) {
     bool ok = make_map(&maps.x, a.X, DX, a.T, a.BH, TC) &&
               make_map(&maps.y, a.Y, DX, a.T, a.BH, TC) &&
               make_map(&maps.z, a.Z, a.DZ, a.T, a.BH, TC) &&
-              make_map(&maps.out, a.out, a.DZ, a.T, a.BH, TC, false);
+              make_map(&maps.out, a.out, a.DZ, a.T, a.BH, TC == 128 ? 32 : 16, false);
     if (ok && a.W != nullptr) ok = make_map(&maps.w, a.W, a.DZ, a.T, a.BH, TC);
     if (!ok) return fail(CLA_ERR_CUDA, "chunk_la: tensor map encoding failed");
     la_tc_kernel<DX, TC, REV><<<grid, C::NT, C::SMEM, s>>>(maps, a);
