@@ -532,15 +532,14 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                 uint32_t r[4];
                 ldsm_x4_trans(zt + sw128(tb * 8 + j, (4 * (g4 & 1) + blk_in) * 8), r);
                 const int t = tb * 8 + 2 * (lane & 3);
-                const float w0 = wst[t], w1 = wst[t + 1];
+                const float2 w2 = *reinterpret_cast<const float2 *>(wst + t);
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float2 f = unpack_bf16(r[i]);
-                    const float x0 = f.x * w0, x1 = f.y * w1;
-                    hi[i] = pack_bf16(x0, x1);
-                    const float2 fh = unpack_bf16(hi[i]);
-                    lo[i] = pack_bf16(x0 - fh.x, x1 - fh.y);
+                    const float2 x = __fmul2_rn(unpack_bf16(r[i]), w2);
+                    hi[i] = pack_bf16(x.x, x.y);
+                    const float2 rr = __ffma2_rn(unpack_bf16(hi[i]), make_float2(-1.f, -1.f), x);  // x - hi, exact
+                    lo[i] = pack_bf16(rr.x, rr.y);
                 }
                 const int nrow = (4 * (g4 & 1) + blk_in) * 8 + j;
                 const uint32_t off = (uint32_t)((tb * 8) >> 6) * 128 * 128 + sw128(nrow, (tb * 8) & 63);
@@ -572,10 +571,10 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    const float x0 = S[c * 8 + 2 * h], x1 = S[c * 8 + 2 * h + 1];
-                    hi[h] = pack_bf16(x0, x1);
-                    const float2 fh = unpack_bf16(hi[h]);
-                    lo[h] = pack_bf16(x0 - fh.x, x1 - fh.y);
+                    const float2 x = make_float2(S[c * 8 + 2 * h], S[c * 8 + 2 * h + 1]);
+                    hi[h] = pack_bf16(x.x, x.y);
+                    const float2 rr = __ffma2_rn(unpack_bf16(hi[h]), make_float2(-1.f, -1.f), x);  // x - hi, exact
+                    lo[h] = pack_bf16(rr.x, rr.y);
                 }
                 const uint32_t off = sw128(srow, hf * 32 + c * 8);
                 *reinterpret_cast<uint4 *>(smem + C::OFF_SH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
