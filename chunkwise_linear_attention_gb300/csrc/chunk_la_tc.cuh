@@ -767,10 +767,15 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                         tmem_st8(tmem + tlane + C::C_PB + (uint32_t)(s0 + 16 + 8 * h), lo);
                     }
                 };
+                // this warp's unmasked pieces (warp-uniform)
+                int pcs[PIECES];
+                int npc = 0;
+#pragma unroll
+                for (int pc = 0; pc < PIECES; ++pc)
+                    if (!piece_masked(hf * PIECES + pc)) pcs[npc++] = hf * PIECES + pc;
 #pragma unroll 1
-                for (int pc = 0; pc < PIECES; ++pc) {
-                    const int piece = hf * PIECES + pc;
-                    if (piece_masked(piece)) continue;  // zeroed before phase 2 (warp-uniform)
+                for (int k = 0; k < npc; ++k) {
+                    const int piece = (k == 0) ? pcs[0] : pcs[PIECES - 1];
                     const int s0 = piece * 32;
                     float2 x[16];
                     uint32_t pr[32];
