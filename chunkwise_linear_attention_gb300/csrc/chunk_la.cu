@@ -54,8 +54,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 // leaves at least kMinBlocks blocks (several waves on a 152-SM part), so the
 // fixed cost of a block's look-back is spread over as many chunks as the
 // grid's size allows; the smallest choice otherwise.
-constexpr int kSegChoices[3] = {32, 16, 8};
-constexpr long long kMinBlocks = 2048;
+constexpr int kSegChoices[4] = {64, 32, 16, 8};
+constexpr long long kMinBlocks = 1024;
 
 // ----------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -808,7 +808,7 @@ LaPlan la_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chun
     p.n_chunks = (int)((T + chunk - 1) / chunk);
     p.nzb_max = (int)((dk > dv ? dk : dv) / 64);
     const size_t BH = (size_t)B * H;
-    p.seg_chunks = kSegChoices[2];
+    p.seg_chunks = kSegChoices[3];
     for (int c : kSegChoices) {
         const long long nseg = (p.n_chunks + c - 1) / c;
         if (nseg * (long long)BH * p.nzb_max >= kMinBlocks) {
