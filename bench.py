@@ -15,7 +15,10 @@ and:
                 HBM copy bandwidth (MEASURED_PEAKS.json)
   cpu_baseline  the float64 C oracle on this host's cores, on a bounded sample
   e2e           the headline metric through the C ABI from pinned host
-                buffers, host<->device copies inside the timed region
+                buffers, host<->device copies of every step inside the timed
+                region; steps pipelined over three streams (inputs of the
+                next step, compute, outputs of the previous step overlap on
+                the full-duplex host link), device buffers in two sets
   clocks        nvidia-smi samples taken during the timed region
 
 --impl reference times the oracle (the reference arm of this build) instead.
@@ -202,39 +205,68 @@ def bench_scan(torch, cla, workloads, dev, steps, warmup, dist_on):
     step_ms = statistics.mean(f + b_ for f, b_ in zip(fwd, bwd))
     res = dict(n=n, B=B, T=T, D=D, step_ms=step_ms, fwd_ms=statistics.mean(fwd), bwd_ms=statistics.mean(bwd),
                bytes_fwd=12 * n, bytes_bwd=20 * n, wall_s=t_wall, launches=2 * steps)
-    # e2e: pinned host inputs -> device, fwd + bwd, outputs -> host
+    # e2e: pinned host inputs -> device, fwd + bwd, outputs -> host, every step; steps are
+    # pipelined over three streams (inputs of step i + 1, compute of step i and outputs of
+    # step i - 1 overlap: the host link is full duplex) with device buffers in two sets.
     host_in = {k: inp[k].pin_memory() for k in ("a", "b", "h0", "dh")}
     host_out = {"h": torch.empty(B, T, D).pin_memory(), "hT": torch.empty(B, D).pin_memory(),
                 "da": torch.empty(B, T, D).pin_memory(), "db": torch.empty(B, T, D).pin_memory(),
                 "dh0": torch.empty(B, D).pin_memory()}
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    for v in host_out.values():
+        v.zero_()  # touch the pages before timing
+    sets = [({k: torch.empty_like(v, device=dev) for k, v in host_in.items()},
+             {k: torch.empty_like(v, device=dev) for k, v in host_out.items()}) for _ in range(2)]
+    s_in, s_cp, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     e2e_steps = max(3, min(steps, 20))
 
-    def e2e_step():
-        for k in host_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
-        cla.scan_diag_fwd(dev_in["a"], dev_in["b"], dev_in["h0"], h=h, hT=hT, workspace=ws, stream=stream)
-        cla.scan_diag_bwd(dev_in["a"], dev_in["h0"], h, dev_in["dh"], da=da, db=db, dh0=dh0, workspace=ws,
-                          stream=stream)
-        host_out["h"].copy_(h, non_blocking=True)
-        host_out["hT"].copy_(hT, non_blocking=True)
-        host_out["da"].copy_(da, non_blocking=True)
-        host_out["db"].copy_(db, non_blocking=True)
-        host_out["dh0"].copy_(dh0, non_blocking=True)
+    def ev():
+        return torch.cuda.Event()
 
-    e2e_step()
+    def run_e2e(n):
+        done_cp = [None, None]   # compute of the step that last used each set
+        done_out = [None, None]  # output copies of the step that last used each set
+        last_out = None
+        for i in range(n):
+            di, do = sets[i % 2]
+            if done_cp[i % 2] is not None:
+                s_in.wait_event(done_cp[i % 2])  # the set's inputs were consumed
+            with torch.cuda.stream(s_in):
+                for k in host_in:
+                    di[k].copy_(host_in[k], non_blocking=True)
+            e_in = ev()
+            e_in.record(s_in)
+            s_cp.wait_event(e_in)
+            if done_out[i % 2] is not None:
+                s_cp.wait_event(done_out[i % 2])  # the set's outputs were copied out
+            cla.scan_diag_fwd(di["a"], di["b"], di["h0"], h=do["h"], hT=do["hT"], workspace=ws, stream=s_cp)
+            cla.scan_diag_bwd(di["a"], di["h0"], do["h"], di["dh"], da=do["da"], db=do["db"], dh0=do["dh0"],
+                              workspace=ws, stream=s_cp)
+            e_cp = ev()
+            e_cp.record(s_cp)
+            done_cp[i % 2] = e_cp
+            s_out.wait_event(e_cp)
+            with torch.cuda.stream(s_out):
+                for k in host_out:
+                    host_out[k].copy_(do[k], non_blocking=True)
+            last_out = ev()
+            last_out.record(s_out)
+            done_out[i % 2] = last_out
+        return last_out
+
+    run_e2e(2)
     torch.cuda.synchronize()
     s, e = _events(torch)
     _sync_all(torch, dist_on)
-    s.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e.record(stream)
+    s.record(s_in)
+    last = run_e2e(e2e_steps)
+    s_in.wait_event(last)  # the last outputs are on the host (they follow every earlier copy and kernel)
+    e.record(s_in)
     _sync_all(torch, dist_on)
     res["e2e_ms"] = s.elapsed_time(e) / e2e_steps
+    cla.check_status(ws)
     res["h2d_bytes"] = sum(v.numel() * v.element_size() for v in host_in.values())
     res["d2h_bytes"] = sum(v.numel() * v.element_size() for v in host_out.values())
-    del a, b, h0, dh, h, da, db, dev_in, host_in, host_out
+    del a, b, h0, dh, h, da, db, sets, host_in, host_out
     return res
 
 
