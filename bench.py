@@ -299,6 +299,27 @@ def bench_scan_small(torch, cla, workloads, dev, flush, peaks, iters=20, shape=N
             "GBps": round(by / ms / 1e6, 1), "frac_hbm": round(by / ms / 1e6 / peaks["hbm_gbs"], 4)}
 
 
+def bench_scan_blelloch(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
+    """Forward diagonal scan on the headline workload with the runs of a chunk
+    composed by Hillis-Steele (the library's path) and by a Blelloch tree (the
+    measured alternative), timed alternately in one process."""
+    inp = workloads.make("scan", **(shape or {}))
+    a, b, h0 = inp["a"].to(dev), inp["b"].to(dev), inp["h0"].to(dev)
+    B, T, D = a.shape
+    ws = torch.empty(cla.scan_diag_workspace_size(B, T, D), dtype=torch.uint8, device=dev)
+    h = torch.empty_like(a)
+    by = 12 * B * T * D
+    hs, bl = [], []
+    for _ in range(iters):
+        hs.append(_time_calls(torch, lambda: cla.scan_diag_fwd(a, b, h0, h=h, workspace=ws), flush, 1))
+        bl.append(_time_calls(torch, lambda: cla.scan_diag_fwd_blelloch(a, b, h0, h=h, workspace=ws), flush, 1))
+    cla.check_status(ws)
+    ms_hs, ms_bl = statistics.median(hs), statistics.median(bl)
+    return {"workload": f"diagonal scan fwd fp32 B={B} T={T} D={D}: Hillis-Steele vs Blelloch across a chunk's runs",
+            "hillis_steele_us": round(ms_hs * 1e3, 2), "blelloch_us": round(ms_bl * 1e3, 2),
+            "hillis_steele_GBps": round(by / ms_hs / 1e6, 1), "blelloch_GBps": round(by / ms_bl / 1e6, 1)}
+
+
 def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=5, shape=None):
     inp = workloads.make(name, **(shape or {}))
     t = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
@@ -436,7 +457,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--only", default=None,
-                    choices=["scan_small", "selective", "la_const", "la_long", "la_long_chunk64"],
+                    choices=["scan_small", "scan_fwd_blelloch", "selective", "la_const", "la_long", "la_long_chunk64"],
                     help="time one workload only (forward and backward), e.g. for profiling")
     ap.add_argument("--shape", default="", help="shape overrides for --only, e.g. H=32,T=4096")
     args = ap.parse_args()
@@ -469,6 +490,7 @@ def main():
         flush = Flusher(torch, dev)
         it = max(1, args.steps)
         fns = {"scan_small": lambda: bench_scan_small(torch, cla, workloads, dev, flush, peaks, it, shape),
+               "scan_fwd_blelloch": lambda: bench_scan_blelloch(torch, cla, workloads, dev, flush, peaks, it, shape),
                "selective": lambda: bench_selective(torch, cla, workloads, dev, flush, peaks, it, shape),
                "la_const": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_const", 64, it, shape),
                "la_long": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 128, it, shape),
@@ -492,6 +514,7 @@ def main():
         flush = Flusher(torch, dev)
         for key, fn in (
                 ("scan_small", lambda: bench_scan_small(torch, cla, workloads, dev, flush, peaks)),
+                ("scan_fwd_blelloch", lambda: bench_scan_blelloch(torch, cla, workloads, dev, flush, peaks)),
                 ("selective", lambda: bench_selective(torch, cla, workloads, dev, flush, peaks)),
                 ("la_const", lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_const", 64)),
                 ("la_long", lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 128)),

@@ -50,6 +50,7 @@ def lib():
                 "cla_selftest_wait_timeout": ([P, SZ, P], INT),
                 "cla_scan_diag_workspace_size": ([I64, I64, I64], SZ),
                 "cla_scan_diag_fwd": ([P, P, P, P, P, I64, I64, I64, P, SZ, P], INT),
+                "cla_scan_diag_fwd_blelloch": ([P, P, P, P, P, I64, I64, I64, P, SZ, P], INT),
                 "cla_scan_diag_bwd": ([P, P, P, P, P, P, P, P, I64, I64, I64, P, SZ, P], INT),
                 "cla_scan_diag_fwd_noalloc": ([P, P, P, P, P, I64, I64, I64, P], INT),
                 "cla_selective_scan_workspace_size": ([I64, I64, I64, I64], SZ),
@@ -136,6 +137,21 @@ def scan_diag_fwd(a, b, h0=None, *, h=None, hT=None, workspace=None, stream=None
     hT = _out(hT, (B, D), f32, dev)
     ws = _ws(scan_diag_workspace_size(B, T, D), dev, workspace)
     _check("cla_scan_diag_fwd", lib().cla_scan_diag_fwd(
+        _ptr(a, f32, "a"), _ptr(b, f32, "b"), _ptr(h0, f32, "h0"), _ptr(h, f32, "h"), _ptr(hT, f32, "hT"),
+        B, T, D, _ptr(ws), ws.numel(), _stream(stream)))
+    return h, hT
+
+
+def scan_diag_fwd_blelloch(a, b, h0=None, *, h=None, hT=None, workspace=None, stream=None):
+    """scan_diag_fwd with a Blelloch tree across the runs of a chunk (a measured
+    alternative to Hillis-Steele); returns (h, hT)."""
+    B, T, D = a.shape
+    dev = a.device
+    f32 = torch.float32
+    h = _out(h, (B, T, D), f32, dev)
+    hT = _out(hT, (B, D), f32, dev)
+    ws = _ws(scan_diag_workspace_size(B, T, D), dev, workspace)
+    _check("cla_scan_diag_fwd_blelloch", lib().cla_scan_diag_fwd_blelloch(
         _ptr(a, f32, "a"), _ptr(b, f32, "b"), _ptr(h0, f32, "h0"), _ptr(h, f32, "h"), _ptr(hT, f32, "hT"),
         B, T, D, _ptr(ws), ws.numel(), _stream(stream)))
     return h, hT

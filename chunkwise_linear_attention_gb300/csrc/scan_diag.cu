@@ -154,7 +154,10 @@ __device__ __forceinline__ size_t unit_index(const ScanGeom &g, int chunk, int b
 }
 
 // ------------------------------------------------------------------ forward
-template <int VEC>
+// BLELLOCH selects how the 8 runs of a chunk are composed: Hillis-Steele
+// (3 rounds, every run combines) or a Blelloch up-sweep / down-sweep (6 rounds,
+// fewer combines), the latter kept as a measured alternative.
+template <int VEC, bool BLELLOCH = false>
 __global__ void __launch_bounds__(kWarps * 32, 2)
 scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
                      const float *__restrict__ h0, float *__restrict__ h,
@@ -199,25 +202,68 @@ scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
             Bc[v] = fmaf(av[i][v], Bc[v], bv[i][v]);
             A[v] *= av[i][v];
         }
-    // 3. Hillis-Steele across the 8 runs: combine with the run 1, 2, 4 to the left.
+    float Aex[VEC], Bex[VEC];  // prefix of the runs before this one
+    if constexpr (!BLELLOCH) {
+        // 3. Hillis-Steele across the 8 runs: combine with the run 1, 2, 4 to the left.
 #pragma unroll
-    for (int off = 1; off < kSub; off <<= 1) {
+        for (int off = 1; off < kSub; off <<= 1) {
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            const float pa = __shfl_up_sync(0xffffffffu, A[v], off * kCg);
-            const float pb = __shfl_up_sync(0xffffffffu, Bc[v], off * kCg);
-            if (sub >= off) {  // (pa, pb) happened first
-                Bc[v] = fmaf(A[v], pb, Bc[v]);
-                A[v] *= pa;
+            for (int v = 0; v < VEC; ++v) {
+                const float pa = __shfl_up_sync(0xffffffffu, A[v], off * kCg);
+                const float pb = __shfl_up_sync(0xffffffffu, Bc[v], off * kCg);
+                if (sub >= off) {  // (pa, pb) happened first
+                    Bc[v] = fmaf(A[v], pb, Bc[v]);
+                    A[v] *= pa;
+                }
             }
         }
-    }
-    float Aex[VEC], Bex[VEC];  // prefix of the runs before this one
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) {
-        Aex[v] = __shfl_up_sync(0xffffffffu, A[v], kCg);
-        Bex[v] = __shfl_up_sync(0xffffffffu, Bc[v], kCg);
-        if (sub == 0) { Aex[v] = 1.f; Bex[v] = 0.f; }
+        for (int v = 0; v < VEC; ++v) {
+            Aex[v] = __shfl_up_sync(0xffffffffu, A[v], kCg);
+            Bex[v] = __shfl_up_sync(0xffffffffu, Bc[v], kCg);
+            if (sub == 0) { Aex[v] = 1.f; Bex[v] = 0.f; }
+        }
+    } else {
+        // 3'. Blelloch: up-sweep (run s with (s + 1) % 2st == 0 folds in run s - st, which
+        // happened first); the last run then holds the chunk's pair.
+#pragma unroll
+        for (int st = 1; st < kSub; st <<= 1) {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float pa = __shfl_up_sync(0xffffffffu, A[v], st * kCg);
+                const float pb = __shfl_up_sync(0xffffffffu, Bc[v], st * kCg);
+                if (((sub + 1) & (2 * st - 1)) == 0) {
+                    Bc[v] = fmaf(A[v], pb, Bc[v]);
+                    A[v] *= pa;
+                }
+            }
+        }
+        // down-sweep from the identity at the last run: a right node becomes (its prefix, then
+        // the left subtree), a left node takes the right node's prefix.
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            Aex[v] = (sub == kSub - 1) ? 1.f : A[v];
+            Bex[v] = (sub == kSub - 1) ? 0.f : Bc[v];
+        }
+#pragma unroll
+        for (int st = kSub / 2; st >= 1; st >>= 1) {
+            const bool right = ((sub + 1) & (2 * st - 1)) == 0;
+            const bool left = ((sub + 1 + st) & (2 * st - 1)) == 0;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float la = __shfl_up_sync(0xffffffffu, Aex[v], st * kCg);
+                const float lb = __shfl_up_sync(0xffffffffu, Bex[v], st * kCg);
+                const float ra = __shfl_down_sync(0xffffffffu, Aex[v], st * kCg);
+                const float rb = __shfl_down_sync(0xffffffffu, Bex[v], st * kCg);
+                if (right) {
+                    Bex[v] = fmaf(la, Bex[v], lb);
+                    Aex[v] *= la;
+                } else if (left) {
+                    Aex[v] = ra;
+                    Bex[v] = rb;
+                }
+            }
+        }
     }
     // 4. decoupled look-back by the lanes holding the chunk aggregate
     float carry[VEC];
@@ -486,11 +532,10 @@ extern "C" size_t cla_scan_diag_workspace_size(int64_t B, int64_t T, int64_t D) 
     return p1.total > p4.total ? p1.total : p4.total;
 }
 
-extern "C" int cla_scan_diag_fwd(const float *a, const float *b, const float *h0, float *h,
-                                 float *hT, int64_t B, int64_t T, int64_t D, void *ws,
-                                 size_t ws_bytes, void *stream) {
+namespace {
+int scan_fwd(const char *fn, bool blelloch, const float *a, const float *b, const float *h0, float *h, float *hT,
+             int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes, void *stream) {
     clear_error();
-    const char *fn = "cla_scan_diag_fwd";
     int st = check_sizes(fn, B, T, D);
     if (st) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -511,9 +556,27 @@ extern "C" int cla_scan_diag_fwd(const float *a, const float *b, const float *h0
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.total, s), fn);
     const ScanWs w = bind_ws(p, ws);
     const unsigned int grid = (unsigned int)((size_t)p.g.n_chunks * p.g.B * p.g.n_cblk);
-    if (v4) scan_diag_fwd_kernel<4><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);
-    else scan_diag_fwd_kernel<1><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);
+    if (blelloch) {
+        if (v4) scan_diag_fwd_kernel<4, true><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);
+        else scan_diag_fwd_kernel<1, true><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);
+    } else {
+        if (v4) scan_diag_fwd_kernel<4><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);
+        else scan_diag_fwd_kernel<1><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);
+    }
     return check_launch(fn);
+}
+}  // namespace
+
+extern "C" int cla_scan_diag_fwd(const float *a, const float *b, const float *h0, float *h,
+                                 float *hT, int64_t B, int64_t T, int64_t D, void *ws,
+                                 size_t ws_bytes, void *stream) {
+    return scan_fwd("cla_scan_diag_fwd", false, a, b, h0, h, hT, B, T, D, ws, ws_bytes, stream);
+}
+
+extern "C" int cla_scan_diag_fwd_blelloch(const float *a, const float *b, const float *h0, float *h,
+                                          float *hT, int64_t B, int64_t T, int64_t D, void *ws,
+                                          size_t ws_bytes, void *stream) {
+    return scan_fwd("cla_scan_diag_fwd_blelloch", true, a, b, h0, h, hT, B, T, D, ws, ws_bytes, stream);
 }
 
 extern "C" int cla_scan_diag_bwd(const float *a, const float *h0, const float *h,

@@ -92,6 +92,17 @@ int cla_scan_diag_fwd(const float *a, const float *b, const float *h0, float *h,
                       float *hT, int64_t B, int64_t T, int64_t D, void *ws,
                       size_t ws_bytes, void *stream);
 
+/* cla_scan_diag_fwd with the runs of a chunk composed by a Blelloch
+ * up-sweep / down-sweep instead of Hillis-Steele ("Parallel Scan", the
+ * work-efficient scan the page contrasts with Hillis-Steele; "Parallel Scan"
+ * (aiwiki), the tree form).  Same arguments, layouts, workspace, ownership
+ * and errors as cla_scan_diag_fwd, and the same results up to rounding order;
+ * kept as a measured alternative (the up-sweep and down-sweep take six
+ * shuffle rounds across the eight runs where Hillis-Steele takes three). */
+int cla_scan_diag_fwd_blelloch(const float *a, const float *b, const float *h0,
+                               float *h, float *hT, int64_t B, int64_t T,
+                               int64_t D, void *ws, size_t ws_bytes, void *stream);
+
 /* Backward ("Parallel Scan", "The backward pass is a scan in reverse"): with
  * direct gradients g_t = dh_t (plus dhT on h_T), the adjoint
  * hbar_t = g_t + a_{t+1} hbar_{t+1} is the same scan on reversed time with

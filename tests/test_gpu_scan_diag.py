@@ -116,3 +116,29 @@ def test_scan_diag_reused_workspace_and_status(cla):
     h2, _ = cla.scan_diag_fwd(a, b, h0, workspace=ws)
     cla.check_status(ws)
     assert float(((h1 - h2).abs() / h2.abs().clamp_min(1.0)).max()) <= 1e-6
+
+
+@pytest.mark.parametrize("B,T,D", [(1, 1, 4), (2, 63, 16), (2, 65, 20), (3, 200, 96), (1, 1000, 7), (2, 513, 130),
+                                   (1, 4097, 8)])
+@pytest.mark.parametrize("with_h0", [False, True])
+def test_scan_diag_blelloch_small(cla, B, T, D, with_h0):
+    """The Blelloch composition of a chunk's runs gives the recurrence's states."""
+    inp = workloads.make("scan", B=B, T=T, D=D)
+    dev = torch.device("cuda")
+    h0 = inp["h0"].to(dev) if with_h0 else None
+    h, hT = cla.scan_diag_fwd_blelloch(inp["a"].to(dev), inp["b"].to(dev), h0)
+    torch.cuda.synchronize()
+    rh, rhT = oracle.scan_diag_fwd(inp["a"], inp["b"], inp["h0"] if with_h0 else None)
+    assert_fp32("h", h, rh)
+    assert_fp32("hT", hT, rhT)
+
+
+def test_scan_diag_blelloch_workload_full(cla):
+    """8 x 4096 x 1024 forward with the Blelloch composition, every element."""
+    inp = workloads.make("scan")
+    dev = torch.device("cuda")
+    h, hT = cla.scan_diag_fwd_blelloch(inp["a"].to(dev), inp["b"].to(dev), inp["h0"].to(dev))
+    torch.cuda.synchronize()
+    rh, rhT = oracle.scan_diag_fwd(inp["a"], inp["b"], inp["h0"])
+    assert_fp32("h", h, rh)
+    assert_fp32("hT", hT, rhT)
