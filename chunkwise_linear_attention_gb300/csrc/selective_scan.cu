@@ -30,6 +30,8 @@
 // transpose-reduce, per-block partials, then a small reduction kernel.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "cla_internal.cuh"
 
 namespace cla {
@@ -76,10 +78,14 @@ __device__ __forceinline__ float exp2_fma(float x) {
 // The same 2^x on two arguments at once: the paired FP32 instructions
 // (add / mul / fma on float2) round each lane exactly as the scalar ones, so
 // the results equal exp2_fma's; the instruction count is about halved.
+// CLAMP = false: the caller guarantees |x| <= 126 (then the clamp changes nothing).
+template <bool CLAMP = true>
 __device__ __forceinline__ float2 exp2_fma2(float2 x) {
     constexpr float kMagic = 12582912.0f;
-    x.x = fminf(fmaxf(x.x, -127.f), 127.f);
-    x.y = fminf(fmaxf(x.y, -127.f), 127.f);
+    if (CLAMP) {
+        x.x = fminf(fmaxf(x.x, -127.f), 127.f);
+        x.y = fminf(fmaxf(x.y, -127.f), 127.f);
+    }
     const float2 km = __fadd2_rn(x, make_float2(kMagic, kMagic));
     const float2 k = __fadd2_rn(km, make_float2(-kMagic, -kMagic));
     const float2 f = __ffma2_rn(k, make_float2(-1.f, -1.f), x);  // x - k, exact
@@ -173,8 +179,12 @@ sel_fwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
 #pragma unroll
     for (int n = 0; n < kN; ++n) A2[n] = cok ? A[(size_t)c * kN + n] * kLog2e : 0.f;
     float2 A2p[kJ];
+    float amax = 0.f;  // steps with |delta| * amax <= 126 need no clamp in 2^x
 #pragma unroll
-    for (int j = 0; j < kJ; ++j) A2p[j] = make_float2(A2[2 * j], A2[2 * j + 1]);
+    for (int j = 0; j < kJ; ++j) {
+        A2p[j] = make_float2(A2[2 * j], A2[2 * j + 1]);
+        amax = fmaxf(amax, fmaxf(fabsf(A2[2 * j]), fabsf(A2[2 * j + 1])));
+    }
 
     // phase 1: the chunk as one pair per n: (exp(A sum delta), Bagg)
     float2 Baggp[kJ];
@@ -185,9 +195,14 @@ sel_fwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
         const float d = s_d[r][tid];
         const float dx = d * __bfloat162float(s_x[r][tid]);
         const float2 *Br = reinterpret_cast<const float2 *>(s_B[r]);
+        auto step = [&](auto clamp) {
 #pragma unroll
-        for (int j = 0; j < kJ; ++j)
-            Baggp[j] = __ffma2_rn(exp2_fma2(__fmul2_rn(f2(d), A2p[j])), Baggp[j], __fmul2_rn(f2(dx), Br[j]));
+            for (int j = 0; j < kJ; ++j)
+                Baggp[j] = __ffma2_rn(exp2_fma2<decltype(clamp)::value>(__fmul2_rn(f2(d), A2p[j])), Baggp[j],
+                                      __fmul2_rn(f2(dx), Br[j]));
+        };
+        if (fabsf(d) * amax <= 126.f) step(std::false_type{});
+        else step(std::true_type{});
         sumd += d;
     }
     float Bagg[kN];
@@ -268,11 +283,16 @@ sel_fwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
         const float2 *Br = reinterpret_cast<const float2 *>(s_B[r]);
         const float2 *Cr = reinterpret_cast<const float2 *>(s_C[r]);
         float2 acc = f2(0.f);  // even and odd entries summed separately, then added
+        auto step = [&](auto clamp) {
 #pragma unroll
-        for (int j = 0; j < kJ; ++j) {
-            hp[j] = __ffma2_rn(exp2_fma2(__fmul2_rn(f2(d), A2p[j])), hp[j], __fmul2_rn(f2(dx), Br[j]));
-            acc = __ffma2_rn(Cr[j], hp[j], acc);
-        }
+            for (int j = 0; j < kJ; ++j) {
+                hp[j] = __ffma2_rn(exp2_fma2<decltype(clamp)::value>(__fmul2_rn(f2(d), A2p[j])), hp[j],
+                                   __fmul2_rn(f2(dx), Br[j]));
+                acc = __ffma2_rn(Cr[j], hp[j], acc);
+            }
+        };
+        if (fabsf(d) * amax <= 126.f) step(std::false_type{});
+        else step(std::true_type{});
         if (cok) __stcs(y + ((size_t)bi * g.T + t0 + r) * g.D + c, acc.x + acc.y);
     }
     if (hT != nullptr && cok && chunk == g.n_chunks - 1) {
