@@ -125,6 +125,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
+// 16 columns of 16 TMEM lanes: threads 0..15 read lanes base+0..15 at the address's column,
+// threads 16..31 the same lanes at column + 16 (the 64-row accumulator layout keeps its rows
+// in the first 16 lanes of each quarter, so both halves of a warp then hold data).
+__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], 16;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+// 8 columns of 16 TMEM lanes, threads 16..31 at column + 8.
+__device__ __forceinline__ void tmem_st8x2(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], 8, {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+// A thread's columns of a row of an accumulator: 32 of 128 lanes (32 per thread), or at 64 rows
+// 16 per thread through the paired-half shape.
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[W]) {
+    if constexpr (W == 32) tmem_ld32(taddr, r);
+    else tmem_ld16x2(taddr, r);
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // 16 consecutive 32-bit TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -512,8 +535,17 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
         const int q = warp & 3;    // TMEM lane quarter
         const int hf = warp >> 2;  // which half of the columns this warp handles
         const int mtid = tid;      // 0..255
-        const int prow = (TC == 128) ? q * 32 + lane : (lane < 16 ? q * 16 + lane : -1);
-        const int srow = (DX == 128) ? q * 32 + lane : (lane < 16 ? q * 16 + lane : -1);
+        // This thread's row and columns.  An accumulator of 128 rows keeps row m in TMEM lane m:
+        // a thread holds its lane's row, 32 columns (this warp's half of 64).  One of 64 rows keeps
+        // rows 16q..16q+15 in lanes 32q..32q+15: both halves of the warp read those lanes, threads
+        // 16..31 taking the upper 16 of the warp's 32 columns.  Token rows (scores, outputs) have
+        // T_c rows, state rows (dS, State) DX.
+        constexpr int OW = (TC == 128) ? 32 : 16;  // output columns per thread
+        constexpr int SW = (DX == 128) ? 32 : 16;  // state columns per thread
+        const int prow = (TC == 128) ? q * 32 + lane : q * 16 + (lane & 15);
+        const int srow = (DX == 128) ? q * 32 + lane : q * 16 + (lane & 15);
+        const int ocol = hf * 32 + ((TC == 128) ? 0 : (lane >> 4) * 16);  // of the 64 output columns
+        const int scol = hf * 32 + ((DX == 128) ? 0 : (lane >> 4) * 16);  // of the 64 state columns
         const uint32_t tlane = (uint32_t)(q * 32) << 16;
         auto wait_dec = [&](int n) {
             if (!mbar_wait(bar(8 + (n & 1)), (uint32_t)((n >> 1) & 1))) timed_out = true;
@@ -547,16 +579,16 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                 stsm_x4(sbase + C::OFF_ZS + off + 64 * 128, lo);
             }
         };
-        float S[32];
+        float S[SW];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) S[c] = 0.f;
+        for (int c = 0; c < SW; ++c) S[c] = 0.f;
         auto state_accumulate = [&](float alpha) {
-            uint32_t rh[32], rl[32];
-            tmem_ld32(tmem + tlane + C::C_DS + hf * 32, rh);
-            tmem_ld32(tmem + tlane + C::C_DS + 64 + hf * 32, rl);
+            uint32_t rh[SW], rl[SW];
+            tmem_ld_cols<SW>(tmem + tlane + C::C_DS + hf * 32, rh);
+            tmem_ld_cols<SW>(tmem + tlane + C::C_DS + 64 + hf * 32, rl);
             tmem_ld_wait();
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
+            for (int jj = 0; jj < SW / 2; ++jj) {
                 const float2 d = __fadd2_rn(make_float2(__uint_as_float(rh[2 * jj]), __uint_as_float(rh[2 * jj + 1])),
                                             make_float2(__uint_as_float(rl[2 * jj]), __uint_as_float(rl[2 * jj + 1])));
                 const float2 v = __ffma2_rn(make_float2(alpha, alpha), make_float2(S[2 * jj], S[2 * jj + 1]), d);
@@ -565,9 +597,8 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
             }
         };
         auto write_s_smem = [&]() {
-            if (srow < 0) return;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < SW / 8; ++c) {
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
@@ -576,7 +607,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                     const float2 rr = __ffma2_rn(unpack_bf16(hi[h]), make_float2(-1.f, -1.f), x);  // x - hi, exact
                     lo[h] = pack_bf16(rr.x, rr.y);
                 }
-                const uint32_t off = sw128(srow, hf * 32 + c * 8);
+                const uint32_t off = sw128(srow, scol + c * 8);
                 *reinterpret_cast<uint4 *>(smem + C::OFF_SH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                 *reinterpret_cast<uint4 *>(smem + C::OFF_SL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
@@ -606,21 +637,20 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
         const bool first = REV ? (seg == p.n_seg - 1) : (seg == 0);
         float4 *agg4 = p.agg + unit * (size_t)(DX * 16);
         float4 *inc4 = p.incl + unit * (size_t)(DX * 16);
-        auto load_state0 = [&](float (&dst)[32], float scale, bool add) {
-            if (srow < 0) return;
-            float v[32];
-            const int col0 = zb * 64 + hf * 32;
+        auto load_state0 = [&](float (&dst)[SW], float scale, bool add) {
+            float v[SW];
+            const int col0 = zb * 64 + scol;
             if (p.state0 == nullptr) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) v[c] = 0.f;
+                for (int c = 0; c < SW; ++c) v[c] = 0.f;
             } else if (p.trans0) {  // [DZ][DX]: lanes read consecutive rows
 #pragma unroll
-                for (int c = 0; c < 32; ++c) v[c] = __ldg(p.state0 + ((size_t)bh * p.DZ + col0 + c) * DX + srow);
-            } else {  // [DX][DZ]: this thread's 32 columns are contiguous
+                for (int c = 0; c < SW; ++c) v[c] = __ldg(p.state0 + ((size_t)bh * p.DZ + col0 + c) * DX + srow);
+            } else {  // [DX][DZ]: this thread's columns are contiguous
                 const float *src = p.state0 + ((size_t)bh * DX + srow) * p.DZ + col0;
                 if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
+                    for (int c4 = 0; c4 < SW / 4; ++c4) {
                         const float4 f = __ldg(reinterpret_cast<const float4 *>(src) + c4);
                         v[4 * c4] = f.x;
                         v[4 * c4 + 1] = f.y;
@@ -629,24 +659,23 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) v[c] = __ldg(src + c);
+                    for (int c = 0; c < SW; ++c) v[c] = __ldg(src + c);
                 }
             }
 #pragma unroll
-            for (int c = 0; c < 32; ++c) dst[c] = add ? fmaf(scale, v[c], dst[c]) : v[c];
+            for (int c = 0; c < SW; ++c) dst[c] = add ? fmaf(scale, v[c], dst[c]) : v[c];
         };
-        float Sin[32];
+        // look-back payloads are [column / 4][row] float4s; this thread's columns start at scol
+        float Sin[SW];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) Sin[c] = 0.f;
+        for (int c = 0; c < SW; ++c) Sin[c] = 0.f;
         if (first) {
             load_state0(Sin, 1.f, false);
         } else {
-            if (srow >= 0) {
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4)
-                    __stcg(agg4 + (hf * 8 + c4) * DX + srow,
-                           make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]));
-            }
+            for (int c4 = 0; c4 < SW / 4; ++c4)
+                __stcg(agg4 + (scol / 4 + c4) * DX + srow,
+                       make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]));
             if (mtid == 0) p.alpha_ws[unit] = alpha_seg;
             bar_sync(kBarMath, kMathThreads);
             // the barrier orders every math thread's stores before thread 0's fence (cumulativity)
@@ -669,15 +698,13 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                 bar_sync(kBarMath, kMathThreads);
                 if (f == 2u || f == 1u) {
                     const float4 *src = (f == 2u ? p.incl : p.agg) + up * (size_t)(DX * 16);
-                    if (srow >= 0) {
 #pragma unroll
-                        for (int c4 = 0; c4 < 8; ++c4) {
-                            const float4 v = ld_cg4(src + (hf * 8 + c4) * DX + srow);
-                            Sin[4 * c4] = fmaf(accA, v.x, Sin[4 * c4]);
-                            Sin[4 * c4 + 1] = fmaf(accA, v.y, Sin[4 * c4 + 1]);
-                            Sin[4 * c4 + 2] = fmaf(accA, v.z, Sin[4 * c4 + 2]);
-                            Sin[4 * c4 + 3] = fmaf(accA, v.w, Sin[4 * c4 + 3]);
-                        }
+                    for (int c4 = 0; c4 < SW / 4; ++c4) {
+                        const float4 v = ld_cg4(src + (scol / 4 + c4) * DX + srow);
+                        Sin[4 * c4] = fmaf(accA, v.x, Sin[4 * c4]);
+                        Sin[4 * c4 + 1] = fmaf(accA, v.y, Sin[4 * c4 + 1]);
+                        Sin[4 * c4 + 2] = fmaf(accA, v.z, Sin[4 * c4 + 2]);
+                        Sin[4 * c4 + 3] = fmaf(accA, v.w, Sin[4 * c4 + 3]);
                     }
                     if (f == 2u) break;
                     accA *= pa;
@@ -691,15 +718,12 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                 }
             }
         }
-        if (srow >= 0) {
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4)
-                __stcg(inc4 + (hf * 8 + c4) * DX + srow,
-                       make_float4(fmaf(alpha_seg, Sin[4 * c4], S[4 * c4]),
-                                   fmaf(alpha_seg, Sin[4 * c4 + 1], S[4 * c4 + 1]),
-                                   fmaf(alpha_seg, Sin[4 * c4 + 2], S[4 * c4 + 2]),
-                                   fmaf(alpha_seg, Sin[4 * c4 + 3], S[4 * c4 + 3])));
-        }
+        for (int c4 = 0; c4 < SW / 4; ++c4)
+            __stcg(inc4 + (scol / 4 + c4) * DX + srow,
+                   make_float4(fmaf(alpha_seg, Sin[4 * c4], S[4 * c4]), fmaf(alpha_seg, Sin[4 * c4 + 1], S[4 * c4 + 1]),
+                               fmaf(alpha_seg, Sin[4 * c4 + 2], S[4 * c4 + 2]),
+                               fmaf(alpha_seg, Sin[4 * c4 + 3], S[4 * c4 + 3])));
         bar_sync(kBarMath, kMathThreads);
         if (mtid == 0) {
             __threadfence();
@@ -726,7 +750,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
             tmem_st_wait();
         }
 #pragma unroll
-        for (int c = 0; c < 32; ++c) S[c] = Sin[c];
+        for (int c = 0; c < SW; ++c) S[c] = Sin[c];
         write_s_smem();
         fence_async_smem();
         tc_fence_before();
@@ -748,8 +772,8 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
             // ---- mask and decay P (fp32, TMEM) into its bf16 parts (TMEM)
             wait(4);
             tc_fence_after();
-            {
-                const int r = prow < 0 ? 0 : prow;
+            if constexpr (TC == 128) {
+                const int r = prow;
                 const float clr = cl[r];
                 const int zrr = zr[r];
                 auto store_parts = [&](int s0, float2 (&x)[16]) {
@@ -834,6 +858,77 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                     store_parts(s0, x);
                 }
                 tmem_st_wait();
+            } else {
+                // 64-row scores: lanes 0..15 hold this warp's 16 rows; threads 0..15 take tokens
+                // s0..s0+15 of the piece, threads 16..31 tokens s0+16..s0+31 (paired-half shapes)
+                const int r = prow;
+                const float clr = cl[r];
+                const int zrr = zr[r];
+                const int piece = hf;  // one 32-token piece per warp
+                if (!piece_masked(piece)) {
+                    const int s0 = piece * 32, tok0 = s0 + 16 * (lane >> 4);
+                    uint32_t pr[16];
+                    tmem_ld16x2(tmem + tlane + C::C_P + (uint32_t)s0, pr);
+                    float cs[16];
+                    int zs[16];
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const float4 g = *reinterpret_cast<const float4 *>((piece != rpiece ? gcol : cl) + tok0 + 4 * c4);
+                        cs[4 * c4] = g.x;
+                        cs[4 * c4 + 1] = g.y;
+                        cs[4 * c4 + 2] = g.z;
+                        cs[4 * c4 + 3] = g.w;
+                        if (REV) {
+                            const int4 zv = *reinterpret_cast<const int4 *>(zr + tok0 + 4 * c4);
+                            zs[4 * c4] = zv.x;
+                            zs[4 * c4 + 1] = zv.y;
+                            zs[4 * c4 + 2] = zv.z;
+                            zs[4 * c4 + 3] = zv.w;
+                        }
+                    }
+                    tmem_ld_wait();
+                    auto pv = [&](int j) { return make_float2(__uint_as_float(pr[2 * j]), __uint_as_float(pr[2 * j + 1])); };
+                    float2 x[8];
+                    if (piece != rpiece) {
+                        const float f = REV ? ex2(cl[s0] - clr) : ex2(clr - cl[s0 + 31]);
+                        const float2 ff = make_float2(f, f);
+                        const bool all_keep = REV ? (zr[s0 + 31] <= r) : (zrr <= s0);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            float2 v = __fmul2_rn(pv(j), __fmul2_rn(ff, make_float2(cs[2 * j], cs[2 * j + 1])));
+                            if (!all_keep) {
+                                const int sa = tok0 + 2 * j;
+                                if (!(REV ? (zs[2 * j] <= r) : (zrr <= sa))) v.x = 0.f;
+                                if (!(REV ? (zs[2 * j + 1] <= r) : (zrr <= sa + 1))) v.y = 0.f;
+                            }
+                            x[j] = v;
+                        }
+                    } else {
+                        const float2 cc = make_float2(clr, clr);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float2 cs2 = make_float2(cs[2 * j], cs[2 * j + 1]);
+                            const float2 arg = REV ? __ffma2_rn(cc, make_float2(-1.f, -1.f), cs2)
+                                                   : __ffma2_rn(cs2, make_float2(-1.f, -1.f), cc);
+                            float2 v = __fmul2_rn(pv(j), make_float2(ex2(arg.x), ex2(arg.y)));
+                            const int sa = tok0 + 2 * j;
+                            if (!(REV ? (sa >= r && zs[2 * j] <= r) : (sa <= r && zrr <= sa))) v.x = 0.f;
+                            if (!(REV ? (sa + 1 >= r && zs[2 * j + 1] <= r) : (sa + 1 <= r && zrr <= sa + 1))) v.y = 0.f;
+                            x[j] = v;
+                        }
+                    }
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        hi[jj] = pack_bf16(x[jj].x, x[jj].y);
+                        const float2 r2 = __ffma2_rn(unpack_bf16(hi[jj]), make_float2(-1.f, -1.f), x[jj]);  // x - hi
+                        lo[jj] = pack_bf16(r2.x, r2.y);
+                    }
+                    // high parts of tokens s0.. at columns s0.., of s0+16.. at s0+8..; low parts 16 further
+                    tmem_st8x2(tmem + tlane + C::C_PB + (uint32_t)s0, hi);
+                    tmem_st8x2(tmem + tlane + C::C_PB + (uint32_t)(s0 + 16), lo);
+                }
+                tmem_st_wait();
             }
             tc_fence_before();
             bar_arrive(kBarPmask, kAllThreads);
@@ -848,27 +943,28 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
             tc_fence_after();
             if (has_w) wait(3);
             {
-                const int r = prow < 0 ? 0 : prow;
+                const int r = prow;
                 const float wr = wout[r];
-                uint32_t oa[32], oi[32];
-                tmem_ld32(tmem + tlane + C::C_OA + hf * 32, oa);
-                tmem_ld32(tmem + tlane + C::C_OI + hf * 32, oi);
+                uint32_t oa[OW], oi[OW];
+                tmem_ld_cols<OW>(tmem + tlane + C::C_OA + hf * 32, oa);
+                tmem_ld_cols<OW>(tmem + tlane + C::C_OI + hf * 32, oi);
                 tmem_ld_wait();
-                float o[32];
+                float o[OW];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
+                for (int jj = 0; jj < OW / 2; ++jj) {
                     const float2 v = __ffma2_rn(make_float2(wr, wr),
                                                 make_float2(__uint_as_float(oi[2 * jj]), __uint_as_float(oi[2 * jj + 1])),
                                                 make_float2(__uint_as_float(oa[2 * jj]), __uint_as_float(oa[2 * jj + 1])));
                     o[2 * jj] = v.x;
                     o[2 * jj + 1] = v.y;
                 }
-                if (prow >= 0) {
+                {
                     const uint32_t row = sbase + C::OFF_ZS + (uint32_t)(hf * TC * 128 + prow * 128);
+                    const int c0 = (ocol - hf * 32) / 4;  // this thread's first 16-byte chunk of the row
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        st_shared_v4(row + (uint32_t)((c ^ (prow & 7)) << 4), o[c * 4], o[c * 4 + 1], o[c * 4 + 2],
-                                     o[c * 4 + 3]);
+                    for (int c = 0; c < OW / 4; ++c)
+                        st_shared_v4(row + (uint32_t)(((c0 + c) ^ (prow & 7)) << 4), o[c * 4], o[c * 4 + 1],
+                                     o[c * 4 + 2], o[c * 4 + 3]);
                 }
                 fence_async_smem();
                 __syncwarp();
@@ -880,19 +976,22 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                                  sbase + C::OFF_ZS + (uint32_t)(hf * TC * 128 + q * WROWS * 128));
                     tma_store_commit();
                 }
-                if (has_w && prow >= 0 && t0 + prow < p.T) {
+                if (has_w) {
                     float dot = 0.f;
+                    if (t0 + prow < p.T) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint4 qq = *reinterpret_cast<const uint4 *>(smem + C::OFF_W + sw128(r, hf * 32 + c * 8));
-                        const uint32_t words[4] = {qq.x, qq.y, qq.z, qq.w};
+                        for (int c = 0; c < OW / 8; ++c) {
+                            const uint4 qq = *reinterpret_cast<const uint4 *>(smem + C::OFF_W + sw128(r, ocol + c * 8));
+                            const uint32_t words[4] = {qq.x, qq.y, qq.z, qq.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 fw = unpack_bf16(words[e]);
-                            dot = fmaf(o[c * 8 + 2 * e], fw.x, fmaf(o[c * 8 + 2 * e + 1], fw.y, dot));
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 fw = unpack_bf16(words[e]);
+                                dot = fmaf(o[c * 8 + 2 * e], fw.x, fmaf(o[c * 8 + 2 * e + 1], fw.y, dot));
+                            }
                         }
                     }
-                    dotp[hf * TC + r] = dot;
+                    if (TC == 64) dot += __shfl_xor_sync(0xffffffffu, dot, 16);  // the row's other 16 columns
+                    if ((TC == 128 || lane < 16) && t0 + prow < p.T) dotp[hf * TC + r] = dot;
                 }
             }
             __syncwarp();
@@ -903,7 +1002,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
             tc_fence_before();
             if (has_w) {
                 bar_sync(kBarMath, kMathThreads);
-                if (hf == 0 && prow >= 0 && t0 + prow < p.T)
+                if (hf == 0 && (TC == 128 || lane < 16) && t0 + prow < p.T)
                     p.wdot[((size_t)zb * p.BH + bh) * p.T + t0 + prow] = dotp[prow] + dotp[TC + prow];
             }
             bar_arrive(kBarDone, kAllThreads);
@@ -912,15 +1011,15 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
 
         // ---- final state of the sequence
         const bool last = REV ? (seg == 0) : (seg == p.n_seg - 1);
-        if (last && p.fs_mode == 1 && srow >= 0) {
+        if (last && p.fs_mode == 1) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) p.fs_out[((size_t)bh * DX + srow) * p.DZ + zb * 64 + hf * 32 + c] = S[c];
+            for (int c = 0; c < SW; ++c) p.fs_out[((size_t)bh * DX + srow) * p.DZ + zb * 64 + scol + c] = S[c];
         } else if (last && p.fs_mode == 2) {
             float acc = 0.f;
-            if (p.fs_dot != nullptr && srow >= 0) {
+            if (p.fs_dot != nullptr) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    acc = fmaf(S[c], p.fs_dot[((size_t)bh * p.DZ + zb * 64 + hf * 32 + c) * DX + srow], acc);
+                for (int c = 0; c < SW; ++c)
+                    acc = fmaf(S[c], p.fs_dot[((size_t)bh * p.DZ + zb * 64 + scol + c) * DX + srow], acc);
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
