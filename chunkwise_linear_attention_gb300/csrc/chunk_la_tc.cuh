@@ -306,10 +306,10 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
     auto chunk_at = [&](int i) { return REV ? (c_end - 1 - i) : (c_begin + i); };
     const bool has_w = p.W != nullptr;
     bool timed_out = false;
-    uint32_t ph[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    uint32_t ph = 0u;  // bit i: the phase parity mbarrier i completes next (a register, not an array)
     auto wait = [&](int i) {
-        if (!mbar_wait(bar(i), ph[i])) timed_out = true;
-        ph[i] ^= 1u;
+        if (!mbar_wait(bar(i), (ph >> i) & 1u)) timed_out = true;
+        ph ^= 1u << i;
     };
     // Decays are computed once per chunk visit, by the decay warp.  Visits are
     // numbered 0..2nc-1 (phase 1, then phase 2); visit n uses decay buffer
@@ -341,17 +341,22 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
         // Descriptors of every operand tile, built once; a K step adds a constant
         // byte offset (>> 4) to the start-address field.
         const uint64_t dX = smem_desc(sbase + C::OFF_X, 16, 1024);                  // K-major
-        const uint64_t dY[2] = {smem_desc(sbase + C::OFF_Y0, 16, 1024), smem_desc(sbase + C::OFF_Y1, 16, 1024)};
-        const uint64_t dYt[2] = {smem_desc(sbase + C::OFF_Y0, TC * 128, 1024),     // MN-major (Y^T)
-                                 smem_desc(sbase + C::OFF_Y1, TC * 128, 1024)};
-        const uint64_t dZ[2] = {smem_desc(sbase + C::OFF_Z0, 8192, 1024),          // MN-major
-                                smem_desc(sbase + C::OFF_Z1, 8192, 1024)};
+        // The two Y and Z buffers differ only in their start address: buffer b's descriptor is
+        // buffer 0's plus b times the buffer size (no arrays indexed at run time: those would
+        // live in local memory, a cache miss in front of an MMA issue).
+        const uint64_t dY0 = smem_desc(sbase + C::OFF_Y0, 16, 1024);                 // K-major
+        const uint64_t dYt0 = smem_desc(sbase + C::OFF_Y0, TC * 128, 1024);          // MN-major (Y^T)
+        const uint64_t dZ0 = smem_desc(sbase + C::OFF_Z0, 8192, 1024);               // MN-major
+        static_assert(C::OFF_Y1 - C::OFF_Y0 == C::X_BYTES && C::OFF_Z1 - C::OFF_Z0 == C::Z_BYTES, "buffer pairs");
+        auto dY = [&](int b) { return dY0 + (uint64_t)(b * (C::X_BYTES >> 4)); };
+        auto dYt = [&](int b) { return dYt0 + (uint64_t)(b * (C::X_BYTES >> 4)); };
+        auto dZ = [&](int b) { return dZ0 + (uint64_t)(b * (C::Z_BYTES >> 4)); };
         const uint64_t dS[2] = {smem_desc(sbase + C::OFF_SH, 8192, 1024), smem_desc(sbase + C::OFF_SL, 8192, 1024)};
         const uint64_t dZs = smem_desc(sbase + C::OFF_ZS, 16, 1024);               // K-major, 128 rows
         auto issue_state_mma = [&](int b) {
             // dS = Y^T [Zs_hi | Zs_lo]  (M = DX, N = 128, K = Tc)
             constexpr uint32_t id = idesc_bf16(DX, 128, 1, 0);
-            const uint64_t a0 = dYt[b];
+            const uint64_t a0 = dYt(b);
 #pragma unroll
             for (int kk = 0; kk < TC / 16; ++kk)
                 mma_ss_w(tmem + C::C_DS, a0 + (uint64_t)(kk * 2048 / 16),
@@ -359,7 +364,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
         };
         auto issue_p = [&](int b) {
             constexpr uint32_t idp = idesc_bf16(TC, TC, 0, 0);
-            const uint64_t b0 = dY[b];
+            const uint64_t b0 = dY(b);
 #pragma unroll
             for (int kk = 0; kk < DX / 16; ++kk) {
                 const uint64_t off = (uint64_t)(((kk >> 2) * TC * 128 + (kk & 3) * 32) / 16);
@@ -378,7 +383,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
         };
         auto issue_intra = [&](int b) {
             constexpr uint32_t id = idesc_bf16(TC, 64, 0, 1);
-            const uint64_t b0 = dZ[b];
+            const uint64_t b0 = dZ(b);
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
 #pragma unroll
@@ -792,14 +797,13 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                     }
                 };
                 // this warp's unmasked pieces (warp-uniform)
-                int pcs[PIECES];
-                int npc = 0;
-#pragma unroll
-                for (int pc = 0; pc < PIECES; ++pc)
-                    if (!piece_masked(hf * PIECES + pc)) pcs[npc++] = hf * PIECES + pc;
+                static_assert(PIECES == 2, "two 32-token pieces per warp at 128-token chunks");
+                const bool lo_masked = piece_masked(2 * hf), hi_masked = piece_masked(2 * hf + 1);
+                const int npc = (lo_masked ? 0 : 1) + (hi_masked ? 0 : 1);
+                const int first = lo_masked ? 2 * hf + 1 : 2 * hf;
 #pragma unroll 1
                 for (int k = 0; k < npc; ++k) {
-                    const int piece = (k == 0) ? pcs[0] : pcs[PIECES - 1];
+                    const int piece = (k == 0) ? first : 2 * hf + 1;
                     const int s0 = piece * 32;
                     float2 x[16];
                     uint32_t pr[32];
