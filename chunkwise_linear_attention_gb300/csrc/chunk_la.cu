@@ -102,6 +102,17 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&u);
     return __bfloat1622float2(v);
 }
+// x = hi + lo + e as two bf16x2 words, by truncation: hi holds the upper 16 bits of each
+// float (a bf16 rounded toward zero), the remainder x - hi is exact in fp32, and lo holds
+// its upper 16 bits; |e| < 2^-16 |x|.  Integer and paired-float operations only (no
+// conversion instructions); element .x goes to the low half of each word.
+__device__ __forceinline__ void split_bf16x2(float2 x, uint32_t &hi, uint32_t &lo) {
+    const uint32_t ux = __float_as_uint(x.x), uy = __float_as_uint(x.y);
+    hi = __byte_perm(ux, uy, 0x7632);
+    const float2 r = __ffma2_rn(make_float2(__uint_as_float(ux & 0xffff0000u), __uint_as_float(uy & 0xffff0000u)),
+                                make_float2(-1.f, -1.f), x);  // x - hi, exact
+    lo = __byte_perm(__float_as_uint(r.x), __float_as_uint(r.y), 0x7632);
+}
 
 // Byte offset of 16-byte chunk c16 of row `row` in a row-major tile with RB
 // bytes per row; chunks are XOR-swizzled by the row's low 3 bits so that the

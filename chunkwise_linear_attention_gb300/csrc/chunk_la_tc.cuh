@@ -10,14 +10,16 @@
 // where Zs = diag(w_state) Z and P is masked and decayed in registers between
 // the first and the last product, split into two bf16 parts and written back
 // to TMEM as the A operand.  OUT = O_intra + diag(w_out) O_inter, State =
-// alpha State + dS.
+// alpha State + dS.  A value x split into bf16 parts is x = hi + lo + e with
+// |e| < 2^-16 |x| (both parts by truncation, see split_bf16x2).
 //
-// Warp roles.  Warp 8 (the producer) issues every TMA load and, from one
-// lane, every MMA, so the tensor pipe works ahead of the elementwise stages
-// (the next chunk's P is formed while this chunk's output is written).
-// Warps 0..7 (the math warps) do the elementwise work: decays, Zs, masking,
-// the State recurrence and the output epilogue, which goes from registers
-// straight to global memory.  They hand work to the producer through named
+// Warp roles.  Warp 8 (the producer) issues every TMA load and every MMA
+// (warp-wide, under elect.sync), so the tensor pipe works ahead of the
+// elementwise stages (the next chunk's P is formed while this chunk's output
+// is written).  Warp 9 computes the decays of each chunk one visit ahead.
+// Warps 0..7 (the math warps) do the elementwise work: Zs, masking, the State
+// recurrence and the output epilogue, staged in shared memory and written by
+// one TMA store per warp.  They hand work to the producer through named
 // barriers and learn of finished MMAs and loads through mbarriers.  A math
 // warp w reads TMEM lane quarter w & 3 (the lanes a warp may access are fixed
 // by its rank within its warpgroup); warps w and w + 4 split the columns.
@@ -573,10 +575,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float2 x = __fmul2_rn(unpack_bf16(r[i]), w2);
-                    hi[i] = pack_bf16(x.x, x.y);
-                    const float2 rr = __ffma2_rn(unpack_bf16(hi[i]), make_float2(-1.f, -1.f), x);  // x - hi, exact
-                    lo[i] = pack_bf16(rr.x, rr.y);
+                    split_bf16x2(__fmul2_rn(unpack_bf16(r[i]), w2), hi[i], lo[i]);
                 }
                 const int nrow = (4 * (g4 & 1) + blk_in) * 8 + j;
                 const uint32_t off = (uint32_t)((tb * 8) >> 6) * 128 * 128 + sw128(nrow, (tb * 8) & 63);
@@ -607,10 +606,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    const float2 x = make_float2(S[c * 8 + 2 * h], S[c * 8 + 2 * h + 1]);
-                    hi[h] = pack_bf16(x.x, x.y);
-                    const float2 rr = __ffma2_rn(unpack_bf16(hi[h]), make_float2(-1.f, -1.f), x);  // x - hi, exact
-                    lo[h] = pack_bf16(rr.x, rr.y);
+                    split_bf16x2(make_float2(S[c * 8 + 2 * h], S[c * 8 + 2 * h + 1]), hi[h], lo[h]);
                 }
                 const uint32_t off = sw128(srow, scol + c * 8);
                 *reinterpret_cast<uint4 *>(smem + C::OFF_SH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -787,10 +783,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                         uint32_t hi[8], lo[8];
 #pragma unroll
                         for (int jj = 0; jj < 8; ++jj) {
-                            const float2 v = x[8 * h + jj];
-                            hi[jj] = pack_bf16(v.x, v.y);
-                            const float2 r2 = __ffma2_rn(unpack_bf16(hi[jj]), make_float2(-1.f, -1.f), v);  // v - hi, exact
-                            lo[jj] = pack_bf16(r2.x, r2.y);
+                            split_bf16x2(x[8 * h + jj], hi[jj], lo[jj]);
                         }
                         tmem_st8(tmem + tlane + C::C_PB + (uint32_t)(s0 + 8 * h), hi);
                         tmem_st8(tmem + tlane + C::C_PB + (uint32_t)(s0 + 16 + 8 * h), lo);
@@ -924,9 +917,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                     uint32_t hi[8], lo[8];
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj) {
-                        hi[jj] = pack_bf16(x[jj].x, x[jj].y);
-                        const float2 r2 = __ffma2_rn(unpack_bf16(hi[jj]), make_float2(-1.f, -1.f), x[jj]);  // x - hi
-                        lo[jj] = pack_bf16(r2.x, r2.y);
+                        split_bf16x2(x[jj], hi[jj], lo[jj]);
                     }
                     // high parts of tokens s0.. at columns s0.., of s0+16.. at s0+8..; low parts 16 further
                     tmem_st8x2(tmem + tlane + C::C_PB + (uint32_t)s0, hi);
