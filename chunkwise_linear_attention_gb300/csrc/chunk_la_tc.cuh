@@ -773,103 +773,21 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
             // ---- mask and decay P (fp32, TMEM) into its bf16 parts (TMEM)
             wait(4);
             tc_fence_after();
-            if constexpr (TC == 128) {
+            {
                 const int r = prow;
                 const float clr = cl[r];
                 const int zrr = zr[r];
-                auto store_parts = [&](int s0, float2 (&x)[16]) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t hi[8], lo[8];
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) {
-                            split_bf16x2(x[8 * h + jj], hi[jj], lo[jj]);
-                        }
-                        tmem_st8(tmem + tlane + C::C_PB + (uint32_t)(s0 + 8 * h), hi);
-                        tmem_st8(tmem + tlane + C::C_PB + (uint32_t)(s0 + 16 + 8 * h), lo);
-                    }
-                };
-                // this warp's unmasked pieces (warp-uniform)
-                static_assert(PIECES == 2, "two 32-token pieces per warp at 128-token chunks");
-                const bool lo_masked = piece_masked(2 * hf), hi_masked = piece_masked(2 * hf + 1);
-                const int npc = (lo_masked ? 0 : 1) + (hi_masked ? 0 : 1);
-                const int first = lo_masked ? 2 * hf + 1 : 2 * hf;
-#pragma unroll 1
-                for (int k = 0; k < npc; ++k) {
-                    const int piece = (k == 0) ? first : 2 * hf + 1;
-                    const int s0 = piece * 32;
-                    float2 x[16];
-                    uint32_t pr[32];
-                    tmem_ld32(tmem + tlane + C::C_P + (uint32_t)s0, pr);
-                    // the piece's per-token values, as 16-byte broadcast loads (same address in every lane)
-                    float cs[32];
-                    int zs[32];
-#pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
-                        const float4 g = *reinterpret_cast<const float4 *>((piece != rpiece ? gcol : cl) + s0 + 4 * c4);
-                        cs[4 * c4] = g.x;
-                        cs[4 * c4 + 1] = g.y;
-                        cs[4 * c4 + 2] = g.z;
-                        cs[4 * c4 + 3] = g.w;
-                        if (REV) {
-                            const int4 zv = *reinterpret_cast<const int4 *>(zr + s0 + 4 * c4);
-                            zs[4 * c4] = zv.x;
-                            zs[4 * c4 + 1] = zv.y;
-                            zs[4 * c4 + 2] = zv.z;
-                            zs[4 * c4 + 3] = zv.w;
-                        }
-                    }
-                    tmem_ld_wait();
-                    auto pv = [&](int j) { return make_float2(__uint_as_float(pr[2 * j]), __uint_as_float(pr[2 * j + 1])); };
-                    if (piece != rpiece) {
-                        // off-diagonal: row factor times column factor; without a reset between
-                        // the piece and the row (zr is nondecreasing) every product is kept
-                        const float f = REV ? ex2(cl[s0] - clr) : ex2(clr - cl[s0 + 31]);
-                        const float2 ff = make_float2(f, f);
-                        const bool all_keep = REV ? (zs[31] <= r) : (zrr <= s0);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            float2 v = __fmul2_rn(pv(j), __fmul2_rn(ff, make_float2(cs[2 * j], cs[2 * j + 1])));
-                            if (!all_keep) {
-                                const int sa = s0 + 2 * j;
-                                if (!(REV ? (zs[2 * j] <= r) : (zrr <= sa))) v.x = 0.f;
-                                if (!(REV ? (zs[2 * j + 1] <= r) : (zrr <= sa + 1))) v.y = 0.f;
-                            }
-                            x[j] = v;
-                        }
-                    } else {
-                        const float2 cc = make_float2(clr, clr);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            // decay exponent: cl_r - cl_s forward, cl_s - cl_r reversed
-                            const float2 cs2 = make_float2(cs[2 * j], cs[2 * j + 1]);
-                            const float2 arg = REV ? __ffma2_rn(cc, make_float2(-1.f, -1.f), cs2)
-                                                   : __ffma2_rn(cs2, make_float2(-1.f, -1.f), cc);
-                            float2 v = __fmul2_rn(pv(j), make_float2(ex2(arg.x), ex2(arg.y)));
-                            const int sa = s0 + 2 * j;
-                            if (!(REV ? (sa >= r && zs[2 * j] <= r) : (sa <= r && zrr <= sa))) v.x = 0.f;
-                            if (!(REV ? (sa + 1 >= r && zs[2 * j + 1] <= r) : (sa + 1 <= r && zrr <= sa + 1))) v.y = 0.f;
-                            x[j] = v;
-                        }
-                    }
-                    store_parts(s0, x);
-                }
-                tmem_st_wait();
-            } else {
-                // 64-row scores: lanes 0..15 hold this warp's 16 rows; threads 0..15 take tokens
-                // s0..s0+15 of the piece, threads 16..31 tokens s0+16..s0+31 (paired-half shapes)
-                const int r = prow;
-                const float clr = cl[r];
-                const int zrr = zr[r];
-                const int piece = hf;  // one 32-token piece per warp
-                if (!piece_masked(piece)) {
-                    const int s0 = piece * 32, tok0 = s0 + 16 * (lane >> 4);
-                    uint32_t pr[16];
-                    tmem_ld16x2(tmem + tlane + C::C_P + (uint32_t)s0, pr);
+                // Masks and decays 16 consecutive tokens tok0.. of a piece for row r (scores p16) and
+                // splits the results into bf16x2 parts.  Off-diagonal pieces take the row factor f
+                // times the column factors g; without a reset between the piece and the row (zr is
+                // nondecreasing) every product is kept (all_keep).  Half a piece at a time keeps the
+                // live registers low enough for the compiler to overlap the pairs.
+                auto mask16 = [&](const uint32_t(&p16)[16], int piece, int tok0, float f, bool all_keep,
+                                  uint32_t(&hi)[8], uint32_t(&lo)[8]) {
                     float cs[16];
                     int zs[16];
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
+                    for (int c4 = 0; c4 < 4; ++c4) {  // 16-byte broadcast loads (same address in every lane)
                         const float4 g = *reinterpret_cast<const float4 *>((piece != rpiece ? gcol : cl) + tok0 + 4 * c4);
                         cs[4 * c4] = g.x;
                         cs[4 * c4 + 1] = g.y;
@@ -883,13 +801,9 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                             zs[4 * c4 + 3] = zv.w;
                         }
                     }
-                    tmem_ld_wait();
-                    auto pv = [&](int j) { return make_float2(__uint_as_float(pr[2 * j]), __uint_as_float(pr[2 * j + 1])); };
-                    float2 x[8];
+                    auto pv = [&](int j) { return make_float2(__uint_as_float(p16[2 * j]), __uint_as_float(p16[2 * j + 1])); };
                     if (piece != rpiece) {
-                        const float f = REV ? ex2(cl[s0] - clr) : ex2(clr - cl[s0 + 31]);
                         const float2 ff = make_float2(f, f);
-                        const bool all_keep = REV ? (zr[s0 + 31] <= r) : (zrr <= s0);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             float2 v = __fmul2_rn(pv(j), __fmul2_rn(ff, make_float2(cs[2 * j], cs[2 * j + 1])));
@@ -898,12 +812,13 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                                 if (!(REV ? (zs[2 * j] <= r) : (zrr <= sa))) v.x = 0.f;
                                 if (!(REV ? (zs[2 * j + 1] <= r) : (zrr <= sa + 1))) v.y = 0.f;
                             }
-                            x[j] = v;
+                            split_bf16x2(v, hi[j], lo[j]);
                         }
                     } else {
                         const float2 cc = make_float2(clr, clr);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
+                            // decay exponent: cl_r - cl_s forward, cl_s - cl_r reversed
                             const float2 cs2 = make_float2(cs[2 * j], cs[2 * j + 1]);
                             const float2 arg = REV ? __ffma2_rn(cc, make_float2(-1.f, -1.f), cs2)
                                                    : __ffma2_rn(cs2, make_float2(-1.f, -1.f), cc);
@@ -911,19 +826,59 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                             const int sa = tok0 + 2 * j;
                             if (!(REV ? (sa >= r && zs[2 * j] <= r) : (sa <= r && zrr <= sa))) v.x = 0.f;
                             if (!(REV ? (sa + 1 >= r && zs[2 * j + 1] <= r) : (sa + 1 <= r && zrr <= sa + 1))) v.y = 0.f;
-                            x[j] = v;
+                            split_bf16x2(v, hi[j], lo[j]);
                         }
                     }
-                    uint32_t hi[8], lo[8];
+                };
+                auto piece_f = [&](int piece, int s0) {
+                    return piece == rpiece ? 0.f : (REV ? ex2(cl[s0] - clr) : ex2(clr - cl[s0 + 31]));
+                };
+                auto piece_keep = [&](int s0) { return REV ? (zr[s0 + 31] <= r) : (zrr <= s0); };
+                if constexpr (TC == 128) {
+                    // this warp's unmasked pieces (warp-uniform)
+                    static_assert(PIECES == 2, "two 32-token pieces per warp at 128-token chunks");
+                    const bool lo_masked = piece_masked(2 * hf), hi_masked = piece_masked(2 * hf + 1);
+                    const int npc = (lo_masked ? 0 : 1) + (hi_masked ? 0 : 1);
+                    const int first = lo_masked ? 2 * hf + 1 : 2 * hf;
+#pragma unroll 1
+                    for (int k = 0; k < npc; ++k) {
+                        const int piece = (k == 0) ? first : 2 * hf + 1;
+                        const int s0 = piece * 32;
+                        uint32_t pr[2][16];
+                        tmem_ld16(tmem + tlane + C::C_P + (uint32_t)s0, pr[0]);
+                        tmem_ld16(tmem + tlane + C::C_P + (uint32_t)(s0 + 16), pr[1]);
+                        const float f = piece_f(piece, s0);
+                        const bool all_keep = piece_keep(s0);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        split_bf16x2(x[jj], hi[jj], lo[jj]);
+                        for (int h = 0; h < 2; ++h) {
+                            // tokens s0 + 16h..: high parts at columns s0 + 8h.., low parts 16 further
+                            uint32_t hi[8], lo[8];
+                            mask16(pr[h], piece, s0 + 16 * h, f, all_keep, hi, lo);
+                            tmem_st8(tmem + tlane + C::C_PB + (uint32_t)(s0 + 8 * h), hi);
+                            tmem_st8(tmem + tlane + C::C_PB + (uint32_t)(s0 + 16 + 8 * h), lo);
+                        }
                     }
-                    // high parts of tokens s0.. at columns s0.., of s0+16.. at s0+8..; low parts 16 further
-                    tmem_st8x2(tmem + tlane + C::C_PB + (uint32_t)s0, hi);
-                    tmem_st8x2(tmem + tlane + C::C_PB + (uint32_t)(s0 + 16), lo);
+                    tmem_st_wait();
+                } else {
+                    // 64-row scores: lanes 0..15 hold this warp's 16 rows; threads 0..15 take tokens
+                    // s0..s0+15 of the piece, threads 16..31 tokens s0+16..s0+31 (paired-half shapes)
+                    const int piece = hf;  // one 32-token piece per warp
+                    if (!piece_masked(piece)) {
+                        const int s0 = piece * 32;
+                        uint32_t pr[16];
+                        tmem_ld16x2(tmem + tlane + C::C_P + (uint32_t)s0, pr);
+                        const float f = piece_f(piece, s0);
+                        const bool all_keep = piece_keep(s0);
+                        tmem_ld_wait();
+                        uint32_t hi[8], lo[8];
+                        mask16(pr, piece, s0 + 16 * (lane >> 4), f, all_keep, hi, lo);
+                        // high parts of tokens s0.. at columns s0.., of s0+16.. at s0+8..; low parts 16 further
+                        tmem_st8x2(tmem + tlane + C::C_PB + (uint32_t)s0, hi);
+                        tmem_st8x2(tmem + tlane + C::C_PB + (uint32_t)(s0 + 16), lo);
+                    }
+                    tmem_st_wait();
                 }
-                tmem_st_wait();
             }
             tc_fence_before();
             bar_arrive(kBarPmask, kAllThreads);
