@@ -167,6 +167,13 @@ struct LaArgs {
     float *alpha_ws;      // [n_seg][BH][nzb]
     float4 *agg;          // [unit][S_TILES][NT] float4
     float4 *incl;
+    // Incoming state of every segment, [n_seg][BH][DX][DZ] fp32 (tensor-core kernel only):
+    // written after the look-back when seg_out is set; when seg_in is set, read instead of
+    // running phase 1 and the look-back (seg_trans = 1: stored as [DZ][DX], i.e. the
+    // transposed state of another traversal).
+    float *seg_out;
+    const float *seg_in;
+    int seg_trans;
 };
 
 // ----------------------------------------------------------------- the kernel
@@ -808,7 +815,7 @@ __global__ void __launch_bounds__(kFinThreads) la_dlog_finalize_kernel(
 struct LaPlan {
     int TC, DXmax, n_chunks, seg_chunks, n_seg, nzb_max;
     size_t units;
-    size_t off_flags, off_alpha, off_agg, off_incl, off_qdq, off_kdk, off_fsp, off_tsum, total;
+    size_t off_flags, off_alpha, off_agg, off_incl, off_qdq, off_kdk, off_fsp, off_tsum, off_seg, total;
     int fin_tiles;
 };
 
@@ -841,7 +848,10 @@ LaPlan la_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chun
     p.off_tsum = align_up(p.off_fsp + (size_t)p.nzb_max * BH * 4, 256);
     p.fin_tiles = (int)((T + kFinTile - 1) / kFinTile);
     if (p.fin_tiles < 1) p.fin_tiles = 1;
-    p.total = align_up(p.off_tsum + (size_t)p.fin_tiles * BH * 4, 256);
+    // the backward's adjoint state entering each segment, written by the dV traversal and
+    // read (transposed) by the dK traversal: [n_seg][BH][dk][dv] fp32
+    p.off_seg = align_up(p.off_tsum + (size_t)p.fin_tiles * BH * 4, 256);
+    p.total = align_up(p.off_seg + (size_t)p.n_seg * BH * (size_t)dk * (size_t)dv * 4, 256);
     return p;
 }
 
@@ -1033,11 +1043,12 @@ extern "C" int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint
     a.DZ = (int)dim_v;
     a.nzb = (int)(dim_v / 64);
     a.ticket_slot = 1;
+    a.seg_out = reinterpret_cast<float *>(w + pl.off_seg);
     grid = (unsigned int)((size_t)pl.n_seg * BH * a.nzb);
     st = run_pass((int)dim_k, chunk, true, a, s, grid);
     if (st) return st;
 
-    // pass 3 (reverse order): dK = [(dO V^T) . D]^T Q + diag(gamma) V dS^T, carrying dS^T
+    // pass 3 (reverse order): dK = [(dO V^T) . D]^T Q + diag(gamma) V dS^T, with dS^T
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, pl.off_agg, s), fn);
     a = base_args(pl, ws, BH, T);
     a.X = reinterpret_cast<const bf16 *>(v);
@@ -1052,6 +1063,11 @@ extern "C" int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint
     a.DZ = (int)dim_k;
     a.nzb = (int)(dim_k / 64);
     a.ticket_slot = 2;
+    // its adjoint state is the transpose of pass 2's: each segment starts from the state pass 2
+    // saved (the tensor-core kernel skips its phase 1 and look-back; the mma.sync kernel, used
+    // when T is shorter than a chunk, recomputes it)
+    a.seg_in = reinterpret_cast<const float *>(w + pl.off_seg);
+    a.seg_trans = 1;
     grid = (unsigned int)((size_t)pl.n_seg * BH * a.nzb);
     st = run_pass((int)dim_v, chunk, true, a, s, grid);
     if (st) return st;

@@ -307,6 +307,10 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
     const size_t unit = ((size_t)seg * p.BH + bh) * p.nzb + zb;
     auto chunk_at = [&](int i) { return REV ? (c_end - 1 - i) : (c_begin + i); };
     const bool has_w = p.W != nullptr;
+    // With the segments' incoming states given (seg_in), phase 1 and the look-back are
+    // skipped: the chunk visits are those of phase 2 only, nc..2nc-1, and v0 is the first.
+    const bool skip1 = p.seg_in != nullptr;
+    const int v0 = skip1 ? nc : 0;
     bool timed_out = false;
     uint32_t ph = 0u;  // bit i: the phase parity mbarrier i completes next (a register, not an array)
     auto wait = [&](int i) {
@@ -318,7 +322,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
     // n & 1, whose full and empty mbarriers complete one phase per use: visit
     // n is use n >> 1 of its buffer.
     float *dec = reinterpret_cast<float *>(smem + C::OFF_DEC);
-    auto dbuf = [&](int n) { return dec + (n & 1) * C::DEC_STRIDE; };
+    auto dbuf = [&](int n) { return dec + ((n - v0) & 1) * C::DEC_STRIDE; };
     float *dotp = dec + 2 * C::DEC_STRIDE;  // [2][Tc] half-row dot products
 
     if (producer) {
@@ -397,11 +401,11 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
             }
         };
         // ---- phase 1: dS per chunk
-        if (leader) {
+        if (leader && !skip1) {
             issue_yz(0, chunk_at(0));
             if (nc > 1) issue_yz(1, chunk_at(1));
         }
-        for (int i = 0; i < nc; ++i) {
+        for (int i = 0; i < (skip1 ? 0 : nc); ++i) {
             const int b = i & 1;
             wait(1 + b);
             bar_sync(kBarZs, kAllThreads);
@@ -528,12 +532,12 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                 gcol[r] = REV ? ex2(v[k] - cl[r & ~31]) : ex2(cl[r | 31] - v[k]);
             }
             if (lane == 0) cl[5 * TC] = zL >= 0 ? 0.f : ex2(cL);
-            mbar_arrive(bar(8 + (n & 1)));  // all 32 lanes: release of this lane's writes
+            mbar_arrive(bar(8 + ((n - v0) & 1)));  // all 32 lanes: release of this lane's writes
         };
-        load_ell(0);
-        for (int n = 0; n < 2 * nc; ++n) {
-            const int use = n >> 1;
-            if (use > 0 && !mbar_wait(bar(10 + (n & 1)), (uint32_t)((use - 1) & 1))) timed_out = true;
+        load_ell(v0);
+        for (int n = v0; n < 2 * nc; ++n) {
+            const int use = (n - v0) >> 1;
+            if (use > 0 && !mbar_wait(bar(10 + ((n - v0) & 1)), (uint32_t)((use - 1) & 1))) timed_out = true;
             compute_decays(n);
             if (n + 1 < 2 * nc) load_ell(n + 1);
         }
@@ -555,7 +559,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
         const int scol = hf * 32 + ((DX == 128) ? 0 : (lane >> 4) * 16);  // of the 64 state columns
         const uint32_t tlane = (uint32_t)(q * 32) << 16;
         auto wait_dec = [&](int n) {
-            if (!mbar_wait(bar(8 + (n & 1)), (uint32_t)((n >> 1) & 1))) timed_out = true;
+            if (!mbar_wait(bar(8 + ((n - v0) & 1)), (uint32_t)(((n - v0) >> 1) & 1))) timed_out = true;
         };
 
         // Zs = diag(w_state) Z as two bf16 parts, K-major [64 rows n][Tc tokens]: 8x8 blocks of
@@ -616,7 +620,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
 
         // ---- phase 1
         float alpha_seg = 1.f;
-        for (int i = 0; i < nc; ++i) {
+        for (int i = 0; i < (skip1 ? 0 : nc); ++i) {
             const int b = i & 1;
             wait(1 + b);
             wait_dec(i);
@@ -670,7 +674,26 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
         float Sin[SW];
 #pragma unroll
         for (int c = 0; c < SW; ++c) Sin[c] = 0.f;
-        if (first) {
+        // a segment's incoming state in [n_seg][BH][rows][cols] (seg_trans = 0) or with rows and
+        // columns swapped (seg_trans = 1)
+        const size_t seg_base = ((size_t)seg * p.BH + bh) * (size_t)DX * p.DZ;
+        if (skip1) {
+            const int col0 = zb * 64 + scol;
+            if (p.seg_trans) {  // lanes read consecutive rows
+#pragma unroll
+                for (int c = 0; c < SW; ++c) Sin[c] = __ldg(p.seg_in + seg_base + (size_t)(col0 + c) * DX + srow);
+            } else {
+                const float4 *src = reinterpret_cast<const float4 *>(p.seg_in + seg_base + (size_t)srow * p.DZ + col0);
+#pragma unroll
+                for (int c4 = 0; c4 < SW / 4; ++c4) {
+                    const float4 f = __ldg(src + c4);
+                    Sin[4 * c4] = f.x;
+                    Sin[4 * c4 + 1] = f.y;
+                    Sin[4 * c4 + 2] = f.z;
+                    Sin[4 * c4 + 3] = f.w;
+                }
+            }
+        } else if (first) {
             load_state0(Sin, 1.f, false);
         } else {
 #pragma unroll
@@ -719,16 +742,24 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                 }
             }
         }
+        if (!skip1) {
 #pragma unroll
-        for (int c4 = 0; c4 < SW / 4; ++c4)
-            __stcg(inc4 + (scol / 4 + c4) * DX + srow,
-                   make_float4(fmaf(alpha_seg, Sin[4 * c4], S[4 * c4]), fmaf(alpha_seg, Sin[4 * c4 + 1], S[4 * c4 + 1]),
-                               fmaf(alpha_seg, Sin[4 * c4 + 2], S[4 * c4 + 2]),
-                               fmaf(alpha_seg, Sin[4 * c4 + 3], S[4 * c4 + 3])));
-        bar_sync(kBarMath, kMathThreads);
-        if (mtid == 0) {
-            __threadfence();
-            st_release(p.flags + unit, 2u);
+            for (int c4 = 0; c4 < SW / 4; ++c4)
+                __stcg(inc4 + (scol / 4 + c4) * DX + srow,
+                       make_float4(fmaf(alpha_seg, Sin[4 * c4], S[4 * c4]), fmaf(alpha_seg, Sin[4 * c4 + 1], S[4 * c4 + 1]),
+                                   fmaf(alpha_seg, Sin[4 * c4 + 2], S[4 * c4 + 2]),
+                                   fmaf(alpha_seg, Sin[4 * c4 + 3], S[4 * c4 + 3])));
+            bar_sync(kBarMath, kMathThreads);
+            if (mtid == 0) {
+                __threadfence();
+                st_release(p.flags + unit, 2u);
+            }
+            if (p.seg_out != nullptr) {  // this segment's incoming state, for a later traversal
+                float4 *dst = reinterpret_cast<float4 *>(p.seg_out + seg_base + (size_t)srow * p.DZ + zb * 64 + scol);
+#pragma unroll
+                for (int c4 = 0; c4 < SW / 4; ++c4)
+                    dst[c4] = make_float4(Sin[4 * c4], Sin[4 * c4 + 1], Sin[4 * c4 + 2], Sin[4 * c4 + 3]);
+            }
         }
 
         // ---- phase 2
@@ -945,7 +976,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(10 + ((nc + i) & 1)));  // done with this visit's decays
+            if (lane == 0) mbar_arrive(bar(10 + ((nc + i - v0) & 1)));  // done with this visit's decays
             // State's bf16 parts for the next chunk (this chunk's O_inter has consumed them)
             write_s_smem();
             fence_async_smem();
