@@ -271,9 +271,10 @@ def bench_scan(torch, cla, workloads, dev, steps, warmup, dist_on):
 
 
 # ------------------------------------------------------------------ other workloads
-def _time_calls(torch, fn, flush, iters):
+def _time_calls(torch, fn, flush, iters, warmup=3):
     stream = torch.cuda.current_stream()
-    fn()
+    for _ in range(warmup):
+        fn()
     torch.cuda.synchronize()
     ts = []
     for _ in range(iters):
@@ -330,9 +331,13 @@ def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=5, sha
     g = [torch.empty(B, H, T, d, device=dev) for _ in range(3)]
     dl = torch.empty(B, H, T, device=dev)
     dS0 = torch.empty(B, H, d, d, device=dev)
-    fwd = lambda: cla.chunk_la_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], chunk=chunk, o=o, ST=ST, workspace=ws)
+    # training step: the forward saves the state entering each segment, the backward starts
+    # its forward-order traversal from them
+    ck = cla.chunk_la_ckpt(t["q"], t["v"], chunk=chunk)
+    fwd = lambda: cla.chunk_la_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], chunk=chunk, o=o, ST=ST, ckpt=ck,
+                                   workspace=ws)
     bwd = lambda: cla.chunk_la_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"], chunk=chunk, dq=g[0],
-                                   dk=g[1], dv=g[2], dlog_decay=dl, dS0=dS0, workspace=ws)
+                                   dk=g[1], dv=g[2], dlog_decay=dl, dS0=dS0, ckpt=ck, workspace=ws)
     tf = _time_calls(torch, fwd, flush, iters)
     tb = _time_calls(torch, bwd, flush, iters)
     cla.check_status(ws)
@@ -352,8 +357,9 @@ def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=5, sha
            "fwd_GBps": round(by_f / (tf / 1e3) / 1e9, 1), "bwd_GBps": round(by_b / (tb / 1e3) / 1e9, 1),
            "frac_bf16_peak": round((fl_f + fl_b) / tot / bf, 4),
            "frac_binding_roofline": round(max(roof) / tot, 4),
-           "binding": "hbm" if roof[0] >= roof[1] else "tensor"}
-    del t, ws, o, g
+           "binding": "hbm" if roof[0] >= roof[1] else "tensor",
+           "ckpt_bytes": cla.chunk_la_ckpt_size(B, H, T, d, d, chunk)}
+    del t, ws, o, g, ck
     torch.cuda.empty_cache()
     return res
 

@@ -60,6 +60,9 @@ def lib():
                 "cla_chunk_la_workspace_size": ([I64] * 5 + [INT], SZ),
                 "cla_chunk_la_fwd": ([P] * 7 + [I64] * 5 + [INT, P, SZ, P], INT),
                 "cla_chunk_la_bwd": ([P] * 12 + [I64] * 5 + [INT, P, SZ, P], INT),
+                "cla_chunk_la_ckpt_size": ([I64] * 5 + [INT], SZ),
+                "cla_chunk_la_fwd_ckpt": ([P] * 8 + [I64] * 5 + [INT, P, SZ, P], INT),
+                "cla_chunk_la_bwd_ckpt": ([P] * 13 + [I64] * 5 + [INT, P, SZ, P], INT),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -243,8 +246,31 @@ def chunk_la_workspace_size(B, H, T, dim_k, dim_v, chunk) -> int:
     return int(lib().cla_chunk_la_workspace_size(B, H, T, dim_k, dim_v, int(chunk)))
 
 
-def chunk_la_fwd(q, k, v, log_decay, S0=None, *, chunk=64, o=None, ST=None, workspace=None, stream=None):
-    """Chunkwise decayed linear attention forward; returns (o, ST)."""
+def chunk_la_ckpt_size(B, H, T, dim_k, dim_v, chunk) -> int:
+    """Bytes of the segment-state checkpoint the forward can save for the backward."""
+    return int(lib().cla_chunk_la_ckpt_size(B, H, T, dim_k, dim_v, int(chunk)))
+
+
+def chunk_la_ckpt(q, v, *, chunk=64):
+    """A device buffer (fp32) for the checkpoint of a forward on q [B, H, T, dk], v [.., dv]."""
+    B, H, T, dk = q.shape
+    n = chunk_la_ckpt_size(B, H, T, dk, v.shape[-1], chunk) // 4
+    return torch.empty(max(n, 1), dtype=torch.float32, device=q.device)
+
+
+def _ckpt_ptr(ckpt, B, H, T, dk, dv, chunk):
+    if ckpt is None:
+        return None
+    need = chunk_la_ckpt_size(B, H, T, dk, dv, chunk)
+    if ckpt.numel() * ckpt.element_size() < need:
+        raise ValueError(f"ckpt: need at least {need} bytes, got {ckpt.numel() * ckpt.element_size()}")
+    return _ptr(ckpt, torch.float32, "ckpt")
+
+
+def chunk_la_fwd(q, k, v, log_decay, S0=None, *, chunk=64, o=None, ST=None, ckpt=None, workspace=None,
+                 stream=None):
+    """Chunkwise decayed linear attention forward; returns (o, ST).  With ckpt (see
+    chunk_la_ckpt) it also saves the state entering each segment for chunk_la_bwd."""
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     dev = q.device
@@ -252,16 +278,21 @@ def chunk_la_fwd(q, k, v, log_decay, S0=None, *, chunk=64, o=None, ST=None, work
     o = _out(o, (B, H, T, dv), f32, dev)
     ST = _out(ST, (B, H, dk, dv), f32, dev)
     ws = _ws(chunk_la_workspace_size(B, H, T, dk, dv, chunk), dev, workspace)
-    _check("cla_chunk_la_fwd", lib().cla_chunk_la_fwd(
-        _ptr(q, bf16, "q"), _ptr(k, bf16, "k"), _ptr(v, bf16, "v"), _ptr(log_decay, f32, "log_decay"),
-        _ptr(S0, f32, "S0"), _ptr(o, f32, "o"), _ptr(ST, f32, "ST"), B, H, T, dk, dv, int(chunk),
-        _ptr(ws), ws.numel(), _stream(stream)))
+    args = (_ptr(q, bf16, "q"), _ptr(k, bf16, "k"), _ptr(v, bf16, "v"), _ptr(log_decay, f32, "log_decay"),
+            _ptr(S0, f32, "S0"), _ptr(o, f32, "o"), _ptr(ST, f32, "ST"))
+    tail = (B, H, T, dk, dv, int(chunk), _ptr(ws), ws.numel(), _stream(stream))
+    if ckpt is None:
+        _check("cla_chunk_la_fwd", lib().cla_chunk_la_fwd(*args, *tail))
+    else:
+        _check("cla_chunk_la_fwd_ckpt", lib().cla_chunk_la_fwd_ckpt(
+            *args, _ckpt_ptr(ckpt, B, H, T, dk, dv, chunk), *tail))
     return o, ST
 
 
 def chunk_la_bwd(q, k, v, log_decay, S0, dO, dST=None, *, chunk=64, dq=None, dk=None, dv=None,
-                 dlog_decay=None, dS0=None, workspace=None, stream=None):
-    """Chunkwise decayed linear attention backward; returns (dq, dk, dv, dlog_decay, dS0)."""
+                 dlog_decay=None, dS0=None, ckpt=None, workspace=None, stream=None):
+    """Chunkwise decayed linear attention backward; returns (dq, dk, dv, dlog_decay, dS0).  ckpt:
+    the checkpoint a chunk_la_fwd on the same inputs saved (its states are then not rebuilt)."""
     B, H, T, dkk = q.shape
     dvv = v.shape[-1]
     dev = q.device
@@ -272,9 +303,13 @@ def chunk_la_bwd(q, k, v, log_decay, S0, dO, dST=None, *, chunk=64, dq=None, dk=
     dlog_decay = _out(dlog_decay, (B, H, T), f32, dev)
     dS0 = _out(dS0, (B, H, dkk, dvv), f32, dev)
     ws = _ws(chunk_la_workspace_size(B, H, T, dkk, dvv, chunk), dev, workspace)
-    _check("cla_chunk_la_bwd", lib().cla_chunk_la_bwd(
-        _ptr(q, bf16, "q"), _ptr(k, bf16, "k"), _ptr(v, bf16, "v"), _ptr(log_decay, f32, "log_decay"),
-        _ptr(S0, f32, "S0"), _ptr(dO, bf16, "dO"), _ptr(dST, f32, "dST"), _ptr(dq, f32, "dq"),
-        _ptr(dk, f32, "dk"), _ptr(dv, f32, "dv"), _ptr(dlog_decay, f32, "dlog_decay"),
-        _ptr(dS0, f32, "dS0"), B, H, T, dkk, dvv, int(chunk), _ptr(ws), ws.numel(), _stream(stream)))
+    args = (_ptr(q, bf16, "q"), _ptr(k, bf16, "k"), _ptr(v, bf16, "v"), _ptr(log_decay, f32, "log_decay"),
+            _ptr(S0, f32, "S0"), _ptr(dO, bf16, "dO"), _ptr(dST, f32, "dST"), _ptr(dq, f32, "dq"),
+            _ptr(dk, f32, "dk"), _ptr(dv, f32, "dv"), _ptr(dlog_decay, f32, "dlog_decay"), _ptr(dS0, f32, "dS0"))
+    tail = (B, H, T, dkk, dvv, int(chunk), _ptr(ws), ws.numel(), _stream(stream))
+    if ckpt is None:
+        _check("cla_chunk_la_bwd", lib().cla_chunk_la_bwd(*args, *tail))
+    else:
+        _check("cla_chunk_la_bwd_ckpt", lib().cla_chunk_la_bwd_ckpt(
+            *args, _ckpt_ptr(ckpt, B, H, T, dkk, dvv, chunk), *tail))
     return dq, dk, dv, dlog_decay, dS0

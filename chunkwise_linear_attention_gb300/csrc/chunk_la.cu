@@ -932,11 +932,19 @@ extern "C" size_t cla_chunk_la_workspace_size(int64_t B, int64_t H, int64_t T, i
     return la_plan(B, H, T, dim_k, dim_v, chunk).total;
 }
 
-extern "C" int cla_chunk_la_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
-                                const float *S0, float *o, float *ST, int64_t B, int64_t H, int64_t T,
-                                int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
+extern "C" size_t cla_chunk_la_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
+                                         int chunk) {
+    if (B < 0 || H < 0 || T < 0 || dim_k <= 0 || dim_v <= 0 || chunk <= 0) return 0;
+    const LaPlan pl = la_plan(B, H, T, dim_k, dim_v, chunk);
+    return (size_t)pl.n_seg * (size_t)(B * H) * (size_t)dim_k * (size_t)dim_v * sizeof(float);
+}
+
+namespace {
+int chunk_la_fwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const float *log_decay, const float *S0, float *o, float *ST, float *ckpt, int64_t B,
+                      int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes,
+                      void *stream) {
     clear_error();
-    const char *fn = "cla_chunk_la_fwd";
     int st = la_validate(fn, B, H, T, dim_k, dim_v, chunk);
     if (st) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -954,6 +962,7 @@ extern "C" int cla_chunk_la_fwd(const uint16_t *q, const uint16_t *k, const uint
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
         return fail(CLA_ERR_INVALID_ARG, "%s: q, k, v, o must be 16-byte aligned", fn);
     if (!ws || !aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace NULL or unaligned", fn);
+    if (ckpt && !aligned16(ckpt)) return fail(CLA_ERR_INVALID_ARG, "%s: ckpt must be 16-byte aligned", fn);
     const LaPlan pl = la_plan(B, H, T, dim_k, dim_v, chunk);
     if (ws_bytes < pl.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, pl.total);
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, pl.off_agg, s), fn);
@@ -970,16 +979,17 @@ extern "C" int cla_chunk_la_fwd(const uint16_t *q, const uint16_t *k, const uint
     a.DZ = (int)dim_v;
     a.nzb = (int)(dim_v / 64);
     a.ticket_slot = 0;
+    a.seg_out = ckpt;  // [n_seg][BH][dim_k][dim_v]: the state entering each segment
     const unsigned int grid = (unsigned int)((size_t)pl.n_seg * BH * a.nzb);
     return run_pass((int)dim_k, chunk, false, a, s, grid);
 }
 
-extern "C" int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
-                                const float *S0, const uint16_t *dO, const float *dST, float *dq, float *dk,
-                                float *dv, float *dlog_decay, float *dS0, int64_t B, int64_t H, int64_t T,
-                                int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
+int chunk_la_bwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const float *log_decay, const float *S0, const uint16_t *dO, const float *dST, float *dq,
+                      float *dk, float *dv, float *dlog_decay, float *dS0, const float *ckpt, int64_t B, int64_t H,
+                      int64_t T, int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes,
+                      void *stream) {
     clear_error();
-    const char *fn = "cla_chunk_la_bwd";
     int st = la_validate(fn, B, H, T, dim_k, dim_v, chunk);
     if (st) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -999,6 +1009,7 @@ extern "C" int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint
         !aligned16(dv))
         return fail(CLA_ERR_INVALID_ARG, "%s: bf16 tensors must be 16-byte aligned", fn);
     if (!ws || !aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace NULL or unaligned", fn);
+    if (ckpt && !aligned16(ckpt)) return fail(CLA_ERR_INVALID_ARG, "%s: ckpt must be 16-byte aligned", fn);
     const LaPlan pl = la_plan(B, H, T, dim_k, dim_v, chunk);
     if (ws_bytes < pl.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, pl.total);
     char *w = static_cast<char *>(ws);
@@ -1024,6 +1035,10 @@ extern "C" int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint
     a.DZ = (int)dim_k;
     a.nzb = (int)(dim_k / 64);
     a.ticket_slot = 0;
+    // its state is the transpose of the forward's: with the forward's checkpoint each segment
+    // starts from the saved state (no phase 1, no look-back)
+    a.seg_in = ckpt;
+    a.seg_trans = 1;
     unsigned int grid = (unsigned int)((size_t)pl.n_seg * BH * a.nzb);
     st = run_pass((int)dim_v, chunk, false, a, s, grid);
     if (st) return st;
@@ -1085,4 +1100,37 @@ extern "C" int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint
         st = check_launch("la_dlog_finalize_kernel");
     }
     return st;
+}
+}  // namespace
+
+extern "C" int cla_chunk_la_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                                const float *S0, float *o, float *ST, int64_t B, int64_t H, int64_t T,
+                                int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
+    return chunk_la_fwd_impl("cla_chunk_la_fwd", q, k, v, log_decay, S0, o, ST, nullptr, B, H, T, dim_k, dim_v,
+                             chunk, ws, ws_bytes, stream);
+}
+
+extern "C" int cla_chunk_la_fwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                     const float *log_decay, const float *S0, float *o, float *ST, float *ckpt,
+                                     int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk,
+                                     void *ws, size_t ws_bytes, void *stream) {
+    return chunk_la_fwd_impl("cla_chunk_la_fwd_ckpt", q, k, v, log_decay, S0, o, ST, ckpt, B, H, T, dim_k, dim_v,
+                             chunk, ws, ws_bytes, stream);
+}
+
+extern "C" int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                                const float *S0, const uint16_t *dO, const float *dST, float *dq, float *dk,
+                                float *dv, float *dlog_decay, float *dS0, int64_t B, int64_t H, int64_t T,
+                                int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
+    return chunk_la_bwd_impl("cla_chunk_la_bwd", q, k, v, log_decay, S0, dO, dST, dq, dk, dv, dlog_decay, dS0,
+                             nullptr, B, H, T, dim_k, dim_v, chunk, ws, ws_bytes, stream);
+}
+
+extern "C" int cla_chunk_la_bwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                     const float *log_decay, const float *S0, const uint16_t *dO,
+                                     const float *dST, float *dq, float *dk, float *dv, float *dlog_decay,
+                                     float *dS0, const float *ckpt, int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                                     int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
+    return chunk_la_bwd_impl("cla_chunk_la_bwd_ckpt", q, k, v, log_decay, S0, dO, dST, dq, dk, dv, dlog_decay,
+                             dS0, ckpt, B, H, T, dim_k, dim_v, chunk, ws, ws_bytes, stream);
 }

@@ -256,6 +256,43 @@ int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                      int64_t T, int64_t dim_k, int64_t dim_v, int chunk,
                      void *ws, size_t ws_bytes, void *stream);
 
+/* Storing chunk states instead of rebuilding them ("Parallel Scan", "The
+ * backward pass is a scan in reverse": the backward needs the forward's
+ * states, which can be stored or recomputed from the inputs).  The library
+ * splits each sequence into segments of chunks; the forward forms the state
+ * entering every segment anyway, and the backward's forward-order traversal
+ * (the one that gives dQ) needs exactly those states.
+ *
+ * Bytes of that checkpoint for these sizes: n_seg * B * H * dim_k * dim_v
+ * fp32 values, n_seg fixed by the sizes and the chunk.  0 for invalid sizes. */
+size_t cla_chunk_la_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                              int64_t dim_v, int chunk);
+
+/* cla_chunk_la_fwd that also writes the checkpoint: ckpt (device,
+ * cla_chunk_la_ckpt_size bytes, 16-byte aligned, owned by the caller) gets
+ * the state entering each segment.  ckpt = NULL is the plain forward.  When
+ * T is shorter than one chunk nothing is written (the backward then rebuilds
+ * its states itself). */
+int cla_chunk_la_fwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const float *log_decay, const float *S0, float *o,
+                          float *ST, float *ckpt, int64_t B, int64_t H, int64_t T,
+                          int64_t dim_k, int64_t dim_v, int chunk, void *ws,
+                          size_t ws_bytes, void *stream);
+
+/* cla_chunk_la_bwd that starts its forward-order traversal from the
+ * checkpoint written by cla_chunk_la_fwd_ckpt with the same q, k, v,
+ * log_decay, S0, sizes and chunk (read only; the results are those of
+ * cla_chunk_la_bwd up to fp32 rounding).  ckpt = NULL rebuilds the states
+ * (cla_chunk_la_bwd).  A checkpoint from other inputs gives wrong gradients;
+ * nothing checks it. */
+int cla_chunk_la_bwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const float *log_decay, const float *S0, const uint16_t *dO,
+                          const float *dST, float *dq, float *dk, float *dv,
+                          float *dlog_decay, float *dS0, const float *ckpt,
+                          int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                          int64_t dim_v, int chunk, void *ws, size_t ws_bytes,
+                          void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,11 +26,15 @@ def _dev(x):
     return None if x is None else x.cuda()
 
 
-def _check(cla, inp, chunk, dST=None, heads=None, check_bwd=True):
+def _check(cla, inp, chunk, dST=None, heads=None, check_bwd=True, ckpt=False):
+    """ckpt: the forward saves its segment states and the backward starts from them (the
+    training-step path the benchmark times)."""
     t = {k: _dev(v) for k, v in inp.items()}
-    o, ST = cla.chunk_la_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], chunk=chunk)
+    cp = cla.chunk_la_ckpt(t["q"], t["v"], chunk=chunk) if ckpt else None
+    o, ST = cla.chunk_la_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], chunk=chunk, ckpt=cp)
     if check_bwd:
-        g = cla.chunk_la_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"], _dev(dST), chunk=chunk)
+        g = cla.chunk_la_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"], _dev(dST), chunk=chunk,
+                             ckpt=cp)
     torch.cuda.synchronize()
     sel = (lambda x: x) if heads is None else (lambda x: None if x is None else x[:, heads])
     ci = {k: sel(v) for k, v in inp.items()}
@@ -101,16 +105,52 @@ def test_chunk_la_empty(cla):
 
 
 def test_chunk_la_constant_decay_workload_full(cla):
-    """4 x 16 x 8192, d = 64, chunk 64, every output element."""
+    """4 x 16 x 8192, d = 64, chunk 64, every output element (forward saving its
+    segment states, backward starting from them, as the benchmark runs it)."""
     inp = workloads.make("la_const")
-    _check(cla, inp, 64)
+    _check(cla, inp, 64, ckpt=True)
 
 
 def test_chunk_la_long_workload_sampled_heads(cla):
     """1 x 32 x 65536, d = 128, chunk 128 on the GPU; heads 0 and 31 against
-    the oracle (heads are independent problems)."""
+    the oracle (heads are independent problems); the benchmark's path, with the
+    forward's segment states."""
     inp = workloads.make("la_long")
-    _check(cla, inp, 128, heads=[0, 31])
+    _check(cla, inp, 128, heads=[0, 31], ckpt=True)
+
+
+@pytest.mark.parametrize("B,H,T,d,chunk", [
+    (1, 2, 40, 64, 64), (1, 1, 3000, 64, 64), (1, 2, 700, 64, 128), (1, 1, 2000, 128, 128),
+    (1, 1, 500, 128, 64), (2, 1, 129, 128, 128),
+])
+def test_chunk_la_ckpt(cla, B, H, T, d, chunk):
+    """The backward started from the forward's saved segment states: against the
+    oracle, and against the backward that rebuilds the states (equal up to fp32
+    rounding: the two build the same states with the operands' roles swapped).
+    T = 40 is shorter than a chunk: nothing is saved and the backward rebuilds."""
+    inp = workloads.make("la_long", B=B, H=H, T=T, dk=d, dv=d)
+    rng = np.random.default_rng(T * 7 + d)
+    dST = torch.from_numpy(rng.normal(0, 0.1, (B, H, d, d)).astype(np.float32))
+    _check(cla, inp, chunk, dST, ckpt=True)
+    t = {k: _dev(v) for k, v in inp.items()}
+    cp = cla.chunk_la_ckpt(t["q"], t["v"], chunk=chunk)
+    cla.chunk_la_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], chunk=chunk, ckpt=cp)
+    with_ck = cla.chunk_la_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"], _dev(dST), chunk=chunk,
+                               ckpt=cp)
+    rebuilt = cla.chunk_la_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"], _dev(dST), chunk=chunk)
+    torch.cuda.synchronize()
+    for name, x, r in zip(("dq", "dk", "dv", "dlog_a", "dS0"), with_ck, rebuilt):
+        rms = float(torch.sqrt(torch.mean(r.double() ** 2)))
+        err = float(torch.max(torch.abs(x.double() - r.double()))) / max(rms, 1e-30)
+        assert err <= 1e-4, f"{name}: checkpointed backward differs from the rebuilding one by {err:.2e} rms"
+
+
+def test_chunk_la_ckpt_rejects_short_buffer(cla):
+    inp = workloads.make("la_long", B=1, H=1, T=300, dk=64, dv=64)
+    t = {k: _dev(v) for k, v in inp.items()}
+    with pytest.raises(ValueError):
+        cla.chunk_la_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], chunk=64,
+                         ckpt=torch.empty(4, dtype=torch.float32, device="cuda"))
 
 
 @pytest.mark.parametrize("d,chunk", [(128, 128), (64, 128), (128, 64)])
@@ -139,7 +179,8 @@ def test_chunk_la_strong_decay(cla, d, chunk):
 
 
 def test_chunk_la_long_workload_chunk64_sampled_heads(cla):
-    """1 x 32 x 65536, d = 128, chunk 64 (segments of 32 chunks) on the GPU;
-    heads 5 and 20 against the oracle."""
+    """1 x 32 x 65536, d = 128, chunk 64 (segments of 64 chunks) on the GPU;
+    heads 5 and 20 against the oracle (with the forward's segment states, as
+    the benchmark runs it)."""
     inp = workloads.make("la_long")
-    _check(cla, inp, 64, heads=[5, 20])
+    _check(cla, inp, 64, heads=[5, 20], ckpt=True)
