@@ -35,7 +35,7 @@ namespace {
 
 constexpr int kSub = 8;      // runs per chunk (lanes along time)
 constexpr int kCg = 4;       // lanes along channels
-constexpr int kWarps = 8;    // warps per block
+constexpr int kWarps = 4;    // warps per block (4 blocks per SM forward, 3 backward: measured best)
 constexpr int kL = 8;        // steps per run
 constexpr int kTc = kSub * kL;  // steps per chunk
 
@@ -158,7 +158,7 @@ __device__ __forceinline__ size_t unit_index(const ScanGeom &g, int chunk, int b
 // (3 rounds, every run combines) or a Blelloch up-sweep / down-sweep (6 rounds,
 // fewer combines), the latter kept as a measured alternative.
 template <int VEC, bool BLELLOCH = false>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+__global__ void __launch_bounds__(kWarps * 32, 4)
 scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
                      const float *__restrict__ h0, float *__restrict__ h,
                      float *__restrict__ hT, ScanGeom g, ScanWs ws) {
@@ -324,7 +324,7 @@ scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
 // (a'_{T-1} = 1 and g_{T-1} includes dhT), i.e. the forward scan on reversed
 // arrays with the decays shifted by one place.
 template <int VEC>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+__global__ void __launch_bounds__(kWarps * 32, 3)
 scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0,
                      const float *__restrict__ h, const float *__restrict__ dh,
                      const float *__restrict__ dhT, float *__restrict__ da,
