@@ -229,8 +229,8 @@ size_t cla_chunk_la_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_
  *   o          [B, H, T, dim_v] fp32 out (the accumulation precision: bf16
  *              rounding of the output alone would exceed the parity tolerance)
  *   ST         [B, H, dim_k, dim_v] fp32 [opt] out: S_T
- * Supported: dim_k = dim_v in {64, 128}, chunk in {64, 128}; any T >= 0 (the
- * last chunk may be shorter). */
+ * Supported: dim_k and dim_v each in {64, 128}, chunk in {64, 128}; any
+ * T >= 0 (the last chunk may be shorter). */
 int cla_chunk_la_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                      const float *log_decay, const float *S0, float *o,
                      float *ST, int64_t B, int64_t H, int64_t T, int64_t dim_k,

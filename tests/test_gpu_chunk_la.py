@@ -184,3 +184,14 @@ def test_chunk_la_long_workload_chunk64_sampled_heads(cla):
     the benchmark runs it)."""
     inp = workloads.make("la_long")
     _check(cla, inp, 64, heads=[5, 20], ckpt=True)
+
+
+@pytest.mark.parametrize("dk,dv,chunk", [(64, 128, 128), (128, 64, 64), (128, 64, 128)])
+@pytest.mark.parametrize("ckpt", [False, True])
+def test_chunk_la_unequal_head_dims(cla, dk, dv, chunk, ckpt):
+    """dim_k != dim_v: the forward's state is dim_k x dim_v, the dQ traversal's
+    its transpose (dim_v rows), the dK traversal's the adjoint's transpose."""
+    inp = workloads.make("la_long", B=1, H=2, T=700, dk=dk, dv=dv)
+    rng = np.random.default_rng(dk * 3 + dv)
+    dST = torch.from_numpy(rng.normal(0, 0.1, (1, 2, dk, dv)).astype(np.float32))
+    _check(cla, inp, chunk, dST, ckpt=ckpt)
