@@ -1,0 +1,99 @@
+"""Maximum sizes: tensors of more than 2^31 elements (64-bit index arithmetic in every
+kernel, look-back unit and tensor-map coordinate), checked against the oracle on slices.
+
+Inputs are drawn on the device (same distributions as the workloads, seeded) since the
+host would take minutes; the oracle reads the slices it checks back from the device."""
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._parity import assert_bf16, assert_fp32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cla():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import chunkwise_linear_attention_gb300 as m
+
+    m.lib()
+    return m
+
+
+def test_scan_diag_beyond_int32_elements(cla):
+    """B=1, T = 2^21 + 71 (a ragged last chunk), D = 1024: 2^31 + 72704 elements per tensor.
+    Channels are independent, so three whole channels (every step) are checked."""
+    dev = torch.device("cuda")
+    B, T, D = 1, (1 << 21) + 71, 1024
+    inp = workloads.scan_inputs_device(B, T, D, seed=21, device=dev)
+    a, b, h0, dh = inp["a"], inp["b"], inp["h0"], inp["dh"]
+    h, hT = cla.scan_diag_fwd(a, b, h0)
+    da, db, dh0 = cla.scan_diag_bwd(a, h0, h, dh)
+    torch.cuda.synchronize()
+    ch = [0, 517, 1023]
+    sub = lambda x: x[..., ch].contiguous().cpu()
+    ra, rb, rh0, rdh = sub(a), sub(b), sub(h0), sub(dh)
+    rh, rhT = oracle.scan_diag_fwd(ra, rb, rh0)
+    rda, rdb, rdh0 = oracle.scan_diag_bwd(ra, rb, rh0, rdh)
+    assert_fp32("h", sub(h), rh)
+    assert_fp32("hT", sub(hT), rhT)
+    assert_fp32("da", sub(da), rda)
+    assert_fp32("db", sub(db), rdb)
+    assert_fp32("dh0", sub(dh0), rdh0)
+
+
+def test_chunk_la_beyond_int32_elements(cla):
+    """B=1, H=16, T = 2^20 + 100, d = 128, chunk 128: 2^31 + 204800 elements per q/k/v/dO
+    tensor (and twice that many bytes in o, dq, dk, dv).  A reset (a = 0) 2500 tokens before
+    the end makes everything after it independent of the earlier tokens, so the oracle runs
+    on that tail alone: the tokens with the highest indices, of the first and last head,
+    forward and backward (the forward saving its checkpoint, the backward using it)."""
+    dev = torch.device("cuda")
+    B, H, T, d, chunk = 1, 16, (1 << 20) + 100, 128, 128
+    inp = workloads.la_long_inputs_device(B, H, T, d, d, seed=22, device=dev)
+    t_r = T - 2500
+    inp["log_a"][:, :, t_r] = -float("inf")
+    t = inp
+    cp = cla.chunk_la_ckpt(t["q"], t["v"], chunk=chunk)
+    o, ST = cla.chunk_la_fwd(t["q"], t["k"], t["v"], t["log_a"], None, chunk=chunk, ckpt=cp)
+    dq, dk, dv, dl, dS0 = cla.chunk_la_bwd(t["q"], t["k"], t["v"], t["log_a"], None, t["dO"], chunk=chunk, ckpt=cp)
+    torch.cuda.synchronize()
+    for hd in (0, H - 1):
+        tail = lambda x: x[:, hd:hd + 1, t_r:].contiguous().cpu()
+        q, k, v, la, dO = (tail(t[n]) for n in ("q", "k", "v", "log_a", "dO"))
+        ro, rST = oracle.la_fwd(q, k, v, la, None)
+        assert_bf16(f"o[head {hd}]", tail(o), ro)
+        assert_bf16(f"S_T[head {hd}]", ST[:, hd:hd + 1].cpu(), rST)
+        rdq, rdk, rdv, rdl, _ = oracle.la_bwd(q, k, v, la, None, dO)
+        for name, x, r in (("dq", dq, rdq), ("dk", dk, rdk), ("dv", dv, rdv)):
+            assert_bf16(f"{name}[head {hd}]", tail(x), r)
+        # the decay gradient from the token after the reset on (at the reset it is 0 by
+        # definition, a sum of terms that cancel in the closed form)
+        assert_bf16(f"dlog_a[head {hd}]", tail(dl)[..., 1:], rdl[..., 1:])
+
+
+def test_selective_beyond_int32_elements(cla):
+    """B=1, T = 2^20 + 37, D = 2048, N = 16: 2^31 + 75776 (t, d) elements (and 16 times as many
+    state entries).  Channels are independent in y, dx, dDelta and dA, so three whole channels
+    are checked; dB and dC sum over every channel and are left to the full-workload test."""
+    dev = torch.device("cuda")
+    B, T, D, N = 1, (1 << 20) + 37, 2048, 16
+    t = workloads.selective_inputs_device(B, T, D, N, seed=23, device=dev)
+    y, hT, ck = cla.selective_scan_fwd(t["x"], t["delta"], t["A"], t["Bm"], t["Cm"], None)
+    dx, dd, dA, dB, dC, dh0 = cla.selective_scan_bwd(t["x"], t["delta"], t["A"], t["Bm"], t["Cm"], None, ck, t["dy"])
+    torch.cuda.synchronize()
+    ch = [0, 1029, 2047]
+    sub = lambda x: x[..., ch].contiguous().cpu()
+    x, delta, dy = sub(t["x"]), sub(t["delta"]), sub(t["dy"])
+    A = t["A"][ch].cpu()
+    Bm, Cm = t["Bm"].cpu(), t["Cm"].cpu()
+    ry, rhT = oracle.selective_fwd(x, delta, A, Bm, Cm, None)
+    assert_fp32("y", sub(y), ry)
+    assert_fp32("hT", hT[:, ch].cpu(), rhT)
+    rdx, rdd, rdA, _, _, _ = oracle.selective_bwd(x, delta, A, Bm, Cm, None, dy)
+    assert_fp32("dx", sub(dx), rdx)
+    assert_fp32("ddelta", sub(dd), rdd)
+    assert_fp32("dA", dA[ch].cpu(), rdA)

@@ -138,3 +138,48 @@ def make(name: str, **shape_overrides):
     kw = {k: spec[k] for k in params if k in spec}
     kw.update(shape_overrides)
     return gen(**kw)
+
+
+# ---------------------------------------------------------------- device-side draws for very large shapes
+# The same distributions drawn on a CUDA device with torch's Philox generator (seeded), for
+# shapes beyond what the host draws in reasonable time (the maximum-size tests: more than
+# 2^31 elements per tensor).  The oracle then reads back the slices it checks.
+def _dev_gen(seed: int, offset: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + int(offset))
+    return g
+
+
+def _dev_normal(seed, offset, shape, device, std=1.0, dtype=torch.float32) -> torch.Tensor:
+    z = torch.empty(shape, dtype=torch.float32, device=device)
+    z.normal_(0.0, float(std), generator=_dev_gen(seed, offset, device))
+    return z if dtype == torch.float32 else z.to(dtype)
+
+
+def scan_inputs_device(B, T, D, seed, device):
+    """The ``scan`` recipe drawn on the device: a = exp(-0.05 softplus(z)), b, h0, dh ~ N(0, 1)."""
+    z = _dev_normal(seed, 0, (B, T, D), device)
+    a = torch.exp(-0.05 * torch.nn.functional.softplus(z))
+    del z
+    return dict(a=a, b=_dev_normal(seed, 1, (B, T, D), device), h0=_dev_normal(seed, 2, (B, D), device),
+                dh=_dev_normal(seed, 3, (B, T, D), device))
+
+
+def la_long_inputs_device(B, H, T, dk, dv, seed, device):
+    """The ``la_long`` recipe drawn on the device (S0 = 0)."""
+    s = 1.0 / math.sqrt(dk)
+    bf = torch.bfloat16
+    log_a = -torch.nn.functional.softplus(_dev_normal(seed, 3, (B, H, T), device)) / 16.0
+    return dict(q=_dev_normal(seed, 0, (B, H, T, dk), device, s, bf), k=_dev_normal(seed, 1, (B, H, T, dk), device, s, bf),
+                v=_dev_normal(seed, 2, (B, H, T, dv), device, s, bf), log_a=log_a, S0=None,
+                dO=_dev_normal(seed, 5, (B, H, T, dv), device, 1.0, bf))
+
+
+def selective_inputs_device(B, T, D, N, seed, device):
+    """The ``selective`` recipe drawn on the device."""
+    bf = torch.bfloat16
+    delta = torch.nn.functional.softplus(_dev_normal(seed, 3, (B, T, D), device, 0.5) - 2.0)
+    A = -torch.arange(1, N + 1, dtype=torch.float32, device=device).expand(D, N).contiguous()
+    return dict(x=_dev_normal(seed, 0, (B, T, D), device, 1.0, bf), delta=delta, A=A,
+                Bm=_dev_normal(seed, 1, (B, T, N), device, 1.0, bf), Cm=_dev_normal(seed, 2, (B, T, N), device, 1.0, bf),
+                h0=None, dy=_dev_normal(seed, 4, (B, T, D), device))
