@@ -662,14 +662,39 @@ __global__ void sel_reduce_bc_kernel(const float *__restrict__ partB, const floa
 }
 
 // dA[d][n]: sum over batch rows and chunks, in that order.
-__global__ void sel_reduce_a_kernel(const float *__restrict__ partA, float *__restrict__ dA, int B, int n_chunks,
-                                    int D) {
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // (d, n)
-    if (i >= (long long)D * kN) return;
+// dA[i] = sum over (b, chunk) of partA[b][chunk][i]: a block takes 32 consecutive i (one
+// coalesced 128-byte row per (b, chunk)); its 8 warps split the (b, chunk) rows (warp w takes
+// rows w, w + 8, ...) and add their sums in warp order, so the order is fixed.
+constexpr int kRedAWarps = 8;
+__global__ void __launch_bounds__(kRedAWarps * 32)
+sel_reduce_a_kernel(const float *__restrict__ partA, float *__restrict__ dA, int B, int n_chunks, int D) {
+    __shared__ float s_part[kRedAWarps][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long n_i = (long long)D * kN;
+    const long long i = (long long)blockIdx.x * 32 + lane;  // (d, n)
+    const long long rows = (long long)B * n_chunks;
     float s = 0.f;
-    for (int b = 0; b < B; ++b)
-        for (int j = 0; j < n_chunks; ++j) s += partA[((size_t)b * n_chunks + j) * D * kN + i];
-    dA[i] = s;
+    if (i < n_i) {
+        long long r = warp;
+        // four rows in flight per thread
+        for (; r + 3 * kRedAWarps < rows; r += 4 * kRedAWarps) {
+            const float v0 = partA[r * n_i + i], v1 = partA[(r + kRedAWarps) * n_i + i];
+            const float v2 = partA[(r + 2 * kRedAWarps) * n_i + i], v3 = partA[(r + 3 * kRedAWarps) * n_i + i];
+            s += v0;
+            s += v1;
+            s += v2;
+            s += v3;
+        }
+        for (; r < rows; r += kRedAWarps) s += partA[r * n_i + i];
+    }
+    s_part[warp][lane] = s;
+    __syncthreads();
+    if (warp == 0 && i < n_i) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kRedAWarps; ++w) t += s_part[w][lane];
+        dA[i] = t;
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -827,8 +852,8 @@ extern "C" int cla_selective_scan_bwd(const uint16_t *x, const float *delta, con
     st = check_launch(fn);
     if (st) return st;
     if (dA) {
-        sel_reduce_a_kernel<<<(unsigned int)((D * kN + 255) / 256), 256, 0, s>>>(w.partA, dA, (int)B, p.g.n_chunks,
-                                                                               (int)D);
+        sel_reduce_a_kernel<<<(unsigned int)((D * kN + 31) / 32), kRedAWarps * 32, 0, s>>>(w.partA, dA, (int)B,
+                                                                                         p.g.n_chunks, (int)D);
         st = check_launch(fn);
     }
     return st;
