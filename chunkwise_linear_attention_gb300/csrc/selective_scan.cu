@@ -126,8 +126,8 @@ struct SelGeom {
 struct SelWs {
     WsHeader *hdr;
     unsigned int *flags;  // per unit (chunk, b, cblk)
-    float *agg;           // forward: [unit][17][128]; backward: [unit][32][128]
-    float *incl;          // [unit][16][128]
+    float *agg;           // forward: [unit][17][kCh]; backward: [unit][32][kChB]
+    float *incl;          // [unit][16][kCh or kChB]
     float *partB;         // [B][T][n_cblk][16]
     float *partC;
     float *partA;         // [B][n_chunks][D][16]
