@@ -61,3 +61,32 @@ def test_host_validation_without_gpu(lib):
     assert st == 5
     assert lib.cla_scan_diag_workspace_size(8, 4096, 1024) > 0
     assert lib.cla_scan_diag_workspace_size(-1, 1, 1) == 0
+
+
+def test_chunk_la_ckpt_size_follows_the_segment_rule(lib):
+    """The checkpoint holds one d_k x d_v fp32 state per segment and head; segments are the
+    largest of 64/32/16/8 chunks that still leave at least 1024 blocks (heads x 64-column
+    blocks x segments).  Long-context workload, chunk 128: 512 chunks per head, 32 heads,
+    2 column blocks -> segments of 32 chunks, 16 of them."""
+    f = lib.cla_chunk_la_ckpt_size
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int64] * 5 + [ctypes.c_int]
+    assert f(1, 32, 65536, 128, 128, 128) == 16 * 32 * 128 * 128 * 4
+    # chunk 64: 1024 chunks, segments of 64 chunks (16 x 32 x 2 = 1024 blocks)
+    assert f(1, 32, 65536, 128, 128, 64) == 16 * 32 * 128 * 128 * 4
+    # constant-decay workload: 128 chunks per head, 64 heads, one column block -> segments of 8
+    assert f(4, 16, 8192, 64, 64, 64) == 16 * 64 * 64 * 64 * 4
+    assert f(-1, 1, 1, 64, 64, 64) == 0 and f(1, 1, 1, 64, 64, 0) == 0
+
+
+def test_chunk_la_ckpt_rejects_unaligned_without_gpu(lib):
+    P = ctypes.c_void_p
+    d = P(256)
+    i64 = ctypes.c_int64
+    st = lib.cla_chunk_la_fwd_ckpt(d, d, d, d, None, d, None, P(260), i64(1), i64(1), i64(256), i64(64), i64(64),
+                                   ctypes.c_int(64), d, ctypes.c_size_t(1 << 30), None)
+    assert st == 1  # CLA_ERR_INVALID_ARG
+    assert b"ckpt" in lib.cla_last_error_message()
+    st = lib.cla_chunk_la_bwd_ckpt(d, d, d, d, None, d, None, d, d, d, None, None, P(260), i64(1), i64(1),
+                                   i64(256), i64(64), i64(64), ctypes.c_int(64), d, ctypes.c_size_t(1 << 30), None)
+    assert st == 1
