@@ -18,6 +18,11 @@ Each function states the passage it follows in the C source; the summary:
   backward pass of linear attention"; "Lightning Attention-2", eqs. 4, 11-12).
 * ``la_dlog_closed_form`` -- the closed-form decay gradient of "The backward
   pass of linear attention".
+* ``gla_fwd`` / ``gla_bwd`` / ``gla_dlog_closed_form`` -- gated linear
+  attention, one decay per key dimension ("Parallel Scan", "What one combine
+  costs" and "The chunkwise algorithm": S_t = G_t (.) S_{t-1} + k_t^T v_t), its
+  adjoint, and the per-dimension closed-form decay gradient (Yang et al.'s, as
+  "The backward pass of linear attention" cites it).
 """
 from __future__ import annotations
 
@@ -65,9 +70,13 @@ def _load():
             lib.oracle_la_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I]
             lib.oracle_la_bwd.argtypes = [P] * 12 + [I, I, I, I, I]
             lib.oracle_la_dlog_closed_form.argtypes = [P] * 7 + [I, I, I, I, I]
+            lib.oracle_gla_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I]
+            lib.oracle_gla_bwd.argtypes = [P] * 12 + [I, I, I, I, I]
+            lib.oracle_gla_dlog_closed_form.argtypes = [P] * 7 + [I, I, I, I, I]
             for fn in ("oracle_scan_diag_fwd", "oracle_scan_diag_bwd", "oracle_selective_fwd",
                        "oracle_selective_bwd", "oracle_la_fwd", "oracle_la_bwd",
-                       "oracle_la_dlog_closed_form"):
+                       "oracle_la_dlog_closed_form", "oracle_gla_fwd", "oracle_gla_bwd",
+                       "oracle_gla_dlog_closed_form"):
                 getattr(lib, fn).restype = None
             _lib = lib
     return _lib
@@ -173,4 +182,44 @@ def la_dlog_closed_form(q, k, dq, dk, dST=None, ST=None):
     out = np.empty((B, H, T))
     _load().oracle_la_dlog_closed_form(_p(q), _p(k), _p(dq), _p(dk), _p(dST), _p(ST), _p(out),
                                        B, H, T, dkk, dv)
+    return out
+
+
+def gla_fwd(q, k, v, log_a, S0=None):
+    """Gated linear attention forward, one decay per key dimension: q, k, log_a
+    [B,H,T,dk], v [B,H,T,dv], S0 [B,H,dk,dv]; returns (o [B,H,T,dv], S_T)."""
+    q, k, v, log_a, S0 = map(_f64, (q, k, v, log_a, S0))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    o = np.empty((B, H, T, dv))
+    ST = np.empty((B, H, dk, dv))
+    _load().oracle_gla_fwd(_p(q), _p(k), _p(v), _p(log_a), _p(S0), _p(o), _p(ST), B, H, T, dk, dv)
+    return o, ST
+
+
+def gla_bwd(q, k, v, log_a, S0, dO, dST=None):
+    """Gated linear attention backward by the adjoint definition; returns
+    (dq, dk, dv, dlog_a [B,H,T,dk], dS0)."""
+    q, k, v, log_a, S0, dO, dST = map(_f64, (q, k, v, log_a, S0, dO, dST))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dq = np.empty((B, H, T, dk))
+    dkk = np.empty((B, H, T, dk))
+    dvv = np.empty((B, H, T, dv))
+    dl = np.empty((B, H, T, dk))
+    dS0 = np.empty((B, H, dk, dv))
+    _load().oracle_gla_bwd(_p(q), _p(k), _p(v), _p(log_a), _p(S0), _p(dO), _p(dST),
+                           _p(dq), _p(dkk), _p(dvv), _p(dl), _p(dS0), B, H, T, dk, dv)
+    return dq, dkk, dvv, dl, dS0
+
+
+def gla_dlog_closed_form(q, k, dq, dk, dST=None, ST=None):
+    """dL/dlog a_u[i] = sum_{t>=u} q_t[i] dq_t[i] - sum_{s>=u} k_s[i] dk_s[i]
+    (+ sum_j dS_T[i][j] S_T[i][j])."""
+    q, k, dq, dk, dST, ST = map(_f64, (q, k, dq, dk, dST, ST))
+    B, H, T, dkk = q.shape
+    dv = ST.shape[-1] if ST is not None else dkk
+    out = np.empty((B, H, T, dkk))
+    _load().oracle_gla_dlog_closed_form(_p(q), _p(k), _p(dq), _p(dk), _p(dST), _p(ST), _p(out),
+                                        B, H, T, dkk, dv)
     return out

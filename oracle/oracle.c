@@ -13,9 +13,10 @@
  * Sources (page title, section):
  *   "Parallel Scan" (zerotofrontier.app/ssm/parallel-scan), sections
  *     "The scan for one number of state", "Scans over vector and matrix
- *     states", "A vectorized scan for diagonal states", "The backward pass is a
- *     scan in reverse", "The backward pass of linear attention", "The
- *     chunkwise algorithm", "When a scan is the wrong tool".
+ *     states", "What one combine costs", "A vectorized scan for diagonal
+ *     states", "The backward pass is a scan in reverse", "The backward pass of
+ *     linear attention", "The chunkwise algorithm", "When a scan is the wrong
+ *     tool".
  *   "Lightning Attention-2" (paper-graph-ui, arXiv 2401.04658), eq. 4
  *     (recurrent form kv_t = lambda kv_{t-1} + k_t^T v_t, o_t = q_t kv_t) and
  *     eqs. 11-12 (per-token gradients).
@@ -26,6 +27,7 @@
  *                     Bm, Cm, dB, dC [B][T][N];  h0, hT, dhT, dh0 [B][D][N]
  *   linear attention: q, k, dq, dk [B][H][T][dk]; v, o, dO, dv [B][H][T][dv];
  *                     log_a, dlog_a [B][H][T];   S0, ST, dST, dS0 [B][H][dk][dv]
+ *   gated (GLA):      as linear attention, with log_a, dlog_a [B][H][T][dk]
  * Optional pointers may be NULL (meaning zero for inputs, "not wanted" for
  * outputs).  Time indices below are 1-based in comments (t = 1..T), matching
  * the pages, and 0-based in code.
@@ -431,6 +433,150 @@ void oracle_la_dlog_closed_form(const double *q, const double *k,
             }
             run += qd - kd;
             dlog_a[u * T + t] = run;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Gated linear attention: one decay per key dimension.                     */
+/* "Parallel Scan", "What one combine costs" (a diagonal transition, one    */
+/* decay per state entry: GLA) and "The chunkwise algorithm" (the GLA form  */
+/* S_t = G_t (.) S_{t-1} + k_t^T v_t, o_t = q_t S_t, G_t holding the        */
+/* decays): here G_t[i][j] = a_t[i], one decay per key dimension i.         */
+/*   log_a, dlog_a [B][H][T][dk]; other layouts as for linear attention.    */
+/* ------------------------------------------------------------------------ */
+void oracle_gla_fwd(const double *q, const double *k, const double *v,
+                    const double *log_a, const double *S0, double *o, double *ST,
+                    i64 B, i64 H, i64 T, i64 dk, i64 dv) {
+    i64 units = B * H;
+#pragma omp parallel
+    {
+        double *S = (double *)malloc(sizeof(double) * (size_t)(dk * dv));
+#pragma omp for schedule(static)
+        for (i64 u = 0; u < units; ++u) {
+            for (i64 i = 0; i < dk * dv; ++i) S[i] = S0 ? S0[u * dk * dv + i] : 0.0;
+            for (i64 t = 0; t < T; ++t) {
+                const double *qt = q + (u * T + t) * dk;
+                const double *kt = k + (u * T + t) * dk;
+                const double *vt = v + (u * T + t) * dv;
+                const double *lt = log_a + (u * T + t) * dk;
+                for (i64 i = 0; i < dk; ++i) {
+                    double ai = exp(lt[i]);
+                    for (i64 j = 0; j < dv; ++j) S[i * dv + j] = ai * S[i * dv + j] + kt[i] * vt[j];
+                }
+                double *ot = o + (u * T + t) * dv;
+                for (i64 j = 0; j < dv; ++j) {
+                    double s = 0.0;
+                    for (i64 i = 0; i < dk; ++i) s += S[i * dv + j] * qt[i];
+                    ot[j] = s;
+                }
+            }
+            if (ST)
+                for (i64 i = 0; i < dk * dv; ++i) ST[u * dk * dv + i] = S[i];
+        }
+        free(S);
+    }
+}
+
+/* Backward by the adjoint definition ("Parallel Scan", "The backward pass of */
+/* linear attention", with the scalar decay replaced by the diagonal one):    */
+/*   Sbar_t = q_t^T obar_t + diag(a_{t+1}) Sbar_{t+1}  (+ dS_T at t = T)      */
+/*   dq_t = S_t obar_t,  dk_t = Sbar_t v_t,  dv_t = Sbar_t^T k_t              */
+/*   dL/dlog a_t[i] = a_t[i] sum_j Sbar_t[i][j] S_{t-1}[i][j]                 */
+/*   dS_0 = diag(a_1) Sbar_1.                                                 */
+/* Every forward state is kept (the oracle runs on short sequences only).    */
+void oracle_gla_bwd(const double *q, const double *k, const double *v,
+                    const double *log_a, const double *S0, const double *dO,
+                    const double *dST, double *dq, double *dkk, double *dvv,
+                    double *dlog_a, double *dS0, i64 B, i64 H, i64 T, i64 dk,
+                    i64 dv) {
+    i64 units = B * H;
+    i64 ss = dk * dv;
+#pragma omp parallel
+    {
+        double *states = (double *)malloc(sizeof(double) * (size_t)((T + 1) * ss)); /* S_0..S_T */
+        double *Sbar = (double *)malloc(sizeof(double) * (size_t)ss);
+        double *anext = (double *)malloc(sizeof(double) * (size_t)dk);
+#pragma omp for schedule(static)
+        for (i64 u = 0; u < units; ++u) {
+            const double *qu = q + u * T * dk, *ku = k + u * T * dk;
+            const double *vu = v + u * T * dv, *du = dO + u * T * dv;
+            const double *lu = log_a + u * T * dk;
+            for (i64 i = 0; i < ss; ++i) states[i] = S0 ? S0[u * ss + i] : 0.0;
+            for (i64 t = 0; t < T; ++t) {
+                const double *prev = states + t * ss;
+                double *cur = states + (t + 1) * ss;
+                for (i64 i = 0; i < dk; ++i) {
+                    double ai = exp(lu[t * dk + i]);
+                    for (i64 j = 0; j < dv; ++j) cur[i * dv + j] = ai * prev[i * dv + j] + ku[t * dk + i] * vu[t * dv + j];
+                }
+                for (i64 i = 0; i < dk; ++i) {
+                    double s = 0.0;
+                    for (i64 j = 0; j < dv; ++j) s += cur[i * dv + j] * du[t * dv + j];
+                    dq[(u * T + t) * dk + i] = s;
+                }
+            }
+            for (i64 i = 0; i < ss; ++i) Sbar[i] = dST ? dST[u * ss + i] : 0.0;
+            for (i64 i = 0; i < dk; ++i) anext[i] = 1.0; /* the dS_T term enters undecayed */
+            for (i64 t = T - 1; t >= 0; --t) {
+                for (i64 i = 0; i < dk; ++i)
+                    for (i64 j = 0; j < dv; ++j)
+                        Sbar[i * dv + j] = anext[i] * Sbar[i * dv + j] + qu[t * dk + i] * du[t * dv + j];
+                for (i64 i = 0; i < dk; ++i) {
+                    double s = 0.0;
+                    for (i64 j = 0; j < dv; ++j) s += Sbar[i * dv + j] * vu[t * dv + j];
+                    dkk[(u * T + t) * dk + i] = s;
+                }
+                for (i64 j = 0; j < dv; ++j) {
+                    double s = 0.0;
+                    for (i64 i = 0; i < dk; ++i) s += Sbar[i * dv + j] * ku[t * dk + i];
+                    dvv[(u * T + t) * dv + j] = s;
+                }
+                const double *Sprev = states + t * ss;
+                for (i64 i = 0; i < dk; ++i) {
+                    double ai = exp(lu[t * dk + i]);
+                    if (dlog_a) {
+                        double s = 0.0;
+                        for (i64 j = 0; j < dv; ++j) s += Sbar[i * dv + j] * Sprev[i * dv + j];
+                        dlog_a[(u * T + t) * dk + i] = ai * s;
+                    }
+                    anext[i] = ai;
+                }
+            }
+            if (dS0)
+                for (i64 i = 0; i < dk; ++i)
+                    for (i64 j = 0; j < dv; ++j) dS0[u * ss + i * dv + j] = anext[i] * Sbar[i * dv + j];
+        }
+        free(states);
+        free(Sbar);
+        free(anext);
+    }
+}
+
+/* Closed-form decay gradient per key dimension ("Parallel Scan", "The        */
+/* backward pass of linear attention": the closed form there is Yang et al.'s */
+/* for gated linear attention, one decay per key dimension): path by path,    */
+/* a contribution through key dimension i crosses step u exactly when its    */
+/* write is before u and its read at or after u, so                           */
+/*   dL/dlog a_u[i] = sum_{t>=u} q_t[i] dq_t[i] - sum_{s>=u} k_s[i] dk_s[i]   */
+/*                    (+ sum_j dS_T[i][j] S_T[i][j]).                          */
+void oracle_gla_dlog_closed_form(const double *q, const double *k,
+                                 const double *dq, const double *dkk,
+                                 const double *dST, const double *ST,
+                                 double *dlog_a, i64 B, i64 H, i64 T, i64 dk,
+                                 i64 dv) {
+    i64 units = B * H;
+#pragma omp parallel for schedule(static)
+    for (i64 u = 0; u < units; ++u) {
+        for (i64 i = 0; i < dk; ++i) {
+            double run = 0.0;
+            if (dST && ST)
+                for (i64 j = 0; j < dv; ++j) run += dST[u * dk * dv + i * dv + j] * ST[u * dk * dv + i * dv + j];
+            for (i64 t = T - 1; t >= 0; --t) {
+                i64 x = (u * T + t) * dk + i;
+                run += q[x] * dq[x] - k[x] * dkk[x];
+                dlog_a[x] = run;
+            }
         }
     }
 }

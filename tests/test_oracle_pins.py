@@ -391,3 +391,90 @@ def test_la_closed_form_decay_gradient_equals_definition():
     dq, dk_, _, dl, _ = oracle.la_bwd(q, k, v, log_a, S0, dO, dST)
     dl_cf = oracle.la_dlog_closed_form(q, k, dq, dk_, dST, ST)
     np.testing.assert_allclose(dl_cf, dl, rtol=1e-10, atol=1e-10)
+
+
+# ---------------------------------------------------------------- gated linear attention
+def _gla_inputs(rng, B, H, T, dk, dv, decay=(0.5, 1.0)):
+    q = rng.standard_normal((B, H, T, dk))
+    k = rng.standard_normal((B, H, T, dk))
+    v = rng.standard_normal((B, H, T, dv))
+    log_a = np.log(rng.uniform(*decay, (B, H, T, dk)))
+    S0 = rng.standard_normal((B, H, dk, dv))
+    return q, k, v, log_a, S0
+
+
+def test_gla_matches_pathwise_sum():
+    """One decay per key dimension, by its paths: o_t[j] = sum_{s<=t} sum_i q_t[i] k_s[i]
+    v_s[j] prod_{u=s+1..t} a_u[i] + sum_i q_t[i] prod_{u<=t} a_u[i] S0[i][j], every product
+    from its own terms (dk != dv, so a decay on the wrong axis cannot pass)."""
+    rng = _rng(21)
+    B, H, T, dk, dv = 1, 2, 9, 3, 4
+    q, k, v, log_a, S0 = _gla_inputs(rng, B, H, T, dk, dv)
+    o, ST = oracle.gla_fwd(q, k, v, log_a, S0)
+    a = np.exp(log_a)
+    for bi in range(B):
+        for h in range(H):
+            for t in range(T):
+                ref = np.zeros(dv)
+                for i in range(dk):
+                    ref += q[bi, h, t, i] * np.prod(a[bi, h, : t + 1, i]) * S0[bi, h, i]
+                    for s in range(t + 1):
+                        ref += q[bi, h, t, i] * k[bi, h, s, i] * np.prod(a[bi, h, s + 1 : t + 1, i]) * v[bi, h, s]
+                np.testing.assert_allclose(o[bi, h, t], ref, rtol=1e-12, atol=1e-12)
+            ST_ref = np.zeros((dk, dv))
+            for i in range(dk):
+                ST_ref[i] = np.prod(a[bi, h, :, i]) * S0[bi, h, i]
+                for s in range(T):
+                    ST_ref[i] += k[bi, h, s, i] * np.prod(a[bi, h, s + 1 :, i]) * v[bi, h, s]
+            np.testing.assert_allclose(ST[bi, h], ST_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gla_with_one_decay_for_all_dims_is_linear_attention():
+    """Every key dimension sharing the step's decay gives the scalar-decay layer; the
+    per-dimension decay gradients then sum to the scalar one."""
+    rng = _rng(22)
+    B, H, T, dk, dv = 2, 1, 13, 4, 3
+    q, k, v, _, S0 = _gla_inputs(rng, B, H, T, dk, dv)
+    la = np.log(rng.uniform(0.6, 1.0, (B, H, T)))
+    lg = np.repeat(la[..., None], dk, axis=-1)
+    dO = rng.standard_normal((B, H, T, dv))
+    dST = rng.standard_normal((B, H, dk, dv))
+    o1, s1 = oracle.gla_fwd(q, k, v, lg, S0)
+    o2, s2 = oracle.la_fwd(q, k, v, la, S0)
+    np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(s1, s2, rtol=1e-12, atol=1e-12)
+    g1 = oracle.gla_bwd(q, k, v, lg, S0, dO, dST)
+    g2 = oracle.la_bwd(q, k, v, la, S0, dO, dST)
+    for x, y in zip((g1[0], g1[1], g1[2], g1[4]), (g2[0], g2[1], g2[2], g2[4])):
+        np.testing.assert_allclose(x, y, rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(g1[3].sum(-1), g2[3], rtol=1e-11, atol=1e-11)
+
+
+def test_gla_backward_finite_differences():
+    rng = _rng(23)
+    B, H, T, dk, dv = 1, 2, 8, 3, 2
+    q, k, v, log_a, S0 = _gla_inputs(rng, B, H, T, dk, dv)
+    dO = rng.standard_normal((B, H, T, dv))
+    dST = rng.standard_normal((B, H, dk, dv))
+
+    def loss():
+        o, ST = oracle.gla_fwd(q, k, v, log_a, S0)
+        return float(np.sum(dO * o) + np.sum(dST * ST))
+
+    dq, dk_, dv_, dl, dS0 = oracle.gla_bwd(q, k, v, log_a, S0, dO, dST)
+    _fd_check(loss, dict(q=q, k=k, v=v, log_a=log_a, S0=S0),
+              dict(q=dq, k=dk_, v=dv_, log_a=dl, S0=dS0), sample=40, tol=2e-7)
+
+
+def test_gla_closed_form_decay_gradient_equals_definition():
+    """Per key dimension: sum_{t>=u} q_t[i] dq_t[i] - sum_{s>=u} k_s[i] dk_s[i]
+    (+ sum_j dS_T[i][j] S_T[i][j]) equals a_u[i] sum_j Sbar_u[i][j] S_{u-1}[i][j]."""
+    rng = _rng(24)
+    B, H, T, dk, dv = 2, 2, 40, 4, 3
+    q, k, v, log_a, S0 = _gla_inputs(rng, B, H, T, dk, dv, decay=(0.8, 1.0))
+    dO = rng.standard_normal((B, H, T, dv))
+    dST = rng.standard_normal((B, H, dk, dv))
+    _, ST = oracle.gla_fwd(q, k, v, log_a, S0)
+    dq, dk_, _, dl, _ = oracle.gla_bwd(q, k, v, log_a, S0, dO, dST)
+    dl_cf = oracle.gla_dlog_closed_form(q, k, dq, dk_, dST, ST)
+    np.testing.assert_allclose(dl_cf, dl, rtol=1e-10, atol=1e-10)
