@@ -9,8 +9,9 @@ write da, db = 20 B per element) / mean step time.
 
 The same line carries, under "workloads", the other workloads of the hot path
 (small diagonal scan, selective scan, chunkwise linear attention with constant
-and with data-dependent decay) with tokens/s, TFLOP/s and roofline fractions,
-and:
+and with data-dependent decay) with tokens/s, TFLOP/s and roofline fractions
+(each forward and backward: 5 warm-up calls, then the median of 20 calls
+timed with CUDA events, L2 flushed before each), and:
   roofline      the dominant kernel of the headline step against the measured
                 HBM copy bandwidth (MEASURED_PEAKS.json)
   cpu_baseline  the float64 C oracle on this host's cores, on a bounded sample
@@ -271,7 +272,8 @@ def bench_scan(torch, cla, workloads, dev, steps, warmup, dist_on):
 
 
 # ------------------------------------------------------------------ other workloads
-def _time_calls(torch, fn, flush, iters, warmup=3):
+def _time_calls(torch, fn, flush, iters, warmup=5):
+    """Median device time of `iters` calls, L2 flushed before each, after `warmup` calls."""
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         fn()
@@ -311,9 +313,14 @@ def bench_scan_blelloch(torch, cla, workloads, dev, flush, peaks, iters=20, shap
     h = torch.empty_like(a)
     by = 12 * B * T * D
     hs, bl = [], []
-    for _ in range(iters):
-        hs.append(_time_calls(torch, lambda: cla.scan_diag_fwd(a, b, h0, h=h, workspace=ws), flush, 1))
-        bl.append(_time_calls(torch, lambda: cla.scan_diag_fwd_blelloch(a, b, h0, h=h, workspace=ws), flush, 1))
+    f_hs = lambda: cla.scan_diag_fwd(a, b, h0, h=h, workspace=ws)
+    f_bl = lambda: cla.scan_diag_fwd_blelloch(a, b, h0, h=h, workspace=ws)
+    for _ in range(5):
+        f_hs()
+        f_bl()
+    for _ in range(iters):  # alternately, one timed call each
+        hs.append(_time_calls(torch, f_hs, flush, 1, warmup=0))
+        bl.append(_time_calls(torch, f_bl, flush, 1, warmup=0))
     cla.check_status(ws)
     ms_hs, ms_bl = statistics.median(hs), statistics.median(bl)
     return {"workload": f"diagonal scan fwd fp32 B={B} T={T} D={D}: Hillis-Steele vs Blelloch across a chunk's runs",
@@ -321,7 +328,7 @@ def bench_scan_blelloch(torch, cla, workloads, dev, flush, peaks, iters=20, shap
             "hillis_steele_GBps": round(by / ms_hs / 1e6, 1), "blelloch_GBps": round(by / ms_bl / 1e6, 1)}
 
 
-def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=5, shape=None):
+def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=20, shape=None):
     inp = workloads.make(name, **(shape or {}))
     t = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     B, H, T, d = t["q"].shape
@@ -364,7 +371,7 @@ def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=5, sha
     return res
 
 
-def bench_selective(torch, cla, workloads, dev, flush, peaks, iters=5, shape=None):
+def bench_selective(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
     inp = workloads.make("selective", **(shape or {}))
     t = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     B, T, D = t["x"].shape
