@@ -195,3 +195,29 @@ def test_chunk_la_unequal_head_dims(cla, dk, dv, chunk, ckpt):
     rng = np.random.default_rng(dk * 3 + dv)
     dST = torch.from_numpy(rng.normal(0, 0.1, (1, 2, dk, dv)).astype(np.float32))
     _check(cla, inp, chunk, dST, ckpt=ckpt)
+
+
+@pytest.mark.parametrize("d,chunk", [(64, 64), (128, 128)])
+def test_chunk_la_ckpt_holds_segment_states(cla, d, chunk):
+    """The checkpoint is the state entering each segment: entry s equals the oracle's state
+    after the first s * seg_chunks * chunk tokens (S0 and the decays included).  One head, so
+    segments are 8 chunks long (the smallest choice when blocks are few)."""
+    T = 3000 if chunk == 64 else 5000
+    inp = workloads.make("la_long", B=1, H=1, T=T, dk=d, dv=d)
+    t = {k: _dev(v) for k, v in inp.items()}
+    cp = cla.chunk_la_ckpt(t["q"], t["v"], chunk=chunk)
+    cla.chunk_la_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], chunk=chunk, ckpt=cp)
+    torch.cuda.synchronize()
+    seg_tokens = 8 * chunk
+    n_seg = (T + seg_tokens - 1) // seg_tokens
+    assert cp.numel() * 4 == cla.chunk_la_ckpt_size(1, 1, T, d, d, chunk) == n_seg * d * d * 4
+    states = cp.view(n_seg, d, d).cpu()
+    for s in range(n_seg):
+        t0 = s * seg_tokens
+        if t0 == 0:
+            ref = inp["S0"][0, 0].double().numpy()
+        else:
+            _, rST = oracle.la_fwd(inp["q"][:, :, :t0], inp["k"][:, :, :t0], inp["v"][:, :, :t0],
+                                   inp["log_a"][:, :, :t0], inp["S0"])
+            ref = rST[0, 0]
+        assert_bf16(f"segment {s} state", states[s].numpy(), ref)
