@@ -31,6 +31,14 @@
 // as TMA writes them: X, Y as K-major A/B operands (blocks of 64 columns),
 // Y as the MN-major A operand of dS, Z and S as MN-major B operands, Zs as
 // a K-major B operand written by the threads.
+//
+// A block covers one segment of chunks of one (batch, head) and 64 output
+// columns.  Phase 1 sums the segment's state from zero; a decoupled look-back
+// over the segments before it gives its incoming state; phase 2 runs the
+// chunks from that state and writes the outputs.  With LaArgs::seg_out the
+// incoming state is also saved; with LaArgs::seg_in it is read from there
+// (possibly transposed: another traversal's state) and phase 1 and the
+// look-back are skipped.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
