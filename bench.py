@@ -56,6 +56,9 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+SM_MAX_HZ = 2.07e9  # GB300 maximum SM clock (nvidia-smi clocks.max.sm, 2070 MHz)
+
+
 def kernel_traffic(kernel: str):
     """dram bytes per launch from the committed ncu summary, if it was taken on
     the current source of the kernel (else None)."""
@@ -395,10 +398,20 @@ def bench_selective(torch, cla, workloads, dev, flush, peaks, iters=20, shape=No
     by_b = nt * (2 + 4 + 4 + 4 + 4) + B * T * N * 4 * 2 + ck.numel() * 4
     upd = nt * N
     tot = (tf + tb) / 1e3
+    # Arithmetic floor of the method per state update (t, d, n): one exp2 and three FP32
+    # operations forward, three times that backward.  Unit rates at the maximum clock:
+    # 16 MUFU results and 128 FP32 FMAs per SM per clock, 152 SMs.  (This build evaluates
+    # 2^x with FMAs instead of the MUFU unit, for accuracy: more work than the floor counts.)
+    sfu = 152 * 16 * SM_MAX_HZ
+    fp32 = 152 * 128 * SM_MAX_HZ
+    floor_alu = max(4 * upd / sfu, 4 * 3 * upd / fp32)  # s, fwd + 3x fwd; the two pipes run side by side
+    floor_hbm = (by_f + by_b) / (peaks["hbm_gbs"] * 1e9)
     return {"workload": f"selective scan B={B} T={T} D={D} N={N}", "fwd_us": round(tf * 1e3, 1),
             "bwd_us": round(tb * 1e3, 1), "fwd_GBps": round(by_f / (tf / 1e3) / 1e9, 1),
             "bwd_GBps": round(by_b / (tb / 1e3) / 1e9, 1),
             "frac_hbm": round((by_f + by_b) / tot / (peaks["hbm_gbs"] * 1e9), 4),
+            "frac_binding_roofline": round(max(floor_alu, floor_hbm) / tot, 4),
+            "binding": "alu (exp2 on the special-function unit)" if floor_alu >= floor_hbm else "hbm",
             "state_updates_per_s": round(2 * upd / tot, 1)}
 
 
