@@ -90,3 +90,17 @@ def test_chunk_la_ckpt_rejects_unaligned_without_gpu(lib):
     st = lib.cla_chunk_la_bwd_ckpt(d, d, d, d, None, d, None, d, d, d, None, None, P(260), i64(1), i64(1),
                                    i64(256), i64(64), i64(64), ctypes.c_int(64), d, ctypes.c_size_t(1 << 30), None)
     assert st == 1
+
+
+def test_binding_refuses_host_tensors(lib):
+    """No CPU fallback: host tensors are rejected before anything reaches the library."""
+    import torch
+
+    import chunkwise_linear_attention_gb300 as cla
+
+    a = torch.rand(1, 8, 4)
+    with pytest.raises(ValueError, match="CUDA"):
+        cla.scan_diag_fwd(a, a)
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        cla.chunk_la_fwd(q, q, q, torch.zeros(1, 1, 8))
