@@ -858,13 +858,9 @@ LaPlan la_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chun
 template <int DX, int TC, bool REV>
 int launch_variant(const LaArgs &a, cudaStream_t s, unsigned int grid) {
     using C = LaCfg<DX, TC>;
-    static bool configured = false;  // per template instance; idempotent
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(la_chunk_kernel<DX, TC, REV>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return fail(CLA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-        configured = true;
-    }
+    static std::atomic<unsigned long long> smem_set{0};  // per template instance
+    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(la_chunk_kernel<DX, TC, REV>), C::SMEM);
+    if (st) return st;
     la_chunk_kernel<DX, TC, REV><<<grid, C::NT, C::SMEM, s>>>(a);
     return check_launch("la_chunk_kernel");
 }
@@ -881,13 +877,23 @@ int launch_pass(int DX, int TC, bool REV, const LaArgs &a, cudaStream_t s, unsig
     return fail(CLA_ERR_UNSUPPORTED, "chunk_la: no kernel for head dim %d and chunk %d", DX, TC);
 }
 
+// Non-negative sizes the kernels and the plan handle: B*H <= 2^24, T <= 2^34,
+// B*H*T <= 2^40 (so no workspace offset can overflow) and every grid, at
+// most one block per chunk and 64 columns of 128, below 2^31 blocks.
+bool la_sizes_fit(int64_t B, int64_t H, int64_t T, int chunk) {
+    if (!product_below({B, H}, 16777217.0) || T > (1ll << 34)) return false;
+    if (!product_below({B, H, T}, 1099511627777.0)) return false;
+    const int64_t n_chunks = (T + chunk - 1) / chunk, fin_tiles = (T + kFinTile - 1) / kFinTile;
+    return product_below({B, H, n_chunks, 2}, 2147483648.0) && product_below({B, H, fin_tiles}, 2147483648.0);
+}
+
 int la_validate(const char *fn, int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chunk) {
     if (B < 0 || H < 0 || T < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
     if (!((dk == 64 || dk == 128) && (dv == 64 || dv == 128)))
         return fail(CLA_ERR_UNSUPPORTED, "%s: head dims must be 64 or 128 (got %lld, %lld)", fn, (long long)dk,
                     (long long)dv);
     if (chunk != 64 && chunk != 128) return fail(CLA_ERR_UNSUPPORTED, "%s: chunk must be 64 or 128", fn);
-    if (B * H > (1 << 24) || T > (1ll << 34)) return fail(CLA_ERR_UNSUPPORTED, "%s: size out of range", fn);
+    if (!la_sizes_fit(B, H, T, chunk)) return fail(CLA_ERR_UNSUPPORTED, "%s: size out of range for one launch", fn);
     return CLA_OK;
 }
 
@@ -928,13 +934,13 @@ using namespace cla;
 
 extern "C" size_t cla_chunk_la_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
                                               int chunk) {
-    if (B < 0 || H < 0 || T < 0 || dim_k <= 0 || dim_v <= 0 || chunk <= 0) return 0;
+    if (B < 0 || H < 0 || T < 0 || dim_k <= 0 || dim_v <= 0 || chunk <= 0 || !la_sizes_fit(B, H, T, chunk)) return 0;
     return la_plan(B, H, T, dim_k, dim_v, chunk).total;
 }
 
 extern "C" size_t cla_chunk_la_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
                                          int chunk) {
-    if (B < 0 || H < 0 || T < 0 || dim_k <= 0 || dim_v <= 0 || chunk <= 0) return 0;
+    if (B < 0 || H < 0 || T < 0 || dim_k <= 0 || dim_v <= 0 || chunk <= 0 || !la_sizes_fit(B, H, T, chunk)) return 0;
     const LaPlan pl = la_plan(B, H, T, dim_k, dim_v, chunk);
     return (size_t)pl.n_seg * (size_t)(B * H) * (size_t)dim_k * (size_t)dim_v * sizeof(float);
 }
@@ -961,6 +967,9 @@ int chunk_la_fwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, cons
     if (!q || !k || !v || !log_decay || !o) return fail(CLA_ERR_INVALID_ARG, "%s: q, k, v, log_decay, o required", fn);
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
         return fail(CLA_ERR_INVALID_ARG, "%s: q, k, v, o must be 16-byte aligned", fn);
+    // the state is read in 16-byte rows
+    if (S0 && !aligned16(S0)) return fail(CLA_ERR_INVALID_ARG, "%s: S0 must be 16-byte aligned", fn);
+    if (!aligned_or_null({log_decay, ST}, 4)) return fail(CLA_ERR_INVALID_ARG, "%s: log_decay, ST misaligned", fn);
     if (!ws || !aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace NULL or unaligned", fn);
     if (ckpt && !aligned16(ckpt)) return fail(CLA_ERR_INVALID_ARG, "%s: ckpt must be 16-byte aligned", fn);
     const LaPlan pl = la_plan(B, H, T, dim_k, dim_v, chunk);
@@ -1007,7 +1016,11 @@ int chunk_la_bwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, cons
         return fail(CLA_ERR_INVALID_ARG, "%s: q, k, v, log_decay, dO, dq, dk, dv required", fn);
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq) || !aligned16(dk) ||
         !aligned16(dv))
-        return fail(CLA_ERR_INVALID_ARG, "%s: bf16 tensors must be 16-byte aligned", fn);
+        return fail(CLA_ERR_INVALID_ARG, "%s: q, k, v, dO, dq, dk, dv must be 16-byte aligned", fn);
+    // dST starts the reverse traversal and is read in 16-byte rows
+    if (dST && !aligned16(dST)) return fail(CLA_ERR_INVALID_ARG, "%s: dST must be 16-byte aligned", fn);
+    if (!aligned_or_null({log_decay, S0, dlog_decay, dS0}, 4))
+        return fail(CLA_ERR_INVALID_ARG, "%s: log_decay, S0, dlog_decay, dS0 misaligned", fn);
     if (!ws || !aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace NULL or unaligned", fn);
     if (ckpt && !aligned16(ckpt)) return fail(CLA_ERR_INVALID_ARG, "%s: ckpt must be 16-byte aligned", fn);
     const LaPlan pl = la_plan(B, H, T, dim_k, dim_v, chunk);

@@ -1032,16 +1032,15 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
 
 // ----------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // looked up once, on first use (a function-local static: thread-safe)
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
     return fn;
 }
 
@@ -1064,13 +1063,9 @@ bool make_map(CUtensorMap *m, const void *base, int cols, long long T, int BH, i
 template <int DX, int TC, bool REV>
 int launch_tc_variant(const LaArgs &a, cudaStream_t s, unsigned int grid) {
     using C = TcCfg<DX, TC>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(la_tc_kernel<DX, TC, REV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return fail(CLA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-        configured = true;
-    }
+    static std::atomic<unsigned long long> smem_set{0};  // per template instance
+    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(la_tc_kernel<DX, TC, REV>), C::SMEM);
+    if (st) return st;
     TcMaps maps;
     memset(&maps, 0, sizeof(maps));
     bool ok = make_map(&maps.x, a.X, DX, a.T, a.BH, TC) &&

@@ -7,6 +7,9 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <atomic>
+#include <initializer_list>
+
 #include "../../include/cla.h"
 
 namespace cla {
@@ -17,10 +20,27 @@ namespace cla {
 int fail(int status, const char *fmt, ...);
 int check_launch(const char *what);  // cudaGetLastError -> CLA_OK / CLA_ERR_CUDA
 void clear_error();
+// Raises func's dynamic shared memory limit to `bytes` on the current device,
+// once per device: `done` (one per kernel) keeps a bit per device ordinal.
+int set_max_dynamic_smem(std::atomic<unsigned long long> &done, const void *func, int bytes);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned16_or_null(const void *p) { return p == nullptr || aligned16(p); }
+// The product of non-negative sizes is below `limit`, computed so that it
+// cannot overflow (a zero factor makes it 0).
+inline bool product_below(std::initializer_list<int64_t> xs, double limit) {
+    double p = 1.0;
+    for (int64_t x : xs) p *= (double)x;
+    return p < limit;
+}
+// Every non-NULL pointer a multiple of n bytes (n a power of two): the element
+// alignment the kernels' plain loads and stores rely on.
+inline bool aligned_or_null(std::initializer_list<const void *> ps, uintptr_t n) {
+    for (const void *p : ps)
+        if (p != nullptr && (reinterpret_cast<uintptr_t>(p) & (n - 1)) != 0) return false;
+    return true;
+}
 
 // Every workspace starts with this header.  It is cleared (with the flag
 // arrays that follow it) by one cudaMemsetAsync at the start of each call.

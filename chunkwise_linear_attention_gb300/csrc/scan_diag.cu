@@ -508,14 +508,19 @@ ScanWs bind_ws(const Plan &p, void *ws) {
     return w;
 }
 
-int check_sizes(const char *fn, int64_t B, int64_t T, int64_t D) {
-    if (B < 0 || T < 0 || D < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
-    if (D > (1ll << 30) || B > (1ll << 24) || T > (1ll << 40))
-        return fail(CLA_ERR_UNSUPPORTED, "%s: size out of range", fn);
+// Sizes every kernel and plan of this file handles (non-negative sizes): the
+// grid stays below 2^31 blocks and every count fits its integer type.
+bool sizes_fit(int64_t B, int64_t T, int64_t D) {
+    if (D > (1ll << 30) || B > (1ll << 24) || T > (1ll << 40)) return false;
     const int64_t n_chunks = (T + kTc - 1) / kTc;
     const int64_t n_cblk = ((D + 15) / 16 + kWarps - 1) / kWarps;
-    if (n_chunks * B * ((D + 3) / 4 + kWarps - 1) >= (1ll << 31) || n_chunks * B * n_cblk >= (1ll << 31))
-        return fail(CLA_ERR_UNSUPPORTED, "%s: problem too large for one launch", fn);
+    return product_below({n_chunks, B, (D + 3) / 4 + kWarps - 1}, 2147483648.0) &&
+           product_below({n_chunks, B, n_cblk}, 2147483648.0);
+}
+
+int check_sizes(const char *fn, int64_t B, int64_t T, int64_t D) {
+    if (B < 0 || T < 0 || D < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (!sizes_fit(B, T, D)) return fail(CLA_ERR_UNSUPPORTED, "%s: size out of range for one launch", fn);
     return CLA_OK;
 }
 
@@ -525,7 +530,7 @@ int check_sizes(const char *fn, int64_t B, int64_t T, int64_t D) {
 using namespace cla;
 
 extern "C" size_t cla_scan_diag_workspace_size(int64_t B, int64_t T, int64_t D) {
-    if (B < 0 || T < 0 || D < 0) return 0;
+    if (B < 0 || T < 0 || D < 0 || !sizes_fit(B, T, D)) return 0;
     // the scalar-channel layout needs the most units; size for it
     const Plan p1 = make_plan(B, T, D, 1);
     const Plan p4 = make_plan(B, T, D, 4);
@@ -538,6 +543,8 @@ int scan_fwd(const char *fn, bool blelloch, const float *a, const float *b, cons
     clear_error();
     int st = check_sizes(fn, B, T, D);
     if (st) return st;
+    if (!aligned_or_null({a, b, h0, h, hT}, 4))
+        return fail(CLA_ERR_INVALID_ARG, "%s: fp32 tensors must be 4-byte aligned", fn);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (B == 0 || D == 0) return CLA_OK;
     if (T == 0) {
@@ -587,6 +594,8 @@ extern "C" int cla_scan_diag_bwd(const float *a, const float *h0, const float *h
     const char *fn = "cla_scan_diag_bwd";
     int st = check_sizes(fn, B, T, D);
     if (st) return st;
+    if (!aligned_or_null({a, h0, h, dh, dhT, da, db, dh0}, 4))
+        return fail(CLA_ERR_INVALID_ARG, "%s: fp32 tensors must be 4-byte aligned", fn);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (B == 0 || D == 0) return CLA_OK;
     if (T == 0) {  // h_T = h0: the gradient passes straight through
@@ -658,6 +667,8 @@ extern "C" int cla_scan_diag_fwd_noalloc(const float *a, const float *b, const f
     const char *fn = "cla_scan_diag_fwd_noalloc";
     int st = check_sizes(fn, B, T, D);
     if (st) return st;
+    if (!aligned_or_null({a, b, h0, h, hT}, 4))
+        return fail(CLA_ERR_INVALID_ARG, "%s: fp32 tensors must be 4-byte aligned", fn);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (B == 0 || D == 0) return CLA_OK;
     if (T == 0) {

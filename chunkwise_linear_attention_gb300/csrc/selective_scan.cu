@@ -739,12 +739,17 @@ SelWs sel_bind(const SelPlan &p, void *ws) {
     return s;
 }
 
+// Non-negative sizes every kernel and plan of this file handles: the larger
+// (backward) grid stays below 2^31 blocks.
+bool sel_sizes_fit(int64_t B, int64_t T, int64_t D) {
+    if (D > (1 << 24) || B > (1 << 20) || T > (1ll << 36)) return false;
+    return product_below({(T + kTc - 1) / kTc, B, (D + kChB - 1) / kChB}, 2147483648.0);
+}
+
 int sel_validate(const char *fn, int64_t B, int64_t T, int64_t D, int64_t N) {
     if (B < 0 || T < 0 || D < 0 || N < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
     if (N != kN) return fail(CLA_ERR_UNSUPPORTED, "%s: N must be %d (got %lld)", fn, kN, (long long)N);
-    if (D > (1 << 24) || B > (1 << 20) || T > (1ll << 36)) return fail(CLA_ERR_UNSUPPORTED, "%s: size out of range", fn);
-    const int64_t grid = ((T + kTc - 1) / kTc) * B * ((D + kChB - 1) / kChB);  // the larger (backward) grid
-    if (grid >= (1ll << 31)) return fail(CLA_ERR_UNSUPPORTED, "%s: problem too large for one launch", fn);
+    if (!sel_sizes_fit(B, T, D)) return fail(CLA_ERR_UNSUPPORTED, "%s: size out of range for one launch", fn);
     return CLA_OK;
 }
 
@@ -754,12 +759,12 @@ int sel_validate(const char *fn, int64_t B, int64_t T, int64_t D, int64_t N) {
 using namespace cla;
 
 extern "C" size_t cla_selective_scan_workspace_size(int64_t B, int64_t T, int64_t D, int64_t N) {
-    if (B < 0 || T < 0 || D < 0 || N != kN) return 0;
+    if (B < 0 || T < 0 || D < 0 || N != kN || !sel_sizes_fit(B, T, D)) return 0;
     return sel_plan(B, T, D).total;
 }
 
 extern "C" size_t cla_selective_scan_ckpt_elems(int64_t B, int64_t T, int64_t D, int64_t N) {
-    if (B < 0 || T < 0 || D < 0 || N < 0) return 0;
+    if (B < 0 || T < 0 || D < 0 || N != kN || !sel_sizes_fit(B, T, D)) return 0;
     return (size_t)B * (size_t)((T + kTc - 1) / kTc) * (size_t)D * (size_t)N;
 }
 
@@ -771,6 +776,8 @@ extern "C" int cla_selective_scan_fwd(const uint16_t *x, const float *delta, con
     const char *fn = "cla_selective_scan_fwd";
     int st = sel_validate(fn, B, T, D, N);
     if (st) return st;
+    if (!aligned_or_null({delta, A, h0, y, hT}, 4) || !aligned_or_null({x, Bm, Cm}, 2))
+        return fail(CLA_ERR_INVALID_ARG, "%s: tensors must be aligned to their element size", fn);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (B == 0 || D == 0) return CLA_OK;
     if (T == 0) {
@@ -788,13 +795,9 @@ extern "C" int cla_selective_scan_fwd(const uint16_t *x, const float *delta, con
     if (ws_bytes < p.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, p.total);
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.off_agg, s), fn);
     const SelWs w = sel_bind(p, ws);
-    static bool configured = false;
-    if (!configured) {
-        CLA_CUDA_TRY(cudaFuncSetAttribute(sel_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)sizeof(SelFwdSmem)),
-                     fn);
-        configured = true;
-    }
+    static std::atomic<unsigned long long> smem_set{0};
+    st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(sel_fwd_kernel), (int)sizeof(SelFwdSmem));
+    if (st) return st;
     const unsigned int grid = (unsigned int)((size_t)p.g.n_chunks * B * p.g.n_cblk);
     sel_fwd_kernel<<<grid, kCh, sizeof(SelFwdSmem), s>>>(reinterpret_cast<const bf16 *>(x), delta, A, reinterpret_cast<const bf16 *>(Bm),
                                         reinterpret_cast<const bf16 *>(Cm), h0, y, hT, ckpt, p.g, w);
@@ -811,6 +814,9 @@ extern "C" int cla_selective_scan_bwd(const uint16_t *x, const float *delta, con
     int st = sel_validate(fn, B, T, D, N);
     if (st) return st;
     (void)h0;  // the checkpoints already contain the initial state
+    if (!aligned_or_null({delta, A, ckpt, dy, dhT, dx, ddelta, dA, dB, dC, dh0}, 4) ||
+        !aligned_or_null({x, Bm, Cm}, 2))
+        return fail(CLA_ERR_INVALID_ARG, "%s: tensors must be aligned to their element size", fn);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (B == 0 || D == 0) {
         if (dA && D > 0) CLA_CUDA_TRY(cudaMemsetAsync(dA, 0, sizeof(float) * D * N, s), fn);
@@ -833,13 +839,9 @@ extern "C" int cla_selective_scan_bwd(const uint16_t *x, const float *delta, con
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.off_agg, s), fn);
     SelWs w = sel_bind(p, ws);
     if (!dA) w.partA = nullptr;
-    static bool configured = false;
-    if (!configured) {
-        CLA_CUDA_TRY(cudaFuncSetAttribute(sel_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)sizeof(SelBwdSmem)),
-                     fn);
-        configured = true;
-    }
+    static std::atomic<unsigned long long> smem_set{0};
+    st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(sel_bwd_kernel), (int)sizeof(SelBwdSmem));
+    if (st) return st;
     const unsigned int grid = (unsigned int)((size_t)p.gb.n_chunks * B * p.gb.n_cblk);
     sel_bwd_kernel<<<grid, kBwdThreads, sizeof(SelBwdSmem), s>>>(
         reinterpret_cast<const bf16 *>(x), delta, A, reinterpret_cast<const bf16 *>(Bm),

@@ -13,6 +13,10 @@
  *    cudaStream_t; NULL = the legacy default stream) and returns.
  *  - Tensors are dense, row-major, with the innermost dimension last, and
  *    16-byte aligned.  `bf16` arguments are bfloat16 bit patterns (uint16_t).
+ *    A pointer misaligned for the way a kernel reads or writes it (below its
+ *    element size anywhere; below 16 bytes for the tensors loaded or stored
+ *    in 16-byte pieces or by TMA) is rejected with CLA_ERR_INVALID_ARG
+ *    before anything is enqueued.
  *  - Arguments marked [opt] may be NULL: an optional input then means zeros,
  *    an optional output is not written.
  *  - `ws`/`ws_bytes` is caller-owned scratch of at least the size returned by

@@ -104,3 +104,86 @@ def test_binding_refuses_host_tensors(lib):
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         cla.chunk_la_fwd(q, q, q, torch.zeros(1, 1, 8))
+
+
+def test_misaligned_pointers_rejected_without_gpu(lib):
+    """A pointer misaligned for the kernel's loads or stores is refused on the host
+    (CLA_ERR_INVALID_ARG) before anything is enqueued, so it never reaches the GPU."""
+    P, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    d, ws, big = P(256), P(1 << 20), sz(1 << 30)
+    odd2, odd4 = P(258), P(260)  # 2-byte and 4-byte aligned, not 16-byte
+
+    # diagonal scan: fp32 tensors need 4-byte alignment
+    st = lib.cla_scan_diag_fwd(odd2, d, None, d, None, i64(2), i64(64), i64(64), ws, big, None)
+    assert st == 1 and b"aligned" in lib.cla_last_error_message()
+    st = lib.cla_scan_diag_bwd(d, None, d, d, None, d, d, odd2, i64(2), i64(64), i64(64), ws, big, None)
+    assert st == 1
+    st = lib.cla_scan_diag_fwd_noalloc(d, d, odd2, d, None, i64(2), i64(64), i64(64), None)
+    assert st == 1
+
+    # selective scan: bf16 inputs need 2 bytes, fp32 tensors 4
+    st = lib.cla_selective_scan_fwd(P(257), d, d, d, d, None, d, None, None, i64(1), i64(64), i64(64), i64(16),
+                                    ws, big, None)
+    assert st == 1
+    st = lib.cla_selective_scan_fwd(d, odd2, d, d, d, None, d, None, None, i64(1), i64(64), i64(64), i64(16),
+                                    ws, big, None)
+    assert st == 1
+    st = lib.cla_selective_scan_bwd(d, d, d, d, d, None, d, d, None, d, d, odd2, d, d, None, i64(1), i64(64),
+                                    i64(64), i64(16), ws, big, None)
+    assert st == 1
+
+    # chunkwise LA: S0 and dST are read in 16-byte rows; the fp32 vectors need 4 bytes
+    fwd = lib.cla_chunk_la_fwd
+    st = fwd(d, d, d, d, odd4, d, None, i64(1), i64(1), i64(256), i64(64), i64(64), ctypes.c_int(64), ws, big, None)
+    assert st == 1 and b"S0" in lib.cla_last_error_message()
+    st = fwd(d, d, d, odd2, None, d, None, i64(1), i64(1), i64(256), i64(64), i64(64), ctypes.c_int(64), ws, big,
+             None)
+    assert st == 1
+    bwd = lib.cla_chunk_la_bwd
+    st = bwd(d, d, d, d, None, d, odd4, d, d, d, None, None, i64(1), i64(1), i64(256), i64(64), i64(64),
+             ctypes.c_int(64), ws, big, None)
+    assert st == 1 and b"dST" in lib.cla_last_error_message()
+    st = bwd(d, d, d, d, None, d, None, d, d, d, None, odd2, i64(1), i64(1), i64(256), i64(64), i64(64),
+             ctypes.c_int(64), ws, big, None)
+    assert st == 1
+    # the same pointers 16-byte aligned pass validation up to the workspace check
+    st = fwd(d, d, d, d, d, d, None, i64(1), i64(1), i64(256), i64(64), i64(64), ctypes.c_int(64), ws, sz(16), None)
+    assert st == 5  # CLA_ERR_WORKSPACE: too small
+
+
+def test_sizes_whose_counts_would_overflow_are_unsupported(lib):
+    """Sizes whose grid or workspace arithmetic would overflow a 64-bit product are refused
+    (CLA_ERR_UNSUPPORTED) and the size queries return 0, instead of wrapping around."""
+    P, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    d, ws, big = P(256), P(1 << 20), sz(1 << 30)
+    for f in (lib.cla_scan_diag_workspace_size, lib.cla_selective_scan_workspace_size,
+              lib.cla_selective_scan_ckpt_elems, lib.cla_chunk_la_workspace_size, lib.cla_chunk_la_ckpt_size):
+        f.restype = ctypes.c_size_t
+
+    B, T, D = 1 << 24, 1 << 40, 1 << 30  # each within its own limit, product far beyond 2^63
+    assert lib.cla_scan_diag_workspace_size(i64(B), i64(T), i64(D)) == 0
+    st = lib.cla_scan_diag_fwd(d, d, None, d, None, i64(B), i64(T), i64(D), ws, big, None)
+    assert st == 2 and b"out of range" in lib.cla_last_error_message()
+
+    B, T, D = 1 << 20, 1 << 36, 1 << 24
+    assert lib.cla_selective_scan_workspace_size(i64(B), i64(T), i64(D), i64(16)) == 0
+    assert lib.cla_selective_scan_ckpt_elems(i64(B), i64(T), i64(D), i64(16)) == 0
+    st = lib.cla_selective_scan_fwd(d, d, d, d, d, None, d, None, None, i64(B), i64(T), i64(D), i64(16), ws, big,
+                                    None)
+    assert st == 2
+
+    # B * H = 2^64 wraps to 0 in 64-bit arithmetic
+    B = H = 1 << 32
+    args = (i64(B), i64(H), i64(256), i64(64), i64(64), ctypes.c_int(64))
+    assert lib.cla_chunk_la_workspace_size(*args) == 0 and lib.cla_chunk_la_ckpt_size(*args) == 0
+    st = lib.cla_chunk_la_fwd(d, d, d, d, None, d, None, *args, ws, big, None)
+    assert st == 2
+    # B*H within 2^24 but B*H*T beyond 2^40
+    args = (i64(1 << 12), i64(1 << 12), i64(1 << 30), i64(64), i64(64), ctypes.c_int(64))
+    assert lib.cla_chunk_la_workspace_size(*args) == 0
+    st = lib.cla_chunk_la_bwd(d, d, d, d, None, d, None, d, d, d, None, None, *args, ws, big, None)
+    assert st == 2
+    # the workloads' own sizes are unaffected
+    assert lib.cla_chunk_la_workspace_size(i64(1), i64(32), i64(65536), i64(128), i64(128), ctypes.c_int(128)) > 0
+    assert lib.cla_selective_scan_workspace_size(i64(4), i64(8192), i64(2048), i64(16)) > 0
+    assert lib.cla_scan_diag_workspace_size(i64(8), i64(4096), i64(1024)) > 0
