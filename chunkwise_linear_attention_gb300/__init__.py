@@ -85,29 +85,57 @@ def _check(fn: str, status: int) -> None:
         raise ClaError(fn, status, last_error_message())
 
 
-def _stream(stream):
+def _stream(stream, device=None):
+    """The cudaStream_t to launch on: `stream` (a torch.cuda.Stream or a raw handle), else the
+    current stream of `device` (else of the current device)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
+    elif device is not None and isinstance(stream, torch.cuda.Stream) and stream.device != device:
+        raise ValueError(f"stream belongs to {stream.device}, the tensors to {device}")
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _ptr(t, dtype=None, name="tensor"):
-    if t is None:
-        return None
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
-    if dtype is not None and t.dtype != dtype:
-        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
-    return ctypes.c_void_p(t.data_ptr())
+def _dims(t, n, name):
+    if t.dim() != n:
+        raise ValueError(f"{name} must have {n} dimensions, got shape {tuple(t.shape)}")
+    return tuple(t.shape)
+
+
+class _T:
+    """A tensor argument of an entry point (None stays NULL), checked by _launch for what the
+    C ABI cannot check: dtype and shape (the sizes the call passes), then device and layout."""
+
+    __slots__ = ("t", "dtype", "name", "shape")
+
+    def __init__(self, t, dtype, name, shape=None):
+        self.t, self.dtype, self.name, self.shape = t, dtype, name, shape
+
+    def check_meta(self):
+        t = self.t
+        if self.dtype is not None and t.dtype != self.dtype:
+            raise ValueError(f"{self.name} must be {self.dtype}, got {t.dtype}")
+        if self.shape is not None and tuple(t.shape) != tuple(self.shape):
+            raise ValueError(f"{self.name} must have shape {tuple(self.shape)}, got {tuple(t.shape)}")
+
+    def check_place(self, device):
+        t = self.t
+        if not t.is_cuda:
+            raise ValueError(f"{self.name} must be a CUDA tensor")
+        if t.device != device:
+            raise ValueError(f"{self.name} is on {t.device}, the call's first tensor on {device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{self.name} must be contiguous")
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
 
 
 def _ws(nbytes, device, workspace):
     if workspace is None:
         workspace = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
-    if workspace.numel() < nbytes:
-        raise ValueError(f"workspace of {workspace.numel()} bytes < {nbytes} needed")
+    if _nbytes(workspace) < nbytes:
+        raise ValueError(f"workspace of {_nbytes(workspace)} bytes < {nbytes} needed")
     return workspace
 
 
@@ -115,15 +143,29 @@ def _out(t, shape, dtype, device):
     return torch.empty(shape, dtype=dtype, device=device) if t is None else t
 
 
+def _launch(fn, device, args, stream):
+    """Calls entry point `fn` with the tensors' device current: `args` are plain values and _T
+    tensor arguments, every one of which is checked (dtype and shape of all of them first)
+    before its pointer is taken; raises ClaError on a non-OK status."""
+    tensors = [a for a in args if isinstance(a, _T) and a.t is not None]
+    for a in tensors:
+        a.check_meta()
+    for a in tensors:
+        a.check_place(device)
+    cargs = [(None if a.t is None else ctypes.c_void_p(a.t.data_ptr())) if isinstance(a, _T) else a for a in args]
+    with torch.cuda.device(device):
+        _check(fn, getattr(lib(), fn)(*cargs, _stream(stream, device)))
+
+
 def check_status(workspace, stream=None) -> None:
     """Synchronise and raise if a kernel of the last call on `workspace` gave up a wait."""
-    _check("cla_check_status", lib().cla_check_status(_ptr(workspace), _stream(stream)))
+    _launch("cla_check_status", workspace.device, (_T(workspace, None, "workspace"),), stream)
 
 
 def selftest_wait_timeout(workspace, stream=None) -> None:
     """Launch the bounded-wait self-test on `workspace` (>= 256 bytes)."""
-    _check("cla_selftest_wait_timeout",
-           lib().cla_selftest_wait_timeout(_ptr(workspace), workspace.numel(), _stream(stream)))
+    _launch("cla_selftest_wait_timeout", workspace.device,
+            (_T(workspace, None, "workspace"), _nbytes(workspace)), stream)
 
 
 # ---------------------------------------------------------------- diagonal scan
@@ -131,62 +173,54 @@ def scan_diag_workspace_size(B, T, D) -> int:
     return int(lib().cla_scan_diag_workspace_size(B, T, D))
 
 
-def scan_diag_fwd(a, b, h0=None, *, h=None, hT=None, workspace=None, stream=None):
-    """h_t = a_t h_{t-1} + b_t over axis 1 of [B, T, D] (fp32); returns (h, hT)."""
-    B, T, D = a.shape
+def _scan_fwd(fn, a, b, h0, h, hT, workspace, stream, with_ws=True):
+    B, T, D = _dims(a, 3, "a")
     dev = a.device
     f32 = torch.float32
     h = _out(h, (B, T, D), f32, dev)
     hT = _out(hT, (B, D), f32, dev)
-    ws = _ws(scan_diag_workspace_size(B, T, D), dev, workspace)
-    _check("cla_scan_diag_fwd", lib().cla_scan_diag_fwd(
-        _ptr(a, f32, "a"), _ptr(b, f32, "b"), _ptr(h0, f32, "h0"), _ptr(h, f32, "h"), _ptr(hT, f32, "hT"),
-        B, T, D, _ptr(ws), ws.numel(), _stream(stream)))
+    bt, bd = (B, T, D), (B, D)
+    args = (_T(a, f32, "a", bt), _T(b, f32, "b", bt), _T(h0, f32, "h0", bd),
+            _T(h, f32, "h", bt), _T(hT, f32, "hT", bd), B, T, D)
+    if with_ws:
+        ws = _ws(scan_diag_workspace_size(B, T, D), dev, workspace)
+        args += (_T(ws, None, "workspace"), _nbytes(ws))
+    _launch(fn, dev, args, stream)
     return h, hT
+
+
+def scan_diag_fwd(a, b, h0=None, *, h=None, hT=None, workspace=None, stream=None):
+    """h_t = a_t h_{t-1} + b_t over axis 1 of [B, T, D] (fp32); returns (h, hT)."""
+    return _scan_fwd("cla_scan_diag_fwd", a, b, h0, h, hT, workspace, stream)
 
 
 def scan_diag_fwd_blelloch(a, b, h0=None, *, h=None, hT=None, workspace=None, stream=None):
     """scan_diag_fwd with a Blelloch tree across the runs of a chunk (a measured
     alternative to Hillis-Steele); returns (h, hT)."""
-    B, T, D = a.shape
-    dev = a.device
-    f32 = torch.float32
-    h = _out(h, (B, T, D), f32, dev)
-    hT = _out(hT, (B, D), f32, dev)
-    ws = _ws(scan_diag_workspace_size(B, T, D), dev, workspace)
-    _check("cla_scan_diag_fwd_blelloch", lib().cla_scan_diag_fwd_blelloch(
-        _ptr(a, f32, "a"), _ptr(b, f32, "b"), _ptr(h0, f32, "h0"), _ptr(h, f32, "h"), _ptr(hT, f32, "hT"),
-        B, T, D, _ptr(ws), ws.numel(), _stream(stream)))
-    return h, hT
+    return _scan_fwd("cla_scan_diag_fwd_blelloch", a, b, h0, h, hT, workspace, stream)
 
 
 def scan_diag_fwd_noalloc(a, b, h0=None, *, h=None, hT=None, stream=None):
     """scan_diag_fwd without a workspace: the library's static scratch array
     is used (limited size; overlapping calls race).  Returns (h, hT)."""
-    B, T, D = a.shape
-    dev = a.device
-    f32 = torch.float32
-    h = _out(h, (B, T, D), f32, dev)
-    hT = _out(hT, (B, D), f32, dev)
-    _check("cla_scan_diag_fwd_noalloc", lib().cla_scan_diag_fwd_noalloc(
-        _ptr(a, f32, "a"), _ptr(b, f32, "b"), _ptr(h0, f32, "h0"), _ptr(h, f32, "h"), _ptr(hT, f32, "hT"),
-        B, T, D, _stream(stream)))
-    return h, hT
+    return _scan_fwd("cla_scan_diag_fwd_noalloc", a, b, h0, h, hT, None, stream, with_ws=False)
 
 
 def scan_diag_bwd(a, h0, h, dh, dhT=None, *, da=None, db=None, dh0=None, workspace=None, stream=None):
     """Adjoint of scan_diag_fwd; returns (da, db, dh0)."""
-    B, T, D = a.shape
+    B, T, D = _dims(a, 3, "a")
     dev = a.device
     f32 = torch.float32
     da = _out(da, (B, T, D), f32, dev)
     db = _out(db, (B, T, D), f32, dev)
     dh0 = _out(dh0, (B, D), f32, dev)
     ws = _ws(scan_diag_workspace_size(B, T, D), dev, workspace)
-    _check("cla_scan_diag_bwd", lib().cla_scan_diag_bwd(
-        _ptr(a, f32, "a"), _ptr(h0, f32, "h0"), _ptr(h, f32, "h"), _ptr(dh, f32, "dh"), _ptr(dhT, f32, "dhT"),
-        _ptr(da, f32, "da"), _ptr(db, f32, "db"), _ptr(dh0, f32, "dh0"), B, T, D, _ptr(ws), ws.numel(),
-        _stream(stream)))
+    bt, bd = (B, T, D), (B, D)
+    _launch("cla_scan_diag_bwd", dev, (
+        _T(a, f32, "a", bt), _T(h0, f32, "h0", bd), _T(h, f32, "h", bt),
+        _T(dh, f32, "dh", bt), _T(dhT, f32, "dhT", bd), _T(da, f32, "da", bt),
+        _T(db, f32, "db", bt), _T(dh0, f32, "dh0", bd), B, T, D,
+        _T(ws, None, "workspace"), _nbytes(ws)), stream)
     return da, db, dh0
 
 
@@ -199,11 +233,20 @@ def selective_scan_ckpt_elems(B, T, D, N) -> int:
     return int(lib().cla_selective_scan_ckpt_elems(B, T, D, N))
 
 
+def _sel_ckpt_arg(ckpt, B, T, D, N):
+    if ckpt is None:
+        return None
+    need = selective_scan_ckpt_elems(B, T, D, N)
+    if ckpt.numel() < need:
+        raise ValueError(f"ckpt: need at least {need} fp32 values, got {ckpt.numel()}")
+    return _T(ckpt, torch.float32, "ckpt")
+
+
 def selective_scan_fwd(x, delta, A, Bm, Cm, h0=None, *, y=None, hT=None, ckpt=None, want_ckpt=True,
                        workspace=None, stream=None):
     """Selective scan forward; returns (y, hT, ckpt)."""
-    B, T, D = x.shape
-    N = A.shape[1]
+    B, T, D = _dims(x, 3, "x")
+    N = _dims(A, 2, "A")[1]
     dev = x.device
     f32, bf16 = torch.float32, torch.bfloat16
     y = _out(y, (B, T, D), f32, dev)
@@ -211,18 +254,20 @@ def selective_scan_fwd(x, delta, A, Bm, Cm, h0=None, *, y=None, hT=None, ckpt=No
     if ckpt is None and want_ckpt:
         ckpt = torch.empty(selective_scan_ckpt_elems(B, T, D, N), dtype=f32, device=dev)
     ws = _ws(selective_scan_workspace_size(B, T, D, N), dev, workspace)
-    _check("cla_selective_scan_fwd", lib().cla_selective_scan_fwd(
-        _ptr(x, bf16, "x"), _ptr(delta, f32, "delta"), _ptr(A, f32, "A"), _ptr(Bm, bf16, "Bm"),
-        _ptr(Cm, bf16, "Cm"), _ptr(h0, f32, "h0"), _ptr(y, f32, "y"), _ptr(hT, f32, "hT"),
-        _ptr(ckpt, f32, "ckpt"), B, T, D, N, _ptr(ws), ws.numel(), _stream(stream)))
+    btd, btn, bdn = (B, T, D), (B, T, N), (B, D, N)
+    _launch("cla_selective_scan_fwd", dev, (
+        _T(x, bf16, "x", btd), _T(delta, f32, "delta", btd), _T(A, f32, "A", (D, N)),
+        _T(Bm, bf16, "Bm", btn), _T(Cm, bf16, "Cm", btn), _T(h0, f32, "h0", bdn),
+        _T(y, f32, "y", btd), _T(hT, f32, "hT", bdn), _sel_ckpt_arg(ckpt, B, T, D, N),
+        B, T, D, N, _T(ws, None, "workspace"), _nbytes(ws)), stream)
     return y, hT, ckpt
 
 
 def selective_scan_bwd(x, delta, A, Bm, Cm, h0, ckpt, dy, dhT=None, *, dx=None, ddelta=None, dA=None,
                        dB=None, dC=None, dh0=None, want_dA=True, want_dh0=True, workspace=None, stream=None):
     """Selective scan backward; returns (dx, ddelta, dA, dB, dC, dh0)."""
-    B, T, D = x.shape
-    N = A.shape[1]
+    B, T, D = _dims(x, 3, "x")
+    N = _dims(A, 2, "A")[1]
     dev = x.device
     f32, bf16 = torch.float32, torch.bfloat16
     dx = _out(dx, (B, T, D), f32, dev)
@@ -232,12 +277,14 @@ def selective_scan_bwd(x, delta, A, Bm, Cm, h0, ckpt, dy, dhT=None, *, dx=None, 
     dC = _out(dC, (B, T, N), f32, dev)
     dh0 = _out(dh0, (B, D, N), f32, dev) if (want_dh0 or dh0 is not None) else None
     ws = _ws(selective_scan_workspace_size(B, T, D, N), dev, workspace)
-    _check("cla_selective_scan_bwd", lib().cla_selective_scan_bwd(
-        _ptr(x, bf16, "x"), _ptr(delta, f32, "delta"), _ptr(A, f32, "A"), _ptr(Bm, bf16, "Bm"),
-        _ptr(Cm, bf16, "Cm"), _ptr(h0, f32, "h0"), _ptr(ckpt, f32, "ckpt"), _ptr(dy, f32, "dy"),
-        _ptr(dhT, f32, "dhT"), _ptr(dx, f32, "dx"), _ptr(ddelta, f32, "ddelta"), _ptr(dA, f32, "dA"),
-        _ptr(dB, f32, "dB"), _ptr(dC, f32, "dC"), _ptr(dh0, f32, "dh0"), B, T, D, N, _ptr(ws), ws.numel(),
-        _stream(stream)))
+    btd, btn, bdn = (B, T, D), (B, T, N), (B, D, N)
+    _launch("cla_selective_scan_bwd", dev, (
+        _T(x, bf16, "x", btd), _T(delta, f32, "delta", btd), _T(A, f32, "A", (D, N)),
+        _T(Bm, bf16, "Bm", btn), _T(Cm, bf16, "Cm", btn), _T(h0, f32, "h0", bdn),
+        _sel_ckpt_arg(ckpt, B, T, D, N), _T(dy, f32, "dy", btd), _T(dhT, f32, "dhT", bdn),
+        _T(dx, f32, "dx", btd), _T(ddelta, f32, "ddelta", btd), _T(dA, f32, "dA", (D, N)),
+        _T(dB, f32, "dB", btn), _T(dC, f32, "dC", btn), _T(dh0, f32, "dh0", bdn),
+        B, T, D, N, _T(ws, None, "workspace"), _nbytes(ws)), stream)
     return dx, ddelta, dA, dB, dC, dh0
 
 
@@ -253,39 +300,41 @@ def chunk_la_ckpt_size(B, H, T, dim_k, dim_v, chunk) -> int:
 
 def chunk_la_ckpt(q, v, *, chunk=64):
     """A device buffer (fp32) for the checkpoint of a forward on q [B, H, T, dk], v [.., dv]."""
-    B, H, T, dk = q.shape
+    B, H, T, dk = _dims(q, 4, "q")
     n = chunk_la_ckpt_size(B, H, T, dk, v.shape[-1], chunk) // 4
     return torch.empty(max(n, 1), dtype=torch.float32, device=q.device)
 
 
-def _ckpt_ptr(ckpt, B, H, T, dk, dv, chunk):
+def _ckpt_arg(ckpt, B, H, T, dk, dv, chunk):
     if ckpt is None:
         return None
     need = chunk_la_ckpt_size(B, H, T, dk, dv, chunk)
-    if ckpt.numel() * ckpt.element_size() < need:
-        raise ValueError(f"ckpt: need at least {need} bytes, got {ckpt.numel() * ckpt.element_size()}")
-    return _ptr(ckpt, torch.float32, "ckpt")
+    if _nbytes(ckpt) < need:
+        raise ValueError(f"ckpt: need at least {need} bytes, got {_nbytes(ckpt)}")
+    return _T(ckpt, torch.float32, "ckpt")
 
 
 def chunk_la_fwd(q, k, v, log_decay, S0=None, *, chunk=64, o=None, ST=None, ckpt=None, workspace=None,
                  stream=None):
     """Chunkwise decayed linear attention forward; returns (o, ST).  With ckpt (see
     chunk_la_ckpt) it also saves the state entering each segment for chunk_la_bwd."""
-    B, H, T, dk = q.shape
-    dv = v.shape[-1]
+    B, H, T, dk = _dims(q, 4, "q")
+    dv = _dims(v, 4, "v")[3]
     dev = q.device
     f32, bf16 = torch.float32, torch.bfloat16
     o = _out(o, (B, H, T, dv), f32, dev)
     ST = _out(ST, (B, H, dk, dv), f32, dev)
     ws = _ws(chunk_la_workspace_size(B, H, T, dk, dv, chunk), dev, workspace)
-    args = (_ptr(q, bf16, "q"), _ptr(k, bf16, "k"), _ptr(v, bf16, "v"), _ptr(log_decay, f32, "log_decay"),
-            _ptr(S0, f32, "S0"), _ptr(o, f32, "o"), _ptr(ST, f32, "ST"))
-    tail = (B, H, T, dk, dv, int(chunk), _ptr(ws), ws.numel(), _stream(stream))
+    tk, tv, st = (B, H, T, dk), (B, H, T, dv), (B, H, dk, dv)
+    args = (_T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
+            _T(log_decay, f32, "log_decay", (B, H, T)), _T(S0, f32, "S0", st),
+            _T(o, f32, "o", tv), _T(ST, f32, "ST", st))
+    tail = (B, H, T, dk, dv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws))
     if ckpt is None:
-        _check("cla_chunk_la_fwd", lib().cla_chunk_la_fwd(*args, *tail))
+        _launch("cla_chunk_la_fwd", dev, args + tail, stream)
     else:
-        _check("cla_chunk_la_fwd_ckpt", lib().cla_chunk_la_fwd_ckpt(
-            *args, _ckpt_ptr(ckpt, B, H, T, dk, dv, chunk), *tail))
+        _launch("cla_chunk_la_fwd_ckpt", dev, args + (_ckpt_arg(ckpt, B, H, T, dk, dv, chunk),) + tail,
+                stream)
     return o, ST
 
 
@@ -293,8 +342,8 @@ def chunk_la_bwd(q, k, v, log_decay, S0, dO, dST=None, *, chunk=64, dq=None, dk=
                  dlog_decay=None, dS0=None, ckpt=None, workspace=None, stream=None):
     """Chunkwise decayed linear attention backward; returns (dq, dk, dv, dlog_decay, dS0).  ckpt:
     the checkpoint a chunk_la_fwd on the same inputs saved (its states are then not rebuilt)."""
-    B, H, T, dkk = q.shape
-    dvv = v.shape[-1]
+    B, H, T, dkk = _dims(q, 4, "q")
+    dvv = _dims(v, 4, "v")[3]
     dev = q.device
     f32, bf16 = torch.float32, torch.bfloat16
     dq = _out(dq, (B, H, T, dkk), f32, dev)
@@ -303,13 +352,16 @@ def chunk_la_bwd(q, k, v, log_decay, S0, dO, dST=None, *, chunk=64, dq=None, dk=
     dlog_decay = _out(dlog_decay, (B, H, T), f32, dev)
     dS0 = _out(dS0, (B, H, dkk, dvv), f32, dev)
     ws = _ws(chunk_la_workspace_size(B, H, T, dkk, dvv, chunk), dev, workspace)
-    args = (_ptr(q, bf16, "q"), _ptr(k, bf16, "k"), _ptr(v, bf16, "v"), _ptr(log_decay, f32, "log_decay"),
-            _ptr(S0, f32, "S0"), _ptr(dO, bf16, "dO"), _ptr(dST, f32, "dST"), _ptr(dq, f32, "dq"),
-            _ptr(dk, f32, "dk"), _ptr(dv, f32, "dv"), _ptr(dlog_decay, f32, "dlog_decay"), _ptr(dS0, f32, "dS0"))
-    tail = (B, H, T, dkk, dvv, int(chunk), _ptr(ws), ws.numel(), _stream(stream))
+    tk, tv, st, bht = (B, H, T, dkk), (B, H, T, dvv), (B, H, dkk, dvv), (B, H, T)
+    args = (_T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
+            _T(log_decay, f32, "log_decay", bht), _T(S0, f32, "S0", st),
+            _T(dO, bf16, "dO", tv), _T(dST, f32, "dST", st), _T(dq, f32, "dq", tk),
+            _T(dk, f32, "dk", tk), _T(dv, f32, "dv", tv),
+            _T(dlog_decay, f32, "dlog_decay", bht), _T(dS0, f32, "dS0", st))
+    tail = (B, H, T, dkk, dvv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws))
     if ckpt is None:
-        _check("cla_chunk_la_bwd", lib().cla_chunk_la_bwd(*args, *tail))
+        _launch("cla_chunk_la_bwd", dev, args + tail, stream)
     else:
-        _check("cla_chunk_la_bwd_ckpt", lib().cla_chunk_la_bwd_ckpt(
-            *args, _ckpt_ptr(ckpt, B, H, T, dkk, dvv, chunk), *tail))
+        _launch("cla_chunk_la_bwd_ckpt", dev, args + (_ckpt_arg(ckpt, B, H, T, dkk, dvv, chunk),) + tail,
+                stream)
     return dq, dk, dv, dlog_decay, dS0

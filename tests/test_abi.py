@@ -187,3 +187,46 @@ def test_sizes_whose_counts_would_overflow_are_unsupported(lib):
     assert lib.cla_chunk_la_workspace_size(i64(1), i64(32), i64(65536), i64(128), i64(128), ctypes.c_int(128)) > 0
     assert lib.cla_selective_scan_workspace_size(i64(4), i64(8192), i64(2048), i64(16)) > 0
     assert lib.cla_scan_diag_workspace_size(i64(8), i64(4096), i64(1024)) > 0
+
+
+def test_binding_checks_shapes_before_anything_else(lib):
+    """The binding checks every tensor's dtype and shape against the sizes it passes (the C ABI
+    sees bare pointers and cannot), for all arguments before any device check."""
+    import torch
+
+    import chunkwise_linear_attention_gb300 as cla
+
+    f32, bf16 = torch.float32, torch.bfloat16
+    a = torch.rand(2, 8, 4)
+
+    def raises(fn, *args, match, **kw):
+        with pytest.raises(ValueError, match=match):
+            fn(*args, **kw)
+
+    raises(cla.scan_diag_fwd, a, torch.rand(2, 8, 3), match=r"b must have shape \(2, 8, 4\)")
+    raises(cla.scan_diag_fwd, a, a, torch.rand(2, 5), match="h0 must have shape")
+    raises(cla.scan_diag_fwd, a, a, h=torch.empty(2, 8, 5), match="h must have shape")
+    raises(cla.scan_diag_fwd, a, a.double(), match="b must be torch.float32")
+    raises(cla.scan_diag_fwd, torch.rand(8, 4), a, match="a must have 3 dimensions")
+    raises(cla.scan_diag_fwd_noalloc, a, a, hT=torch.empty(3, 4), match="hT must have shape")
+    raises(cla.scan_diag_bwd, a, None, a, torch.rand(2, 7, 4), match="dh must have shape")
+
+    x = torch.zeros(1, 64, 32, dtype=bf16)
+    A = torch.zeros(32, 16)
+    Bm = torch.zeros(1, 64, 16, dtype=bf16)
+    raises(cla.selective_scan_fwd, x, torch.zeros(1, 64, 32), A, Bm, torch.zeros(1, 64, 8, dtype=bf16),
+           match="Cm must have shape")
+    raises(cla.selective_scan_fwd, x, torch.zeros(1, 64, 32), torch.zeros(31, 16), Bm, Bm, match="A must have shape")
+    raises(cla.selective_scan_bwd, x, torch.zeros(1, 64, 32), A, Bm, Bm, None, torch.zeros(3), torch.zeros(1, 64, 32),
+           match="ckpt: need at least")
+
+    q = torch.zeros(1, 2, 16, 64, dtype=bf16)
+    ld = torch.zeros(1, 2, 16)
+    raises(cla.chunk_la_fwd, q, q, q, torch.zeros(1, 2, 15), match="log_decay must have shape")
+    raises(cla.chunk_la_fwd, q, q, q, ld, torch.zeros(1, 2, 64, 32), match="S0 must have shape")
+    raises(cla.chunk_la_fwd, q, q.float(), q, ld, match="k must be torch.bfloat16")
+    raises(cla.chunk_la_fwd, q, q, q, ld, ckpt=torch.zeros(1), match="ckpt: need at least")
+    raises(cla.chunk_la_bwd, q, q, q, ld, None, torch.zeros(1, 2, 16, 32, dtype=bf16), match="dO must have shape")
+    raises(cla.chunk_la_bwd, q, q, q, ld, None, q, dST=torch.zeros(2, 64, 64), match="dST must have shape")
+    # with every shape right, the first host tensor stops the call
+    raises(cla.chunk_la_bwd, q, q, q, ld, None, q, match="q must be a CUDA tensor")
