@@ -1,25 +1,34 @@
-"""Precision model of a tensor-core forward for gated linear attention (one decay per key
-dimension), against the float64 oracle: which operands a kernel must carry beyond one bf16
-rounding to stay inside the bf16-path tolerance (max 2e-2 and mean 5e-3 of the output RMS).
+"""Precision model of a tensor-core gated linear attention (one decay per key dimension),
+forward and backward, against the float64 oracle: which operands a kernel must carry beyond one
+bf16 rounding to stay inside the bf16-path tolerance (max 2e-2 and mean 5e-3 of each output's RMS).
 
 With scalar decays the decay multiplies the scores after the product ("Parallel Scan", "The
-chunkwise algorithm").  With a decay per key dimension it sits inside the contraction, so it
-has to scale the operands before the product:
+chunkwise algorithm").  With a decay per key dimension it sits inside the contraction over keys,
+so it scales the operands.  With c the in-chunk cumulative log2 decays (fp32) and 64-token blocks
+(the smallest tensor-core tile height):
 
-* scores of a query block R and an earlier key block S' (64 tokens each, the smallest
-  tensor-core tile height): (Q_R * 2^(c - c_e)) (K_S' * 2^(c_e - c))^T, e the last token of S'
-  (both factors <= 1);
-* scores inside a diagonal 64-token block, in one product: the same with e the block's 32nd
-  token, so each factor is at most the decay over 32 tokens (finite while that stays within
-  2^126; stronger decays need a slower path);
-* inter-chunk read (Q * 2^c) S and state update (K * 2^(c_L - c))^T V,
+* scores of a query block and an earlier key block: (Q * 2^(c - c_e)) (K * 2^(c_e - c))^T, e the
+  key block's last token (both factors <= 1); inside a diagonal block, e its 32nd token, so each
+  factor is at most the decay over 32 tokens (finite while that stays within 2^126; stronger
+  decays need a slower path);
+* inter-chunk read (Q * 2^c) S and state update (K * 2^(c_L - c))^T V;
+* backward, dQ of a query block: 2^(c - c_m) * [tril(dO V^T) (K * 2^(c_m - c)) + dO (2^c_m * S)^T],
+  and dK of a key block the same with Q and the adjoint state, m the block's 32nd token (a
+  reference at the block's first token spans 64 tokens of decay and overflows sooner); dV from
+  the scores as in the forward; the decay gradient by the closed form
+  sum_{t>=u} (q_t * dq_t - k_t * dk_t) plus the final-state term.
 
-with c the in-chunk cumulative log2 decays (fp32).  Products accumulate in fp32; the scaled
-operands are rounded once to bf16, split into bf16 high and low parts (|x - hi - lo| < 2^-16|x|),
-or passed as tf32 (the tensor core reads an fp32 operand's upper 19 bits).  The model shows
-that one bf16 rounding of the scaled Q and K misses the max-error bound once decays are strong,
-and that tf32 Q and K, with the scores and the state split into bf16 parts as in the scalar
-kernel, stay well inside it for every decay strength up to that range limit.
+Each MMA takes both operands in one kind.  A scaled operand is rounded once to bf16, split into
+bf16 high and low parts (three products: hi.hi + hi.lo + lo.hi, |x - hi - lo| < 2^-16|x|), or
+passed as tf32 (the tensor core reads an fp32 operand's upper 19 bits); products accumulate in
+fp32.  The model shows:
+
+* forward: tf32 scaled operands (scores, inter-chunk read, state update) with the masked scores
+  split into bf16 parts for P.V stay well inside the bound; one bf16 rounding misses it under
+  strong decay;
+* backward: tf32 everywhere passes for dq, dk, dv and dS0, but the decay gradient (suffix sums of
+  q.dq - k.dk, which cancel when decays are strong) then misses the bound; split dQ and dK
+  contractions bring it well inside.
 """
 import numpy as np
 import pytest
@@ -68,6 +77,7 @@ def _model_fwd(q, k, v, la, S0, Tc, qk, state, scores, blk=64):
         o[t0:t0 + n] = _operand(P, scores) @ V + _operand(Q * np.exp2(c.astype(np.float32)), qk) @ _operand(S, state)
         cL = c[n - 1]
         S = np.exp2(cL.astype(np.float32))[:, None] * S + _operand(K * np.exp2((cL - c).astype(np.float32)), qk).T @ V
+        # (V is exact in bf16 and in tf32, so it needs no rounding of its own)
         S = S.astype(np.float32).astype(np.float64)
     return o, S
 
@@ -110,7 +120,7 @@ def test_decays_stay_within_the_midpoint_range(case):
 @pytest.mark.parametrize("Tc", [64, 128])
 def test_tf32_scaled_operands_meet_the_tolerance(case, Tc):
     name, inp, ro, rST = case
-    o, ST = _model_fwd(*inp, Tc, qk="tf32", state="split", scores="split")
+    o, ST = _model_fwd(*inp, Tc, qk="tf32", state="tf32", scores="split")
     emax, emean = _errors(o, ro)
     assert emax <= 1.2e-2 and emean <= 1e-3, (name, Tc, emax, emean)
     assert _errors(ST, rST)[0] <= 5e-3, name
@@ -130,3 +140,121 @@ def test_one_bf16_rounding_of_scaled_operands_misses_the_bound_under_strong_deca
     ro = oracle.gla_fwd(*(x[None, None] for x in (q, k, v, la)), S0[None, None])[0][0, 0]
     o, _ = _model_fwd(q, k, v, la, S0, 128, qk="bf16", state="split", scores="split")
     assert _errors(o, ro)[0] > 2e-2
+
+
+# ----------------------------------------------------------------------------- backward
+def _f32(x):
+    return np.asarray(x, np.float32).astype(np.float64)
+
+
+def _e2(x):
+    return _f32(np.exp2(np.asarray(x, np.float32)))
+
+
+def _cum(la):
+    return np.cumsum((la * L2E).astype(np.float32), axis=0, dtype=np.float32).astype(np.float64)
+
+
+def _scores(Q, K, c, kind, blk=64):
+    """Masked decayed scores of one chunk, with the forward's block references."""
+    n = Q.shape[0]
+    P = np.zeros((n, n))
+    for R in range(0, n, blk):
+        rr = slice(R, min(R + blk, n))
+        for Sb in range(0, R + 1, blk):
+            ss = slice(Sb, min(Sb + blk, n))
+            e = c[min(Sb + blk, n) - 1] if Sb < R else c[min(R + blk // 2, n) - 1]
+            bp = _operand(Q[rr] * _e2(c[rr] - e), kind) @ _operand(K[ss] * _e2(e - c[ss]), kind).T
+            P[rr, ss] = np.tril(bp) if Sb == R else bp
+    return _f32(P)
+
+
+def _model_bwd(q, k, v, la, S0, dO, dST, Tc, grad_kind, ref="mid", blk=64):
+    """dq, dk, dv, dlog_a, dS0; `grad_kind` is the operand kind of the dQ and dK contractions,
+    tf32 elsewhere; `ref` the reference token of a dQ/dK block ("mid": its 32nd, "start": the
+    token before it)."""
+    T, d = q.shape
+    starts = list(range(0, T, Tc))
+    states, S = [], S0.copy()  # state entering each chunk, rebuilt as the dQ traversal does
+    for t0 in starts:
+        K, V, c = k[t0:t0 + Tc], v[t0:t0 + Tc], _cum(la[t0:t0 + Tc])
+        states.append(S)
+        S = _f32(_e2(c[-1])[:, None] * S + _operand(K * _e2(c[-1] - c), "tf32").T @ V)
+    ST = S
+
+    def ref_of(c, B0, n):
+        if ref == "mid":
+            return c[min(B0 + blk // 2, n) - 1]
+        return c[B0 - 1] if B0 > 0 else np.zeros(d)
+
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for j, t0 in enumerate(starts):  # forward order: dQ
+        K, V, G, c = k[t0:t0 + Tc], v[t0:t0 + Tc], dO[t0:t0 + Tc], _cum(la[t0:t0 + Tc])
+        n = K.shape[0]
+        A = _f32(np.tril(G @ V.T))
+        for R in range(0, n, blk):
+            hi = min(R + blk, n)
+            m = ref_of(c, R, n)
+            acc = _operand(A[R:hi, :hi], grad_kind) @ _operand(K[:hi] * _e2(m - c[:hi]), grad_kind)
+            acc += _operand(G[R:hi], grad_kind) @ _operand(_e2(m)[:, None] * states[j], grad_kind).T
+            dq[t0 + R:t0 + hi] = _f32(_e2(c[R:hi] - m) * _f32(acc))
+    dS = dST.copy()
+    for t0 in reversed(starts):  # reverse order: dK, dV with the adjoint state
+        Q, K, V, G, c = q[t0:t0 + Tc], k[t0:t0 + Tc], v[t0:t0 + Tc], dO[t0:t0 + Tc], _cum(la[t0:t0 + Tc])
+        n, cL = Q.shape[0], c[-1]
+        A = _f32(np.tril(G @ V.T))
+        dv[t0:t0 + n] = _f32(_operand(_scores(Q, K, c, "tf32"), "split").T @ G
+                             + _operand(K * _e2(cL - c), "tf32") @ _operand(dS, "tf32"))
+        for Sb in range(0, n, blk):
+            hi = min(Sb + blk, n)
+            m = ref_of(c, Sb, n)
+            acc = _operand(A[Sb:, Sb:hi].T, grad_kind) @ _operand(Q[Sb:] * _e2(c[Sb:] - m), grad_kind)
+            acc += _operand(V[Sb:hi], grad_kind) @ _operand(_e2(cL - m)[:, None] * dS, grad_kind).T
+            dk[t0 + Sb:t0 + hi] = _f32(_e2(m - c[Sb:hi]) * _f32(acc))
+        dS = _f32(_e2(cL)[:, None] * dS + _operand(Q * _e2(c), "tf32").T @ G)
+    dl = np.cumsum((q * dq - k * dk)[::-1], axis=0)[::-1] + np.sum(dST * ST, axis=1)[None, :]
+    return dq, dk, dv, dl, dS
+
+
+@pytest.fixture(scope="module", params=list(REGIMES))
+def bwd_case(request):
+    q, k, v, la, S0 = _inputs(5, 768, 128, *REGIMES[request.param])
+    rng = np.random.default_rng(9)
+    dO = _bf16_rn(rng.standard_normal((768, 128)))
+    dST = _f32(rng.standard_normal((128, 128)) * 0.1)
+    ref = oracle.gla_bwd(*(x[None, None] for x in (q, k, v, la, S0, dO)), dST[None, None])
+    return request.param, (q, k, v, la, S0, dO, dST), [x[0, 0] for x in ref]
+
+
+NAMES = ("dq", "dk", "dv", "dlog_a", "dS0")
+
+
+@pytest.mark.parametrize("Tc", [64, 128])
+def test_backward_with_split_dq_dk_contractions_meets_the_tolerance(bwd_case, Tc):
+    name, inp, ref = bwd_case
+    got = _model_bwd(*inp, Tc, grad_kind="split")
+    for nm, g, r in zip(NAMES, got, ref):
+        emax, emean = _errors(g, r)
+        assert emax <= 1.2e-2 and emean <= 1e-3, (name, Tc, nm, emax, emean)
+
+
+def test_all_tf32_backward_loses_the_decay_gradient_under_strong_decay(bwd_case):
+    """dq, dk, dv and dS0 pass with tf32 everywhere; the decay gradient's suffix sums of
+    q.dq - k.dk cancel and magnify their rounding once decays are strong."""
+    name, inp, ref = bwd_case
+    got = _model_bwd(*inp, 128, grad_kind="tf32")
+    for nm, g, r in list(zip(NAMES, got, ref))[:3] + [(NAMES[4], got[4], ref[4])]:
+        assert _errors(g, r)[0] <= 1.2e-2, (name, nm)
+    if name != "long-context recipe":
+        assert _errors(got[3], ref[3])[0] > 2e-2, name
+
+
+def test_block_start_references_overflow_where_midpoints_do_not():
+    q, k, v, la, S0 = _inputs(5, 768, 128, *REGIMES["near the range limit"])
+    rng = np.random.default_rng(9)
+    dO = _bf16_rn(rng.standard_normal((768, 128)))
+    dST = np.zeros((128, 128))
+    with np.errstate(over="ignore", invalid="ignore"):
+        start = _model_bwd(q, k, v, la, S0, dO, dST, 128, grad_kind="split", ref="start")
+    mid = _model_bwd(q, k, v, la, S0, dO, dST, 128, grad_kind="split", ref="mid")
+    assert not np.isfinite(start[0]).all() and np.isfinite(mid[0]).all()
