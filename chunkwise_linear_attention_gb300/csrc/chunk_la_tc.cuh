@@ -5,12 +5,12 @@
 // documented there:
 //     P       = X Y^T                     (M = Tc, N = Tc, K = DX)   smem x smem
 //     O_inter = X S_hi + X S_lo           (M = Tc, N = 64, K = DX)   smem x smem
-//     dS      = Y^T Zs_hi + Y^T Zs_lo     (M = DX, N = 64, K = Tc)   smem x smem
+//     dS      = Y^T [Zs_hi | Zs_lo]       (M = DX, N = 128, K = Tc)  smem x smem
 //     O_intra = P_hi Z + P_lo Z           (M = Tc, N = 64, K = Tc)   tmem x smem
 // where Zs = diag(w_state) Z and P is masked and decayed in registers between
 // the first and the last product, split into two bf16 parts and written back
 // to TMEM as the A operand.  OUT = O_intra + diag(w_out) O_inter, State =
-// alpha State + dS.  A value x split into bf16 parts is x = hi + lo + e with
+// alpha State + (dS_hi + dS_lo), the two 64-column halves of the dS product.  A value x split into bf16 parts is x = hi + lo + e with
 // |e| < 2^-16 |x| (both parts by truncation, see split_bf16x2).
 //
 // Warp roles.  Warp 8 (the producer) issues every TMA load and every MMA
