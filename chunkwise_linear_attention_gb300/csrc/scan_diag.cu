@@ -11,8 +11,9 @@
 // channels):
 //   lane = (sub, cg): cg in 0..3 picks 4 adjacent channels (one float4),
 //   sub in 0..7 picks a run of L consecutive steps.  A warp load instruction
-//   touches 8 rows x 64 contiguous bytes; the 8 warps of a block cover 128
-//   adjacent channels, so every 128-byte line is consumed by one block.
+//   touches 8 rows x 64 contiguous bytes; the 4 warps of a block cover 64
+//   adjacent channels (two whole 128-byte lines per row), so every line is
+//   consumed by one block.
 // Per tile:
 //   1. every lane loads its L rows of (a, b) into registers (16-byte loads);
 //   2. composes them sequentially into one pair (A, B) per channel;
