@@ -30,9 +30,13 @@
 // from that state and writes OUT.  Phase 2 re-reads the segment's Y and Z,
 // which phase 1 read shortly before (L2-resident for the segment sizes used).
 //
-// Tensor-core products use mma.sync m16n8k16 (bf16 in, fp32 accumulate) on
-// tiles staged in shared memory with cp.async (double-buffered) and XOR-
-// swizzled rows; the state is kept in fp32 registers.  The three operands that
+// Two kernels implement the template.  la_tc_kernel (chunk_la_tc.cuh) runs
+// every sequence with at least one full chunk: tcgen05 MMAs with the
+// accumulators in tensor memory, TMA tile loads and stores, warp-specialised.
+// la_chunk_kernel below runs the shorter ones (the TMA boxes are one chunk
+// tall): mma.sync m16n8k16 (bf16 in, fp32 accumulate) on tiles staged in
+// shared memory with cp.async (double-buffered) and XOR-swizzled rows.  Both
+// keep the state in fp32 registers.  The three operands that
 // are not inputs -- the masked scores, the state fed to the X State product
 // and w_state * Z in the state update -- are each split into a high and a low
 // bf16 part (two MMAs), so their rounding stays far below the fp32 outputs'
