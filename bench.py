@@ -170,6 +170,66 @@ def replica_throughput(world, bytes_per_step, slowest_step_ms):
     return world * bytes_per_step / (slowest_step_ms / 1e3) / 1e9
 
 
+# ------------------------------------------------------------------ end to end
+def e2e_pipelined(torch, dev, host_in, host_out, compute, n, dist_on=False):
+    """Mean ms per step of `n` end-to-end steps: each step copies every pinned host input to
+    the device, runs compute(device_inputs, device_outputs, stream) and copies every output
+    back to its pinned host buffer.  Steps are pipelined over three streams (inputs of step
+    i + 1, compute of step i and outputs of step i - 1 overlap: the host link is full duplex)
+    with device buffers in two sets; the timed region ends when the last outputs are on the
+    host."""
+    for v in host_out.values():
+        v.zero_()  # touch the pages before timing
+    sets = [({k: torch.empty_like(v, device=dev) for k, v in host_in.items()},
+             {k: torch.empty_like(v, device=dev) for k, v in host_out.items()}) for _ in range(2)]
+    s_in, s_cp, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def ev():
+        return torch.cuda.Event()
+
+    def run(n):
+        done_cp = [None, None]   # compute of the step that last used each set
+        done_out = [None, None]  # output copies of the step that last used each set
+        last_out = None
+        for i in range(n):
+            di, do = sets[i % 2]
+            if done_cp[i % 2] is not None:
+                s_in.wait_event(done_cp[i % 2])  # the set's inputs were consumed
+            with torch.cuda.stream(s_in):
+                for k in host_in:
+                    di[k].copy_(host_in[k], non_blocking=True)
+            e_in = ev()
+            e_in.record(s_in)
+            s_cp.wait_event(e_in)
+            if done_out[i % 2] is not None:
+                s_cp.wait_event(done_out[i % 2])  # the set's outputs were copied out
+            compute(di, do, s_cp)
+            e_cp = ev()
+            e_cp.record(s_cp)
+            done_cp[i % 2] = e_cp
+            s_out.wait_event(e_cp)
+            with torch.cuda.stream(s_out):
+                for k in host_out:
+                    host_out[k].copy_(do[k], non_blocking=True)
+            last_out = ev()
+            last_out.record(s_out)
+            done_out[i % 2] = last_out
+        return last_out
+
+    run(2)
+    torch.cuda.synchronize()
+    s, e = _events(torch)
+    _sync_all(torch, dist_on)
+    s.record(s_in)
+    last = run(n)
+    s_in.wait_event(last)  # the last outputs are on the host (they follow every earlier copy and kernel)
+    e.record(s_in)
+    _sync_all(torch, dist_on)
+    ms = s.elapsed_time(e) / n
+    del sets
+    return ms
+
+
 # ------------------------------------------------------------------ headline: diagonal scan
 def bench_scan(torch, cla, workloads, dev, steps, warmup, dist_on):
     inp = workloads.make("scan")
@@ -188,7 +248,7 @@ def bench_scan(torch, cla, workloads, dev, steps, warmup, dist_on):
         ev[0].record(stream)
         cla.scan_diag_fwd(a, b, h0, h=h, hT=hT, workspace=ws, stream=stream)
         ev[1].record(stream)
-        cla.scan_diag_bwd(a, h0, h, dh, da=da, db=db, dh0=dh0, workspace=ws, stream=stream)
+        cla.scan_diag_bwd(a, None, h0, h, dh, da=da, db=db, dh0=dh0, workspace=ws, stream=stream)
         ev[2].record(stream)
 
     for _ in range(warmup):
@@ -209,68 +269,22 @@ def bench_scan(torch, cla, workloads, dev, steps, warmup, dist_on):
     step_ms = statistics.mean(f + b_ for f, b_ in zip(fwd, bwd))
     res = dict(n=n, B=B, T=T, D=D, step_ms=step_ms, fwd_ms=statistics.mean(fwd), bwd_ms=statistics.mean(bwd),
                bytes_fwd=12 * n, bytes_bwd=20 * n, wall_s=t_wall, launches=2 * steps)
-    # e2e: pinned host inputs -> device, fwd + bwd, outputs -> host, every step; steps are
-    # pipelined over three streams (inputs of step i + 1, compute of step i and outputs of
-    # step i - 1 overlap: the host link is full duplex) with device buffers in two sets.
+    # e2e: pinned host inputs -> device, fwd + bwd, outputs -> host, every step
     host_in = {k: inp[k].pin_memory() for k in ("a", "b", "h0", "dh")}
     host_out = {"h": torch.empty(B, T, D).pin_memory(), "hT": torch.empty(B, D).pin_memory(),
                 "da": torch.empty(B, T, D).pin_memory(), "db": torch.empty(B, T, D).pin_memory(),
                 "dh0": torch.empty(B, D).pin_memory()}
-    for v in host_out.values():
-        v.zero_()  # touch the pages before timing
-    sets = [({k: torch.empty_like(v, device=dev) for k, v in host_in.items()},
-             {k: torch.empty_like(v, device=dev) for k, v in host_out.items()}) for _ in range(2)]
-    s_in, s_cp, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    e2e_steps = max(3, min(steps, 20))
 
-    def ev():
-        return torch.cuda.Event()
+    def compute(di, do, s):
+        cla.scan_diag_fwd(di["a"], di["b"], di["h0"], h=do["h"], hT=do["hT"], workspace=ws, stream=s)
+        cla.scan_diag_bwd(di["a"], None, di["h0"], do["h"], di["dh"], da=do["da"], db=do["db"], dh0=do["dh0"],
+                          workspace=ws, stream=s)
 
-    def run_e2e(n):
-        done_cp = [None, None]   # compute of the step that last used each set
-        done_out = [None, None]  # output copies of the step that last used each set
-        last_out = None
-        for i in range(n):
-            di, do = sets[i % 2]
-            if done_cp[i % 2] is not None:
-                s_in.wait_event(done_cp[i % 2])  # the set's inputs were consumed
-            with torch.cuda.stream(s_in):
-                for k in host_in:
-                    di[k].copy_(host_in[k], non_blocking=True)
-            e_in = ev()
-            e_in.record(s_in)
-            s_cp.wait_event(e_in)
-            if done_out[i % 2] is not None:
-                s_cp.wait_event(done_out[i % 2])  # the set's outputs were copied out
-            cla.scan_diag_fwd(di["a"], di["b"], di["h0"], h=do["h"], hT=do["hT"], workspace=ws, stream=s_cp)
-            cla.scan_diag_bwd(di["a"], di["h0"], do["h"], di["dh"], da=do["da"], db=do["db"], dh0=do["dh0"],
-                              workspace=ws, stream=s_cp)
-            e_cp = ev()
-            e_cp.record(s_cp)
-            done_cp[i % 2] = e_cp
-            s_out.wait_event(e_cp)
-            with torch.cuda.stream(s_out):
-                for k in host_out:
-                    host_out[k].copy_(do[k], non_blocking=True)
-            last_out = ev()
-            last_out.record(s_out)
-            done_out[i % 2] = last_out
-        return last_out
-
-    run_e2e(2)
-    torch.cuda.synchronize()
-    s, e = _events(torch)
-    _sync_all(torch, dist_on)
-    s.record(s_in)
-    last = run_e2e(e2e_steps)
-    s_in.wait_event(last)  # the last outputs are on the host (they follow every earlier copy and kernel)
-    e.record(s_in)
-    _sync_all(torch, dist_on)
-    res["e2e_ms"] = s.elapsed_time(e) / e2e_steps
+    res["e2e_ms"] = e2e_pipelined(torch, dev, host_in, host_out, compute, max(3, min(steps, 20)), dist_on)
     cla.check_status(ws)
     res["h2d_bytes"] = sum(v.numel() * v.element_size() for v in host_in.values())
     res["d2h_bytes"] = sum(v.numel() * v.element_size() for v in host_out.values())
-    del a, b, h0, dh, h, da, db, sets, host_in, host_out
+    del a, b, h0, dh, h, da, db, host_in, host_out
     return res
 
 
@@ -331,7 +345,32 @@ def bench_scan_blelloch(torch, cla, workloads, dev, flush, peaks, iters=20, shap
             "hillis_steele_GBps": round(by / ms_hs / 1e6, 1), "blelloch_GBps": round(by / ms_bl / 1e6, 1)}
 
 
-def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=20, shape=None):
+def bench_scan_bwd_recompute(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
+    """Backward diagonal scan on the headline workload given the forward's states h (read:
+    a, h, dh; written: da, db) and without them (read: a, b, dh; states rebuilt from the state
+    entering each chunk, which a forward pass without h output writes first)."""
+    inp = workloads.make("scan", **(shape or {}))
+    a, b, h0, dh = (inp[k].to(dev) for k in ("a", "b", "h0", "dh"))
+    B, T, D = a.shape
+    ws = torch.empty(cla.scan_diag_workspace_size(B, T, D), dtype=torch.uint8, device=dev)
+    h, _ = cla.scan_diag_fwd(a, b, h0, workspace=ws)
+    da, db = torch.empty_like(a), torch.empty_like(a)
+    dh0 = torch.empty(B, D, device=dev)
+    f_h = lambda: cla.scan_diag_bwd(a, None, h0, h, dh, da=da, db=db, dh0=dh0, workspace=ws)
+    f_r = lambda: cla.scan_diag_bwd(a, b, h0, None, dh, da=da, db=db, dh0=dh0, workspace=ws)
+    ms_h = _time_calls(torch, f_h, flush, iters)
+    ms_r = _time_calls(torch, f_r, flush, iters)
+    cla.check_status(ws)
+    by = 20 * B * T * D
+    return {"workload": f"diagonal scan bwd fp32 B={B} T={T} D={D}: saved states vs recomputed",
+            "with_h_us": round(ms_h * 1e3, 2), "recompute_us": round(ms_r * 1e3, 2),
+            "with_h_GBps": round(by / ms_h / 1e6, 1), "recompute_GBps_of_20B": round(by / ms_r / 1e6, 1),
+            "recompute_hbm_bytes_per_element": 28,
+            "note": "recompute = forward scan writing only chunk states (8 B/elem read) + backward reading b "
+                    "in place of h (20 B/elem)"}
+
+
+def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=20, shape=None, e2e_steps=0):
     inp = workloads.make(name, **(shape or {}))
     t = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     B, H, T, d = t["q"].shape
@@ -354,11 +393,16 @@ def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=20, sh
     ntok = B * H * T
     fl_f = ntok * (2 * chunk * 2 * d + 4 * d * d)
     fl_b = ntok * (5 * 2 * chunk * d + 5 * 2 * d * d)
+    # bytes as this library moves them (bf16 inputs, fp32 outputs o, dq, dk, dv) ...
     by_f = ntok * (3 * 2 * d + 4 + 4 * d)
     by_b = ntok * (4 * 2 * d + 4 + 3 * 4 * d + 4)
+    # ... and the method's minimum with bf16 outputs (516 and 904 B per token and head at d = 64)
+    by_f_min = ntok * (3 * 2 * d + 4 + 2 * d)
+    by_b_min = ntok * (4 * 2 * d + 4 + 3 * 2 * d + 4)
     hbm = peaks["hbm_gbs"] * 1e9
     bf = peaks["bf16_tflops"] * 1e12
     roof = max(by_f + by_b, 0) / hbm, (fl_f + fl_b) / bf
+    roof_min = (by_f_min + by_b_min) / hbm, (fl_f + fl_b) / bf
     tot = (tf + tb) / 1e3
     res = {"workload": f"chunkwise linear attention {name} B={B} H={H} T={T} d={d} chunk={chunk}",
            "fwd_us": round(tf * 1e3, 1), "bwd_us": round(tb * 1e3, 1),
@@ -367,9 +411,43 @@ def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=20, sh
            "fwd_GBps": round(by_f / (tf / 1e3) / 1e9, 1), "bwd_GBps": round(by_b / (tb / 1e3) / 1e9, 1),
            "frac_bf16_peak": round((fl_f + fl_b) / tot / bf, 4),
            "frac_binding_roofline": round(max(roof) / tot, 4),
+           "frac_binding_roofline_note": "HBM bytes as moved: bf16 inputs, fp32 outputs o, dq, dk, dv",
+           "frac_binding_roofline_min_bytes": round(max(roof_min) / tot, 4),
+           "frac_binding_roofline_min_bytes_note": "HBM bytes of the method with bf16 outputs "
+                                                   f"({(by_f_min + by_b_min) // ntok} B per token and head fwd+bwd)",
            "binding": "hbm" if roof[0] >= roof[1] else "tensor",
            "ckpt_bytes": cla.chunk_la_ckpt_size(B, H, T, d, d, chunk)}
-    del t, ws, o, g, ck
+    if e2e_steps > 0:
+        # end to end through the C ABI: inputs from pinned host buffers, outputs back, every step
+        keys_in = [k for k in ("q", "k", "v", "log_a", "S0", "dO") if inp.get(k) is not None]
+        host_in = {k: inp[k].pin_memory() for k in keys_in}
+        host_out = {"o": torch.empty(B, H, T, d).pin_memory(), "ST": torch.empty(B, H, d, d).pin_memory(),
+                    "dq": torch.empty(B, H, T, d).pin_memory(), "dk": torch.empty(B, H, T, d).pin_memory(),
+                    "dv": torch.empty(B, H, T, d).pin_memory(), "dlog_decay": torch.empty(B, H, T).pin_memory(),
+                    "dS0": torch.empty(B, H, d, d).pin_memory()}
+        del t, o, g, dl, dS0
+        torch.cuda.empty_cache()
+
+        def compute(di, do, s):
+            cla.chunk_la_fwd(di["q"], di["k"], di["v"], di["log_a"], di.get("S0"), chunk=chunk, o=do["o"],
+                             ST=do["ST"], ckpt=ck, workspace=ws, stream=s)
+            cla.chunk_la_bwd(di["q"], di["k"], di["v"], di["log_a"], di.get("S0"), di["dO"], chunk=chunk,
+                             dq=do["dq"], dk=do["dk"], dv=do["dv"], dlog_decay=do["dlog_decay"], dS0=do["dS0"],
+                             ckpt=ck, workspace=ws, stream=s)
+
+        ms = e2e_pipelined(torch, dev, host_in, host_out, compute, e2e_steps)
+        cla.check_status(ws)
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+        res["e2e"] = {"value": round(B * T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 3),
+                      "steps": e2e_steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "note": "fwd + bwd through the C ABI from pinned host buffers, copies inside the timed "
+                              "region, pipelined over three streams (the compute stream shares one workspace and "
+                              "checkpoint, so the kernels of consecutive steps do not overlap)"}
+        del host_in, host_out
+    else:
+        del t, o, g
+    del ws, ck
     torch.cuda.empty_cache()
     return res
 
@@ -483,7 +561,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--only", default=None,
-                    choices=["scan_small", "scan_fwd_blelloch", "selective", "la_const", "la_long", "la_long_chunk64"],
+                    choices=["scan_small", "scan_fwd_blelloch", "scan_bwd_recompute", "selective", "la_const", "la_long", "la_long_chunk64"],
                     help="time one workload only (forward and backward), e.g. for profiling")
     ap.add_argument("--shape", default="", help="shape overrides for --only, e.g. H=32,T=4096")
     args = ap.parse_args()
@@ -517,6 +595,8 @@ def main():
         it = max(1, args.steps)
         fns = {"scan_small": lambda: bench_scan_small(torch, cla, workloads, dev, flush, peaks, it, shape),
                "scan_fwd_blelloch": lambda: bench_scan_blelloch(torch, cla, workloads, dev, flush, peaks, it, shape),
+               "scan_bwd_recompute": lambda: bench_scan_bwd_recompute(torch, cla, workloads, dev, flush, peaks, it,
+                                                                      shape),
                "selective": lambda: bench_selective(torch, cla, workloads, dev, flush, peaks, it, shape),
                "la_const": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_const", 64, it, shape),
                "la_long": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 128, it, shape),
@@ -541,9 +621,10 @@ def main():
         for key, fn in (
                 ("scan_small", lambda: bench_scan_small(torch, cla, workloads, dev, flush, peaks)),
                 ("scan_fwd_blelloch", lambda: bench_scan_blelloch(torch, cla, workloads, dev, flush, peaks)),
+                ("scan_bwd_recompute", lambda: bench_scan_bwd_recompute(torch, cla, workloads, dev, flush, peaks)),
                 ("selective", lambda: bench_selective(torch, cla, workloads, dev, flush, peaks)),
                 ("la_const", lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_const", 64)),
-                ("la_long", lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 128)),
+                ("la_long", lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 128, e2e_steps=3)),
                 ("la_long_chunk64", lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 64))):
             try:
                 extra[key] = fn()

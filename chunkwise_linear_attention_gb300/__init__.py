@@ -51,8 +51,9 @@ def lib():
                 "cla_scan_diag_workspace_size": ([I64, I64, I64], SZ),
                 "cla_scan_diag_fwd": ([P, P, P, P, P, I64, I64, I64, P, SZ, P], INT),
                 "cla_scan_diag_fwd_blelloch": ([P, P, P, P, P, I64, I64, I64, P, SZ, P], INT),
-                "cla_scan_diag_bwd": ([P, P, P, P, P, P, P, P, I64, I64, I64, P, SZ, P], INT),
+                "cla_scan_diag_bwd": ([P] * 9 + [I64, I64, I64, P, SZ, P], INT),
                 "cla_scan_diag_fwd_noalloc": ([P, P, P, P, P, I64, I64, I64, P], INT),
+                "cla_scan_diag_noalloc_check_status": ([P], INT),
                 "cla_selective_scan_workspace_size": ([I64, I64, I64, I64], SZ),
                 "cla_selective_scan_ckpt_elems": ([I64, I64, I64, I64], SZ),
                 "cla_selective_scan_fwd": ([P] * 9 + [I64] * 4 + [P, SZ, P], INT),
@@ -163,7 +164,8 @@ def check_status(workspace, stream=None) -> None:
 
 
 def selftest_wait_timeout(workspace, stream=None) -> None:
-    """Launch the bounded-wait self-test on `workspace` (>= 256 bytes)."""
+    """Launch the bounded-wait self-test on `workspace` (16-byte aligned, at least the
+    256-byte workspace header)."""
     _launch("cla_selftest_wait_timeout", workspace.device,
             (_T(workspace, None, "workspace"), _nbytes(workspace)), stream)
 
@@ -206,8 +208,17 @@ def scan_diag_fwd_noalloc(a, b, h0=None, *, h=None, hT=None, stream=None):
     return _scan_fwd("cla_scan_diag_fwd_noalloc", a, b, h0, h, hT, None, stream, with_ws=False)
 
 
-def scan_diag_bwd(a, h0, h, dh, dhT=None, *, da=None, db=None, dh0=None, workspace=None, stream=None):
-    """Adjoint of scan_diag_fwd; returns (da, db, dh0)."""
+def scan_diag_noalloc_check_status(stream=None, device=None) -> None:
+    """Synchronise and raise if the last scan_diag_fwd_noalloc on `device` gave up a wait."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check("cla_scan_diag_noalloc_check_status",
+               lib().cla_scan_diag_noalloc_check_status(_stream(stream, dev)))
+
+
+def scan_diag_bwd(a, b, h0, h, dh, dhT=None, *, da=None, db=None, dh0=None, workspace=None, stream=None):
+    """Adjoint of scan_diag_fwd; returns (da, db, dh0).  h: the forward's states, or None to
+    recompute them from (a, b, h0) (then b is required; b may be None when h is given)."""
     B, T, D = _dims(a, 3, "a")
     dev = a.device
     f32 = torch.float32
@@ -217,7 +228,7 @@ def scan_diag_bwd(a, h0, h, dh, dhT=None, *, da=None, db=None, dh0=None, workspa
     ws = _ws(scan_diag_workspace_size(B, T, D), dev, workspace)
     bt, bd = (B, T, D), (B, D)
     _launch("cla_scan_diag_bwd", dev, (
-        _T(a, f32, "a", bt), _T(h0, f32, "h0", bd), _T(h, f32, "h", bt),
+        _T(a, f32, "a", bt), _T(b, f32, "b", bt), _T(h0, f32, "h0", bd), _T(h, f32, "h", bt),
         _T(dh, f32, "dh", bt), _T(dhT, f32, "dhT", bd), _T(da, f32, "da", bt),
         _T(db, f32, "db", bt), _T(dh0, f32, "dh0", bd), B, T, D,
         _T(ws, None, "workspace"), _nbytes(ws)), stream)

@@ -64,7 +64,7 @@ __global__ void selftest_wait_kernel(WsHeader *hdr) {
 extern "C" int cla_selftest_wait_timeout(void *ws, size_t ws_bytes, void *stream) {
     cla::clear_error();
     if (ws == nullptr || ws_bytes < sizeof(cla::WsHeader) || !cla::aligned16(ws))
-        return cla::fail(CLA_ERR_WORKSPACE, "cla_selftest_wait_timeout: need a 256-byte aligned workspace");
+        return cla::fail(CLA_ERR_WORKSPACE, "cla_selftest_wait_timeout: need a 16-byte aligned workspace of at least %zu bytes", sizeof(cla::WsHeader));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(cla::WsHeader), s), "cla_selftest_wait_timeout");
     cla::selftest_wait_kernel<<<1, 32, 0, s>>>(static_cast<cla::WsHeader *>(ws));

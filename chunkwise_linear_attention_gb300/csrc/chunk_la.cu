@@ -936,15 +936,21 @@ int run_pass(int DX, int TC, bool REV, const LaArgs &a, cudaStream_t s, unsigned
 
 using namespace cla;
 
+// Sizes, head dims and chunk that the fwd / bwd calls accept (la_validate without its message).
+static bool la_supported(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk) {
+    return B >= 0 && H >= 0 && T >= 0 && (dim_k == 64 || dim_k == 128) && (dim_v == 64 || dim_v == 128) &&
+           (chunk == 64 || chunk == 128) && la_sizes_fit(B, H, T, chunk);
+}
+
 extern "C" size_t cla_chunk_la_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
                                               int chunk) {
-    if (B < 0 || H < 0 || T < 0 || dim_k <= 0 || dim_v <= 0 || chunk <= 0 || !la_sizes_fit(B, H, T, chunk)) return 0;
+    if (!la_supported(B, H, T, dim_k, dim_v, chunk)) return 0;
     return la_plan(B, H, T, dim_k, dim_v, chunk).total;
 }
 
 extern "C" size_t cla_chunk_la_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
                                          int chunk) {
-    if (B < 0 || H < 0 || T < 0 || dim_k <= 0 || dim_v <= 0 || chunk <= 0 || !la_sizes_fit(B, H, T, chunk)) return 0;
+    if (!la_supported(B, H, T, dim_k, dim_v, chunk)) return 0;
     const LaPlan pl = la_plan(B, H, T, dim_k, dim_v, chunk);
     return (size_t)pl.n_seg * (size_t)(B * H) * (size_t)dim_k * (size_t)dim_v * sizeof(float);
 }

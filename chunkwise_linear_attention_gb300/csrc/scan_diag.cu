@@ -27,8 +27,6 @@
 // HBM traffic is the algorithmic 12 B per element forward (read a, b; write
 // h) and 20 B backward (read a, h, dh; write da, db), plus 24 B of look-back
 // payload per chunk and channel (about 0.4 B per element, L2-resident).
-#include <mutex>
-
 #include "cla_internal.cuh"
 
 namespace cla {
@@ -158,7 +156,9 @@ __device__ __forceinline__ size_t unit_index(const ScanGeom &g, int chunk, int b
 // BLELLOCH selects how the 8 runs of a chunk are composed: Hillis-Steele
 // (3 rounds, every run combines) or a Blelloch up-sweep / down-sweep (6 rounds,
 // fewer combines), the latter kept as a measured alternative.
-template <int VEC, bool BLELLOCH = false>
+// STATES: instead of h, write only the state entering every chunk,
+// h_in[chunk][B][D] (the backward's recompute path rebuilds h from it).
+template <int VEC, bool BLELLOCH = false, bool STATES = false>
 __global__ void __launch_bounds__(kWarps * 32, 4)
 scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
                      const float *__restrict__ h0, float *__restrict__ h,
@@ -301,6 +301,13 @@ scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
     }
 #pragma unroll
     for (int v = 0; v < VEC; ++v) carry[v] = __shfl_sync(0xffffffffu, carry[v], (kSub - 1) * kCg + cg);
+    if constexpr (STATES) {
+        if (sub == 0 && cok) {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) h[((size_t)chunk * g.B + bi) * g.D + c0 + v] = carry[v];
+        }
+        if (hT == nullptr) return;
+    }
     // 5. re-run this lane's steps from its true starting state; write h once
     float hs[VEC];
 #pragma unroll
@@ -312,7 +319,7 @@ scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
         for (int v = 0; v < VEC; ++v) hs[v] = fmaf(av[i][v], hs[v], bv[i][v]);
         if (cok && t < g.T) {
             const size_t idx = ((size_t)bi * g.T + t) * g.D + c0;
-            VecIO<VEC>::store(h + idx, hs);
+            if constexpr (!STATES) VecIO<VEC>::store(h + idx, hs);
             if (hT != nullptr && t == g.T - 1)
 #pragma unroll
                 for (int v = 0; v < VEC; ++v) hT[(size_t)bi * g.D + c0 + v] = hs[v];
@@ -324,9 +331,17 @@ scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
 // Reversed time: hbar_t = a'_t hbar_{t+1} + g_t with a'_t = a_{t+1}
 // (a'_{T-1} = 1 and g_{T-1} includes dhT), i.e. the forward scan on reversed
 // arrays with the decays shifted by one place.
-template <int VEC>
+//
+// RECOMP: h is not given.  `h` then points at the state entering every chunk,
+// h_in[chunk][B][D] (written by the STATES forward), and `b` at the forward's
+// inputs; each lane rebuilds h_{t-1} over its run from them -- the run's own
+// (a, b) composed forward, Hillis-Steele across the runs of the chunk, applied
+// to the chunk's entry state -- instead of reading it ("The backward pass is a
+// scan in reverse": store the states or recompute them).
+template <int VEC, bool RECOMP = false>
 __global__ void __launch_bounds__(kWarps * 32, 3)
-scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0,
+scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
+                     const float *__restrict__ h0,
                      const float *__restrict__ h, const float *__restrict__ dh,
                      const float *__restrict__ dhT, float *__restrict__ da,
                      float *__restrict__ db, float *__restrict__ dh0, ScanGeom g,
@@ -349,21 +364,45 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0,
 
     // h_{t-1} is only needed in the last pass: stage it in shared memory now
     // (asynchronously, holding no registers) so its latency overlaps the rest.
-    __shared__ __align__(16) float s_hp[kL][kWarps * 32][VEC];
+    __shared__ __align__(16) float s_hp[RECOMP ? 1 : kL][kWarps * 32][VEC];
+    if constexpr (!RECOMP) {
 #pragma unroll
-    for (int i = 0; i < kL; ++i) {
-        const long long t = t_begin + i;
-        const bool ok = cok && t >= 1 && t < g.T;
-        const float *src = h + (ok ? ((size_t)bi * g.T + t - 1) * g.D + c0 : 0);
-        const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(&s_hp[i][threadIdx.x][0]));
-        if (VEC == 4)
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(ok ? 16u : 0u)
-                         : "memory");
-        else
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(ok ? 4u : 0u)
-                         : "memory");
+        for (int i = 0; i < kL; ++i) {
+            const long long t = t_begin + i;
+            const bool ok = cok && t >= 1 && t < g.T;
+            const float *src = h + (ok ? ((size_t)bi * g.T + t - 1) * g.D + c0 : 0);
+            const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(&s_hp[i][threadIdx.x][0]));
+            if (VEC == 4)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+                             "r"(ok ? 16u : 0u)
+                             : "memory");
+            else
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(ok ? 4u : 0u)
+                             : "memory");
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
     }
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
+    // RECOMP: the forward inputs b_t of this run and a_t of its first step (a_t of the
+    // others is ap[i - 1] below); hp[i] becomes h_{t-1}
+    float hp[RECOMP ? kL : 1][VEC], a_first[VEC];
+    if constexpr (RECOMP) {
+#pragma unroll
+        for (int i = 0; i < kL; ++i) {
+            const long long t = t_begin + i;
+            if (cok && t < g.T) {
+                VecIO<VEC>::load_cs(b + ((size_t)bi * g.T + t) * g.D + c0, hp[i]);
+            } else {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) hp[i][v] = 0.f;
+            }
+        }
+        if (cok && t_begin < g.T) {
+            VecIO<VEC>::load(a + ((size_t)bi * g.T + t_begin) * g.D + c0, a_first);
+        } else {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) a_first[v] = 1.f;
+        }
+    }
     float ap[kL][VEC], gv[kL][VEC];
 #pragma unroll
     for (int i = 0; i < kL; ++i) {
@@ -416,6 +455,51 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0,
         Bex[v] = __shfl_down_sync(0xffffffffu, Bc[v], kCg);
         if (sub == kSub - 1) { Aex[v] = 1.f; Bex[v] = 0.f; }
     }
+    if constexpr (RECOMP) {
+        // forward composition of this run, then Hillis-Steele across the runs of the chunk
+        // (exclusive prefix), applied to the chunk's entry state: h entering this run
+        float FA[VEC], FB[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { FA[v] = 1.f; FB[v] = 0.f; }
+#pragma unroll
+        for (int i = 0; i < kL; ++i)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float at = i == 0 ? a_first[v] : ap[i - 1][v];
+                FB[v] = fmaf(at, FB[v], hp[i][v]);
+                FA[v] *= at;
+            }
+#pragma unroll
+        for (int off = 1; off < kSub; off <<= 1) {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float pa = __shfl_up_sync(0xffffffffu, FA[v], off * kCg);
+                const float pb = __shfl_up_sync(0xffffffffu, FB[v], off * kCg);
+                if (sub >= off) {
+                    FB[v] = fmaf(FA[v], pb, FB[v]);
+                    FA[v] *= pa;
+                }
+            }
+        }
+        float hs[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            float ea = __shfl_up_sync(0xffffffffu, FA[v], kCg);
+            float eb = __shfl_up_sync(0xffffffffu, FB[v], kCg);
+            if (sub == 0) { ea = 1.f; eb = 0.f; }
+            const float s0 = cok ? __ldcg(h + ((size_t)chunk * g.B + bi) * g.D + c0 + v) : 0.f;
+            hs[v] = fmaf(ea, s0, eb);
+        }
+#pragma unroll
+        for (int i = 0; i < kL; ++i)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float at = i == 0 ? a_first[v] : ap[i - 1][v];
+                const float bt = hp[i][v];
+                hp[i][v] = hs[v];
+                hs[v] = fmaf(at, hs[v], bt);
+            }
+    }
     float carry[VEC];
     if (sub == 0) {
         const size_t u = unit_index(g, chunk, bi, cw, cg);
@@ -445,7 +529,7 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0,
     }
 #pragma unroll
     for (int v = 0; v < VEC; ++v) carry[v] = __shfl_sync(0xffffffffu, carry[v], cg);
-    asm volatile("cp.async.wait_group 0;\n" ::: "memory");  // own copies of h_{t-1}
+    if constexpr (!RECOMP) asm volatile("cp.async.wait_group 0;\n" ::: "memory");  // own copies of h_{t-1}
     float hb[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) hb[v] = fmaf(Aex[v], carry[v], Bex[v]);
@@ -456,17 +540,20 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0,
         for (int v = 0; v < VEC; ++v) hb[v] = fmaf(ap[i][v], hb[v], gv[i][v]);
         if (cok && t < g.T) {
             const size_t idx = ((size_t)bi * g.T + t) * g.D + c0;
-            float hp[VEC];  // h_{t-1}
-            if (t >= 1) {
+            float hprev[VEC];  // h_{t-1}
+            if constexpr (RECOMP) {
 #pragma unroll
-                for (int v = 0; v < VEC; ++v) hp[v] = s_hp[i][threadIdx.x][v];
+                for (int v = 0; v < VEC; ++v) hprev[v] = hp[i][v];
+            } else if (t >= 1) {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) hprev[v] = s_hp[i][threadIdx.x][v];
             } else {
 #pragma unroll
-                for (int v = 0; v < VEC; ++v) hp[v] = (h0 != nullptr) ? h0[(size_t)bi * g.D + c0 + v] : 0.f;
+                for (int v = 0; v < VEC; ++v) hprev[v] = (h0 != nullptr) ? h0[(size_t)bi * g.D + c0 + v] : 0.f;
             }
             float dav[VEC];
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) dav[v] = hb[v] * hp[v];
+            for (int v = 0; v < VEC; ++v) dav[v] = hb[v] * hprev[v];
             VecIO<VEC>::store(db + idx, hb);
             VecIO<VEC>::store(da + idx, dav);
             if (dh0 != nullptr && t == 0) {
@@ -484,6 +571,9 @@ struct Plan {
     ScanGeom g;
     int vec;
     size_t words_off, total;
+    // the backward's recompute path also keeps the state entering every chunk,
+    // [n_chunks][B][D] fp32, after the look-back words
+    size_t states_off, total_recomp;
 };
 
 Plan make_plan(int64_t B, int64_t T, int64_t D, int vec) {
@@ -498,6 +588,8 @@ Plan make_plan(int64_t B, int64_t T, int64_t D, int vec) {
     p.g.n_cblk = (p.g.n_cw + kWarps - 1) / kWarps;
     p.words_off = sizeof(WsHeader);
     p.total = p.words_off + scan_units(p.g) * 12 * sizeof(unsigned long long);
+    p.states_off = align_up(p.total, 256);
+    p.total_recomp = p.states_off + (size_t)p.g.n_chunks * (size_t)B * (size_t)D * sizeof(float);
     return p;
 }
 
@@ -535,7 +627,7 @@ extern "C" size_t cla_scan_diag_workspace_size(int64_t B, int64_t T, int64_t D) 
     // the scalar-channel layout needs the most units; size for it
     const Plan p1 = make_plan(B, T, D, 1);
     const Plan p4 = make_plan(B, T, D, 4);
-    return p1.total > p4.total ? p1.total : p4.total;
+    return p1.total_recomp > p4.total_recomp ? p1.total_recomp : p4.total_recomp;
 }
 
 namespace {
@@ -587,7 +679,7 @@ extern "C" int cla_scan_diag_fwd_blelloch(const float *a, const float *b, const 
     return scan_fwd("cla_scan_diag_fwd_blelloch", true, a, b, h0, h, hT, B, T, D, ws, ws_bytes, stream);
 }
 
-extern "C" int cla_scan_diag_bwd(const float *a, const float *h0, const float *h,
+extern "C" int cla_scan_diag_bwd(const float *a, const float *b, const float *h0, const float *h,
                                  const float *dh, const float *dhT, float *da, float *db,
                                  float *dh0, int64_t B, int64_t T, int64_t D, void *ws,
                                  size_t ws_bytes, void *stream) {
@@ -595,7 +687,7 @@ extern "C" int cla_scan_diag_bwd(const float *a, const float *h0, const float *h
     const char *fn = "cla_scan_diag_bwd";
     int st = check_sizes(fn, B, T, D);
     if (st) return st;
-    if (!aligned_or_null({a, h0, h, dh, dhT, da, db, dh0}, 4))
+    if (!aligned_or_null({a, b, h0, h, dh, dhT, da, db, dh0}, 4))
         return fail(CLA_ERR_INVALID_ARG, "%s: fp32 tensors must be 4-byte aligned", fn);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (B == 0 || D == 0) return CLA_OK;
@@ -606,17 +698,36 @@ extern "C" int cla_scan_diag_bwd(const float *a, const float *h0, const float *h
         }
         return CLA_OK;
     }
-    if (!a || !h || !dh || !da || !db) return fail(CLA_ERR_INVALID_ARG, "%s: a, h, dh, da and db are required", fn);
+    if (!a || !dh || !da || !db) return fail(CLA_ERR_INVALID_ARG, "%s: a, dh, da and db are required", fn);
+    if (!h && !b) return fail(CLA_ERR_INVALID_ARG, "%s: give h (the forward's states) or b (to recompute them)", fn);
     if (!ws) return fail(CLA_ERR_WORKSPACE, "%s: workspace is NULL", fn);
     if (!aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace not 16-byte aligned", fn);
-    const bool v4 = (D % 4 == 0) && aligned16(a) && aligned16(h) && aligned16(dh) && aligned16(da) && aligned16(db);
+    const bool recomp = (h == nullptr);
+    const float *hsrc = recomp ? b : h;  // the tensor read in place of h
+    const bool v4 = (D % 4 == 0) && aligned16(a) && aligned16(hsrc) && aligned16(dh) && aligned16(da) &&
+                    aligned16(db);
     const Plan p = make_plan(B, T, D, v4 ? 4 : 1);
-    if (ws_bytes < p.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, p.total);
-    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.total, s), fn);
+    const size_t need = recomp ? p.total_recomp : p.total;
+    if (ws_bytes < need) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, need);
     const ScanWs w = bind_ws(p, ws);
     const unsigned int grid = (unsigned int)((size_t)p.g.n_chunks * p.g.B * p.g.n_cblk);
-    if (v4) scan_diag_bwd_kernel<4><<<grid, kWarps * 32, 0, s>>>(a, h0, h, dh, dhT, da, db, dh0, p.g, w);
-    else scan_diag_bwd_kernel<1><<<grid, kWarps * 32, 0, s>>>(a, h0, h, dh, dhT, da, db, dh0, p.g, w);
+    float *states = reinterpret_cast<float *>(static_cast<char *>(ws) + p.states_off);
+    if (recomp) {
+        // the state entering every chunk, by the forward scan without writing h
+        CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.total, s), fn);
+        if (v4) scan_diag_fwd_kernel<4, false, true><<<grid, kWarps * 32, 0, s>>>(a, b, h0, states, nullptr, p.g, w);
+        else scan_diag_fwd_kernel<1, false, true><<<grid, kWarps * 32, 0, s>>>(a, b, h0, states, nullptr, p.g, w);
+        st = check_launch(fn);
+        if (st) return st;
+    }
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.total, s), fn);
+    if (recomp) {
+        if (v4) scan_diag_bwd_kernel<4, true><<<grid, kWarps * 32, 0, s>>>(a, b, h0, states, dh, dhT, da, db, dh0, p.g, w);
+        else scan_diag_bwd_kernel<1, true><<<grid, kWarps * 32, 0, s>>>(a, b, h0, states, dh, dhT, da, db, dh0, p.g, w);
+    } else {
+        if (v4) scan_diag_bwd_kernel<4><<<grid, kWarps * 32, 0, s>>>(a, nullptr, h0, h, dh, dhT, da, db, dh0, p.g, w);
+        else scan_diag_bwd_kernel<1><<<grid, kWarps * 32, 0, s>>>(a, nullptr, h0, h, dh, dhT, da, db, dh0, p.g, w);
+    }
     return check_launch(fn);
 }
 
@@ -636,26 +747,17 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
 static __device__ __align__(256) unsigned char g_scan_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of the array, looked up once per device.  The name
+// Device address of the array in the current device's context.  The name
 // g_scan_noalloc_scratch is only a host-side stand-in in host code and must
-// never be passed to a kernel directly.
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[kMaxDevices] = {};
-
-int noalloc_scratch(void **out) {
-    int dev = -1;
-    CLA_CUDA_TRY(cudaGetDevice(&dev), "cla_scan_diag_fwd_noalloc: cudaGetDevice");
-    if (dev < 0 || dev >= kMaxDevices) return fail(CLA_ERR_UNSUPPORTED, "cla_scan_diag_fwd_noalloc: device %d", dev);
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (g_noalloc_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_scan_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr)
-            return fail(CLA_ERR_CUDA, "cla_scan_diag_fwd_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+// never be passed to a kernel directly.  The address is looked up on every
+// call (the lookup allocates nothing): a cached address would go stale when
+// the module is loaded again, after cudaDeviceReset or in another context.
+int noalloc_scratch(const char *fn, void **out) {
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_scan_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr)
+        return fail(CLA_ERR_CUDA, "%s: cudaGetSymbolAddress: %s", fn, cudaGetErrorString(e));
+    *out = p;
     return CLA_OK;
 }
 
@@ -688,7 +790,7 @@ extern "C" int cla_scan_diag_fwd_noalloc(const float *a, const float *b, const f
                     "use cla_scan_diag_fwd with a caller workspace",
                     fn, p.total, kNoAllocScratchBytes);
     void *ws = nullptr;
-    st = noalloc_scratch(&ws);
+    st = noalloc_scratch(fn, &ws);
     if (st) return st;
     // tickets and flags must start at zero; the payload is always written before it is read
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.total, s), fn);
@@ -697,4 +799,17 @@ extern "C" int cla_scan_diag_fwd_noalloc(const float *a, const float *b, const f
     if (v4) scan_diag_fwd_kernel<4><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);
     else scan_diag_fwd_kernel<1><<<grid, kWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, w);
     return check_launch(fn);
+}
+
+extern "C" int cla_scan_diag_noalloc_check_status(void *stream) {
+    clear_error();
+    const char *fn = "cla_scan_diag_noalloc_check_status";
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CLA_CUDA_TRY(cudaStreamSynchronize(s), fn);
+    WsHeader hdr;
+    // a copy into host memory: nothing is allocated
+    CLA_CUDA_TRY(cudaMemcpyFromSymbol(&hdr, g_scan_noalloc_scratch, sizeof(hdr), 0, cudaMemcpyDeviceToHost), fn);
+    if (hdr.error & kErrTimeout)
+        return fail(CLA_ERR_TIMEOUT, "%s: a cross-block wait gave up (site %u)", fn, hdr.where);
+    return CLA_OK;
 }

@@ -68,7 +68,8 @@ int cla_check_status(const void *ws, void *stream);
 
 /* Self-test of the failure path: launches one warp that polls a workspace
  * word nothing ever sets.  Its bounded wait gives up after about a second,
- * records the timeout in `ws` (>= 256 bytes) and returns; a following
+ * records the timeout in `ws` (16-byte aligned, at least 256 bytes: the
+ * workspace header) and returns; a following
  * cla_check_status(ws, stream) then reports CLA_ERR_TIMEOUT.  No GPU fault,
  * trap or hang is involved. */
 int cla_selftest_wait_timeout(void *ws, size_t ws_bytes, void *stream);
@@ -111,15 +112,22 @@ int cla_scan_diag_fwd_blelloch(const float *a, const float *b, const float *h0,
  * direct gradients g_t = dh_t (plus dhT on h_T), the adjoint
  * hbar_t = g_t + a_{t+1} hbar_{t+1} is the same scan on reversed time with
  * the decays shifted by one; then db_t = hbar_t, da_t = hbar_t * h_{t-1},
- * dh0 = a_1 * hbar_1.
+ * dh0 = a_1 * hbar_1.  The states h_{t-1} are read from the forward's output
+ * when `h` is given, else recomputed from (a, b, h0) -- the store-or-recompute
+ * choice of the same section: a forward scan that keeps only the state
+ * entering every 64-step chunk (in the workspace), then the backward kernel
+ * rebuilds each chunk's states from it and b.
  *   a      [B, T, D] fp32   decays of the forward call
+ *   b      [B, T, D] fp32   [opt] inputs of the forward call (required when h is NULL)
  *   h0     [B, D]    fp32   [opt] initial state of the forward call
- *   h      [B, T, D] fp32   states returned by the forward call
+ *   h      [B, T, D] fp32   [opt] states returned by the forward call (NULL = recompute)
  *   dh     [B, T, D] fp32   upstream gradient on every state
  *   dhT    [B, D]    fp32   [opt] upstream gradient on the returned h_T
  *   da, db [B, T, D] fp32   out
- *   dh0    [B, D]    fp32   [opt] out */
-int cla_scan_diag_bwd(const float *a, const float *h0, const float *h,
+ *   dh0    [B, D]    fp32   [opt] out
+ * Both h and b NULL is CLA_ERR_INVALID_ARG.  The workspace size query covers
+ * the recompute path (it adds ceil(T/64) * B * D fp32 chunk states). */
+int cla_scan_diag_bwd(const float *a, const float *b, const float *h0, const float *h,
                       const float *dh, const float *dhT, float *da, float *db,
                       float *dh0, int64_t B, int64_t T, int64_t D, void *ws,
                       size_t ws_bytes, void *stream);
@@ -140,17 +148,27 @@ int cla_scan_diag_bwd(const float *a, const float *h0, const float *h,
  *    CLA_ERR_UNSUPPORTED and nothing is enqueued: about 44 million elements
  *    of B*T*D when D is a multiple of 4 (8 x 4096 x 1024 fits), about 11
  *    million otherwise.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
+ *  - Every call looks up the array's device address (cudaGetSymbolAddress)
+ *    in the current device's context; the first lookup on a device may load
+ *    the library's device code there, so make the first call on each device
  *    before any stream capture.
  *  - Every call shares the one array; the call clears what must start at
  *    zero.  Calls that overlap on the GPU (other streams, other host threads)
  *    race on it and must be serialised by the caller.
- *  - There is no workspace to pass to cla_check_status(); a look-back wait
- *    that gives up is not reported by this variant. */
+ *  - There is no workspace to pass to cla_check_status(): a look-back wait
+ *    that gives up is reported by cla_scan_diag_noalloc_check_status(), until
+ *    the next call clears it. */
 int cla_scan_diag_fwd_noalloc(const float *a, const float *b, const float *h0,
                               float *h, float *hT, int64_t B, int64_t T,
                               int64_t D, void *stream);
+
+/* Status of the last cla_scan_diag_fwd_noalloc call on the current device:
+ * synchronises `stream` (the stream of that call), then reports
+ * CLA_ERR_TIMEOUT if one of its look-back waits gave up, CLA_ERR_CUDA if the
+ * stream holds an error, else CLA_OK.  Reads the static array's header into
+ * host memory; allocates nothing.  The pages have no counterpart (a
+ * deployment aid, as above). */
+int cla_scan_diag_noalloc_check_status(void *stream);
 
 /* ======================================================================== */
 /* Selective (Mamba-1 style) diagonal scan                                  */
@@ -208,7 +226,8 @@ int cla_selective_scan_bwd(const uint16_t *x, const float *delta, const float *A
 /* Chunkwise decayed linear attention (matrix state)                        */
 /* ======================================================================== */
 
-/* Bytes of workspace for cla_chunk_la_fwd / _bwd. */
+/* Bytes of workspace for cla_chunk_la_fwd / _bwd; 0 for sizes, head dims
+ * or chunks those calls refuse. */
 size_t cla_chunk_la_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
                                    int64_t dim_v, int chunk);
 
@@ -268,7 +287,8 @@ int cla_chunk_la_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
  * (the one that gives dQ) needs exactly those states.
  *
  * Bytes of that checkpoint for these sizes: n_seg * B * H * dim_k * dim_v
- * fp32 values, n_seg fixed by the sizes and the chunk.  0 for invalid sizes. */
+ * fp32 values, n_seg fixed by the sizes and the chunk.  0 for sizes, head
+ * dims or chunks the fwd / bwd calls refuse. */
 size_t cla_chunk_la_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
                               int64_t dim_v, int chunk);
 

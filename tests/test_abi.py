@@ -79,6 +79,26 @@ def test_chunk_la_ckpt_size_follows_the_segment_rule(lib):
     assert f(-1, 1, 1, 64, 64, 64) == 0 and f(1, 1, 1, 64, 64, 0) == 0
 
 
+def test_chunk_la_size_queries_refuse_what_the_calls_refuse(lib):
+    """The workspace and checkpoint size queries return 0 for head dims or chunks the fwd / bwd
+    calls reject (CLA_ERR_UNSUPPORTED), so no caller sizes a buffer for a call that cannot run."""
+    i64, ci = ctypes.c_int64, ctypes.c_int
+    for f in (lib.cla_chunk_la_workspace_size, lib.cla_chunk_la_ckpt_size):
+        f.restype = ctypes.c_size_t
+        f.argtypes = [ctypes.c_int64] * 5 + [ctypes.c_int]
+    P = ctypes.c_void_p
+    d, ws, big = P(256), P(1 << 20), ctypes.c_size_t(1 << 30)
+    for dk, dv, chunk in ((32, 64, 64), (64, 96, 64), (256, 256, 128), (64, 64, 32), (128, 128, 256)):
+        assert lib.cla_chunk_la_workspace_size(1, 2, 1000, dk, dv, chunk) == 0, (dk, dv, chunk)
+        assert lib.cla_chunk_la_ckpt_size(1, 2, 1000, dk, dv, chunk) == 0, (dk, dv, chunk)
+        st = lib.cla_chunk_la_fwd(d, d, d, d, None, d, None, i64(1), i64(2), i64(1000), i64(dk), i64(dv), ci(chunk),
+                                  ws, big, None)
+        assert st == 2, (dk, dv, chunk)
+    for dk, dv, chunk in ((64, 64, 64), (64, 128, 128), (128, 64, 64), (128, 128, 128)):
+        assert lib.cla_chunk_la_workspace_size(1, 2, 1000, dk, dv, chunk) > 0
+        assert lib.cla_chunk_la_ckpt_size(1, 2, 1000, dk, dv, chunk) > 0
+
+
 def test_chunk_la_ckpt_rejects_unaligned_without_gpu(lib):
     P = ctypes.c_void_p
     d = P(256)
@@ -116,7 +136,7 @@ def test_misaligned_pointers_rejected_without_gpu(lib):
     # diagonal scan: fp32 tensors need 4-byte alignment
     st = lib.cla_scan_diag_fwd(odd2, d, None, d, None, i64(2), i64(64), i64(64), ws, big, None)
     assert st == 1 and b"aligned" in lib.cla_last_error_message()
-    st = lib.cla_scan_diag_bwd(d, None, d, d, None, d, d, odd2, i64(2), i64(64), i64(64), ws, big, None)
+    st = lib.cla_scan_diag_bwd(d, None, None, d, d, None, d, d, odd2, i64(2), i64(64), i64(64), ws, big, None)
     assert st == 1
     st = lib.cla_scan_diag_fwd_noalloc(d, d, odd2, d, None, i64(2), i64(64), i64(64), None)
     assert st == 1
@@ -209,7 +229,8 @@ def test_binding_checks_shapes_before_anything_else(lib):
     raises(cla.scan_diag_fwd, a, a.double(), match="b must be torch.float32")
     raises(cla.scan_diag_fwd, torch.rand(8, 4), a, match="a must have 3 dimensions")
     raises(cla.scan_diag_fwd_noalloc, a, a, hT=torch.empty(3, 4), match="hT must have shape")
-    raises(cla.scan_diag_bwd, a, None, a, torch.rand(2, 7, 4), match="dh must have shape")
+    raises(cla.scan_diag_bwd, a, None, None, a, torch.rand(2, 7, 4), match="dh must have shape")
+    raises(cla.scan_diag_bwd, a, torch.rand(2, 8, 5), None, None, a, match="b must have shape")
 
     x = torch.zeros(1, 64, 32, dtype=bf16)
     A = torch.zeros(32, 16)

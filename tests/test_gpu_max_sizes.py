@@ -31,7 +31,7 @@ def test_scan_diag_beyond_int32_elements(cla):
     inp = workloads.scan_inputs_device(B, T, D, seed=21, device=dev)
     a, b, h0, dh = inp["a"], inp["b"], inp["h0"], inp["dh"]
     h, hT = cla.scan_diag_fwd(a, b, h0)
-    da, db, dh0 = cla.scan_diag_bwd(a, h0, h, dh)
+    da, db, dh0 = cla.scan_diag_bwd(a, None, h0, h, dh)
     torch.cuda.synchronize()
     ch = [0, 517, 1023]
     sub = lambda x: x[..., ch].contiguous().cpu()

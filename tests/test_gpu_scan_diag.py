@@ -20,7 +20,8 @@ def cla():
     return m
 
 
-def _run(cla, inp, with_h0=True, with_dhT=False, seed=0):
+def _run(cla, inp, with_h0=True, with_dhT=False, seed=0, recompute=False):
+    """recompute: the backward gets b instead of the forward's h and rebuilds the states."""
     dev = torch.device("cuda")
     a, b = inp["a"].to(dev), inp["b"].to(dev)
     h0 = inp["h0"].to(dev) if (with_h0 and inp.get("h0") is not None) else None
@@ -30,7 +31,10 @@ def _run(cla, inp, with_h0=True, with_dhT=False, seed=0):
         dh = torch.from_numpy(np.random.default_rng(seed).standard_normal((B, T, D)).astype(np.float32))
     dhT = torch.from_numpy(np.random.default_rng(seed + 1).standard_normal((B, D)).astype(np.float32)) if with_dhT else None
     h, hT = cla.scan_diag_fwd(a, b, h0)
-    da, db, dh0 = cla.scan_diag_bwd(a, h0, h, dh.to(dev), dhT.to(dev) if dhT is not None else None)
+    if recompute:
+        da, db, dh0 = cla.scan_diag_bwd(a, b, h0, None, dh.to(dev), dhT.to(dev) if dhT is not None else None)
+    else:
+        da, db, dh0 = cla.scan_diag_bwd(a, None, h0, h, dh.to(dev), dhT.to(dev) if dhT is not None else None)
     torch.cuda.synchronize()
     h0c = h0.cpu() if h0 is not None else None
     rh, rhT = oracle.scan_diag_fwd(inp["a"], inp["b"], h0c)
@@ -48,6 +52,21 @@ def _run(cla, inp, with_h0=True, with_dhT=False, seed=0):
 def test_scan_diag_small(cla, B, T, D, with_h0):
     inp = workloads.make("scan", B=B, T=T, D=D)
     _run(cla, inp, with_h0=with_h0, with_dhT=True)
+
+
+@pytest.mark.parametrize("B,T,D", [(1, 1, 4), (2, 63, 16), (2, 64, 16), (2, 65, 20), (3, 200, 96),
+                                   (1, 1000, 7), (2, 513, 130), (1, 4097, 8), (2, 130, 3)])
+@pytest.mark.parametrize("with_h0", [False, True])
+def test_scan_diag_bwd_recompute_small(cla, B, T, D, with_h0):
+    """Backward without the forward's states: rebuilt from (a, b, h0) chunk by chunk."""
+    inp = workloads.make("scan", B=B, T=T, D=D)
+    _run(cla, inp, with_h0=with_h0, with_dhT=True, recompute=True)
+
+
+def test_scan_diag_bwd_recompute_workload_full(cla):
+    """8 x 4096 x 1024 backward with recomputed states, every output element."""
+    inp = workloads.make("scan")
+    _run(cla, inp, with_h0=True, with_dhT=True, recompute=True)
 
 
 def test_scan_diag_small_workload_full(cla):
@@ -72,7 +91,7 @@ def test_scan_diag_empty(cla):
     h0 = torch.randn(2, 8, device=dev)
     a = torch.empty(2, 0, 8, device=dev)
     h, hT = cla.scan_diag_fwd(a, a, h0)
-    da, db, dh0 = cla.scan_diag_bwd(a, h0, h, a, hT * 0 + 3.0)
+    da, db, dh0 = cla.scan_diag_bwd(a, None, h0, h, a, hT * 0 + 3.0)
     torch.cuda.synchronize()
     assert torch.equal(hT, h0)
     assert torch.all(dh0 == 3.0)
@@ -97,7 +116,7 @@ def test_scan_diag_canaries_untouched(cla):
     dab, da = guarded(B * T * D)
     dbb, db = guarded(B * T * D)
     d0b, dh0 = guarded(B * D)
-    cla.scan_diag_bwd(inp["a"].to(dev), inp["h0"].to(dev), h.view(B, T, D), inp["dh"].to(dev),
+    cla.scan_diag_bwd(inp["a"].to(dev), None, inp["h0"].to(dev), h.view(B, T, D), inp["dh"].to(dev),
                       da=da.view(B, T, D), db=db.view(B, T, D), dh0=dh0.view(B, D))
     torch.cuda.synchronize()
     for buf in (hb, tb, dab, dbb, d0b):
