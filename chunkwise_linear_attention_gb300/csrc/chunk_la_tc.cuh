@@ -198,16 +198,23 @@ struct TcCfg {
     static constexpr int NT = 320;  // 8 math warps (w and w + 4 share TMEM lane quarter w), producer, decay warp
     static constexpr int KBX = DX / 64;  // 64-column blocks of X and Y
     static constexpr int KBT = TC / 64;  // 64-token blocks of Zs
+    // Compact layout (DX = Tc = 64, whose every stage is short): two blocks per SM, so one
+    // block's tensor-core and barrier latencies overlap the other's work.  It needs half the
+    // TMEM (256 columns): the scores are masked in place, and dS accumulates Y^T Zs_hi and
+    // Y^T Zs_lo in one 64-column accumulator (two N = 64 products instead of one N = 128).
+    static constexpr bool COMPACT = (DX == 64 && TC == 64);
+    static constexpr int MIN_BLOCKS = COMPACT ? 2 : 1;
     // TMEM columns: P (fp32), the accumulators, and the masked P as bf16 parts.
     static constexpr uint32_t C_P = 0;
     static constexpr uint32_t C_OI = TC;        // O_inter
     static constexpr uint32_t C_OA = TC + 64;   // O_intra
-    static constexpr uint32_t C_DS = TC + 128;  // dS: Y^T Zs_hi in 64 columns, then Y^T Zs_lo in 64
+    // dS: Y^T Zs_hi in 64 columns, then Y^T Zs_lo in 64 (compact: both in the same 64)
+    static constexpr uint32_t C_DS = TC + 128;
     // masked, decayed P as the bf16 A operand of O_intra: per 32-token piece,
     // the high part in its first 16 columns and the low part in the next 16
-    static constexpr uint32_t C_PB = TC + 256;
-    static constexpr uint32_t TMEM_COLS = 512;
-    static_assert(C_PB + TC <= TMEM_COLS, "tensor memory budget");
+    static constexpr uint32_t C_PB = COMPACT ? C_P : TC + 256;
+    static constexpr uint32_t TMEM_COLS = COMPACT ? 256 : 512;
+    static_assert(COMPACT ? (C_DS + 64 <= TMEM_COLS) : (C_PB + TC <= TMEM_COLS), "tensor memory budget");
     // shared memory (offsets from a 1024-aligned base)
     static constexpr int X_BYTES = KBX * TC * 128;
     static constexpr int Z_BYTES = TC * 128;
@@ -215,8 +222,15 @@ struct TcCfg {
     // Zs as the K-major B operand of dS, N = 128: per 64-token block, rows
     // 0..63 hold Zs_hi and rows 64..127 Zs_lo (16 KB per block)
     static constexpr int ZS_BYTES = KBT * 128 * 128;
+    static constexpr int DEC_STRIDE = 5 * TC + 4;  // floats per decay buffer (below)
+    static constexpr int DEC_BYTES = (2 * DEC_STRIDE + 2 * TC) * 4;
+    // X is double-buffered where shared memory allows (every shape but DX = Tc = 128), so
+    // the next chunk's X load overlaps this chunk instead of waiting for its O_inter
+    static constexpr int SMEM_ONE_X = 3 * X_BYTES + 3 * Z_BYTES + 2 * S_BYTES + ZS_BYTES + DEC_BYTES + 128 + 1024;
+    static constexpr bool XDB = SMEM_ONE_X + X_BYTES <= 227 * 1024;
     static constexpr int OFF_X = 0;
-    static constexpr int OFF_Y0 = OFF_X + X_BYTES;
+    static constexpr int OFF_X1 = XDB ? X_BYTES : 0;
+    static constexpr int OFF_Y0 = OFF_X + (XDB ? 2 : 1) * X_BYTES;
     static constexpr int OFF_Y1 = OFF_Y0 + X_BYTES;
     static constexpr int OFF_Z0 = OFF_Y1 + X_BYTES;
     static constexpr int OFF_Z1 = OFF_Z0 + Z_BYTES;
@@ -229,10 +243,9 @@ struct TcCfg {
     static constexpr int OFF_DEC = OFF_ZS + ZS_BYTES;
     // decays, two buffers (chunk sequence number parity) of cl, zr, w_out,
     // w_state, g [Tc] and alpha; then the two half-row dot products [2][Tc]
-    static constexpr int DEC_STRIDE = 5 * TC + 4;  // floats per buffer
-    static constexpr int DEC_BYTES = (2 * DEC_STRIDE + 2 * TC) * 4;
     static constexpr int OFF_BAR = OFF_DEC + DEC_BYTES;
-    static constexpr int SMEM = OFF_BAR + 128 + 1024;  // 12 mbarriers + alignment slack
+    static constexpr int SMEM = OFF_BAR + 128 + 1024;  // 13 mbarriers + alignment slack
+    static_assert(SMEM == SMEM_ONE_X + (XDB ? X_BYTES : 0), "shared memory layout");
     static_assert(ZS_BYTES == TC * 64 * 4, "the output tile fits the Zs buffer");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
@@ -267,7 +280,8 @@ __device__ __forceinline__ void bar_arrive(int id, int n) {
 }
 
 template <int DX, int TC, bool REV>
-__global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_constant__ TcMaps maps, const LaArgs p) {
+__global__ void __launch_bounds__(kBlockThreads, TcCfg<DX, TC>::MIN_BLOCKS)
+    la_tc_kernel(const __grid_constant__ TcMaps maps, const LaArgs p) {
     using C = TcCfg<DX, TC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -279,8 +293,9 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool producer = (warp == 8);
-    // mbarriers: 0 X, 1 YZ0, 2 YZ1, 3 W, 4 P, 5 dS, 6 O_intra, 7 O_inter, 8-9 decay buffers
-    // full (the decay warp's 32 lanes arrive), 10-11 decay buffers empty (one arrival per math warp)
+    // mbarriers: 0 X (buffer 0), 1 YZ0, 2 YZ1, 3 W, 4 P, 5 dS, 6 O_intra, 7 O_inter, 8-9 decay
+    // buffers full (the decay warp's 32 lanes arrive), 10-11 decay buffers empty (one arrival per
+    // math warp), 12 X buffer 1
     const uint32_t bar0 = sbase + C::OFF_BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
@@ -293,6 +308,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
     }
     if (tid == 0) {
         for (int i = 0; i < 8; ++i) mbar_init(bar(i), 1);
+        mbar_init(bar(12), 1);
         mbar_init(bar(8), 32);
         mbar_init(bar(9), 32);
         mbar_init(bar(10), 8);
@@ -336,10 +352,13 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
     if (producer) {
         // ============================================================ producer warp
         const bool leader = (lane == 0);
-        auto issue_x = [&](int chunk) {
-            mbar_expect_tx(bar(0), (uint32_t)C::X_BYTES);
+        // X buffer xb (always 0 without double buffering) and its full barrier
+        auto xbar = [&](int xb) { return xb ? 12 : 0; };
+        auto issue_x = [&](int xb, int chunk) {
+            const uint32_t bx = bar(xbar(xb));
+            mbar_expect_tx(bx, (uint32_t)C::X_BYTES);
             for (int kb = 0; kb < C::KBX; ++kb)
-                tma_load_3d(sbase + C::OFF_X + kb * TC * 128, &maps.x, kb * 64, chunk * TC, bh, bar(0));
+                tma_load_3d(sbase + (xb ? C::OFF_X1 : C::OFF_X) + kb * TC * 128, &maps.x, kb * 64, chunk * TC, bh, bx);
         };
         auto issue_yz = [&](int b, int chunk) {
             mbar_expect_tx(bar(1 + b), (uint32_t)(C::X_BYTES + C::Z_BYTES));
@@ -354,7 +373,8 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
         };
         // Descriptors of every operand tile, built once; a K step adds a constant
         // byte offset (>> 4) to the start-address field.
-        const uint64_t dX = smem_desc(sbase + C::OFF_X, 16, 1024);                  // K-major
+        const uint64_t dX0 = smem_desc(sbase + C::OFF_X, 16, 1024);                 // K-major
+        auto dX = [&](int xb) { return dX0 + (uint64_t)(xb * ((C::OFF_X1 - C::OFF_X) >> 4)); };
         // The two Y and Z buffers differ only in their start address: buffer b's descriptor is
         // buffer 0's plus b times the buffer size (no arrays indexed at run time: those would
         // live in local memory, a cache miss in front of an MMA issue).
@@ -368,30 +388,43 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
         const uint64_t dS[2] = {smem_desc(sbase + C::OFF_SH, 8192, 1024), smem_desc(sbase + C::OFF_SL, 8192, 1024)};
         const uint64_t dZs = smem_desc(sbase + C::OFF_ZS, 16, 1024);               // K-major, 128 rows
         auto issue_state_mma = [&](int b) {
-            // dS = Y^T [Zs_hi | Zs_lo]  (M = DX, N = 128, K = Tc)
-            constexpr uint32_t id = idesc_bf16(DX, 128, 1, 0);
             const uint64_t a0 = dYt(b);
+            if constexpr (C::COMPACT) {
+                // dS = Y^T Zs_hi + Y^T Zs_lo in one accumulator (M = DX, N = 64, K = Tc, twice)
+                constexpr uint32_t id = idesc_bf16(DX, 64, 1, 0);
 #pragma unroll
-            for (int kk = 0; kk < TC / 16; ++kk)
-                mma_ss_w(tmem + C::C_DS, a0 + (uint64_t)(kk * 2048 / 16),
-                         dZs + (uint64_t)(((kk >> 2) * 128 * 128 + (kk & 3) * 32) / 16), id, kk ? 1u : 0u);
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < TC / 16; ++kk)
+                        mma_ss_w(tmem + C::C_DS, a0 + (uint64_t)(kk * 2048 / 16),
+                                 dZs + (uint64_t)(((kk >> 2) * 128 * 128 + (kk & 3) * 32 + part * 64 * 128) / 16), id,
+                                 (part | kk) ? 1u : 0u);
+            } else {
+                // dS = Y^T [Zs_hi | Zs_lo]  (M = DX, N = 128, K = Tc)
+                constexpr uint32_t id = idesc_bf16(DX, 128, 1, 0);
+#pragma unroll
+                for (int kk = 0; kk < TC / 16; ++kk)
+                    mma_ss_w(tmem + C::C_DS, a0 + (uint64_t)(kk * 2048 / 16),
+                             dZs + (uint64_t)(((kk >> 2) * 128 * 128 + (kk & 3) * 32) / 16), id, kk ? 1u : 0u);
+            }
         };
-        auto issue_p = [&](int b) {
+        auto issue_p = [&](int b, int xb) {
             constexpr uint32_t idp = idesc_bf16(TC, TC, 0, 0);
-            const uint64_t b0 = dY(b);
+            const uint64_t b0 = dY(b), a0 = dX(xb);
 #pragma unroll
             for (int kk = 0; kk < DX / 16; ++kk) {
                 const uint64_t off = (uint64_t)(((kk >> 2) * TC * 128 + (kk & 3) * 32) / 16);
-                mma_ss_w(tmem + C::C_P, dX + off, b0 + off, idp, kk ? 1u : 0u);
+                mma_ss_w(tmem + C::C_P, a0 + off, b0 + off, idp, kk ? 1u : 0u);
             }
         };
-        auto issue_inter = [&]() {
+        auto issue_inter = [&](int xb) {
             constexpr uint32_t ido = idesc_bf16(TC, 64, 0, 1);
+            const uint64_t a0 = dX(xb);
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
 #pragma unroll
                 for (int kk = 0; kk < DX / 16; ++kk)
-                    mma_ss_w(tmem + C::C_OI, dX + (uint64_t)(((kk >> 2) * TC * 128 + (kk & 3) * 32) / 16),
+                    mma_ss_w(tmem + C::C_OI, a0 + (uint64_t)(((kk >> 2) * TC * 128 + (kk & 3) * 32) / 16),
                              dS[part] + (uint64_t)(kk * 2048 / 16), ido, (part | kk) ? 1u : 0u);
             }
         };
@@ -424,22 +457,25 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
             if (leader && i + 2 < nc) issue_yz(b, chunk_at(i + 2));
         }
         // ---- phase 2 loads and the first scores while the math warps look back
+        // (chunk i's X sits in buffer i & 1 with double buffering, else in buffer 0)
+        auto xbuf = [&](int i) { return C::XDB ? (i & 1) : 0; };
         if (leader) {
             issue_yz(0, chunk_at(0));
             if (nc > 1) issue_yz(1, chunk_at(1));
-            issue_x(chunk_at(0));
+            issue_x(0, chunk_at(0));
+            if (C::XDB && nc > 1) issue_x(1, chunk_at(1));
             if (has_w) issue_w(chunk_at(0));
         }
         wait(1);
-        wait(0);
+        wait(xbar(0));
         tc_fence_after();
-        issue_p(0);
+        issue_p(0, 0);
         mma_commit_w(bar(4));
         for (int i = 0; i < nc; ++i) {
             const int b = i & 1;
             bar_sync(kBarDone, kAllThreads);  // previous chunk finished; State's bf16 parts written
             tc_fence_after();
-            issue_inter();
+            issue_inter(xbuf(i));
             mma_commit_w(bar(7));
             if (leader && has_w && i > 0) issue_w(chunk_at(i));
             __syncwarp();
@@ -447,20 +483,28 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
             tc_fence_after();
             issue_state_mma(b);
             mma_commit_w(bar(5));
-            wait(7);  // P and O_inter done: X is free
-            if (leader && i + 1 < nc) issue_x(chunk_at(i + 1));
+            wait(7);  // P and O_inter done: chunk i's X buffer is free
+            if (leader) {
+                if (C::XDB) {
+                    if (i + 2 < nc) issue_x(b, chunk_at(i + 2));
+                } else if (i + 1 < nc) {
+                    issue_x(0, chunk_at(i + 1));
+                }
+            }
             bar_sync(kBarPmask, kAllThreads);  // masked P written, P read
             tc_fence_after();
             issue_intra(b);
             mma_commit_w(bar(6));
+            // compact: the next P overwrites the masked scores O_intra reads
+            if (C::COMPACT) wait(6);
             if (i + 1 < nc) {
                 wait(1 + (b ^ 1));
-                wait(0);
+                wait(xbar(xbuf(i + 1)));
                 tc_fence_after();
-                issue_p(b ^ 1);
+                issue_p(b ^ 1, xbuf(i + 1));
                 mma_commit_w(bar(4));
             }
-            wait(6);
+            if (!C::COMPACT) wait(6);
             wait(5);
             if (leader && i + 2 < nc) issue_yz(b, chunk_at(i + 2));
         }
@@ -599,6 +643,19 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
 #pragma unroll
         for (int c = 0; c < SW; ++c) S[c] = 0.f;
         auto state_accumulate = [&](float alpha) {
+            if constexpr (C::COMPACT) {  // both bf16 parts of Zs already summed in one accumulator
+                uint32_t rd[SW];
+                tmem_ld_cols<SW>(tmem + tlane + C::C_DS + hf * 32, rd);
+                tmem_ld_wait();
+#pragma unroll
+                for (int jj = 0; jj < SW / 2; ++jj) {
+                    const float2 v = __ffma2_rn(make_float2(alpha, alpha), make_float2(S[2 * jj], S[2 * jj + 1]),
+                                                make_float2(__uint_as_float(rd[2 * jj]), __uint_as_float(rd[2 * jj + 1])));
+                    S[2 * jj] = v.x;
+                    S[2 * jj + 1] = v.y;
+                }
+                return;
+            }
             uint32_t rh[SW], rl[SW];
             tmem_ld_cols<SW>(tmem + tlane + C::C_DS + hf * 32, rh);
             tmem_ld_cols<SW>(tmem + tlane + C::C_DS + 64 + hf * 32, rl);
@@ -915,6 +972,11 @@ __global__ void __launch_bounds__(kBlockThreads, 1) la_tc_kernel(const __grid_co
                         // high parts of tokens s0.. at columns s0.., of s0+16.. at s0+8..; low parts 16 further
                         tmem_st8x2(tmem + tlane + C::C_PB + (uint32_t)s0, hi);
                         tmem_st8x2(tmem + tlane + C::C_PB + (uint32_t)(s0 + 16), lo);
+                    } else if constexpr (C::COMPACT) {
+                        // masked in place: every P product rewrites this fully masked piece
+                        const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                        tmem_st8x2(tmem + tlane + C::C_PB + (uint32_t)(piece * 32), zero);
+                        tmem_st8x2(tmem + tlane + C::C_PB + (uint32_t)(piece * 32 + 16), zero);
                     }
                     tmem_st_wait();
                 }
@@ -1064,7 +1126,20 @@ template <int DX, int TC, bool REV>
 int launch_tc_variant(const LaArgs &a, cudaStream_t s, unsigned int grid) {
     using C = TcCfg<DX, TC>;
     static std::atomic<unsigned long long> smem_set{0};  // per template instance
-    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(la_tc_kernel<DX, TC, REV>), C::SMEM);
+    const void *fn = reinterpret_cast<const void *>(la_tc_kernel<DX, TC, REV>);
+    if constexpr (C::COMPACT) {
+        // all of the unified L1 / shared array as shared memory, so that two blocks fit an SM
+        static std::atomic<unsigned long long> carve_set{0};
+        int dev = 0;
+        CLA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+        const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+        if (bit == 0ull || (carve_set.load(std::memory_order_acquire) & bit) == 0ull) {
+            CLA_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100),
+                         "cudaFuncSetAttribute");
+            carve_set.fetch_or(bit, std::memory_order_acq_rel);
+        }
+    }
+    const int st = set_max_dynamic_smem(smem_set, fn, C::SMEM);
     if (st) return st;
     TcMaps maps;
     memset(&maps, 0, sizeof(maps));
