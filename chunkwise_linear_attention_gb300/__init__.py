@@ -64,6 +64,8 @@ def lib():
                 "cla_chunk_la_ckpt_size": ([I64] * 5 + [INT], SZ),
                 "cla_chunk_la_fwd_ckpt": ([P] * 8 + [I64] * 5 + [INT, P, SZ, P], INT),
                 "cla_chunk_la_bwd_ckpt": ([P] * 13 + [I64] * 5 + [INT, P, SZ, P], INT),
+                "cla_gla_workspace_size": ([I64] * 5 + [INT], SZ),
+                "cla_gla_fwd": ([P] * 7 + [I64] * 5 + [INT, P, SZ, P], INT),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -376,3 +378,27 @@ def chunk_la_bwd(q, k, v, log_decay, S0, dO, dST=None, *, chunk=64, dq=None, dk=
         _launch("cla_chunk_la_bwd_ckpt", dev, args + (_ckpt_arg(ckpt, B, H, T, dkk, dvv, chunk),) + tail,
                 stream)
     return dq, dk, dv, dlog_decay, dS0
+
+
+# ---------------------------------------------------------------- gated linear attention
+def gla_workspace_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
+    return int(lib().cla_gla_workspace_size(B, H, T, dim_k, dim_v, int(chunk)))
+
+
+def gla_fwd(q, k, v, log_decay, S0=None, *, chunk=64, o=None, ST=None, workspace=None, stream=None):
+    """Gated linear attention forward (one decay per key dimension: log_decay [B, H, T, dk]);
+    returns (o, ST).  check_status(workspace) reports decays outside the kernel's range."""
+    B, H, T, dk = _dims(q, 4, "q")
+    dv = _dims(v, 4, "v")[3]
+    dev = q.device
+    f32, bf16 = torch.float32, torch.bfloat16
+    o = _out(o, (B, H, T, dv), f32, dev)
+    ST = _out(ST, (B, H, dk, dv), f32, dev)
+    ws = _ws(gla_workspace_size(B, H, T, dk, dv, chunk), dev, workspace)
+    tk, tv, st = (B, H, T, dk), (B, H, T, dv), (B, H, dk, dv)
+    _launch("cla_gla_fwd", dev, (
+        _T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
+        _T(log_decay, f32, "log_decay", tk), _T(S0, f32, "S0", st),
+        _T(o, f32, "o", tv), _T(ST, f32, "ST", st),
+        B, H, T, dk, dv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws)), stream)
+    return o, ST

@@ -79,5 +79,10 @@ extern "C" int cla_check_status(const void *ws, void *stream) {
     CLA_CUDA_TRY(cudaStreamSynchronize(s), "cla_check_status: synchronize");
     if (hdr.error & cla::kErrTimeout)
         return cla::fail(CLA_ERR_TIMEOUT, "a cross-block wait gave up (site %u)", hdr.where);
+    if (hdr.error & cla::kErrRange)
+        return cla::fail(CLA_ERR_UNSUPPORTED,
+                         "an input was outside the kernel's range (gated linear attention: a key dimension whose "
+                         "decay over 32 tokens of a chunk is below 2^-120, or a zero or non-finite gate); the "
+                         "results of that call are not valid");
     return CLA_OK;
 }

@@ -53,6 +53,9 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 constexpr unsigned int kErrTimeout = 1u;
+// An input outside what a kernel handles was met on the device (data the host
+// cannot check without a synchronisation); the results are not valid.
+constexpr unsigned int kErrRange = 2u;
 
 // Bound on polls of one flag (each poll after the first few sleeps ~100 ns):
 // about a second before a block gives up, far beyond any legitimate wait.

@@ -1,0 +1,660 @@
+// gla.cu -- gated linear attention (one decay per key dimension), forward,
+// chunkwise, for GB300 (sm_103a).
+//
+// "Parallel Scan" (zerotofrontier.app), "What one combine costs" (a diagonal
+// transition: one decay per state entry) and "The chunkwise algorithm" (the
+// GLA form S_t = G_t (.) S_{t-1} + k_t^T v_t, o_t = q_t S_t), with G_t[i][j] =
+// a_t[i]: every key dimension i has its own decay.
+//
+// With c_t[i] the in-chunk cumulative log2 decay of dimension i up to token t
+// (c includes the chunk's first token) and m the chunk's 32nd token, the
+// decay between a read at r and a write at s <= r factors through m:
+//     2^(c_r - c_s) = 2^(c_r - c_m) * 2^(c_m - c_s)
+// so, with Q~ = Q (.) 2^(c - c_m) and K~ = K (.) 2^(c_m - c) (per element),
+//     O_chunk = (Q~ K~^T . M) V + Q~ (diag(2^c_m) S_prev)
+//     S_next  = diag(2^(c_L - c_m)) (diag(2^c_m) S_prev + K~^T V)
+// (M the causal mask, c_L the chunk's last token).  Every factor except the
+// operand scalings of Q~ and K~ is at most 1; those two are at most the decay
+// over 32 tokens.  The kernel therefore needs |c_t - c_m| <= 120 in every
+// dimension of every chunk (a gate product over 32 tokens of at least
+// 2^-120) and finite log decays; a chunk outside that range sets an error
+// flag that cla_check_status reports (the products would overflow fp32).
+//
+// Q~, K~ and the state are scaled in fp32 and split into bf16 high and low
+// parts, and each product takes the parts that keep the rounding below the
+// outputs' tolerance: Q~ K~^T and Q~ S' as hi.hi + hi.lo + lo.hi, P V and
+// K~^T V as hi + lo (V is an exact bf16 input).  Products run on mma.sync
+// m16n8k16 (bf16 in, fp32 accumulate).
+//
+// Chunk parallelism as in chunk_la.cu: a block owns one segment of chunks of
+// one (batch, head) and 64 value columns; phase 1 folds the segment into one
+// affine pair (diag(alpha_seg), dS_seg), now with one decay per key
+// dimension; decoupled look-back over earlier segments gives the incoming
+// state; phase 2 runs the chunks from it and writes O.
+#include "cla_internal.cuh"
+#include "mma_sync.cuh"
+
+namespace cla {
+namespace {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr float kGlaLog2e = 1.4426950408889634f;
+constexpr int kGlaTc = 64;        // tokens per chunk
+constexpr int kGlaMid = 31;       // reference token of a chunk
+constexpr float kGlaSpan = 120.f; // largest |c_t - c_mid| (log2) the operand scalings allow
+constexpr int kGlaThreads = 128;  // warp w: rows 16w..16w+15 of a chunk, state rows 16(w S_MT)..
+constexpr int kGlaSegChoices[4] = {64, 32, 16, 8};
+constexpr long long kGlaMinBlocks = 1024;
+
+template <int DK>
+struct GlaCfg {
+    static constexpr int QRB = DK * 2;  // bytes per row of a Q or K tile (bf16)
+    static constexpr int VRB = 128;     // bytes per row of a 64-column V slab (bf16)
+    static constexpr int GRB = DK * 4;  // bytes per row of log decays / cumulative decays (fp32)
+    static constexpr int Q_BYTES = kGlaTc * QRB;
+    static constexpr int V_BYTES = kGlaTc * VRB;
+    static constexpr int G_BYTES = kGlaTc * GRB;
+    // one stage: Q (then the high part of Q~), K (then K~'s high part), V, log decays (then c)
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = Q_BYTES;
+    static constexpr int OFF_V = 2 * Q_BYTES;
+    static constexpr int OFF_G = 2 * Q_BYTES + V_BYTES;
+    static constexpr int STAGE = 2 * Q_BYTES + V_BYTES + G_BYTES;
+    static constexpr int OFF_QLO = 2 * STAGE;             // low part of Q~
+    static constexpr int OFF_KLO = OFF_QLO + Q_BYTES;     // low part of K~
+    static constexpr int OFF_SH = OFF_KLO + Q_BYTES;      // S' = diag(2^c_m) S, high part, [DK][64]
+    static constexpr int OFF_SL = OFF_SH + DK * VRB;      // and its low part
+    static constexpr int OFF_AS = OFF_SL + DK * VRB;      // alpha of the segment per key dimension
+    static constexpr int SMEM = OFF_AS + DK * 4;
+    static constexpr int S_MT = DK / 64;  // 16-row state tiles per warp (DK / 16 over 4 warps)
+    static constexpr int S_NT = 8;        // 8-column state tiles: all 64 columns
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+struct GlaArgs {
+    const bf16 *q, *k, *v;  // q, k: [BH][T][DK]; v: [BH][T][DV]
+    const float *g;         // [BH][T][DK] natural-log decays
+    const float *S0;        // [BH][DK][DV] or NULL
+    float *o;               // [BH][T][DV]
+    float *ST;              // [BH][DK][DV] or NULL
+    int BH, DV, nzb, n_chunks, seg_chunks, n_seg;
+    long long T;
+    WsHeader *hdr;
+    unsigned int *flags;  // [unit]
+    float *alpha;         // [unit][DK]
+    float4 *agg, *incl;   // [unit][tiles][threads]
+};
+
+template <int DK>
+__global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p) {
+    using C = GlaCfg<DK>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ unsigned int s_ticket, s_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    if (tid == 0) s_ticket = atomicAdd(&p.hdr->ticket[0], 1u);
+    __syncthreads();
+    const unsigned int tk = s_ticket;
+    const int per_seg = p.BH * p.nzb;
+    const int seg = (int)(tk / per_seg);
+    const int bh = (int)(tk % per_seg) / p.nzb;
+    const int zb = (int)(tk % per_seg) % p.nzb;
+    const int c_begin = seg * p.seg_chunks;
+    const int c_end = min(c_begin + p.seg_chunks, p.n_chunks);
+    const int nc = c_end - c_begin;
+    const size_t unit = ((size_t)seg * p.BH + bh) * p.nzb + zb;
+
+    const bf16 *Qb = p.q + (size_t)bh * p.T * DK;
+    const bf16 *Kb = p.k + (size_t)bh * p.T * DK;
+    const bf16 *Vb = p.v + (size_t)bh * p.T * p.DV + zb * 64;
+    const float *Gb = p.g + (size_t)bh * p.T * DK;
+    float *alpha_s = reinterpret_cast<float *>(smem + C::OFF_AS);
+
+    auto load_stage = [&](int stage, int chunk, bool withQ) {
+        uint8_t *st = smem + stage * C::STAGE;
+        const long long t0 = (long long)chunk * kGlaTc;
+        constexpr int QC = C::QRB / 16, GC = C::GRB / 16;
+        for (int i = tid; i < kGlaTc * QC; i += kGlaThreads) {
+            const int row = i / QC, c16 = i % QC;
+            const long long t = t0 + row;
+            const bool ok = t < p.T;
+            const size_t off = (size_t)(ok ? t : 0) * DK + c16 * 8;
+            cp_async16(smem_u32(st + C::OFF_K + swz<C::QRB>(row, c16)), Kb + off, ok ? 16u : 0u);
+            if (withQ) cp_async16(smem_u32(st + C::OFF_Q + swz<C::QRB>(row, c16)), Qb + off, ok ? 16u : 0u);
+        }
+        for (int i = tid; i < kGlaTc * 8; i += kGlaThreads) {
+            const int row = i >> 3, c16 = i & 7;
+            const long long t = t0 + row;
+            const bool ok = t < p.T;
+            cp_async16(smem_u32(st + C::OFF_V + swz<C::VRB>(row, c16)), Vb + (size_t)(ok ? t : 0) * p.DV + c16 * 8,
+                       ok ? 16u : 0u);
+        }
+        for (int i = tid; i < kGlaTc * GC; i += kGlaThreads) {  // padding tokens: log a = 0
+            const int row = i / GC, c16 = i % GC;
+            const long long t = t0 + row;
+            const bool ok = t < p.T;
+            cp_async16(smem_u32(st + C::OFF_G + row * C::GRB + c16 * 16), Gb + (size_t)(ok ? t : 0) * DK + c16 * 4,
+                       ok ? 16u : 0u);
+        }
+    };
+
+    // In-chunk cumulative log2 decays, in place (thread i < DK scans dimension i), with the
+    // range check; returns (to thread i) the chunk's total c_L[i].
+    auto cumulate = [&](int stage) {
+        float *G = reinterpret_cast<float *>(smem + stage * C::STAGE + C::OFF_G);
+        float total = 0.f;
+        if (tid < DK) {
+            float run = 0.f, lo = 0.f, hi = 0.f;
+            bool finite = true;
+            for (int t = 0; t < kGlaTc; ++t) {
+                const float l = G[t * DK + tid];
+                finite = finite && isfinite(l);
+                run += l * kGlaLog2e;
+                G[t * DK + tid] = run;
+                lo = fminf(lo, run);
+                hi = fmaxf(hi, run);
+            }
+            const float cm = G[kGlaMid * DK + tid];
+            // the running sum starts at 0 before token 0: include it in the span as well
+            if (!finite || hi - cm > kGlaSpan || cm - lo > kGlaSpan || cm > kGlaSpan)
+                atomicOr(&p.hdr->error, kErrRange);
+            total = run;
+        }
+        return total;
+    };
+
+    // Q~ = Q 2^(c - c_m) (high part over Q, low part in QLO) and K~ = K 2^(c_m - c).
+    auto scale_operands = [&](int stage, bool withQ) {
+        uint8_t *st = smem + stage * C::STAGE;
+        const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
+        constexpr int QC = C::QRB / 16;
+        for (int i = tid; i < kGlaTc * QC; i += kGlaThreads) {
+            const int row = i / QC, c16 = i % QC;
+            const float4 *crow = reinterpret_cast<const float4 *>(G + row * DK + c16 * 8);
+            const float4 *cmid = reinterpret_cast<const float4 *>(G + kGlaMid * DK + c16 * 8);
+            float d[8];
+            {
+                const float4 a = crow[0], b = crow[1], ma = cmid[0], mb = cmid[1];
+                d[0] = a.x - ma.x; d[1] = a.y - ma.y; d[2] = a.z - ma.z; d[3] = a.w - ma.w;
+                d[4] = b.x - mb.x; d[5] = b.y - mb.y; d[6] = b.z - mb.z; d[7] = b.w - mb.w;
+            }
+            const uint32_t off = swz<C::QRB>(row, c16);
+            {
+                const uint4 kv = *reinterpret_cast<const uint4 *>(st + C::OFF_K + off);
+                const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 x = unpack_bf16(w[e]);
+                    split_bf16x2(make_float2(x.x * ex2(-d[2 * e]), x.y * ex2(-d[2 * e + 1])), hi[e], lo[e]);
+                }
+                *reinterpret_cast<uint4 *>(st + C::OFF_K + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(smem + C::OFF_KLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            if (withQ) {
+                const uint4 qv = *reinterpret_cast<const uint4 *>(st + C::OFF_Q + off);
+                const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 x = unpack_bf16(w[e]);
+                    split_bf16x2(make_float2(x.x * ex2(d[2 * e]), x.y * ex2(d[2 * e + 1])), hi[e], lo[e]);
+                }
+                *reinterpret_cast<uint4 *>(st + C::OFF_Q + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(smem + C::OFF_QLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+    };
+
+    // State fragments: warp w owns rows (key dimensions) 16(w S_MT + mi) + {g, g + 8} and the
+    // columns of all 8 m16n8 tiles.
+    constexpr int S_MT = C::S_MT, S_NT = C::S_NT;
+    float S[S_MT][S_NT][4];
+    auto s_row = [&](int mi, int h) { return (warp * S_MT + mi) * 16 + g + h * 8; };
+    auto s_col = [&](int nj, int e) { return nj * 8 + tq * 2 + (e & 1); };
+    auto zero_state = [&](float (&X)[S_MT][S_NT][4]) {
+#pragma unroll
+        for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+            for (int nj = 0; nj < S_NT; ++nj)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) X[mi][nj][e] = 0.f;
+    };
+    // per-row scaling of the state by 2^(x[row]) read from a [.][DK] row of log2 values
+    auto scale_rows = [&](const float *lg2, float sub_from) {
+#pragma unroll
+        for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float f = ex2(lg2[s_row(mi, h)] - sub_from);
+#pragma unroll
+                for (int nj = 0; nj < S_NT; ++nj) {
+                    S[mi][nj][2 * h] *= f;
+                    S[mi][nj][2 * h + 1] *= f;
+                }
+            }
+    };
+    // S' = diag(2^c_m) S, in place (registers)
+    auto state_to_mid = [&](int stage) {
+        const float *G = reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G);
+        scale_rows(G + kGlaMid * DK, 0.f);
+    };
+    // S' as two bf16 parts for the Q~ S' product
+    auto write_sb = [&]() {
+#pragma unroll
+        for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+            for (int nj = 0; nj < S_NT; ++nj)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = s_row(mi, h), col = s_col(nj, 0);
+                    const uint32_t off = swz<C::VRB>(row, col >> 3) + (col & 7) * 2;
+                    uint32_t hi, lo;
+                    split_bf16x2(make_float2(S[mi][nj][2 * h], S[mi][nj][2 * h + 1]), hi, lo);
+                    *reinterpret_cast<uint32_t *>(smem + C::OFF_SH + off) = hi;
+                    *reinterpret_cast<uint32_t *>(smem + C::OFF_SL + off) = lo;
+                }
+    };
+    // S' + K~^T V (two products: K~'s parts), then rows scaled by 2^(c_L - c_m)
+    auto state_update = [&](int stage) {
+        const uint8_t *st = smem + stage * C::STAGE;
+#pragma unroll
+        for (int kt = 0; kt < kGlaTc / 16; ++kt) {
+            uint32_t b[S_NT / 2][4];
+#pragma unroll
+            for (int pp = 0; pp < S_NT / 2; ++pp) {
+                const int brow = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                ldsm_x4_t(smem_u32(st + C::OFF_V + swz<C::VRB>(brow, 2 * pp + (lane >> 4))), b[pp]);
+            }
+#pragma unroll
+            for (int mi = 0; mi < S_MT; ++mi) {
+                const int arow = kt * 16 + (lane & 7) + (lane >> 4) * 8;
+                const int ac16 = 2 * (warp * S_MT + mi) + ((lane >> 3) & 1);
+                uint32_t ah[4], al[4];
+                ldsm_x4_t(smem_u32(st + C::OFF_K + swz<C::QRB>(arow, ac16)), ah);
+                ldsm_x4_t(smem_u32(smem + C::OFF_KLO + swz<C::QRB>(arow, ac16)), al);
+#pragma unroll
+                for (int pp = 0; pp < S_NT / 2; ++pp) {
+                    mma16816(S[mi][2 * pp], ah, b[pp][0], b[pp][1]);
+                    mma16816(S[mi][2 * pp + 1], ah, b[pp][2], b[pp][3]);
+                    mma16816(S[mi][2 * pp], al, b[pp][0], b[pp][1]);
+                    mma16816(S[mi][2 * pp + 1], al, b[pp][2], b[pp][3]);
+                }
+            }
+        }
+        const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
+#pragma unroll
+        for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = s_row(mi, h);
+                const float f = ex2(G[(kGlaTc - 1) * DK + row] - G[kGlaMid * DK + row]);
+#pragma unroll
+                for (int nj = 0; nj < S_NT; ++nj) {
+                    S[mi][nj][2 * h] *= f;
+                    S[mi][nj][2 * h + 1] *= f;
+                }
+            }
+    };
+
+    // ------------------------------------------------ phase 1: the segment's affine pair
+    zero_state(S);
+    float la_seg = 0.f;  // thread i < DK: log2 of alpha_seg[i]
+    load_stage(0, c_begin, false);
+    cp_async_commit();
+    if (nc > 1) load_stage(1, c_begin + 1, false);
+    cp_async_commit();
+    for (int i = 0; i < nc; ++i) {
+        const int stage = i & 1;
+        cp_async_wait<1>();
+        __syncthreads();
+        la_seg += cumulate(stage);
+        __syncthreads();
+        scale_operands(stage, false);
+        state_to_mid(stage);
+        __syncthreads();
+        state_update(stage);
+        __syncthreads();
+        if (i + 2 < nc) load_stage(stage, c_begin + i + 2, false);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ------------------------------------------------ look-back for the incoming state
+    constexpr int TILES = S_MT * S_NT;
+    auto ws_index = [&](size_t u, int tile) { return u * (size_t)(TILES * kGlaThreads) + (size_t)tile * kGlaThreads + tid; };
+    float Sin[S_MT][S_NT][4];
+    auto add_state0 = [&](const float (&scale)[S_MT][2]) {
+        if (p.S0 == nullptr) return;
+#pragma unroll
+        for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+            for (int nj = 0; nj < S_NT; ++nj)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int row = s_row(mi, e >> 1), col = zb * 64 + s_col(nj, e);
+                    Sin[mi][nj][e] = fmaf(scale[mi][e >> 1], __ldg(p.S0 + ((size_t)bh * DK + row) * p.DV + col),
+                                          Sin[mi][nj][e]);
+                }
+    };
+    zero_state(Sin);
+    if (tid < DK) alpha_s[tid] = ex2(la_seg);
+    if (seg == 0) {
+        float one[S_MT][2];
+#pragma unroll
+        for (int mi = 0; mi < S_MT; ++mi) one[mi][0] = one[mi][1] = 1.f;
+        add_state0(one);
+    } else {
+#pragma unroll
+        for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+            for (int nj = 0; nj < S_NT; ++nj)
+                __stcg(p.agg + ws_index(unit, mi * S_NT + nj),
+                       make_float4(S[mi][nj][0], S[mi][nj][1], S[mi][nj][2], S[mi][nj][3]));
+        if (tid < DK) __stcg(p.alpha + unit * DK + tid, ex2(la_seg));
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release(p.flags + unit, 1u);
+        float accA[S_MT][2];
+#pragma unroll
+        for (int mi = 0; mi < S_MT; ++mi) accA[mi][0] = accA[mi][1] = 1.f;
+        int j = seg - 1;
+        while (true) {
+            const size_t up = ((size_t)j * p.BH + bh) * p.nzb + zb;
+            if (tid == 0) s_flag = wait_flag(p.flags + up, p.hdr, 60u);
+            __syncthreads();
+            const unsigned int f = s_flag;
+            __syncthreads();
+            if (f != 1u && f != 2u) break;  // the wait gave up (recorded in the header)
+            const float4 *src = (f == 2u) ? p.incl : p.agg;
+#pragma unroll
+            for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+                for (int nj = 0; nj < S_NT; ++nj) {
+                    const float4 v = ld_cg4(src + ws_index(up, mi * S_NT + nj));
+                    Sin[mi][nj][0] = fmaf(accA[mi][0], v.x, Sin[mi][nj][0]);
+                    Sin[mi][nj][1] = fmaf(accA[mi][0], v.y, Sin[mi][nj][1]);
+                    Sin[mi][nj][2] = fmaf(accA[mi][1], v.z, Sin[mi][nj][2]);
+                    Sin[mi][nj][3] = fmaf(accA[mi][1], v.w, Sin[mi][nj][3]);
+                }
+            if (f == 2u) break;
+#pragma unroll
+            for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) accA[mi][h] *= ld_cg(p.alpha + up * DK + s_row(mi, h));
+            if (--j < 0) {
+                add_state0(accA);
+                break;
+            }
+        }
+    }
+    __syncthreads();  // alpha_s visible
+    if (seg != p.n_seg - 1) {
+        // inclusive state at the segment's end: diag(alpha_seg) S_in + dS_seg
+#pragma unroll
+        for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+            for (int nj = 0; nj < S_NT; ++nj) {
+                const float a0 = alpha_s[s_row(mi, 0)], a1 = alpha_s[s_row(mi, 1)];
+                __stcg(p.incl + ws_index(unit, mi * S_NT + nj),
+                       make_float4(fmaf(a0, Sin[mi][nj][0], S[mi][nj][0]), fmaf(a0, Sin[mi][nj][1], S[mi][nj][1]),
+                                   fmaf(a1, Sin[mi][nj][2], S[mi][nj][2]), fmaf(a1, Sin[mi][nj][3], S[mi][nj][3])));
+            }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release(p.flags + unit, 2u);
+    }
+
+    // ------------------------------------------------ phase 2: outputs from the true state
+#pragma unroll
+    for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+        for (int nj = 0; nj < S_NT; ++nj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) S[mi][nj][e] = Sin[mi][nj][e];
+    load_stage(0, c_begin, true);
+    cp_async_commit();
+    if (nc > 1) load_stage(1, c_begin + 1, true);
+    cp_async_commit();
+    for (int i = 0; i < nc; ++i) {
+        const int stage = i & 1;
+        const uint8_t *st = smem + stage * C::STAGE;
+        const long long t0 = (long long)(c_begin + i) * kGlaTc;
+        cp_async_wait<1>();
+        __syncthreads();
+        cumulate(stage);
+        __syncthreads();
+        scale_operands(stage, true);
+        state_to_mid(stage);
+        write_sb();
+        __syncthreads();
+
+        // scores of this warp's 16 rows against the chunk's 64 tokens: Q~ K~^T (three products)
+        float P[8][4];
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) P[nj][e] = 0.f;
+        const int arow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll 2
+        for (int kk = 0; kk < DK / 16; ++kk) {
+            uint32_t qh[4], ql[4];
+            const uint32_t aoff = swz<C::QRB>(arow, 2 * kk + (lane >> 4));
+            ldsm_x4(smem_u32(st + C::OFF_Q + aoff), qh);
+            ldsm_x4(smem_u32(smem + C::OFF_QLO + aoff), ql);
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                const int brow = 16 * pp + (lane & 7) + (lane >> 4) * 8;
+                const uint32_t boff = swz<C::QRB>(brow, 2 * kk + ((lane >> 3) & 1));
+                uint32_t kh[4], kl[4];
+                ldsm_x4(smem_u32(st + C::OFF_K + boff), kh);
+                ldsm_x4(smem_u32(smem + C::OFF_KLO + boff), kl);
+                mma16816(P[2 * pp], qh, kh[0], kh[1]);
+                mma16816(P[2 * pp + 1], qh, kh[2], kh[3]);
+                mma16816(P[2 * pp], qh, kl[0], kl[1]);
+                mma16816(P[2 * pp + 1], qh, kl[2], kl[3]);
+                mma16816(P[2 * pp], ql, kh[0], kh[1]);
+                mma16816(P[2 * pp + 1], ql, kh[2], kh[3]);
+            }
+        }
+        // causal mask (token s <= row r), then the masked scores as A fragments in two parts
+        uint32_t ph[4][4], pl[4][4];
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = warp * 16 + g + 8 * h, s = nj * 8 + 2 * tq;
+                const float x0 = (s <= r) ? P[nj][2 * h] : 0.f;
+                const float x1 = (s + 1 <= r) ? P[nj][2 * h + 1] : 0.f;
+                // A fragment of k-step nj / 2: regs {row g, k lo}, {g + 8, lo}, {g, hi}, {g + 8, hi}
+                split_bf16x2(make_float2(x0, x1), ph[nj >> 1][(nj & 1) * 2 + h], pl[nj >> 1][(nj & 1) * 2 + h]);
+            }
+        float O[8][4];
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) O[nj][e] = 0.f;
+        // O = P V (two products) ...
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                uint32_t b[4];
+                const int brow = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                ldsm_x4_t(smem_u32(st + C::OFF_V + swz<C::VRB>(brow, 2 * pp + (lane >> 4))), b);
+                mma16816(O[2 * pp], ph[kt], b[0], b[1]);
+                mma16816(O[2 * pp + 1], ph[kt], b[2], b[3]);
+                mma16816(O[2 * pp], pl[kt], b[0], b[1]);
+                mma16816(O[2 * pp + 1], pl[kt], b[2], b[3]);
+            }
+        }
+        // ... + Q~ S' (three products)
+#pragma unroll 2
+        for (int kk = 0; kk < DK / 16; ++kk) {
+            uint32_t qh[4], ql[4];
+            const uint32_t aoff = swz<C::QRB>(arow, 2 * kk + (lane >> 4));
+            ldsm_x4(smem_u32(st + C::OFF_Q + aoff), qh);
+            ldsm_x4(smem_u32(smem + C::OFF_QLO + aoff), ql);
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                const int brow = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const uint32_t boff = swz<C::VRB>(brow, 2 * pp + (lane >> 4));
+                uint32_t sh[4], sl[4];
+                ldsm_x4_t(smem_u32(smem + C::OFF_SH + boff), sh);
+                ldsm_x4_t(smem_u32(smem + C::OFF_SL + boff), sl);
+                mma16816(O[2 * pp], qh, sh[0], sh[1]);
+                mma16816(O[2 * pp + 1], qh, sh[2], sh[3]);
+                mma16816(O[2 * pp], qh, sl[0], sl[1]);
+                mma16816(O[2 * pp + 1], qh, sl[2], sl[3]);
+                mma16816(O[2 * pp], ql, sh[0], sh[1]);
+                mma16816(O[2 * pp + 1], ql, sh[2], sh[3]);
+            }
+        }
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const long long t = t0 + warp * 16 + g + 8 * h;
+                if (t < p.T)
+                    *reinterpret_cast<float2 *>(p.o + ((size_t)bh * p.T + t) * p.DV + zb * 64 + nj * 8 + 2 * tq) =
+                        make_float2(O[nj][2 * h], O[nj][2 * h + 1]);
+            }
+        state_update(stage);
+        __syncthreads();
+        if (i + 2 < nc) load_stage(stage, c_begin + i + 2, true);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+
+    if (seg == p.n_seg - 1 && p.ST != nullptr) {
+#pragma unroll
+        for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+            for (int nj = 0; nj < S_NT; ++nj)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    p.ST[((size_t)bh * DK + s_row(mi, e >> 1)) * p.DV + zb * 64 + s_col(nj, e)] = S[mi][nj][e];
+    }
+}
+
+// ----------------------------------------------------------------- host side
+struct GlaPlan {
+    int n_chunks, seg_chunks, n_seg, nzb;
+    size_t units, off_flags, off_alpha, off_agg, off_incl, total;
+};
+
+GlaPlan gla_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv) {
+    GlaPlan p;
+    p.n_chunks = (int)((T + kGlaTc - 1) / kGlaTc);
+    p.nzb = (int)(dv / 64);
+    const size_t BH = (size_t)B * H;
+    p.seg_chunks = kGlaSegChoices[3];
+    for (int c : kGlaSegChoices) {
+        const long long nseg = (p.n_chunks + c - 1) / c;
+        if (nseg * (long long)BH * p.nzb >= kGlaMinBlocks) {
+            p.seg_chunks = c;
+            break;
+        }
+    }
+    p.n_seg = (p.n_chunks + p.seg_chunks - 1) / p.seg_chunks;
+    if (p.n_seg < 1) p.n_seg = 1;
+    p.units = (size_t)p.n_seg * BH * p.nzb;
+    p.off_flags = sizeof(WsHeader);
+    p.off_alpha = align_up(p.off_flags + p.units * 4, 256);
+    p.off_agg = align_up(p.off_alpha + p.units * (size_t)dk * 4, 256);
+    const size_t state_bytes = (size_t)dk * 64 * 4;  // one block's state tiles
+    p.off_incl = align_up(p.off_agg + p.units * state_bytes, 256);
+    p.total = align_up(p.off_incl + p.units * state_bytes, 256);
+    return p;
+}
+
+// Sizes the kernel handles: B*H <= 2^24, T <= 2^34, B*H*T <= 2^40, grid below 2^31 blocks.
+bool gla_sizes_fit(int64_t B, int64_t H, int64_t T) {
+    if (!product_below({B, H}, 16777217.0) || T > (1ll << 34)) return false;
+    if (!product_below({B, H, T}, 1099511627777.0)) return false;
+    const int64_t n_chunks = (T + kGlaTc - 1) / kGlaTc;
+    return product_below({B, H, n_chunks, 2}, 2147483648.0);
+}
+
+bool gla_supported(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chunk) {
+    return B >= 0 && H >= 0 && T >= 0 && (dk == 64 || dk == 128) && dv > 0 && dv % 64 == 0 && dv <= 1024 &&
+           chunk == kGlaTc && gla_sizes_fit(B, H, T);
+}
+
+template <int DK>
+int launch_gla_fwd(const GlaArgs &a, cudaStream_t s, unsigned int grid) {
+    using C = GlaCfg<DK>;
+    static std::atomic<unsigned long long> smem_set{0};
+    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_fwd_kernel<DK>), C::SMEM);
+    if (st) return st;
+    gla_fwd_kernel<DK><<<grid, kGlaThreads, C::SMEM, s>>>(a);
+    return check_launch("gla_fwd_kernel");
+}
+
+}  // namespace
+}  // namespace cla
+
+using namespace cla;
+
+extern "C" size_t cla_gla_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk) {
+    if (!gla_supported(B, H, T, dim_k, dim_v, chunk)) return 0;
+    return gla_plan(B, H, T, dim_k, dim_v).total;
+}
+
+extern "C" int cla_gla_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                           const float *S0, float *o, float *ST, int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                           int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
+    clear_error();
+    const char *fn = "cla_gla_fwd";
+    if (B < 0 || H < 0 || T < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (!gla_supported(B, H, T, dim_k, dim_v, chunk))
+        return fail(CLA_ERR_UNSUPPORTED, "%s: needs dim_k 64 or 128, dim_v a multiple of 64 up to 1024, chunk 64 "
+                    "and sizes within one launch (got dim_k %lld, dim_v %lld, chunk %d)", fn, (long long)dim_k,
+                    (long long)dim_v, chunk);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t BH = B * H;
+    if (BH == 0) return CLA_OK;
+    const size_t sbytes = sizeof(float) * BH * dim_k * dim_v;
+    if (T == 0) {
+        if (ST) {
+            if (S0) CLA_CUDA_TRY(cudaMemcpyAsync(ST, S0, sbytes, cudaMemcpyDeviceToDevice, s), fn);
+            else CLA_CUDA_TRY(cudaMemsetAsync(ST, 0, sbytes, s), fn);
+        }
+        return CLA_OK;
+    }
+    if (!q || !k || !v || !log_decay || !o) return fail(CLA_ERR_INVALID_ARG, "%s: q, k, v, log_decay, o required", fn);
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_decay))
+        return fail(CLA_ERR_INVALID_ARG, "%s: q, k, v, log_decay must be 16-byte aligned", fn);
+    if (!aligned_or_null({o}, 8) || !aligned_or_null({S0, ST}, 4))
+        return fail(CLA_ERR_INVALID_ARG, "%s: o must be 8-byte aligned, S0 and ST 4-byte aligned", fn);
+    if (!ws || !aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace NULL or unaligned", fn);
+    const GlaPlan pl = gla_plan(B, H, T, dim_k, dim_v);
+    if (ws_bytes < pl.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, pl.total);
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, pl.off_alpha, s), fn);
+    char *w = static_cast<char *>(ws);
+    GlaArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = reinterpret_cast<const bf16 *>(q);
+    a.k = reinterpret_cast<const bf16 *>(k);
+    a.v = reinterpret_cast<const bf16 *>(v);
+    a.g = log_decay;
+    a.S0 = S0;
+    a.o = o;
+    a.ST = ST;
+    a.BH = (int)BH;
+    a.DV = (int)dim_v;
+    a.nzb = pl.nzb;
+    a.n_chunks = pl.n_chunks;
+    a.seg_chunks = pl.seg_chunks;
+    a.n_seg = pl.n_seg;
+    a.T = T;
+    a.hdr = reinterpret_cast<WsHeader *>(w);
+    a.flags = reinterpret_cast<unsigned int *>(w + pl.off_flags);
+    a.alpha = reinterpret_cast<float *>(w + pl.off_alpha);
+    a.agg = reinterpret_cast<float4 *>(w + pl.off_agg);
+    a.incl = reinterpret_cast<float4 *>(w + pl.off_incl);
+    const unsigned int grid = (unsigned int)(pl.units);
+    return dim_k == 64 ? launch_gla_fwd<64>(a, s, grid) : launch_gla_fwd<128>(a, s, grid);
+}

@@ -62,8 +62,10 @@ const char *cla_status_string(int status);
 const char *cla_last_error_message(void);
 
 /* Synchronises `stream`, then reports CLA_ERR_TIMEOUT if a kernel of the last
- * call that used `ws` gave up a cross-block wait, CLA_ERR_CUDA if the stream
- * holds an error, else CLA_OK.  `ws` must be the workspace of that call. */
+ * call that used `ws` gave up a cross-block wait, CLA_ERR_UNSUPPORTED if it
+ * met data outside its range (cla_gla_fwd's decay bound), CLA_ERR_CUDA if the
+ * stream holds an error, else CLA_OK.  `ws` must be the workspace of that
+ * call. */
 int cla_check_status(const void *ws, void *stream);
 
 /* Self-test of the failure path: launches one warp that polls a workspace
@@ -316,6 +318,44 @@ int cla_chunk_la_bwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *
                           int64_t B, int64_t H, int64_t T, int64_t dim_k,
                           int64_t dim_v, int chunk, void *ws, size_t ws_bytes,
                           void *stream);
+
+/* ======================================================================== */
+/* Gated linear attention (matrix state, one decay per key dimension)       */
+/* ======================================================================== */
+
+/* Bytes of workspace for cla_gla_fwd; 0 for sizes, head dims or chunks that
+ * call refuses. */
+size_t cla_gla_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                              int64_t dim_v, int chunk);
+
+/* Forward of S_t = diag(a_t) S_{t-1} + k_t v_t^T (S is [dim_k, dim_v], rows
+ * indexed by keys; a_t = exp(log_decay_t) holds one decay per key
+ * dimension), o_t = S_t^T q_t, computed chunkwise ("Parallel Scan", "What one
+ * combine costs": a diagonal transition, and "The chunkwise algorithm": the
+ * gated form S_t = G_t (.) S_{t-1} + k_t^T v_t).  With c the in-chunk
+ * cumulative log2 decays and m a chunk's 32nd token, the decay between a
+ * read at r and a write at s factors as 2^(c_r - c_m) 2^(c_m - c_s), so the
+ * queries and keys are scaled per element and the intra-chunk scores are one
+ * product, masked causally:
+ *   O_[j]  = ((Q~ K~^T) . M) V_[j] + Q~ diag(2^c_m) S_[j-1]
+ *   S_[j]  = diag(2^(c_L - c_m)) (diag(2^c_m) S_[j-1] + K~^T V_[j])
+ * with Q~ = Q (.) 2^(c - c_m), K~ = K (.) 2^(c_m - c).
+ *   q, k       [B, H, T, dim_k] bf16
+ *   v          [B, H, T, dim_v] bf16
+ *   log_decay  [B, H, T, dim_k] fp32 (natural log of the gates, <= 0)
+ *   S0         [B, H, dim_k, dim_v] fp32 [opt]
+ *   o          [B, H, T, dim_v] fp32 out
+ *   ST         [B, H, dim_k, dim_v] fp32 [opt] out: S_T
+ * Supported: dim_k 64 or 128, dim_v a multiple of 64 up to 1024, chunk 64,
+ * any T >= 0.  Range: in every key dimension of every 64-token chunk, the
+ * gate product over the chunk's first 32 tokens and over its last 32 must be
+ * at least 2^-120 (no zero gates); the kernel checks this on the device and a
+ * violation makes cla_check_status(ws, stream) return CLA_ERR_UNSUPPORTED
+ * (the call's outputs are then not valid). */
+int cla_gla_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                const float *log_decay, const float *S0, float *o, float *ST,
+                int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
+                int chunk, void *ws, size_t ws_bytes, void *stream);
 
 #ifdef __cplusplus
 }

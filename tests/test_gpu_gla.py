@@ -1,0 +1,97 @@
+"""Gated linear attention forward (one decay per key dimension): GPU (through
+the C ABI) vs the oracle's per-token recurrence, with the bf16 tolerance (per
+output tensor, |x - r| / rms(r): max <= 2e-2, mean <= 5e-3), and the kernel's
+range check on decays it cannot factor."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._parity import assert_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cla():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import chunkwise_linear_attention_gb300 as m
+
+    m.lib()
+    return m
+
+
+def _dev(x):
+    return None if x is None else x.cuda()
+
+
+def _run(cla, inp, heads=None):
+    t = {k: _dev(v) for k, v in inp.items()}
+    ws = torch.empty(max(cla.gla_workspace_size(*t["q"].shape, t["v"].shape[-1], 64), 256), dtype=torch.uint8,
+                     device="cuda")
+    o, ST = cla.gla_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], workspace=ws)
+    cla.check_status(ws)
+    sel = (lambda x: x) if heads is None else (lambda x: None if x is None else x[:, heads])
+    ci = {k: sel(v) for k, v in inp.items()}
+    ro, rST = oracle.gla_fwd(ci["q"], ci["k"], ci["v"], ci["log_a"], ci["S0"])
+    assert_bf16("o", sel(o), ro)
+    assert_bf16("S_T", sel(ST), rST)
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv", [
+    (1, 2, 64, 64, 64), (1, 2, 300, 64, 64), (2, 1, 1, 64, 64), (1, 1, 1000, 128, 128),
+    (1, 2, 700, 128, 64), (1, 1, 129, 64, 192), (2, 2, 2000, 128, 128), (1, 1, 4097, 64, 128),
+])
+@pytest.mark.parametrize("with_state", [False, True])
+def test_gla_small(cla, B, H, T, dk, dv, with_state):
+    inp = workloads.make("gla", B=B, H=H, T=T, dk=dk, dv=dv)
+    if not with_state:
+        inp["S0"] = None
+    _run(cla, inp)
+
+
+def test_gla_strong_decay_within_range(cla):
+    """Gates down to e^-2.5 per token in some dimensions (a 32-token product near 2^-115, inside
+    the kernel's 2^-120 range), others near 1: the factored scores stay finite and exact."""
+    inp = workloads.make("gla", B=1, H=2, T=900, dk=64, dv=64)
+    la = inp["log_a"].clone()
+    la[:, :, :, ::3] = -2.5
+    la[:, :, :, 1::7] = -1e-4
+    inp["log_a"] = la
+    _run(cla, inp)
+
+
+def test_gla_decay_out_of_range_is_reported(cla):
+    """A zero gate (log a = -inf) or a 32-token product below 2^-120 cannot be factored:
+    cla_check_status reports CLA_ERR_UNSUPPORTED instead of returning overflowed results."""
+    for bad in (-float("inf"), -6.0):
+        inp = workloads.make("gla", B=1, H=1, T=200, dk=64, dv=64)
+        la = inp["log_a"].clone()
+        la[0, 0, 100:140, 5] = bad
+        t = {k: _dev(v) for k, v in inp.items()}
+        ws = torch.empty(cla.gla_workspace_size(1, 1, 200, 64, 64, 64), dtype=torch.uint8, device="cuda")
+        cla.gla_fwd(t["q"], t["k"], t["v"], la.cuda(), t["S0"], workspace=ws)
+        with pytest.raises(cla.ClaError, match="outside the kernel's range") as ei:
+            cla.check_status(ws)
+        assert ei.value.status == 2
+        # the context stays usable: a valid call right after passes
+        ws2 = torch.empty(cla.gla_workspace_size(1, 1, 200, 64, 64, 64), dtype=torch.uint8, device="cuda")
+        cla.gla_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], workspace=ws2)
+        cla.check_status(ws2)
+
+
+def test_gla_empty(cla):
+    q = torch.empty(1, 2, 0, 64, dtype=torch.bfloat16, device="cuda")
+    S0 = torch.randn(1, 2, 64, 64, device="cuda")
+    o, ST = cla.gla_fwd(q, q, q, torch.empty(1, 2, 0, 64, device="cuda"), S0)
+    torch.cuda.synchronize()
+    assert torch.equal(ST, S0)
+
+
+def test_gla_workload_full_sampled_heads(cla):
+    """The full gla workload (2 x 16 x 16384, d = 128), every output of three heads spread over
+    the batch (the heads are independent problems)."""
+    inp = workloads.make("gla")
+    _run(cla, inp, heads=[0, 7, 15])

@@ -24,6 +24,11 @@ Workloads (each runnable at any smaller shape with the same distributions):
   log a = -softplus(N(0, 1))/16 per (head, token); S0 ~ N(0, 0.01^2) fp32;
   chunk 128; dL/do ~ N(0, 1) bf16.
 
+* ``gla``         gated linear attention, one decay per key dimension (the next
+  row after the five above): B=2, H=16, T=16384, d_k=d_v=128; q, k, v bf16
+  ~ N(0, 1)/sqrt(128); log a = -softplus(N(0, 1))/16 per (head, token, key
+  dimension); S0 ~ N(0, 0.01^2) fp32; chunk 64; dL/do ~ N(0, 1) bf16.
+
 The second parameter of N(mu, s) is read as a standard deviation.
 """
 from __future__ import annotations
@@ -39,6 +44,7 @@ WORKLOADS = {
     "selective": dict(kind="selective", B=4, T=8192, D=2048, N=16, seed=3, backward=True),
     "la_const": dict(kind="chunk_la", B=4, H=16, T=8192, dk=64, dv=64, chunk=64, seed=4, backward=True),
     "la_long": dict(kind="chunk_la", B=1, H=32, T=65536, dk=128, dv=128, chunk=128, seed=5, backward=True),
+    "gla": dict(kind="gla", B=2, H=16, T=16384, dk=128, dv=128, chunk=64, seed=6, backward=False),
 }
 
 
@@ -119,12 +125,24 @@ def la_long_inputs(B=1, H=32, T=65536, dk=128, dv=128, seed=5):
     return dict(q=q, k=k, v=v, log_a=_f32(log_a), S0=_f32(S0), dO=dO)
 
 
+def gla_inputs(B=2, H=16, T=16384, dk=128, dv=128, seed=6):
+    s = 1.0 / math.sqrt(dk)
+    q = _bf16(_normal(seed, 0, (B, H, T, dk), std=s))
+    k = _bf16(_normal(seed, 1, (B, H, T, dk), std=s))
+    v = _bf16(_normal(seed, 2, (B, H, T, dv), std=s))
+    log_a = (-_softplus(_normal(seed, 3, (B, H, T, dk))) / 16.0).astype(np.float32)
+    S0 = _normal(seed, 4, (B, H, dk, dv), std=0.01)
+    dO = _bf16(_normal(seed, 5, (B, H, T, dv)))
+    return dict(q=q, k=k, v=v, log_a=_f32(log_a), S0=_f32(S0), dO=dO)
+
+
 GENERATORS = {
     "scan_small": scan_small_inputs,
     "scan": scan_inputs,
     "selective": selective_inputs,
     "la_const": la_const_inputs,
     "la_long": la_long_inputs,
+    "gla": gla_inputs,
 }
 
 
