@@ -452,6 +452,49 @@ def bench_la(torch, cla, workloads, dev, flush, peaks, name, chunk, iters=20, sh
     return res
 
 
+def bench_gla(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
+    """Gated linear attention forward and backward (one decay per key dimension), chunk 64."""
+    inp = workloads.make("gla", **(shape or {}))
+    t = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    B, H, T, dk = t["q"].shape
+    dv = t["v"].shape[-1]
+    ws = torch.empty(cla.gla_workspace_size(B, H, T, dk, dv, 64), dtype=torch.uint8, device=dev)
+    o = torch.empty(B, H, T, dv, device=dev)
+    ST = torch.empty(B, H, dk, dv, device=dev)
+    wb = torch.empty(cla.gla_bwd_workspace_size(B, H, T, dk, dv, 64), dtype=torch.uint8, device=dev)
+    grads = dict(dq=torch.empty(B, H, T, dk, device=dev), dk=torch.empty(B, H, T, dk, device=dev),
+                 dv=torch.empty(B, H, T, dv, device=dev), dlog_decay=torch.empty(B, H, T, dk, device=dev),
+                 dS0=torch.empty(B, H, dk, dv, device=dev))
+    fwd = lambda: cla.gla_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], o=o, ST=ST, workspace=ws)
+    bwd = lambda: cla.gla_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"], workspace=wb, **grads)
+    tf = _time_calls(torch, fwd, flush, iters)
+    tb = _time_calls(torch, bwd, flush, iters)
+    cla.check_status(ws)
+    cla.check_status(wb)
+    ntok = B * H * T
+    fl = ntok * (2 * 64 * (dk + dv) + 4 * dk * dv)
+    # backward: dQ and dK traversals (scores, two products each) and the adjoint traversal
+    # giving dV, at the same count per product as the forward's
+    fl_b = ntok * (5 * 2 * 64 * max(dk, dv) + 5 * 2 * dk * dv)
+    by = ntok * (2 * (2 * dk + dv) + 4 * dk + 4 * dv)  # q, k, v bf16, log decays fp32 per key dim, o fp32
+    by_min = ntok * (2 * (2 * dk + dv) + 4 * dk + 2 * dv)
+    by_b_min = ntok * (2 * (2 * dk + 2 * dv) + 4 * dk + 2 * (2 * dk + dv) + 4 * dk)
+    hbm = peaks["hbm_gbs"] * 1e9
+    bf = peaks["bf16_tflops"] * 1e12
+    sec, secb = tf / 1e3, tb / 1e3
+    res = {"workload": f"gated linear attention fwd+bwd B={B} H={H} T={T} dk={dk} dv={dv} chunk=64",
+           "fwd_us": round(tf * 1e3, 1), "bwd_us": round(tb * 1e3, 1), "tokens_per_s": round(B * T / (sec + secb), 1),
+           "fwd_TFLOPs": round(fl / sec / 1e12, 2), "bwd_TFLOPs": round(fl_b / secb / 1e12, 2),
+           "fwd_GBps": round(by / sec / 1e9, 1),
+           "frac_bf16_peak": round((fl + fl_b) / (sec + secb) / bf, 4),
+           "frac_binding_roofline_min_bytes": round(max((by_min + by_b_min) / hbm, (fl + fl_b) / bf) / (sec + secb), 4),
+           "kernels": "gla_fwd_kernel, gla_bwd_qk_kernel (mma.sync m16n8k16, bf16 hi/lo operand parts), "
+                      "gla_dlog_tile_sums/finalize"}
+    del t, ws, wb, o, ST, grads
+    torch.cuda.empty_cache()
+    return res
+
+
 def bench_selective(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
     inp = workloads.make("selective", **(shape or {}))
     t = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
@@ -561,7 +604,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--only", default=None,
-                    choices=["scan_small", "scan_fwd_blelloch", "scan_bwd_recompute", "selective", "la_const", "la_long", "la_long_chunk64"],
+                    choices=["scan_small", "scan_fwd_blelloch", "scan_bwd_recompute", "selective", "la_const", "la_long",
+                             "la_long_chunk64", "gla"],
                     help="time one workload only (forward and backward), e.g. for profiling")
     ap.add_argument("--shape", default="", help="shape overrides for --only, e.g. H=32,T=4096")
     args = ap.parse_args()
@@ -600,7 +644,8 @@ def main():
                "selective": lambda: bench_selective(torch, cla, workloads, dev, flush, peaks, it, shape),
                "la_const": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_const", 64, it, shape),
                "la_long": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 128, it, shape),
-               "la_long_chunk64": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 64, it, shape)}
+               "la_long_chunk64": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 64, it, shape),
+               "gla": lambda: bench_gla(torch, cla, workloads, dev, flush, peaks, it, shape)}
         print(json.dumps({"only": args.only, "shape": shape, "result": fns[args.only]()}), flush=True)
         return 0
 
@@ -625,7 +670,8 @@ def main():
                 ("selective", lambda: bench_selective(torch, cla, workloads, dev, flush, peaks)),
                 ("la_const", lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_const", 64)),
                 ("la_long", lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 128, e2e_steps=3)),
-                ("la_long_chunk64", lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 64))):
+                ("la_long_chunk64", lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 64)),
+                ("gla", lambda: bench_gla(torch, cla, workloads, dev, flush, peaks))):
             try:
                 extra[key] = fn()
             except Exception as e:  # an entry point without a kernel yet reports itself

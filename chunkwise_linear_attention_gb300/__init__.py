@@ -66,6 +66,8 @@ def lib():
                 "cla_chunk_la_bwd_ckpt": ([P] * 13 + [I64] * 5 + [INT, P, SZ, P], INT),
                 "cla_gla_workspace_size": ([I64] * 5 + [INT], SZ),
                 "cla_gla_fwd": ([P] * 7 + [I64] * 5 + [INT, P, SZ, P], INT),
+                "cla_gla_bwd_workspace_size": ([I64] * 5 + [INT], SZ),
+                "cla_gla_bwd": ([P] * 12 + [I64] * 5 + [INT, P, SZ, P], INT),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -402,3 +404,30 @@ def gla_fwd(q, k, v, log_decay, S0=None, *, chunk=64, o=None, ST=None, workspace
         _T(o, f32, "o", tv), _T(ST, f32, "ST", st),
         B, H, T, dk, dv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws)), stream)
     return o, ST
+
+
+def gla_bwd_workspace_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
+    return int(lib().cla_gla_bwd_workspace_size(B, H, T, dim_k, dim_v, int(chunk)))
+
+
+def gla_bwd(q, k, v, log_decay, S0, dO, dST=None, *, chunk=64, dq=None, dk=None, dv=None, dlog_decay=None,
+            dS0=None, workspace=None, stream=None):
+    """Gated linear attention backward; returns (dq, dk, dv, dlog_decay [B, H, T, dk], dS0)."""
+    B, H, T, dkk = _dims(q, 4, "q")
+    dvv = _dims(v, 4, "v")[3]
+    dev = q.device
+    f32, bf16 = torch.float32, torch.bfloat16
+    dq = _out(dq, (B, H, T, dkk), f32, dev)
+    dk = _out(dk, (B, H, T, dkk), f32, dev)
+    dv = _out(dv, (B, H, T, dvv), f32, dev)
+    dlog_decay = _out(dlog_decay, (B, H, T, dkk), f32, dev)
+    dS0 = _out(dS0, (B, H, dkk, dvv), f32, dev)
+    ws = _ws(gla_bwd_workspace_size(B, H, T, dkk, dvv, chunk), dev, workspace)
+    tk, tv, st = (B, H, T, dkk), (B, H, T, dvv), (B, H, dkk, dvv)
+    _launch("cla_gla_bwd", dev, (
+        _T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
+        _T(log_decay, f32, "log_decay", tk), _T(S0, f32, "S0", st), _T(dO, bf16, "dO", tv),
+        _T(dST, f32, "dST", st), _T(dq, f32, "dq", tk), _T(dk, f32, "dk", tk), _T(dv, f32, "dv", tv),
+        _T(dlog_decay, f32, "dlog_decay", tk), _T(dS0, f32, "dS0", st),
+        B, H, T, dkk, dvv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws)), stream)
+    return dq, dk, dv, dlog_decay, dS0

@@ -72,12 +72,19 @@ struct GlaCfg {
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
+// One traversal of the gated recurrence.  Forward (rev = 0): q, k, v, S0 -> o, ST.  Reversed
+// (rev = 1, the adjoint of the backward): token t' of the traversal is token T-1-t' of the
+// arrays and its decay is the one of token T-t' (none for t' = 0), which turns the adjoint
+// recursion Sbar_t = q_t^T obar_t + diag(a_{t+1}) Sbar_{t+1} into the same forward form; with
+// q <- k, k <- q, v <- dO and S0 <- dST it gives o = dV and ST = Sbar_0, and ST is then scaled
+// by a_0 to give dS0.
 struct GlaArgs {
     const bf16 *q, *k, *v;  // q, k: [BH][T][DK]; v: [BH][T][DV]
     const float *g;         // [BH][T][DK] natural-log decays
     const float *S0;        // [BH][DK][DV] or NULL
     float *o;               // [BH][T][DV]
     float *ST;              // [BH][DK][DV] or NULL
+    int rev;
     int BH, DV, nzb, n_chunks, seg_chunks, n_seg;
     long long T;
     WsHeader *hdr;
@@ -111,6 +118,8 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
     const float *Gb = p.g + (size_t)bh * p.T * DK;
     float *alpha_s = reinterpret_cast<float *>(smem + C::OFF_AS);
 
+    // array row of traversal token t (reversed: T-1-t), and of its decay (reversed: T-t, none at 0)
+    auto arow_of = [&](long long t) { return p.rev ? p.T - 1 - t : t; };
     auto load_stage = [&](int stage, int chunk, bool withQ) {
         uint8_t *st = smem + stage * C::STAGE;
         const long long t0 = (long long)chunk * kGlaTc;
@@ -119,7 +128,7 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
             const int row = i / QC, c16 = i % QC;
             const long long t = t0 + row;
             const bool ok = t < p.T;
-            const size_t off = (size_t)(ok ? t : 0) * DK + c16 * 8;
+            const size_t off = (size_t)(ok ? arow_of(t) : 0) * DK + c16 * 8;
             cp_async16(smem_u32(st + C::OFF_K + swz<C::QRB>(row, c16)), Kb + off, ok ? 16u : 0u);
             if (withQ) cp_async16(smem_u32(st + C::OFF_Q + swz<C::QRB>(row, c16)), Qb + off, ok ? 16u : 0u);
         }
@@ -127,14 +136,15 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
             const int row = i >> 3, c16 = i & 7;
             const long long t = t0 + row;
             const bool ok = t < p.T;
-            cp_async16(smem_u32(st + C::OFF_V + swz<C::VRB>(row, c16)), Vb + (size_t)(ok ? t : 0) * p.DV + c16 * 8,
-                       ok ? 16u : 0u);
+            cp_async16(smem_u32(st + C::OFF_V + swz<C::VRB>(row, c16)),
+                       Vb + (size_t)(ok ? arow_of(t) : 0) * p.DV + c16 * 8, ok ? 16u : 0u);
         }
         for (int i = tid; i < kGlaTc * GC; i += kGlaThreads) {  // padding tokens: log a = 0
             const int row = i / GC, c16 = i % GC;
             const long long t = t0 + row;
-            const bool ok = t < p.T;
-            cp_async16(smem_u32(st + C::OFF_G + row * C::GRB + c16 * 16), Gb + (size_t)(ok ? t : 0) * DK + c16 * 4,
+            const bool ok = t < p.T && !(p.rev && t == 0);
+            const long long ga = p.rev ? p.T - t : t;
+            cp_async16(smem_u32(st + C::OFF_G + row * C::GRB + c16 * 16), Gb + (size_t)(ok ? ga : 0) * DK + c16 * 4,
                        ok ? 16u : 0u);
         }
     };
@@ -518,8 +528,8 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
             for (int h = 0; h < 2; ++h) {
                 const long long t = t0 + warp * 16 + g + 8 * h;
                 if (t < p.T)
-                    *reinterpret_cast<float2 *>(p.o + ((size_t)bh * p.T + t) * p.DV + zb * 64 + nj * 8 + 2 * tq) =
-                        make_float2(O[nj][2 * h], O[nj][2 * h + 1]);
+                    *reinterpret_cast<float2 *>(p.o + ((size_t)bh * p.T + arow_of(t)) * p.DV + zb * 64 + nj * 8 +
+                                                2 * tq) = make_float2(O[nj][2 * h], O[nj][2 * h + 1]);
             }
         state_update(stage);
         __syncthreads();
@@ -532,10 +542,492 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
 #pragma unroll
         for (int mi = 0; mi < S_MT; ++mi)
 #pragma unroll
-            for (int nj = 0; nj < S_NT; ++nj)
+            for (int e = 0; e < 4; ++e) {
+                const int row = s_row(mi, e >> 1);
+                // reversed: the state before token 0 of the arrays, decayed by a_0
+                const float f = p.rev ? __expf(__ldg(Gb + row)) : 1.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    p.ST[((size_t)bh * DK + s_row(mi, e >> 1)) * p.DV + zb * 64 + s_col(nj, e)] = S[mi][nj][e];
+                for (int nj = 0; nj < S_NT; ++nj)
+                    p.ST[((size_t)bh * DK + row) * p.DV + zb * 64 + s_col(nj, e)] = f * S[mi][nj][e];
+            }
+    }
+}
+
+// ----------------------------------------------------------------- backward: decay on the output columns
+// The gradients of the queries and keys carry the decay of the output's own
+// column (key dimension i) rather than inside a contraction:
+//   dq_r[i] = sum_{s<=r} (do_r . v_s) k_s[i] 2^(c_r[i] - c_s[i]) + 2^(c_r[i]) (do_r S_prev^T)[i]
+// With Z~ = Z (.) 2^(c_m - c) and S' = diag(2^c_m) S this is
+//   OUT = 2^(c - c_m) (.) [ ((X Y^T) . M) Z~ + X S'^T ]
+//   S  <- diag(2^(c_L - c_m)) (S' + Z~^T Y)
+// in the roles  dQ: X = dO, Y = V, Z = K, S = the forward state from S0;
+//               dK (reversed traversal): X = V, Y = dO, Z = Q, S = the adjoint state from dST.
+// X Y^T takes exact bf16 inputs (one product); the masked scores and Z~ are
+// split into two bf16 parts (three products), S' too (two products with X).
+// A block owns 64 output columns (key dimensions zb*64..) and the state rows
+// of those dimensions, [64][DV]; warp w holds state rows 16w..16w+15.
+struct GlaBArgs {
+    const bf16 *x, *y, *z;  // x, y: [BH][T][DV]; z: [BH][T][DK]
+    const float *g;         // [BH][T][DK] natural-log decays
+    const float *S0;        // [BH][DK][DV] or NULL
+    float *out;             // [BH][T][DK]
+    const float *fs_dot;    // [BH][DK][DV] or NULL: each final state row dotted with its row here
+    float *fs_part;         // [BH][DK]
+    int rev;
+    int BH, DK, nzb, n_chunks, seg_chunks, n_seg;
+    long long T;
+    WsHeader *hdr;
+    unsigned int *flags;
+    float *alpha;  // [unit][64]
+    float4 *agg, *incl;
+};
+
+template <int DV>
+struct GlaBCfg {
+    static constexpr int XRB = DV * 2;  // bytes per row of X, Y tiles and of S' (bf16)
+    static constexpr int ZRB = 128;     // 64 key dimensions, bf16
+    static constexpr int GRB = 256;     // 64 key dimensions, fp32
+    static constexpr int X_BYTES = kGlaTc * XRB;
+    static constexpr int Z_BYTES = kGlaTc * ZRB;
+    static constexpr int G_BYTES = kGlaTc * GRB;
+    static constexpr int OFF_X = 0;
+    static constexpr int OFF_Y = X_BYTES;
+    static constexpr int OFF_Z = 2 * X_BYTES;
+    static constexpr int OFF_G = 2 * X_BYTES + Z_BYTES;
+    static constexpr int STAGE = 2 * X_BYTES + Z_BYTES + G_BYTES;
+    static constexpr int OFF_ZLO = 2 * STAGE;
+    static constexpr int OFF_SH = OFF_ZLO + Z_BYTES;  // S' rows (key dimensions) [64][DV], high part
+    static constexpr int OFF_SL = OFF_SH + 64 * XRB;
+    static constexpr int OFF_AS = OFF_SL + 64 * XRB;
+    static constexpr int SMEM = OFF_AS + 64 * 4;
+    static constexpr int S_NT = DV / 8;
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+template <int DV>
+__global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBArgs p) {
+    using C = GlaBCfg<DV>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ unsigned int s_ticket, s_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    if (tid == 0) s_ticket = atomicAdd(&p.hdr->ticket[0], 1u);
+    __syncthreads();
+    const unsigned int tk = s_ticket;
+    const int per_seg = p.BH * p.nzb;
+    const int seg = (int)(tk / per_seg);
+    const int bh = (int)(tk % per_seg) / p.nzb;
+    const int zb = (int)(tk % per_seg) % p.nzb;
+    const int c_begin = seg * p.seg_chunks;
+    const int c_end = min(c_begin + p.seg_chunks, p.n_chunks);
+    const int nc = c_end - c_begin;
+    const size_t unit = ((size_t)seg * p.BH + bh) * p.nzb + zb;
+
+    const bf16 *Xb = p.x + (size_t)bh * p.T * DV;
+    const bf16 *Yb = p.y + (size_t)bh * p.T * DV;
+    const bf16 *Zb = p.z + (size_t)bh * p.T * p.DK + zb * 64;
+    const float *Gb = p.g + (size_t)bh * p.T * p.DK + zb * 64;
+    float *alpha_s = reinterpret_cast<float *>(smem + C::OFF_AS);
+
+    auto arow_of = [&](long long t) { return p.rev ? p.T - 1 - t : t; };
+    auto load_stage = [&](int stage, int chunk, bool withX) {
+        uint8_t *st = smem + stage * C::STAGE;
+        const long long t0 = (long long)chunk * kGlaTc;
+        constexpr int XC = C::XRB / 16;
+        for (int i = tid; i < kGlaTc * XC; i += kGlaThreads) {
+            const int row = i / XC, c16 = i % XC;
+            const long long t = t0 + row;
+            const bool ok = t < p.T;
+            const size_t off = (size_t)(ok ? arow_of(t) : 0) * DV + c16 * 8;
+            cp_async16(smem_u32(st + C::OFF_Y + swz<C::XRB>(row, c16)), Yb + off, ok ? 16u : 0u);
+            if (withX) cp_async16(smem_u32(st + C::OFF_X + swz<C::XRB>(row, c16)), Xb + off, ok ? 16u : 0u);
+        }
+        for (int i = tid; i < kGlaTc * 8; i += kGlaThreads) {
+            const int row = i >> 3, c16 = i & 7;
+            const long long t = t0 + row;
+            const bool ok = t < p.T;
+            cp_async16(smem_u32(st + C::OFF_Z + swz<C::ZRB>(row, c16)),
+                       Zb + (size_t)(ok ? arow_of(t) : 0) * p.DK + c16 * 8, ok ? 16u : 0u);
+        }
+        for (int i = tid; i < kGlaTc * 16; i += kGlaThreads) {
+            const int row = i >> 4, c16 = i & 15;
+            const long long t = t0 + row;
+            const bool ok = t < p.T && !(p.rev && t == 0);
+            const long long ga = p.rev ? p.T - t : t;
+            cp_async16(smem_u32(st + C::OFF_G + row * C::GRB + c16 * 16), Gb + (size_t)(ok ? ga : 0) * p.DK + c16 * 4,
+                       ok ? 16u : 0u);
+        }
+    };
+    auto cumulate = [&](int stage) {
+        float *G = reinterpret_cast<float *>(smem + stage * C::STAGE + C::OFF_G);
+        float total = 0.f;
+        if (tid < 64) {
+            float run = 0.f, lo = 0.f, hi = 0.f;
+            bool finite = true;
+#pragma unroll 8
+            for (int t = 0; t < kGlaTc; ++t) {
+                const float l = G[t * 64 + tid];
+                finite = finite && isfinite(l);
+                run += l * kGlaLog2e;
+                G[t * 64 + tid] = run;
+                lo = fminf(lo, run);
+                hi = fmaxf(hi, run);
+            }
+            const float cm = G[kGlaMid * 64 + tid];
+            if (!finite || hi - cm > kGlaSpan || cm - lo > kGlaSpan || cm > kGlaSpan)
+                atomicOr(&p.hdr->error, kErrRange);
+            total = run;
+        }
+        return total;
+    };
+    // Z~ = Z 2^(c_m - c): high part over Z, low part in ZLO
+    auto scale_z = [&](int stage) {
+        uint8_t *st = smem + stage * C::STAGE;
+        const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
+        for (int i = tid; i < kGlaTc * 8; i += kGlaThreads) {
+            const int row = i >> 3, c16 = i & 7;
+            const float4 *crow = reinterpret_cast<const float4 *>(G + row * 64 + c16 * 8);
+            const float4 *cmid = reinterpret_cast<const float4 *>(G + kGlaMid * 64 + c16 * 8);
+            const float4 a = crow[0], b = crow[1], ma = cmid[0], mb = cmid[1];
+            const float d[8] = {ma.x - a.x, ma.y - a.y, ma.z - a.z, ma.w - a.w,
+                                mb.x - b.x, mb.y - b.y, mb.z - b.z, mb.w - b.w};
+            const uint32_t off = swz<C::ZRB>(row, c16);
+            const uint4 zv = *reinterpret_cast<const uint4 *>(st + C::OFF_Z + off);
+            const uint32_t w[4] = {zv.x, zv.y, zv.z, zv.w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = unpack_bf16(w[e]);
+                split_bf16x2(make_float2(x.x * ex2(d[2 * e]), x.y * ex2(d[2 * e + 1])), hi[e], lo[e]);
+            }
+            *reinterpret_cast<uint4 *>(st + C::OFF_Z + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(smem + C::OFF_ZLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+    };
+
+    constexpr int S_NT = C::S_NT;
+    float S[S_NT][4];
+    auto s_row = [&](int h) { return warp * 16 + g + h * 8; };  // local key dimension
+    auto s_col = [&](int nj, int e) { return nj * 8 + tq * 2 + (e & 1); };
+    auto scale_rows_by = [&](const float *G, int a_row, int b_row) {  // rows *= 2^(c[a_row] - c[b_row])
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = s_row(h);
+            const float f = ex2(G[a_row * 64 + r] - (b_row >= 0 ? G[b_row * 64 + r] : 0.f));
+#pragma unroll
+            for (int nj = 0; nj < S_NT; ++nj) {
+                S[nj][2 * h] *= f;
+                S[nj][2 * h + 1] *= f;
+            }
+        }
+    };
+    auto write_sb = [&]() {
+#pragma unroll
+        for (int nj = 0; nj < S_NT; ++nj)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = s_row(h), col = s_col(nj, 0);
+                const uint32_t off = swz<C::XRB>(row, col >> 3) + (col & 7) * 2;
+                uint32_t hi, lo;
+                split_bf16x2(make_float2(S[nj][2 * h], S[nj][2 * h + 1]), hi, lo);
+                *reinterpret_cast<uint32_t *>(smem + C::OFF_SH + off) = hi;
+                *reinterpret_cast<uint32_t *>(smem + C::OFF_SL + off) = lo;
+            }
+    };
+    // S' + Z~^T Y (Z~ in two parts), then rows scaled by 2^(c_L - c_m)
+    auto state_update = [&](int stage) {
+        const uint8_t *st = smem + stage * C::STAGE;
+#pragma unroll
+        for (int kt = 0; kt < kGlaTc / 16; ++kt) {
+            const int arow = kt * 16 + (lane & 7) + (lane >> 4) * 8;
+            const int ac16 = 2 * warp + ((lane >> 3) & 1);
+            uint32_t ah[4], al[4];
+            ldsm_x4_t(smem_u32(st + C::OFF_Z + swz<C::ZRB>(arow, ac16)), ah);
+            ldsm_x4_t(smem_u32(smem + C::OFF_ZLO + swz<C::ZRB>(arow, ac16)), al);
+#pragma unroll
+            for (int pp = 0; pp < S_NT / 2; ++pp) {
+                uint32_t b[4];
+                const int brow = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                ldsm_x4_t(smem_u32(st + C::OFF_Y + swz<C::XRB>(brow, 2 * pp + (lane >> 4))), b);
+                mma16816(S[2 * pp], ah, b[0], b[1]);
+                mma16816(S[2 * pp + 1], ah, b[2], b[3]);
+                mma16816(S[2 * pp], al, b[0], b[1]);
+                mma16816(S[2 * pp + 1], al, b[2], b[3]);
+            }
+        }
+        scale_rows_by(reinterpret_cast<const float *>(st + C::OFF_G), kGlaTc - 1, kGlaMid);
+    };
+
+    // ------------------------------------------------ phase 1
+#pragma unroll
+    for (int nj = 0; nj < S_NT; ++nj)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) S[nj][e] = 0.f;
+    float la_seg = 0.f;
+    load_stage(0, c_begin, false);
+    cp_async_commit();
+    if (nc > 1) load_stage(1, c_begin + 1, false);
+    cp_async_commit();
+    for (int i = 0; i < nc; ++i) {
+        const int stage = i & 1;
+        cp_async_wait<1>();
+        __syncthreads();
+        la_seg += cumulate(stage);
+        __syncthreads();
+        scale_z(stage);
+        scale_rows_by(reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G), kGlaMid, -1);
+        __syncthreads();
+        state_update(stage);
+        __syncthreads();
+        if (i + 2 < nc) load_stage(stage, c_begin + i + 2, false);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ------------------------------------------------ look-back
+    auto ws_index = [&](size_t u, int tile) { return u * (size_t)(S_NT * kGlaThreads) + (size_t)tile * kGlaThreads + tid; };
+    float Sin[S_NT][4];
+#pragma unroll
+    for (int nj = 0; nj < S_NT; ++nj)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) Sin[nj][e] = 0.f;
+    auto add_state0 = [&](float s0, float s1) {
+        if (p.S0 == nullptr) return;
+#pragma unroll
+        for (int nj = 0; nj < S_NT; ++nj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = zb * 64 + s_row(e >> 1);
+                Sin[nj][e] = fmaf((e >> 1) ? s1 : s0, __ldg(p.S0 + ((size_t)bh * p.DK + row) * DV + s_col(nj, e)),
+                                  Sin[nj][e]);
+            }
+    };
+    if (tid < 64) alpha_s[tid] = ex2(la_seg);
+    if (seg == 0) {
+        add_state0(1.f, 1.f);
+    } else {
+#pragma unroll
+        for (int nj = 0; nj < S_NT; ++nj)
+            __stcg(p.agg + ws_index(unit, nj), make_float4(S[nj][0], S[nj][1], S[nj][2], S[nj][3]));
+        if (tid < 64) __stcg(p.alpha + unit * 64 + tid, ex2(la_seg));
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release(p.flags + unit, 1u);
+        float acc0 = 1.f, acc1 = 1.f;
+        int j = seg - 1;
+        while (true) {
+            const size_t up = ((size_t)j * p.BH + bh) * p.nzb + zb;
+            if (tid == 0) s_flag = wait_flag(p.flags + up, p.hdr, 61u);
+            __syncthreads();
+            const unsigned int f = s_flag;
+            __syncthreads();
+            if (f != 1u && f != 2u) break;
+            const float4 *src = (f == 2u) ? p.incl : p.agg;
+#pragma unroll
+            for (int nj = 0; nj < S_NT; ++nj) {
+                const float4 v = ld_cg4(src + ws_index(up, nj));
+                Sin[nj][0] = fmaf(acc0, v.x, Sin[nj][0]);
+                Sin[nj][1] = fmaf(acc0, v.y, Sin[nj][1]);
+                Sin[nj][2] = fmaf(acc1, v.z, Sin[nj][2]);
+                Sin[nj][3] = fmaf(acc1, v.w, Sin[nj][3]);
+            }
+            if (f == 2u) break;
+            acc0 *= ld_cg(p.alpha + up * 64 + s_row(0));
+            acc1 *= ld_cg(p.alpha + up * 64 + s_row(1));
+            if (--j < 0) {
+                add_state0(acc0, acc1);
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    if (seg != p.n_seg - 1) {
+        const float a0 = alpha_s[s_row(0)], a1 = alpha_s[s_row(1)];
+#pragma unroll
+        for (int nj = 0; nj < S_NT; ++nj)
+            __stcg(p.incl + ws_index(unit, nj),
+                   make_float4(fmaf(a0, Sin[nj][0], S[nj][0]), fmaf(a0, Sin[nj][1], S[nj][1]),
+                               fmaf(a1, Sin[nj][2], S[nj][2]), fmaf(a1, Sin[nj][3], S[nj][3])));
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release(p.flags + unit, 2u);
+    }
+
+    // ------------------------------------------------ phase 2
+#pragma unroll
+    for (int nj = 0; nj < S_NT; ++nj)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) S[nj][e] = Sin[nj][e];
+    load_stage(0, c_begin, true);
+    cp_async_commit();
+    if (nc > 1) load_stage(1, c_begin + 1, true);
+    cp_async_commit();
+    for (int i = 0; i < nc; ++i) {
+        const int stage = i & 1;
+        const uint8_t *st = smem + stage * C::STAGE;
+        const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
+        const long long t0 = (long long)(c_begin + i) * kGlaTc;
+        cp_async_wait<1>();
+        __syncthreads();
+        cumulate(stage);
+        __syncthreads();
+        scale_z(stage);
+        scale_rows_by(G, kGlaMid, -1);
+        write_sb();
+        __syncthreads();
+
+        // D = X Y^T for this warp's 16 rows (exact bf16 inputs: one product)
+        float D[8][4];
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) D[nj][e] = 0.f;
+        const int arow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll 2
+        for (int kk = 0; kk < DV / 16; ++kk) {
+            uint32_t a[4];
+            ldsm_x4(smem_u32(st + C::OFF_X + swz<C::XRB>(arow, 2 * kk + (lane >> 4))), a);
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                uint32_t b[4];
+                const int brow = 16 * pp + (lane & 7) + (lane >> 4) * 8;
+                ldsm_x4(smem_u32(st + C::OFF_Y + swz<C::XRB>(brow, 2 * kk + ((lane >> 3) & 1))), b);
+                mma16816(D[2 * pp], a, b[0], b[1]);
+                mma16816(D[2 * pp + 1], a, b[2], b[3]);
+            }
+        }
+        uint32_t dh[4][4], dl[4][4];
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = warp * 16 + g + 8 * h, s = nj * 8 + 2 * tq;
+                const float x0 = (s <= r) ? D[nj][2 * h] : 0.f;
+                const float x1 = (s + 1 <= r) ? D[nj][2 * h + 1] : 0.f;
+                split_bf16x2(make_float2(x0, x1), dh[nj >> 1][(nj & 1) * 2 + h], dl[nj >> 1][(nj & 1) * 2 + h]);
+            }
+        float O[8][4];
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) O[nj][e] = 0.f;
+        // (D . M) Z~ (three products) ...
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                const int brow = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const uint32_t boff = swz<C::ZRB>(brow, 2 * pp + (lane >> 4));
+                uint32_t zh[4], zl[4];
+                ldsm_x4_t(smem_u32(st + C::OFF_Z + boff), zh);
+                ldsm_x4_t(smem_u32(smem + C::OFF_ZLO + boff), zl);
+                mma16816(O[2 * pp], dh[kt], zh[0], zh[1]);
+                mma16816(O[2 * pp + 1], dh[kt], zh[2], zh[3]);
+                mma16816(O[2 * pp], dh[kt], zl[0], zl[1]);
+                mma16816(O[2 * pp + 1], dh[kt], zl[2], zl[3]);
+                mma16816(O[2 * pp], dl[kt], zh[0], zh[1]);
+                mma16816(O[2 * pp + 1], dl[kt], zh[2], zh[3]);
+            }
+        }
+        // ... + X S'^T (two products: S' in two parts)
+#pragma unroll 2
+        for (int kk = 0; kk < DV / 16; ++kk) {
+            uint32_t a[4];
+            ldsm_x4(smem_u32(st + C::OFF_X + swz<C::XRB>(arow, 2 * kk + (lane >> 4))), a);
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                const int brow = 16 * pp + (lane & 7) + (lane >> 4) * 8;
+                const uint32_t boff = swz<C::XRB>(brow, 2 * kk + ((lane >> 3) & 1));
+                uint32_t sh[4], sl[4];
+                ldsm_x4(smem_u32(smem + C::OFF_SH + boff), sh);
+                ldsm_x4(smem_u32(smem + C::OFF_SL + boff), sl);
+                mma16816(O[2 * pp], a, sh[0], sh[1]);
+                mma16816(O[2 * pp + 1], a, sh[2], sh[3]);
+                mma16816(O[2 * pp], a, sl[0], sl[1]);
+                mma16816(O[2 * pp + 1], a, sl[2], sl[3]);
+            }
+        }
+        // OUT = 2^(c_r - c_m) per (row, key dimension)
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = warp * 16 + g + 8 * h, col = nj * 8 + 2 * tq;
+                const long long t = t0 + r;
+                if (t < p.T) {
+                    const float2 cr = *reinterpret_cast<const float2 *>(G + r * 64 + col);
+                    const float2 cm = *reinterpret_cast<const float2 *>(G + kGlaMid * 64 + col);
+                    *reinterpret_cast<float2 *>(p.out + ((size_t)bh * p.T + arow_of(t)) * p.DK + zb * 64 + col) =
+                        make_float2(O[nj][2 * h] * ex2(cr.x - cm.x), O[nj][2 * h + 1] * ex2(cr.y - cm.y));
+                }
+            }
+        state_update(stage);
+        __syncthreads();
+        if (i + 2 < nc) load_stage(stage, c_begin + i + 2, true);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+
+    // the final state's rows dotted with fs_dot (the decay gradient's final-state term)
+    if (seg == p.n_seg - 1 && p.fs_part != nullptr) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = zb * 64 + s_row(h);
+            float acc = 0.f;
+            if (p.fs_dot != nullptr) {
+#pragma unroll
+                for (int nj = 0; nj < S_NT; ++nj)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        acc = fmaf(S[nj][2 * h + e], __ldg(p.fs_dot + ((size_t)bh * p.DK + row) * DV + s_col(nj, e)), acc);
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if (tq == 0) p.fs_part[(size_t)bh * p.DK + row] = acc;
+        }
+    }
+}
+
+// ----------------------------------------------------------------- backward: decay gradient
+// Closed form per key dimension ("The backward pass of linear attention",
+// Yang et al.'s form for gated linear attention):
+//   dlog a_u[i] = sum_{t>=u} (q_t[i] dq_t[i] - k_t[i] dk_t[i]) + fs[i],
+// fs[i] = sum_j dST[i][j] S_T[i][j].  A reverse scan over tiles of
+// kGlaDlTile tokens: per-tile column sums first, then each tile's suffix sums
+// plus every later tile and fs.  Thread = key dimension; fixed summation order.
+constexpr int kGlaDlTile = 256;
+
+__global__ void gla_dlog_tile_sums_kernel(const bf16 *__restrict__ q, const float *__restrict__ dq,
+                                          const bf16 *__restrict__ k, const float *__restrict__ dk,
+                                          float *__restrict__ tsum, int DK, long long T, int n_tiles) {
+    const int tile = (int)(blockIdx.x % (unsigned)n_tiles);
+    const size_t bh = blockIdx.x / (unsigned)n_tiles;
+    const int i = threadIdx.x;
+    const long long t0 = (long long)tile * kGlaDlTile;
+    const long long t1 = min(t0 + kGlaDlTile, T);
+    float acc = 0.f;
+    for (long long t = t0; t < t1; ++t) {
+        const size_t x = (bh * T + t) * DK + i;
+        acc += __bfloat162float(q[x]) * dq[x] - __bfloat162float(k[x]) * dk[x];
+    }
+    tsum[(bh * n_tiles + tile) * DK + i] = acc;
+}
+
+__global__ void gla_dlog_finalize_kernel(const bf16 *__restrict__ q, const float *__restrict__ dq,
+                                         const bf16 *__restrict__ k, const float *__restrict__ dk,
+                                         const float *__restrict__ tsum, const float *__restrict__ fs,
+                                         float *__restrict__ dlog, int DK, long long T, int n_tiles) {
+    const int tile = (int)(blockIdx.x % (unsigned)n_tiles);
+    const size_t bh = blockIdx.x / (unsigned)n_tiles;
+    const int i = threadIdx.x;
+    float run = fs ? fs[bh * DK + i] : 0.f;
+    for (int j = n_tiles - 1; j > tile; --j) run += tsum[(bh * n_tiles + j) * DK + i];
+    const long long t0 = (long long)tile * kGlaDlTile;
+    for (long long t = min(t0 + kGlaDlTile, T) - 1; t >= t0; --t) {
+        const size_t x = (bh * T + t) * DK + i;
+        run += __bfloat162float(q[x]) * dq[x] - __bfloat162float(k[x]) * dk[x];
+        dlog[x] = run;
     }
 }
 
@@ -581,6 +1073,63 @@ bool gla_sizes_fit(int64_t B, int64_t H, int64_t T) {
 bool gla_supported(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chunk) {
     return B >= 0 && H >= 0 && T >= 0 && (dk == 64 || dk == 128) && dv > 0 && dv % 64 == 0 && dv <= 1024 &&
            chunk == kGlaTc && gla_sizes_fit(B, H, T);
+}
+
+// Segments for a traversal with nzb column blocks per head (the forward's rule).
+void gla_segments(int64_t BH, int n_chunks, int nzb, int &seg_chunks, int &n_seg) {
+    seg_chunks = kGlaSegChoices[3];
+    for (int c : kGlaSegChoices) {
+        if ((long long)((n_chunks + c - 1) / c) * BH * nzb >= kGlaMinBlocks) {
+            seg_chunks = c;
+            break;
+        }
+    }
+    n_seg = (n_chunks + seg_chunks - 1) / seg_chunks;
+    if (n_seg < 1) n_seg = 1;
+}
+
+// Backward workspace: the look-back arrays of the largest traversal (reused by the three in
+// turn), the final-state term per key dimension and the decay gradient's tile sums.
+struct GlaBwdPlan {
+    int n_chunks, segA, nsegA, segB, nsegB, tiles;
+    size_t off_flags, off_alpha, off_agg, off_incl, off_fs, off_tsum, total;
+};
+
+GlaBwdPlan gla_bwd_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv) {
+    GlaBwdPlan p;
+    const int64_t BH = B * H;
+    p.n_chunks = (int)((T + kGlaTc - 1) / kGlaTc);
+    gla_segments(BH, p.n_chunks, (int)(dv / 64), p.segA, p.nsegA);
+    gla_segments(BH, p.n_chunks, (int)(dk / 64), p.segB, p.nsegB);
+    const size_t unitsA = (size_t)p.nsegA * BH * (dv / 64), unitsB = (size_t)p.nsegB * BH * (dk / 64);
+    const size_t units = unitsA > unitsB ? unitsA : unitsB;
+    const size_t alpha_floats = unitsA * dk > unitsB * 64 ? unitsA * dk : unitsB * 64;
+    const size_t state_floats = unitsA * dk * 64 > unitsB * 64 * dv ? unitsA * dk * 64 : unitsB * 64 * dv;
+    p.tiles = (int)((T + kGlaDlTile - 1) / kGlaDlTile);
+    if (p.tiles < 1) p.tiles = 1;
+    p.off_flags = sizeof(WsHeader);
+    p.off_alpha = align_up(p.off_flags + units * 4, 256);
+    p.off_agg = align_up(p.off_alpha + alpha_floats * 4, 256);
+    p.off_incl = align_up(p.off_agg + state_floats * 4, 256);
+    p.off_fs = align_up(p.off_incl + state_floats * 4, 256);
+    p.off_tsum = align_up(p.off_fs + (size_t)BH * dk * 4, 256);
+    p.total = align_up(p.off_tsum + (size_t)BH * p.tiles * dk * 4, 256);
+    return p;
+}
+
+bool gla_bwd_supported(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chunk) {
+    return B >= 0 && H >= 0 && T >= 0 && (dk == 64 || dk == 128) && (dv == 64 || dv == 128) && chunk == kGlaTc &&
+           gla_sizes_fit(B, H, T) && product_below({B, H, (T + kGlaDlTile - 1) / kGlaDlTile}, 2147483648.0);
+}
+
+template <int DV>
+int launch_gla_bwd_qk(const GlaBArgs &a, cudaStream_t s, unsigned int grid) {
+    using C = GlaBCfg<DV>;
+    static std::atomic<unsigned long long> smem_set{0};
+    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_bwd_qk_kernel<DV>), C::SMEM);
+    if (st) return st;
+    gla_bwd_qk_kernel<DV><<<grid, kGlaThreads, C::SMEM, s>>>(a);
+    return check_launch("gla_bwd_qk_kernel");
 }
 
 template <int DK>
@@ -643,6 +1192,7 @@ extern "C" int cla_gla_fwd(const uint16_t *q, const uint16_t *k, const uint16_t 
     a.S0 = S0;
     a.o = o;
     a.ST = ST;
+    a.rev = 0;
     a.BH = (int)BH;
     a.DV = (int)dim_v;
     a.nzb = pl.nzb;
@@ -657,4 +1207,132 @@ extern "C" int cla_gla_fwd(const uint16_t *q, const uint16_t *k, const uint16_t 
     a.incl = reinterpret_cast<float4 *>(w + pl.off_incl);
     const unsigned int grid = (unsigned int)(pl.units);
     return dim_k == 64 ? launch_gla_fwd<64>(a, s, grid) : launch_gla_fwd<128>(a, s, grid);
+}
+
+extern "C" size_t cla_gla_bwd_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
+                                             int chunk) {
+    if (!gla_bwd_supported(B, H, T, dim_k, dim_v, chunk)) return 0;
+    return gla_bwd_plan(B, H, T, dim_k, dim_v).total;
+}
+
+extern "C" int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                           const float *S0, const uint16_t *dO, const float *dST, float *dq, float *dk, float *dv,
+                           float *dlog_decay, float *dS0, int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                           int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
+    clear_error();
+    const char *fn = "cla_gla_bwd";
+    if (B < 0 || H < 0 || T < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (!gla_bwd_supported(B, H, T, dim_k, dim_v, chunk))
+        return fail(CLA_ERR_UNSUPPORTED, "%s: needs dim_k and dim_v 64 or 128, chunk 64 and sizes within one launch "
+                    "(got dim_k %lld, dim_v %lld, chunk %d)", fn, (long long)dim_k, (long long)dim_v, chunk);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t BH = B * H;
+    if (BH == 0) return CLA_OK;
+    const size_t sbytes = sizeof(float) * BH * dim_k * dim_v;
+    if (T == 0) {
+        if (dS0) {
+            if (dST) CLA_CUDA_TRY(cudaMemcpyAsync(dS0, dST, sbytes, cudaMemcpyDeviceToDevice, s), fn);
+            else CLA_CUDA_TRY(cudaMemsetAsync(dS0, 0, sbytes, s), fn);
+        }
+        return CLA_OK;
+    }
+    if (!q || !k || !v || !log_decay || !dO || !dq || !dk || !dv)
+        return fail(CLA_ERR_INVALID_ARG, "%s: q, k, v, log_decay, dO, dq, dk, dv required", fn);
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(log_decay))
+        return fail(CLA_ERR_INVALID_ARG, "%s: q, k, v, dO, log_decay must be 16-byte aligned", fn);
+    if (!aligned_or_null({dq, dk, dv}, 8) || !aligned_or_null({S0, dST, dlog_decay, dS0}, 4))
+        return fail(CLA_ERR_INVALID_ARG, "%s: dq, dk, dv must be 8-byte aligned, S0, dST, dlog_decay, dS0 4-byte", fn);
+    if (!ws || !aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace NULL or unaligned", fn);
+    const GlaBwdPlan pl = gla_bwd_plan(B, H, T, dim_k, dim_v);
+    if (ws_bytes < pl.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, pl.total);
+    char *w = static_cast<char *>(ws);
+    float *fs = reinterpret_cast<float *>(w + pl.off_fs);
+    const bf16 *Q = reinterpret_cast<const bf16 *>(q), *K = reinterpret_cast<const bf16 *>(k);
+    const bf16 *V = reinterpret_cast<const bf16 *>(v), *DO = reinterpret_cast<const bf16 *>(dO);
+
+    auto args_b = [&](int rev) {
+        GlaBArgs b;
+        memset(&b, 0, sizeof(b));
+        b.g = log_decay;
+        b.S0 = dST;
+        b.rev = rev;
+        b.BH = (int)BH;
+        b.DK = (int)dim_k;
+        b.nzb = (int)(dim_k / 64);
+        b.n_chunks = pl.n_chunks;
+        b.seg_chunks = pl.segB;
+        b.n_seg = pl.nsegB;
+        b.T = T;
+        b.hdr = reinterpret_cast<WsHeader *>(w);
+        b.flags = reinterpret_cast<unsigned int *>(w + pl.off_flags);
+        b.alpha = reinterpret_cast<float *>(w + pl.off_alpha);
+        b.agg = reinterpret_cast<float4 *>(w + pl.off_agg);
+        b.incl = reinterpret_cast<float4 *>(w + pl.off_incl);
+        return b;
+    };
+    const unsigned int gridB = (unsigned int)((size_t)pl.nsegB * BH * (dim_k / 64));
+    int st;
+    // dQ: forward traversal, X = dO, Y = V, Z = K, the state from S0; its final state dotted
+    // with dST gives the decay gradient's final-state term
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, pl.off_alpha, s), fn);
+    GlaBArgs b = args_b(0);
+    b.x = DO;
+    b.y = V;
+    b.z = K;
+    b.S0 = S0;
+    b.out = dq;
+    b.fs_dot = dST;
+    b.fs_part = fs;
+    st = dim_v == 64 ? launch_gla_bwd_qk<64>(b, s, gridB) : launch_gla_bwd_qk<128>(b, s, gridB);
+    if (st) return st;
+
+    // dV and dS0: the forward kernel on the reversed adjoint (q <- k, k <- q, v <- dO, S0 <- dST)
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, pl.off_alpha, s), fn);
+    GlaArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = K;
+    a.k = Q;
+    a.v = DO;
+    a.g = log_decay;
+    a.S0 = dST;
+    a.o = dv;
+    a.ST = dS0;
+    a.rev = 1;
+    a.BH = (int)BH;
+    a.DV = (int)dim_v;
+    a.nzb = (int)(dim_v / 64);
+    a.n_chunks = pl.n_chunks;
+    a.seg_chunks = pl.segA;
+    a.n_seg = pl.nsegA;
+    a.T = T;
+    a.hdr = reinterpret_cast<WsHeader *>(w);
+    a.flags = reinterpret_cast<unsigned int *>(w + pl.off_flags);
+    a.alpha = reinterpret_cast<float *>(w + pl.off_alpha);
+    a.agg = reinterpret_cast<float4 *>(w + pl.off_agg);
+    a.incl = reinterpret_cast<float4 *>(w + pl.off_incl);
+    const unsigned int gridA = (unsigned int)((size_t)pl.nsegA * BH * (dim_v / 64));
+    st = dim_k == 64 ? launch_gla_fwd<64>(a, s, gridA) : launch_gla_fwd<128>(a, s, gridA);
+    if (st) return st;
+
+    // dK: reversed traversal, X = V, Y = dO, Z = Q, the adjoint state from dST
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, pl.off_alpha, s), fn);
+    b = args_b(1);
+    b.x = V;
+    b.y = DO;
+    b.z = Q;
+    b.out = dk;
+    st = dim_v == 64 ? launch_gla_bwd_qk<64>(b, s, gridB) : launch_gla_bwd_qk<128>(b, s, gridB);
+    if (st) return st;
+
+    if (dlog_decay) {
+        float *tsum = reinterpret_cast<float *>(w + pl.off_tsum);
+        const unsigned int grid = (unsigned int)((size_t)pl.tiles * BH);
+        gla_dlog_tile_sums_kernel<<<grid, (unsigned int)dim_k, 0, s>>>(Q, dq, K, dk, tsum, (int)dim_k, T, pl.tiles);
+        st = check_launch("gla_dlog_tile_sums_kernel");
+        if (st) return st;
+        gla_dlog_finalize_kernel<<<grid, (unsigned int)dim_k, 0, s>>>(Q, dq, K, dk, tsum, fs, dlog_decay, (int)dim_k, T,
+                                                                      pl.tiles);
+        st = check_launch("gla_dlog_finalize_kernel");
+    }
+    return st;
 }

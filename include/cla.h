@@ -357,6 +357,37 @@ int cla_gla_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                 int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
                 int chunk, void *ws, size_t ws_bytes, void *stream);
 
+/* Bytes of workspace for cla_gla_bwd; 0 for sizes, head dims or chunks that
+ * call refuses. */
+size_t cla_gla_bwd_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                                  int64_t dim_v, int chunk);
+
+/* Backward of cla_gla_fwd ("Parallel Scan", "The backward pass of linear
+ * attention", with the scalar decay replaced by the diagonal one, and the
+ * closed-form decay gradient per key dimension of Yang et al. that the
+ * section cites):
+ *   dQ  a forward-order traversal that rebuilds the states from S0;
+ *   dV, dS0  the forward kernel run on the reversed adjoint recursion
+ *       Sbar_t = q_t^T dO_t + diag(a_{t+1}) Sbar_{t+1} (from dST);
+ *   dK  a reverse-order traversal carrying the adjoint state;
+ *   dlog_decay_u[i] = sum_{t>=u} (q_t[i] dq_t[i] - k_t[i] dk_t[i])
+ *                     + sum_j dST[i][j] S_T[i][j]
+ * (no per-token states).  The decay of the query and key gradients sits on
+ * their own column, dq_r[i] = 2^(c_r - c_m)[i] (((dO V^T) . M) K~ + dO S'^T)
+ * [r][i], with the same midpoint factoring as the forward.
+ *   dO          [B, H, T, dim_v] bf16   upstream gradient on o
+ *   dST         [B, H, dim_k, dim_v] fp32 [opt] upstream gradient on S_T
+ *   dq, dk      [B, H, T, dim_k] fp32 out;  dv [B, H, T, dim_v] fp32 out
+ *   dlog_decay  [B, H, T, dim_k] fp32 [opt] out;  dS0 [B, H, dim_k, dim_v] fp32 [opt] out
+ * Supported: dim_k and dim_v 64 or 128, chunk 64; the forward's decay range
+ * (reported the same way through cla_check_status). */
+int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                const float *log_decay, const float *S0, const uint16_t *dO,
+                const float *dST, float *dq, float *dk, float *dv,
+                float *dlog_decay, float *dS0, int64_t B, int64_t H, int64_t T,
+                int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes,
+                void *stream);
+
 #ifdef __cplusplus
 }
 #endif

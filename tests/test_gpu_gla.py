@@ -1,7 +1,7 @@
-"""Gated linear attention forward (one decay per key dimension): GPU (through
-the C ABI) vs the oracle's per-token recurrence, with the bf16 tolerance (per
-output tensor, |x - r| / rms(r): max <= 2e-2, mean <= 5e-3), and the kernel's
-range check on decays it cannot factor."""
+"""Gated linear attention forward and backward (one decay per key dimension):
+GPU (through the C ABI) vs the oracle's per-token recurrence and its adjoint,
+with the bf16 tolerance (per output tensor, |x - r| / rms(r): max <= 2e-2,
+mean <= 5e-3), and the kernels' range check on decays they cannot factor."""
 import numpy as np
 import pytest
 import torch
@@ -27,7 +27,7 @@ def _dev(x):
     return None if x is None else x.cuda()
 
 
-def _run(cla, inp, heads=None):
+def _run(cla, inp, heads=None, bwd=False, dST=None):
     t = {k: _dev(v) for k, v in inp.items()}
     ws = torch.empty(max(cla.gla_workspace_size(*t["q"].shape, t["v"].shape[-1], 64), 256), dtype=torch.uint8,
                      device="cuda")
@@ -38,6 +38,15 @@ def _run(cla, inp, heads=None):
     ro, rST = oracle.gla_fwd(ci["q"], ci["k"], ci["v"], ci["log_a"], ci["S0"])
     assert_bf16("o", sel(o), ro)
     assert_bf16("S_T", sel(ST), rST)
+    if not bwd:
+        return
+    wb = torch.empty(max(cla.gla_bwd_workspace_size(*t["q"].shape, t["v"].shape[-1], 64), 256), dtype=torch.uint8,
+                     device="cuda")
+    g = cla.gla_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"], _dev(dST), workspace=wb)
+    cla.check_status(wb)
+    ref = oracle.gla_bwd(ci["q"], ci["k"], ci["v"], ci["log_a"], ci["S0"], ci["dO"], sel(dST))
+    for name, x, r in zip(("dq", "dk", "dv", "dlog_a", "dS0"), map(sel, g), ref):
+        assert_bf16(name, x, r)
 
 
 @pytest.mark.parametrize("B,H,T,dk,dv", [
@@ -95,3 +104,37 @@ def test_gla_workload_full_sampled_heads(cla):
     the batch (the heads are independent problems)."""
     inp = workloads.make("gla")
     _run(cla, inp, heads=[0, 7, 15])
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv", [
+    (1, 2, 64, 64, 64), (1, 2, 300, 64, 64), (2, 1, 1, 64, 64), (1, 1, 1000, 128, 128),
+    (1, 2, 700, 128, 64), (1, 1, 777, 64, 128), (2, 2, 2000, 128, 128),
+])
+@pytest.mark.parametrize("with_state", [False, True])
+def test_gla_bwd_small(cla, B, H, T, dk, dv, with_state):
+    inp = workloads.make("gla", B=B, H=H, T=T, dk=dk, dv=dv)
+    dST = None
+    if not with_state:
+        inp["S0"] = None
+    else:
+        rng = np.random.default_rng(T + dk + dv)
+        dST = torch.from_numpy(rng.normal(0, 0.1, (B, H, dk, dv)).astype(np.float32))
+    _run(cla, inp, bwd=True, dST=dST)
+
+
+def test_gla_bwd_strong_decay_within_range(cla):
+    """Backward with gates down to e^-2.5 per token in some dimensions (the decay gradient's
+    suffix sums then cancel strongly) and near 1 in others."""
+    inp = workloads.make("gla", B=1, H=2, T=900, dk=64, dv=64)
+    la = inp["log_a"].clone()
+    la[:, :, :, ::3] = -2.5
+    la[:, :, :, 1::7] = -1e-4
+    inp["log_a"] = la
+    dST = torch.from_numpy(np.random.default_rng(1).normal(0, 0.1, (1, 2, 64, 64)).astype(np.float32))
+    _run(cla, inp, bwd=True, dST=dST)
+
+
+def test_gla_bwd_workload_full_sampled_heads(cla):
+    """The full gla workload, backward, every output of two heads."""
+    inp = workloads.make("gla")
+    _run(cla, inp, heads=[3, 12], bwd=True)
