@@ -68,6 +68,8 @@ def lib():
                 "cla_gla_fwd": ([P] * 7 + [I64] * 5 + [INT, P, SZ, P], INT),
                 "cla_gla_bwd_workspace_size": ([I64] * 5 + [INT], SZ),
                 "cla_gla_bwd": ([P] * 12 + [I64] * 5 + [INT, P, SZ, P], INT),
+                "cla_decay_total": ([P, P, I64, I64, I64, P], INT),
+                "cla_state_compose": ([P] * 4 + [I64] * 7 + [P], INT),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -431,3 +433,35 @@ def gla_bwd(q, k, v, log_decay, S0, dO, dST=None, *, chunk=64, dq=None, dk=None,
         _T(dlog_decay, f32, "dlog_decay", tk), _T(dS0, f32, "dS0", st),
         B, H, T, dkk, dvv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws)), stream)
     return dq, dk, dv, dlog_decay, dS0
+
+
+# ---------------------------------------------------------------- state passing between slices
+def decay_total(log_decay, *, alpha=None, stream=None):
+    """exp of the sum over the slice of log_decay: [B, H, T] -> [B, H] (one decay per head) or
+    [B, H, T, dk] -> [B, H, dk] (gated)."""
+    if log_decay.dim() == 3:
+        B, H, T = log_decay.shape
+        A, shape = 1, (B, H)
+    else:
+        B, H, T, A = _dims(log_decay, 4, "log_decay")
+        shape = (B, H, A)
+    dev = log_decay.device
+    alpha = _out(alpha, shape, torch.float32, dev)
+    _launch("cla_decay_total", dev, (_T(log_decay, torch.float32, "log_decay", tuple(log_decay.shape)),
+                                     _T(alpha, torch.float32, "alpha", shape), B * H, T, A), stream)
+    return alpha
+
+
+def state_compose(alphas, dSs, edge, first, count, step, *, out=None, stream=None):
+    """Fold acc <- diag(alpha_j) acc + dS_j over j = first + c * step (c < count) from edge.
+    alphas [P, B, H] or [P, B, H, dk]; dSs [P, B, H, dk, dv]; edge [B, H, dk, dv] or None."""
+    P, B, H, dk, dv = _dims(dSs, 5, "dSs")
+    A = 1 if alphas.dim() == 3 else alphas.shape[3]
+    dev = dSs.device
+    out = _out(out, (B, H, dk, dv), torch.float32, dev)
+    st = (B, H, dk, dv)
+    _launch("cla_state_compose", dev, (
+        _T(alphas, torch.float32, "alphas", (P, B, H) if A == 1 else (P, B, H, A)),
+        _T(dSs, torch.float32, "dSs", (P, B, H, dk, dv)), _T(edge, torch.float32, "edge", st),
+        _T(out, torch.float32, "out", st), P, B * H, dk * dv, A, int(first), int(count), int(step)), stream)
+    return out

@@ -388,6 +388,36 @@ int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                 int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes,
                 void *stream);
 
+/* ======================================================================== */
+/* State passing between slices of one sequence                             */
+/* ======================================================================== */
+
+/* Total decay of a slice ("Parallel Scan", "Splitting one sequence across
+ * devices": each device's pair holds its slice's product of decays):
+ *   alpha[bh][a] = exp(sum_t log_decay[bh][t][a])
+ *   log_decay  [BH, T, A] fp32 (A = 1: one decay per head, as chunk_la's
+ *              [B, H, T]; A = dim_k: gated decays, as gla's [B, H, T, dim_k])
+ *   alpha      [BH, A] fp32 out (0 where the slice holds a reset). */
+int cla_decay_total(const float *log_decay, float *alpha, int64_t BH, int64_t T,
+                    int64_t A, void *stream);
+
+/* The state entering a slice, from the pairs (alpha_j, dS_j) of the slices
+ * before it (same section; the combine (a1, b1) . (a2, b2) = (a1 a2,
+ * a2 b1 + b2) of "The scan for one number of state"):
+ *   out = fold over c = 0..count-1, j = first + c * step, of
+ *         acc <- diag(alpha_j) acc + dS_j,  from acc = edge (0 if NULL).
+ *   alpha  [P, BH, A] fp32: A = 1 scales a head's whole state, A > 1 scales
+ *          state row r by alpha[.][.][r / (n / A)] (one decay per key row)
+ *   dS     [P, BH, n] fp32 (n = dim_k * dim_v state entries, rows first)
+ *   edge   [BH, n] fp32 [opt]: the initial state (forward) or the upstream
+ *          gradient of the final state (backward, composed from the right
+ *          with step = -1)
+ *   out    [BH, n] fp32 out
+ * n must be a multiple of A; pair indices must lie in [0, P). */
+int cla_state_compose(const float *alpha, const float *dS, const float *edge,
+                      float *out, int64_t P, int64_t BH, int64_t n, int64_t A,
+                      int64_t first, int64_t count, int64_t step, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,6 +18,9 @@ Each function states the passage it follows in the C source; the summary:
   backward pass of linear attention"; "Lightning Attention-2", eqs. 4, 11-12).
 * ``la_dlog_closed_form`` -- the closed-form decay gradient of "The backward
   pass of linear attention".
+* ``decay_total`` / ``state_compose`` -- state passing between slices of one
+  sequence ("Parallel Scan", "Splitting one sequence across devices"): a
+  slice's total decay, and the fold of slice pairs under the combine.
 * ``gla_fwd`` / ``gla_bwd`` / ``gla_dlog_closed_form`` -- gated linear
   attention, one decay per key dimension ("Parallel Scan", "What one combine
   costs" and "The chunkwise algorithm": S_t = G_t (.) S_{t-1} + k_t^T v_t), its
@@ -73,10 +76,12 @@ def _load():
             lib.oracle_gla_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I]
             lib.oracle_gla_bwd.argtypes = [P] * 12 + [I, I, I, I, I]
             lib.oracle_gla_dlog_closed_form.argtypes = [P] * 7 + [I, I, I, I, I]
+            lib.oracle_decay_total.argtypes = [P, P, I, I, I]
+            lib.oracle_state_compose.argtypes = [P, P, P, P] + [I] * 7
             for fn in ("oracle_scan_diag_fwd", "oracle_scan_diag_bwd", "oracle_selective_fwd",
                        "oracle_selective_bwd", "oracle_la_fwd", "oracle_la_bwd",
                        "oracle_la_dlog_closed_form", "oracle_gla_fwd", "oracle_gla_bwd",
-                       "oracle_gla_dlog_closed_form"):
+                       "oracle_gla_dlog_closed_form", "oracle_decay_total", "oracle_state_compose"):
                 getattr(lib, fn).restype = None
             _lib = lib
     return _lib
@@ -222,4 +227,25 @@ def gla_dlog_closed_form(q, k, dq, dk, dST=None, ST=None):
     out = np.empty((B, H, T, dkk))
     _load().oracle_gla_dlog_closed_form(_p(q), _p(k), _p(dq), _p(dk), _p(dST), _p(ST), _p(out),
                                         B, H, T, dkk, dv)
+    return out
+
+
+def decay_total(log_decay):
+    """alpha = exp(sum over axis -2 of log_decay) for log_decay [BH..., T, A] given as
+    [BH, T, A] (A = 1 for one decay per head); returns [BH, A]."""
+    ld = _f64(log_decay)
+    BH, T, A = ld.shape
+    out = np.empty((BH, A))
+    _load().oracle_decay_total(_p(ld), _p(out), BH, T, A)
+    return out
+
+
+def state_compose(alpha, dS, edge, first, count, step):
+    """Fold of pairs j = first + c * step (c < count): acc <- alpha_j acc + dS_j from acc = edge.
+    alpha [P, BH, A], dS [P, BH, n], edge [BH, n] or None; returns [BH, n]."""
+    alpha, dS, edge = _f64(alpha), _f64(dS), _f64(edge)
+    P, BH, n = dS.shape
+    A = alpha.shape[2]
+    out = np.empty((BH, n))
+    _load().oracle_state_compose(_p(alpha), _p(dS), _p(edge), _p(out), P, BH, n, A, first, count, step)
     return out

@@ -580,3 +580,40 @@ void oracle_gla_dlog_closed_form(const double *q, const double *k,
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* State passing between slices of one sequence ("Parallel Scan", "Splitting */
+/* one sequence across devices"): a slice run from a zero state gives its   */
+/* pair (alpha, dS): its total decay and its own contribution to its final  */
+/* state.  The state entering a later slice is the earlier pairs composed    */
+/* under (a1, b1) . (a2, b2) = (a1 a2, a2 b1 + b2) and applied to the       */
+/* initial state ("The scan for one number of state": the combine), i.e.    */
+/* the fold acc <- alpha_j acc + dS_j over the pairs in order.               */
+/*   decay_total: alpha[bh][a] = exp(sum_t log_decay[bh][t][a])              */
+/*   state_compose: pairs j = first + c * step, c = 0..count-1; alpha       */
+/*   [P][BH][A] (A = 1: one decay per head; A = rows: one per state row),    */
+/*   dS [P][BH][n], edge [BH][n] or NULL, out [BH][n].                       */
+/* ------------------------------------------------------------------------ */
+void oracle_decay_total(const double *log_decay, double *alpha, i64 BH, i64 T, i64 A) {
+    for (i64 bh = 0; bh < BH; ++bh)
+        for (i64 a = 0; a < A; ++a) {
+            double s = 0.0;
+            for (i64 t = 0; t < T; ++t) s += log_decay[(bh * T + t) * A + a];
+            alpha[bh * A + a] = exp(s);
+        }
+}
+
+void oracle_state_compose(const double *alpha, const double *dS, const double *edge, double *out,
+                          i64 P, i64 BH, i64 n, i64 A, i64 first, i64 count, i64 step) {
+    (void)P;
+    i64 per = n / A;
+    for (i64 bh = 0; bh < BH; ++bh)
+        for (i64 e = 0; e < n; ++e) {
+            double acc = edge ? edge[bh * n + e] : 0.0;
+            for (i64 c = 0; c < count; ++c) {
+                i64 j = first + c * step;
+                acc = alpha[(j * BH + bh) * A + e / per] * acc + dS[(j * BH + bh) * n + e];
+            }
+            out[bh * n + e] = acc;
+        }
+}

@@ -57,6 +57,12 @@ MUTANTS = [
      "for (i64 i = 0; i < dk; ++i) s += Sbar[i * dv + j] * qu[t * dk + i];", 0),
     ("la closed form: sign of the key term", "run += qd - kd;", "run += qd + kd;", 0),
     ("la closed form: drops the final-state term", "double run = tail;", "double run = 0.0;", 0),
+    # state passing between slices
+    ("state compose: decays the slice's own contribution",
+     "acc = alpha[(j * BH + bh) * A + e / per] * acc + dS[(j * BH + bh) * n + e];",
+     "acc = alpha[(j * BH + bh) * A + e / per] * (acc + dS[(j * BH + bh) * n + e]);", 0),
+    ("state compose: ignores the edge state", "double acc = edge ? edge[bh * n + e] : 0.0;", "double acc = 0.0;", 0),
+    ("decay total: sums decays instead of their logs", "alpha[bh * A + a] = exp(s);", "alpha[bh * A + a] = s;", 0),
     # gated linear attention
     ("gla fwd: one decay for every key dimension", "double ai = exp(lt[i]);", "double ai = exp(lt[0]);", 0),
     ("gla bwd: adjoint decayed by the first dimension's decay",

@@ -478,3 +478,55 @@ def test_gla_closed_form_decay_gradient_equals_definition():
     dq, dk_, _, dl, _ = oracle.gla_bwd(q, k, v, log_a, S0, dO, dST)
     dl_cf = oracle.gla_dlog_closed_form(q, k, dq, dk_, dST, ST)
     np.testing.assert_allclose(dl_cf, dl, rtol=1e-10, atol=1e-10)
+
+
+# ---------------------------------------------------------------- state passing between slices
+def test_state_compose_worked_composition():
+    """The fold of the pairs (0.5, 1) then (0.5, 0) onto h0 is the single pair (0.25, 0.5)
+    applied to h0 ("The scan for one number of state", golden), for several h0 and both
+    directions of traversal of the pair list."""
+    (a1, b1, a2, b2, A, Bc), = [list(map(float, r)) for r in _golden_rows("composition_example.txt")]
+    alphas = np.array([[[a1]], [[a2]]])
+    dS = np.array([[[b1]], [[b2]]])
+    for h0 in (0.0, 2.0, -3.5):
+        out = oracle.state_compose(alphas, dS, np.array([[h0]]), 0, 2, 1)
+        assert out[0, 0] == A * h0 + Bc
+        # the same list stored in the other order, read from its end
+        out_r = oracle.state_compose(alphas[::-1].copy(), dS[::-1].copy(), np.array([[h0]]), 1, 2, -1)
+        assert out_r[0, 0] == A * h0 + Bc
+    (h0, a1, b1, h1), = [list(map(float, r)) for r in _golden_rows("fold_example.txt")]
+    assert oracle.state_compose(np.array([[[a1]]]), np.array([[[b1]]]), np.array([[h0]]), 0, 1, 1)[0, 0] == h1
+
+
+def test_state_compose_of_slice_pairs_equals_the_sequential_scan():
+    """Split a diagonal recurrence into slices; each slice's pair (product of its decays, its
+    final state from 0) composed in order onto h0 gives the state entering every later slice --
+    the sequential scan's state there ("Splitting one sequence across devices")."""
+    rng = np.random.default_rng(11)
+    T, D = 57, 5
+    a = rng.uniform(0.6, 1.0, (1, T, D))
+    b = rng.normal(size=(1, T, D))
+    h0 = rng.normal(size=(1, D))
+    h, _ = oracle.scan_diag_fwd(a, b, h0)
+    bounds = [0, 9, 10, 31, 57]
+    alphas, dS = [], []
+    for lo, hi in zip(bounds[:-1], bounds[1:]):
+        _, hT = oracle.scan_diag_fwd(a[:, lo:hi], b[:, lo:hi])
+        alphas.append(np.prod(a[0, lo:hi], axis=0)[:, None])  # one decay per channel (row)
+        dS.append(hT[0][:, None])
+    alphas = np.stack(alphas)[:, None, :, 0]  # [P, BH=1, A=D]
+    dS = np.stack(dS)[:, None, :, 0]          # [P, BH=1, n=D]
+    for p in range(1, len(bounds) - 1):
+        s_in = oracle.state_compose(alphas, dS, h0, 0, p, 1)
+        np.testing.assert_allclose(s_in[0], h[0, bounds[p] - 1], rtol=1e-12, atol=1e-12)
+
+
+def test_decay_total_closed_forms():
+    """exp of the summed log decays: lambda^T for a constant decay, 0 across a reset."""
+    T = 37
+    lam = np.array([0.9, 0.5, 0.999])
+    ld = np.broadcast_to(np.log(lam)[None, None, :], (2, T, 3)).copy()
+    np.testing.assert_allclose(oracle.decay_total(ld), np.broadcast_to(lam ** T, (2, 3)), rtol=1e-12)
+    ld[1, 20, 1] = -np.inf
+    out = oracle.decay_total(ld)
+    assert out[1, 1] == 0.0 and out[0, 1] > 0.0
