@@ -18,6 +18,11 @@ Each function states the passage it follows in the C source; the summary:
   backward pass of linear attention"; "Lightning Attention-2", eqs. 4, 11-12).
 * ``la_dlog_closed_form`` -- the closed-form decay gradient of "The backward
   pass of linear attention".
+* ``delta_fwd`` / ``delta_bwd`` -- the delta rule with a decay per head
+  (Gated DeltaNet: "Parallel Scan", "What one combine costs", the identity
+  minus a rank-one transition that overwrites what a key stores, and "At
+  real scale"), S_t = a_t (I - beta_t k_t^T k_t) S_{t-1} + beta_t k_t^T v_t,
+  and its adjoint.
 * ``decay_total`` / ``state_compose`` -- state passing between slices of one
   sequence ("Parallel Scan", "Splitting one sequence across devices"): a
   slice's total decay, and the fold of slice pairs under the combine.
@@ -77,11 +82,14 @@ def _load():
             lib.oracle_gla_bwd.argtypes = [P] * 12 + [I, I, I, I, I]
             lib.oracle_gla_dlog_closed_form.argtypes = [P] * 7 + [I, I, I, I, I]
             lib.oracle_decay_total.argtypes = [P, P, I, I, I]
+            lib.oracle_delta_fwd.argtypes = [P] * 8 + [I] * 5
+            lib.oracle_delta_bwd.argtypes = [P] * 14 + [I] * 5
             lib.oracle_state_compose.argtypes = [P, P, P, P] + [I] * 7
             for fn in ("oracle_scan_diag_fwd", "oracle_scan_diag_bwd", "oracle_selective_fwd",
                        "oracle_selective_bwd", "oracle_la_fwd", "oracle_la_bwd",
                        "oracle_la_dlog_closed_form", "oracle_gla_fwd", "oracle_gla_bwd",
-                       "oracle_gla_dlog_closed_form", "oracle_decay_total", "oracle_state_compose"):
+                       "oracle_gla_dlog_closed_form", "oracle_decay_total", "oracle_state_compose",
+                       "oracle_delta_fwd", "oracle_delta_bwd"):
                 getattr(lib, fn).restype = None
             _lib = lib
     return _lib
@@ -249,3 +257,31 @@ def state_compose(alpha, dS, edge, first, count, step):
     out = np.empty((BH, n))
     _load().oracle_state_compose(_p(alpha), _p(dS), _p(edge), _p(out), P, BH, n, A, first, count, step)
     return out
+
+
+def delta_fwd(q, k, v, log_a, beta, S0=None):
+    """Delta rule with a decay per head: q, k [B,H,T,dk], v [B,H,T,dv], log_a, beta [B,H,T],
+    S0 [B,H,dk,dv]; returns (o [B,H,T,dv], S_T)."""
+    q, k, v, log_a, beta, S0 = map(_f64, (q, k, v, log_a, beta, S0))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    o = np.empty((B, H, T, dv))
+    ST = np.empty((B, H, dk, dv))
+    _load().oracle_delta_fwd(_p(q), _p(k), _p(v), _p(log_a), _p(beta), _p(S0), _p(o), _p(ST), B, H, T, dk, dv)
+    return o, ST
+
+
+def delta_bwd(q, k, v, log_a, beta, S0, dO, dST=None):
+    """Adjoint of delta_fwd; returns (dq, dk, dv, dlog_a, dbeta, dS0)."""
+    q, k, v, log_a, beta, S0, dO, dST = map(_f64, (q, k, v, log_a, beta, S0, dO, dST))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dq = np.empty((B, H, T, dk))
+    dkk = np.empty((B, H, T, dk))
+    dvv = np.empty((B, H, T, dv))
+    dl = np.empty((B, H, T))
+    db = np.empty((B, H, T))
+    dS0 = np.empty((B, H, dk, dv))
+    _load().oracle_delta_bwd(_p(q), _p(k), _p(v), _p(log_a), _p(beta), _p(S0), _p(dO), _p(dST), _p(dq), _p(dkk),
+                             _p(dvv), _p(dl), _p(db), _p(dS0), B, H, T, dk, dv)
+    return dq, dkk, dvv, dl, db, dS0

@@ -617,3 +617,152 @@ void oracle_state_compose(const double *alpha, const double *dS, const double *e
             out[bh * n + e] = acc;
         }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Delta rule with a decay per head (Gated DeltaNet).  "Parallel Scan",     */
+/* "What one combine costs": the transition is the identity minus a rank-   */
+/* one matrix, and the write overwrites what the state stores under a key   */
+/* instead of only adding to it; "At real scale": the Gated DeltaNet layer  */
+/* has a scalar decay per head besides.  In the pages' row convention       */
+/* (S [dk][dv], rows indexed by keys, o_t = q_t S_t):                       */
+/*   S_t = a_t (I - beta_t k_t^T k_t) S_{t-1} + beta_t k_t^T v_t            */
+/* with a_t = exp(log_a_t) per (head, token) and beta_t per (head, token):  */
+/* with beta = 1 and a unit key, k_t S_t = v_t -- the value now stored      */
+/* under k_t is exactly v_t.                                                 */
+/*   q, k [B][H][T][dk]; v [B][H][T][dv]; log_a, beta [B][H][T];           */
+/*   S0, ST [B][H][dk][dv].                                                  */
+/* ------------------------------------------------------------------------ */
+static void delta_step(const double *kt, const double *vt, double at, double bt, const double *prev,
+                       double *cur, double *u, i64 dk, i64 dv) {
+    /* u = k_t S_{t-1} (the value stored under k_t before the write) */
+    for (i64 j = 0; j < dv; ++j) {
+        double s = 0.0;
+        for (i64 i = 0; i < dk; ++i) s += kt[i] * prev[i * dv + j];
+        u[j] = s;
+    }
+    for (i64 i = 0; i < dk; ++i)
+        for (i64 j = 0; j < dv; ++j)
+            cur[i * dv + j] = at * (prev[i * dv + j] - bt * kt[i] * u[j]) + bt * kt[i] * vt[j];
+}
+
+void oracle_delta_fwd(const double *q, const double *k, const double *v, const double *log_a,
+                      const double *beta, const double *S0, double *o, double *ST, i64 B, i64 H,
+                      i64 T, i64 dk, i64 dv) {
+    i64 units = B * H, ss = dk * dv;
+#pragma omp parallel
+    {
+        double *S = (double *)malloc(sizeof(double) * (size_t)ss);
+        double *N = (double *)malloc(sizeof(double) * (size_t)ss);
+        double *u = (double *)malloc(sizeof(double) * (size_t)dv);
+#pragma omp for schedule(static)
+        for (i64 un = 0; un < units; ++un) {
+            for (i64 i = 0; i < ss; ++i) S[i] = S0 ? S0[un * ss + i] : 0.0;
+            for (i64 t = 0; t < T; ++t) {
+                const double *qt = q + (un * T + t) * dk;
+                delta_step(k + (un * T + t) * dk, v + (un * T + t) * dv, exp(log_a[un * T + t]),
+                           beta[un * T + t], S, N, u, dk, dv);
+                for (i64 i = 0; i < ss; ++i) S[i] = N[i];
+                for (i64 j = 0; j < dv; ++j) {
+                    double s = 0.0;
+                    for (i64 i = 0; i < dk; ++i) s += qt[i] * S[i * dv + j];
+                    o[(un * T + t) * dv + j] = s;
+                }
+            }
+            if (ST)
+                for (i64 i = 0; i < ss; ++i) ST[un * ss + i] = S[i];
+        }
+        free(S);
+        free(N);
+        free(u);
+    }
+}
+
+/* Backward by the adjoint.  With M_t = a_t (I - beta_t k_t^T k_t)           */
+/* (symmetric), u_t = k_t S_{t-1} and Sbar_t = dL/dS_t:                      */
+/*   Sbar_t = q_t^T obar_t + M_{t+1} Sbar_{t+1}   (+ dST at t = T)           */
+/*   dq_t = obar_t S_t^T                                                     */
+/*   dv_t = beta_t k_t Sbar_t                                                */
+/*   dbeta_t = (k_t Sbar_t) . (v_t - a_t u_t)                                */
+/*   dk_t[m] = beta_t Sbar_t[m] . (v_t - a_t u_t)                            */
+/*             - a_t beta_t S_{t-1}[m] . (k_t Sbar_t)                        */
+/*   dlog a_t = <Sbar_t, M_t S_{t-1}>,   dS0 = M_1 Sbar_1.                   */
+/* Every state is kept (short sequences only).                               */
+void oracle_delta_bwd(const double *q, const double *k, const double *v, const double *log_a,
+                      const double *beta, const double *S0, const double *dO, const double *dST,
+                      double *dq, double *dkk, double *dvv, double *dlog_a, double *dbeta,
+                      double *dS0, i64 B, i64 H, i64 T, i64 dk, i64 dv) {
+    i64 units = B * H, ss = dk * dv;
+#pragma omp parallel
+    {
+        double *states = (double *)malloc(sizeof(double) * (size_t)((T + 1) * ss));
+        double *Sbar = (double *)malloc(sizeof(double) * (size_t)ss);
+        double *tmp = (double *)malloc(sizeof(double) * (size_t)ss);
+        double *u = (double *)malloc(sizeof(double) * (size_t)dv);
+        double *kS = (double *)malloc(sizeof(double) * (size_t)dv);
+#pragma omp for schedule(static)
+        for (i64 un = 0; un < units; ++un) {
+            const double *qu = q + un * T * dk, *ku = k + un * T * dk;
+            const double *vu = v + un * T * dv, *du = dO + un * T * dv;
+            for (i64 i = 0; i < ss; ++i) states[i] = S0 ? S0[un * ss + i] : 0.0;
+            for (i64 t = 0; t < T; ++t) {
+                delta_step(ku + t * dk, vu + t * dv, exp(log_a[un * T + t]), beta[un * T + t],
+                           states + t * ss, states + (t + 1) * ss, u, dk, dv);
+                const double *cur = states + (t + 1) * ss;
+                for (i64 i = 0; i < dk; ++i) {
+                    double s = 0.0;
+                    for (i64 j = 0; j < dv; ++j) s += cur[i * dv + j] * du[t * dv + j];
+                    dq[(un * T + t) * dk + i] = s;
+                }
+            }
+            for (i64 i = 0; i < ss; ++i) Sbar[i] = dST ? dST[un * ss + i] : 0.0;
+            for (i64 t = T - 1; t >= 0; --t) {
+                const double *kt = ku + t * dk, *vt = vu + t * dv, *qt = qu + t * dk;
+                const double at = exp(log_a[un * T + t]), bt = beta[un * T + t];
+                const double *prev = states + t * ss;
+                /* Sbar_t: the later step's contribution is already in Sbar (M_{t+1} Sbar_{t+1}) */
+                for (i64 i = 0; i < dk; ++i)
+                    for (i64 j = 0; j < dv; ++j) Sbar[i * dv + j] += qt[i] * du[t * dv + j];
+                for (i64 j = 0; j < dv; ++j) {
+                    double su = 0.0, sk = 0.0;
+                    for (i64 i = 0; i < dk; ++i) {
+                        su += kt[i] * prev[i * dv + j];
+                        sk += kt[i] * Sbar[i * dv + j];
+                    }
+                    u[j] = su;
+                    kS[j] = sk;
+                    dvv[(un * T + t) * dv + j] = bt * sk;
+                }
+                double db = 0.0;
+                for (i64 j = 0; j < dv; ++j) db += kS[j] * (vt[j] - at * u[j]);
+                if (dbeta) dbeta[un * T + t] = db;
+                for (i64 m = 0; m < dk; ++m) {
+                    double s1 = 0.0, s2 = 0.0;
+                    for (i64 j = 0; j < dv; ++j) {
+                        s1 += Sbar[m * dv + j] * (vt[j] - at * u[j]);
+                        s2 += prev[m * dv + j] * kS[j];
+                    }
+                    dkk[(un * T + t) * dk + m] = bt * s1 - at * bt * s2;
+                }
+                if (dlog_a) {
+                    /* <Sbar_t, M_t S_{t-1}> = a_t (<Sbar, S_{t-1}> - beta (k Sbar) . u) */
+                    double s = 0.0;
+                    for (i64 i = 0; i < ss; ++i) s += Sbar[i] * prev[i];
+                    double c = 0.0;
+                    for (i64 j = 0; j < dv; ++j) c += kS[j] * u[j];
+                    dlog_a[un * T + t] = at * (s - bt * c);
+                }
+                /* Sbar <- M_t Sbar (the gradient on S_{t-1}) */
+                for (i64 i = 0; i < dk; ++i)
+                    for (i64 j = 0; j < dv; ++j) tmp[i * dv + j] = at * (Sbar[i * dv + j] - bt * kt[i] * kS[j]);
+                for (i64 i = 0; i < ss; ++i) Sbar[i] = tmp[i];
+            }
+            if (dS0)
+                for (i64 i = 0; i < ss; ++i) dS0[un * ss + i] = Sbar[i];
+        }
+        free(states);
+        free(Sbar);
+        free(tmp);
+        free(u);
+        free(kS);
+    }
+}

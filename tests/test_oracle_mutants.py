@@ -1,7 +1,7 @@
 """The oracle's pins catch plausible mistakes: each mutant below is oracle.c with one planted
 error (a dropped term, a wrong sign, a time index off by one, an operand swapped for another),
-compiled on its own, and the pins of tests/test_oracle_pins.py must fail against every one of
-them.  The unmutated source, compiled the same way, must pass them.  Mistakes are planted in
+compiled on its own, and the pins of tests/test_oracle_pins.py and tests/test_delta_rule.py must
+fail against every one of them.  The unmutated source, compiled the same way, must pass them.  Mistakes are planted in
 the oracle on the CPU only; nothing here touches the CUDA library.
 """
 import concurrent.futures as cf
@@ -73,6 +73,19 @@ MUTANTS = [
     ("gla bwd: dS0 without a_1", "dS0[u * ss + i * dv + j] = anext[i] * Sbar[i * dv + j];",
      "dS0[u * ss + i * dv + j] = Sbar[i * dv + j];", 0),
     ("gla closed form: drops the key term", "run += q[x] * dq[x] - k[x] * dkk[x];", "run += q[x] * dq[x];", 0),
+    # delta rule
+    ("delta: corrects with the new value instead of the stored one",
+     "cur[i * dv + j] = at * (prev[i * dv + j] - bt * kt[i] * u[j]) + bt * kt[i] * vt[j];",
+     "cur[i * dv + j] = at * (prev[i * dv + j] - bt * kt[i] * vt[j]) + bt * kt[i] * vt[j];", 0),
+    ("delta: decays the token's own write",
+     "cur[i * dv + j] = at * (prev[i * dv + j] - bt * kt[i] * u[j]) + bt * kt[i] * vt[j];",
+     "cur[i * dv + j] = at * (prev[i * dv + j] - bt * kt[i] * u[j] + bt * kt[i] * vt[j]);", 0),
+    ("delta bwd: dk without the stored-value term", "dkk[(un * T + t) * dk + m] = bt * s1 - at * bt * s2;",
+     "dkk[(un * T + t) * dk + m] = bt * s1;", 0),
+    ("delta bwd: sign of the correction in dbeta", "db += kS[j] * (vt[j] - at * u[j]);",
+     "db += kS[j] * (vt[j] + at * u[j]);", 0),
+    ("delta bwd: adjoint without the rank-one part",
+     "tmp[i * dv + j] = at * (Sbar[i * dv + j] - bt * kt[i] * kS[j]);", "tmp[i * dv + j] = at * Sbar[i * dv + j];", 0),
 ]
 
 
@@ -96,9 +109,9 @@ def _compile(src_text, path):
 
 def _run_pins(lib):
     env = dict(os.environ, OMP_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"), "-q",
-                        "-p", "no:cacheprovider", "--oracle-lib", lib], capture_output=True, text=True, cwd=ROOT,
-                       env=env, timeout=600)
+    pins = [os.path.join(ROOT, "tests", f) for f in ("test_oracle_pins.py", "test_delta_rule.py")]
+    r = subprocess.run([sys.executable, "-m", "pytest"] + pins + ["-q", "-p", "no:cacheprovider", "--oracle-lib", lib],
+                       capture_output=True, text=True, cwd=ROOT, env=env, timeout=600)
     failed = sorted({line.split("::")[1].split(" ")[0].split("[")[0] for line in r.stdout.splitlines()
                      if line.startswith("FAILED ")})
     return r.returncode, failed, r.stdout[-2000:]
