@@ -495,6 +495,31 @@ def bench_gla(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
     return res
 
 
+def bench_delta(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
+    """Delta rule with a decay per head (Gated DeltaNet) forward, chunk 64."""
+    inp = workloads.make("delta", **(shape or {}))
+    t = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    B, H, T, dk = t["q"].shape
+    dv = t["v"].shape[-1]
+    ws = torch.empty(max(cla.delta_workspace_size(B, H, T, dk, dv, 64), 256), dtype=torch.uint8, device=dev)
+    o = torch.empty(B, H, T, dv, device=dev)
+    ST = torch.empty(B, H, dk, dv, device=dev)
+    fwd = lambda: cla.delta_fwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], t["S0"], o=o, ST=ST, workspace=ws)
+    tf = _time_calls(torch, fwd, flush, iters)
+    cla.check_status(ws)
+    ntok = B * H * T
+    # the decayed-linear-attention part (scores, P Veff, Q S, state update) plus the chunk's own
+    # extra products (K K^T, K S, (I + A)^-1 X): 2 C (2 dk + 2 dv) + 6 dk dv per token
+    fl = ntok * (2 * 64 * (2 * dk + 2 * dv) + 6 * dk * dv)
+    by_min = ntok * (2 * (2 * dk + dv) + 8 + 2 * dv)
+    sec = tf / 1e3
+    return {"workload": f"delta rule (Gated DeltaNet) fwd B={B} H={H} T={T} dk={dk} dv={dv} chunk=64",
+            "fwd_us": round(tf * 1e3, 1), "tokens_per_s": round(B * T / sec, 1),
+            "fwd_TFLOPs": round(fl / sec / 1e12, 2), "frac_bf16_peak": round(fl / sec / (peaks["bf16_tflops"] * 1e12), 4),
+            "frac_hbm_min_bytes": round(by_min / sec / (peaks["hbm_gbs"] * 1e9), 4),
+            "kernel": "delta_fwd_kernel (mma.sync m16n8k16; chunks of a head in order, no look-back)"}
+
+
 def bench_selective(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
     inp = workloads.make("selective", **(shape or {}))
     t = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
@@ -605,7 +630,7 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--only", default=None,
                     choices=["scan_small", "scan_fwd_blelloch", "scan_bwd_recompute", "selective", "la_const", "la_long",
-                             "la_long_chunk64", "gla"],
+                             "la_long_chunk64", "gla", "delta"],
                     help="time one workload only (forward and backward), e.g. for profiling")
     ap.add_argument("--shape", default="", help="shape overrides for --only, e.g. H=32,T=4096")
     args = ap.parse_args()
@@ -645,7 +670,8 @@ def main():
                "la_const": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_const", 64, it, shape),
                "la_long": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 128, it, shape),
                "la_long_chunk64": lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 64, it, shape),
-               "gla": lambda: bench_gla(torch, cla, workloads, dev, flush, peaks, it, shape)}
+               "gla": lambda: bench_gla(torch, cla, workloads, dev, flush, peaks, it, shape),
+               "delta": lambda: bench_delta(torch, cla, workloads, dev, flush, peaks, it, shape)}
         print(json.dumps({"only": args.only, "shape": shape, "result": fns[args.only]()}), flush=True)
         return 0
 
@@ -671,7 +697,8 @@ def main():
                 ("la_const", lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_const", 64)),
                 ("la_long", lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 128, e2e_steps=3)),
                 ("la_long_chunk64", lambda: bench_la(torch, cla, workloads, dev, flush, peaks, "la_long", 64)),
-                ("gla", lambda: bench_gla(torch, cla, workloads, dev, flush, peaks))):
+                ("gla", lambda: bench_gla(torch, cla, workloads, dev, flush, peaks)),
+                ("delta", lambda: bench_delta(torch, cla, workloads, dev, flush, peaks))):
             try:
                 extra[key] = fn()
             except Exception as e:  # an entry point without a kernel yet reports itself

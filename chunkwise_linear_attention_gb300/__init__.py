@@ -69,6 +69,8 @@ def lib():
                 "cla_gla_bwd_workspace_size": ([I64] * 5 + [INT], SZ),
                 "cla_gla_bwd": ([P] * 12 + [I64] * 5 + [INT, P, SZ, P], INT),
                 "cla_decay_total": ([P, P, I64, I64, I64, P], INT),
+                "cla_delta_workspace_size": ([I64] * 5 + [INT], SZ),
+                "cla_delta_fwd": ([P] * 8 + [I64] * 5 + [INT, P, SZ, P], INT),
                 "cla_state_compose": ([P] * 4 + [I64] * 7 + [P], INT),
             }
             for name, (args, res) in sig.items():
@@ -465,3 +467,27 @@ def state_compose(alphas, dSs, edge, first, count, step, *, out=None, stream=Non
         _T(dSs, torch.float32, "dSs", (P, B, H, dk, dv)), _T(edge, torch.float32, "edge", st),
         _T(out, torch.float32, "out", st), P, B * H, dk * dv, A, int(first), int(count), int(step)), stream)
     return out
+
+
+# ---------------------------------------------------------------- delta rule (Gated DeltaNet)
+def delta_workspace_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
+    return int(lib().cla_delta_workspace_size(B, H, T, dim_k, dim_v, int(chunk)))
+
+
+def delta_fwd(q, k, v, log_decay, beta, S0=None, *, chunk=64, o=None, ST=None, workspace=None, stream=None):
+    """Delta rule with a decay per head: S_t = a_t (I - beta_t k_t^T k_t) S_{t-1} + beta_t k_t^T v_t,
+    o_t = q_t S_t; log_decay, beta [B, H, T].  Returns (o, ST)."""
+    B, H, T, dk = _dims(q, 4, "q")
+    dv = _dims(v, 4, "v")[3]
+    dev = q.device
+    f32, bf16 = torch.float32, torch.bfloat16
+    o = _out(o, (B, H, T, dv), f32, dev)
+    ST = _out(ST, (B, H, dk, dv), f32, dev)
+    ws = _ws(delta_workspace_size(B, H, T, dk, dv, chunk), dev, workspace)
+    tk, tv, st, bht = (B, H, T, dk), (B, H, T, dv), (B, H, dk, dv), (B, H, T)
+    _launch("cla_delta_fwd", dev, (
+        _T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
+        _T(log_decay, f32, "log_decay", bht), _T(beta, f32, "beta", bht), _T(S0, f32, "S0", st),
+        _T(o, f32, "o", tv), _T(ST, f32, "ST", st),
+        B, H, T, dk, dv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws)), stream)
+    return o, ST

@@ -82,7 +82,7 @@ extern "C" int cla_check_status(const void *ws, void *stream) {
     if (hdr.error & cla::kErrRange)
         return cla::fail(CLA_ERR_UNSUPPORTED,
                          "an input was outside the kernel's range (gated linear attention: a key dimension whose "
-                         "decay over 32 tokens of a chunk is below 2^-120, or a zero or non-finite gate); the "
-                         "results of that call are not valid");
+                         "decay over 32 tokens of a chunk is below 2^-120, or a zero or non-finite gate; delta "
+                         "rule: a non-finite log decay or beta); the results of that call are not valid");
     return CLA_OK;
 }

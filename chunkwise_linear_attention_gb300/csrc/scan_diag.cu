@@ -566,6 +566,136 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
     }
 }
 
+// ------------------------------------------------------------------ short sequences
+// A problem too small to fill the GPU with chunk blocks (at most kSmallBlocks
+// channel groups, each at most kSmallMaxChunks chunks long) runs in one block
+// per (batch row, channel group), with no workspace and no cross-block
+// look-back: warp w owns a contiguous run of chunks; it folds them into one
+// pair per channel (phase 1), the block composes the warps' pairs in shared
+// memory onto h0, and each warp re-runs its chunks from its true incoming
+// state and writes h (phase 2; the re-read hits L2).  Inside a chunk the
+// composition is the one of scan_diag_fwd_kernel: a sequential run per lane,
+// then Hillis-Steele across the 8 runs.
+constexpr int kSmallWarps = 8;
+constexpr int kSmallMaxChunks = 64;
+constexpr long long kSmallBlocks = 152;
+
+template <int VEC>
+__global__ void __launch_bounds__(kSmallWarps * 32)
+scan_diag_fwd_small_kernel(const float *__restrict__ a, const float *__restrict__ b,
+                           const float *__restrict__ h0, float *__restrict__ h,
+                           float *__restrict__ hT, ScanGeom g) {
+    __shared__ float sA[kSmallWarps][kCg * VEC], sB[kSmallWarps][kCg * VEC];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane >> 2, cg = lane & 3;
+    const int bi = blockIdx.y, cw = blockIdx.x;
+    const int c0 = cw * (kCg * VEC) + cg * VEC;
+    const bool cok = c0 < g.D;
+    const int per = (g.n_chunks + kSmallWarps - 1) / kSmallWarps;
+    const int ch_begin = min(warp * per, g.n_chunks), ch_end = min(ch_begin + per, g.n_chunks);
+
+    // the runs of one chunk: this lane's steps, its run's pair and its prefix within the chunk,
+    // and the chunk's pair (the last run's inclusive prefix, on every lane)
+    float av[kL][VEC], bv[kL][VEC], Aex[VEC], Bex[VEC], CA[VEC], CB[VEC];
+    auto chunk_pairs = [&](int chunk) {
+        const long long t_begin = (long long)chunk * kTc + sub * kL;
+#pragma unroll
+        for (int i = 0; i < kL; ++i) {
+            const long long t = t_begin + i;
+            if (cok && t < g.T) {
+                const size_t idx = ((size_t)bi * g.T + t) * g.D + c0;
+                VecIO<VEC>::load(a + idx, av[i]);
+                VecIO<VEC>::load(b + idx, bv[i]);
+            } else {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) { av[i][v] = 1.f; bv[i][v] = 0.f; }
+            }
+        }
+        float A[VEC], Bc[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { A[v] = 1.f; Bc[v] = 0.f; }
+#pragma unroll
+        for (int i = 0; i < kL; ++i)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                Bc[v] = fmaf(av[i][v], Bc[v], bv[i][v]);
+                A[v] *= av[i][v];
+            }
+#pragma unroll
+        for (int off = 1; off < kSub; off <<= 1) {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float pa = __shfl_up_sync(0xffffffffu, A[v], off * kCg);
+                const float pb = __shfl_up_sync(0xffffffffu, Bc[v], off * kCg);
+                if (sub >= off) {
+                    Bc[v] = fmaf(A[v], pb, Bc[v]);
+                    A[v] *= pa;
+                }
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            Aex[v] = __shfl_up_sync(0xffffffffu, A[v], kCg);
+            Bex[v] = __shfl_up_sync(0xffffffffu, Bc[v], kCg);
+            if (sub == 0) { Aex[v] = 1.f; Bex[v] = 0.f; }
+            CA[v] = __shfl_sync(0xffffffffu, A[v], (kSub - 1) * kCg + cg);
+            CB[v] = __shfl_sync(0xffffffffu, Bc[v], (kSub - 1) * kCg + cg);
+        }
+    };
+
+    // phase 1: this warp's chunks folded into one pair per channel
+    float SA[VEC], SB[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) { SA[v] = 1.f; SB[v] = 0.f; }
+    for (int chunk = ch_begin; chunk < ch_end; ++chunk) {
+        chunk_pairs(chunk);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            SB[v] = fmaf(CA[v], SB[v], CB[v]);
+            SA[v] *= CA[v];
+        }
+    }
+    if (sub == 0) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            sA[warp][cg * VEC + v] = SA[v];
+            sB[warp][cg * VEC + v] = SB[v];
+        }
+    }
+    __syncthreads();
+    // the state entering this warp's chunks: h0, then the earlier warps' pairs in order
+    float carry[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) carry[v] = (h0 != nullptr && cok) ? h0[(size_t)bi * g.D + c0 + v] : 0.f;
+    for (int w = 0; w < warp; ++w)
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) carry[v] = fmaf(sA[w][cg * VEC + v], carry[v], sB[w][cg * VEC + v]);
+
+    // phase 2: re-run from the true state, write h once
+    for (int chunk = ch_begin; chunk < ch_end; ++chunk) {
+        chunk_pairs(chunk);
+        const long long t_begin = (long long)chunk * kTc + sub * kL;
+        float hs[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) hs[v] = fmaf(Aex[v], carry[v], Bex[v]);
+#pragma unroll
+        for (int i = 0; i < kL; ++i) {
+            const long long t = t_begin + i;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) hs[v] = fmaf(av[i][v], hs[v], bv[i][v]);
+            if (cok && t < g.T) {
+                const size_t idx = ((size_t)bi * g.T + t) * g.D + c0;
+                VecIO<VEC>::store(h + idx, hs);
+                if (hT != nullptr && t == g.T - 1)
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) hT[(size_t)bi * g.D + c0 + v] = hs[v];
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) carry[v] = fmaf(CA[v], carry[v], CB[v]);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 struct Plan {
     ScanGeom g;
@@ -653,6 +783,13 @@ int scan_fwd(const char *fn, bool blelloch, const float *a, const float *b, cons
     const bool v4 = (D % 4 == 0) && aligned16(a) && aligned16(b) && aligned16(h);
     const Plan p = make_plan(B, T, D, v4 ? 4 : 1);
     if (ws_bytes < p.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, p.total);
+    if (!blelloch && p.g.n_chunks <= kSmallMaxChunks && (long long)p.g.B * p.g.n_cw <= kSmallBlocks) {
+        // short sequence, few channel groups: one block per group, no workspace traffic
+        const dim3 grid((unsigned int)p.g.n_cw, (unsigned int)p.g.B);
+        if (v4) scan_diag_fwd_small_kernel<4><<<grid, kSmallWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g);
+        else scan_diag_fwd_small_kernel<1><<<grid, kSmallWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g);
+        return check_launch(fn);
+    }
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.total, s), fn);
     const ScanWs w = bind_ws(p, ws);
     const unsigned int grid = (unsigned int)((size_t)p.g.n_chunks * p.g.B * p.g.n_cblk);

@@ -389,6 +389,43 @@ int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                 void *stream);
 
 /* ======================================================================== */
+/* Delta rule with a decay per head (Gated DeltaNet)                         */
+/* ======================================================================== */
+
+/* Bytes of workspace for cla_delta_fwd (its header: the error flag); 0 for
+ * sizes, head dims or chunks that call refuses. */
+size_t cla_delta_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                                int64_t dim_v, int chunk);
+
+/* Forward of S_t = a_t (I - beta_t k_t^T k_t) S_{t-1} + beta_t k_t^T v_t,
+ * o_t = S_t^T q_t ("Parallel Scan", "What one combine costs": a transition
+ * that is the identity minus a rank-one matrix, overwriting what the state
+ * stores under a key, and its WY representation; "At real scale": the Gated
+ * DeltaNet layer's decay per head), chunkwise: inside a 64-token chunk with
+ * cumulative decays gamma and A_rs = beta_r (gamma_r / gamma_s) k_r . k_s
+ * (s < r),
+ *   Veff = (I + A)^-1 diag(beta) (V - diag(gamma) K S)
+ *   O    = diag(gamma) Q S + ((Q K^T) . D) Veff
+ *   S'   = gamma_L S + K^T diag(gamma_L / gamma) Veff.
+ * The chunks of a head run in order (one block per head and 64 value
+ * columns).
+ *   q, k       [B, H, T, dim_k] bf16 (keys are used as given; the layer
+ *              normally L2-normalises them)
+ *   v          [B, H, T, dim_v] bf16
+ *   log_decay  [B, H, T] fp32 (natural log of a_t, finite)
+ *   beta       [B, H, T] fp32 (write strengths, finite)
+ *   S0         [B, H, dim_k, dim_v] fp32 [opt]
+ *   o          [B, H, T, dim_v] fp32 out;  ST [B, H, dim_k, dim_v] fp32 [opt] out
+ * Supported: dim_k 64 or 128, dim_v a multiple of 64 up to 1024, chunk 64.
+ * A non-finite log decay or beta makes cla_check_status(ws, stream) return
+ * CLA_ERR_UNSUPPORTED (the outputs are then not valid). */
+int cla_delta_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                  const float *log_decay, const float *beta, const float *S0,
+                  float *o, float *ST, int64_t B, int64_t H, int64_t T,
+                  int64_t dim_k, int64_t dim_v, int chunk, void *ws,
+                  size_t ws_bytes, void *stream);
+
+/* ======================================================================== */
 /* State passing between slices of one sequence                             */
 /* ======================================================================== */
 
