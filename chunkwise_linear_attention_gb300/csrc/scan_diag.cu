@@ -576,7 +576,7 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
 // state and writes h (phase 2; the re-read hits L2).  Inside a chunk the
 // composition is the one of scan_diag_fwd_kernel: a sequential run per lane,
 // then Hillis-Steele across the 8 runs.
-constexpr int kSmallWarps = 8;
+constexpr int kSmallWarps = 16;        // one chunk per warp up to 1024 steps
 constexpr int kSmallMaxChunks = 64;
 constexpr long long kSmallBlocks = 152;
 

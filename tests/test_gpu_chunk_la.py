@@ -112,11 +112,13 @@ def test_chunk_la_constant_decay_workload_full(cla):
 
 
 def test_chunk_la_long_workload_sampled_heads(cla):
-    """1 x 32 x 65536, d = 128, chunk 128 on the GPU; heads 0 and 31 against
-    the oracle (heads are independent problems); the benchmark's path, with the
-    forward's segment states."""
+    """1 x 32 x 65536, d = 128, chunk 128 on the GPU; heads 0, 31 and two seeded
+    middle heads against the oracle (heads are independent problems); the
+    benchmark's path, with the forward's segment states."""
     inp = workloads.make("la_long")
-    _check(cla, inp, 128, heads=[0, 31], ckpt=True)
+    # the first and last heads and two seeded middle ones
+    mid = sorted(np.random.default_rng(128).choice(np.arange(1, 31), 2, replace=False).tolist())
+    _check(cla, inp, 128, heads=[0] + mid + [31], ckpt=True)
 
 
 @pytest.mark.parametrize("B,H,T,d,chunk", [

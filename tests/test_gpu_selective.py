@@ -65,11 +65,14 @@ def test_selective_general_A(cla):
 
 def test_selective_workload_full(cla):
     """4 x 8192 x 2048 x 16 on the GPU.  Per-channel outputs (y, hT, dx,
-    ddelta, dA) are checked on 64 channels over every batch row and step; the
-    channel sums dB, dC on batch row 0 over all channels."""
+    ddelta, dA) are checked on 96 channels (first, last and seeded middle ones)
+    over every batch row and step; the channel sums dB, dC on batch row 0 and a
+    seeded other row over all channels."""
     inp = workloads.make("selective")
     y, hT, (dx, dd, dA, dB, dC, dh0) = _run_gpu(cla, inp)
-    chans = list(range(32)) + list(range(2016, 2048))
+    # the first and last 32 channels, and 32 seeded ones from the middle
+    mid = np.random.default_rng(2048).choice(np.arange(32, 2016), 32, replace=False)
+    chans = list(range(32)) + sorted(mid.tolist()) + list(range(2016, 2048))
     sub = {k: (v[:, :, chans] if k in ("x", "delta", "dy") else v) for k, v in inp.items() if v is not None}
     sub["A"] = inp["A"][chans]
     ry, rhT = oracle.selective_fwd(sub["x"], sub["delta"], sub["A"], sub["Bm"], sub["Cm"])
@@ -80,10 +83,13 @@ def test_selective_workload_full(cla):
     assert_fp32("dx", dx[:, :, chans], rdx)
     assert_fp32("ddelta", dd[:, :, chans], rdd)
     assert_fp32("dA", dA[chans], rdA)
-    b0 = {k: (v[:1] if k not in ("A",) else v) for k, v in inp.items() if v is not None}
-    _, _, _, rdB, rdC, _ = oracle.selective_bwd(b0["x"], b0["delta"], b0["A"], b0["Bm"], b0["Cm"], None, b0["dy"])
-    assert_fp32("dB", dB[:1], rdB)
-    assert_fp32("dC", dC[:1], rdC)
+    # channel sums over all channels: batch row 0 and a seeded middle row
+    for row in (0, int(np.random.default_rng(4).integers(1, 4))):
+        b0 = {k: (v[row:row + 1] if k not in ("A",) else v) for k, v in inp.items() if v is not None}
+        _, _, _, rdB, rdC, _ = oracle.selective_bwd(b0["x"], b0["delta"], b0["A"], b0["Bm"], b0["Cm"], None,
+                                                    b0["dy"])
+        assert_fp32("dB", dB[row:row + 1], rdB)
+        assert_fp32("dC", dC[row:row + 1], rdC)
 
 
 def test_selective_decay_accuracy(cla):
