@@ -570,7 +570,8 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
 // A problem too small to fill the GPU with chunk blocks (at most kSmallBlocks
 // channel groups, each at most kSmallMaxChunks chunks long) runs in one block
 // per (batch row, channel group), with no workspace and no cross-block
-// look-back: warp w owns a contiguous run of chunks; it folds them into one
+// look-back (it only clears the workspace header's status): warp w owns a
+// contiguous run of chunks; it folds them into one
 // pair per channel (phase 1), the block composes the warps' pairs in shared
 // memory onto h0, and each warp re-runs its chunks from its true incoming
 // state and writes h (phase 2; the re-read hits L2).  Inside a chunk the
@@ -584,8 +585,13 @@ template <int VEC>
 __global__ void __launch_bounds__(kSmallWarps * 32)
 scan_diag_fwd_small_kernel(const float *__restrict__ a, const float *__restrict__ b,
                            const float *__restrict__ h0, float *__restrict__ h,
-                           float *__restrict__ hT, ScanGeom g) {
+                           float *__restrict__ hT, ScanGeom g, WsHeader *hdr) {
     __shared__ float sA[kSmallWarps][kCg * VEC], sB[kSmallWarps][kCg * VEC];
+    // this call's status, for cla_check_status: the kernel has no cross-block wait to give up
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        hdr->error = 0u;
+        hdr->where = 0u;
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane >> 2, cg = lane & 3;
     const int bi = blockIdx.y, cw = blockIdx.x;
@@ -786,8 +792,9 @@ int scan_fwd(const char *fn, bool blelloch, const float *a, const float *b, cons
     if (!blelloch && p.g.n_chunks <= kSmallMaxChunks && (long long)p.g.B * p.g.n_cw <= kSmallBlocks) {
         // short sequence, few channel groups: one block per group, no workspace traffic
         const dim3 grid((unsigned int)p.g.n_cw, (unsigned int)p.g.B);
-        if (v4) scan_diag_fwd_small_kernel<4><<<grid, kSmallWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g);
-        else scan_diag_fwd_small_kernel<1><<<grid, kSmallWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g);
+        WsHeader *hdr = static_cast<WsHeader *>(ws);
+        if (v4) scan_diag_fwd_small_kernel<4><<<grid, kSmallWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, hdr);
+        else scan_diag_fwd_small_kernel<1><<<grid, kSmallWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, hdr);
         return check_launch(fn);
     }
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.total, s), fn);

@@ -20,6 +20,11 @@ def test_bounded_wait_reports_timeout():
     x = torch.ones(1000, device="cuda")
     assert float(x.sum()) == 1000.0
     a = torch.full((1, 10, 4), 0.5, device="cuda")
-    h, hT = cla.scan_diag_fwd(a, torch.ones_like(a))
-    cla.check_status(torch.empty(cla.scan_diag_workspace_size(1, 10, 4), dtype=torch.uint8, device="cuda"))
+    # reusing the workspace that timed out: the new call's status replaces the old one
+    h, hT = cla.scan_diag_fwd(a, torch.ones_like(a), workspace=ws)
+    cla.check_status(ws)
+    ws2 = torch.empty(cla.scan_diag_workspace_size(8, 4096, 64), dtype=torch.uint8, device="cuda")
+    a2 = torch.full((8, 4096, 64), 0.5, device="cuda")
+    cla.scan_diag_fwd(a2, torch.ones_like(a2), workspace=ws2)  # the multi-block path
+    cla.check_status(ws2)
     assert abs(float(hT[0, 0]) - 2.0 * (1 - 0.5 ** 10)) < 1e-6
