@@ -22,7 +22,7 @@
 // parts for its product with X.
 //
 // This first kernel runs the chunks of a head in order (one block per head
-// and 64 value columns): the chunk map S -> S' is a dk x dk matrix here, not
+// and 64 value columns, two blocks per SM): the chunk map S -> S' is a dk x dk matrix here, not
 // a scalar, so the segment look-back of the other kernels would compose
 // matrices; it is not built.  Products on mma.sync m16n8k16 with the operands
 // that are not exact bf16 inputs split into two bf16 parts (K S, T X, P Veff,
@@ -55,20 +55,24 @@ struct DeltaCfg {
     static constexpr int OFF_L = 2 * Q_BYTES + V_BYTES;
     static constexpr int OFF_B = OFF_L + kDlTc * 4;
     static constexpr int STAGE = OFF_B + kDlTc * 4;
-    static constexpr int OFF_A = 2 * STAGE;                 // A, fp32 [64][64] (row stride 65)
+    // Buffers whose lives do not overlap share memory (two blocks then fit an SM):
+    // A (fp32) until (I + A)^-1 is built, then X and Veff in the same bytes;
+    // (I + A)^-1 until Veff is formed, then diag(gamma_L / gamma) Veff.
+    static constexpr int OFF_A = STAGE;                     // A, fp32 [64][64] (row stride 65)
     static constexpr int A_FLOATS = kDlTc * (kDlTc + 1);
+    static constexpr int OFF_XH = OFF_A;                    // X, then Veff, two bf16 parts [64][64]
+    static constexpr int OFF_XL = OFF_XH + kDlTc * VRB;
     static constexpr int OFF_TH = OFF_A + A_FLOATS * 4;     // (I + A)^-1 as two bf16 parts [64][64]
     static constexpr int OFF_TL = OFF_TH + kDlTc * VRB;
+    static constexpr int OFF_WH = OFF_TH;                   // diag(gamma_L / gamma) Veff, two parts
+    static constexpr int OFF_WL = OFF_TL;
     static constexpr int OFF_SH = OFF_TL + kDlTc * VRB;     // the state, two bf16 parts [DK][64]
     static constexpr int OFF_SL = OFF_SH + DK * VRB;
-    static constexpr int OFF_XH = OFF_SL + DK * VRB;        // X, then Veff, two bf16 parts [64][64]
-    static constexpr int OFF_XL = OFF_XH + kDlTc * VRB;
-    static constexpr int OFF_WH = OFF_XL + kDlTc * VRB;     // diag(gamma_L / gamma) Veff, two parts
-    static constexpr int OFF_WL = OFF_WH + kDlTc * VRB;
-    static constexpr int OFF_C = OFF_WL + kDlTc * VRB;      // in-chunk log2 decays c_r [64]
+    static constexpr int OFF_C = OFF_SL + DK * VRB;         // in-chunk log2 decays c_r [64]
     static constexpr int SMEM = OFF_C + kDlTc * 4;
     static constexpr int S_MT = DK / 64;  // 16-row state tiles per warp
-    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(2 * kDlTc * VRB <= A_FLOATS * 4, "X fits where A was");
+    static_assert(2 * (SMEM + 1024) <= 228 * 1024, "two blocks per SM");
 };
 
 struct DeltaArgs {
@@ -82,7 +86,7 @@ struct DeltaArgs {
 };
 
 template <int DK>
-__global__ void __launch_bounds__(kDlThreads, 1) delta_fwd_kernel(const DeltaArgs p) {
+__global__ void __launch_bounds__(kDlThreads, 2) delta_fwd_kernel(const DeltaArgs p) {
     using C = DeltaCfg<DK>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -174,17 +178,17 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_fwd_kernel(const DeltaArg
     };
     const int arow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 
+    // one stage of loads: the next chunk's is issued once this chunk's inputs are consumed (a
+    // second block on the SM runs meanwhile)
     load_stage(0, 0);
     cp_async_commit();
-    if (p.n_chunks > 1) load_stage(1, 1);
-    cp_async_commit();
     for (int i = 0; i < p.n_chunks; ++i) {
-        const int stage = i & 1;
-        uint8_t *st = smem + stage * C::STAGE;
+        const int stage = 0;
+        uint8_t *st = smem;
         const float *ls = reinterpret_cast<const float *>(st + C::OFF_L);
         const float *bs = reinterpret_cast<const float *>(st + C::OFF_B);
         const long long t0 = (long long)i * kDlTc;
-        cp_async_wait<1>();
+        cp_async_wait<0>();
         __syncthreads();
         // ---- in-chunk log2 decays (warp 0) and the state's bf16 parts (everyone)
         if (warp == 0) {
@@ -436,7 +440,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_fwd_kernel(const DeltaArg
             }
         }
         __syncthreads();
-        if (i + 2 < p.n_chunks) load_stage(stage, i + 2);
+        if (i + 1 < p.n_chunks) load_stage(stage, i + 1);
         cp_async_commit();
     }
     cp_async_wait<0>();

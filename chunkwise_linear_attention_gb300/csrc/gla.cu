@@ -995,8 +995,10 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
 //   dlog a_u[i] = sum_{t>=u} (q_t[i] dq_t[i] - k_t[i] dk_t[i]) + fs[i],
 // fs[i] = sum_j dST[i][j] S_T[i][j].  A reverse scan over tiles of
 // kGlaDlTile tokens: per-tile column sums first, then each tile's suffix sums
-// plus every later tile and fs.  Thread = key dimension; fixed summation order.
-constexpr int kGlaDlTile = 256;
+// plus every later tile and fs.  Thread = key dimension (coalesced rows);
+// fixed summation order; loops unrolled so a thread's loads are in flight
+// together.
+constexpr int kGlaDlTile = 128;
 
 __global__ void gla_dlog_tile_sums_kernel(const bf16 *__restrict__ q, const float *__restrict__ dq,
                                           const bf16 *__restrict__ k, const float *__restrict__ dk,
@@ -1007,9 +1009,10 @@ __global__ void gla_dlog_tile_sums_kernel(const bf16 *__restrict__ q, const floa
     const long long t0 = (long long)tile * kGlaDlTile;
     const long long t1 = min(t0 + kGlaDlTile, T);
     float acc = 0.f;
+#pragma unroll 8
     for (long long t = t0; t < t1; ++t) {
         const size_t x = (bh * T + t) * DK + i;
-        acc += __bfloat162float(q[x]) * dq[x] - __bfloat162float(k[x]) * dk[x];
+        acc += __bfloat162float(__ldg(q + x)) * __ldg(dq + x) - __bfloat162float(__ldg(k + x)) * __ldg(dk + x);
     }
     tsum[(bh * n_tiles + tile) * DK + i] = acc;
 }
@@ -1024,9 +1027,10 @@ __global__ void gla_dlog_finalize_kernel(const bf16 *__restrict__ q, const float
     float run = fs ? fs[bh * DK + i] : 0.f;
     for (int j = n_tiles - 1; j > tile; --j) run += tsum[(bh * n_tiles + j) * DK + i];
     const long long t0 = (long long)tile * kGlaDlTile;
+#pragma unroll 8
     for (long long t = min(t0 + kGlaDlTile, T) - 1; t >= t0; --t) {
         const size_t x = (bh * T + t) * DK + i;
-        run += __bfloat162float(q[x]) * dq[x] - __bfloat162float(k[x]) * dk[x];
+        run += __bfloat162float(__ldg(q + x)) * __ldg(dq + x) - __bfloat162float(__ldg(k + x)) * __ldg(dk + x);
         dlog[x] = run;
     }
 }
