@@ -71,6 +71,8 @@ def lib():
                 "cla_decay_total": ([P, P, I64, I64, I64, P], INT),
                 "cla_delta_workspace_size": ([I64] * 5 + [INT], SZ),
                 "cla_delta_fwd": ([P] * 8 + [I64] * 5 + [INT, P, SZ, P], INT),
+                "cla_delta_bwd_workspace_size": ([I64] * 5 + [INT], SZ),
+                "cla_delta_bwd": ([P] * 14 + [I64] * 5 + [INT, P, SZ, P], INT),
                 "cla_state_compose": ([P] * 4 + [I64] * 7 + [P], INT),
             }
             for name, (args, res) in sig.items():
@@ -410,6 +412,34 @@ def gla_fwd(q, k, v, log_decay, S0=None, *, chunk=64, o=None, ST=None, workspace
     return o, ST
 
 
+def delta_bwd_workspace_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
+    return int(lib().cla_delta_bwd_workspace_size(B, H, T, dim_k, dim_v, int(chunk)))
+
+
+def delta_bwd(q, k, v, log_decay, beta, S0, dO, dST=None, *, chunk=64, dq=None, dk=None, dv=None,
+              dlog_decay=None, dbeta=None, dS0=None, workspace=None, stream=None):
+    """Adjoint of delta_fwd (dO bf16 [B, H, T, dv]); returns (dq, dk, dv, dlog_decay, dbeta, dS0)."""
+    B, H, T, dkk = _dims(q, 4, "q")
+    dvv = _dims(v, 4, "v")[3]
+    dev = q.device
+    f32, bf16 = torch.float32, torch.bfloat16
+    dq = _out(dq, (B, H, T, dkk), f32, dev)
+    dk = _out(dk, (B, H, T, dkk), f32, dev)
+    dv = _out(dv, (B, H, T, dvv), f32, dev)
+    dlog_decay = _out(dlog_decay, (B, H, T), f32, dev)
+    dbeta = _out(dbeta, (B, H, T), f32, dev)
+    dS0 = _out(dS0, (B, H, dkk, dvv), f32, dev)
+    ws = _ws(delta_bwd_workspace_size(B, H, T, dkk, dvv, chunk), dev, workspace)
+    tk, tv, st, bht = (B, H, T, dkk), (B, H, T, dvv), (B, H, dkk, dvv), (B, H, T)
+    _launch("cla_delta_bwd", dev, (
+        _T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
+        _T(log_decay, f32, "log_decay", bht), _T(beta, f32, "beta", bht), _T(S0, f32, "S0", st),
+        _T(dO, bf16, "dO", tv), _T(dST, f32, "dST", st), _T(dq, f32, "dq", tk), _T(dk, f32, "dk", tk),
+        _T(dv, f32, "dv", tv), _T(dlog_decay, f32, "dlog_decay", bht), _T(dbeta, f32, "dbeta", bht),
+        _T(dS0, f32, "dS0", st), B, H, T, dkk, dvv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws)), stream)
+    return dq, dk, dv, dlog_decay, dbeta, dS0
+
+
 def gla_bwd_workspace_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
     return int(lib().cla_gla_bwd_workspace_size(B, H, T, dim_k, dim_v, int(chunk)))
 
@@ -491,3 +521,31 @@ def delta_fwd(q, k, v, log_decay, beta, S0=None, *, chunk=64, o=None, ST=None, w
         _T(o, f32, "o", tv), _T(ST, f32, "ST", st),
         B, H, T, dk, dv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws)), stream)
     return o, ST
+
+
+def delta_bwd_workspace_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
+    return int(lib().cla_delta_bwd_workspace_size(B, H, T, dim_k, dim_v, int(chunk)))
+
+
+def delta_bwd(q, k, v, log_decay, beta, S0, dO, dST=None, *, chunk=64, dq=None, dk=None, dv=None,
+              dlog_decay=None, dbeta=None, dS0=None, workspace=None, stream=None):
+    """Adjoint of delta_fwd (dO bf16 [B, H, T, dv]); returns (dq, dk, dv, dlog_decay, dbeta, dS0)."""
+    B, H, T, dkk = _dims(q, 4, "q")
+    dvv = _dims(v, 4, "v")[3]
+    dev = q.device
+    f32, bf16 = torch.float32, torch.bfloat16
+    dq = _out(dq, (B, H, T, dkk), f32, dev)
+    dk = _out(dk, (B, H, T, dkk), f32, dev)
+    dv = _out(dv, (B, H, T, dvv), f32, dev)
+    dlog_decay = _out(dlog_decay, (B, H, T), f32, dev)
+    dbeta = _out(dbeta, (B, H, T), f32, dev)
+    dS0 = _out(dS0, (B, H, dkk, dvv), f32, dev)
+    ws = _ws(delta_bwd_workspace_size(B, H, T, dkk, dvv, chunk), dev, workspace)
+    tk, tv, st, bht = (B, H, T, dkk), (B, H, T, dvv), (B, H, dkk, dvv), (B, H, T)
+    _launch("cla_delta_bwd", dev, (
+        _T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
+        _T(log_decay, f32, "log_decay", bht), _T(beta, f32, "beta", bht), _T(S0, f32, "S0", st),
+        _T(dO, bf16, "dO", tv), _T(dST, f32, "dST", st), _T(dq, f32, "dq", tk), _T(dk, f32, "dk", tk),
+        _T(dv, f32, "dv", tv), _T(dlog_decay, f32, "dlog_decay", bht), _T(dbeta, f32, "dbeta", bht),
+        _T(dS0, f32, "dS0", st), B, H, T, dkk, dvv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws)), stream)
+    return dq, dk, dv, dlog_decay, dbeta, dS0

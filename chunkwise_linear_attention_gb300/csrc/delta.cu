@@ -30,6 +30,8 @@
 //
 // Range: finite log decays (no exact-zero gates).  A chunk with a non-finite
 // log decay or gate strength sets an error flag that cla_check_status reports.
+#include <algorithm>
+
 #include "cla_internal.cuh"
 #include "mma_sync.cuh"
 
@@ -79,7 +81,8 @@ struct DeltaArgs {
     const bf16 *q, *k, *v;
     const float *g, *beta;  // [BH][T]
     const float *S0;        // [BH][DK][DV] or NULL
-    float *o, *ST;
+    float *o, *ST;          // o NULL: the output is not formed (the backward's states pass)
+    float *states;          // [BH][n_chunks][DK][DV], the state entering every chunk, or NULL
     int BH, DV, nzb, n_chunks;
     long long T;
     WsHeader *hdr;
@@ -188,6 +191,17 @@ __global__ void __launch_bounds__(kDlThreads, 2) delta_fwd_kernel(const DeltaArg
         const float *ls = reinterpret_cast<const float *>(st + C::OFF_L);
         const float *bs = reinterpret_cast<const float *>(st + C::OFF_B);
         const long long t0 = (long long)i * kDlTc;
+        if (p.states != nullptr) {  // the state entering chunk i, for the backward
+            float *sg = p.states + ((size_t)bh * p.n_chunks + i) * DK * p.DV + zb * 64;
+#pragma unroll
+            for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+                for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        __stcg(reinterpret_cast<float2 *>(sg + (size_t)s_row(mi, h) * p.DV + nj * 8 + 2 * tq),
+                               make_float2(S[mi][nj][2 * h], S[mi][nj][2 * h + 1]));
+        }
         cp_async_wait<0>();
         __syncthreads();
         // ---- in-chunk log2 decays (warp 0) and the state's bf16 parts (everyone)
@@ -337,7 +351,7 @@ __global__ void __launch_bounds__(kDlThreads, 2) delta_fwd_kernel(const DeltaArg
         __syncthreads();
 
         // ---- O = diag(gamma) Q S + ((Q K^T) . D) Veff
-        {
+        if (p.o != nullptr) {
             float O[8][4], P[8][4];
             zero8(O);
             zero8(P);
@@ -466,6 +480,906 @@ int launch_delta_fwd(const DeltaArgs &a, cudaStream_t s, unsigned int grid) {
     return check_launch("delta_fwd_kernel");
 }
 
+// Operand loaders of m16n8k16 from XOR-swizzled row-major tiles (RB bytes per row).
+// A operand: 16 rows from row0, k-step kk, of the tile itself.
+template <int RB>
+__device__ __forceinline__ void lda_rows(uint32_t (&a)[4], const uint8_t *t, int row0, int kk, int lane) {
+    ldsm_x4(smem_u32(t + swz<RB>(row0 + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * kk + (lane >> 4))), a);
+}
+// A operand: rows 16 mt.. of the transpose of a tile stored [k][m], k-step kk.
+template <int RB>
+__device__ __forceinline__ void lda_trans(uint32_t (&a)[4], const uint8_t *t, int mt, int kk, int lane) {
+    ldsm_x4_t(smem_u32(t + swz<RB>(kk * 16 + (lane & 7) + (lane >> 4) * 8, 2 * mt + ((lane >> 3) & 1))), a);
+}
+// B operands of the n-tiles 2pp and 2pp + 1 at k-step kk, B[k][n] = tile[n][k].
+template <int RB>
+__device__ __forceinline__ void ldb_nk(uint32_t (&b)[4], const uint8_t *t, int pp, int kk, int lane) {
+    ldsm_x4(smem_u32(t + swz<RB>(16 * pp + (lane & 7) + (lane >> 4) * 8, 2 * kk + ((lane >> 3) & 1))), b);
+}
+// The same with B[k][n] = tile[k][n].
+template <int RB>
+__device__ __forceinline__ void ldb_kn(uint32_t (&b)[4], const uint8_t *t, int pp, int kk, int lane) {
+    ldsm_x4_t(smem_u32(t + swz<RB>(kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * pp + (lane >> 4))), b);
+}
+template <int N>
+__device__ __forceinline__ void mma_pair(float (&F)[N][4], int pp, const uint32_t (&a)[4], const uint32_t (&b)[4]) {
+    mma16816(F[2 * pp], a, b[0], b[1]);
+    mma16816(F[2 * pp + 1], a, b[2], b[3]);
+}
+// Sum over the four lanes of a quad (the lanes holding one accumulator row).
+__device__ __forceinline__ float quad_sum(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+
+// ------------------------------------------------------------------ backward
+// The adjoint of the chunk form, chunks of a head in reverse, from the state
+// entering every chunk (written by the forward kernel's states pass).  Per
+// chunk, with P = (Q K^T) . D, E_rs = D_rs k_r . k_s (s < r), A = diag(beta) E,
+// U = (I + A)^-1 X, w_r = gamma_L / gamma_r and dS' the adjoint of the state
+// leaving the chunk:
+//     dU = P^T dO + diag(w) K dS'          dX = (I + A)^-T dU     dV = diag(beta) dX
+//     dP = dO U^T (s <= r)                 dA = -dX U^T (s < r)   F  = diag(beta) dA . D
+//     dQ = (dP . D) K + diag(gamma) dO S^T
+//     dK = (dP . D)^T Q + (F + F^T) K + diag(w) U dS'^T - diag(beta gamma) dX S^T
+//     dbeta_r = (V - diag(gamma) K S)_r . dX_r + sum_s dA_rs E_rs
+//     dS = gamma_L dS' + Q^T diag(gamma) dO - K^T diag(beta gamma) dX
+// and the gradient on the in-chunk log-decay sums c: every decay ratio
+// exp(c_r - c_s) differentiated in c (row sums minus column sums of
+// dP . P and dA . A), gamma_r q_r . (dO S^T)_r, -beta_r gamma_r (K S)_r . dX_r,
+// -w_r (K dS')_r . U_r, and at the chunk's last position
+// sum_r w_r (K dS')_r . U_r + gamma_L <S, dS'>; its suffix sums inside the
+// chunk are the gradient on each token's log decay.
+//
+// One block per (head, 64 value columns), 4 warps, warp w the chunk's rows
+// 16w..16w+15; the adjoint state dS [DK][64] in registers like the forward's
+// state.  dQ, dK, dbeta and dlog_a sum over the value-column blocks: the block
+// of columns 0..63 writes them to the outputs, the others to workspace
+// partials that delta_bwd_reduce_kernel adds.  dV and dS0 belong to one block.
+template <int DK>
+struct DeltaBwdCfg {
+    static constexpr int QRB = DK * 2;  // bytes per Q / K row
+    static constexpr int VRB = 128;     // bytes per row of a [..][64] bf16 tile
+    static constexpr int Q_BYTES = kDlTc * QRB;
+    static constexpr int V_BYTES = kDlTc * VRB;
+    static constexpr int S_BYTES = DK * VRB;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + Q_BYTES;
+    static constexpr int OFF_V = OFF_K + Q_BYTES;
+    static constexpr int OFF_DO = OFF_V + V_BYTES;
+    static constexpr int OFF_L = OFF_DO + V_BYTES;   // log decays [64]
+    static constexpr int OFF_B = OFF_L + 256;        // gate strengths [64]
+    static constexpr int OFF_C = OFF_B + 256;        // in-chunk log2 decays c_r [64]
+    static constexpr int OFF_SH = OFF_C + 256;       // S entering the chunk, two bf16 parts [DK][64]
+    static constexpr int OFF_SL = OFF_SH + S_BYTES;
+    static constexpr int OFF_GH = OFF_SL + S_BYTES;  // dS' (adjoint of the state leaving it), two parts
+    static constexpr int OFF_GL = OFF_GH + S_BYTES;
+    static constexpr int OFF_E = OFF_GL + S_BYTES;   // E fp32 [64][65]; then F as two parts
+    static constexpr int E_BYTES = kDlTc * (kDlTc + 1) * 4;
+    static constexpr int OFF_FH = OFF_E;
+    static constexpr int OFF_FL = OFF_E + V_BYTES;
+    static constexpr int OFF_TH = OFF_E + E_BYTES;   // (I + A)^-1; then diag(gamma) dO (two parts each)
+    static constexpr int OFF_TL = OFF_TH + V_BYTES;
+    static constexpr int OFF_XH = OFF_TL + V_BYTES;  // X; then dU; then dP . D
+    static constexpr int OFF_XL = OFF_XH + V_BYTES;
+    static constexpr int OFF_UH = OFF_XL + V_BYTES;  // U
+    static constexpr int OFF_UL = OFF_UH + V_BYTES;
+    static constexpr int OFF_WH = OFF_UL + V_BYTES;  // diag(w) U
+    static constexpr int OFF_WL = OFF_WH + V_BYTES;
+    static constexpr int OFF_ZH = OFF_WL + V_BYTES;  // -diag(beta gamma) dX
+    static constexpr int OFF_ZL = OFF_ZH + V_BYTES;
+    static constexpr int OFF_ROW = OFF_ZL + V_BYTES;  // row parts of the gradient on c [64]
+    static constexpr int OFF_COL = OFF_ROW + 256;     // column parts, one row per warp [4][64]
+    static constexpr int OFF_DB = OFF_COL + 1024;     // dbeta [64]
+    static constexpr int OFF_RED = OFF_DB + 256;      // the last position's extra term, per warp [4]
+    static constexpr int SMEM = OFF_RED + 64;
+    static constexpr int S_MT = DK / 64;
+    static_assert(2 * V_BYTES <= E_BYTES, "F fits where E was");
+    static_assert(E_BYTES % 128 == 0, "tiles after E stay 128-byte aligned");
+    static_assert(SMEM + 1024 <= 227 * 1024, "one block per SM");
+};
+
+struct DeltaBwdArgs {
+    const bf16 *q, *k, *v, *dO;
+    const float *g, *beta;  // [BH][T]
+    const float *dST;       // [BH][DK][DV] or NULL
+    const float *states;    // [BH][n_chunks][DK][DV]
+    float *dq, *dk, *dv, *dlog, *dbeta, *dS0;
+    float *part;            // partials of the column blocks 1.. (NULL when DV == 64)
+    long long part_stride;  // floats per column block: BH T (2 DK + 2)
+    int BH, DV, nzb, n_chunks;
+    long long T;
+};
+
+template <int DK>
+__global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwdArgs p) {
+    using C = DeltaBwdCfg<DK>;
+    constexpr int S_MT = C::S_MT;
+    constexpr int NQ = DK / 8;  // 8-column tiles of a [..][DK] output
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    const int bh = blockIdx.x / p.nzb, zb = blockIdx.x % p.nzb;
+    const size_t tok0 = (size_t)bh * p.T;
+    const bf16 *Qb = p.q + tok0 * DK;
+    const bf16 *Kb = p.k + tok0 * DK;
+    const bf16 *Vb = p.v + tok0 * p.DV + zb * 64;
+    const bf16 *dOb = p.dO + tok0 * p.DV + zb * 64;
+    const float *Lb = p.g + tok0;
+    const float *Bb = p.beta + tok0;
+    float *dq_out, *dk_out, *dl_out, *db_out;
+    if (zb == 0) {
+        dq_out = p.dq + tok0 * DK;
+        dk_out = p.dk + tok0 * DK;
+        dl_out = p.dlog + tok0;
+        db_out = p.dbeta + tok0;
+    } else {
+        float *base = p.part + (size_t)(zb - 1) * p.part_stride;
+        const size_t ntok = (size_t)p.BH * p.T;
+        dq_out = base + tok0 * DK;
+        dk_out = base + ntok * DK + tok0 * DK;
+        dl_out = base + 2 * ntok * DK + tok0;
+        db_out = base + 2 * ntok * DK + ntok + tok0;
+    }
+    float *Em = reinterpret_cast<float *>(smem + C::OFF_E);
+    float *cs = reinterpret_cast<float *>(smem + C::OFF_C);
+    const float *ls = reinterpret_cast<const float *>(smem + C::OFF_L);
+    const float *bs = reinterpret_cast<const float *>(smem + C::OFF_B);
+    float *rowp = reinterpret_cast<float *>(smem + C::OFF_ROW);
+    float *colp = reinterpret_cast<float *>(smem + C::OFF_COL);
+    float *dbs = reinterpret_cast<float *>(smem + C::OFF_DB);
+    float *red = reinterpret_cast<float *>(smem + C::OFF_RED);
+
+    auto load_stage = [&](int chunk) {
+        const long long t0 = (long long)chunk * kDlTc;
+        constexpr int QC = C::QRB / 16;
+        for (int i = tid; i < kDlTc * QC; i += kDlThreads) {
+            const int row = i / QC, c16 = i % QC;
+            const long long t = t0 + row;
+            const bool ok = t < p.T;
+            const size_t off = (size_t)(ok ? t : 0) * DK + c16 * 8;
+            cp_async16(smem_u32(smem + C::OFF_Q + swz<C::QRB>(row, c16)), Qb + off, ok ? 16u : 0u);
+            cp_async16(smem_u32(smem + C::OFF_K + swz<C::QRB>(row, c16)), Kb + off, ok ? 16u : 0u);
+        }
+        for (int i = tid; i < kDlTc * 8; i += kDlThreads) {
+            const int row = i >> 3, c16 = i & 7;
+            const long long t = t0 + row;
+            const bool ok = t < p.T;
+            const size_t off = (size_t)(ok ? t : 0) * p.DV + c16 * 8;
+            cp_async16(smem_u32(smem + C::OFF_V + swz<C::VRB>(row, c16)), Vb + off, ok ? 16u : 0u);
+            cp_async16(smem_u32(smem + C::OFF_DO + swz<C::VRB>(row, c16)), dOb + off, ok ? 16u : 0u);
+        }
+        for (int i = tid; i < kDlTc; i += kDlThreads) {  // padding tokens: no decay, no write
+            const long long t = t0 + i;
+            const bool ok = t < p.T;
+            cp_async4(smem_u32(smem + C::OFF_L + i * 4), Lb + (ok ? t : 0), ok ? 4u : 0u);
+            cp_async4(smem_u32(smem + C::OFF_B + i * 4), Bb + (ok ? t : 0), ok ? 4u : 0u);
+        }
+        // the state entering the chunk, fp32 -> two bf16 parts (plain loads, read once)
+        const float *sg = p.states + ((size_t)bh * p.n_chunks + chunk) * DK * p.DV + zb * 64;
+        for (int i = tid; i < DK * 16; i += kDlThreads) {
+            const int row = i >> 4, c4 = i & 15;
+            const float4 x = __ldcs(reinterpret_cast<const float4 *>(sg + (size_t)row * p.DV + c4 * 4));
+            uint2 hi, lo;
+            split_bf16x2(make_float2(x.x, x.y), hi.x, lo.x);
+            split_bf16x2(make_float2(x.z, x.w), hi.y, lo.y);
+            const uint32_t off = swz<C::VRB>(row, c4 >> 1) + (c4 & 1) * 8;
+            *reinterpret_cast<uint2 *>(smem + C::OFF_SH + off) = hi;
+            *reinterpret_cast<uint2 *>(smem + C::OFF_SL + off) = lo;
+        }
+    };
+
+    // adjoint state fragments: warp w owns rows 16(w S_MT + mi) + {g, g + 8}
+    float dS[S_MT][8][4];
+    auto s_row = [&](int mi, int h) { return (warp * S_MT + mi) * 16 + g + 8 * h; };
+#pragma unroll
+    for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                dS[mi][nj][e] = p.dST ? __ldg(p.dST + ((size_t)bh * DK + s_row(mi, e >> 1)) * p.DV + zb * 64 +
+                                              nj * 8 + 2 * tq + (e & 1))
+                                      : 0.f;
+    auto zero8 = [&](float (&F)[8][4]) {
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) F[nj][e] = 0.f;
+    };
+    // a [64][64] tile of fp32 fragments (this warp's 16 rows) into two bf16 tiles, [row][col]
+    auto store_parts = [&](const float (&F)[8][4], int off_hi, int off_lo) {
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = warp * 16 + g + 8 * h, col = nj * 8 + 2 * tq;
+                const uint32_t off = swz<C::VRB>(row, col >> 3) + (col & 7) * 2;
+                uint32_t hi, lo;
+                split_bf16x2(make_float2(F[nj][2 * h], F[nj][2 * h + 1]), hi, lo);
+                *reinterpret_cast<uint32_t *>(smem + off_hi + off) = hi;
+                *reinterpret_cast<uint32_t *>(smem + off_lo + off) = lo;
+            }
+    };
+    // an fp32 pair at (row, col) of a [..][64] tile held as two bf16 parts
+    auto read_parts = [&](int off_hi, int off_lo, int row, int col) {
+        const uint32_t off = swz<C::VRB>(row, col >> 3) + (col & 7) * 2;
+        const float2 h = unpack_bf16(*reinterpret_cast<const uint32_t *>(smem + off_hi + off));
+        const float2 l = unpack_bf16(*reinterpret_cast<const uint32_t *>(smem + off_lo + off));
+        return make_float2(h.x + l.x, h.y + l.y);
+    };
+    auto bf_pair = [&](int off, int rb_row_bytes, int row, int col) {  // a bf16 pair of an input tile
+        const uint32_t o = (rb_row_bytes == C::QRB ? swz<C::QRB>(row, col >> 3) : swz<C::VRB>(row, col >> 3)) +
+                           (col & 7) * 2;
+        return unpack_bf16(*reinterpret_cast<const uint32_t *>(smem + off + o));
+    };
+
+    const uint8_t *sQ = smem + C::OFF_Q, *sK = smem + C::OFF_K, *sV = smem + C::OFF_V, *sdO = smem + C::OFF_DO;
+    constexpr int QRB = C::QRB, VRB = C::VRB;
+    constexpr int KQ = DK / 16;  // k-steps over the key dimension
+
+    load_stage(p.n_chunks - 1);
+    cp_async_commit();
+    for (int i = p.n_chunks - 1; i >= 0; --i) {
+        const long long t0 = (long long)i * kDlTc;
+        // dS' (the adjoint of the state leaving chunk i) as two bf16 parts
+#pragma unroll
+        for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+            for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = s_row(mi, h), col = nj * 8 + 2 * tq;
+                    const uint32_t off = swz<VRB>(row, col >> 3) + (col & 7) * 2;
+                    uint32_t hi, lo;
+                    split_bf16x2(make_float2(dS[mi][nj][2 * h], dS[mi][nj][2 * h + 1]), hi, lo);
+                    *reinterpret_cast<uint32_t *>(smem + C::OFF_GH + off) = hi;
+                    *reinterpret_cast<uint32_t *>(smem + C::OFF_GL + off) = lo;
+                }
+        cp_async_wait<0>();
+        __syncthreads();
+        // ---- in-chunk log2 decays (warp 0); this thread's share of <S, dS'>
+        if (warp == 0) {
+            const float v0 = ls[2 * lane] * kDlLog2e;
+            const float v1 = v0 + ls[2 * lane + 1] * kDlLog2e;
+            float tot = v1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, tot, off);
+                if (lane >= off) tot += o;
+            }
+            const float ex = tot - v1;
+            cs[2 * lane] = ex + v0;
+            cs[2 * lane + 1] = ex + v1;
+        }
+        float sd = 0.f;
+#pragma unroll
+        for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+            for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float2 s = read_parts(C::OFF_SH, C::OFF_SL, s_row(mi, h), nj * 8 + 2 * tq);
+                    sd += s.x * dS[mi][nj][2 * h] + s.y * dS[mi][nj][2 * h + 1];
+                }
+        __syncthreads();
+        const float cL = cs[kDlTc - 1];
+        int rr[2];  // this thread's two rows of the chunk
+        rr[0] = warp * 16 + g;
+        rr[1] = rr[0] + 8;
+
+        // ---- E = strictly lower (2^(c_r - c_s) k_r . k_s), this warp's rows
+        {
+            float F[8][4];
+            zero8(F);
+#pragma unroll 2
+            for (int kk = 0; kk < KQ; ++kk) {
+                uint32_t a[4];
+                lda_rows<QRB>(a, sK, warp * 16, kk, lane);
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {
+                    uint32_t b[4];
+                    ldb_nk<QRB>(b, sK, pp, kk, lane);
+                    mma_pair(F, pp, a, b);
+                }
+            }
+#pragma unroll
+            for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = rr[e >> 1], s = nj * 8 + 2 * tq + (e & 1);
+                    Em[r * (kDlTc + 1) + s] = (s < r) ? ex2(cs[r] - cs[s]) * F[nj][e] : 0.f;
+                }
+        }
+        __syncthreads();
+        // ---- (I + A)^-1 by forward substitution (threads 0..63, one column each), while every
+        // warp forms K S, Yv = V - diag(gamma) K S and X = diag(beta) Yv for its rows
+        if (tid < kDlTc) {
+            const int j = tid;
+            float tc[kDlTc];
+#pragma unroll
+            for (int r = 0; r < kDlTc; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 < r; ++s2) acc = fmaf(Em[r * (kDlTc + 1) + s2], tc[s2], acc);
+                tc[r] = (r < j) ? 0.f : (r == j ? 1.f : -bs[r] * acc);
+            }
+#pragma unroll
+            for (int r = 0; r < kDlTc; ++r) {
+                const uint32_t off = swz<VRB>(r, j >> 3) + (j & 7) * 2;
+                const uint32_t bits = __float_as_uint(tc[r]) & 0xffff0000u;
+                const float rest = tc[r] - __uint_as_float(bits);  // exact
+                *reinterpret_cast<uint16_t *>(smem + C::OFF_TH + off) = (uint16_t)(bits >> 16);
+                *reinterpret_cast<uint16_t *>(smem + C::OFF_TL + off) = (uint16_t)(__float_as_uint(rest) >> 16);
+            }
+        }
+        float Yv[8][4];
+        {
+            zero8(Yv);
+#pragma unroll 2
+            for (int kk = 0; kk < KQ; ++kk) {
+                uint32_t a[4];
+                lda_rows<QRB>(a, sK, warp * 16, kk, lane);
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {
+                    uint32_t sh[4], sl[4];
+                    ldb_kn<VRB>(sh, smem + C::OFF_SH, pp, kk, lane);
+                    ldb_kn<VRB>(sl, smem + C::OFF_SL, pp, kk, lane);
+                    mma_pair(Yv, pp, a, sh);
+                    mma_pair(Yv, pp, a, sl);
+                }
+            }
+            float X[8][4];
+#pragma unroll
+            for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int r = rr[h];
+                    const float2 vv = bf_pair(C::OFF_V, VRB, r, nj * 8 + 2 * tq);
+                    const float gm = ex2(cs[r]), bt = bs[r];
+                    Yv[nj][2 * h] = vv.x - gm * Yv[nj][2 * h];
+                    Yv[nj][2 * h + 1] = vv.y - gm * Yv[nj][2 * h + 1];
+                    X[nj][2 * h] = bt * Yv[nj][2 * h];
+                    X[nj][2 * h + 1] = bt * Yv[nj][2 * h + 1];
+                }
+            store_parts(X, C::OFF_XH, C::OFF_XL);
+        }
+        __syncthreads();
+        // ---- U = (I + A)^-1 X (three products); U and diag(w) U as bf16 parts
+        {
+            float U[8][4];
+            zero8(U);
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt) {
+                uint32_t th[4], tl[4];
+                lda_rows<VRB>(th, smem + C::OFF_TH, warp * 16, kt, lane);
+                lda_rows<VRB>(tl, smem + C::OFF_TL, warp * 16, kt, lane);
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {
+                    uint32_t xh[4], xl[4];
+                    ldb_kn<VRB>(xh, smem + C::OFF_XH, pp, kt, lane);
+                    ldb_kn<VRB>(xl, smem + C::OFF_XL, pp, kt, lane);
+                    mma_pair(U, pp, th, xh);
+                    mma_pair(U, pp, th, xl);
+                    mma_pair(U, pp, tl, xh);
+                }
+            }
+            store_parts(U, C::OFF_UH, C::OFF_UL);
+#pragma unroll
+            for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float w = ex2(cL - cs[rr[h]]);
+                    U[nj][2 * h] *= w;
+                    U[nj][2 * h + 1] *= w;
+                }
+            store_parts(U, C::OFF_WH, C::OFF_WL);
+        }
+        __syncthreads();
+
+        // ---- dU = P^T dO + diag(w) K dS' for this warp's rows s; e_s = w_s (K dS')_s . U_s
+        float rt[2];      // the row part of the gradient on c (quad sums: each lane of a quad holds it)
+        float esum = 0.f;  // sum of e over this thread's rows (counted once per quad)
+        {
+            float D[8][4];
+            zero8(D);
+#pragma unroll 2
+            for (int kk = 0; kk < KQ; ++kk) {
+                uint32_t a[4];
+                lda_rows<QRB>(a, sK, warp * 16, kk, lane);
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {
+                    uint32_t gh[4], gl[4];
+                    ldb_kn<VRB>(gh, smem + C::OFF_GH, pp, kk, lane);
+                    ldb_kn<VRB>(gl, smem + C::OFF_GL, pp, kk, lane);
+                    mma_pair(D, pp, a, gh);
+                    mma_pair(D, pp, a, gl);
+                }
+            }
+            float eu[2] = {0.f, 0.f};
+#pragma unroll
+            for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float2 u = read_parts(C::OFF_UH, C::OFF_UL, rr[h], nj * 8 + 2 * tq);
+                    eu[h] += D[nj][2 * h] * u.x + D[nj][2 * h + 1] * u.y;
+                }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float w = ex2(cL - cs[rr[h]]);
+                const float e = w * quad_sum(eu[h]);
+                rt[h] = -e;
+                esum += (tq == 0) ? e : 0.f;
+#pragma unroll
+                for (int nj = 0; nj < 8; ++nj) {
+                    D[nj][2 * h] *= w;
+                    D[nj][2 * h + 1] *= w;
+                }
+            }
+            // P^T for this warp's rows s: (K Q^T)_sr 2^(c_r - c_s) for r >= s, as A fragments
+            uint32_t ph[4][4], pl[4][4];
+            {
+                float Pt[8][4];
+                zero8(Pt);
+#pragma unroll 2
+                for (int kk = 0; kk < KQ; ++kk) {
+                    uint32_t a[4];
+                    lda_rows<QRB>(a, sK, warp * 16, kk, lane);
+#pragma unroll
+                    for (int pp = 0; pp < 4; ++pp) {
+                        uint32_t b[4];
+                        ldb_nk<QRB>(b, sQ, pp, kk, lane);
+                        mma_pair(Pt, pp, a, b);
+                    }
+                }
+#pragma unroll
+                for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int s = rr[h], r0 = nj * 8 + 2 * tq;
+                        const float x0 = (r0 >= s) ? Pt[nj][2 * h] * ex2(cs[r0] - cs[s]) : 0.f;
+                        const float x1 = (r0 + 1 >= s) ? Pt[nj][2 * h + 1] * ex2(cs[r0 + 1] - cs[s]) : 0.f;
+                        split_bf16x2(make_float2(x0, x1), ph[nj >> 1][(nj & 1) * 2 + h], pl[nj >> 1][(nj & 1) * 2 + h]);
+                    }
+            }
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt)
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {
+                    uint32_t b[4];
+                    ldb_kn<VRB>(b, sdO, pp, kt, lane);
+                    mma_pair(D, pp, ph[kt], b);
+                    mma_pair(D, pp, pl[kt], b);
+                }
+            store_parts(D, C::OFF_XH, C::OFF_XL);  // X is dead: every warp has formed U
+        }
+        __syncthreads();
+        // ---- dX = (I + A)^-T dU; dV; the dots with Yv and V; Zk = -diag(beta gamma) dX
+        uint32_t xh[4][4], xl[4][4];  // dX as A fragments
+        float dbr[2];
+        {
+            float F[8][4];
+            zero8(F);
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt) {
+                uint32_t th[4], tl[4];
+                lda_trans<VRB>(th, smem + C::OFF_TH, warp, kt, lane);
+                lda_trans<VRB>(tl, smem + C::OFF_TL, warp, kt, lane);
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {
+                    uint32_t dh[4], dl[4];
+                    ldb_kn<VRB>(dh, smem + C::OFF_XH, pp, kt, lane);
+                    ldb_kn<VRB>(dl, smem + C::OFF_XL, pp, kt, lane);
+                    mma_pair(F, pp, th, dh);
+                    mma_pair(F, pp, th, dl);
+                    mma_pair(F, pp, tl, dh);
+                }
+            }
+            float ydx[2] = {0.f, 0.f}, vdx[2] = {0.f, 0.f};
+#pragma unroll
+            for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int r = rr[h], col = nj * 8 + 2 * tq;
+                    const long long t = t0 + r;
+                    const float bt = bs[r];
+                    if (t < p.T)
+                        *reinterpret_cast<float2 *>(p.dv + (tok0 + t) * p.DV + zb * 64 + col) =
+                            make_float2(bt * F[nj][2 * h], bt * F[nj][2 * h + 1]);
+                    const float2 vv = bf_pair(C::OFF_V, VRB, r, col);
+                    ydx[h] += Yv[nj][2 * h] * F[nj][2 * h] + Yv[nj][2 * h + 1] * F[nj][2 * h + 1];
+                    vdx[h] += vv.x * F[nj][2 * h] + vv.y * F[nj][2 * h + 1];
+                    split_bf16x2(make_float2(F[nj][2 * h], F[nj][2 * h + 1]), xh[nj >> 1][(nj & 1) * 2 + h],
+                                 xl[nj >> 1][(nj & 1) * 2 + h]);
+                }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = rr[h];
+                const float y = quad_sum(ydx[h]), vx = quad_sum(vdx[h]);
+                rt[h] -= bs[r] * (vx - y);
+                dbr[h] = y;
+                const float m = -bs[r] * ex2(cs[r]);
+#pragma unroll
+                for (int nj = 0; nj < 8; ++nj) {
+                    F[nj][2 * h] *= m;
+                    F[nj][2 * h + 1] *= m;
+                }
+            }
+            store_parts(F, C::OFF_ZH, C::OFF_ZL);
+        }
+        __syncthreads();  // every warp has read (I + A)^-1 and dU
+        // ---- dP = dO U^T (s <= r) with P = (Q K^T) . D; G1 = dP . D; Zq = diag(gamma) dO
+        float rowm[2] = {0.f, 0.f};
+        float colacc[8][2];
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj) colacc[nj][0] = colacc[nj][1] = 0.f;
+        {
+            float dP[8][4], P[8][4];
+            zero8(dP);
+            zero8(P);
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt) {
+                uint32_t a[4];
+                lda_rows<VRB>(a, sdO, warp * 16, kt, lane);
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {
+                    uint32_t uh[4], ul[4];
+                    ldb_nk<VRB>(uh, smem + C::OFF_UH, pp, kt, lane);
+                    ldb_nk<VRB>(ul, smem + C::OFF_UL, pp, kt, lane);
+                    mma_pair(dP, pp, a, uh);
+                    mma_pair(dP, pp, a, ul);
+                }
+            }
+#pragma unroll 2
+            for (int kk = 0; kk < KQ; ++kk) {
+                uint32_t a[4];
+                lda_rows<QRB>(a, sQ, warp * 16, kk, lane);
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {
+                    uint32_t b[4];
+                    ldb_nk<QRB>(b, sK, pp, kk, lane);
+                    mma_pair(P, pp, a, b);
+                }
+            }
+#pragma unroll
+            for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = rr[e >> 1], s = nj * 8 + 2 * tq + (e & 1);
+                    if (s <= r) {
+                        const float d = ex2(cs[r] - cs[s]);
+                        const float m1 = dP[nj][e] * P[nj][e] * d;
+                        rowm[e >> 1] += m1;
+                        colacc[nj][e & 1] += m1;
+                        dP[nj][e] *= d;
+                    } else {
+                        dP[nj][e] = 0.f;
+                    }
+                }
+            store_parts(dP, C::OFF_XH, C::OFF_XL);
+#pragma unroll
+            for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float2 vv = bf_pair(C::OFF_DO, VRB, rr[h], nj * 8 + 2 * tq);
+                    const float gm = ex2(cs[rr[h]]);
+                    P[nj][2 * h] = gm * vv.x;
+                    P[nj][2 * h + 1] = gm * vv.y;
+                }
+            store_parts(P, C::OFF_TH, C::OFF_TL);  // Zq, where (I + A)^-1 was
+        }
+        // ---- dA = -dX U^T (s < r); dbeta and the gradient on c; F = diag(beta) dA . D
+        float Fm[8][4];
+        float dba[2] = {0.f, 0.f};
+        {
+            zero8(Fm);
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt)
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {
+                    uint32_t uh[4], ul[4];
+                    ldb_nk<VRB>(uh, smem + C::OFF_UH, pp, kt, lane);
+                    ldb_nk<VRB>(ul, smem + C::OFF_UL, pp, kt, lane);
+                    mma_pair(Fm, pp, xh[kt], uh);
+                    mma_pair(Fm, pp, xh[kt], ul);
+                    mma_pair(Fm, pp, xl[kt], uh);
+                }
+#pragma unroll
+            for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = rr[e >> 1], s = nj * 8 + 2 * tq + (e & 1);
+                    if (s < r) {
+                        const float Ers = Em[r * (kDlTc + 1) + s];
+                        const float dA = -Fm[nj][e], bt = bs[r];
+                        dba[e >> 1] += dA * Ers;
+                        const float m2 = dA * bt * Ers;
+                        rowm[e >> 1] += m2;
+                        colacc[nj][e & 1] += m2;
+                        Fm[nj][e] = bt * dA * ex2(cs[r] - cs[s]);
+                    } else {
+                        Fm[nj][e] = 0.f;
+                    }
+                }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            rt[h] += quad_sum(rowm[h]);
+            dbr[h] += quad_sum(dba[h]);
+        }
+        __syncthreads();  // every warp has read E
+        store_parts(Fm, C::OFF_FH, C::OFF_FL);
+
+        // row and column parts of the gradient on c, dbeta, the last position's extra term
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float x = colacc[nj][c];
+                x += __shfl_xor_sync(0xffffffffu, x, 4);
+                x += __shfl_xor_sync(0xffffffffu, x, 8);
+                x += __shfl_xor_sync(0xffffffffu, x, 16);
+                if (g == 0) colp[warp * kDlTc + nj * 8 + 2 * tq + c] = x;
+            }
+        if (tq == 0) {
+            dbs[rr[0]] = dbr[0];
+            dbs[rr[1]] = dbr[1];
+        }
+        {
+            float ex = esum + ex2(cL) * sd;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ex += __shfl_xor_sync(0xffffffffu, ex, off);
+            if (lane == 0) red[warp] = ex;
+        }
+        __syncthreads();  // F, G1, Zq in shared memory
+        // ---- dQ = G1 K + diag(gamma) dO S^T, and gamma_r q_r . (dO S^T)_r
+        {
+            float Acc[NQ][4];
+#pragma unroll
+            for (int j = 0; j < NQ; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) Acc[j][e] = 0.f;
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt) {
+                uint32_t a[4];
+                lda_rows<VRB>(a, sdO, warp * 16, kt, lane);
+#pragma unroll
+                for (int pp = 0; pp < DK / 16; ++pp) {
+                    uint32_t sh[4], sl[4];
+                    ldb_nk<VRB>(sh, smem + C::OFF_SH, pp, kt, lane);
+                    ldb_nk<VRB>(sl, smem + C::OFF_SL, pp, kt, lane);
+                    mma_pair(Acc, pp, a, sh);
+                    mma_pair(Acc, pp, a, sl);
+                }
+            }
+            float qd[2] = {0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < NQ; ++j)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float2 qq = bf_pair(C::OFF_Q, QRB, rr[h], j * 8 + 2 * tq);
+                    qd[h] += qq.x * Acc[j][2 * h] + qq.y * Acc[j][2 * h + 1];
+                }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float gm = ex2(cs[rr[h]]);
+                rt[h] += gm * quad_sum(qd[h]);
+#pragma unroll
+                for (int j = 0; j < NQ; ++j) {
+                    Acc[j][2 * h] *= gm;
+                    Acc[j][2 * h + 1] *= gm;
+                }
+            }
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt) {
+                uint32_t ah[4], al[4];
+                lda_rows<VRB>(ah, smem + C::OFF_XH, warp * 16, kt, lane);
+                lda_rows<VRB>(al, smem + C::OFF_XL, warp * 16, kt, lane);
+#pragma unroll
+                for (int pp = 0; pp < DK / 16; ++pp) {
+                    uint32_t b[4];
+                    ldb_kn<QRB>(b, sK, pp, kt, lane);
+                    mma_pair(Acc, pp, ah, b);
+                    mma_pair(Acc, pp, al, b);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < NQ; ++j)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const long long t = t0 + rr[h];
+                    if (t < p.T)
+                        *reinterpret_cast<float2 *>(dq_out + (size_t)t * DK + j * 8 + 2 * tq) =
+                            make_float2(Acc[j][2 * h], Acc[j][2 * h + 1]);
+                }
+        }
+        if (tq == 0) {
+            rowp[rr[0]] = rt[0];
+            rowp[rr[1]] = rt[1];
+        }
+        // ---- dK = G1^T Q + (F^T + F) K + diag(w) U dS'^T + Zk S^T
+        {
+            float Acc[NQ][4];
+#pragma unroll
+            for (int j = 0; j < NQ; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) Acc[j][e] = 0.f;
+#pragma unroll 1
+            for (int kt = 0; kt < 4; ++kt) {  // k over the chunk's tokens
+                uint32_t gh[4], gl[4], fth[4], ftl[4], fh[4], fl[4];
+                lda_trans<VRB>(gh, smem + C::OFF_XH, warp, kt, lane);
+                lda_trans<VRB>(gl, smem + C::OFF_XL, warp, kt, lane);
+                lda_trans<VRB>(fth, smem + C::OFF_FH, warp, kt, lane);
+                lda_trans<VRB>(ftl, smem + C::OFF_FL, warp, kt, lane);
+                lda_rows<VRB>(fh, smem + C::OFF_FH, warp * 16, kt, lane);
+                lda_rows<VRB>(fl, smem + C::OFF_FL, warp * 16, kt, lane);
+#pragma unroll
+                for (int pp = 0; pp < DK / 16; ++pp) {
+                    uint32_t bq[4], bk[4];
+                    ldb_kn<QRB>(bq, sQ, pp, kt, lane);
+                    ldb_kn<QRB>(bk, sK, pp, kt, lane);
+                    mma_pair(Acc, pp, gh, bq);
+                    mma_pair(Acc, pp, gl, bq);
+                    mma_pair(Acc, pp, fth, bk);
+                    mma_pair(Acc, pp, ftl, bk);
+                    mma_pair(Acc, pp, fh, bk);
+                    mma_pair(Acc, pp, fl, bk);
+                }
+            }
+#pragma unroll 1
+            for (int kt = 0; kt < 4; ++kt) {  // k over the 64 value columns
+                uint32_t wh[4], wl[4], zh[4], zl[4];
+                lda_rows<VRB>(wh, smem + C::OFF_WH, warp * 16, kt, lane);
+                lda_rows<VRB>(wl, smem + C::OFF_WL, warp * 16, kt, lane);
+                lda_rows<VRB>(zh, smem + C::OFF_ZH, warp * 16, kt, lane);
+                lda_rows<VRB>(zl, smem + C::OFF_ZL, warp * 16, kt, lane);
+#pragma unroll
+                for (int pp = 0; pp < DK / 16; ++pp) {
+                    uint32_t b1[4], b2[4];
+                    ldb_nk<VRB>(b1, smem + C::OFF_GH, pp, kt, lane);
+                    ldb_nk<VRB>(b2, smem + C::OFF_GL, pp, kt, lane);
+                    mma_pair(Acc, pp, wh, b1);
+                    mma_pair(Acc, pp, wh, b2);
+                    mma_pair(Acc, pp, wl, b1);
+                    ldb_nk<VRB>(b1, smem + C::OFF_SH, pp, kt, lane);
+                    ldb_nk<VRB>(b2, smem + C::OFF_SL, pp, kt, lane);
+                    mma_pair(Acc, pp, zh, b1);
+                    mma_pair(Acc, pp, zh, b2);
+                    mma_pair(Acc, pp, zl, b1);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < NQ; ++j)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const long long t = t0 + rr[h];
+                    if (t < p.T)
+                        *reinterpret_cast<float2 *>(dk_out + (size_t)t * DK + j * 8 + 2 * tq) =
+                            make_float2(Acc[j][2 * h], Acc[j][2 * h + 1]);
+                }
+        }
+        // ---- dS = gamma_L dS' + Q^T Zq + K^T Zk   (two products each)
+        {
+            const float gL = ex2(cL);
+#pragma unroll
+            for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+                for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dS[mi][nj][e] *= gL;
+#pragma unroll 1
+            for (int kt = 0; kt < 4; ++kt)
+#pragma unroll
+                for (int which = 0; which < 2; ++which) {
+                    const uint8_t *zt_h = smem + (which ? C::OFF_ZH : C::OFF_TH);
+                    const uint8_t *zt_l = smem + (which ? C::OFF_ZL : C::OFF_TL);
+                    const uint8_t *yt = which ? sK : sQ;
+                    uint32_t b[4][4], bl[4][4];
+#pragma unroll
+                    for (int pp = 0; pp < 4; ++pp) {
+                        ldb_kn<VRB>(b[pp], zt_h, pp, kt, lane);
+                        ldb_kn<VRB>(bl[pp], zt_l, pp, kt, lane);
+                    }
+#pragma unroll
+                    for (int mi = 0; mi < S_MT; ++mi) {
+                        uint32_t a[4];
+                        lda_trans<QRB>(a, yt, warp * S_MT + mi, kt, lane);
+#pragma unroll
+                        for (int pp = 0; pp < 4; ++pp) {
+                            mma_pair(dS[mi], pp, a, b[pp]);
+                            mma_pair(dS[mi], pp, a, bl[pp]);
+                        }
+                    }
+                }
+        }
+        __syncthreads();  // row parts, column parts, dbeta
+        // ---- the gradient on c -> suffix sums in the chunk -> dlog_a; dbeta (warp 0, two rows a lane)
+        if (warp == 0) {
+            const float extra = red[0] + red[1] + red[2] + red[3];
+            const int r0 = 2 * lane;
+            float d0 = rowp[r0] - (colp[r0] + colp[kDlTc + r0] + colp[2 * kDlTc + r0] + colp[3 * kDlTc + r0]);
+            float d1 = rowp[r0 + 1] -
+                       (colp[r0 + 1] + colp[kDlTc + r0 + 1] + colp[2 * kDlTc + r0 + 1] + colp[3 * kDlTc + r0 + 1]);
+            if (lane == 31) d1 += extra;
+            float tot = d0 + d1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_down_sync(0xffffffffu, tot, off);
+                if (lane + off < 32) tot += o;
+            }
+            const long long ta = t0 + r0;
+            if (ta < p.T) {
+                dl_out[ta] = tot;
+                db_out[ta] = dbs[r0];
+            }
+            if (ta + 1 < p.T) {
+                dl_out[ta + 1] = tot - d0;
+                db_out[ta + 1] = dbs[r0 + 1];
+            }
+        }
+        __syncthreads();  // before the next chunk's loads overwrite shared memory
+        if (i > 0) load_stage(i - 1);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+    if (p.dS0 != nullptr) {
+#pragma unroll
+        for (int mi = 0; mi < S_MT; ++mi)
+#pragma unroll
+            for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *reinterpret_cast<float2 *>(p.dS0 + ((size_t)bh * DK + s_row(mi, h)) * p.DV + zb * 64 + nj * 8 +
+                                                2 * tq) = make_float2(dS[mi][nj][2 * h], dS[mi][nj][2 * h + 1]);
+    }
+}
+
+// dq, dk, dlog_a, dbeta += the partials of the value-column blocks 1..nzb-1, in block order.
+__global__ void delta_bwd_reduce_kernel(float *dq, float *dk, float *dl, float *db, const float *part,
+                                        long long part_stride, long long ntok, int dim_k, int nparts) {
+    const long long nqk = ntok * dim_k;  // even: dim_k is a multiple of 64
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    for (long long i = i0; i < nqk; i += stride) {  // the stacked [dq | dk], two floats per step
+        const long long e = 2 * i;
+        float *dst = e < nqk ? dq + e : dk + (e - nqk);
+        float2 s = *reinterpret_cast<const float2 *>(dst);
+        for (int z = 0; z < nparts; ++z) {
+            const float2 x = __ldcs(reinterpret_cast<const float2 *>(part + z * part_stride + e));
+            s.x += x.x;
+            s.y += x.y;
+        }
+        *reinterpret_cast<float2 *>(dst) = s;
+    }
+    for (long long i = i0; i < 2 * ntok; i += stride) {  // dlog_a and dbeta
+        float *dst = i < ntok ? dl + i : db + (i - ntok);
+        float s = *dst;
+        for (int z = 0; z < nparts; ++z) s += __ldcs(part + z * part_stride + 2 * nqk + i);
+        *dst = s;
+    }
+}
+
+template <int DK>
+int launch_delta_bwd(const DeltaBwdArgs &a, cudaStream_t s, unsigned int grid) {
+    using C = DeltaBwdCfg<DK>;
+    static std::atomic<unsigned long long> smem_set{0};
+    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(delta_bwd_kernel<DK>), C::SMEM);
+    if (st) return st;
+    delta_bwd_kernel<DK><<<grid, kDlThreads, C::SMEM, s>>>(a);
+    return check_launch("delta_bwd_kernel");
+}
+
+// Workspace of the backward: the header, the state entering every chunk, and the partials of the
+// value-column blocks after the first.  0 when the shape is unsupported or the size overflows.
+size_t delta_bwd_ws_bytes(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv) {
+    const double BH = (double)B * H, nc = (double)((T + kDlTc - 1) / kDlTc);
+    const double states = BH * nc * dk * dv * 4.0;
+    const double parts = (double)(dv / 64 - 1) * BH * T * (2.0 * dk + 2.0) * 4.0;
+    const double total = sizeof(WsHeader) + states + 16.0 + parts;
+    if (total > 9.0e18) return 0;
+    return sizeof(WsHeader) + align_up((size_t)states, 16) + (size_t)parts;
+}
+
 bool delta_supported(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chunk) {
     return B >= 0 && H >= 0 && T >= 0 && (dk == 64 || dk == 128) && dv > 0 && dv % 64 == 0 && dv <= 1024 &&
            chunk == kDlTc && product_below({B, H}, 16777217.0) && T <= (1ll << 34) &&
@@ -532,4 +1446,103 @@ extern "C" int cla_delta_fwd(const uint16_t *q, const uint16_t *k, const uint16_
     a.hdr = static_cast<WsHeader *>(ws);
     const unsigned int grid = (unsigned int)(BH * (dim_v / 64));
     return dim_k == 64 ? launch_delta_fwd<64>(a, s, grid) : launch_delta_fwd<128>(a, s, grid);
+}
+
+extern "C" size_t cla_delta_bwd_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
+                                               int chunk) {
+    if (!delta_supported(B, H, T, dim_k, dim_v, chunk)) return 0;
+    return delta_bwd_ws_bytes(B, H, T, dim_k, dim_v);
+}
+
+extern "C" int cla_delta_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                             const float *beta, const float *S0, const uint16_t *dO, const float *dST, float *dq,
+                             float *dk, float *dv, float *dlog_decay, float *dbeta, float *dS0, int64_t B,
+                             int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk, void *ws,
+                             size_t ws_bytes, void *stream) {
+    clear_error();
+    const char *fn = "cla_delta_bwd";
+    if (B < 0 || H < 0 || T < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (!delta_supported(B, H, T, dim_k, dim_v, chunk))
+        return fail(CLA_ERR_UNSUPPORTED, "%s: needs dim_k 64 or 128, dim_v a multiple of 64 up to 1024 and chunk 64 "
+                    "(got dim_k %lld, dim_v %lld, chunk %d)", fn, (long long)dim_k, (long long)dim_v, chunk);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t BH = B * H;
+    if (BH == 0) return CLA_OK;
+    if (T == 0) {  // nothing but the final state's adjoint passes through
+        if (dS0) {
+            const size_t sbytes = sizeof(float) * BH * dim_k * dim_v;
+            if (dST) CLA_CUDA_TRY(cudaMemcpyAsync(dS0, dST, sbytes, cudaMemcpyDeviceToDevice, s), fn);
+            else CLA_CUDA_TRY(cudaMemsetAsync(dS0, 0, sbytes, s), fn);
+        }
+        return CLA_OK;
+    }
+    if (!q || !k || !v || !log_decay || !beta || !dO || !dq || !dk || !dv || !dlog_decay || !dbeta)
+        return fail(CLA_ERR_INVALID_ARG, "%s: q, k, v, log_decay, beta, dO, dq, dk, dv, dlog_decay, dbeta required",
+                    fn);
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO))
+        return fail(CLA_ERR_INVALID_ARG, "%s: q, k, v, dO must be 16-byte aligned", fn);
+    if (!aligned_or_null({dq, dk, dv, dS0, dST, S0}, 8) || !aligned_or_null({log_decay, beta, dlog_decay, dbeta}, 4))
+        return fail(CLA_ERR_INVALID_ARG, "%s: dq, dk, dv, dS0, dST, S0 must be 8-byte aligned, log_decay, beta, "
+                    "dlog_decay, dbeta 4-byte", fn);
+    const size_t need = delta_bwd_ws_bytes(B, H, T, dim_k, dim_v);
+    if (need == 0) return fail(CLA_ERR_UNSUPPORTED, "%s: workspace size overflows", fn);
+    if (!ws || !aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace NULL or unaligned", fn);
+    if (ws_bytes < need) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, need);
+    CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), s), fn);
+    const int n_chunks = (int)((T + kDlTc - 1) / kDlTc);
+    float *states = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + sizeof(WsHeader));
+    const size_t states_bytes = align_up(sizeof(float) * (size_t)BH * n_chunks * dim_k * dim_v, 16);
+    const unsigned int grid = (unsigned int)(BH * (dim_v / 64));
+    // the states pass: the forward kernel writes the state entering every chunk, no output
+    DeltaArgs f;
+    memset(&f, 0, sizeof(f));
+    f.q = reinterpret_cast<const bf16 *>(q);
+    f.k = reinterpret_cast<const bf16 *>(k);
+    f.v = reinterpret_cast<const bf16 *>(v);
+    f.g = log_decay;
+    f.beta = beta;
+    f.S0 = S0;
+    f.states = states;
+    f.BH = (int)BH;
+    f.DV = (int)dim_v;
+    f.nzb = (int)(dim_v / 64);
+    f.n_chunks = n_chunks;
+    f.T = T;
+    f.hdr = static_cast<WsHeader *>(ws);
+    int st = dim_k == 64 ? launch_delta_fwd<64>(f, s, grid) : launch_delta_fwd<128>(f, s, grid);
+    if (st) return st;
+    DeltaBwdArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = f.q;
+    a.k = f.k;
+    a.v = f.v;
+    a.dO = reinterpret_cast<const bf16 *>(dO);
+    a.g = log_decay;
+    a.beta = beta;
+    a.dST = dST;
+    a.states = states;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dlog = dlog_decay;
+    a.dbeta = dbeta;
+    a.dS0 = dS0;
+    a.part = dim_v > 64 ? reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(states) + states_bytes) : nullptr;
+    a.part_stride = (long long)BH * T * (2 * dim_k + 2);
+    a.BH = (int)BH;
+    a.DV = (int)dim_v;
+    a.nzb = (int)(dim_v / 64);
+    a.n_chunks = n_chunks;
+    a.T = T;
+    st = dim_k == 64 ? launch_delta_bwd<64>(a, s, grid) : launch_delta_bwd<128>(a, s, grid);
+    if (st) return st;
+    if (a.nzb > 1) {
+        const long long ntok = (long long)BH * T;
+        const long long work = ntok * dim_k;
+        const unsigned int blocks = (unsigned int)std::min<long long>((work + 255) / 256, 152LL * 16);
+        delta_bwd_reduce_kernel<<<blocks, 256, 0, s>>>(dq, dk, dlog_decay, dbeta, a.part, a.part_stride, ntok,
+                                                       (int)dim_k, a.nzb - 1);
+        return check_launch("delta_bwd_reduce_kernel");
+    }
+    return CLA_OK;
 }

@@ -425,6 +425,42 @@ int cla_delta_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                   int64_t dim_k, int64_t dim_v, int chunk, void *ws,
                   size_t ws_bytes, void *stream);
 
+/* Bytes of workspace for cla_delta_bwd: the header, the state entering every
+ * chunk (B H ceil(T / 64) dim_k dim_v fp32) and, for dim_v > 64, partial
+ * key-side gradients of the value-column blocks after the first
+ * ((dim_v / 64 - 1) B H T (2 dim_k + 2) fp32); 0 for sizes, head dims or
+ * chunks that call refuses. */
+size_t cla_delta_bwd_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                                    int64_t dim_v, int chunk);
+
+/* Backward of cla_delta_fwd: the adjoint of the chunk form ("Parallel Scan",
+ * "What one combine costs" for the transition and its WY factors; "The
+ * backward pass is a scan in reverse" for the adjoint carried from the last
+ * chunk to the first).  A states pass of the forward kernel writes the state
+ * S entering every chunk; then, chunks in reverse with dS' the adjoint of the
+ * state leaving the chunk, U = Veff, w_r = gamma_L / gamma_r:
+ *   dU = P^T dO + diag(w) K dS',  dX = (I + A)^-T dU,  dV = diag(beta) dX
+ *   dP = dO U^T (s <= r),  dA = -dX U^T (s < r),  F = diag(beta) dA . D
+ *   dQ = (dP . D) K + diag(gamma) dO S^T
+ *   dK = (dP . D)^T Q + (F + F^T) K + diag(w) U dS'^T - diag(beta gamma) dX S^T
+ *   dbeta_r = (V - diag(gamma) K S)_r . dX_r + sum_s dA_rs D_rs k_r . k_s
+ *   dS = gamma_L dS' + Q^T diag(gamma) dO - K^T diag(beta gamma) dX
+ * and dlog_decay the in-chunk suffix sums of the gradient on the cumulative
+ * log decays.
+ *   dO          [B, H, T, dim_v] bf16   upstream gradient on o
+ *   dST         [B, H, dim_k, dim_v] fp32 [opt] upstream gradient on S_T
+ *   dq, dk      [B, H, T, dim_k] fp32 out;  dv [B, H, T, dim_v] fp32 out
+ *   dlog_decay, dbeta [B, H, T] fp32 out;  dS0 [B, H, dim_k, dim_v] fp32 [opt] out
+ * Supported and checked as cla_delta_fwd; dq, dk, dv, dS0, dST and S0 8-byte
+ * aligned.  A non-finite log decay or beta is reported through
+ * cla_check_status(ws, stream) as in the forward. */
+int cla_delta_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                  const float *log_decay, const float *beta, const float *S0,
+                  const uint16_t *dO, const float *dST, float *dq, float *dk,
+                  float *dv, float *dlog_decay, float *dbeta, float *dS0,
+                  int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
+                  int chunk, void *ws, size_t ws_bytes, void *stream);
+
 /* ======================================================================== */
 /* State passing between slices of one sequence                             */
 /* ======================================================================== */

@@ -158,3 +158,86 @@ def test_wy_factors_are_the_product_of_rank_one_corrections():
         P = (np.eye(dk) - bt[r] * np.outer(K[r], K[r])) @ P
         np.testing.assert_allclose(P, np.eye(dk) - K[: r + 1].T @ W[: r + 1], rtol=1e-12, atol=1e-12)
         assert np.linalg.matrix_rank(np.eye(dk) - P) <= r + 1
+
+
+def chunked_delta_bwd(q, k, v, la, beta, S0, dO, dST, C):
+    """The adjoint of the chunkwise form, chunk by chunk in reverse, float64: the states entering
+    each chunk from a forward pass, then per chunk (n tokens, in-chunk log decays c, w = gamma_L / gamma)
+        dU = P^T dO + diag(w) K dS',     dX = (I + A)^-T dU,     dV = diag(beta) dX
+        dP = dO U^T (s <= r),            dA = -dX U^T (s < r)
+        dQ = (dP . D) K + diag(gamma) dO S^T
+        dK = (dP . D)^T Q + (F + F^T) K + diag(w) U dS'^T - diag(beta gamma) dX S^T,  F = beta_r dA_rs D_rs
+        dbeta_r = (V - diag(gamma) K S)_r . dX_r + sum_s dA_rs D_rs k_r . k_s
+        dS = gamma_L dS' + Q^T diag(gamma) dO - K^T diag(beta gamma) dX
+    and the gradient on the in-chunk sums c (each product of decays differentiated in c),
+    whose suffix sums inside the chunk are the gradient on each token's log decay."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dq, dkk = np.zeros((B, H, T, dk)), np.zeros((B, H, T, dk))
+    dvv = np.zeros((B, H, T, dv))
+    dl, db = np.zeros((B, H, T)), np.zeros((B, H, T))
+    dS0 = np.zeros((B, H, dk, dv))
+    for b in range(B):
+        for h in range(H):
+            S = S0[b, h].copy() if S0 is not None else np.zeros((dk, dv))
+            starts = []
+            for c0 in range(0, T, C):  # the states entering every chunk
+                sl = slice(c0, min(c0 + C, T))
+                starts.append(S.copy())
+                _, S = chunked_delta_fwd(q[None, None, b, h, sl], k[None, None, b, h, sl], v[None, None, b, h, sl],
+                                         la[None, None, b, h, sl], beta[None, None, b, h, sl], S[None, None], C)
+                S = S[0, 0]
+            dS = dST[b, h].copy() if dST is not None else np.zeros((dk, dv))
+            for j, c0 in reversed(list(enumerate(range(0, T, C)))):
+                sl = slice(c0, min(c0 + C, T))
+                Q, K, V, dOc = q[b, h, sl], k[b, h, sl], v[b, h, sl], dO[b, h, sl]
+                S = starts[j]
+                c = np.cumsum(la[b, h, sl])
+                bt = beta[b, h, sl]
+                n = len(c)
+                gam = np.exp(c)
+                G = np.exp(c[:, None] - c[None, :])
+                E = np.tril(G * (K @ K.T), -1)
+                A = bt[:, None] * E
+                Ti = np.linalg.inv(np.eye(n) + A)
+                Yv = V - gam[:, None] * (K @ S)
+                U = Ti @ (bt[:, None] * Yv)
+                Dl = np.tril(G)
+                P = (Q @ K.T) * Dl
+                w = np.exp(c[-1] - c)
+                KdS = K @ dS
+                dU = P.T @ dOc + w[:, None] * KdS
+                dX = Ti.T @ dU
+                dP = np.tril(dOc @ U.T)
+                dA = -np.tril(dX @ U.T, -1)
+                G1 = dP * Dl
+                F = bt[:, None] * dA * G
+                dOSt = dOc @ S.T
+                dq[b, h, sl] = G1 @ K + gam[:, None] * dOSt
+                dkk[b, h, sl] = (G1.T @ Q + (F + F.T) @ K + (w[:, None] * U) @ dS.T
+                                 - ((bt * gam)[:, None] * dX) @ S.T)
+                dvv[b, h, sl] = bt[:, None] * dX
+                db[b, h, sl] = np.sum(Yv * dX, 1) + np.sum(dA * E, 1)
+                M1, M2 = dP * P, dA * A
+                e = w * np.sum(KdS * U, 1)
+                dc = (M1.sum(1) - M1.sum(0) + M2.sum(1) - M2.sum(0) + gam * np.sum(Q * dOSt, 1) - e
+                      - bt * np.sum((V - Yv) * dX, 1))
+                dc[-1] += e.sum() + gam[-1] * np.sum(S * dS)
+                dl[b, h, sl] = np.cumsum(dc[::-1])[::-1]
+                dS = gam[-1] * dS + Q.T @ (gam[:, None] * dOc) - K.T @ ((bt * gam)[:, None] * dX)
+            dS0[b, h] = dS
+    return dq, dkk, dvv, dl, db, dS0
+
+
+@pytest.mark.parametrize("C", [1, 2, 3, 5, 8, 23, 64])
+def test_chunkwise_adjoint_equals_the_recurrence_adjoint(C):
+    """The chunk-by-chunk adjoint (what a backward kernel computes per chunk) gives the
+    oracle's per-token adjoint for every chunking, short last chunks included."""
+    q, k, v, la, beta, S0 = _rand(T=23, unit_keys=False)
+    rng = np.random.default_rng(11)
+    dO = rng.normal(size=(1, 2, 23, 4))
+    dST = rng.normal(size=(1, 2, 5, 4))
+    got = chunked_delta_bwd(q, k, v, la, beta, S0, dO, dST, C)
+    want = oracle.delta_bwd(q, k, v, la, beta, S0, dO, dST)
+    for name, g, r in zip(("dq", "dk", "dv", "dlog_a", "dbeta", "dS0"), got, want):
+        np.testing.assert_allclose(g, r, rtol=1e-9, atol=1e-10, err_msg=name)

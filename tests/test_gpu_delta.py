@@ -1,7 +1,8 @@
-"""Delta rule with a decay per head (Gated DeltaNet), forward: GPU (through the
-C ABI) vs the oracle's per-token recurrence, with the bf16 tolerance (per
-output tensor, |x - r| / rms(r): max <= 2e-2, mean <= 5e-3), and the range
-check on non-finite decays."""
+"""Delta rule with a decay per head (Gated DeltaNet), forward and backward:
+GPU (through the C ABI) vs the oracle's per-token recurrence and its adjoint,
+with the bf16 tolerance (per output tensor, |x - r| / rms(r): max <= 2e-2,
+mean <= 5e-3), and the range check on non-finite decays."""
+import numpy as np
 import pytest
 import torch
 
@@ -72,3 +73,59 @@ def test_delta_workload_full_sampled_heads(cla):
     """The full delta workload (4 x 32 x 4096, d = 128), every output of three heads."""
     inp = workloads.make("delta")
     _run(cla, inp, heads=[0, 17, 31])
+
+
+# ---------------------------------------------------------------- backward
+def _run_bwd(cla, inp, heads=None, dST=None):
+    """The backward through the C ABI against the oracle's adjoint: dq, dk, dv, dlog_a, dbeta, dS0."""
+    t = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    B, H, T, dk = t["q"].shape
+    dv = t["v"].shape[-1]
+    ws = torch.empty(max(cla.delta_bwd_workspace_size(B, H, T, dk, dv, 64), 256), dtype=torch.uint8, device="cuda")
+    got = cla.delta_bwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], t["S0"], t["dO"],
+                        None if dST is None else dST.cuda(), workspace=ws)
+    cla.check_status(ws)
+    sel = (lambda x: x) if heads is None else (lambda x: None if x is None else x[:, heads])
+    ci = {k: sel(v) for k, v in inp.items()}
+    ref = oracle.delta_bwd(ci["q"], ci["k"], ci["v"], ci["log_a"], ci["beta"], ci["S0"], ci["dO"], sel(dST))
+    for name, g, r in zip(("dq", "dk", "dv", "dlog_a", "dbeta", "dS0"), got, ref):
+        assert_bf16(name, sel(g), r)
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv", [
+    (1, 2, 64, 64, 64), (1, 2, 300, 64, 64), (2, 1, 1, 64, 64), (1, 1, 1000, 128, 128),
+    (1, 2, 700, 128, 64), (1, 1, 129, 64, 192), (2, 2, 1100, 128, 128),
+])
+@pytest.mark.parametrize("with_state", [False, True])
+def test_delta_bwd_small(cla, B, H, T, dk, dv, with_state):
+    """Ragged last chunks, one-token sequences, d_k != d_v and three value-column blocks; with
+    S0 and an upstream gradient on S_T, or neither."""
+    inp = workloads.make("delta", B=B, H=H, T=T, dk=dk, dv=dv)
+    dST = None
+    if with_state:
+        dST = torch.from_numpy(np.random.default_rng(T).normal(size=(B, H, dk, dv)).astype(np.float32))
+    else:
+        inp["S0"] = None
+    _run_bwd(cla, inp, dST=dST)
+
+
+def test_delta_bwd_full_writes_and_strong_decay(cla):
+    """beta = 1 in one head, e^-3 per token in the other."""
+    inp = workloads.make("delta", B=1, H=2, T=900, dk=64, dv=64)
+    inp["beta"][:, 0] = 1.0
+    inp["log_a"][:, 1] = -3.0
+    _run_bwd(cla, inp)
+
+
+def test_delta_bwd_zero_length_passes_the_state_gradient(cla):
+    inp = workloads.make("delta", B=1, H=2, T=0, dk=64, dv=128)
+    dST = torch.randn(1, 2, 64, 128)
+    t = {k: v.cuda() for k, v in inp.items()}
+    g = cla.delta_bwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], t["S0"], t["dO"], dST.cuda())
+    assert torch.equal(g[5].cpu(), dST)
+
+
+def test_delta_bwd_workload_full_sampled_heads(cla):
+    """The full delta workload (4 x 32 x 4096, d = 128), every gradient of two heads."""
+    inp = workloads.make("delta")
+    _run_bwd(cla, inp, heads=[5, 26])

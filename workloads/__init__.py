@@ -33,7 +33,7 @@ Workloads (each runnable at any smaller shape with the same distributions):
   T=4096, d_k=d_v=128; q, v bf16 ~ N(0, 1)/sqrt(128); k ~ N(0, 1) per
   element, L2-normalised per token, then bf16; log a = -softplus(N(0, 1))/16
   and beta = sigmoid(N(0, 1)) per (head, token); S0 ~ N(0, 0.01^2) fp32;
-  chunk 64.
+  upstream dL/do ~ N(0, 1) bf16; chunk 64.
 
 The second parameter of N(mu, s) is read as a standard deviation.
 """
@@ -50,8 +50,8 @@ WORKLOADS = {
     "selective": dict(kind="selective", B=4, T=8192, D=2048, N=16, seed=3, backward=True),
     "la_const": dict(kind="chunk_la", B=4, H=16, T=8192, dk=64, dv=64, chunk=64, seed=4, backward=True),
     "la_long": dict(kind="chunk_la", B=1, H=32, T=65536, dk=128, dv=128, chunk=128, seed=5, backward=True),
-    "gla": dict(kind="gla", B=2, H=16, T=16384, dk=128, dv=128, chunk=64, seed=6, backward=False),
-    "delta": dict(kind="delta", B=4, H=32, T=4096, dk=128, dv=128, chunk=64, seed=7, backward=False),
+    "gla": dict(kind="gla", B=2, H=16, T=16384, dk=128, dv=128, chunk=64, seed=6, backward=True),
+    "delta": dict(kind="delta", B=4, H=32, T=4096, dk=128, dv=128, chunk=64, seed=7, backward=True),
 }
 
 
@@ -152,7 +152,8 @@ def delta_inputs(B=4, H=32, T=4096, dk=128, dv=128, seed=7):
     log_a = (-_softplus(_normal(seed, 3, (B, H, T))) / 16.0).astype(np.float32)
     beta = (1.0 / (1.0 + np.exp(-_normal(seed, 4, (B, H, T)).astype(np.float64)))).astype(np.float32)
     S0 = _normal(seed, 5, (B, H, dk, dv), std=0.01)
-    return dict(q=q, k=k, v=v, log_a=_f32(log_a), beta=_f32(beta), S0=_f32(S0))
+    dO = _bf16(_normal(seed, 6, (B, H, T, dv)))
+    return dict(q=q, k=k, v=v, log_a=_f32(log_a), beta=_f32(beta), S0=_f32(S0), dO=dO)
 
 
 GENERATORS = {
