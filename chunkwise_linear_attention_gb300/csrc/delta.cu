@@ -31,6 +31,7 @@
 // Range: finite log decays (no exact-zero gates).  A chunk with a non-finite
 // log decay or gate strength sets an error flag that cla_check_status reports.
 #include <algorithm>
+#include <type_traits>
 
 #include "cla_internal.cuh"
 #include "mma_sync.cuh"
@@ -43,6 +44,27 @@ typedef __nv_bfloat16 bf16;
 constexpr float kDlLog2e = 1.4426950408889634f;
 constexpr int kDlTc = 64;        // tokens per chunk
 constexpr int kDlThreads = 128;  // warp w: rows 16w..16w+15 of a chunk
+constexpr int kDlBwdThreads = 256;  // backward: warp w rows 16(w & 3).., column half w >> 2
+constexpr int kAS = kDlTc + 4;    // row stride (floats) of the fp32 [64][64] triangle: 16-byte aligned rows
+
+// sum_{s < r} row[s] x[s] for the forward substitution of a unit lower triangular system:
+// 16-byte loads of the row (broadcast: every thread reads the same row) and four partial sums,
+// so the dependent chain per row is a quarter as long.  r is a compile-time constant after
+// unrolling; x stays in registers.
+__device__ __forceinline__ float tri_row_dot(const float *row, const float (&x)[kDlTc], int r) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int s4 = 0; s4 + 4 <= r; s4 += 4) {
+        const float4 e = *reinterpret_cast<const float4 *>(row + s4);
+        a0 = fmaf(e.x, x[s4], a0);
+        a1 = fmaf(e.y, x[s4 + 1], a1);
+        a2 = fmaf(e.z, x[s4 + 2], a2);
+        a3 = fmaf(e.w, x[s4 + 3], a3);
+    }
+#pragma unroll
+    for (int s = r & ~3; s < r; ++s) a0 = fmaf(row[s], x[s], a0);
+    return (a0 + a1) + (a2 + a3);
+}
 
 template <int DK>
 struct DeltaCfg {
@@ -61,7 +83,7 @@ struct DeltaCfg {
     // A (fp32) until (I + A)^-1 is built, then X and Veff in the same bytes;
     // (I + A)^-1 until Veff is formed, then diag(gamma_L / gamma) Veff.
     static constexpr int OFF_A = STAGE;                     // A, fp32 [64][64] (row stride 65)
-    static constexpr int A_FLOATS = kDlTc * (kDlTc + 1);
+    static constexpr int A_FLOATS = kDlTc * kAS;
     static constexpr int OFF_XH = OFF_A;                    // X, then Veff, two bf16 parts [64][64]
     static constexpr int OFF_XL = OFF_XH + kDlTc * VRB;
     static constexpr int OFF_TH = OFF_A + A_FLOATS * 4;     // (I + A)^-1 as two bf16 parts [64][64]
@@ -247,7 +269,7 @@ __global__ void __launch_bounds__(kDlThreads, 2) delta_fwd_kernel(const DeltaArg
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int r = warp * 16 + g + 8 * (e >> 1), s = nj * 8 + 2 * tq + (e & 1);
-                    Am[r * (kDlTc + 1) + s] = (s < r) ? bs[r] * ex2(cs[r] - cs[s]) * F[nj][e] : 0.f;
+                    Am[r * kAS + s] = (s < r) ? bs[r] * ex2(cs[r] - cs[s]) * F[nj][e] : 0.f;
                 }
         }
         __syncthreads();
@@ -259,9 +281,7 @@ __global__ void __launch_bounds__(kDlThreads, 2) delta_fwd_kernel(const DeltaArg
             float tc[kDlTc];
 #pragma unroll
             for (int r = 0; r < kDlTc; ++r) {
-                float acc = 0.f;
-#pragma unroll
-                for (int s2 = 0; s2 < r; ++s2) acc = fmaf(Am[r * (kDlTc + 1) + s2], tc[s2], acc);
+                const float acc = tri_row_dot(Am + r * kAS, tc, r);
                 tc[r] = (r < j) ? 0.f : (r == j ? 1.f : -acc);
             }
 #pragma unroll
@@ -531,9 +551,11 @@ __device__ __forceinline__ float quad_sum(float x) {
 // sum_r w_r (K dS')_r . U_r + gamma_L <S, dS'>; its suffix sums inside the
 // chunk are the gradient on each token's log decay.
 //
-// One block per (head, 64 value columns), 4 warps, warp w the chunk's rows
-// 16w..16w+15; the adjoint state dS [DK][64] in registers like the forward's
-// state.  dQ, dK, dbeta and dlog_a sum over the value-column blocks: the block
+// One block per (head, 64 value columns), 8 warps: warp w takes the chunk's rows
+// 16(w & 3)..+15 and half (w >> 2) of the output columns of every product (the
+// score-shaped products whose result feeds another product's k dimension are
+// formed whole by both warps of a row group, or pass through shared memory);
+// the adjoint state dS [DK][64] in registers, split the same way.  dQ, dK, dbeta and dlog_a sum over the value-column blocks: the block
 // of columns 0..63 writes them to the outputs, the others to workspace
 // partials that delta_bwd_reduce_kernel adds.  dV and dS0 belong to one block.
 template <int DK>
@@ -555,7 +577,7 @@ struct DeltaBwdCfg {
     static constexpr int OFF_GH = OFF_SL + S_BYTES;  // dS' (adjoint of the state leaving it), two parts
     static constexpr int OFF_GL = OFF_GH + S_BYTES;
     static constexpr int OFF_E = OFF_GL + S_BYTES;   // E fp32 [64][65]; then F as two parts
-    static constexpr int E_BYTES = kDlTc * (kDlTc + 1) * 4;
+    static constexpr int E_BYTES = kDlTc * kAS * 4;
     static constexpr int OFF_FH = OFF_E;
     static constexpr int OFF_FL = OFF_E + V_BYTES;
     static constexpr int OFF_TH = OFF_E + E_BYTES;   // (I + A)^-1; then diag(gamma) dO (two parts each)
@@ -568,12 +590,12 @@ struct DeltaBwdCfg {
     static constexpr int OFF_WL = OFF_WH + V_BYTES;
     static constexpr int OFF_ZH = OFF_WL + V_BYTES;  // -diag(beta gamma) dX
     static constexpr int OFF_ZL = OFF_ZH + V_BYTES;
-    static constexpr int OFF_ROW = OFF_ZL + V_BYTES;  // row parts of the gradient on c [64]
-    static constexpr int OFF_COL = OFF_ROW + 256;     // column parts, one row per warp [4][64]
-    static constexpr int OFF_DB = OFF_COL + 1024;     // dbeta [64]
-    static constexpr int OFF_RED = OFF_DB + 256;      // the last position's extra term, per warp [4]
+    static constexpr int OFF_ROW = OFF_ZL + V_BYTES;  // row parts of the gradient on c [2][64]
+    static constexpr int OFF_COL = OFF_ROW + 512;     // column parts, one row per warp [8][64]
+    static constexpr int OFF_DB = OFF_COL + 2048;     // dbeta parts [2][64]
+    static constexpr int OFF_RED = OFF_DB + 512;      // the last position's extra term, per warp [8]
     static constexpr int SMEM = OFF_RED + 64;
-    static constexpr int S_MT = DK / 64;
+    static constexpr int S_MT = DK / 64;  // 16-row tiles of the state per row group
     static_assert(2 * V_BYTES <= E_BYTES, "F fits where E was");
     static_assert(E_BYTES % 128 == 0, "tiles after E stay 128-byte aligned");
     static_assert(SMEM + 1024 <= 227 * 1024, "one block per SM");
@@ -592,13 +614,14 @@ struct DeltaBwdArgs {
 };
 
 template <int DK>
-__global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwdArgs p) {
+__global__ void __launch_bounds__(kDlBwdThreads, 1) delta_bwd_kernel(const DeltaBwdArgs p) {
     using C = DeltaBwdCfg<DK>;
     constexpr int S_MT = C::S_MT;
-    constexpr int NQ = DK / 8;  // 8-column tiles of a [..][DK] output
+    constexpr int NQ2 = DK / 16;  // 8-column tiles of this warp's half of a [..][DK] output
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tq = lane & 3;
+    const int wr = warp & 3, hf = warp >> 2;  // row group, column half
     const int bh = blockIdx.x / p.nzb, zb = blockIdx.x % p.nzb;
     const size_t tok0 = (size_t)bh * p.T;
     const bf16 *Qb = p.q + tok0 * DK;
@@ -625,15 +648,18 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
     float *cs = reinterpret_cast<float *>(smem + C::OFF_C);
     const float *ls = reinterpret_cast<const float *>(smem + C::OFF_L);
     const float *bs = reinterpret_cast<const float *>(smem + C::OFF_B);
-    float *rowp = reinterpret_cast<float *>(smem + C::OFF_ROW);
-    float *colp = reinterpret_cast<float *>(smem + C::OFF_COL);
-    float *dbs = reinterpret_cast<float *>(smem + C::OFF_DB);
-    float *red = reinterpret_cast<float *>(smem + C::OFF_RED);
+    float *rowp = reinterpret_cast<float *>(smem + C::OFF_ROW);  // [2][64]: per column half
+    float *colp = reinterpret_cast<float *>(smem + C::OFF_COL);  // [8][64]: per warp, its half's columns
+    float *dbs = reinterpret_cast<float *>(smem + C::OFF_DB);    // [2][64]
+    float *red = reinterpret_cast<float *>(smem + C::OFF_RED);   // [8]
+    const uint8_t *sQ = smem + C::OFF_Q, *sK = smem + C::OFF_K, *sdO = smem + C::OFF_DO;
+    constexpr int QRB = C::QRB, VRB = C::VRB;
+    constexpr int KQ = DK / 16;  // k-steps over the key dimension
 
     auto load_stage = [&](int chunk) {
         const long long t0 = (long long)chunk * kDlTc;
         constexpr int QC = C::QRB / 16;
-        for (int i = tid; i < kDlTc * QC; i += kDlThreads) {
+        for (int i = tid; i < kDlTc * QC; i += kDlBwdThreads) {
             const int row = i / QC, c16 = i % QC;
             const long long t = t0 + row;
             const bool ok = t < p.T;
@@ -641,7 +667,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
             cp_async16(smem_u32(smem + C::OFF_Q + swz<C::QRB>(row, c16)), Qb + off, ok ? 16u : 0u);
             cp_async16(smem_u32(smem + C::OFF_K + swz<C::QRB>(row, c16)), Kb + off, ok ? 16u : 0u);
         }
-        for (int i = tid; i < kDlTc * 8; i += kDlThreads) {
+        for (int i = tid; i < kDlTc * 8; i += kDlBwdThreads) {
             const int row = i >> 3, c16 = i & 7;
             const long long t = t0 + row;
             const bool ok = t < p.T;
@@ -649,7 +675,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
             cp_async16(smem_u32(smem + C::OFF_V + swz<C::VRB>(row, c16)), Vb + off, ok ? 16u : 0u);
             cp_async16(smem_u32(smem + C::OFF_DO + swz<C::VRB>(row, c16)), dOb + off, ok ? 16u : 0u);
         }
-        for (int i = tid; i < kDlTc; i += kDlThreads) {  // padding tokens: no decay, no write
+        for (int i = tid; i < kDlTc; i += kDlBwdThreads) {  // padding tokens: no decay, no write
             const long long t = t0 + i;
             const bool ok = t < p.T;
             cp_async4(smem_u32(smem + C::OFF_L + i * 4), Lb + (ok ? t : 0), ok ? 4u : 0u);
@@ -657,7 +683,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
         }
         // the state entering the chunk, fp32 -> two bf16 parts (plain loads, read once)
         const float *sg = p.states + ((size_t)bh * p.n_chunks + chunk) * DK * p.DV + zb * 64;
-        for (int i = tid; i < DK * 16; i += kDlThreads) {
+        for (int i = tid; i < DK * 16; i += kDlBwdThreads) {
             const int row = i >> 4, c4 = i & 15;
             const float4 x = __ldcs(reinterpret_cast<const float4 *>(sg + (size_t)row * p.DV + c4 * 4));
             uint2 hi, lo;
@@ -669,31 +695,31 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
         }
     };
 
-    // adjoint state fragments: warp w owns rows 16(w S_MT + mi) + {g, g + 8}
-    float dS[S_MT][8][4];
-    auto s_row = [&](int mi, int h) { return (warp * S_MT + mi) * 16 + g + 8 * h; };
+    // adjoint state fragments: rows 16(wr S_MT + mi) + {g, g + 8}, columns 8(4 hf + nj) + 2 tq + {0, 1}
+    float dS[S_MT][4][4];
+    auto s_row = [&](int mi, int h) { return (wr * S_MT + mi) * 16 + g + 8 * h; };
 #pragma unroll
     for (int mi = 0; mi < S_MT; ++mi)
 #pragma unroll
-        for (int nj = 0; nj < 8; ++nj)
+        for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 dS[mi][nj][e] = p.dST ? __ldg(p.dST + ((size_t)bh * DK + s_row(mi, e >> 1)) * p.DV + zb * 64 +
-                                              nj * 8 + 2 * tq + (e & 1))
+                                              (4 * hf + nj) * 8 + 2 * tq + (e & 1))
                                       : 0.f;
-    auto zero8 = [&](float (&F)[8][4]) {
+    auto zero4 = [&](float (&F)[4][4]) {
 #pragma unroll
-        for (int nj = 0; nj < 8; ++nj)
+        for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
             for (int e = 0; e < 4; ++e) F[nj][e] = 0.f;
     };
-    // a [64][64] tile of fp32 fragments (this warp's 16 rows) into two bf16 tiles, [row][col]
-    auto store_parts = [&](const float (&F)[8][4], int off_hi, int off_lo) {
+    // this warp's [16 rows][32 columns] of a [64][64] tile, fp32 fragments, into two bf16 tiles
+    auto store_parts = [&](const float (&F)[4][4], int off_hi, int off_lo) {
 #pragma unroll
-        for (int nj = 0; nj < 8; ++nj)
+        for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int row = warp * 16 + g + 8 * h, col = nj * 8 + 2 * tq;
+                const int row = wr * 16 + g + 8 * h, col = (4 * hf + nj) * 8 + 2 * tq;
                 const uint32_t off = swz<C::VRB>(row, col >> 3) + (col & 7) * 2;
                 uint32_t hi, lo;
                 split_bf16x2(make_float2(F[nj][2 * h], F[nj][2 * h + 1]), hi, lo);
@@ -701,22 +727,58 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
                 *reinterpret_cast<uint32_t *>(smem + off_lo + off) = lo;
             }
     };
-    // an fp32 pair at (row, col) of a [..][64] tile held as two bf16 parts
     auto read_parts = [&](int off_hi, int off_lo, int row, int col) {
         const uint32_t off = swz<C::VRB>(row, col >> 3) + (col & 7) * 2;
         const float2 h = unpack_bf16(*reinterpret_cast<const uint32_t *>(smem + off_hi + off));
         const float2 l = unpack_bf16(*reinterpret_cast<const uint32_t *>(smem + off_lo + off));
         return make_float2(h.x + l.x, h.y + l.y);
     };
-    auto bf_pair = [&](int off, int rb_row_bytes, int row, int col) {  // a bf16 pair of an input tile
-        const uint32_t o = (rb_row_bytes == C::QRB ? swz<C::QRB>(row, col >> 3) : swz<C::VRB>(row, col >> 3)) +
-                           (col & 7) * 2;
-        return unpack_bf16(*reinterpret_cast<const uint32_t *>(smem + off + o));
+    auto bf_v = [&](int off, int row, int col) {  // a bf16 pair of a [64][64] input tile
+        return unpack_bf16(*reinterpret_cast<const uint32_t *>(smem + off + swz<C::VRB>(row, col >> 3) + (col & 7) * 2));
     };
-
-    const uint8_t *sQ = smem + C::OFF_Q, *sK = smem + C::OFF_K, *sV = smem + C::OFF_V, *sdO = smem + C::OFF_DO;
-    constexpr int QRB = C::QRB, VRB = C::VRB;
-    constexpr int KQ = DK / 16;  // k-steps over the key dimension
+    auto bf_q = [&](int row, int col) {  // a bf16 pair of Q
+        return unpack_bf16(*reinterpret_cast<const uint32_t *>(sQ + swz<C::QRB>(row, col >> 3) + (col & 7) * 2));
+    };
+    // F [16 rows][this warp's 32 columns] += A (rows of a row-major tile, KS k-steps) x B, B from
+    // rows of a tile [n][k] (NK) or from a tile [k][n] (KN); pp = n-tile pair 2 hf + p2
+    auto mma_half_nk = [&](float (&F)[4][4], const uint8_t *at, const uint8_t *bt, auto rb_a, auto rb_b, auto ks) {
+        constexpr int RA = decltype(rb_a)::value, RB = decltype(rb_b)::value, KS = decltype(ks)::value;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            uint32_t a[4];
+            lda_rows<RA>(a, at, wr * 16, kk, lane);
+#pragma unroll
+            for (int p2 = 0; p2 < 2; ++p2) {
+                uint32_t b[4];
+                ldb_nk<RB>(b, bt, 2 * hf + p2, kk, lane);
+                mma16816(F[2 * p2], a, b[0], b[1]);
+                mma16816(F[2 * p2 + 1], a, b[2], b[3]);
+            }
+        }
+    };
+    auto mma_half_kn = [&](float (&F)[4][4], const uint8_t *at, const uint8_t *bt, auto rb_a, auto rb_b, auto ks) {
+        constexpr int RA = decltype(rb_a)::value, RB = decltype(rb_b)::value, KS = decltype(ks)::value;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            uint32_t a[4];
+            lda_rows<RA>(a, at, wr * 16, kk, lane);
+#pragma unroll
+            for (int p2 = 0; p2 < 2; ++p2) {
+                uint32_t b[4];
+                ldb_kn<RB>(b, bt, 2 * hf + p2, kk, lane);
+                mma16816(F[2 * p2], a, b[0], b[1]);
+                mma16816(F[2 * p2 + 1], a, b[2], b[3]);
+            }
+        }
+    };
+    using IQ = std::integral_constant<int, C::QRB>;
+    using IV = std::integral_constant<int, C::VRB>;
+    using K4 = std::integral_constant<int, 4>;        // k-steps over 64 tokens or 64 value columns
+    using KD = std::integral_constant<int, DK / 16>;  // k-steps over the key dimension
+    int rr[2];  // this thread's two rows of the chunk
+    rr[0] = wr * 16 + g;
+    rr[1] = rr[0] + 8;
+    auto colof = [&](int nj) { return (4 * hf + nj) * 8 + 2 * tq; };  // first column of a half-tile pair
 
     load_stage(p.n_chunks - 1);
     cp_async_commit();
@@ -726,10 +788,10 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
 #pragma unroll
         for (int mi = 0; mi < S_MT; ++mi)
 #pragma unroll
-            for (int nj = 0; nj < 8; ++nj)
+            for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int row = s_row(mi, h), col = nj * 8 + 2 * tq;
+                    const int row = s_row(mi, h), col = colof(nj);
                     const uint32_t off = swz<VRB>(row, col >> 3) + (col & 7) * 2;
                     uint32_t hi, lo;
                     split_bf16x2(make_float2(dS[mi][nj][2 * h], dS[mi][nj][2 * h + 1]), hi, lo);
@@ -756,52 +818,40 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
 #pragma unroll
         for (int mi = 0; mi < S_MT; ++mi)
 #pragma unroll
-            for (int nj = 0; nj < 8; ++nj)
+            for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const float2 s = read_parts(C::OFF_SH, C::OFF_SL, s_row(mi, h), nj * 8 + 2 * tq);
+                    const float2 s = read_parts(C::OFF_SH, C::OFF_SL, s_row(mi, h), colof(nj));
                     sd += s.x * dS[mi][nj][2 * h] + s.y * dS[mi][nj][2 * h + 1];
                 }
         __syncthreads();
         const float cL = cs[kDlTc - 1];
-        int rr[2];  // this thread's two rows of the chunk
-        rr[0] = warp * 16 + g;
-        rr[1] = rr[0] + 8;
+        float rt[2] = {0.f, 0.f};   // this warp's row parts of the gradient on c (quad sums)
+        float dbr[2] = {0.f, 0.f};  // this warp's parts of dbeta (quad sums)
+        float esum = 0.f;           // sum of e over this thread's rows (counted once per quad)
 
-        // ---- E = strictly lower (2^(c_r - c_s) k_r . k_s), this warp's rows
+        // ---- E = strictly lower (2^(c_r - c_s) k_r . k_s): rows of this warp, its column half
         {
-            float F[8][4];
-            zero8(F);
-#pragma unroll 2
-            for (int kk = 0; kk < KQ; ++kk) {
-                uint32_t a[4];
-                lda_rows<QRB>(a, sK, warp * 16, kk, lane);
+            float F[4][4];
+            zero4(F);
+            mma_half_nk(F, sK, sK, IQ{}, IQ{}, KD{});
 #pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
-                    uint32_t b[4];
-                    ldb_nk<QRB>(b, sK, pp, kk, lane);
-                    mma_pair(F, pp, a, b);
-                }
-            }
-#pragma unroll
-            for (int nj = 0; nj < 8; ++nj)
+            for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int r = rr[e >> 1], s = nj * 8 + 2 * tq + (e & 1);
-                    Em[r * (kDlTc + 1) + s] = (s < r) ? ex2(cs[r] - cs[s]) * F[nj][e] : 0.f;
+                    const int r = rr[e >> 1], s = colof(nj) + (e & 1);
+                    Em[r * kAS + s] = (s < r) ? ex2(cs[r] - cs[s]) * F[nj][e] : 0.f;
                 }
         }
         __syncthreads();
         // ---- (I + A)^-1 by forward substitution (threads 0..63, one column each), while every
-        // warp forms K S, Yv = V - diag(gamma) K S and X = diag(beta) Yv for its rows
+        // warp forms K S, Yv = V - diag(gamma) K S and X = diag(beta) Yv for its part
         if (tid < kDlTc) {
             const int j = tid;
             float tc[kDlTc];
 #pragma unroll
             for (int r = 0; r < kDlTc; ++r) {
-                float acc = 0.f;
-#pragma unroll
-                for (int s2 = 0; s2 < r; ++s2) acc = fmaf(Em[r * (kDlTc + 1) + s2], tc[s2], acc);
+                const float acc = tri_row_dot(Em + r * kAS, tc, r);
                 tc[r] = (r < j) ? 0.f : (r == j ? 1.f : -bs[r] * acc);
             }
 #pragma unroll
@@ -813,29 +863,18 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
                 *reinterpret_cast<uint16_t *>(smem + C::OFF_TL + off) = (uint16_t)(__float_as_uint(rest) >> 16);
             }
         }
-        float Yv[8][4];
+        float Yv[4][4];
         {
-            zero8(Yv);
-#pragma unroll 2
-            for (int kk = 0; kk < KQ; ++kk) {
-                uint32_t a[4];
-                lda_rows<QRB>(a, sK, warp * 16, kk, lane);
+            zero4(Yv);
+            mma_half_kn(Yv, sK, smem + C::OFF_SH, IQ{}, IV{}, KD{});
+            mma_half_kn(Yv, sK, smem + C::OFF_SL, IQ{}, IV{}, KD{});
+            float X[4][4];
 #pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
-                    uint32_t sh[4], sl[4];
-                    ldb_kn<VRB>(sh, smem + C::OFF_SH, pp, kk, lane);
-                    ldb_kn<VRB>(sl, smem + C::OFF_SL, pp, kk, lane);
-                    mma_pair(Yv, pp, a, sh);
-                    mma_pair(Yv, pp, a, sl);
-                }
-            }
-            float X[8][4];
-#pragma unroll
-            for (int nj = 0; nj < 8; ++nj)
+            for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int r = rr[h];
-                    const float2 vv = bf_pair(C::OFF_V, VRB, r, nj * 8 + 2 * tq);
+                    const float2 vv = bf_v(C::OFF_V, r, colof(nj));
                     const float gm = ex2(cs[r]), bt = bs[r];
                     Yv[nj][2 * h] = vv.x - gm * Yv[nj][2 * h];
                     Yv[nj][2 * h + 1] = vv.y - gm * Yv[nj][2 * h + 1];
@@ -847,26 +886,14 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
         __syncthreads();
         // ---- U = (I + A)^-1 X (three products); U and diag(w) U as bf16 parts
         {
-            float U[8][4];
-            zero8(U);
-#pragma unroll
-            for (int kt = 0; kt < 4; ++kt) {
-                uint32_t th[4], tl[4];
-                lda_rows<VRB>(th, smem + C::OFF_TH, warp * 16, kt, lane);
-                lda_rows<VRB>(tl, smem + C::OFF_TL, warp * 16, kt, lane);
-#pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
-                    uint32_t xh[4], xl[4];
-                    ldb_kn<VRB>(xh, smem + C::OFF_XH, pp, kt, lane);
-                    ldb_kn<VRB>(xl, smem + C::OFF_XL, pp, kt, lane);
-                    mma_pair(U, pp, th, xh);
-                    mma_pair(U, pp, th, xl);
-                    mma_pair(U, pp, tl, xh);
-                }
-            }
+            float U[4][4];
+            zero4(U);
+            mma_half_kn(U, smem + C::OFF_TH, smem + C::OFF_XH, IV{}, IV{}, K4{});
+            mma_half_kn(U, smem + C::OFF_TH, smem + C::OFF_XL, IV{}, IV{}, K4{});
+            mma_half_kn(U, smem + C::OFF_TL, smem + C::OFF_XH, IV{}, IV{}, K4{});
             store_parts(U, C::OFF_UH, C::OFF_UL);
 #pragma unroll
-            for (int nj = 0; nj < 8; ++nj)
+            for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const float w = ex2(cL - cs[rr[h]]);
@@ -876,55 +903,44 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
             store_parts(U, C::OFF_WH, C::OFF_WL);
         }
         __syncthreads();
-
-        // ---- dU = P^T dO + diag(w) K dS' for this warp's rows s; e_s = w_s (K dS')_s . U_s
-        float rt[2];      // the row part of the gradient on c (quad sums: each lane of a quad holds it)
-        float esum = 0.f;  // sum of e over this thread's rows (counted once per quad)
+        // ---- dU = P^T dO + diag(w) K dS' (this warp's column half); e_s = w_s (K dS')_s . U_s
         {
-            float D[8][4];
-            zero8(D);
-#pragma unroll 2
-            for (int kk = 0; kk < KQ; ++kk) {
-                uint32_t a[4];
-                lda_rows<QRB>(a, sK, warp * 16, kk, lane);
-#pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
-                    uint32_t gh[4], gl[4];
-                    ldb_kn<VRB>(gh, smem + C::OFF_GH, pp, kk, lane);
-                    ldb_kn<VRB>(gl, smem + C::OFF_GL, pp, kk, lane);
-                    mma_pair(D, pp, a, gh);
-                    mma_pair(D, pp, a, gl);
-                }
-            }
+            float D[4][4];
+            zero4(D);
+            mma_half_kn(D, sK, smem + C::OFF_GH, IQ{}, IV{}, KD{});
+            mma_half_kn(D, sK, smem + C::OFF_GL, IQ{}, IV{}, KD{});
             float eu[2] = {0.f, 0.f};
 #pragma unroll
-            for (int nj = 0; nj < 8; ++nj)
+            for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const float2 u = read_parts(C::OFF_UH, C::OFF_UL, rr[h], nj * 8 + 2 * tq);
+                    const float2 u = read_parts(C::OFF_UH, C::OFF_UL, rr[h], colof(nj));
                     eu[h] += D[nj][2 * h] * u.x + D[nj][2 * h + 1] * u.y;
                 }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const float w = ex2(cL - cs[rr[h]]);
                 const float e = w * quad_sum(eu[h]);
-                rt[h] = -e;
+                rt[h] -= e;
                 esum += (tq == 0) ? e : 0.f;
 #pragma unroll
-                for (int nj = 0; nj < 8; ++nj) {
+                for (int nj = 0; nj < 4; ++nj) {
                     D[nj][2 * h] *= w;
                     D[nj][2 * h + 1] *= w;
                 }
             }
-            // P^T for this warp's rows s: (K Q^T)_sr 2^(c_r - c_s) for r >= s, as A fragments
+            // P^T for this warp's rows s, all 64 columns r: (K Q^T)_sr 2^(c_r - c_s), r >= s
             uint32_t ph[4][4], pl[4][4];
             {
                 float Pt[8][4];
-                zero8(Pt);
-#pragma unroll 2
+#pragma unroll
+                for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) Pt[nj][e] = 0.f;
+#pragma unroll
                 for (int kk = 0; kk < KQ; ++kk) {
                     uint32_t a[4];
-                    lda_rows<QRB>(a, sK, warp * 16, kk, lane);
+                    lda_rows<QRB>(a, sK, wr * 16, kk, lane);
 #pragma unroll
                     for (int pp = 0; pp < 4; ++pp) {
                         uint32_t b[4];
@@ -945,152 +961,87 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
 #pragma unroll
             for (int kt = 0; kt < 4; ++kt)
 #pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
+                for (int p2 = 0; p2 < 2; ++p2) {
                     uint32_t b[4];
-                    ldb_kn<VRB>(b, sdO, pp, kt, lane);
-                    mma_pair(D, pp, ph[kt], b);
-                    mma_pair(D, pp, pl[kt], b);
+                    ldb_kn<VRB>(b, sdO, 2 * hf + p2, kt, lane);
+                    mma16816(D[2 * p2], ph[kt], b[0], b[1]);
+                    mma16816(D[2 * p2 + 1], ph[kt], b[2], b[3]);
+                    mma16816(D[2 * p2], pl[kt], b[0], b[1]);
+                    mma16816(D[2 * p2 + 1], pl[kt], b[2], b[3]);
                 }
             store_parts(D, C::OFF_XH, C::OFF_XL);  // X is dead: every warp has formed U
         }
         __syncthreads();
-        // ---- dX = (I + A)^-T dU; dV; the dots with Yv and V; Zk = -diag(beta gamma) dX
-        uint32_t xh[4][4], xl[4][4];  // dX as A fragments
-        float dbr[2];
+        // ---- dX = (I + A)^-T dU (this warp's column half); dV; the dots with Yv and V;
+        // Zk = -diag(beta gamma) dX
+        float dXf[4][4];
         {
-            float F[8][4];
-            zero8(F);
+            zero4(dXf);
 #pragma unroll
             for (int kt = 0; kt < 4; ++kt) {
                 uint32_t th[4], tl[4];
-                lda_trans<VRB>(th, smem + C::OFF_TH, warp, kt, lane);
-                lda_trans<VRB>(tl, smem + C::OFF_TL, warp, kt, lane);
+                lda_trans<VRB>(th, smem + C::OFF_TH, wr, kt, lane);
+                lda_trans<VRB>(tl, smem + C::OFF_TL, wr, kt, lane);
 #pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
+                for (int p2 = 0; p2 < 2; ++p2) {
                     uint32_t dh[4], dl[4];
-                    ldb_kn<VRB>(dh, smem + C::OFF_XH, pp, kt, lane);
-                    ldb_kn<VRB>(dl, smem + C::OFF_XL, pp, kt, lane);
-                    mma_pair(F, pp, th, dh);
-                    mma_pair(F, pp, th, dl);
-                    mma_pair(F, pp, tl, dh);
+                    ldb_kn<VRB>(dh, smem + C::OFF_XH, 2 * hf + p2, kt, lane);
+                    ldb_kn<VRB>(dl, smem + C::OFF_XL, 2 * hf + p2, kt, lane);
+                    mma_pair(dXf, p2, th, dh);
+                    mma_pair(dXf, p2, th, dl);
+                    mma_pair(dXf, p2, tl, dh);
                 }
             }
             float ydx[2] = {0.f, 0.f}, vdx[2] = {0.f, 0.f};
+            float Z[4][4];
 #pragma unroll
-            for (int nj = 0; nj < 8; ++nj)
+            for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int r = rr[h], col = nj * 8 + 2 * tq;
+                    const int r = rr[h], col = colof(nj);
                     const long long t = t0 + r;
                     const float bt = bs[r];
+                    const float f0 = dXf[nj][2 * h], f1 = dXf[nj][2 * h + 1];
                     if (t < p.T)
                         *reinterpret_cast<float2 *>(p.dv + (tok0 + t) * p.DV + zb * 64 + col) =
-                            make_float2(bt * F[nj][2 * h], bt * F[nj][2 * h + 1]);
-                    const float2 vv = bf_pair(C::OFF_V, VRB, r, col);
-                    ydx[h] += Yv[nj][2 * h] * F[nj][2 * h] + Yv[nj][2 * h + 1] * F[nj][2 * h + 1];
-                    vdx[h] += vv.x * F[nj][2 * h] + vv.y * F[nj][2 * h + 1];
-                    split_bf16x2(make_float2(F[nj][2 * h], F[nj][2 * h + 1]), xh[nj >> 1][(nj & 1) * 2 + h],
-                                 xl[nj >> 1][(nj & 1) * 2 + h]);
+                            make_float2(bt * f0, bt * f1);
+                    const float2 vv = bf_v(C::OFF_V, r, col);
+                    ydx[h] += Yv[nj][2 * h] * f0 + Yv[nj][2 * h + 1] * f1;
+                    vdx[h] += vv.x * f0 + vv.y * f1;
+                    const float m = -bt * ex2(cs[r]);
+                    Z[nj][2 * h] = m * f0;
+                    Z[nj][2 * h + 1] = m * f1;
                 }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int r = rr[h];
                 const float y = quad_sum(ydx[h]), vx = quad_sum(vdx[h]);
-                rt[h] -= bs[r] * (vx - y);
-                dbr[h] = y;
-                const float m = -bs[r] * ex2(cs[r]);
-#pragma unroll
-                for (int nj = 0; nj < 8; ++nj) {
-                    F[nj][2 * h] *= m;
-                    F[nj][2 * h + 1] *= m;
-                }
+                rt[h] -= bs[rr[h]] * (vx - y);
+                dbr[h] += y;
             }
-            store_parts(F, C::OFF_ZH, C::OFF_ZL);
+            store_parts(Z, C::OFF_ZH, C::OFF_ZL);
         }
         __syncthreads();  // every warp has read (I + A)^-1 and dU
-        // ---- dP = dO U^T (s <= r) with P = (Q K^T) . D; G1 = dP . D; Zq = diag(gamma) dO
-        float rowm[2] = {0.f, 0.f};
-        float colacc[8][2];
+        store_parts(dXf, C::OFF_TH, C::OFF_TL);  // dX, where (I + A)^-1 was
+        __syncthreads();
+        // ---- dA = -dX U^T (s < r) and dP = dO U^T (s <= r) with P = (Q K^T) . D, for this warp's
+        // column half s: dbeta, the gradient on c, F = diag(beta) dA . D, G1 = dP . D
+        float colacc[4][2];
 #pragma unroll
-        for (int nj = 0; nj < 8; ++nj) colacc[nj][0] = colacc[nj][1] = 0.f;
+        for (int nj = 0; nj < 4; ++nj) colacc[nj][0] = colacc[nj][1] = 0.f;
+        float Fm[4][4], G1[4][4];
         {
-            float dP[8][4], P[8][4];
-            zero8(dP);
-            zero8(P);
+            float rowm[2] = {0.f, 0.f}, dba[2] = {0.f, 0.f};
+            zero4(Fm);
+            mma_half_nk(Fm, smem + C::OFF_TH, smem + C::OFF_UH, IV{}, IV{}, K4{});
+            mma_half_nk(Fm, smem + C::OFF_TH, smem + C::OFF_UL, IV{}, IV{}, K4{});
+            mma_half_nk(Fm, smem + C::OFF_TL, smem + C::OFF_UH, IV{}, IV{}, K4{});
 #pragma unroll
-            for (int kt = 0; kt < 4; ++kt) {
-                uint32_t a[4];
-                lda_rows<VRB>(a, sdO, warp * 16, kt, lane);
-#pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
-                    uint32_t uh[4], ul[4];
-                    ldb_nk<VRB>(uh, smem + C::OFF_UH, pp, kt, lane);
-                    ldb_nk<VRB>(ul, smem + C::OFF_UL, pp, kt, lane);
-                    mma_pair(dP, pp, a, uh);
-                    mma_pair(dP, pp, a, ul);
-                }
-            }
-#pragma unroll 2
-            for (int kk = 0; kk < KQ; ++kk) {
-                uint32_t a[4];
-                lda_rows<QRB>(a, sQ, warp * 16, kk, lane);
-#pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
-                    uint32_t b[4];
-                    ldb_nk<QRB>(b, sK, pp, kk, lane);
-                    mma_pair(P, pp, a, b);
-                }
-            }
-#pragma unroll
-            for (int nj = 0; nj < 8; ++nj)
+            for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int r = rr[e >> 1], s = nj * 8 + 2 * tq + (e & 1);
-                    if (s <= r) {
-                        const float d = ex2(cs[r] - cs[s]);
-                        const float m1 = dP[nj][e] * P[nj][e] * d;
-                        rowm[e >> 1] += m1;
-                        colacc[nj][e & 1] += m1;
-                        dP[nj][e] *= d;
-                    } else {
-                        dP[nj][e] = 0.f;
-                    }
-                }
-            store_parts(dP, C::OFF_XH, C::OFF_XL);
-#pragma unroll
-            for (int nj = 0; nj < 8; ++nj)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const float2 vv = bf_pair(C::OFF_DO, VRB, rr[h], nj * 8 + 2 * tq);
-                    const float gm = ex2(cs[rr[h]]);
-                    P[nj][2 * h] = gm * vv.x;
-                    P[nj][2 * h + 1] = gm * vv.y;
-                }
-            store_parts(P, C::OFF_TH, C::OFF_TL);  // Zq, where (I + A)^-1 was
-        }
-        // ---- dA = -dX U^T (s < r); dbeta and the gradient on c; F = diag(beta) dA . D
-        float Fm[8][4];
-        float dba[2] = {0.f, 0.f};
-        {
-            zero8(Fm);
-#pragma unroll
-            for (int kt = 0; kt < 4; ++kt)
-#pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
-                    uint32_t uh[4], ul[4];
-                    ldb_nk<VRB>(uh, smem + C::OFF_UH, pp, kt, lane);
-                    ldb_nk<VRB>(ul, smem + C::OFF_UL, pp, kt, lane);
-                    mma_pair(Fm, pp, xh[kt], uh);
-                    mma_pair(Fm, pp, xh[kt], ul);
-                    mma_pair(Fm, pp, xl[kt], uh);
-                }
-#pragma unroll
-            for (int nj = 0; nj < 8; ++nj)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = rr[e >> 1], s = nj * 8 + 2 * tq + (e & 1);
+                    const int r = rr[e >> 1], s = colof(nj) + (e & 1);
                     if (s < r) {
-                        const float Ers = Em[r * (kDlTc + 1) + s];
+                        const float Ers = Em[r * kAS + s];
                         const float dA = -Fm[nj][e], bt = bs[r];
                         dba[e >> 1] += dA * Ers;
                         const float m2 = dA * bt * Ers;
@@ -1101,30 +1052,60 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
                         Fm[nj][e] = 0.f;
                     }
                 }
-        }
+            zero4(G1);
+            mma_half_nk(G1, sdO, smem + C::OFF_UH, IV{}, IV{}, K4{});
+            mma_half_nk(G1, sdO, smem + C::OFF_UL, IV{}, IV{}, K4{});
+            float P[4][4];
+            zero4(P);
+            mma_half_nk(P, sQ, sK, IQ{}, IQ{}, KD{});
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            rt[h] += quad_sum(rowm[h]);
-            dbr[h] += quad_sum(dba[h]);
-        }
-        __syncthreads();  // every warp has read E
-        store_parts(Fm, C::OFF_FH, C::OFF_FL);
-
-        // row and column parts of the gradient on c, dbeta, the last position's extra term
+            for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
-        for (int nj = 0; nj < 8; ++nj)
+                for (int e = 0; e < 4; ++e) {
+                    const int r = rr[e >> 1], s = colof(nj) + (e & 1);
+                    if (s <= r) {
+                        const float d = ex2(cs[r] - cs[s]);
+                        const float m1 = G1[nj][e] * P[nj][e] * d;
+                        rowm[e >> 1] += m1;
+                        colacc[nj][e & 1] += m1;
+                        G1[nj][e] *= d;
+                    } else {
+                        G1[nj][e] = 0.f;
+                    }
+                }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                rt[h] += quad_sum(rowm[h]);
+                dbr[h] += quad_sum(dba[h]);
+            }
+        }
+        __syncthreads();  // every warp has read E, dX and dU
+        store_parts(Fm, C::OFF_FH, C::OFF_FL);  // F, where E was
+        store_parts(G1, C::OFF_XH, C::OFF_XL);  // dP . D, where dU was
+        {
+            float Zq[4][4];  // diag(gamma) dO, where dX was
+#pragma unroll
+            for (int nj = 0; nj < 4; ++nj)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float2 vv = bf_v(C::OFF_DO, rr[h], colof(nj));
+                    const float gm = ex2(cs[rr[h]]);
+                    Zq[nj][2 * h] = gm * vv.x;
+                    Zq[nj][2 * h + 1] = gm * vv.y;
+                }
+            store_parts(Zq, C::OFF_TH, C::OFF_TL);
+        }
+        // column parts of the gradient on c (this warp's 32 columns), the last position's extra
+#pragma unroll
+        for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 float x = colacc[nj][c];
                 x += __shfl_xor_sync(0xffffffffu, x, 4);
                 x += __shfl_xor_sync(0xffffffffu, x, 8);
                 x += __shfl_xor_sync(0xffffffffu, x, 16);
-                if (g == 0) colp[warp * kDlTc + nj * 8 + 2 * tq + c] = x;
+                if (g == 0) colp[warp * kDlTc + colof(nj) + c] = x;
             }
-        if (tq == 0) {
-            dbs[rr[0]] = dbr[0];
-            dbs[rr[1]] = dbr[1];
-        }
         {
             float ex = esum + ex2(cL) * sd;
 #pragma unroll
@@ -1132,32 +1113,34 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
             if (lane == 0) red[warp] = ex;
         }
         __syncthreads();  // F, G1, Zq in shared memory
-        // ---- dQ = G1 K + diag(gamma) dO S^T, and gamma_r q_r . (dO S^T)_r
+        // ---- dQ = G1 K + diag(gamma) dO S^T (this warp's half of the DK columns), and
+        // gamma_r q_r . (dO S^T)_r
         {
-            float Acc[NQ][4];
+            float Acc[NQ2][4];
 #pragma unroll
-            for (int j = 0; j < NQ; ++j)
+            for (int j = 0; j < NQ2; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) Acc[j][e] = 0.f;
+            constexpr int PP = DK / 32;  // n-tile pairs of a half
 #pragma unroll
             for (int kt = 0; kt < 4; ++kt) {
                 uint32_t a[4];
-                lda_rows<VRB>(a, sdO, warp * 16, kt, lane);
+                lda_rows<VRB>(a, sdO, wr * 16, kt, lane);
 #pragma unroll
-                for (int pp = 0; pp < DK / 16; ++pp) {
+                for (int p2 = 0; p2 < PP; ++p2) {
                     uint32_t sh[4], sl[4];
-                    ldb_nk<VRB>(sh, smem + C::OFF_SH, pp, kt, lane);
-                    ldb_nk<VRB>(sl, smem + C::OFF_SL, pp, kt, lane);
-                    mma_pair(Acc, pp, a, sh);
-                    mma_pair(Acc, pp, a, sl);
+                    ldb_nk<VRB>(sh, smem + C::OFF_SH, hf * PP + p2, kt, lane);
+                    ldb_nk<VRB>(sl, smem + C::OFF_SL, hf * PP + p2, kt, lane);
+                    mma_pair(Acc, p2, a, sh);
+                    mma_pair(Acc, p2, a, sl);
                 }
             }
             float qd[2] = {0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < NQ; ++j)
+            for (int j = 0; j < NQ2; ++j)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const float2 qq = bf_pair(C::OFF_Q, QRB, rr[h], j * 8 + 2 * tq);
+                    const float2 qq = bf_q(rr[h], (hf * NQ2 + j) * 8 + 2 * tq);
                     qd[h] += qq.x * Acc[j][2 * h] + qq.y * Acc[j][2 * h + 1];
                 }
 #pragma unroll
@@ -1165,7 +1148,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
                 const float gm = ex2(cs[rr[h]]);
                 rt[h] += gm * quad_sum(qd[h]);
 #pragma unroll
-                for (int j = 0; j < NQ; ++j) {
+                for (int j = 0; j < NQ2; ++j) {
                     Acc[j][2 * h] *= gm;
                     Acc[j][2 * h + 1] *= gm;
                 }
@@ -1173,98 +1156,101 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
 #pragma unroll
             for (int kt = 0; kt < 4; ++kt) {
                 uint32_t ah[4], al[4];
-                lda_rows<VRB>(ah, smem + C::OFF_XH, warp * 16, kt, lane);
-                lda_rows<VRB>(al, smem + C::OFF_XL, warp * 16, kt, lane);
+                lda_rows<VRB>(ah, smem + C::OFF_XH, wr * 16, kt, lane);
+                lda_rows<VRB>(al, smem + C::OFF_XL, wr * 16, kt, lane);
 #pragma unroll
-                for (int pp = 0; pp < DK / 16; ++pp) {
+                for (int p2 = 0; p2 < PP; ++p2) {
                     uint32_t b[4];
-                    ldb_kn<QRB>(b, sK, pp, kt, lane);
-                    mma_pair(Acc, pp, ah, b);
-                    mma_pair(Acc, pp, al, b);
+                    ldb_kn<QRB>(b, sK, hf * PP + p2, kt, lane);
+                    mma_pair(Acc, p2, ah, b);
+                    mma_pair(Acc, p2, al, b);
                 }
             }
 #pragma unroll
-            for (int j = 0; j < NQ; ++j)
+            for (int j = 0; j < NQ2; ++j)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const long long t = t0 + rr[h];
                     if (t < p.T)
-                        *reinterpret_cast<float2 *>(dq_out + (size_t)t * DK + j * 8 + 2 * tq) =
+                        *reinterpret_cast<float2 *>(dq_out + (size_t)t * DK + (hf * NQ2 + j) * 8 + 2 * tq) =
                             make_float2(Acc[j][2 * h], Acc[j][2 * h + 1]);
                 }
         }
         if (tq == 0) {
-            rowp[rr[0]] = rt[0];
-            rowp[rr[1]] = rt[1];
+            rowp[hf * kDlTc + rr[0]] = rt[0];
+            rowp[hf * kDlTc + rr[1]] = rt[1];
+            dbs[hf * kDlTc + rr[0]] = dbr[0];
+            dbs[hf * kDlTc + rr[1]] = dbr[1];
         }
-        // ---- dK = G1^T Q + (F^T + F) K + diag(w) U dS'^T + Zk S^T
+        // ---- dK = G1^T Q + (F^T + F) K + diag(w) U dS'^T + Zk S^T (this warp's half of DK)
         {
-            float Acc[NQ][4];
+            float Acc[NQ2][4];
 #pragma unroll
-            for (int j = 0; j < NQ; ++j)
+            for (int j = 0; j < NQ2; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) Acc[j][e] = 0.f;
+            constexpr int PP = DK / 32;
 #pragma unroll 1
             for (int kt = 0; kt < 4; ++kt) {  // k over the chunk's tokens
                 uint32_t gh[4], gl[4], fth[4], ftl[4], fh[4], fl[4];
-                lda_trans<VRB>(gh, smem + C::OFF_XH, warp, kt, lane);
-                lda_trans<VRB>(gl, smem + C::OFF_XL, warp, kt, lane);
-                lda_trans<VRB>(fth, smem + C::OFF_FH, warp, kt, lane);
-                lda_trans<VRB>(ftl, smem + C::OFF_FL, warp, kt, lane);
-                lda_rows<VRB>(fh, smem + C::OFF_FH, warp * 16, kt, lane);
-                lda_rows<VRB>(fl, smem + C::OFF_FL, warp * 16, kt, lane);
+                lda_trans<VRB>(gh, smem + C::OFF_XH, wr, kt, lane);
+                lda_trans<VRB>(gl, smem + C::OFF_XL, wr, kt, lane);
+                lda_trans<VRB>(fth, smem + C::OFF_FH, wr, kt, lane);
+                lda_trans<VRB>(ftl, smem + C::OFF_FL, wr, kt, lane);
+                lda_rows<VRB>(fh, smem + C::OFF_FH, wr * 16, kt, lane);
+                lda_rows<VRB>(fl, smem + C::OFF_FL, wr * 16, kt, lane);
 #pragma unroll
-                for (int pp = 0; pp < DK / 16; ++pp) {
+                for (int p2 = 0; p2 < PP; ++p2) {
                     uint32_t bq[4], bk[4];
-                    ldb_kn<QRB>(bq, sQ, pp, kt, lane);
-                    ldb_kn<QRB>(bk, sK, pp, kt, lane);
-                    mma_pair(Acc, pp, gh, bq);
-                    mma_pair(Acc, pp, gl, bq);
-                    mma_pair(Acc, pp, fth, bk);
-                    mma_pair(Acc, pp, ftl, bk);
-                    mma_pair(Acc, pp, fh, bk);
-                    mma_pair(Acc, pp, fl, bk);
+                    ldb_kn<QRB>(bq, sQ, hf * PP + p2, kt, lane);
+                    ldb_kn<QRB>(bk, sK, hf * PP + p2, kt, lane);
+                    mma_pair(Acc, p2, gh, bq);
+                    mma_pair(Acc, p2, gl, bq);
+                    mma_pair(Acc, p2, fth, bk);
+                    mma_pair(Acc, p2, ftl, bk);
+                    mma_pair(Acc, p2, fh, bk);
+                    mma_pair(Acc, p2, fl, bk);
                 }
             }
 #pragma unroll 1
             for (int kt = 0; kt < 4; ++kt) {  // k over the 64 value columns
                 uint32_t wh[4], wl[4], zh[4], zl[4];
-                lda_rows<VRB>(wh, smem + C::OFF_WH, warp * 16, kt, lane);
-                lda_rows<VRB>(wl, smem + C::OFF_WL, warp * 16, kt, lane);
-                lda_rows<VRB>(zh, smem + C::OFF_ZH, warp * 16, kt, lane);
-                lda_rows<VRB>(zl, smem + C::OFF_ZL, warp * 16, kt, lane);
+                lda_rows<VRB>(wh, smem + C::OFF_WH, wr * 16, kt, lane);
+                lda_rows<VRB>(wl, smem + C::OFF_WL, wr * 16, kt, lane);
+                lda_rows<VRB>(zh, smem + C::OFF_ZH, wr * 16, kt, lane);
+                lda_rows<VRB>(zl, smem + C::OFF_ZL, wr * 16, kt, lane);
 #pragma unroll
-                for (int pp = 0; pp < DK / 16; ++pp) {
+                for (int p2 = 0; p2 < PP; ++p2) {
                     uint32_t b1[4], b2[4];
-                    ldb_nk<VRB>(b1, smem + C::OFF_GH, pp, kt, lane);
-                    ldb_nk<VRB>(b2, smem + C::OFF_GL, pp, kt, lane);
-                    mma_pair(Acc, pp, wh, b1);
-                    mma_pair(Acc, pp, wh, b2);
-                    mma_pair(Acc, pp, wl, b1);
-                    ldb_nk<VRB>(b1, smem + C::OFF_SH, pp, kt, lane);
-                    ldb_nk<VRB>(b2, smem + C::OFF_SL, pp, kt, lane);
-                    mma_pair(Acc, pp, zh, b1);
-                    mma_pair(Acc, pp, zh, b2);
-                    mma_pair(Acc, pp, zl, b1);
+                    ldb_nk<VRB>(b1, smem + C::OFF_GH, hf * PP + p2, kt, lane);
+                    ldb_nk<VRB>(b2, smem + C::OFF_GL, hf * PP + p2, kt, lane);
+                    mma_pair(Acc, p2, wh, b1);
+                    mma_pair(Acc, p2, wh, b2);
+                    mma_pair(Acc, p2, wl, b1);
+                    ldb_nk<VRB>(b1, smem + C::OFF_SH, hf * PP + p2, kt, lane);
+                    ldb_nk<VRB>(b2, smem + C::OFF_SL, hf * PP + p2, kt, lane);
+                    mma_pair(Acc, p2, zh, b1);
+                    mma_pair(Acc, p2, zh, b2);
+                    mma_pair(Acc, p2, zl, b1);
                 }
             }
 #pragma unroll
-            for (int j = 0; j < NQ; ++j)
+            for (int j = 0; j < NQ2; ++j)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const long long t = t0 + rr[h];
                     if (t < p.T)
-                        *reinterpret_cast<float2 *>(dk_out + (size_t)t * DK + j * 8 + 2 * tq) =
+                        *reinterpret_cast<float2 *>(dk_out + (size_t)t * DK + (hf * NQ2 + j) * 8 + 2 * tq) =
                             make_float2(Acc[j][2 * h], Acc[j][2 * h + 1]);
                 }
         }
-        // ---- dS = gamma_L dS' + Q^T Zq + K^T Zk   (two products each)
+        // ---- dS = gamma_L dS' + Q^T Zq + K^T Zk   (two products each; this warp's part)
         {
             const float gL = ex2(cL);
 #pragma unroll
             for (int mi = 0; mi < S_MT; ++mi)
 #pragma unroll
-                for (int nj = 0; nj < 8; ++nj)
+                for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) dS[mi][nj][e] *= gL;
 #pragma unroll 1
@@ -1274,20 +1260,20 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
                     const uint8_t *zt_h = smem + (which ? C::OFF_ZH : C::OFF_TH);
                     const uint8_t *zt_l = smem + (which ? C::OFF_ZL : C::OFF_TL);
                     const uint8_t *yt = which ? sK : sQ;
-                    uint32_t b[4][4], bl[4][4];
+                    uint32_t b[2][4], bl[2][4];
 #pragma unroll
-                    for (int pp = 0; pp < 4; ++pp) {
-                        ldb_kn<VRB>(b[pp], zt_h, pp, kt, lane);
-                        ldb_kn<VRB>(bl[pp], zt_l, pp, kt, lane);
+                    for (int p2 = 0; p2 < 2; ++p2) {
+                        ldb_kn<VRB>(b[p2], zt_h, 2 * hf + p2, kt, lane);
+                        ldb_kn<VRB>(bl[p2], zt_l, 2 * hf + p2, kt, lane);
                     }
 #pragma unroll
                     for (int mi = 0; mi < S_MT; ++mi) {
                         uint32_t a[4];
-                        lda_trans<QRB>(a, yt, warp * S_MT + mi, kt, lane);
+                        lda_trans<QRB>(a, yt, wr * S_MT + mi, kt, lane);
 #pragma unroll
-                        for (int pp = 0; pp < 4; ++pp) {
-                            mma_pair(dS[mi], pp, a, b[pp]);
-                            mma_pair(dS[mi], pp, a, bl[pp]);
+                        for (int p2 = 0; p2 < 2; ++p2) {
+                            mma_pair(dS[mi], p2, a, b[p2]);
+                            mma_pair(dS[mi], p2, a, bl[p2]);
                         }
                     }
                 }
@@ -1295,26 +1281,34 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
         __syncthreads();  // row parts, column parts, dbeta
         // ---- the gradient on c -> suffix sums in the chunk -> dlog_a; dbeta (warp 0, two rows a lane)
         if (warp == 0) {
-            const float extra = red[0] + red[1] + red[2] + red[3];
-            const int r0 = 2 * lane;
-            float d0 = rowp[r0] - (colp[r0] + colp[kDlTc + r0] + colp[2 * kDlTc + r0] + colp[3 * kDlTc + r0]);
-            float d1 = rowp[r0 + 1] -
-                       (colp[r0 + 1] + colp[kDlTc + r0 + 1] + colp[2 * kDlTc + r0 + 1] + colp[3 * kDlTc + r0 + 1]);
-            if (lane == 31) d1 += extra;
-            float tot = d0 + d1;
+            float extra = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDlBwdThreads / 32; ++w) extra += red[w];
+            float d[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int r = 2 * lane + u;
+                float cp = 0.f;  // the four warps of column r's half
+#pragma unroll
+                for (int w = 0; w < 4; ++w) cp += colp[(4 * (r >> 5) + w) * kDlTc + r];
+                d[u] = (rowp[r] + rowp[kDlTc + r]) - cp;
+            }
+            if (lane == 31) d[1] += extra;
+            float tot = d[0] + d[1];
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const float o = __shfl_down_sync(0xffffffffu, tot, off);
                 if (lane + off < 32) tot += o;
             }
+            const int r0 = 2 * lane;
             const long long ta = t0 + r0;
             if (ta < p.T) {
                 dl_out[ta] = tot;
-                db_out[ta] = dbs[r0];
+                db_out[ta] = dbs[r0] + dbs[kDlTc + r0];
             }
             if (ta + 1 < p.T) {
-                dl_out[ta + 1] = tot - d0;
-                db_out[ta + 1] = dbs[r0 + 1];
+                dl_out[ta + 1] = tot - d[0];
+                db_out[ta + 1] = dbs[r0 + 1] + dbs[kDlTc + r0 + 1];
             }
         }
         __syncthreads();  // before the next chunk's loads overwrite shared memory
@@ -1326,11 +1320,11 @@ __global__ void __launch_bounds__(kDlThreads, 1) delta_bwd_kernel(const DeltaBwd
 #pragma unroll
         for (int mi = 0; mi < S_MT; ++mi)
 #pragma unroll
-            for (int nj = 0; nj < 8; ++nj)
+            for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    *reinterpret_cast<float2 *>(p.dS0 + ((size_t)bh * DK + s_row(mi, h)) * p.DV + zb * 64 + nj * 8 +
-                                                2 * tq) = make_float2(dS[mi][nj][2 * h], dS[mi][nj][2 * h + 1]);
+                    *reinterpret_cast<float2 *>(p.dS0 + ((size_t)bh * DK + s_row(mi, h)) * p.DV + zb * 64 +
+                                                colof(nj)) = make_float2(dS[mi][nj][2 * h], dS[mi][nj][2 * h + 1]);
     }
 }
 
@@ -1365,7 +1359,7 @@ int launch_delta_bwd(const DeltaBwdArgs &a, cudaStream_t s, unsigned int grid) {
     static std::atomic<unsigned long long> smem_set{0};
     const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(delta_bwd_kernel<DK>), C::SMEM);
     if (st) return st;
-    delta_bwd_kernel<DK><<<grid, kDlThreads, C::SMEM, s>>>(a);
+    delta_bwd_kernel<DK><<<grid, kDlBwdThreads, C::SMEM, s>>>(a);
     return check_launch("delta_bwd_kernel");
 }
 
