@@ -43,7 +43,8 @@ constexpr float kGlaLog2e = 1.4426950408889634f;
 constexpr int kGlaTc = 64;        // tokens per chunk
 constexpr int kGlaMid = 31;       // reference token of a chunk
 constexpr float kGlaSpan = 120.f; // largest |c_t - c_mid| (log2) the operand scalings allow
-constexpr int kGlaThreads = 128;  // warp w: rows 16w..16w+15 of a chunk, state rows 16(w S_MT)..
+constexpr int kGlaThreads = 128;  // backward: warp w rows 16w..16w+15 of a chunk, state rows 16w..
+constexpr int kGlaFwdThreads = 256;  // forward: warp w rows 16(w & 3).. of a chunk, column / token half w >> 2
 constexpr int kGlaSegChoices[4] = {64, 32, 16, 8};
 constexpr long long kGlaMinBlocks = 1024;
 
@@ -66,9 +67,9 @@ struct GlaCfg {
     static constexpr int OFF_SH = OFF_KLO + Q_BYTES;      // S' = diag(2^c_m) S, high part, [DK][64]
     static constexpr int OFF_SL = OFF_SH + DK * VRB;      // and its low part
     static constexpr int OFF_AS = OFF_SL + DK * VRB;      // alpha of the segment per key dimension
-    static constexpr int SMEM = OFF_AS + DK * 4;
-    static constexpr int S_MT = DK / 64;  // 16-row state tiles per warp (DK / 16 over 4 warps)
-    static constexpr int S_NT = 8;        // 8-column state tiles: all 64 columns
+    static constexpr int OFF_XO = OFF_AS + DK * 4;        // partial outputs exchanged between the token halves
+    static constexpr int SMEM = OFF_XO + 8 * 16 * 32 * 4;
+    static constexpr int S_MT = DK / 64;  // 16-row state tiles per row group (DK / 16 over 4 groups)
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
@@ -94,12 +95,13 @@ struct GlaArgs {
 };
 
 template <int DK>
-__global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p) {
+__global__ void __launch_bounds__(kGlaFwdThreads, 1) gla_fwd_kernel(const GlaArgs p) {
     using C = GlaCfg<DK>;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ unsigned int s_ticket, s_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tq = lane & 3;
+    const int wr = warp & 3, hf = warp >> 2;  // row group, column half
     if (tid == 0) s_ticket = atomicAdd(&p.hdr->ticket[0], 1u);
     __syncthreads();
     const unsigned int tk = s_ticket;
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
         uint8_t *st = smem + stage * C::STAGE;
         const long long t0 = (long long)chunk * kGlaTc;
         constexpr int QC = C::QRB / 16, GC = C::GRB / 16;
-        for (int i = tid; i < kGlaTc * QC; i += kGlaThreads) {
+        for (int i = tid; i < kGlaTc * QC; i += kGlaFwdThreads) {
             const int row = i / QC, c16 = i % QC;
             const long long t = t0 + row;
             const bool ok = t < p.T;
@@ -132,14 +134,14 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
             cp_async16(smem_u32(st + C::OFF_K + swz<C::QRB>(row, c16)), Kb + off, ok ? 16u : 0u);
             if (withQ) cp_async16(smem_u32(st + C::OFF_Q + swz<C::QRB>(row, c16)), Qb + off, ok ? 16u : 0u);
         }
-        for (int i = tid; i < kGlaTc * 8; i += kGlaThreads) {
+        for (int i = tid; i < kGlaTc * 8; i += kGlaFwdThreads) {
             const int row = i >> 3, c16 = i & 7;
             const long long t = t0 + row;
             const bool ok = t < p.T;
             cp_async16(smem_u32(st + C::OFF_V + swz<C::VRB>(row, c16)),
                        Vb + (size_t)(ok ? arow_of(t) : 0) * p.DV + c16 * 8, ok ? 16u : 0u);
         }
-        for (int i = tid; i < kGlaTc * GC; i += kGlaThreads) {  // padding tokens: log a = 0
+        for (int i = tid; i < kGlaTc * GC; i += kGlaFwdThreads) {  // padding tokens: log a = 0
             const int row = i / GC, c16 = i % GC;
             const long long t = t0 + row;
             const bool ok = t < p.T && !(p.rev && t == 0);
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
         uint8_t *st = smem + stage * C::STAGE;
         const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
         constexpr int QC = C::QRB / 16;
-        for (int i = tid; i < kGlaTc * QC; i += kGlaThreads) {
+        for (int i = tid; i < kGlaTc * QC; i += kGlaFwdThreads) {
             const int row = i / QC, c16 = i % QC;
             const float4 *crow = reinterpret_cast<const float4 *>(G + row * DK + c16 * 8);
             const float4 *cmid = reinterpret_cast<const float4 *>(G + kGlaMid * DK + c16 * 8);
@@ -217,12 +219,12 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
         }
     };
 
-    // State fragments: warp w owns rows (key dimensions) 16(w S_MT + mi) + {g, g + 8} and the
-    // columns of all 8 m16n8 tiles.
-    constexpr int S_MT = C::S_MT, S_NT = C::S_NT;
+    // State fragments: warp w owns rows (key dimensions) 16((w & 3) S_MT + mi) + {g, g + 8} and
+    // the columns of m16n8 tiles 4 (w >> 2) .. 4 (w >> 2) + 3 (its half of the 64 columns).
+    constexpr int S_MT = C::S_MT, S_NT = 4;
     float S[S_MT][S_NT][4];
-    auto s_row = [&](int mi, int h) { return (warp * S_MT + mi) * 16 + g + h * 8; };
-    auto s_col = [&](int nj, int e) { return nj * 8 + tq * 2 + (e & 1); };
+    auto s_row = [&](int mi, int h) { return (wr * S_MT + mi) * 16 + g + h * 8; };
+    auto s_col = [&](int nj, int e) { return (4 * hf + nj) * 8 + tq * 2 + (e & 1); };
     auto zero_state = [&](float (&X)[S_MT][S_NT][4]) {
 #pragma unroll
         for (int mi = 0; mi < S_MT; ++mi)
@@ -275,12 +277,12 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
 #pragma unroll
             for (int pp = 0; pp < S_NT / 2; ++pp) {
                 const int brow = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                ldsm_x4_t(smem_u32(st + C::OFF_V + swz<C::VRB>(brow, 2 * pp + (lane >> 4))), b[pp]);
+                ldsm_x4_t(smem_u32(st + C::OFF_V + swz<C::VRB>(brow, 2 * (2 * hf + pp) + (lane >> 4))), b[pp]);
             }
 #pragma unroll
             for (int mi = 0; mi < S_MT; ++mi) {
                 const int arow = kt * 16 + (lane & 7) + (lane >> 4) * 8;
-                const int ac16 = 2 * (warp * S_MT + mi) + ((lane >> 3) & 1);
+                const int ac16 = 2 * (wr * S_MT + mi) + ((lane >> 3) & 1);
                 uint32_t ah[4], al[4];
                 ldsm_x4_t(smem_u32(st + C::OFF_K + swz<C::QRB>(arow, ac16)), ah);
                 ldsm_x4_t(smem_u32(smem + C::OFF_KLO + swz<C::QRB>(arow, ac16)), al);
@@ -334,7 +336,7 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
 
     // ------------------------------------------------ look-back for the incoming state
     constexpr int TILES = S_MT * S_NT;
-    auto ws_index = [&](size_t u, int tile) { return u * (size_t)(TILES * kGlaThreads) + (size_t)tile * kGlaThreads + tid; };
+    auto ws_index = [&](size_t u, int tile) { return u * (size_t)(TILES * kGlaFwdThreads) + (size_t)tile * kGlaFwdThreads + tid; };
     float Sin[S_MT][S_NT][4];
     auto add_state0 = [&](const float (&scale)[S_MT][2]) {
         if (p.S0 == nullptr) return;
@@ -441,66 +443,83 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
         write_sb();
         __syncthreads();
 
-        // scores of this warp's 16 rows against the chunk's 64 tokens: Q~ K~^T (three products)
-        float P[8][4];
-#pragma unroll
-        for (int nj = 0; nj < 8; ++nj)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) P[nj][e] = 0.f;
-        const int arow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll 2
-        for (int kk = 0; kk < DK / 16; ++kk) {
-            uint32_t qh[4], ql[4];
-            const uint32_t aoff = swz<C::QRB>(arow, 2 * kk + (lane >> 4));
-            ldsm_x4(smem_u32(st + C::OFF_Q + aoff), qh);
-            ldsm_x4(smem_u32(smem + C::OFF_QLO + aoff), ql);
-#pragma unroll
-            for (int pp = 0; pp < 4; ++pp) {
-                const int brow = 16 * pp + (lane & 7) + (lane >> 4) * 8;
-                const uint32_t boff = swz<C::QRB>(brow, 2 * kk + ((lane >> 3) & 1));
-                uint32_t kh[4], kl[4];
-                ldsm_x4(smem_u32(st + C::OFF_K + boff), kh);
-                ldsm_x4(smem_u32(smem + C::OFF_KLO + boff), kl);
-                mma16816(P[2 * pp], qh, kh[0], kh[1]);
-                mma16816(P[2 * pp + 1], qh, kh[2], kh[3]);
-                mma16816(P[2 * pp], qh, kl[0], kl[1]);
-                mma16816(P[2 * pp + 1], qh, kl[2], kl[3]);
-                mma16816(P[2 * pp], ql, kh[0], kh[1]);
-                mma16816(P[2 * pp + 1], ql, kh[2], kh[3]);
-            }
-        }
-        // causal mask (token s <= row r), then the masked scores as A fragments in two parts
-        uint32_t ph[4][4], pl[4][4];
-#pragma unroll
-        for (int nj = 0; nj < 8; ++nj)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = warp * 16 + g + 8 * h, s = nj * 8 + 2 * tq;
-                const float x0 = (s <= r) ? P[nj][2 * h] : 0.f;
-                const float x1 = (s + 1 <= r) ? P[nj][2 * h + 1] : 0.f;
-                // A fragment of k-step nj / 2: regs {row g, k lo}, {g + 8, lo}, {g, hi}, {g + 8, hi}
-                split_bf16x2(make_float2(x0, x1), ph[nj >> 1][(nj & 1) * 2 + h], pl[nj >> 1][(nj & 1) * 2 + h]);
-            }
-        float O[8][4];
+        // Scores of this warp's 16 rows against its half of the chunk's tokens (s in 32 hf ..
+        // 32 hf + 31): Q~ K~^T (three products), causal mask (s <= r), then P V over those
+        // tokens for all 64 columns; a half that lies after every row of the group is skipped.
+        const int arow = wr * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        float O[8][4];  // this warp's partial output: its token half, all 64 columns
 #pragma unroll
         for (int nj = 0; nj < 8; ++nj)
 #pragma unroll
             for (int e = 0; e < 4; ++e) O[nj][e] = 0.f;
-        // O = P V (two products) ...
+        if (32 * hf <= wr * 16 + 15) {
+            float P[4][4];
 #pragma unroll
-        for (int kt = 0; kt < 4; ++kt) {
+            for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
-            for (int pp = 0; pp < 4; ++pp) {
-                uint32_t b[4];
-                const int brow = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                ldsm_x4_t(smem_u32(st + C::OFF_V + swz<C::VRB>(brow, 2 * pp + (lane >> 4))), b);
-                mma16816(O[2 * pp], ph[kt], b[0], b[1]);
-                mma16816(O[2 * pp + 1], ph[kt], b[2], b[3]);
-                mma16816(O[2 * pp], pl[kt], b[0], b[1]);
-                mma16816(O[2 * pp + 1], pl[kt], b[2], b[3]);
+                for (int e = 0; e < 4; ++e) P[nj][e] = 0.f;
+#pragma unroll 2
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                uint32_t qh[4], ql[4];
+                const uint32_t aoff = swz<C::QRB>(arow, 2 * kk + (lane >> 4));
+                ldsm_x4(smem_u32(st + C::OFF_Q + aoff), qh);
+                ldsm_x4(smem_u32(smem + C::OFF_QLO + aoff), ql);
+#pragma unroll
+                for (int p2 = 0; p2 < 2; ++p2) {
+                    const int brow = 16 * (2 * hf + p2) + (lane & 7) + (lane >> 4) * 8;
+                    const uint32_t boff = swz<C::QRB>(brow, 2 * kk + ((lane >> 3) & 1));
+                    uint32_t kh[4], kl[4];
+                    ldsm_x4(smem_u32(st + C::OFF_K + boff), kh);
+                    ldsm_x4(smem_u32(smem + C::OFF_KLO + boff), kl);
+                    mma16816(P[2 * p2], qh, kh[0], kh[1]);
+                    mma16816(P[2 * p2 + 1], qh, kh[2], kh[3]);
+                    mma16816(P[2 * p2], qh, kl[0], kl[1]);
+                    mma16816(P[2 * p2 + 1], qh, kl[2], kl[3]);
+                    mma16816(P[2 * p2], ql, kh[0], kh[1]);
+                    mma16816(P[2 * p2 + 1], ql, kh[2], kh[3]);
+                }
+            }
+            // the masked scores as A fragments (two k-steps of 16 tokens) in two parts
+            uint32_t ph[2][4], pl[2][4];
+#pragma unroll
+            for (int nj = 0; nj < 4; ++nj)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int r = wr * 16 + g + 8 * h, s = (4 * hf + nj) * 8 + 2 * tq;
+                    const float x0 = (s <= r) ? P[nj][2 * h] : 0.f;
+                    const float x1 = (s + 1 <= r) ? P[nj][2 * h + 1] : 0.f;
+                    // A fragment of k-step nj / 2: regs {row g, k lo}, {g + 8, lo}, {g, hi}, {g + 8, hi}
+                    split_bf16x2(make_float2(x0, x1), ph[nj >> 1][(nj & 1) * 2 + h], pl[nj >> 1][(nj & 1) * 2 + h]);
+                }
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt) {
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {
+                    uint32_t b[4];
+                    const int brow = (2 * hf + kt) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    ldsm_x4_t(smem_u32(st + C::OFF_V + swz<C::VRB>(brow, 2 * pp + (lane >> 4))), b);
+                    mma16816(O[2 * pp], ph[kt], b[0], b[1]);
+                    mma16816(O[2 * pp + 1], ph[kt], b[2], b[3]);
+                    mma16816(O[2 * pp], pl[kt], b[0], b[1]);
+                    mma16816(O[2 * pp + 1], pl[kt], b[2], b[3]);
+                }
             }
         }
-        // ... + Q~ S' (three products)
+        // the other column half of the partial output goes to the partner warp (w ^ 4)
+        float *xo = reinterpret_cast<float *>(smem + C::OFF_XO);  // [8 warps][16 rows][32 columns]
+#pragma unroll
+        for (int nj = 0; nj < 4; ++nj)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                *reinterpret_cast<float2 *>(xo + (warp * 16 + g + 8 * h) * 32 + nj * 8 + 2 * tq) =
+                    hf ? make_float2(O[nj][2 * h], O[nj][2 * h + 1])
+                       : make_float2(O[4 + nj][2 * h], O[4 + nj][2 * h + 1]);
+        // ... + Q~ S' for this warp's column half (three products)
+        float Oh[4][4];
+#pragma unroll
+        for (int nj = 0; nj < 4; ++nj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) Oh[nj][e] = hf ? O[4 + nj][e] : O[nj][e];
 #pragma unroll 2
         for (int kk = 0; kk < DK / 16; ++kk) {
             uint32_t qh[4], ql[4];
@@ -508,28 +527,31 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
             ldsm_x4(smem_u32(st + C::OFF_Q + aoff), qh);
             ldsm_x4(smem_u32(smem + C::OFF_QLO + aoff), ql);
 #pragma unroll
-            for (int pp = 0; pp < 4; ++pp) {
+            for (int p2 = 0; p2 < 2; ++p2) {
                 const int brow = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const uint32_t boff = swz<C::VRB>(brow, 2 * pp + (lane >> 4));
+                const uint32_t boff = swz<C::VRB>(brow, 2 * (2 * hf + p2) + (lane >> 4));
                 uint32_t sh[4], sl[4];
                 ldsm_x4_t(smem_u32(smem + C::OFF_SH + boff), sh);
                 ldsm_x4_t(smem_u32(smem + C::OFF_SL + boff), sl);
-                mma16816(O[2 * pp], qh, sh[0], sh[1]);
-                mma16816(O[2 * pp + 1], qh, sh[2], sh[3]);
-                mma16816(O[2 * pp], qh, sl[0], sl[1]);
-                mma16816(O[2 * pp + 1], qh, sl[2], sl[3]);
-                mma16816(O[2 * pp], ql, sh[0], sh[1]);
-                mma16816(O[2 * pp + 1], ql, sh[2], sh[3]);
+                mma16816(Oh[2 * p2], qh, sh[0], sh[1]);
+                mma16816(Oh[2 * p2 + 1], qh, sh[2], sh[3]);
+                mma16816(Oh[2 * p2], qh, sl[0], sl[1]);
+                mma16816(Oh[2 * p2 + 1], qh, sl[2], sl[3]);
+                mma16816(Oh[2 * p2], ql, sh[0], sh[1]);
+                mma16816(Oh[2 * p2 + 1], ql, sh[2], sh[3]);
             }
         }
+        __syncthreads();  // the partner's partial output is in shared memory
 #pragma unroll
-        for (int nj = 0; nj < 8; ++nj)
+        for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const long long t = t0 + warp * 16 + g + 8 * h;
+                const float2 x = *reinterpret_cast<const float2 *>(xo + ((warp ^ 4) * 16 + g + 8 * h) * 32 + nj * 8 + 2 * tq);
+                const long long t = t0 + wr * 16 + g + 8 * h;
                 if (t < p.T)
-                    *reinterpret_cast<float2 *>(p.o + ((size_t)bh * p.T + arow_of(t)) * p.DV + zb * 64 + nj * 8 +
-                                                2 * tq) = make_float2(O[nj][2 * h], O[nj][2 * h + 1]);
+                    *reinterpret_cast<float2 *>(p.o + ((size_t)bh * p.T + arow_of(t)) * p.DV + zb * 64 +
+                                                (4 * hf + nj) * 8 + 2 * tq) =
+                        make_float2(Oh[nj][2 * h] + x.x, Oh[nj][2 * h + 1] + x.y);
             }
         state_update(stage);
         __syncthreads();
@@ -1142,7 +1164,7 @@ int launch_gla_fwd(const GlaArgs &a, cudaStream_t s, unsigned int grid) {
     static std::atomic<unsigned long long> smem_set{0};
     const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_fwd_kernel<DK>), C::SMEM);
     if (st) return st;
-    gla_fwd_kernel<DK><<<grid, kGlaThreads, C::SMEM, s>>>(a);
+    gla_fwd_kernel<DK><<<grid, kGlaFwdThreads, C::SMEM, s>>>(a);
     return check_launch("gla_fwd_kernel");
 }
 
