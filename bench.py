@@ -290,7 +290,10 @@ def bench_scan(torch, cla, workloads, dev, steps, warmup, dist_on):
 
 # ------------------------------------------------------------------ other workloads
 def _time_calls(torch, fn, flush, iters, warmup=5):
-    """Median device time of `iters` calls, L2 flushed before each, after `warmup` calls."""
+    """Median device time of `iters` calls, L2 flushed before each, after `warmup` calls.
+    A short device-side sleep after the flush keeps the GPU busy while the host enqueues
+    the call, so that the events bracket the call's device time and not the host's launch
+    path (which matters for the microsecond-scale calls)."""
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         fn()
@@ -298,6 +301,7 @@ def _time_calls(torch, fn, flush, iters, warmup=5):
     ts = []
     for _ in range(iters):
         flush()
+        torch.cuda._sleep(100_000)  # about 50 us at the SM clock
         s, e = _events(torch)
         s.record(stream)
         fn()
