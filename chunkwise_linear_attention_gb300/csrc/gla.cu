@@ -43,8 +43,7 @@ constexpr float kGlaLog2e = 1.4426950408889634f;
 constexpr int kGlaTc = 64;        // tokens per chunk
 constexpr int kGlaMid = 31;       // reference token of a chunk
 constexpr float kGlaSpan = 120.f; // largest |c_t - c_mid| (log2) the operand scalings allow
-constexpr int kGlaThreads = 128;  // backward: warp w rows 16w..16w+15 of a chunk, state rows 16w..
-constexpr int kGlaFwdThreads = 256;  // forward: warp w rows 16(w & 3).. of a chunk, column / token half w >> 2
+constexpr int kGlaThreads = 256;  // warp w: rows 16(w & 3).. of a chunk, column / token half w >> 2
 constexpr int kGlaSegChoices[4] = {64, 32, 16, 8};
 constexpr long long kGlaMinBlocks = 1024;
 
@@ -95,7 +94,7 @@ struct GlaArgs {
 };
 
 template <int DK>
-__global__ void __launch_bounds__(kGlaFwdThreads, 1) gla_fwd_kernel(const GlaArgs p) {
+__global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p) {
     using C = GlaCfg<DK>;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ unsigned int s_ticket, s_flag;
@@ -126,7 +125,7 @@ __global__ void __launch_bounds__(kGlaFwdThreads, 1) gla_fwd_kernel(const GlaArg
         uint8_t *st = smem + stage * C::STAGE;
         const long long t0 = (long long)chunk * kGlaTc;
         constexpr int QC = C::QRB / 16, GC = C::GRB / 16;
-        for (int i = tid; i < kGlaTc * QC; i += kGlaFwdThreads) {
+        for (int i = tid; i < kGlaTc * QC; i += kGlaThreads) {
             const int row = i / QC, c16 = i % QC;
             const long long t = t0 + row;
             const bool ok = t < p.T;
@@ -134,14 +133,14 @@ __global__ void __launch_bounds__(kGlaFwdThreads, 1) gla_fwd_kernel(const GlaArg
             cp_async16(smem_u32(st + C::OFF_K + swz<C::QRB>(row, c16)), Kb + off, ok ? 16u : 0u);
             if (withQ) cp_async16(smem_u32(st + C::OFF_Q + swz<C::QRB>(row, c16)), Qb + off, ok ? 16u : 0u);
         }
-        for (int i = tid; i < kGlaTc * 8; i += kGlaFwdThreads) {
+        for (int i = tid; i < kGlaTc * 8; i += kGlaThreads) {
             const int row = i >> 3, c16 = i & 7;
             const long long t = t0 + row;
             const bool ok = t < p.T;
             cp_async16(smem_u32(st + C::OFF_V + swz<C::VRB>(row, c16)),
                        Vb + (size_t)(ok ? arow_of(t) : 0) * p.DV + c16 * 8, ok ? 16u : 0u);
         }
-        for (int i = tid; i < kGlaTc * GC; i += kGlaFwdThreads) {  // padding tokens: log a = 0
+        for (int i = tid; i < kGlaTc * GC; i += kGlaThreads) {  // padding tokens: log a = 0
             const int row = i / GC, c16 = i % GC;
             const long long t = t0 + row;
             const bool ok = t < p.T && !(p.rev && t == 0);
@@ -181,7 +180,7 @@ __global__ void __launch_bounds__(kGlaFwdThreads, 1) gla_fwd_kernel(const GlaArg
         uint8_t *st = smem + stage * C::STAGE;
         const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
         constexpr int QC = C::QRB / 16;
-        for (int i = tid; i < kGlaTc * QC; i += kGlaFwdThreads) {
+        for (int i = tid; i < kGlaTc * QC; i += kGlaThreads) {
             const int row = i / QC, c16 = i % QC;
             const float4 *crow = reinterpret_cast<const float4 *>(G + row * DK + c16 * 8);
             const float4 *cmid = reinterpret_cast<const float4 *>(G + kGlaMid * DK + c16 * 8);
@@ -336,7 +335,7 @@ __global__ void __launch_bounds__(kGlaFwdThreads, 1) gla_fwd_kernel(const GlaArg
 
     // ------------------------------------------------ look-back for the incoming state
     constexpr int TILES = S_MT * S_NT;
-    auto ws_index = [&](size_t u, int tile) { return u * (size_t)(TILES * kGlaFwdThreads) + (size_t)tile * kGlaFwdThreads + tid; };
+    auto ws_index = [&](size_t u, int tile) { return u * (size_t)(TILES * kGlaThreads) + (size_t)tile * kGlaThreads + tid; };
     float Sin[S_MT][S_NT][4];
     auto add_state0 = [&](const float (&scale)[S_MT][2]) {
         if (p.S0 == nullptr) return;
@@ -587,7 +586,8 @@ __global__ void __launch_bounds__(kGlaFwdThreads, 1) gla_fwd_kernel(const GlaArg
 // X Y^T takes exact bf16 inputs (one product); the masked scores and Z~ are
 // split into two bf16 parts (three products), S' too (two products with X).
 // A block owns 64 output columns (key dimensions zb*64..) and the state rows
-// of those dimensions, [64][DV]; warp w holds state rows 16w..16w+15.
+// of those dimensions, [64][DV]; warp w holds state rows 16(w & 3).. and half
+// w >> 2 of the state's columns, and takes the scores of token half w >> 2.
 struct GlaBArgs {
     const bf16 *x, *y, *z;  // x, y: [BH][T][DV]; z: [BH][T][DK]
     const float *g;         // [BH][T][DK] natural-log decays
@@ -621,7 +621,8 @@ struct GlaBCfg {
     static constexpr int OFF_SH = OFF_ZLO + Z_BYTES;  // S' rows (key dimensions) [64][DV], high part
     static constexpr int OFF_SL = OFF_SH + 64 * XRB;
     static constexpr int OFF_AS = OFF_SL + 64 * XRB;
-    static constexpr int SMEM = OFF_AS + 64 * 4;
+    static constexpr int OFF_XO = OFF_AS + 64 * 4;  // partial outputs exchanged between the token halves
+    static constexpr int SMEM = OFF_XO + 8 * 16 * 32 * 4;
     static constexpr int S_NT = DV / 8;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
@@ -633,6 +634,7 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
     __shared__ unsigned int s_ticket, s_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tq = lane & 3;
+    const int wr = warp & 3, hf = warp >> 2;  // row group, column half
     if (tid == 0) s_ticket = atomicAdd(&p.hdr->ticket[0], 1u);
     __syncthreads();
     const unsigned int tk = s_ticket;
@@ -727,10 +729,11 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
         }
     };
 
-    constexpr int S_NT = C::S_NT;
+    // state fragments: local key dimensions 16 (w & 3) + {g, g + 8}, columns in half w >> 2
+    constexpr int S_NT = C::S_NT / 2;
     float S[S_NT][4];
-    auto s_row = [&](int h) { return warp * 16 + g + h * 8; };  // local key dimension
-    auto s_col = [&](int nj, int e) { return nj * 8 + tq * 2 + (e & 1); };
+    auto s_row = [&](int h) { return wr * 16 + g + h * 8; };  // local key dimension
+    auto s_col = [&](int nj, int e) { return (hf * S_NT + nj) * 8 + tq * 2 + (e & 1); };
     auto scale_rows_by = [&](const float *G, int a_row, int b_row) {  // rows *= 2^(c[a_row] - c[b_row])
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -762,7 +765,7 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
 #pragma unroll
         for (int kt = 0; kt < kGlaTc / 16; ++kt) {
             const int arow = kt * 16 + (lane & 7) + (lane >> 4) * 8;
-            const int ac16 = 2 * warp + ((lane >> 3) & 1);
+            const int ac16 = 2 * wr + ((lane >> 3) & 1);
             uint32_t ah[4], al[4];
             ldsm_x4_t(smem_u32(st + C::OFF_Z + swz<C::ZRB>(arow, ac16)), ah);
             ldsm_x4_t(smem_u32(smem + C::OFF_ZLO + swz<C::ZRB>(arow, ac16)), al);
@@ -770,7 +773,7 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
             for (int pp = 0; pp < S_NT / 2; ++pp) {
                 uint32_t b[4];
                 const int brow = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                ldsm_x4_t(smem_u32(st + C::OFF_Y + swz<C::XRB>(brow, 2 * pp + (lane >> 4))), b);
+                ldsm_x4_t(smem_u32(st + C::OFF_Y + swz<C::XRB>(brow, 2 * (hf * S_NT / 2 + pp) + (lane >> 4))), b);
                 mma16816(S[2 * pp], ah, b[0], b[1]);
                 mma16816(S[2 * pp + 1], ah, b[2], b[3]);
                 mma16816(S[2 * pp], al, b[0], b[1]);
@@ -899,89 +902,108 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
         write_sb();
         __syncthreads();
 
-        // D = X Y^T for this warp's 16 rows (exact bf16 inputs: one product)
-        float D[8][4];
-#pragma unroll
-        for (int nj = 0; nj < 8; ++nj)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) D[nj][e] = 0.f;
-        const int arow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll 2
-        for (int kk = 0; kk < DV / 16; ++kk) {
-            uint32_t a[4];
-            ldsm_x4(smem_u32(st + C::OFF_X + swz<C::XRB>(arow, 2 * kk + (lane >> 4))), a);
-#pragma unroll
-            for (int pp = 0; pp < 4; ++pp) {
-                uint32_t b[4];
-                const int brow = 16 * pp + (lane & 7) + (lane >> 4) * 8;
-                ldsm_x4(smem_u32(st + C::OFF_Y + swz<C::XRB>(brow, 2 * kk + ((lane >> 3) & 1))), b);
-                mma16816(D[2 * pp], a, b[0], b[1]);
-                mma16816(D[2 * pp + 1], a, b[2], b[3]);
-            }
-        }
-        uint32_t dh[4][4], dl[4][4];
-#pragma unroll
-        for (int nj = 0; nj < 8; ++nj)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = warp * 16 + g + 8 * h, s = nj * 8 + 2 * tq;
-                const float x0 = (s <= r) ? D[nj][2 * h] : 0.f;
-                const float x1 = (s + 1 <= r) ? D[nj][2 * h + 1] : 0.f;
-                split_bf16x2(make_float2(x0, x1), dh[nj >> 1][(nj & 1) * 2 + h], dl[nj >> 1][(nj & 1) * 2 + h]);
-            }
+        // D = X Y^T for this warp's 16 rows and its half of the chunk's tokens (s in 32 hf ..;
+        // exact bf16 inputs: one product), causal mask, then (D . M) Z~ over those tokens for
+        // all 64 output columns (three products); a half after every row of the group is skipped
+        const int arow = wr * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
         float O[8][4];
 #pragma unroll
         for (int nj = 0; nj < 8; ++nj)
 #pragma unroll
             for (int e = 0; e < 4; ++e) O[nj][e] = 0.f;
-        // (D . M) Z~ (three products) ...
+        if (32 * hf <= wr * 16 + 15) {
+            float D[4][4];
 #pragma unroll
-        for (int kt = 0; kt < 4; ++kt) {
+            for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
-            for (int pp = 0; pp < 4; ++pp) {
-                const int brow = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const uint32_t boff = swz<C::ZRB>(brow, 2 * pp + (lane >> 4));
-                uint32_t zh[4], zl[4];
-                ldsm_x4_t(smem_u32(st + C::OFF_Z + boff), zh);
-                ldsm_x4_t(smem_u32(smem + C::OFF_ZLO + boff), zl);
-                mma16816(O[2 * pp], dh[kt], zh[0], zh[1]);
-                mma16816(O[2 * pp + 1], dh[kt], zh[2], zh[3]);
-                mma16816(O[2 * pp], dh[kt], zl[0], zl[1]);
-                mma16816(O[2 * pp + 1], dh[kt], zl[2], zl[3]);
-                mma16816(O[2 * pp], dl[kt], zh[0], zh[1]);
-                mma16816(O[2 * pp + 1], dl[kt], zh[2], zh[3]);
+                for (int e = 0; e < 4; ++e) D[nj][e] = 0.f;
+#pragma unroll 2
+            for (int kk = 0; kk < DV / 16; ++kk) {
+                uint32_t a[4];
+                ldsm_x4(smem_u32(st + C::OFF_X + swz<C::XRB>(arow, 2 * kk + (lane >> 4))), a);
+#pragma unroll
+                for (int p2 = 0; p2 < 2; ++p2) {
+                    uint32_t b[4];
+                    const int brow = 16 * (2 * hf + p2) + (lane & 7) + (lane >> 4) * 8;
+                    ldsm_x4(smem_u32(st + C::OFF_Y + swz<C::XRB>(brow, 2 * kk + ((lane >> 3) & 1))), b);
+                    mma16816(D[2 * p2], a, b[0], b[1]);
+                    mma16816(D[2 * p2 + 1], a, b[2], b[3]);
+                }
+            }
+            uint32_t dh[2][4], dl[2][4];
+#pragma unroll
+            for (int nj = 0; nj < 4; ++nj)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int r = wr * 16 + g + 8 * h, s = (4 * hf + nj) * 8 + 2 * tq;
+                    const float x0 = (s <= r) ? D[nj][2 * h] : 0.f;
+                    const float x1 = (s + 1 <= r) ? D[nj][2 * h + 1] : 0.f;
+                    split_bf16x2(make_float2(x0, x1), dh[nj >> 1][(nj & 1) * 2 + h], dl[nj >> 1][(nj & 1) * 2 + h]);
+                }
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt) {
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {
+                    const int brow = (2 * hf + kt) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const uint32_t boff = swz<C::ZRB>(brow, 2 * pp + (lane >> 4));
+                    uint32_t zh[4], zl[4];
+                    ldsm_x4_t(smem_u32(st + C::OFF_Z + boff), zh);
+                    ldsm_x4_t(smem_u32(smem + C::OFF_ZLO + boff), zl);
+                    mma16816(O[2 * pp], dh[kt], zh[0], zh[1]);
+                    mma16816(O[2 * pp + 1], dh[kt], zh[2], zh[3]);
+                    mma16816(O[2 * pp], dh[kt], zl[0], zl[1]);
+                    mma16816(O[2 * pp + 1], dh[kt], zl[2], zl[3]);
+                    mma16816(O[2 * pp], dl[kt], zh[0], zh[1]);
+                    mma16816(O[2 * pp + 1], dl[kt], zh[2], zh[3]);
+                }
             }
         }
-        // ... + X S'^T (two products: S' in two parts)
+        // the other column half of the partial output goes to the partner warp (w ^ 4)
+        float *xo = reinterpret_cast<float *>(smem + C::OFF_XO);  // [8 warps][16 rows][32 columns]
+#pragma unroll
+        for (int nj = 0; nj < 4; ++nj)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                *reinterpret_cast<float2 *>(xo + (warp * 16 + g + 8 * h) * 32 + nj * 8 + 2 * tq) =
+                    hf ? make_float2(O[nj][2 * h], O[nj][2 * h + 1])
+                       : make_float2(O[4 + nj][2 * h], O[4 + nj][2 * h + 1]);
+        // ... + X S'^T for this warp's column half (two products: S' in two parts)
+        float Oh[4][4];
+#pragma unroll
+        for (int nj = 0; nj < 4; ++nj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) Oh[nj][e] = hf ? O[4 + nj][e] : O[nj][e];
 #pragma unroll 2
         for (int kk = 0; kk < DV / 16; ++kk) {
             uint32_t a[4];
             ldsm_x4(smem_u32(st + C::OFF_X + swz<C::XRB>(arow, 2 * kk + (lane >> 4))), a);
 #pragma unroll
-            for (int pp = 0; pp < 4; ++pp) {
-                const int brow = 16 * pp + (lane & 7) + (lane >> 4) * 8;
+            for (int p2 = 0; p2 < 2; ++p2) {
+                const int brow = 16 * (2 * hf + p2) + (lane & 7) + (lane >> 4) * 8;
                 const uint32_t boff = swz<C::XRB>(brow, 2 * kk + ((lane >> 3) & 1));
                 uint32_t sh[4], sl[4];
                 ldsm_x4(smem_u32(smem + C::OFF_SH + boff), sh);
                 ldsm_x4(smem_u32(smem + C::OFF_SL + boff), sl);
-                mma16816(O[2 * pp], a, sh[0], sh[1]);
-                mma16816(O[2 * pp + 1], a, sh[2], sh[3]);
-                mma16816(O[2 * pp], a, sl[0], sl[1]);
-                mma16816(O[2 * pp + 1], a, sl[2], sl[3]);
+                mma16816(Oh[2 * p2], a, sh[0], sh[1]);
+                mma16816(Oh[2 * p2 + 1], a, sh[2], sh[3]);
+                mma16816(Oh[2 * p2], a, sl[0], sl[1]);
+                mma16816(Oh[2 * p2 + 1], a, sl[2], sl[3]);
             }
         }
+        __syncthreads();  // the partner's partial output is in shared memory
         // OUT = 2^(c_r - c_m) per (row, key dimension)
 #pragma unroll
-        for (int nj = 0; nj < 8; ++nj)
+        for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int r = warp * 16 + g + 8 * h, col = nj * 8 + 2 * tq;
+                const int r = wr * 16 + g + 8 * h, col = (4 * hf + nj) * 8 + 2 * tq;
                 const long long t = t0 + r;
+                const float2 x = *reinterpret_cast<const float2 *>(xo + ((warp ^ 4) * 16 + g + 8 * h) * 32 + nj * 8 + 2 * tq);
                 if (t < p.T) {
                     const float2 cr = *reinterpret_cast<const float2 *>(G + r * 64 + col);
                     const float2 cm = *reinterpret_cast<const float2 *>(G + kGlaMid * 64 + col);
                     *reinterpret_cast<float2 *>(p.out + ((size_t)bh * p.T + arow_of(t)) * p.DK + zb * 64 + col) =
-                        make_float2(O[nj][2 * h] * ex2(cr.x - cm.x), O[nj][2 * h + 1] * ex2(cr.y - cm.y));
+                        make_float2((Oh[nj][2 * h] + x.x) * ex2(cr.x - cm.x), (Oh[nj][2 * h + 1] + x.y) * ex2(cr.y - cm.y));
                 }
             }
         state_update(stage);
@@ -991,8 +1013,10 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
     }
     cp_async_wait<0>();
 
-    // the final state's rows dotted with fs_dot (the decay gradient's final-state term)
+    // the final state's rows dotted with fs_dot (the decay gradient's final-state term), the
+    // two column halves summed through shared memory
     if (seg == p.n_seg - 1 && p.fs_part != nullptr) {
+        float *fsx = reinterpret_cast<float *>(smem + C::OFF_XO);  // [2 halves][64 rows]
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int row = zb * 64 + s_row(h);
@@ -1006,8 +1030,10 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
             }
             acc += __shfl_xor_sync(0xffffffffu, acc, 1);
             acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            if (tq == 0) p.fs_part[(size_t)bh * p.DK + row] = acc;
+            if (tq == 0) fsx[hf * 64 + s_row(h)] = acc;
         }
+        __syncthreads();
+        if (tid < 64) p.fs_part[(size_t)bh * p.DK + zb * 64 + tid] = fsx[tid] + fsx[64 + tid];
     }
 }
 
@@ -1164,7 +1190,7 @@ int launch_gla_fwd(const GlaArgs &a, cudaStream_t s, unsigned int grid) {
     static std::atomic<unsigned long long> smem_set{0};
     const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_fwd_kernel<DK>), C::SMEM);
     if (st) return st;
-    gla_fwd_kernel<DK><<<grid, kGlaFwdThreads, C::SMEM, s>>>(a);
+    gla_fwd_kernel<DK><<<grid, kGlaThreads, C::SMEM, s>>>(a);
     return check_launch("gla_fwd_kernel");
 }
 
