@@ -1,5 +1,5 @@
-// gla.cu -- gated linear attention (one decay per key dimension), forward,
-// chunkwise, for GB300 (sm_103a).
+// gla.cu -- gated linear attention (one decay per key dimension), forward and
+// backward, chunkwise, for GB300 (sm_103a).
 //
 // "Parallel Scan" (zerotofrontier.app), "What one combine costs" (a diagonal
 // transition: one decay per state entry) and "The chunkwise algorithm" (the
@@ -23,8 +23,10 @@
 // Q~, K~ and the state are scaled in fp32 and split into bf16 high and low
 // parts, and each product takes the parts that keep the rounding below the
 // outputs' tolerance: Q~ K~^T and Q~ S' as hi.hi + hi.lo + lo.hi, P V and
-// K~^T V as hi + lo (V is an exact bf16 input).  Products run on mma.sync
-// m16n8k16 (bf16 in, fp32 accumulate).
+// K~^T V as hi + lo (V is an exact bf16 input).  The forward (and the
+// backward's reversed dV traversal) runs its products on tcgen05.mma
+// (kind::f16, fp32 accumulators in tensor memory); the backward's dQ / dK
+// traversal on mma.sync m16n8k16.
 //
 // Chunk parallelism as in chunk_la.cu: a block owns one segment of chunks of
 // one (batch, head) and 64 value columns; phase 1 folds the segment into one
@@ -33,6 +35,7 @@
 // state; phase 2 runs the chunks from it and writes O.
 #include "cla_internal.cuh"
 #include "mma_sync.cuh"
+#include "tc_ptx.cuh"
 
 namespace cla {
 namespace {
@@ -43,34 +46,9 @@ constexpr float kGlaLog2e = 1.4426950408889634f;
 constexpr int kGlaTc = 64;        // tokens per chunk
 constexpr int kGlaMid = 31;       // reference token of a chunk
 constexpr float kGlaSpan = 120.f; // largest |c_t - c_mid| (log2) the operand scalings allow
-constexpr int kGlaThreads = 256;  // warp w: rows 16(w & 3).. of a chunk, column / token half w >> 2
+constexpr int kGlaThreads = 256;  // dQ / dK traversal: warp w rows 16(w & 3).. of a chunk, column / token half w >> 2
 constexpr int kGlaSegChoices[4] = {64, 32, 16, 8};
 constexpr long long kGlaMinBlocks = 1024;
-
-template <int DK>
-struct GlaCfg {
-    static constexpr int QRB = DK * 2;  // bytes per row of a Q or K tile (bf16)
-    static constexpr int VRB = 128;     // bytes per row of a 64-column V slab (bf16)
-    static constexpr int GRB = DK * 4;  // bytes per row of log decays / cumulative decays (fp32)
-    static constexpr int Q_BYTES = kGlaTc * QRB;
-    static constexpr int V_BYTES = kGlaTc * VRB;
-    static constexpr int G_BYTES = kGlaTc * GRB;
-    // one stage: Q (then the high part of Q~), K (then K~'s high part), V, log decays (then c)
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = Q_BYTES;
-    static constexpr int OFF_V = 2 * Q_BYTES;
-    static constexpr int OFF_G = 2 * Q_BYTES + V_BYTES;
-    static constexpr int STAGE = 2 * Q_BYTES + V_BYTES + G_BYTES;
-    static constexpr int OFF_QLO = 2 * STAGE;             // low part of Q~
-    static constexpr int OFF_KLO = OFF_QLO + Q_BYTES;     // low part of K~
-    static constexpr int OFF_SH = OFF_KLO + Q_BYTES;      // S' = diag(2^c_m) S, high part, [DK][64]
-    static constexpr int OFF_SL = OFF_SH + DK * VRB;      // and its low part
-    static constexpr int OFF_AS = OFF_SL + DK * VRB;      // alpha of the segment per key dimension
-    static constexpr int OFF_XO = OFF_AS + DK * 4;        // partial outputs exchanged between the token halves
-    static constexpr int SMEM = OFF_XO + 8 * 16 * 32 * 4;
-    static constexpr int S_MT = DK / 64;  // 16-row state tiles per row group (DK / 16 over 4 groups)
-    static_assert(SMEM <= 227 * 1024, "shared memory budget");
-};
 
 // One traversal of the gated recurrence.  Forward (rev = 0): q, k, v, S0 -> o, ST.  Reversed
 // (rev = 1, the adjoint of the backward): token t' of the traversal is token T-1-t' of the
@@ -93,16 +71,86 @@ struct GlaArgs {
     float4 *agg, *incl;   // [unit][tiles][threads]
 };
 
+// ----------------------------------------------------------------- forward on tcgen05
+// One traversal of the gated recurrence on the fifth-generation tensor cores.
+// Per 64-token chunk, with Q~ = Q (.) 2^(c - c_m), K~ = K (.) 2^(c_m - c) and
+// S' = diag(2^c_m) S (each split into two bf16 parts by the threads):
+//     P     = Q~ K~^T                       (M = 64, N = 64, K = DK)   three products
+//     O     = Q~ S'                         (M = 64, N = 64, K = DK)   three products
+//     U     = K~^T V                        (M = DK, N = 64, K = 64)   two products
+//     O    += (P . M)_hi V + (P . M)_lo V   (A from tensor memory)     two products
+//     S_next = diag(2^(c_L - c_m)) (S' + U)                            threads
+// with fp32 accumulators in tensor memory.  The block's 8 warps prepare the
+// operands, mask the scores and apply the state update (warps w and w + 4 read
+// lane quarter w & 3 of tensor memory and split its columns); one elected lane
+// of warp 0 issues the products, whose completion every thread waits for on an
+// mbarrier (bounded waits).  Operand tiles use the 128-byte swizzle: Q~ and K~
+// K-major ([64 tokens][DK] in 64-element blocks; K~ is also the MN-major A of
+// U), V and S' MN-major.  A warp reads its own quarter of tensor-memory lanes:
+// the 64-row accumulators keep row 16q + i in lane 32q + i (i < 16), the DK-row
+// one (DK = 128) row r in lane r.
+//
+// Segments and look-back as before: phase 1 folds the segment's chunks into
+// (diag(alpha_seg), dS_seg) from a zero state, decoupled look-back gives the
+// incoming state, phase 2 runs the chunks from it and writes O.
 template <int DK>
-__global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p) {
-    using C = GlaCfg<DK>;
-    extern __shared__ __align__(128) uint8_t smem[];
+struct GlaTcCfg {
+    static constexpr int KB = DK / 64;             // 64-element blocks along the key dimension
+    static constexpr int QT_BYTES = KB * 64 * 128;  // a [64 tokens][DK] bf16 operand tile
+    static constexpr int V_BYTES = 64 * 128;        // a [64 tokens][64 columns] bf16 operand tile
+    static constexpr int G_BYTES = 64 * DK * 4;     // log decays, then in-chunk cumulative log2 decays
+    // one stage: Q (then the high part of Q~), K (then K~'s high part), V, G
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = QT_BYTES;
+    static constexpr int OFF_V = 2 * QT_BYTES;
+    static constexpr int OFF_G = 2 * QT_BYTES + V_BYTES;
+    static constexpr int STAGE = 2 * QT_BYTES + V_BYTES + G_BYTES;
+    static constexpr int OFF_QL = 2 * STAGE;            // low part of Q~
+    static constexpr int OFF_KL = OFF_QL + QT_BYTES;    // low part of K~
+    static constexpr int OFF_SH = OFF_KL + QT_BYTES;    // S' high part, [DK rows][64 columns] MN-major
+    static constexpr int OFF_SL = OFF_SH + DK * 128;
+    static constexpr int OFF_AS = OFF_SL + DK * 128;    // alpha of the segment per key dimension
+    static constexpr int OFF_BAR = OFF_AS + DK * 4;     // two mbarriers
+    static constexpr int SMEM = OFF_BAR + 16 + 1024;    // + alignment slack of the 1024-byte base
+    static constexpr int MIN_BLOCKS = (2 * (SMEM + 1024) <= 228 * 1024) ? 2 : 1;
+    // tensor memory: scores, masked score parts, output, state product
+    static constexpr uint32_t C_P = 0, C_PB = 64, C_O = 128, C_U = 192, TMEM_COLS = 256;
+    static constexpr int SC = (DK == 128) ? 32 : 16;  // state columns per thread
+    static_assert(STAGE % 1024 == 0 && QT_BYTES % 1024 == 0, "1024-byte aligned operand tiles");
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+constexpr int kGlaTcThreads = 256;
+
+template <int DK>
+__global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS) gla_tc_kernel(const GlaArgs p) {
+    using C = GlaTcCfg<DK>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    __shared__ uint32_t s_tmem;
     __shared__ unsigned int s_ticket, s_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, tq = lane & 3;
-    const int wr = warp & 3, hf = warp >> 2;  // row group, column half
-    if (tid == 0) s_ticket = atomicAdd(&p.hdr->ticket[0], 1u);
+    const uint32_t barA = sbase + C::OFF_BAR, barB = barA + 8;
+
+    // tensor memory first (before taking a ticket, so every ticket holder owns its columns)
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(C::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        tc_fence_before();
+    }
+    if (tid == 0) {
+        mbar_init(barA, 1);
+        mbar_init(barB, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_ticket = atomicAdd(&p.hdr->ticket[0], 1u);
+    }
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const int q = warp & 3, hf = warp >> 2;              // lane quarter, column half
+    const uint32_t tlane = (uint32_t)(q * 32) << 16;     // this warp's lane quarter
     const unsigned int tk = s_ticket;
     const int per_seg = p.BH * p.nzb;
     const int seg = (int)(tk / per_seg);
@@ -112,6 +160,16 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
     const int c_end = min(c_begin + p.seg_chunks, p.n_chunks);
     const int nc = c_end - c_begin;
     const size_t unit = ((size_t)seg * p.BH + bh) * p.nzb + zb;
+    bool timed_out = false;
+    uint32_t phA = 0u, phB = 0u;
+    auto waitA = [&]() {
+        if (!mbar_wait(barA, phA)) timed_out = true;
+        phA ^= 1u;
+    };
+    auto waitB = [&]() {
+        if (!mbar_wait(barB, phB)) timed_out = true;
+        phB ^= 1u;
+    };
 
     const bf16 *Qb = p.q + (size_t)bh * p.T * DK;
     const bf16 *Kb = p.k + (size_t)bh * p.T * DK;
@@ -121,31 +179,34 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
 
     // array row of traversal token t (reversed: T-1-t), and of its decay (reversed: T-t, none at 0)
     auto arow_of = [&](long long t) { return p.rev ? p.T - 1 - t : t; };
+    // Q, K into their K-major swizzled operand positions, V into its MN-major one, G plain.
     auto load_stage = [&](int stage, int chunk, bool withQ) {
         uint8_t *st = smem + stage * C::STAGE;
         const long long t0 = (long long)chunk * kGlaTc;
-        constexpr int QC = C::QRB / 16, GC = C::GRB / 16;
-        for (int i = tid; i < kGlaTc * QC; i += kGlaThreads) {
+        constexpr int QC = DK / 8;  // 16-byte chunks of a Q / K row
+        for (int i = tid; i < kGlaTc * QC; i += kGlaTcThreads) {
             const int row = i / QC, c16 = i % QC;
             const long long t = t0 + row;
             const bool ok = t < p.T;
             const size_t off = (size_t)(ok ? arow_of(t) : 0) * DK + c16 * 8;
-            cp_async16(smem_u32(st + C::OFF_K + swz<C::QRB>(row, c16)), Kb + off, ok ? 16u : 0u);
-            if (withQ) cp_async16(smem_u32(st + C::OFF_Q + swz<C::QRB>(row, c16)), Qb + off, ok ? 16u : 0u);
+            const uint32_t so = (uint32_t)((c16 >> 3) * 8192) + sw128(row, (c16 & 7) * 8);
+            cp_async16(smem_u32(st + C::OFF_K) + so, Kb + off, ok ? 16u : 0u);
+            if (withQ) cp_async16(smem_u32(st + C::OFF_Q) + so, Qb + off, ok ? 16u : 0u);
         }
-        for (int i = tid; i < kGlaTc * 8; i += kGlaThreads) {
+        for (int i = tid; i < kGlaTc * 8; i += kGlaTcThreads) {
             const int row = i >> 3, c16 = i & 7;
             const long long t = t0 + row;
             const bool ok = t < p.T;
-            cp_async16(smem_u32(st + C::OFF_V + swz<C::VRB>(row, c16)),
-                       Vb + (size_t)(ok ? arow_of(t) : 0) * p.DV + c16 * 8, ok ? 16u : 0u);
+            cp_async16(smem_u32(st + C::OFF_V) + sw128(row, c16 * 8), Vb + (size_t)(ok ? arow_of(t) : 0) * p.DV + c16 * 8,
+                       ok ? 16u : 0u);
         }
-        for (int i = tid; i < kGlaTc * GC; i += kGlaThreads) {  // padding tokens: log a = 0
+        constexpr int GC = DK / 4;
+        for (int i = tid; i < kGlaTc * GC; i += kGlaTcThreads) {  // padding tokens: log a = 0
             const int row = i / GC, c16 = i % GC;
             const long long t = t0 + row;
             const bool ok = t < p.T && !(p.rev && t == 0);
             const long long ga = p.rev ? p.T - t : t;
-            cp_async16(smem_u32(st + C::OFF_G + row * C::GRB + c16 * 16), Gb + (size_t)(ok ? ga : 0) * DK + c16 * 4,
+            cp_async16(smem_u32(st + C::OFF_G + row * DK * 4 + c16 * 16), Gb + (size_t)(ok ? ga : 0) * DK + c16 * 4,
                        ok ? 16u : 0u);
         }
     };
@@ -158,6 +219,7 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
         if (tid < DK) {
             float run = 0.f, lo = 0.f, hi = 0.f;
             bool finite = true;
+#pragma unroll 8
             for (int t = 0; t < kGlaTc; ++t) {
                 const float l = G[t * DK + tid];
                 finite = finite && isfinite(l);
@@ -175,12 +237,12 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
         return total;
     };
 
-    // Q~ = Q 2^(c - c_m) (high part over Q, low part in QLO) and K~ = K 2^(c_m - c).
+    // K~ = K 2^(c_m - c) (high part over K, low part in KL) and, withQ, Q~ = Q 2^(c - c_m).
     auto scale_operands = [&](int stage, bool withQ) {
         uint8_t *st = smem + stage * C::STAGE;
         const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
-        constexpr int QC = C::QRB / 16;
-        for (int i = tid; i < kGlaTc * QC; i += kGlaThreads) {
+        constexpr int QC = DK / 8;
+        for (int i = tid; i < kGlaTc * QC; i += kGlaTcThreads) {
             const int row = i / QC, c16 = i % QC;
             const float4 *crow = reinterpret_cast<const float4 *>(G + row * DK + c16 * 8);
             const float4 *cmid = reinterpret_cast<const float4 *>(G + kGlaMid * DK + c16 * 8);
@@ -190,7 +252,7 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
                 d[0] = a.x - ma.x; d[1] = a.y - ma.y; d[2] = a.z - ma.z; d[3] = a.w - ma.w;
                 d[4] = b.x - mb.x; d[5] = b.y - mb.y; d[6] = b.z - mb.z; d[7] = b.w - mb.w;
             }
-            const uint32_t off = swz<C::QRB>(row, c16);
+            const uint32_t off = (uint32_t)((c16 >> 3) * 8192) + sw128(row, (c16 & 7) * 8);
             {
                 const uint4 kv = *reinterpret_cast<const uint4 *>(st + C::OFF_K + off);
                 const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
@@ -201,7 +263,7 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
                     split_bf16x2(make_float2(x.x * ex2(-d[2 * e]), x.y * ex2(-d[2 * e + 1])), hi[e], lo[e]);
                 }
                 *reinterpret_cast<uint4 *>(st + C::OFF_K + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(smem + C::OFF_KLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                *reinterpret_cast<uint4 *>(smem + C::OFF_KL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
             if (withQ) {
                 const uint4 qv = *reinterpret_cast<const uint4 *>(st + C::OFF_Q + off);
@@ -213,104 +275,162 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
                     split_bf16x2(make_float2(x.x * ex2(d[2 * e]), x.y * ex2(d[2 * e + 1])), hi[e], lo[e]);
                 }
                 *reinterpret_cast<uint4 *>(st + C::OFF_Q + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(smem + C::OFF_QLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                *reinterpret_cast<uint4 *>(smem + C::OFF_QL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
     };
 
-    // State fragments: warp w owns rows (key dimensions) 16((w & 3) S_MT + mi) + {g, g + 8} and
-    // the columns of m16n8 tiles 4 (w >> 2) .. 4 (w >> 2) + 3 (its half of the 64 columns).
-    constexpr int S_MT = C::S_MT, S_NT = 4;
-    float S[S_MT][S_NT][4];
-    auto s_row = [&](int mi, int h) { return (wr * S_MT + mi) * 16 + g + h * 8; };
-    auto s_col = [&](int nj, int e) { return (4 * hf + nj) * 8 + tq * 2 + (e & 1); };
-    auto zero_state = [&](float (&X)[S_MT][S_NT][4]) {
+    // This thread's state: one row (key dimension) srow and SC consecutive columns of half hf.
+    // DK = 128: row 32 q + lane (the lane of a 128-row accumulator), columns 32 hf + {0..31}.
+    // DK = 64: row 16 q + (lane & 15), columns 32 hf + 16 (lane >> 4) + {0..15} (the paired-half
+    // shape of a 64-row accumulator).
+    constexpr int SC = C::SC;
+    const int srow = (DK == 128) ? 32 * q + lane : 16 * q + (lane & 15);
+    const int scol0 = (DK == 128) ? 32 * hf : 32 * hf + 16 * (lane >> 4);
+    auto scol = [&](int j) { return scol0 + j; };
+    float S[SC];
+    // the state product U of this thread's row, from tensor memory
+    auto load_u = [&](float (&u)[SC]) {
+        uint32_t r[SC];
+        tmem_ld_cols<SC>(tmem + tlane + C::C_U + (uint32_t)(32 * hf), r);
+        tmem_ld_wait();
 #pragma unroll
-        for (int mi = 0; mi < S_MT; ++mi)
-#pragma unroll
-            for (int nj = 0; nj < S_NT; ++nj)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) X[mi][nj][e] = 0.f;
+        for (int j = 0; j < SC; ++j) u[j] = __uint_as_float(r[j]);
     };
-    // per-row scaling of the state by 2^(x[row]) read from a [.][DK] row of log2 values
-    auto scale_rows = [&](const float *lg2, float sub_from) {
-#pragma unroll
-        for (int mi = 0; mi < S_MT; ++mi)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float f = ex2(lg2[s_row(mi, h)] - sub_from);
-#pragma unroll
-                for (int nj = 0; nj < S_NT; ++nj) {
-                    S[mi][nj][2 * h] *= f;
-                    S[mi][nj][2 * h + 1] *= f;
-                }
-            }
-    };
-    // S' = diag(2^c_m) S, in place (registers)
+    // S' = diag(2^c_m) S in place, and its two bf16 parts into the MN-major B tile [DK][64]
     auto state_to_mid = [&](int stage) {
         const float *G = reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G);
-        scale_rows(G + kGlaMid * DK, 0.f);
+        const float f = ex2(G[kGlaMid * DK + srow]);
+#pragma unroll
+        for (int j = 0; j < SC; ++j) S[j] *= f;
     };
-    // S' as two bf16 parts for the Q~ S' product
     auto write_sb = [&]() {
 #pragma unroll
-        for (int mi = 0; mi < S_MT; ++mi)
+        for (int j8 = 0; j8 < SC / 8; ++j8) {  // 8 consecutive columns per 16-byte store
+            uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int nj = 0; nj < S_NT; ++nj)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int row = s_row(mi, h), col = s_col(nj, 0);
-                    const uint32_t off = swz<C::VRB>(row, col >> 3) + (col & 7) * 2;
-                    uint32_t hi, lo;
-                    split_bf16x2(make_float2(S[mi][nj][2 * h], S[mi][nj][2 * h + 1]), hi, lo);
-                    *reinterpret_cast<uint32_t *>(smem + C::OFF_SH + off) = hi;
-                    *reinterpret_cast<uint32_t *>(smem + C::OFF_SL + off) = lo;
-                }
+            for (int e = 0; e < 4; ++e) split_bf16x2(make_float2(S[8 * j8 + 2 * e], S[8 * j8 + 2 * e + 1]), hi[e], lo[e]);
+            const uint32_t off = sw128(srow, scol(8 * j8));
+            *reinterpret_cast<uint4 *>(smem + C::OFF_SH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(smem + C::OFF_SL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
     };
-    // S' + K~^T V (two products: K~'s parts), then rows scaled by 2^(c_L - c_m)
-    auto state_update = [&](int stage) {
-        const uint8_t *st = smem + stage * C::STAGE;
+    // S_next = diag(2^(c_L - c_m)) (S' + U)
+    auto state_finish = [&](int stage) {
+        const float *G = reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G);
+        const float f = ex2(G[(kGlaTc - 1) * DK + srow] - G[kGlaMid * DK + srow]);
+        float u[SC];
+        load_u(u);
 #pragma unroll
-        for (int kt = 0; kt < kGlaTc / 16; ++kt) {
-            uint32_t b[S_NT / 2][4];
+        for (int j = 0; j < SC; ++j) S[j] = f * (S[j] + u[j]);
+    };
+
+    // ---- descriptors (built once; a K step adds a constant to the start-address field)
+    auto qdesc = [&](uint32_t off) { return smem_desc(sbase + off, 16, 1024); };      // K-major
+    auto ktdesc = [&](uint32_t off) { return smem_desc(sbase + off, 8192, 1024); };   // MN-major A (K~^T)
+    auto mndesc = [&](uint32_t off) { return smem_desc(sbase + off, 8192, 1024); };   // MN-major B
+    auto kstep_k = [&](int kk) { return (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4); };  // K-major
+    auto kstep_mn = [&](int kk) { return (uint64_t)((kk * 2048) >> 4); };                      // MN-major
+    constexpr uint32_t id_s = idesc_bf16(64, 64, 0, 0);   // scores: Q~ K~^T
+    constexpr uint32_t id_o = idesc_bf16(64, 64, 0, 1);   // Q~ S', P V
+    constexpr uint32_t id_u = idesc_bf16(DK, 64, 1, 1);   // K~^T V
+    // U = K~_hi^T V + K~_lo^T V into C_U (stage's K~ and V)
+    auto issue_u = [&](int stage) {
+        const uint32_t so = (uint32_t)(stage * C::STAGE);
+        const uint64_t b0 = mndesc(so + C::OFF_V);
 #pragma unroll
-            for (int pp = 0; pp < S_NT / 2; ++pp) {
-                const int brow = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                ldsm_x4_t(smem_u32(st + C::OFF_V + swz<C::VRB>(brow, 2 * (2 * hf + pp) + (lane >> 4))), b[pp]);
-            }
+        for (int part = 0; part < 2; ++part) {
+            const uint64_t a0 = ktdesc(part ? C::OFF_KL : so + C::OFF_K);
 #pragma unroll
-            for (int mi = 0; mi < S_MT; ++mi) {
-                const int arow = kt * 16 + (lane & 7) + (lane >> 4) * 8;
-                const int ac16 = 2 * (wr * S_MT + mi) + ((lane >> 3) & 1);
-                uint32_t ah[4], al[4];
-                ldsm_x4_t(smem_u32(st + C::OFF_K + swz<C::QRB>(arow, ac16)), ah);
-                ldsm_x4_t(smem_u32(smem + C::OFF_KLO + swz<C::QRB>(arow, ac16)), al);
+            for (int kk = 0; kk < kGlaTc / 16; ++kk)
+                mma_ss_w(tmem + C::C_U, a0 + kstep_mn(kk), b0 + kstep_mn(kk), id_u, (part | kk) ? 1u : 0u);
+        }
+    };
+    // P = Q~ K~^T (hi hi, hi lo, lo hi) into C_P and O = Q~ S' (hi hi, hi lo, lo hi) into C_O
+    auto issue_p_o = [&](int stage) {
+        const uint32_t so = (uint32_t)(stage * C::STAGE);
+        const uint64_t qh = qdesc(so + C::OFF_Q), ql = qdesc(C::OFF_QL);
+        const uint64_t kh = qdesc(so + C::OFF_K), kl = qdesc(C::OFF_KL);
+        const uint64_t sh = mndesc(C::OFF_SH), sl = mndesc(C::OFF_SL);
 #pragma unroll
-                for (int pp = 0; pp < S_NT / 2; ++pp) {
-                    mma16816(S[mi][2 * pp], ah, b[pp][0], b[pp][1]);
-                    mma16816(S[mi][2 * pp + 1], ah, b[pp][2], b[pp][3]);
-                    mma16816(S[mi][2 * pp], al, b[pp][0], b[pp][1]);
-                    mma16816(S[mi][2 * pp + 1], al, b[pp][2], b[pp][3]);
-                }
+        for (int part = 0; part < 3; ++part) {
+            const uint64_t a0 = (part == 2) ? ql : qh;
+            const uint64_t bp = (part == 1) ? kl : kh, bs = (part == 1) ? sl : sh;
+#pragma unroll
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                mma_ss_w(tmem + C::C_P, a0 + kstep_k(kk), bp + kstep_k(kk), id_s, (part | kk) ? 1u : 0u);
+                mma_ss_w(tmem + C::C_O, a0 + kstep_k(kk), bs + kstep_mn(kk), id_o, (part | kk) ? 1u : 0u);
             }
         }
-        const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
+    };
+    // O += (P . M)_hi V + (P . M)_lo V, the masked parts from tensor memory: tokens 16kk.. lie in
+    // piece kk / 2, its high part in the piece's columns 0..15, the low part in 16..31
+    auto issue_pv = [&](int stage) {
+        const uint64_t b0 = mndesc((uint32_t)(stage * C::STAGE) + C::OFF_V);
 #pragma unroll
-        for (int mi = 0; mi < S_MT; ++mi)
+        for (int part = 0; part < 2; ++part)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = s_row(mi, h);
-                const float f = ex2(G[(kGlaTc - 1) * DK + row] - G[kGlaMid * DK + row]);
-#pragma unroll
-                for (int nj = 0; nj < S_NT; ++nj) {
-                    S[mi][nj][2 * h] *= f;
-                    S[mi][nj][2 * h + 1] *= f;
-                }
+            for (int kk = 0; kk < kGlaTc / 16; ++kk) {
+                const uint32_t acol = C::C_PB + (uint32_t)(kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
+                mma_ts_w(tmem + C::C_O, tmem + acol, b0 + kstep_mn(kk), id_o, 1u);
             }
+    };
+
+    // Causal mask of the scores (token s <= row r), split into two bf16 parts as the A operand of
+    // P V: row r = 16 q + (lane & 15), the 32-token piece hf; threads 0..15 take tokens s0..,
+    // 16..31 tokens s0 + 16..
+    auto mask_scores = [&]() {
+        const int r = 16 * q + (lane & 15);
+        {
+            const int s0 = hf * 32;
+            uint32_t pr[16];
+            tmem_ld16x2(tmem + tlane + C::C_P + (uint32_t)s0, pr);
+            tmem_ld_wait();
+            const int sb = s0 + 16 * (lane >> 4);
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int s = sb + 2 * j;
+                float2 v = make_float2(__uint_as_float(pr[2 * j]), __uint_as_float(pr[2 * j + 1]));
+                if (s > r) v.x = 0.f;
+                if (s + 1 > r) v.y = 0.f;
+                split_bf16x2(v, hi[j], lo[j]);
+            }
+            // high parts of tokens s0.. at columns s0.., of s0 + 16.. at s0 + 8..; low parts 16 further
+            tmem_st8x2(tmem + tlane + C::C_PB + (uint32_t)s0, hi);
+            tmem_st8x2(tmem + tlane + C::C_PB + (uint32_t)(s0 + 16), lo);
+        }
+        tmem_st_wait();
+    };
+    // O of this thread: row 16 q + (lane & 15), columns 32 hf + 16 (lane >> 4) + 0..15
+    auto write_out = [&](long long t0) {
+        const long long t = t0 + 16 * q + (lane & 15);
+        {
+            const int half = hf;
+            uint32_t o[16];
+            tmem_ld16x2(tmem + tlane + C::C_O + (uint32_t)(32 * half), o);
+            tmem_ld_wait();
+            if (t < p.T) {
+                float *dst = p.o + ((size_t)bh * p.T + arow_of(t)) * p.DV + zb * 64 + 32 * half + 16 * (lane >> 4);
+#pragma unroll
+                for (int c2 = 0; c2 < 8; ++c2)
+                    *reinterpret_cast<float2 *>(dst + 2 * c2) =
+                        make_float2(__uint_as_float(o[2 * c2]), __uint_as_float(o[2 * c2 + 1]));
+            }
+        }
+    };
+    // operands written by the threads (and cp.async data) -> the tensor core: every thread fences
+    // its writes, the block synchronises, and warp 0 issues
+    auto hand_to_tc = [&]() {
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
     };
 
     // ------------------------------------------------ phase 1: the segment's affine pair
-    zero_state(S);
+#pragma unroll
+    for (int j = 0; j < SC; ++j) S[j] = 0.f;
     float la_seg = 0.f;  // thread i < DK: log2 of alpha_seg[i]
     load_stage(0, c_begin, false);
     cp_async_commit();
@@ -324,9 +444,16 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
         __syncthreads();
         scale_operands(stage, false);
         state_to_mid(stage);
-        __syncthreads();
-        state_update(stage);
-        __syncthreads();
+        hand_to_tc();
+        if (warp == 0) {
+            issue_u(stage);
+            mma_commit_w(barA);
+        }
+        waitA();
+        tc_fence_after();
+        state_finish(stage);
+        tc_fence_before();
+        __syncthreads();  // the stage and the state product are consumed
         if (i + 2 < nc) load_stage(stage, c_begin + i + 2, false);
         cp_async_commit();
     }
@@ -334,67 +461,50 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
     __syncthreads();
 
     // ------------------------------------------------ look-back for the incoming state
-    constexpr int TILES = S_MT * S_NT;
-    auto ws_index = [&](size_t u, int tile) { return u * (size_t)(TILES * kGlaThreads) + (size_t)tile * kGlaThreads + tid; };
-    float Sin[S_MT][S_NT][4];
-    auto add_state0 = [&](const float (&scale)[S_MT][2]) {
+    constexpr int TILES = SC / 4;
+    auto ws_index = [&](size_t u, int tile) {
+        return u * (size_t)(TILES * kGlaTcThreads) + (size_t)tile * kGlaTcThreads + tid;
+    };
+    float Sin[SC];
+#pragma unroll
+    for (int j = 0; j < SC; ++j) Sin[j] = 0.f;
+    auto add_state0 = [&](float scale) {
         if (p.S0 == nullptr) return;
 #pragma unroll
-        for (int mi = 0; mi < S_MT; ++mi)
-#pragma unroll
-            for (int nj = 0; nj < S_NT; ++nj)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int row = s_row(mi, e >> 1), col = zb * 64 + s_col(nj, e);
-                    Sin[mi][nj][e] = fmaf(scale[mi][e >> 1], __ldg(p.S0 + ((size_t)bh * DK + row) * p.DV + col),
-                                          Sin[mi][nj][e]);
-                }
+        for (int j = 0; j < SC; ++j)
+            Sin[j] = fmaf(scale, __ldg(p.S0 + ((size_t)bh * DK + srow) * p.DV + zb * 64 + scol(j)), Sin[j]);
     };
-    zero_state(Sin);
     if (tid < DK) alpha_s[tid] = ex2(la_seg);
     if (seg == 0) {
-        float one[S_MT][2];
-#pragma unroll
-        for (int mi = 0; mi < S_MT; ++mi) one[mi][0] = one[mi][1] = 1.f;
-        add_state0(one);
+        add_state0(1.f);
     } else {
 #pragma unroll
-        for (int mi = 0; mi < S_MT; ++mi)
-#pragma unroll
-            for (int nj = 0; nj < S_NT; ++nj)
-                __stcg(p.agg + ws_index(unit, mi * S_NT + nj),
-                       make_float4(S[mi][nj][0], S[mi][nj][1], S[mi][nj][2], S[mi][nj][3]));
+        for (int tl = 0; tl < TILES; ++tl)
+            __stcg(p.agg + ws_index(unit, tl), make_float4(S[4 * tl], S[4 * tl + 1], S[4 * tl + 2], S[4 * tl + 3]));
         if (tid < DK) __stcg(p.alpha + unit * DK + tid, ex2(la_seg));
         __threadfence();
         __syncthreads();
         if (tid == 0) st_release(p.flags + unit, 1u);
-        float accA[S_MT][2];
-#pragma unroll
-        for (int mi = 0; mi < S_MT; ++mi) accA[mi][0] = accA[mi][1] = 1.f;
+        float accA = 1.f;  // the decay of this thread's row since the segment's start
         int j = seg - 1;
         while (true) {
             const size_t up = ((size_t)j * p.BH + bh) * p.nzb + zb;
-            if (tid == 0) s_flag = wait_flag(p.flags + up, p.hdr, 60u);
+            if (tid == 0) s_flag = wait_flag(p.flags + up, p.hdr, 62u);
             __syncthreads();
             const unsigned int f = s_flag;
             __syncthreads();
             if (f != 1u && f != 2u) break;  // the wait gave up (recorded in the header)
             const float4 *src = (f == 2u) ? p.incl : p.agg;
 #pragma unroll
-            for (int mi = 0; mi < S_MT; ++mi)
-#pragma unroll
-                for (int nj = 0; nj < S_NT; ++nj) {
-                    const float4 v = ld_cg4(src + ws_index(up, mi * S_NT + nj));
-                    Sin[mi][nj][0] = fmaf(accA[mi][0], v.x, Sin[mi][nj][0]);
-                    Sin[mi][nj][1] = fmaf(accA[mi][0], v.y, Sin[mi][nj][1]);
-                    Sin[mi][nj][2] = fmaf(accA[mi][1], v.z, Sin[mi][nj][2]);
-                    Sin[mi][nj][3] = fmaf(accA[mi][1], v.w, Sin[mi][nj][3]);
-                }
+            for (int tl = 0; tl < TILES; ++tl) {
+                const float4 v = ld_cg4(src + ws_index(up, tl));
+                Sin[4 * tl] = fmaf(accA, v.x, Sin[4 * tl]);
+                Sin[4 * tl + 1] = fmaf(accA, v.y, Sin[4 * tl + 1]);
+                Sin[4 * tl + 2] = fmaf(accA, v.z, Sin[4 * tl + 2]);
+                Sin[4 * tl + 3] = fmaf(accA, v.w, Sin[4 * tl + 3]);
+            }
             if (f == 2u) break;
-#pragma unroll
-            for (int mi = 0; mi < S_MT; ++mi)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) accA[mi][h] *= ld_cg(p.alpha + up * DK + s_row(mi, h));
+            accA *= ld_cg(p.alpha + up * DK + srow);
             if (--j < 0) {
                 add_state0(accA);
                 break;
@@ -404,15 +514,12 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
     __syncthreads();  // alpha_s visible
     if (seg != p.n_seg - 1) {
         // inclusive state at the segment's end: diag(alpha_seg) S_in + dS_seg
+        const float a = alpha_s[srow];
 #pragma unroll
-        for (int mi = 0; mi < S_MT; ++mi)
-#pragma unroll
-            for (int nj = 0; nj < S_NT; ++nj) {
-                const float a0 = alpha_s[s_row(mi, 0)], a1 = alpha_s[s_row(mi, 1)];
-                __stcg(p.incl + ws_index(unit, mi * S_NT + nj),
-                       make_float4(fmaf(a0, Sin[mi][nj][0], S[mi][nj][0]), fmaf(a0, Sin[mi][nj][1], S[mi][nj][1]),
-                                   fmaf(a1, Sin[mi][nj][2], S[mi][nj][2]), fmaf(a1, Sin[mi][nj][3], S[mi][nj][3])));
-            }
+        for (int tl = 0; tl < TILES; ++tl)
+            __stcg(p.incl + ws_index(unit, tl),
+                   make_float4(fmaf(a, Sin[4 * tl], S[4 * tl]), fmaf(a, Sin[4 * tl + 1], S[4 * tl + 1]),
+                               fmaf(a, Sin[4 * tl + 2], S[4 * tl + 2]), fmaf(a, Sin[4 * tl + 3], S[4 * tl + 3])));
         __threadfence();
         __syncthreads();
         if (tid == 0) st_release(p.flags + unit, 2u);
@@ -420,18 +527,13 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
 
     // ------------------------------------------------ phase 2: outputs from the true state
 #pragma unroll
-    for (int mi = 0; mi < S_MT; ++mi)
-#pragma unroll
-        for (int nj = 0; nj < S_NT; ++nj)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) S[mi][nj][e] = Sin[mi][nj][e];
+    for (int j = 0; j < SC; ++j) S[j] = Sin[j];
     load_stage(0, c_begin, true);
     cp_async_commit();
     if (nc > 1) load_stage(1, c_begin + 1, true);
     cp_async_commit();
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
-        const uint8_t *st = smem + stage * C::STAGE;
         const long long t0 = (long long)(c_begin + i) * kGlaTc;
         cp_async_wait<1>();
         __syncthreads();
@@ -440,138 +542,46 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_fwd_kernel(const GlaArgs p
         scale_operands(stage, true);
         state_to_mid(stage);
         write_sb();
-        __syncthreads();
-
-        // Scores of this warp's 16 rows against its half of the chunk's tokens (s in 32 hf ..
-        // 32 hf + 31): Q~ K~^T (three products), causal mask (s <= r), then P V over those
-        // tokens for all 64 columns; a half that lies after every row of the group is skipped.
-        const int arow = wr * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        float O[8][4];  // this warp's partial output: its token half, all 64 columns
-#pragma unroll
-        for (int nj = 0; nj < 8; ++nj)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) O[nj][e] = 0.f;
-        if (32 * hf <= wr * 16 + 15) {
-            float P[4][4];
-#pragma unroll
-            for (int nj = 0; nj < 4; ++nj)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) P[nj][e] = 0.f;
-#pragma unroll 2
-            for (int kk = 0; kk < DK / 16; ++kk) {
-                uint32_t qh[4], ql[4];
-                const uint32_t aoff = swz<C::QRB>(arow, 2 * kk + (lane >> 4));
-                ldsm_x4(smem_u32(st + C::OFF_Q + aoff), qh);
-                ldsm_x4(smem_u32(smem + C::OFF_QLO + aoff), ql);
-#pragma unroll
-                for (int p2 = 0; p2 < 2; ++p2) {
-                    const int brow = 16 * (2 * hf + p2) + (lane & 7) + (lane >> 4) * 8;
-                    const uint32_t boff = swz<C::QRB>(brow, 2 * kk + ((lane >> 3) & 1));
-                    uint32_t kh[4], kl[4];
-                    ldsm_x4(smem_u32(st + C::OFF_K + boff), kh);
-                    ldsm_x4(smem_u32(smem + C::OFF_KLO + boff), kl);
-                    mma16816(P[2 * p2], qh, kh[0], kh[1]);
-                    mma16816(P[2 * p2 + 1], qh, kh[2], kh[3]);
-                    mma16816(P[2 * p2], qh, kl[0], kl[1]);
-                    mma16816(P[2 * p2 + 1], qh, kl[2], kl[3]);
-                    mma16816(P[2 * p2], ql, kh[0], kh[1]);
-                    mma16816(P[2 * p2 + 1], ql, kh[2], kh[3]);
-                }
-            }
-            // the masked scores as A fragments (two k-steps of 16 tokens) in two parts
-            uint32_t ph[2][4], pl[2][4];
-#pragma unroll
-            for (int nj = 0; nj < 4; ++nj)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int r = wr * 16 + g + 8 * h, s = (4 * hf + nj) * 8 + 2 * tq;
-                    const float x0 = (s <= r) ? P[nj][2 * h] : 0.f;
-                    const float x1 = (s + 1 <= r) ? P[nj][2 * h + 1] : 0.f;
-                    // A fragment of k-step nj / 2: regs {row g, k lo}, {g + 8, lo}, {g, hi}, {g + 8, hi}
-                    split_bf16x2(make_float2(x0, x1), ph[nj >> 1][(nj & 1) * 2 + h], pl[nj >> 1][(nj & 1) * 2 + h]);
-                }
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
-#pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
-                    uint32_t b[4];
-                    const int brow = (2 * hf + kt) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                    ldsm_x4_t(smem_u32(st + C::OFF_V + swz<C::VRB>(brow, 2 * pp + (lane >> 4))), b);
-                    mma16816(O[2 * pp], ph[kt], b[0], b[1]);
-                    mma16816(O[2 * pp + 1], ph[kt], b[2], b[3]);
-                    mma16816(O[2 * pp], pl[kt], b[0], b[1]);
-                    mma16816(O[2 * pp + 1], pl[kt], b[2], b[3]);
-                }
-            }
+        hand_to_tc();
+        if (warp == 0) {
+            issue_p_o(stage);
+            issue_u(stage);
+            mma_commit_w(barA);
         }
-        // the other column half of the partial output goes to the partner warp (w ^ 4)
-        float *xo = reinterpret_cast<float *>(smem + C::OFF_XO);  // [8 warps][16 rows][32 columns]
-#pragma unroll
-        for (int nj = 0; nj < 4; ++nj)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-                *reinterpret_cast<float2 *>(xo + (warp * 16 + g + 8 * h) * 32 + nj * 8 + 2 * tq) =
-                    hf ? make_float2(O[nj][2 * h], O[nj][2 * h + 1])
-                       : make_float2(O[4 + nj][2 * h], O[4 + nj][2 * h + 1]);
-        // ... + Q~ S' for this warp's column half (three products)
-        float Oh[4][4];
-#pragma unroll
-        for (int nj = 0; nj < 4; ++nj)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) Oh[nj][e] = hf ? O[4 + nj][e] : O[nj][e];
-#pragma unroll 2
-        for (int kk = 0; kk < DK / 16; ++kk) {
-            uint32_t qh[4], ql[4];
-            const uint32_t aoff = swz<C::QRB>(arow, 2 * kk + (lane >> 4));
-            ldsm_x4(smem_u32(st + C::OFF_Q + aoff), qh);
-            ldsm_x4(smem_u32(smem + C::OFF_QLO + aoff), ql);
-#pragma unroll
-            for (int p2 = 0; p2 < 2; ++p2) {
-                const int brow = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const uint32_t boff = swz<C::VRB>(brow, 2 * (2 * hf + p2) + (lane >> 4));
-                uint32_t sh[4], sl[4];
-                ldsm_x4_t(smem_u32(smem + C::OFF_SH + boff), sh);
-                ldsm_x4_t(smem_u32(smem + C::OFF_SL + boff), sl);
-                mma16816(Oh[2 * p2], qh, sh[0], sh[1]);
-                mma16816(Oh[2 * p2 + 1], qh, sh[2], sh[3]);
-                mma16816(Oh[2 * p2], qh, sl[0], sl[1]);
-                mma16816(Oh[2 * p2 + 1], qh, sl[2], sl[3]);
-                mma16816(Oh[2 * p2], ql, sh[0], sh[1]);
-                mma16816(Oh[2 * p2 + 1], ql, sh[2], sh[3]);
-            }
+        waitA();
+        tc_fence_after();
+        mask_scores();
+        tc_fence_before();
+        __syncthreads();  // the masked parts are in tensor memory
+        tc_fence_after();
+        if (warp == 0) {
+            issue_pv(stage);
+            mma_commit_w(barB);
         }
-        __syncthreads();  // the partner's partial output is in shared memory
-#pragma unroll
-        for (int nj = 0; nj < 4; ++nj)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float2 x = *reinterpret_cast<const float2 *>(xo + ((warp ^ 4) * 16 + g + 8 * h) * 32 + nj * 8 + 2 * tq);
-                const long long t = t0 + wr * 16 + g + 8 * h;
-                if (t < p.T)
-                    *reinterpret_cast<float2 *>(p.o + ((size_t)bh * p.T + arow_of(t)) * p.DV + zb * 64 +
-                                                (4 * hf + nj) * 8 + 2 * tq) =
-                        make_float2(Oh[nj][2 * h] + x.x, Oh[nj][2 * h + 1] + x.y);
-            }
-        state_update(stage);
-        __syncthreads();
+        state_finish(stage);
+        waitB();
+        tc_fence_after();
+        write_out(t0);
+        tc_fence_before();
+        __syncthreads();  // the stage and the accumulators are consumed
         if (i + 2 < nc) load_stage(stage, c_begin + i + 2, true);
         cp_async_commit();
     }
     cp_async_wait<0>();
 
     if (seg == p.n_seg - 1 && p.ST != nullptr) {
+        // reversed: the state before token 0 of the arrays, decayed by a_0
+        const float f = p.rev ? __expf(__ldg(Gb + srow)) : 1.f;
 #pragma unroll
-        for (int mi = 0; mi < S_MT; ++mi)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int row = s_row(mi, e >> 1);
-                // reversed: the state before token 0 of the arrays, decayed by a_0
-                const float f = p.rev ? __expf(__ldg(Gb + row)) : 1.f;
-#pragma unroll
-                for (int nj = 0; nj < S_NT; ++nj)
-                    p.ST[((size_t)bh * DK + row) * p.DV + zb * 64 + s_col(nj, e)] = f * S[mi][nj][e];
-            }
+        for (int j = 0; j < SC; ++j) p.ST[((size_t)bh * DK + srow) * p.DV + zb * 64 + scol(j)] = f * S[j];
     }
+    if (timed_out) {
+        atomicOr(&p.hdr->error, kErrTimeout);
+        atomicExch(&p.hdr->where, 63u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
 }
 
 // ----------------------------------------------------------------- backward: decay on the output columns
@@ -1186,12 +1196,12 @@ int launch_gla_bwd_qk(const GlaBArgs &a, cudaStream_t s, unsigned int grid) {
 
 template <int DK>
 int launch_gla_fwd(const GlaArgs &a, cudaStream_t s, unsigned int grid) {
-    using C = GlaCfg<DK>;
+    using C = GlaTcCfg<DK>;
     static std::atomic<unsigned long long> smem_set{0};
-    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_fwd_kernel<DK>), C::SMEM);
+    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_tc_kernel<DK>), C::SMEM);
     if (st) return st;
-    gla_fwd_kernel<DK><<<grid, kGlaThreads, C::SMEM, s>>>(a);
-    return check_launch("gla_fwd_kernel");
+    gla_tc_kernel<DK><<<grid, kGlaTcThreads, C::SMEM, s>>>(a);
+    return check_launch("gla_tc_kernel");
 }
 
 }  // namespace
