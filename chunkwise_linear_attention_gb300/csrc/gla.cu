@@ -117,6 +117,7 @@ struct GlaTcCfg {
     static constexpr uint32_t C_P = 0, C_PB = 64, C_O = 128, C_U = 192, TMEM_COLS = 256;
     static constexpr int SC = (DK == 128) ? 32 : 16;  // state columns per thread
     static_assert(STAGE % 1024 == 0 && QT_BYTES % 1024 == 0, "1024-byte aligned operand tiles");
+    static_assert(2 * QT_BYTES >= 64 * 64 * 4, "the output tile fits over a stage's Q~ and K~");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
@@ -402,20 +403,33 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS) gla_t
         }
         tmem_st_wait();
     };
-    // O of this thread: row 16 q + (lane & 15), columns 32 hf + 16 (lane >> 4) + 0..15
-    auto write_out = [&](long long t0) {
-        const long long t = t0 + 16 * q + (lane & 15);
+    // O of the chunk: from tensor memory (row 16 q + (lane & 15), columns 32 hf + 16 (lane >> 4)
+    // + 0..15) into a [64][64] fp32 staging tile over the stage's Q~ / K~ high parts (dead once
+    // the products have run; 16-byte chunks XOR-ed with the row), then whole rows to global
+    // memory (a warp stores one row per instruction)
+    auto write_out = [&](int stage, long long t0) {
+        float *ot = reinterpret_cast<float *>(smem + stage * C::STAGE + C::OFF_Q);
         {
-            const int half = hf;
+            const int r = 16 * q + (lane & 15), c0 = 32 * hf + 16 * (lane >> 4);
             uint32_t o[16];
-            tmem_ld16x2(tmem + tlane + C::C_O + (uint32_t)(32 * half), o);
+            tmem_ld16x2(tmem + tlane + C::C_O + (uint32_t)(32 * hf), o);
             tmem_ld_wait();
-            if (t < p.T) {
-                float *dst = p.o + ((size_t)bh * p.T + arow_of(t)) * p.DV + zb * 64 + 32 * half + 16 * (lane >> 4);
 #pragma unroll
-                for (int c2 = 0; c2 < 8; ++c2)
-                    *reinterpret_cast<float2 *>(dst + 2 * c2) =
-                        make_float2(__uint_as_float(o[2 * c2]), __uint_as_float(o[2 * c2 + 1]));
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const int ch = ((c0 >> 2) + c4) ^ (r & 15);
+                *reinterpret_cast<float4 *>(ot + r * 64 + ch * 4) =
+                    make_float4(__uint_as_float(o[4 * c4]), __uint_as_float(o[4 * c4 + 1]),
+                                __uint_as_float(o[4 * c4 + 2]), __uint_as_float(o[4 * c4 + 3]));
+            }
+        }
+        __syncthreads();
+        for (int idx = tid; idx < kGlaTc * 32; idx += kGlaTcThreads) {
+            const int r = idx >> 5, c2 = idx & 31;
+            const long long t = t0 + r;
+            if (t < p.T) {
+                const int ch = (c2 >> 1) ^ (r & 15);
+                const float2 v = *reinterpret_cast<const float2 *>(ot + r * 64 + ch * 4 + (c2 & 1) * 2);
+                *reinterpret_cast<float2 *>(p.o + ((size_t)bh * p.T + arow_of(t)) * p.DV + zb * 64 + 2 * c2) = v;
             }
         }
     };
@@ -561,7 +575,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS) gla_t
         state_finish(stage);
         waitB();
         tc_fence_after();
-        write_out(t0);
+        write_out(stage, t0);
         tc_fence_before();
         __syncthreads();  // the stage and the accumulators are consumed
         if (i + 2 < nc) load_stage(stage, c_begin + i + 2, true);
