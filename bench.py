@@ -509,34 +509,40 @@ def bench_delta(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
     ws = torch.empty(max(cla.delta_workspace_size(B, H, T, dk, dv, 64), 256), dtype=torch.uint8, device=dev)
     o = torch.empty(B, H, T, dv, device=dev)
     ST = torch.empty(B, H, dk, dv, device=dev)
-    fwd = lambda: cla.delta_fwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], t["S0"], o=o, ST=ST, workspace=ws)
+    # the training step's path: the forward saves the state entering every chunk, the backward starts from it
+    ck = cla.delta_ckpt(t["q"], t["v"])
+    fwd = lambda: cla.delta_fwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], t["S0"], o=o, ST=ST, ckpt=ck,
+                                workspace=ws)
     tf = _time_calls(torch, fwd, flush, iters)
     cla.check_status(ws)
     wb = torch.empty(max(cla.delta_bwd_workspace_size(B, H, T, dk, dv, 64), 256), dtype=torch.uint8, device=dev)
     g = [torch.empty(B, H, T, dk, device=dev), torch.empty(B, H, T, dk, device=dev), torch.empty(B, H, T, dv, device=dev),
          torch.empty(B, H, T, device=dev), torch.empty(B, H, T, device=dev), torch.empty(B, H, dk, dv, device=dev)]
-    bwd = lambda: cla.delta_bwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], t["S0"], t["dO"], None, dq=g[0],
-                                dk=g[1], dv=g[2], dlog_decay=g[3], dbeta=g[4], dS0=g[5], workspace=wb)
-    tb = _time_calls(torch, bwd, flush, iters)
+    bwd = lambda ckpt: cla.delta_bwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], t["S0"], t["dO"], None, dq=g[0],
+                                     dk=g[1], dv=g[2], dlog_decay=g[3], dbeta=g[4], dS0=g[5], ckpt=ckpt, workspace=wb)
+    tb = _time_calls(torch, lambda: bwd(ck), flush, iters)
+    tb_plain = _time_calls(torch, lambda: bwd(None), flush, iters)
     cla.check_status(wb)
     ntok = B * H * T
     # the decayed-linear-attention part (scores, P Veff, Q S, state update) plus the chunk's own
     # extra products (K K^T, K S, (I + A)^-1 X): 2 C (2 dk + 2 dv) + 6 dk dv per token
     fl = ntok * (2 * 64 * (2 * dk + 2 * dv) + 6 * dk * dv)
-    # backward: the states pass (K K^T, K S, (I + A)^-1 X, state update) and the chunk adjoint
-    # (recomputed K K^T, K S, U; P^T, P^T dO, K dS', dX, dP, P, dA, dQ's two products, dK's five,
-    # dS's two): 2 C (8 dk + 6 dv) + 18 dk dv per token
-    flb = ntok * (2 * 64 * (8 * dk + 6 * dv) + 18 * dk * dv)
+    # backward from the checkpoint: the chunk adjoint (recomputed K K^T, K S, U; P^T, P^T dO, K dS', dX,
+    # dP, P, dA, dQ's two products, dK's five, dS's two): 2 C (7 dk + 5 dv) + 16 dk dv per token
+    flb = ntok * (2 * 64 * (7 * dk + 5 * dv) + 16 * dk * dv)
     by_min = ntok * (2 * (2 * dk + dv) + 8 + 2 * dv)
     sec, secb = tf / 1e3, tb / 1e3
     return {"workload": f"delta rule (Gated DeltaNet) fwd+bwd B={B} H={H} T={T} dk={dk} dv={dv} chunk=64",
             "fwd_us": round(tf * 1e3, 1), "bwd_us": round(tb * 1e3, 1),
+            "bwd_us_without_checkpoint": round(tb_plain * 1e3, 1),
+            "checkpoint": "the forward saves the state entering every chunk; the backward starts from it",
             "tokens_per_s": round(B * T / (sec + secb), 1),
             "fwd_TFLOPs": round(fl / sec / 1e12, 2), "bwd_TFLOPs": round(flb / secb / 1e12, 2),
             "frac_bf16_peak": round((fl + flb) / (sec + secb) / (peaks["bf16_tflops"] * 1e12), 4),
             "frac_hbm_min_bytes": round(by_min / sec / (peaks["hbm_gbs"] * 1e9), 4),
-            "kernels": "delta_fwd_kernel (mma.sync m16n8k16; chunks of a head in order, no look-back); backward: "
-                       "delta_fwd_kernel states pass, delta_bwd_kernel (chunks in reverse), delta_bwd_reduce_kernel"}
+            "kernels": "delta_fwd_kernel (mma.sync m16n8k16; chunks of a head in order, no look-back; saves the "
+                       "checkpoint); backward: delta_bwd_kernel (chunks in reverse, from the checkpoint; without "
+                       "one a states pass of delta_fwd_kernel runs first), delta_bwd_reduce_kernel"}
 
 
 def bench_selective(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):

@@ -73,6 +73,9 @@ def lib():
                 "cla_delta_fwd": ([P] * 8 + [I64] * 5 + [INT, P, SZ, P], INT),
                 "cla_delta_bwd_workspace_size": ([I64] * 5 + [INT], SZ),
                 "cla_delta_bwd": ([P] * 14 + [I64] * 5 + [INT, P, SZ, P], INT),
+                "cla_delta_ckpt_size": ([I64] * 5 + [INT], SZ),
+                "cla_delta_fwd_ckpt": ([P] * 9 + [I64] * 5 + [INT, P, SZ, P], INT),
+                "cla_delta_bwd_ckpt": ([P] * 15 + [I64] * 5 + [INT, P, SZ, P], INT),
                 "cla_state_compose": ([P] * 4 + [I64] * 7 + [P], INT),
             }
             for name, (args, res) in sig.items():
@@ -412,34 +415,6 @@ def gla_fwd(q, k, v, log_decay, S0=None, *, chunk=64, o=None, ST=None, workspace
     return o, ST
 
 
-def delta_bwd_workspace_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
-    return int(lib().cla_delta_bwd_workspace_size(B, H, T, dim_k, dim_v, int(chunk)))
-
-
-def delta_bwd(q, k, v, log_decay, beta, S0, dO, dST=None, *, chunk=64, dq=None, dk=None, dv=None,
-              dlog_decay=None, dbeta=None, dS0=None, workspace=None, stream=None):
-    """Adjoint of delta_fwd (dO bf16 [B, H, T, dv]); returns (dq, dk, dv, dlog_decay, dbeta, dS0)."""
-    B, H, T, dkk = _dims(q, 4, "q")
-    dvv = _dims(v, 4, "v")[3]
-    dev = q.device
-    f32, bf16 = torch.float32, torch.bfloat16
-    dq = _out(dq, (B, H, T, dkk), f32, dev)
-    dk = _out(dk, (B, H, T, dkk), f32, dev)
-    dv = _out(dv, (B, H, T, dvv), f32, dev)
-    dlog_decay = _out(dlog_decay, (B, H, T), f32, dev)
-    dbeta = _out(dbeta, (B, H, T), f32, dev)
-    dS0 = _out(dS0, (B, H, dkk, dvv), f32, dev)
-    ws = _ws(delta_bwd_workspace_size(B, H, T, dkk, dvv, chunk), dev, workspace)
-    tk, tv, st, bht = (B, H, T, dkk), (B, H, T, dvv), (B, H, dkk, dvv), (B, H, T)
-    _launch("cla_delta_bwd", dev, (
-        _T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
-        _T(log_decay, f32, "log_decay", bht), _T(beta, f32, "beta", bht), _T(S0, f32, "S0", st),
-        _T(dO, bf16, "dO", tv), _T(dST, f32, "dST", st), _T(dq, f32, "dq", tk), _T(dk, f32, "dk", tk),
-        _T(dv, f32, "dv", tv), _T(dlog_decay, f32, "dlog_decay", bht), _T(dbeta, f32, "dbeta", bht),
-        _T(dS0, f32, "dS0", st), B, H, T, dkk, dvv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws)), stream)
-    return dq, dk, dv, dlog_decay, dbeta, dS0
-
-
 def gla_bwd_workspace_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
     return int(lib().cla_gla_bwd_workspace_size(B, H, T, dim_k, dim_v, int(chunk)))
 
@@ -504,9 +479,30 @@ def delta_workspace_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
     return int(lib().cla_delta_workspace_size(B, H, T, dim_k, dim_v, int(chunk)))
 
 
-def delta_fwd(q, k, v, log_decay, beta, S0=None, *, chunk=64, o=None, ST=None, workspace=None, stream=None):
+def delta_ckpt_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
+    """Bytes of the checkpoint (the state entering every chunk) the forward can save for the backward."""
+    return int(lib().cla_delta_ckpt_size(B, H, T, dim_k, dim_v, int(chunk)))
+
+
+def delta_ckpt(q, v, *, chunk=64):
+    """A device buffer (fp32) for the checkpoint of a delta_fwd on q [B, H, T, dk], v [.., dv]."""
+    B, H, T, dk = _dims(q, 4, "q")
+    n = delta_ckpt_size(B, H, T, dk, v.shape[-1], chunk) // 4
+    return torch.empty(max(n, 1), dtype=torch.float32, device=q.device)
+
+
+def _delta_ckpt_arg(ckpt, B, H, T, dk, dv, chunk):
+    need = delta_ckpt_size(B, H, T, dk, dv, chunk)
+    if _nbytes(ckpt) < need:
+        raise ValueError(f"ckpt: need at least {need} bytes, got {_nbytes(ckpt)}")
+    return _T(ckpt, torch.float32, "ckpt")
+
+
+def delta_fwd(q, k, v, log_decay, beta, S0=None, *, chunk=64, o=None, ST=None, ckpt=None, workspace=None,
+              stream=None):
     """Delta rule with a decay per head: S_t = a_t (I - beta_t k_t^T k_t) S_{t-1} + beta_t k_t^T v_t,
-    o_t = q_t S_t; log_decay, beta [B, H, T].  Returns (o, ST)."""
+    o_t = q_t S_t; log_decay, beta [B, H, T].  Returns (o, ST).  With ckpt (see delta_ckpt) it also
+    saves the state entering every chunk for delta_bwd."""
     B, H, T, dk = _dims(q, 4, "q")
     dv = _dims(v, 4, "v")[3]
     dev = q.device
@@ -515,11 +511,14 @@ def delta_fwd(q, k, v, log_decay, beta, S0=None, *, chunk=64, o=None, ST=None, w
     ST = _out(ST, (B, H, dk, dv), f32, dev)
     ws = _ws(delta_workspace_size(B, H, T, dk, dv, chunk), dev, workspace)
     tk, tv, st, bht = (B, H, T, dk), (B, H, T, dv), (B, H, dk, dv), (B, H, T)
-    _launch("cla_delta_fwd", dev, (
-        _T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
-        _T(log_decay, f32, "log_decay", bht), _T(beta, f32, "beta", bht), _T(S0, f32, "S0", st),
-        _T(o, f32, "o", tv), _T(ST, f32, "ST", st),
-        B, H, T, dk, dv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws)), stream)
+    args = (_T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
+            _T(log_decay, f32, "log_decay", bht), _T(beta, f32, "beta", bht), _T(S0, f32, "S0", st),
+            _T(o, f32, "o", tv), _T(ST, f32, "ST", st))
+    tail = (B, H, T, dk, dv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws))
+    if ckpt is None:
+        _launch("cla_delta_fwd", dev, args + tail, stream)
+    else:
+        _launch("cla_delta_fwd_ckpt", dev, args + (_delta_ckpt_arg(ckpt, B, H, T, dk, dv, chunk),) + tail, stream)
     return o, ST
 
 
@@ -528,8 +527,9 @@ def delta_bwd_workspace_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
 
 
 def delta_bwd(q, k, v, log_decay, beta, S0, dO, dST=None, *, chunk=64, dq=None, dk=None, dv=None,
-              dlog_decay=None, dbeta=None, dS0=None, workspace=None, stream=None):
-    """Adjoint of delta_fwd (dO bf16 [B, H, T, dv]); returns (dq, dk, dv, dlog_decay, dbeta, dS0)."""
+              dlog_decay=None, dbeta=None, dS0=None, ckpt=None, workspace=None, stream=None):
+    """Adjoint of delta_fwd (dO bf16 [B, H, T, dv]); returns (dq, dk, dv, dlog_decay, dbeta, dS0).  ckpt:
+    the checkpoint a delta_fwd on the same inputs saved (the states are then not recomputed)."""
     B, H, T, dkk = _dims(q, 4, "q")
     dvv = _dims(v, 4, "v")[3]
     dev = q.device
@@ -540,12 +540,19 @@ def delta_bwd(q, k, v, log_decay, beta, S0, dO, dST=None, *, chunk=64, dq=None, 
     dlog_decay = _out(dlog_decay, (B, H, T), f32, dev)
     dbeta = _out(dbeta, (B, H, T), f32, dev)
     dS0 = _out(dS0, (B, H, dkk, dvv), f32, dev)
-    ws = _ws(delta_bwd_workspace_size(B, H, T, dkk, dvv, chunk), dev, workspace)
+    need = delta_bwd_workspace_size(B, H, T, dkk, dvv, chunk)
+    if ckpt is not None:  # no states in the workspace: the header and the partials only
+        need = max(need - delta_ckpt_size(B, H, T, dkk, dvv, chunk), 256)
+    ws = _ws(need, dev, workspace)
     tk, tv, st, bht = (B, H, T, dkk), (B, H, T, dvv), (B, H, dkk, dvv), (B, H, T)
-    _launch("cla_delta_bwd", dev, (
-        _T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
-        _T(log_decay, f32, "log_decay", bht), _T(beta, f32, "beta", bht), _T(S0, f32, "S0", st),
-        _T(dO, bf16, "dO", tv), _T(dST, f32, "dST", st), _T(dq, f32, "dq", tk), _T(dk, f32, "dk", tk),
-        _T(dv, f32, "dv", tv), _T(dlog_decay, f32, "dlog_decay", bht), _T(dbeta, f32, "dbeta", bht),
-        _T(dS0, f32, "dS0", st), B, H, T, dkk, dvv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws)), stream)
+    args = (_T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
+            _T(log_decay, f32, "log_decay", bht), _T(beta, f32, "beta", bht), _T(S0, f32, "S0", st),
+            _T(dO, bf16, "dO", tv), _T(dST, f32, "dST", st), _T(dq, f32, "dq", tk), _T(dk, f32, "dk", tk),
+            _T(dv, f32, "dv", tv), _T(dlog_decay, f32, "dlog_decay", bht), _T(dbeta, f32, "dbeta", bht),
+            _T(dS0, f32, "dS0", st))
+    tail = (B, H, T, dkk, dvv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws))
+    if ckpt is None:
+        _launch("cla_delta_bwd", dev, args + tail, stream)
+    else:
+        _launch("cla_delta_bwd_ckpt", dev, args + (_delta_ckpt_arg(ckpt, B, H, T, dkk, dvv, chunk),) + tail, stream)
     return dq, dk, dv, dlog_decay, dbeta, dS0

@@ -1363,6 +1363,11 @@ int launch_delta_bwd(const DeltaBwdArgs &a, cudaStream_t s, unsigned int grid) {
     return check_launch("delta_bwd_kernel");
 }
 
+// Bytes of the states the backward works from (the state entering every chunk), 16-aligned.
+size_t delta_states_bytes(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv) {
+    return align_up(sizeof(float) * (size_t)(B * H) * (size_t)((T + kDlTc - 1) / kDlTc) * (size_t)dk * (size_t)dv, 16);
+}
+
 // Workspace of the backward: the header, the state entering every chunk, and the partials of the
 // value-column blocks after the first.  0 when the shape is unsupported or the size overflows.
 size_t delta_bwd_ws_bytes(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv) {
@@ -1391,12 +1396,11 @@ extern "C" size_t cla_delta_workspace_size(int64_t B, int64_t H, int64_t T, int6
     return sizeof(WsHeader);
 }
 
-extern "C" int cla_delta_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
-                             const float *beta, const float *S0, float *o, float *ST, int64_t B, int64_t H,
-                             int64_t T, int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes,
-                             void *stream) {
+namespace {
+int delta_fwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                   const float *beta, const float *S0, float *o, float *ST, float *ckpt, int64_t B, int64_t H,
+                   int64_t T, int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
     clear_error();
-    const char *fn = "cla_delta_fwd";
     if (B < 0 || H < 0 || T < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
     if (!delta_supported(B, H, T, dim_k, dim_v, chunk))
         return fail(CLA_ERR_UNSUPPORTED, "%s: needs dim_k 64 or 128, dim_v a multiple of 64 up to 1024 and chunk 64 "
@@ -1438,8 +1442,34 @@ extern "C" int cla_delta_fwd(const uint16_t *q, const uint16_t *k, const uint16_
     a.n_chunks = (int)((T + kDlTc - 1) / kDlTc);
     a.T = T;
     a.hdr = static_cast<WsHeader *>(ws);
+    a.states = ckpt;
     const unsigned int grid = (unsigned int)(BH * (dim_v / 64));
     return dim_k == 64 ? launch_delta_fwd<64>(a, s, grid) : launch_delta_fwd<128>(a, s, grid);
+}
+}  // namespace
+
+extern "C" size_t cla_delta_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk) {
+    if (!delta_supported(B, H, T, dim_k, dim_v, chunk)) return 0;
+    const double bytes = (double)B * H * (double)((T + kDlTc - 1) / kDlTc) * dim_k * dim_v * 4.0;
+    return bytes > 9.0e18 ? 0 : (size_t)bytes;
+}
+
+extern "C" int cla_delta_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                             const float *beta, const float *S0, float *o, float *ST, int64_t B, int64_t H,
+                             int64_t T, int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes,
+                             void *stream) {
+    return delta_fwd_impl("cla_delta_fwd", q, k, v, log_decay, beta, S0, o, ST, nullptr, B, H, T, dim_k, dim_v,
+                          chunk, ws, ws_bytes, stream);
+}
+
+extern "C" int cla_delta_fwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                                  const float *beta, const float *S0, float *o, float *ST, float *ckpt, int64_t B,
+                                  int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk, void *ws,
+                                  size_t ws_bytes, void *stream) {
+    if (ckpt != nullptr && !aligned16(ckpt))
+        return fail(CLA_ERR_INVALID_ARG, "cla_delta_fwd_ckpt: ckpt must be 16-byte aligned");
+    return delta_fwd_impl("cla_delta_fwd_ckpt", q, k, v, log_decay, beta, S0, o, ST, ckpt, B, H, T, dim_k, dim_v,
+                          chunk, ws, ws_bytes, stream);
 }
 
 extern "C" size_t cla_delta_bwd_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
@@ -1448,13 +1478,12 @@ extern "C" size_t cla_delta_bwd_workspace_size(int64_t B, int64_t H, int64_t T, 
     return delta_bwd_ws_bytes(B, H, T, dim_k, dim_v);
 }
 
-extern "C" int cla_delta_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
-                             const float *beta, const float *S0, const uint16_t *dO, const float *dST, float *dq,
-                             float *dk, float *dv, float *dlog_decay, float *dbeta, float *dS0, int64_t B,
-                             int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk, void *ws,
-                             size_t ws_bytes, void *stream) {
+namespace {
+int delta_bwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                   const float *beta, const float *S0, const uint16_t *dO, const float *dST, float *dq, float *dk,
+                   float *dv, float *dlog_decay, float *dbeta, float *dS0, const float *ckpt, int64_t B, int64_t H,
+                   int64_t T, int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
     clear_error();
-    const char *fn = "cla_delta_bwd";
     if (B < 0 || H < 0 || T < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
     if (!delta_supported(B, H, T, dim_k, dim_v, chunk))
         return fail(CLA_ERR_UNSUPPORTED, "%s: needs dim_k 64 or 128, dim_v a multiple of 64 up to 1024 and chunk 64 "
@@ -1478,38 +1507,44 @@ extern "C" int cla_delta_bwd(const uint16_t *q, const uint16_t *k, const uint16_
     if (!aligned_or_null({dq, dk, dv, dS0, dST, S0}, 8) || !aligned_or_null({log_decay, beta, dlog_decay, dbeta}, 4))
         return fail(CLA_ERR_INVALID_ARG, "%s: dq, dk, dv, dS0, dST, S0 must be 8-byte aligned, log_decay, beta, "
                     "dlog_decay, dbeta 4-byte", fn);
-    const size_t need = delta_bwd_ws_bytes(B, H, T, dim_k, dim_v);
-    if (need == 0) return fail(CLA_ERR_UNSUPPORTED, "%s: workspace size overflows", fn);
+    if (ckpt != nullptr && !aligned16(ckpt)) return fail(CLA_ERR_INVALID_ARG, "%s: ckpt must be 16-byte aligned", fn);
+    // with a checkpoint the states pass is skipped and the workspace holds the header and the partials only
+    const size_t full = delta_bwd_ws_bytes(B, H, T, dim_k, dim_v);
+    if (full == 0) return fail(CLA_ERR_UNSUPPORTED, "%s: workspace size overflows", fn);
+    const size_t need = ckpt ? full - delta_states_bytes(B, H, T, dim_k, dim_v) : full;
     if (!ws || !aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace NULL or unaligned", fn);
     if (ws_bytes < need) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, need);
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), s), fn);
     const int n_chunks = (int)((T + kDlTc - 1) / kDlTc);
-    float *states = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + sizeof(WsHeader));
-    const size_t states_bytes = align_up(sizeof(float) * (size_t)BH * n_chunks * dim_k * dim_v, 16);
+    float *ws_states = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + sizeof(WsHeader));
+    const size_t states_bytes = ckpt ? 0 : delta_states_bytes(B, H, T, dim_k, dim_v);
     const unsigned int grid = (unsigned int)(BH * (dim_v / 64));
-    // the states pass: the forward kernel writes the state entering every chunk, no output
-    DeltaArgs f;
-    memset(&f, 0, sizeof(f));
-    f.q = reinterpret_cast<const bf16 *>(q);
-    f.k = reinterpret_cast<const bf16 *>(k);
-    f.v = reinterpret_cast<const bf16 *>(v);
-    f.g = log_decay;
-    f.beta = beta;
-    f.S0 = S0;
-    f.states = states;
-    f.BH = (int)BH;
-    f.DV = (int)dim_v;
-    f.nzb = (int)(dim_v / 64);
-    f.n_chunks = n_chunks;
-    f.T = T;
-    f.hdr = static_cast<WsHeader *>(ws);
-    int st = dim_k == 64 ? launch_delta_fwd<64>(f, s, grid) : launch_delta_fwd<128>(f, s, grid);
-    if (st) return st;
+    const float *states = ckpt ? ckpt : ws_states;
+    // the states pass (no checkpoint): the forward kernel writes the state entering every chunk, no output
+    if (!ckpt) {
+        DeltaArgs f;
+        memset(&f, 0, sizeof(f));
+        f.q = reinterpret_cast<const bf16 *>(q);
+        f.k = reinterpret_cast<const bf16 *>(k);
+        f.v = reinterpret_cast<const bf16 *>(v);
+        f.g = log_decay;
+        f.beta = beta;
+        f.S0 = S0;
+        f.states = ws_states;
+        f.BH = (int)BH;
+        f.DV = (int)dim_v;
+        f.nzb = (int)(dim_v / 64);
+        f.n_chunks = n_chunks;
+        f.T = T;
+        f.hdr = static_cast<WsHeader *>(ws);
+        const int st = dim_k == 64 ? launch_delta_fwd<64>(f, s, grid) : launch_delta_fwd<128>(f, s, grid);
+        if (st) return st;
+    }
     DeltaBwdArgs a;
     memset(&a, 0, sizeof(a));
-    a.q = f.q;
-    a.k = f.k;
-    a.v = f.v;
+    a.q = reinterpret_cast<const bf16 *>(q);
+    a.k = reinterpret_cast<const bf16 *>(k);
+    a.v = reinterpret_cast<const bf16 *>(v);
     a.dO = reinterpret_cast<const bf16 *>(dO);
     a.g = log_decay;
     a.beta = beta;
@@ -1521,15 +1556,15 @@ extern "C" int cla_delta_bwd(const uint16_t *q, const uint16_t *k, const uint16_
     a.dlog = dlog_decay;
     a.dbeta = dbeta;
     a.dS0 = dS0;
-    a.part = dim_v > 64 ? reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(states) + states_bytes) : nullptr;
+    a.part = dim_v > 64 ? reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws_states) + states_bytes) : nullptr;
     a.part_stride = (long long)BH * T * (2 * dim_k + 2);
     a.BH = (int)BH;
     a.DV = (int)dim_v;
     a.nzb = (int)(dim_v / 64);
     a.n_chunks = n_chunks;
     a.T = T;
-    st = dim_k == 64 ? launch_delta_bwd<64>(a, s, grid) : launch_delta_bwd<128>(a, s, grid);
-    if (st) return st;
+    const int st2 = dim_k == 64 ? launch_delta_bwd<64>(a, s, grid) : launch_delta_bwd<128>(a, s, grid);
+    if (st2) return st2;
     if (a.nzb > 1) {
         const long long ntok = (long long)BH * T;
         const long long work = ntok * dim_k;
@@ -1539,4 +1574,23 @@ extern "C" int cla_delta_bwd(const uint16_t *q, const uint16_t *k, const uint16_
         return check_launch("delta_bwd_reduce_kernel");
     }
     return CLA_OK;
+}
+}  // namespace
+
+extern "C" int cla_delta_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                             const float *beta, const float *S0, const uint16_t *dO, const float *dST, float *dq,
+                             float *dk, float *dv, float *dlog_decay, float *dbeta, float *dS0, int64_t B,
+                             int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk, void *ws,
+                             size_t ws_bytes, void *stream) {
+    return delta_bwd_impl("cla_delta_bwd", q, k, v, log_decay, beta, S0, dO, dST, dq, dk, dv, dlog_decay, dbeta, dS0,
+                          nullptr, B, H, T, dim_k, dim_v, chunk, ws, ws_bytes, stream);
+}
+
+extern "C" int cla_delta_bwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                                  const float *beta, const float *S0, const uint16_t *dO, const float *dST, float *dq,
+                                  float *dk, float *dv, float *dlog_decay, float *dbeta, float *dS0,
+                                  const float *ckpt, int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
+                                  int chunk, void *ws, size_t ws_bytes, void *stream) {
+    return delta_bwd_impl("cla_delta_bwd_ckpt", q, k, v, log_decay, beta, S0, dO, dST, dq, dk, dv, dlog_decay, dbeta,
+                          dS0, ckpt, B, H, T, dim_k, dim_v, chunk, ws, ws_bytes, stream);
 }

@@ -461,6 +461,40 @@ int cla_delta_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                   int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
                   int chunk, void *ws, size_t ws_bytes, void *stream);
 
+/* Checkpoint of the delta rule's forward for its backward ("The backward pass
+ * is a scan in reverse": store the states or recompute them).  The backward
+ * works from the state entering every chunk; the forward computes exactly
+ * those states, so it can save them instead of the backward re-running it.
+ * Bytes of the checkpoint: B H ceil(T / 64) dim_k dim_v fp32 values; 0 for
+ * sizes, head dims or chunks the fwd / bwd calls refuse. */
+size_t cla_delta_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                           int64_t dim_v, int chunk);
+
+/* cla_delta_fwd that also writes the checkpoint: ckpt (device,
+ * cla_delta_ckpt_size bytes, 16-byte aligned, owned by the caller) gets the
+ * state entering each 64-token chunk, [B, H, ceil(T / 64), dim_k, dim_v].
+ * ckpt = NULL is the plain forward. */
+int cla_delta_fwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const float *log_decay, const float *beta, const float *S0,
+                       float *o, float *ST, float *ckpt, int64_t B, int64_t H,
+                       int64_t T, int64_t dim_k, int64_t dim_v, int chunk, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/* cla_delta_bwd from the checkpoint a cla_delta_fwd_ckpt call on the same q,
+ * k, v, log_decay, beta, S0, sizes and chunk wrote (read only): no states
+ * pass, and the workspace needs only the header and the partial gradients
+ * (cla_delta_bwd_workspace_size bytes are always enough).  The gradients are
+ * those of cla_delta_bwd (the same states, bit for bit).  ckpt = NULL is
+ * cla_delta_bwd.  A checkpoint from other inputs gives wrong gradients;
+ * nothing checks it, and the non-finite input check ran in the forward. */
+int cla_delta_bwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const float *log_decay, const float *beta, const float *S0,
+                       const uint16_t *dO, const float *dST, float *dq, float *dk,
+                       float *dv, float *dlog_decay, float *dbeta, float *dS0,
+                       const float *ckpt, int64_t B, int64_t H, int64_t T,
+                       int64_t dim_k, int64_t dim_v, int chunk, void *ws,
+                       size_t ws_bytes, void *stream);
+
 /* ======================================================================== */
 /* State passing between slices of one sequence                             */
 /* ======================================================================== */

@@ -129,3 +129,29 @@ def test_delta_bwd_workload_full_sampled_heads(cla):
     """The full delta workload (4 x 32 x 4096, d = 128), every gradient of two heads."""
     inp = workloads.make("delta")
     _run_bwd(cla, inp, heads=[5, 26])
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv", [(1, 2, 700, 128, 64), (1, 1, 129, 64, 192), (2, 2, 1100, 128, 128)])
+def test_delta_checkpoint_gives_the_same_gradients(cla, B, H, T, dk, dv):
+    """A forward that saves the state entering every chunk, then the backward from it (no states
+    pass): the same output and, bit for bit, the same gradients as the plain calls, which match
+    the oracle; the backward's workspace then needs no room for the states."""
+    inp = workloads.make("delta", B=B, H=H, T=T, dk=dk, dv=dv)
+    t = {k: v.cuda() for k, v in inp.items()}
+    dST = torch.from_numpy(np.random.default_rng(5).normal(size=(B, H, dk, dv)).astype(np.float32)).cuda()
+    ck = cla.delta_ckpt(t["q"], t["v"])
+    o1, ST1 = cla.delta_fwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], t["S0"])
+    o2, ST2 = cla.delta_fwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], t["S0"], ckpt=ck)
+    assert torch.equal(o1, o2) and torch.equal(ST1, ST2)
+    g1 = cla.delta_bwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], t["S0"], t["dO"], dST)
+    full = cla.delta_bwd_workspace_size(B, H, T, dk, dv, 64)
+    small = full - cla.delta_ckpt_size(B, H, T, dk, dv, 64)
+    ws = torch.empty(max(small, 256) + 16, dtype=torch.uint8, device="cuda")
+    g2 = cla.delta_bwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], t["S0"], t["dO"], dST, ckpt=ck,
+                       workspace=ws[: max(small, 256)])
+    cla.check_status(ws)
+    for name, a, b in zip(("dq", "dk", "dv", "dlog_a", "dbeta", "dS0"), g1, g2):
+        assert torch.equal(a, b), name
+    ref = oracle.delta_bwd(inp["q"], inp["k"], inp["v"], inp["log_a"], inp["beta"], inp["S0"], inp["dO"], dST.cpu())
+    for name, g, r in zip(("dq", "dk", "dv", "dlog_a", "dbeta", "dS0"), g2, ref):
+        assert_bf16(name, g, r)
