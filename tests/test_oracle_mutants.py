@@ -86,6 +86,11 @@ MUTANTS = [
      "db += kS[j] * (vt[j] + at * u[j]);", 0),
     ("delta bwd: adjoint without the rank-one part",
      "tmp[i * dv + j] = at * (Sbar[i * dv + j] - bt * kt[i] * kS[j]);", "tmp[i * dv + j] = at * Sbar[i * dv + j];", 0),
+    ("delta bwd: dv without beta", "dvv[(un * T + t) * dv + j] = bt * sk;", "dvv[(un * T + t) * dv + j] = sk;", 0),
+    ("delta bwd: dlog a without the rank-one part", "dlog_a[un * T + t] = at * (s - bt * c);",
+     "dlog_a[un * T + t] = at * s;", 0),
+    ("delta bwd: dq read from the state before the step", "const double *cur = states + (t + 1) * ss;",
+     "const double *cur = states + t * ss;", 0),
 ]
 
 
