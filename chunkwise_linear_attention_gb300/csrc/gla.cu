@@ -1066,8 +1066,9 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
 // Yang et al.'s form for gated linear attention):
 //   dlog a_u[i] = sum_{t>=u} (q_t[i] dq_t[i] - k_t[i] dk_t[i]) + fs[i],
 // fs[i] = sum_j dST[i][j] S_T[i][j].  A reverse scan over tiles of
-// kGlaDlTile tokens: per-tile column sums first, then each tile's suffix sums
-// plus every later tile and fs.  Thread = key dimension (coalesced rows);
+// kGlaDlTile tokens: per-tile column sums first, then (one short pass per
+// batch and head) the sum of every later tile and fs for each tile, then
+// each tile's suffix sums from it.  Thread = key dimension (coalesced rows);
 // fixed summation order; loops unrolled so a thread's loads are in flight
 // together.
 constexpr int kGlaDlTile = 128;
@@ -1089,15 +1090,30 @@ __global__ void gla_dlog_tile_sums_kernel(const bf16 *__restrict__ q, const floa
     tsum[(bh * n_tiles + tile) * DK + i] = acc;
 }
 
+// The tile sums of one (batch, head) become, in place and in the same fixed order, the sums of
+// every later tile plus the final-state term: what each tile's suffix scan starts from.
+__global__ void gla_dlog_tile_suffix_kernel(float *__restrict__ tsum, const float *__restrict__ fs, int DK,
+                                            int n_tiles) {
+    const size_t bh = blockIdx.x;
+    const int i = threadIdx.x;
+    float run = fs ? fs[bh * DK + i] : 0.f;
+#pragma unroll 4
+    for (int j = n_tiles - 1; j >= 0; --j) {
+        float *x = tsum + (bh * n_tiles + j) * DK + i;
+        const float v = *x;
+        *x = run;
+        run += v;
+    }
+}
+
 __global__ void gla_dlog_finalize_kernel(const bf16 *__restrict__ q, const float *__restrict__ dq,
                                          const bf16 *__restrict__ k, const float *__restrict__ dk,
-                                         const float *__restrict__ tsum, const float *__restrict__ fs,
-                                         float *__restrict__ dlog, int DK, long long T, int n_tiles) {
+                                         const float *__restrict__ tsum, float *__restrict__ dlog, int DK,
+                                         long long T, int n_tiles) {
     const int tile = (int)(blockIdx.x % (unsigned)n_tiles);
     const size_t bh = blockIdx.x / (unsigned)n_tiles;
     const int i = threadIdx.x;
-    float run = fs ? fs[bh * DK + i] : 0.f;
-    for (int j = n_tiles - 1; j > tile; --j) run += tsum[(bh * n_tiles + j) * DK + i];
+    float run = tsum[(bh * n_tiles + tile) * DK + i];  // the later tiles and the final-state term
     const long long t0 = (long long)tile * kGlaDlTile;
 #pragma unroll 8
     for (long long t = min(t0 + kGlaDlTile, T) - 1; t >= t0; --t) {
@@ -1406,7 +1422,10 @@ extern "C" int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t 
         gla_dlog_tile_sums_kernel<<<grid, (unsigned int)dim_k, 0, s>>>(Q, dq, K, dk, tsum, (int)dim_k, T, pl.tiles);
         st = check_launch("gla_dlog_tile_sums_kernel");
         if (st) return st;
-        gla_dlog_finalize_kernel<<<grid, (unsigned int)dim_k, 0, s>>>(Q, dq, K, dk, tsum, fs, dlog_decay, (int)dim_k, T,
+        gla_dlog_tile_suffix_kernel<<<(unsigned int)BH, (unsigned int)dim_k, 0, s>>>(tsum, fs, (int)dim_k, pl.tiles);
+        st = check_launch("gla_dlog_tile_suffix_kernel");
+        if (st) return st;
+        gla_dlog_finalize_kernel<<<grid, (unsigned int)dim_k, 0, s>>>(Q, dq, K, dk, tsum, dlog_decay, (int)dim_k, T,
                                                                       pl.tiles);
         st = check_launch("gla_dlog_finalize_kernel");
     }
