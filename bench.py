@@ -492,9 +492,9 @@ def bench_gla(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
            "fwd_GBps": round(by / sec / 1e9, 1),
            "frac_bf16_peak": round((fl + fl_b) / (sec + secb) / bf, 4),
            "frac_binding_roofline_min_bytes": round(max((by_min + by_b_min) / hbm, (fl + fl_b) / bf) / (sec + secb), 4),
-           "kernels": "gla_tc_kernel (tcgen05.mma kind::f16, fp32 accumulators in tensor memory: the forward and "
-                      "the backward's reversed dV traversal), gla_bwd_qk_kernel (mma.sync m16n8k16: dQ, dK), "
-                      "gla_dlog_tile_sums/finalize; bf16 hi/lo operand parts"}
+           "kernels": "gla_tc_kernel (the forward and the backward's reversed dV traversal), gla_tc_qk_kernel "
+                      "(dQ, dK): tcgen05.mma kind::f16, fp32 accumulators in tensor memory, bf16 hi/lo operand "
+                      "parts; gla_dlog_tile_sums/tile_suffix/finalize"}
     del t, ws, wb, o, ST, grads
     torch.cuda.empty_cache()
     return res

@@ -23,10 +23,10 @@
 // Q~, K~ and the state are scaled in fp32 and split into bf16 high and low
 // parts, and each product takes the parts that keep the rounding below the
 // outputs' tolerance: Q~ K~^T and Q~ S' as hi.hi + hi.lo + lo.hi, P V and
-// K~^T V as hi + lo (V is an exact bf16 input).  The forward (and the
-// backward's reversed dV traversal) runs its products on tcgen05.mma
-// (kind::f16, fp32 accumulators in tensor memory); the backward's dQ / dK
-// traversal on mma.sync m16n8k16.
+// K~^T V as hi + lo (V is an exact bf16 input).  Every traversal (the
+// forward, the backward's reversed dV traversal and its dQ / dK traversals)
+// runs its products on tcgen05.mma (kind::f16, fp32 accumulators in tensor
+// memory).
 //
 // Chunk parallelism as in chunk_la.cu: a block owns one segment of chunks of
 // one (batch, head) and 64 value columns; phase 1 folds the segment into one
@@ -46,7 +46,6 @@ constexpr float kGlaLog2e = 1.4426950408889634f;
 constexpr int kGlaTc = 64;        // tokens per chunk
 constexpr int kGlaMid = 31;       // reference token of a chunk
 constexpr float kGlaSpan = 120.f; // largest |c_t - c_mid| (log2) the operand scalings allow
-constexpr int kGlaThreads = 256;  // dQ / dK traversal: warp w rows 16(w & 3).. of a chunk, column / token half w >> 2
 constexpr int kGlaSegChoices[4] = {64, 32, 16, 8};
 constexpr long long kGlaMinBlocks = 1024;
 
@@ -610,8 +609,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS) gla_t
 // X Y^T takes exact bf16 inputs (one product); the masked scores and Z~ are
 // split into two bf16 parts (three products), S' too (two products with X).
 // A block owns 64 output columns (key dimensions zb*64..) and the state rows
-// of those dimensions, [64][DV]; warp w holds state rows 16(w & 3).. and half
-// w >> 2 of the state's columns, and takes the scores of token half w >> 2.
+// of those dimensions, [64][DV].
 struct GlaBArgs {
     const bf16 *x, *y, *z;  // x, y: [BH][T][DV]; z: [BH][T][DK]
     const float *g;         // [BH][T][DK] natural-log decays
@@ -628,39 +626,73 @@ struct GlaBArgs {
     float4 *agg, *incl;
 };
 
+// ----------------------------------------------------------------- dQ / dK traversal on tcgen05
+// The traversal of the equations above on the tensor cores, per 64-token chunk, with Z~ = Z (.) 2^(c_m - c) and S' = diag(2^c_m) S (the
+// block's 64 key dimensions; both split into two bf16 parts by the threads):
+//     D    = X Y^T                     (M = 64, N = 64, K = DV)   one product (exact inputs)
+//     O    = X S'^T                    (M = 64, N = 64, K = DV)   two products
+//     U    = Z~^T Y                    (M = 64, N = DV, K = 64)   two products
+//     O   += (D . M) Z~                (A from tensor memory)     three products
+//     OUT  = 2^(c - c_m) (.) O,  S_next = diag(2^(c_L - c_m)) (S' + U)
+// Tiles use the 128-byte swizzle: X, Y K-major ([64 tokens][DV]; Y also the
+// MN-major B of U), Z~ MN-major (B of the last product, A of U), S' K-major
+// ([64 key dimensions][DV]).  8 warps as in gla_tc_kernel: warps w and w + 4
+// read lane quarter w & 3 of tensor memory and split its columns.
 template <int DV>
-struct GlaBCfg {
-    static constexpr int XRB = DV * 2;  // bytes per row of X, Y tiles and of S' (bf16)
-    static constexpr int ZRB = 128;     // 64 key dimensions, bf16
-    static constexpr int GRB = 256;     // 64 key dimensions, fp32
-    static constexpr int X_BYTES = kGlaTc * XRB;
-    static constexpr int Z_BYTES = kGlaTc * ZRB;
-    static constexpr int G_BYTES = kGlaTc * GRB;
+struct GlaQkCfg {
+    static constexpr int KB = DV / 64;             // 64-element blocks along the value dimension
+    static constexpr int XT_BYTES = KB * 64 * 128;  // a [64 tokens][DV] bf16 operand tile
+    static constexpr int Z_BYTES = 64 * 128;        // a [64 tokens][64 key dimensions] bf16 tile
+    static constexpr int G_BYTES = 64 * 64 * 4;     // log decays of the 64 key dimensions
     static constexpr int OFF_X = 0;
-    static constexpr int OFF_Y = X_BYTES;
-    static constexpr int OFF_Z = 2 * X_BYTES;
-    static constexpr int OFF_G = 2 * X_BYTES + Z_BYTES;
-    static constexpr int STAGE = 2 * X_BYTES + Z_BYTES + G_BYTES;
-    static constexpr int OFF_ZLO = 2 * STAGE;
-    static constexpr int OFF_SH = OFF_ZLO + Z_BYTES;  // S' rows (key dimensions) [64][DV], high part
-    static constexpr int OFF_SL = OFF_SH + 64 * XRB;
-    static constexpr int OFF_AS = OFF_SL + 64 * XRB;
-    static constexpr int OFF_XO = OFF_AS + 64 * 4;  // partial outputs exchanged between the token halves
-    static constexpr int SMEM = OFF_XO + 8 * 16 * 32 * 4;
-    static constexpr int S_NT = DV / 8;
+    static constexpr int OFF_Y = XT_BYTES;
+    static constexpr int OFF_Z = 2 * XT_BYTES;
+    static constexpr int OFF_G = 2 * XT_BYTES + Z_BYTES;
+    static constexpr int STAGE = 2 * XT_BYTES + Z_BYTES + G_BYTES;
+    static constexpr int OFF_ZL = 2 * STAGE;             // low part of Z~
+    static constexpr int OFF_SH = OFF_ZL + Z_BYTES;      // S' high part, [64 key dimensions][DV] K-major
+    static constexpr int OFF_SL = OFF_SH + XT_BYTES;
+    static constexpr int OFF_AS = OFF_SL + XT_BYTES;     // alpha of the segment per key dimension [64]
+    static constexpr int OFF_FS = OFF_AS + 64 * 4;       // the final-state dot, per column half [2][64]
+    static constexpr int OFF_BAR = OFF_FS + 2 * 64 * 4;  // two mbarriers
+    static constexpr int SMEM = OFF_BAR + 16 + 1024;     // + alignment slack of the 1024-byte base
+    // tensor memory: D, masked D parts, O, U (DV columns)
+    static constexpr uint32_t C_D = 0, C_DB = 64, C_O = 128, C_U = 192, TMEM_COLS = 512;
+    static constexpr int SC = DV / 4;  // state columns per thread
+    static_assert(STAGE % 1024 == 0 && XT_BYTES % 1024 == 0, "1024-byte aligned operand tiles");
+    static_assert(2 * XT_BYTES >= 64 * 64 * 4, "the output tile fits over a stage's X and Y");
+    static_assert(C_U + DV <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
 template <int DV>
-__global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBArgs p) {
-    using C = GlaBCfg<DV>;
-    extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(kGlaTcThreads, 1) gla_tc_qk_kernel(const GlaBArgs p) {
+    using C = GlaQkCfg<DV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    __shared__ uint32_t s_tmem;
     __shared__ unsigned int s_ticket, s_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, tq = lane & 3;
-    const int wr = warp & 3, hf = warp >> 2;  // row group, column half
-    if (tid == 0) s_ticket = atomicAdd(&p.hdr->ticket[0], 1u);
+    const uint32_t barA = sbase + C::OFF_BAR, barB = barA + 8;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(C::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        tc_fence_before();
+    }
+    if (tid == 0) {
+        mbar_init(barA, 1);
+        mbar_init(barB, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_ticket = atomicAdd(&p.hdr->ticket[0], 1u);
+    }
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const int q = warp & 3, hf = warp >> 2;
+    const uint32_t tlane = (uint32_t)(q * 32) << 16;
     const unsigned int tk = s_ticket;
     const int per_seg = p.BH * p.nzb;
     const int seg = (int)(tk / per_seg);
@@ -670,6 +702,16 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
     const int c_end = min(c_begin + p.seg_chunks, p.n_chunks);
     const int nc = c_end - c_begin;
     const size_t unit = ((size_t)seg * p.BH + bh) * p.nzb + zb;
+    bool timed_out = false;
+    uint32_t phA = 0u, phB = 0u;
+    auto waitA = [&]() {
+        if (!mbar_wait(barA, phA)) timed_out = true;
+        phA ^= 1u;
+    };
+    auto waitB = [&]() {
+        if (!mbar_wait(barB, phB)) timed_out = true;
+        phB ^= 1u;
+    };
 
     const bf16 *Xb = p.x + (size_t)bh * p.T * DV;
     const bf16 *Yb = p.y + (size_t)bh * p.T * DV;
@@ -681,28 +723,29 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
     auto load_stage = [&](int stage, int chunk, bool withX) {
         uint8_t *st = smem + stage * C::STAGE;
         const long long t0 = (long long)chunk * kGlaTc;
-        constexpr int XC = C::XRB / 16;
-        for (int i = tid; i < kGlaTc * XC; i += kGlaThreads) {
+        constexpr int XC = DV / 8;
+        for (int i = tid; i < kGlaTc * XC; i += kGlaTcThreads) {
             const int row = i / XC, c16 = i % XC;
             const long long t = t0 + row;
             const bool ok = t < p.T;
             const size_t off = (size_t)(ok ? arow_of(t) : 0) * DV + c16 * 8;
-            cp_async16(smem_u32(st + C::OFF_Y + swz<C::XRB>(row, c16)), Yb + off, ok ? 16u : 0u);
-            if (withX) cp_async16(smem_u32(st + C::OFF_X + swz<C::XRB>(row, c16)), Xb + off, ok ? 16u : 0u);
+            const uint32_t so = (uint32_t)((c16 >> 3) * 8192) + sw128(row, (c16 & 7) * 8);
+            cp_async16(smem_u32(st + C::OFF_Y) + so, Yb + off, ok ? 16u : 0u);
+            if (withX) cp_async16(smem_u32(st + C::OFF_X) + so, Xb + off, ok ? 16u : 0u);
         }
-        for (int i = tid; i < kGlaTc * 8; i += kGlaThreads) {
+        for (int i = tid; i < kGlaTc * 8; i += kGlaTcThreads) {
             const int row = i >> 3, c16 = i & 7;
             const long long t = t0 + row;
             const bool ok = t < p.T;
-            cp_async16(smem_u32(st + C::OFF_Z + swz<C::ZRB>(row, c16)),
-                       Zb + (size_t)(ok ? arow_of(t) : 0) * p.DK + c16 * 8, ok ? 16u : 0u);
+            cp_async16(smem_u32(st + C::OFF_Z) + sw128(row, c16 * 8), Zb + (size_t)(ok ? arow_of(t) : 0) * p.DK + c16 * 8,
+                       ok ? 16u : 0u);
         }
-        for (int i = tid; i < kGlaTc * 16; i += kGlaThreads) {
+        for (int i = tid; i < kGlaTc * 16; i += kGlaTcThreads) {
             const int row = i >> 4, c16 = i & 15;
             const long long t = t0 + row;
             const bool ok = t < p.T && !(p.rev && t == 0);
             const long long ga = p.rev ? p.T - t : t;
-            cp_async16(smem_u32(st + C::OFF_G + row * C::GRB + c16 * 16), Gb + (size_t)(ok ? ga : 0) * p.DK + c16 * 4,
+            cp_async16(smem_u32(st + C::OFF_G + row * 256 + c16 * 16), Gb + (size_t)(ok ? ga : 0) * p.DK + c16 * 4,
                        ok ? 16u : 0u);
         }
     };
@@ -728,18 +771,18 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
         }
         return total;
     };
-    // Z~ = Z 2^(c_m - c): high part over Z, low part in ZLO
+    // Z~ = Z 2^(c_m - c): high part over Z, low part in ZL
     auto scale_z = [&](int stage) {
         uint8_t *st = smem + stage * C::STAGE;
         const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
-        for (int i = tid; i < kGlaTc * 8; i += kGlaThreads) {
+        for (int i = tid; i < kGlaTc * 8; i += kGlaTcThreads) {
             const int row = i >> 3, c16 = i & 7;
             const float4 *crow = reinterpret_cast<const float4 *>(G + row * 64 + c16 * 8);
             const float4 *cmid = reinterpret_cast<const float4 *>(G + kGlaMid * 64 + c16 * 8);
             const float4 a = crow[0], b = crow[1], ma = cmid[0], mb = cmid[1];
             const float d[8] = {ma.x - a.x, ma.y - a.y, ma.z - a.z, ma.w - a.w,
                                 mb.x - b.x, mb.y - b.y, mb.z - b.z, mb.w - b.w};
-            const uint32_t off = swz<C::ZRB>(row, c16);
+            const uint32_t off = sw128(row, c16 * 8);
             const uint4 zv = *reinterpret_cast<const uint4 *>(st + C::OFF_Z + off);
             const uint32_t w[4] = {zv.x, zv.y, zv.z, zv.w};
             uint32_t hi[4], lo[4];
@@ -749,69 +792,161 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
                 split_bf16x2(make_float2(x.x * ex2(d[2 * e]), x.y * ex2(d[2 * e + 1])), hi[e], lo[e]);
             }
             *reinterpret_cast<uint4 *>(st + C::OFF_Z + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4 *>(smem + C::OFF_ZLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4 *>(smem + C::OFF_ZL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
     };
 
-    // state fragments: local key dimensions 16 (w & 3) + {g, g + 8}, columns in half w >> 2
-    constexpr int S_NT = C::S_NT / 2;
-    float S[S_NT][4];
-    auto s_row = [&](int h) { return wr * 16 + g + h * 8; };  // local key dimension
-    auto s_col = [&](int nj, int e) { return (hf * S_NT + nj) * 8 + tq * 2 + (e & 1); };
-    auto scale_rows_by = [&](const float *G, int a_row, int b_row) {  // rows *= 2^(c[a_row] - c[b_row])
+    // This thread's state: key dimension srow (row of the 64-row accumulator U) and SC columns of
+    // the value half hf, in runs of 16: 64-row layout, paired-half shape.
+    constexpr int SC = C::SC;
+    const int srow = 16 * q + (lane & 15);
+    auto scol = [&](int j) { return (DV / 2) * hf + ((j >> 4) << 5) + 16 * (lane >> 4) + (j & 15); };
+    float S[SC];
+    auto load_u = [&](float (&u)[SC]) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int r = s_row(h);
-            const float f = ex2(G[a_row * 64 + r] - (b_row >= 0 ? G[b_row * 64 + r] : 0.f));
+        for (int g32 = 0; g32 < SC / 16; ++g32) {
+            uint32_t r[16];
+            tmem_ld16x2(tmem + tlane + C::C_U + (uint32_t)((DV / 2) * hf + 32 * g32), r);
+            tmem_ld_wait();
 #pragma unroll
-            for (int nj = 0; nj < S_NT; ++nj) {
-                S[nj][2 * h] *= f;
-                S[nj][2 * h + 1] *= f;
-            }
+            for (int j = 0; j < 16; ++j) u[16 * g32 + j] = __uint_as_float(r[j]);
         }
     };
+    auto state_to_mid = [&](int stage) {
+        const float *G = reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G);
+        const float f = ex2(G[kGlaMid * 64 + srow]);
+#pragma unroll
+        for (int j = 0; j < SC; ++j) S[j] *= f;
+    };
+    // S' as two bf16 parts, K-major [64 key dimensions][DV] (the B operand of X S'^T)
     auto write_sb = [&]() {
 #pragma unroll
-        for (int nj = 0; nj < S_NT; ++nj)
+        for (int j8 = 0; j8 < SC / 8; ++j8) {
+            uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = s_row(h), col = s_col(nj, 0);
-                const uint32_t off = swz<C::XRB>(row, col >> 3) + (col & 7) * 2;
-                uint32_t hi, lo;
-                split_bf16x2(make_float2(S[nj][2 * h], S[nj][2 * h + 1]), hi, lo);
-                *reinterpret_cast<uint32_t *>(smem + C::OFF_SH + off) = hi;
-                *reinterpret_cast<uint32_t *>(smem + C::OFF_SL + off) = lo;
-            }
+            for (int e = 0; e < 4; ++e) split_bf16x2(make_float2(S[8 * j8 + 2 * e], S[8 * j8 + 2 * e + 1]), hi[e], lo[e]);
+            const int col = scol(8 * j8);
+            const uint32_t off = (uint32_t)((col >> 6) * 8192) + sw128(srow, col & 63);
+            *reinterpret_cast<uint4 *>(smem + C::OFF_SH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(smem + C::OFF_SL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
     };
-    // S' + Z~^T Y (Z~ in two parts), then rows scaled by 2^(c_L - c_m)
-    auto state_update = [&](int stage) {
-        const uint8_t *st = smem + stage * C::STAGE;
+    auto state_finish = [&](int stage) {
+        const float *G = reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G);
+        const float f = ex2(G[(kGlaTc - 1) * 64 + srow] - G[kGlaMid * 64 + srow]);
+        float u[SC];
+        load_u(u);
 #pragma unroll
-        for (int kt = 0; kt < kGlaTc / 16; ++kt) {
-            const int arow = kt * 16 + (lane & 7) + (lane >> 4) * 8;
-            const int ac16 = 2 * wr + ((lane >> 3) & 1);
-            uint32_t ah[4], al[4];
-            ldsm_x4_t(smem_u32(st + C::OFF_Z + swz<C::ZRB>(arow, ac16)), ah);
-            ldsm_x4_t(smem_u32(smem + C::OFF_ZLO + swz<C::ZRB>(arow, ac16)), al);
+        for (int j = 0; j < SC; ++j) S[j] = f * (S[j] + u[j]);
+    };
+
+    // ---- descriptors
+    auto kdesc = [&](uint32_t off) { return smem_desc(sbase + off, 16, 1024); };     // K-major
+    auto mndesc = [&](uint32_t off) { return smem_desc(sbase + off, 8192, 1024); };  // MN-major
+    auto kstep_k = [&](int kk) { return (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4); };
+    auto kstep_mn = [&](int kk) { return (uint64_t)((kk * 2048) >> 4); };
+    constexpr uint32_t id_d = idesc_bf16(64, 64, 0, 0);   // D = X Y^T
+    constexpr uint32_t id_o = idesc_bf16(64, 64, 0, 0);   // O = X S'^T (S' K-major)
+    constexpr uint32_t id_u = idesc_bf16(64, DV, 1, 1);   // U = Z~^T Y
+    constexpr uint32_t id_i = idesc_bf16(64, 64, 0, 1);   // O += (D . M) Z~
+    auto issue_u = [&](int stage) {
+        const uint32_t so = (uint32_t)(stage * C::STAGE);
+        const uint64_t b0 = mndesc(so + C::OFF_Y);
 #pragma unroll
-            for (int pp = 0; pp < S_NT / 2; ++pp) {
-                uint32_t b[4];
-                const int brow = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                ldsm_x4_t(smem_u32(st + C::OFF_Y + swz<C::XRB>(brow, 2 * (hf * S_NT / 2 + pp) + (lane >> 4))), b);
-                mma16816(S[2 * pp], ah, b[0], b[1]);
-                mma16816(S[2 * pp + 1], ah, b[2], b[3]);
-                mma16816(S[2 * pp], al, b[0], b[1]);
-                mma16816(S[2 * pp + 1], al, b[2], b[3]);
+        for (int part = 0; part < 2; ++part) {
+            const uint64_t a0 = mndesc(part ? C::OFF_ZL : so + C::OFF_Z);
+#pragma unroll
+            for (int kk = 0; kk < kGlaTc / 16; ++kk)
+                mma_ss_w(tmem + C::C_U, a0 + kstep_mn(kk), b0 + kstep_mn(kk), id_u, (part | kk) ? 1u : 0u);
+        }
+    };
+    auto issue_d_o = [&](int stage) {
+        const uint32_t so = (uint32_t)(stage * C::STAGE);
+        const uint64_t a0 = kdesc(so + C::OFF_X), by = kdesc(so + C::OFF_Y);
+        const uint64_t sh = kdesc(C::OFF_SH), sl = kdesc(C::OFF_SL);
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk) {
+            mma_ss_w(tmem + C::C_D, a0 + kstep_k(kk), by + kstep_k(kk), id_d, kk ? 1u : 0u);
+            mma_ss_w(tmem + C::C_O, a0 + kstep_k(kk), sh + kstep_k(kk), id_o, kk ? 1u : 0u);
+            mma_ss_w(tmem + C::C_O, a0 + kstep_k(kk), sl + kstep_k(kk), id_o, 1u);
+        }
+    };
+    // O += (D . M)_hi Z~_hi + (D . M)_hi Z~_lo + (D . M)_lo Z~_hi
+    auto issue_intra = [&](int stage) {
+        const uint64_t zh = mndesc((uint32_t)(stage * C::STAGE) + C::OFF_Z), zl = mndesc(C::OFF_ZL);
+#pragma unroll
+        for (int part = 0; part < 3; ++part) {
+            const int apart = (part == 2) ? 1 : 0;
+            const uint64_t b0 = (part == 1) ? zl : zh;
+#pragma unroll
+            for (int kk = 0; kk < kGlaTc / 16; ++kk) {
+                const uint32_t acol = C::C_DB + (uint32_t)(kk >> 1) * 32 + apart * 16 + (kk & 1) * 8;
+                mma_ts_w(tmem + C::C_O, tmem + acol, b0 + kstep_mn(kk), id_i, 1u);
             }
         }
-        scale_rows_by(reinterpret_cast<const float *>(st + C::OFF_G), kGlaTc - 1, kGlaMid);
+    };
+    auto mask_d = [&]() {
+        const int r = 16 * q + (lane & 15);
+        const int s0 = hf * 32;
+        uint32_t pr[16];
+        tmem_ld16x2(tmem + tlane + C::C_D + (uint32_t)s0, pr);
+        tmem_ld_wait();
+        const int sb = s0 + 16 * (lane >> 4);
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int s = sb + 2 * j;
+            float2 v = make_float2(__uint_as_float(pr[2 * j]), __uint_as_float(pr[2 * j + 1]));
+            if (s > r) v.x = 0.f;
+            if (s + 1 > r) v.y = 0.f;
+            split_bf16x2(v, hi[j], lo[j]);
+        }
+        tmem_st8x2(tmem + tlane + C::C_DB + (uint32_t)s0, hi);
+        tmem_st8x2(tmem + tlane + C::C_DB + (uint32_t)(s0 + 16), lo);
+        tmem_st_wait();
+    };
+    // OUT = 2^(c_r - c_m) O per (token r, key dimension), staged over the stage's X and Y (dead
+    // once the products have run; 16-byte chunks XOR-ed with the row), written a row per warp
+    auto write_out = [&](int stage, long long t0) {
+        const float *G = reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G);
+        float *ot = reinterpret_cast<float *>(smem + stage * C::STAGE + C::OFF_X);
+        {
+            const int r = 16 * q + (lane & 15), c0 = 32 * hf + 16 * (lane >> 4);
+            uint32_t o[16];
+            tmem_ld16x2(tmem + tlane + C::C_O + (uint32_t)(32 * hf), o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const int col = c0 + 4 * c4;
+                const float4 cr = *reinterpret_cast<const float4 *>(G + r * 64 + col);
+                const float4 cm = *reinterpret_cast<const float4 *>(G + kGlaMid * 64 + col);
+                const int ch = ((c0 >> 2) + c4) ^ (r & 15);
+                *reinterpret_cast<float4 *>(ot + r * 64 + ch * 4) =
+                    make_float4(__uint_as_float(o[4 * c4]) * ex2(cr.x - cm.x), __uint_as_float(o[4 * c4 + 1]) * ex2(cr.y - cm.y),
+                                __uint_as_float(o[4 * c4 + 2]) * ex2(cr.z - cm.z), __uint_as_float(o[4 * c4 + 3]) * ex2(cr.w - cm.w));
+            }
+        }
+        __syncthreads();
+        for (int idx = tid; idx < kGlaTc * 32; idx += kGlaTcThreads) {
+            const int r = idx >> 5, c2 = idx & 31;
+            const long long t = t0 + r;
+            if (t < p.T) {
+                const int ch = (c2 >> 1) ^ (r & 15);
+                const float2 v = *reinterpret_cast<const float2 *>(ot + r * 64 + ch * 4 + (c2 & 1) * 2);
+                *reinterpret_cast<float2 *>(p.out + ((size_t)bh * p.T + arow_of(t)) * p.DK + zb * 64 + 2 * c2) = v;
+            }
+        }
+    };
+    auto hand_to_tc = [&]() {
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
     };
 
     // ------------------------------------------------ phase 1
 #pragma unroll
-    for (int nj = 0; nj < S_NT; ++nj)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) S[nj][e] = 0.f;
+    for (int j = 0; j < SC; ++j) S[j] = 0.f;
     float la_seg = 0.f;
     load_stage(0, c_begin, false);
     cp_async_commit();
@@ -824,9 +959,16 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
         la_seg += cumulate(stage);
         __syncthreads();
         scale_z(stage);
-        scale_rows_by(reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G), kGlaMid, -1);
-        __syncthreads();
-        state_update(stage);
+        state_to_mid(stage);
+        hand_to_tc();
+        if (warp == 0) {
+            issue_u(stage);
+            mma_commit_w(barA);
+        }
+        waitA();
+        tc_fence_after();
+        state_finish(stage);
+        tc_fence_before();
         __syncthreads();
         if (i + 2 < nc) load_stage(stage, c_begin + i + 2, false);
         cp_async_commit();
@@ -835,69 +977,64 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
     __syncthreads();
 
     // ------------------------------------------------ look-back
-    auto ws_index = [&](size_t u, int tile) { return u * (size_t)(S_NT * kGlaThreads) + (size_t)tile * kGlaThreads + tid; };
-    float Sin[S_NT][4];
+    constexpr int TILES = SC / 4;
+    auto ws_index = [&](size_t u, int tile) {
+        return u * (size_t)(TILES * kGlaTcThreads) + (size_t)tile * kGlaTcThreads + tid;
+    };
+    float Sin[SC];
 #pragma unroll
-    for (int nj = 0; nj < S_NT; ++nj)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) Sin[nj][e] = 0.f;
-    auto add_state0 = [&](float s0, float s1) {
+    for (int j = 0; j < SC; ++j) Sin[j] = 0.f;
+    auto add_state0 = [&](float scale) {
         if (p.S0 == nullptr) return;
 #pragma unroll
-        for (int nj = 0; nj < S_NT; ++nj)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int row = zb * 64 + s_row(e >> 1);
-                Sin[nj][e] = fmaf((e >> 1) ? s1 : s0, __ldg(p.S0 + ((size_t)bh * p.DK + row) * DV + s_col(nj, e)),
-                                  Sin[nj][e]);
-            }
+        for (int j = 0; j < SC; ++j)
+            Sin[j] = fmaf(scale, __ldg(p.S0 + ((size_t)bh * p.DK + zb * 64 + srow) * DV + scol(j)), Sin[j]);
     };
     if (tid < 64) alpha_s[tid] = ex2(la_seg);
     if (seg == 0) {
-        add_state0(1.f, 1.f);
+        add_state0(1.f);
     } else {
 #pragma unroll
-        for (int nj = 0; nj < S_NT; ++nj)
-            __stcg(p.agg + ws_index(unit, nj), make_float4(S[nj][0], S[nj][1], S[nj][2], S[nj][3]));
+        for (int tl = 0; tl < TILES; ++tl)
+            __stcg(p.agg + ws_index(unit, tl), make_float4(S[4 * tl], S[4 * tl + 1], S[4 * tl + 2], S[4 * tl + 3]));
         if (tid < 64) __stcg(p.alpha + unit * 64 + tid, ex2(la_seg));
         __threadfence();
         __syncthreads();
         if (tid == 0) st_release(p.flags + unit, 1u);
-        float acc0 = 1.f, acc1 = 1.f;
+        float accA = 1.f;
         int j = seg - 1;
         while (true) {
             const size_t up = ((size_t)j * p.BH + bh) * p.nzb + zb;
-            if (tid == 0) s_flag = wait_flag(p.flags + up, p.hdr, 61u);
+            if (tid == 0) s_flag = wait_flag(p.flags + up, p.hdr, 64u);
             __syncthreads();
             const unsigned int f = s_flag;
             __syncthreads();
             if (f != 1u && f != 2u) break;
             const float4 *src = (f == 2u) ? p.incl : p.agg;
 #pragma unroll
-            for (int nj = 0; nj < S_NT; ++nj) {
-                const float4 v = ld_cg4(src + ws_index(up, nj));
-                Sin[nj][0] = fmaf(acc0, v.x, Sin[nj][0]);
-                Sin[nj][1] = fmaf(acc0, v.y, Sin[nj][1]);
-                Sin[nj][2] = fmaf(acc1, v.z, Sin[nj][2]);
-                Sin[nj][3] = fmaf(acc1, v.w, Sin[nj][3]);
+            for (int tl = 0; tl < TILES; ++tl) {
+                const float4 v = ld_cg4(src + ws_index(up, tl));
+                Sin[4 * tl] = fmaf(accA, v.x, Sin[4 * tl]);
+                Sin[4 * tl + 1] = fmaf(accA, v.y, Sin[4 * tl + 1]);
+                Sin[4 * tl + 2] = fmaf(accA, v.z, Sin[4 * tl + 2]);
+                Sin[4 * tl + 3] = fmaf(accA, v.w, Sin[4 * tl + 3]);
             }
             if (f == 2u) break;
-            acc0 *= ld_cg(p.alpha + up * 64 + s_row(0));
-            acc1 *= ld_cg(p.alpha + up * 64 + s_row(1));
+            accA *= ld_cg(p.alpha + up * 64 + srow);
             if (--j < 0) {
-                add_state0(acc0, acc1);
+                add_state0(accA);
                 break;
             }
         }
     }
     __syncthreads();
     if (seg != p.n_seg - 1) {
-        const float a0 = alpha_s[s_row(0)], a1 = alpha_s[s_row(1)];
+        const float a = alpha_s[srow];
 #pragma unroll
-        for (int nj = 0; nj < S_NT; ++nj)
-            __stcg(p.incl + ws_index(unit, nj),
-                   make_float4(fmaf(a0, Sin[nj][0], S[nj][0]), fmaf(a0, Sin[nj][1], S[nj][1]),
-                               fmaf(a1, Sin[nj][2], S[nj][2]), fmaf(a1, Sin[nj][3], S[nj][3])));
+        for (int tl = 0; tl < TILES; ++tl)
+            __stcg(p.incl + ws_index(unit, tl),
+                   make_float4(fmaf(a, Sin[4 * tl], S[4 * tl]), fmaf(a, Sin[4 * tl + 1], S[4 * tl + 1]),
+                               fmaf(a, Sin[4 * tl + 2], S[4 * tl + 2]), fmaf(a, Sin[4 * tl + 3], S[4 * tl + 3])));
         __threadfence();
         __syncthreads();
         if (tid == 0) st_release(p.flags + unit, 2u);
@@ -905,160 +1042,70 @@ __global__ void __launch_bounds__(kGlaThreads, 1) gla_bwd_qk_kernel(const GlaBAr
 
     // ------------------------------------------------ phase 2
 #pragma unroll
-    for (int nj = 0; nj < S_NT; ++nj)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) S[nj][e] = Sin[nj][e];
+    for (int j = 0; j < SC; ++j) S[j] = Sin[j];
     load_stage(0, c_begin, true);
     cp_async_commit();
     if (nc > 1) load_stage(1, c_begin + 1, true);
     cp_async_commit();
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
-        const uint8_t *st = smem + stage * C::STAGE;
-        const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
         const long long t0 = (long long)(c_begin + i) * kGlaTc;
         cp_async_wait<1>();
         __syncthreads();
         cumulate(stage);
         __syncthreads();
         scale_z(stage);
-        scale_rows_by(G, kGlaMid, -1);
+        state_to_mid(stage);
         write_sb();
+        hand_to_tc();
+        if (warp == 0) {
+            issue_d_o(stage);
+            issue_u(stage);
+            mma_commit_w(barA);
+        }
+        waitA();
+        tc_fence_after();
+        mask_d();
+        tc_fence_before();
         __syncthreads();
-
-        // D = X Y^T for this warp's 16 rows and its half of the chunk's tokens (s in 32 hf ..;
-        // exact bf16 inputs: one product), causal mask, then (D . M) Z~ over those tokens for
-        // all 64 output columns (three products); a half after every row of the group is skipped
-        const int arow = wr * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        float O[8][4];
-#pragma unroll
-        for (int nj = 0; nj < 8; ++nj)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) O[nj][e] = 0.f;
-        if (32 * hf <= wr * 16 + 15) {
-            float D[4][4];
-#pragma unroll
-            for (int nj = 0; nj < 4; ++nj)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) D[nj][e] = 0.f;
-#pragma unroll 2
-            for (int kk = 0; kk < DV / 16; ++kk) {
-                uint32_t a[4];
-                ldsm_x4(smem_u32(st + C::OFF_X + swz<C::XRB>(arow, 2 * kk + (lane >> 4))), a);
-#pragma unroll
-                for (int p2 = 0; p2 < 2; ++p2) {
-                    uint32_t b[4];
-                    const int brow = 16 * (2 * hf + p2) + (lane & 7) + (lane >> 4) * 8;
-                    ldsm_x4(smem_u32(st + C::OFF_Y + swz<C::XRB>(brow, 2 * kk + ((lane >> 3) & 1))), b);
-                    mma16816(D[2 * p2], a, b[0], b[1]);
-                    mma16816(D[2 * p2 + 1], a, b[2], b[3]);
-                }
-            }
-            uint32_t dh[2][4], dl[2][4];
-#pragma unroll
-            for (int nj = 0; nj < 4; ++nj)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int r = wr * 16 + g + 8 * h, s = (4 * hf + nj) * 8 + 2 * tq;
-                    const float x0 = (s <= r) ? D[nj][2 * h] : 0.f;
-                    const float x1 = (s + 1 <= r) ? D[nj][2 * h + 1] : 0.f;
-                    split_bf16x2(make_float2(x0, x1), dh[nj >> 1][(nj & 1) * 2 + h], dl[nj >> 1][(nj & 1) * 2 + h]);
-                }
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
-#pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
-                    const int brow = (2 * hf + kt) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const uint32_t boff = swz<C::ZRB>(brow, 2 * pp + (lane >> 4));
-                    uint32_t zh[4], zl[4];
-                    ldsm_x4_t(smem_u32(st + C::OFF_Z + boff), zh);
-                    ldsm_x4_t(smem_u32(smem + C::OFF_ZLO + boff), zl);
-                    mma16816(O[2 * pp], dh[kt], zh[0], zh[1]);
-                    mma16816(O[2 * pp + 1], dh[kt], zh[2], zh[3]);
-                    mma16816(O[2 * pp], dh[kt], zl[0], zl[1]);
-                    mma16816(O[2 * pp + 1], dh[kt], zl[2], zl[3]);
-                    mma16816(O[2 * pp], dl[kt], zh[0], zh[1]);
-                    mma16816(O[2 * pp + 1], dl[kt], zh[2], zh[3]);
-                }
-            }
+        tc_fence_after();
+        if (warp == 0) {
+            issue_intra(stage);
+            mma_commit_w(barB);
         }
-        // the other column half of the partial output goes to the partner warp (w ^ 4)
-        float *xo = reinterpret_cast<float *>(smem + C::OFF_XO);  // [8 warps][16 rows][32 columns]
-#pragma unroll
-        for (int nj = 0; nj < 4; ++nj)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-                *reinterpret_cast<float2 *>(xo + (warp * 16 + g + 8 * h) * 32 + nj * 8 + 2 * tq) =
-                    hf ? make_float2(O[nj][2 * h], O[nj][2 * h + 1])
-                       : make_float2(O[4 + nj][2 * h], O[4 + nj][2 * h + 1]);
-        // ... + X S'^T for this warp's column half (two products: S' in two parts)
-        float Oh[4][4];
-#pragma unroll
-        for (int nj = 0; nj < 4; ++nj)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) Oh[nj][e] = hf ? O[4 + nj][e] : O[nj][e];
-#pragma unroll 2
-        for (int kk = 0; kk < DV / 16; ++kk) {
-            uint32_t a[4];
-            ldsm_x4(smem_u32(st + C::OFF_X + swz<C::XRB>(arow, 2 * kk + (lane >> 4))), a);
-#pragma unroll
-            for (int p2 = 0; p2 < 2; ++p2) {
-                const int brow = 16 * (2 * hf + p2) + (lane & 7) + (lane >> 4) * 8;
-                const uint32_t boff = swz<C::XRB>(brow, 2 * kk + ((lane >> 3) & 1));
-                uint32_t sh[4], sl[4];
-                ldsm_x4(smem_u32(smem + C::OFF_SH + boff), sh);
-                ldsm_x4(smem_u32(smem + C::OFF_SL + boff), sl);
-                mma16816(Oh[2 * p2], a, sh[0], sh[1]);
-                mma16816(Oh[2 * p2 + 1], a, sh[2], sh[3]);
-                mma16816(Oh[2 * p2], a, sl[0], sl[1]);
-                mma16816(Oh[2 * p2 + 1], a, sl[2], sl[3]);
-            }
-        }
-        __syncthreads();  // the partner's partial output is in shared memory
-        // OUT = 2^(c_r - c_m) per (row, key dimension)
-#pragma unroll
-        for (int nj = 0; nj < 4; ++nj)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = wr * 16 + g + 8 * h, col = (4 * hf + nj) * 8 + 2 * tq;
-                const long long t = t0 + r;
-                const float2 x = *reinterpret_cast<const float2 *>(xo + ((warp ^ 4) * 16 + g + 8 * h) * 32 + nj * 8 + 2 * tq);
-                if (t < p.T) {
-                    const float2 cr = *reinterpret_cast<const float2 *>(G + r * 64 + col);
-                    const float2 cm = *reinterpret_cast<const float2 *>(G + kGlaMid * 64 + col);
-                    *reinterpret_cast<float2 *>(p.out + ((size_t)bh * p.T + arow_of(t)) * p.DK + zb * 64 + col) =
-                        make_float2((Oh[nj][2 * h] + x.x) * ex2(cr.x - cm.x), (Oh[nj][2 * h + 1] + x.y) * ex2(cr.y - cm.y));
-                }
-            }
-        state_update(stage);
+        state_finish(stage);
+        waitB();
+        tc_fence_after();
+        write_out(stage, t0);
+        tc_fence_before();
         __syncthreads();
         if (i + 2 < nc) load_stage(stage, c_begin + i + 2, true);
         cp_async_commit();
     }
     cp_async_wait<0>();
 
-    // the final state's rows dotted with fs_dot (the decay gradient's final-state term), the
-    // two column halves summed through shared memory
+    // the final state's rows dotted with fs_dot (the decay gradient's final-state term): the
+    // paired halves of a warp, then the two column halves, summed through shared memory
     if (seg == p.n_seg - 1 && p.fs_part != nullptr) {
-        float *fsx = reinterpret_cast<float *>(smem + C::OFF_XO);  // [2 halves][64 rows]
+        float *fsx = reinterpret_cast<float *>(smem + C::OFF_FS);
+        float acc = 0.f;
+        if (p.fs_dot != nullptr) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int row = zb * 64 + s_row(h);
-            float acc = 0.f;
-            if (p.fs_dot != nullptr) {
-#pragma unroll
-                for (int nj = 0; nj < S_NT; ++nj)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        acc = fmaf(S[nj][2 * h + e], __ldg(p.fs_dot + ((size_t)bh * p.DK + row) * DV + s_col(nj, e)), acc);
-            }
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            if (tq == 0) fsx[hf * 64 + s_row(h)] = acc;
+            for (int j = 0; j < SC; ++j)
+                acc = fmaf(S[j], __ldg(p.fs_dot + ((size_t)bh * p.DK + zb * 64 + srow) * DV + scol(j)), acc);
         }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+        if (lane < 16) fsx[hf * 64 + srow] = acc;
         __syncthreads();
         if (tid < 64) p.fs_part[(size_t)bh * p.DK + zb * 64 + tid] = fsx[tid] + fsx[64 + tid];
     }
+    if (timed_out) {
+        atomicOr(&p.hdr->error, kErrTimeout);
+        atomicExch(&p.hdr->where, 65u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
 }
 
 // ----------------------------------------------------------------- backward: decay gradient
@@ -1216,12 +1263,12 @@ bool gla_bwd_supported(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, 
 
 template <int DV>
 int launch_gla_bwd_qk(const GlaBArgs &a, cudaStream_t s, unsigned int grid) {
-    using C = GlaBCfg<DV>;
+    using C = GlaQkCfg<DV>;
     static std::atomic<unsigned long long> smem_set{0};
-    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_bwd_qk_kernel<DV>), C::SMEM);
+    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_tc_qk_kernel<DV>), C::SMEM);
     if (st) return st;
-    gla_bwd_qk_kernel<DV><<<grid, kGlaThreads, C::SMEM, s>>>(a);
-    return check_launch("gla_bwd_qk_kernel");
+    gla_tc_qk_kernel<DV><<<grid, kGlaTcThreads, C::SMEM, s>>>(a);
+    return check_launch("gla_tc_qk_kernel");
 }
 
 template <int DK>
