@@ -937,35 +937,6 @@ __global__ void __launch_bounds__(kBlockThreads, TcCfg<DX, TC>::MIN_BLOCKS)
 }
 
 // ----------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    // looked up once, on first use (a function-local static: thread-safe)
-    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
-    }();
-    return fn;
-}
-
-// 3-D map over a [BH][T][cols] array with 128-byte-swizzled boxes of 128-byte rows:
-// {64, rows, 1} for bf16 operands, {32, rows, 1} for the fp32 output.
-bool make_map(CUtensorMap *m, const void *base, int cols, long long T, int BH, int rows, bool bf16 = true) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    const size_t es = bf16 ? 2 : 4;
-    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)T, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)cols * es, (cuuint64_t)cols * es * (cuuint64_t)T};
-    cuuint32_t box[3] = {bf16 ? 64u : 32u, (cuuint32_t)rows, 1u};
-    cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <int DX, int TC, bool REV>
 int launch_tc_variant(const LaArgs &a, cudaStream_t s, unsigned int grid) {
     using C = TcCfg<DX, TC>;

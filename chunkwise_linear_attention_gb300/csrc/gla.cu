@@ -109,8 +109,8 @@ struct GlaTcCfg {
     static constexpr int OFF_SH = OFF_KL + QT_BYTES;    // S' high part, [DK rows][64 columns] MN-major
     static constexpr int OFF_SL = OFF_SH + DK * 128;
     static constexpr int OFF_AS = OFF_SL + DK * 128;    // alpha of the segment per key dimension
-    static constexpr int OFF_BAR = OFF_AS + DK * 4;     // two mbarriers
-    static constexpr int SMEM = OFF_BAR + 16 + 1024;    // + alignment slack of the 1024-byte base
+    static constexpr int OFF_BAR = OFF_AS + DK * 4;     // four mbarriers: two products, two stage loads
+    static constexpr int SMEM = OFF_BAR + 32 + 1024;    // + alignment slack of the 1024-byte base
     static constexpr int MIN_BLOCKS = (2 * (SMEM + 1024) <= 228 * 1024) ? 2 : 1;
     // tensor memory: scores, masked score parts, output, state product
     static constexpr uint32_t C_P = 0, C_PB = 64, C_O = 128, C_U = 192, TMEM_COLS = 256;
@@ -122,8 +122,19 @@ struct GlaTcCfg {
 
 constexpr int kGlaTcThreads = 256;
 
-template <int DK>
-__global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS) gla_tc_kernel(const GlaArgs p) {
+// Tensor maps of the forward traversal's operands ([BH][T][cols] arrays): q, k and v in
+// 128-byte-swizzled boxes of 64 tokens x 64 columns (bf16), log decays in plain boxes of
+// 64 tokens x d_k (fp32).  Rows past T read as zeros (log a = 0 for the padding tokens).
+struct GlaMaps {
+    CUtensorMap q, k, v, g;
+};
+
+// TMA: the stages are filled by the tensor memory accelerator (forward traversal only; one
+// thread issues, completion on a per-stage mbarrier); otherwise by cp.async from every thread
+// (the reversed traversal reads its rows in reverse order, which a tile copy cannot).
+template <int DK, bool TMA>
+__global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
+    gla_tc_kernel(const GlaArgs p, const __grid_constant__ GlaMaps maps) {
     using C = GlaTcCfg<DK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -131,7 +142,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS) gla_t
     __shared__ uint32_t s_tmem;
     __shared__ unsigned int s_ticket, s_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t barA = sbase + C::OFF_BAR, barB = barA + 8;
+    const uint32_t barA = sbase + C::OFF_BAR, barB = barA + 8, barL = barA + 16;  // barL + 8 stage
 
     // tensor memory first (before taking a ticket, so every ticket holder owns its columns)
     if (warp == 0) {
@@ -143,6 +154,8 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS) gla_t
     if (tid == 0) {
         mbar_init(barA, 1);
         mbar_init(barB, 1);
+        mbar_init(barL, 1);
+        mbar_init(barL + 8, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_ticket = atomicAdd(&p.hdr->ticket[0], 1u);
     }
@@ -170,6 +183,16 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS) gla_t
         if (!mbar_wait(barB, phB)) timed_out = true;
         phB ^= 1u;
     };
+    uint32_t phL = 0u;  // bit s: parity of stage s's next load
+    auto stage_ready = [&](int stage) {
+        if constexpr (TMA) {
+            if (!mbar_wait(barL + 8u * (uint32_t)stage, (phL >> stage) & 1u)) timed_out = true;
+            phL ^= 1u << stage;
+        } else {
+            cp_async_wait<1>();
+            __syncthreads();
+        }
+    };
 
     const bf16 *Qb = p.q + (size_t)bh * p.T * DK;
     const bf16 *Kb = p.k + (size_t)bh * p.T * DK;
@@ -183,6 +206,21 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS) gla_t
     auto load_stage = [&](int stage, int chunk, bool withQ) {
         uint8_t *st = smem + stage * C::STAGE;
         const long long t0 = (long long)chunk * kGlaTc;
+        if constexpr (TMA) {
+            if (tid == 0) {
+                const uint32_t bar = barL + 8u * (uint32_t)stage, s0 = smem_u32(st);
+                mbar_expect_tx(bar, (uint32_t)((withQ ? 2 : 1) * C::QT_BYTES + C::V_BYTES + C::G_BYTES));
+                const int y = (int)t0;
+#pragma unroll
+                for (int kb = 0; kb < C::KB; ++kb) {
+                    tma_load_3d(s0 + C::OFF_K + kb * 8192, &maps.k, kb * 64, y, bh, bar);
+                    if (withQ) tma_load_3d(s0 + C::OFF_Q + kb * 8192, &maps.q, kb * 64, y, bh, bar);
+                }
+                tma_load_3d(s0 + C::OFF_V, &maps.v, zb * 64, y, bh, bar);
+                tma_load_3d(s0 + C::OFF_G, &maps.g, 0, y, bh, bar);
+            }
+            return;
+        }
         constexpr int QC = DK / 8;  // 16-byte chunks of a Q / K row
         for (int i = tid; i < kGlaTc * QC; i += kGlaTcThreads) {
             const int row = i / QC, c16 = i % QC;
@@ -451,8 +489,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS) gla_t
     cp_async_commit();
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
-        cp_async_wait<1>();
-        __syncthreads();
+        stage_ready(stage);
         la_seg += cumulate(stage);
         __syncthreads();
         scale_operands(stage, false);
@@ -465,6 +502,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS) gla_t
         waitA();
         tc_fence_after();
         state_finish(stage);
+        if constexpr (TMA) fence_async_smem();  // this thread's writes to the stage before its reload
         tc_fence_before();
         __syncthreads();  // the stage and the state product are consumed
         if (i + 2 < nc) load_stage(stage, c_begin + i + 2, false);
@@ -548,8 +586,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS) gla_t
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
         const long long t0 = (long long)(c_begin + i) * kGlaTc;
-        cp_async_wait<1>();
-        __syncthreads();
+        stage_ready(stage);
         cumulate(stage);
         __syncthreads();
         scale_operands(stage, true);
@@ -575,6 +612,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS) gla_t
         waitB();
         tc_fence_after();
         write_out(stage, t0);
+        if constexpr (TMA) fence_async_smem();
         tc_fence_before();
         __syncthreads();  // the stage and the accumulators are consumed
         if (i + 2 < nc) load_stage(stage, c_begin + i + 2, true);
@@ -1271,14 +1309,27 @@ int launch_gla_bwd_qk(const GlaBArgs &a, cudaStream_t s, unsigned int grid) {
     return check_launch("gla_tc_qk_kernel");
 }
 
+template <int DK, bool TMA>
+int launch_gla_fwd_variant(const GlaArgs &a, const GlaMaps &maps, cudaStream_t s, unsigned int grid) {
+    using C = GlaTcCfg<DK>;
+    static std::atomic<unsigned long long> smem_set{0};  // per template instance
+    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_tc_kernel<DK, TMA>), C::SMEM);
+    if (st) return st;
+    gla_tc_kernel<DK, TMA><<<grid, kGlaTcThreads, C::SMEM, s>>>(a, maps);
+    return check_launch("gla_tc_kernel");
+}
+
+// The forward traversal loads its stages by TMA; the reversed one by cp.async.
 template <int DK>
 int launch_gla_fwd(const GlaArgs &a, cudaStream_t s, unsigned int grid) {
-    using C = GlaTcCfg<DK>;
-    static std::atomic<unsigned long long> smem_set{0};
-    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_tc_kernel<DK>), C::SMEM);
-    if (st) return st;
-    gla_tc_kernel<DK><<<grid, kGlaTcThreads, C::SMEM, s>>>(a);
-    return check_launch("gla_tc_kernel");
+    GlaMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (a.rev) return launch_gla_fwd_variant<DK, false>(a, maps, s, grid);
+    const bool ok = make_map(&maps.q, a.q, DK, a.T, a.BH, kGlaTc) && make_map(&maps.k, a.k, DK, a.T, a.BH, kGlaTc) &&
+                    make_map(&maps.v, a.v, a.DV, a.T, a.BH, kGlaTc) &&
+                    make_map_f32_rows(&maps.g, a.g, DK, a.T, a.BH, kGlaTc);
+    if (!ok) return fail(CLA_ERR_CUDA, "gla_tc_kernel: tensor map encoding failed");
+    return launch_gla_fwd_variant<DK, true>(a, maps, s, grid);
 }
 
 }  // namespace

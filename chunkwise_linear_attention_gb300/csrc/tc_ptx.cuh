@@ -2,10 +2,13 @@
 // by the tcgen05 kernels (chunk_la_tc.cuh, gla.cu): mbarriers with bounded
 // waits, TMA tile loads and stores, tcgen05.mma on descriptors of
 // 128-byte-swizzled shared-memory operands (or an A operand in tensor memory),
-// tensor-memory loads and stores, and the swizzled tile addressing.
+// tensor-memory loads and stores, the swizzled tile addressing, and the host
+// side's tensor-map encoding.
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace cla {
@@ -166,6 +169,51 @@ __device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
     asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]), "r"(r[1]),
                  "r"(r[2]), "r"(r[3])
                  : "memory");
+}
+
+// ----------------------------------------------------------------- host side: tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    // looked up once, on first use (a function-local static: thread-safe)
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
+    return fn;
+}
+
+// 3-D map over a [BH][T][cols] array with 128-byte-swizzled boxes of 128-byte rows:
+// {64, rows, 1} for bf16 operands, {32, rows, 1} for the fp32 output.
+bool make_map(CUtensorMap *m, const void *base, int cols, long long T, int BH, int rows, bool bf16 = true) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const size_t es = bf16 ? 2 : 4;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * es, (cuuint64_t)cols * es * (cuuint64_t)T};
+    cuuint32_t box[3] = {bf16 ? 64u : 32u, (cuuint32_t)rows, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 3-D map over a [BH][T][cols] fp32 array with plain (unswizzled) boxes {cols, rows, 1}: whole
+// rows of up to 256 elements, landing row-major in shared memory.
+bool make_map_f32_rows(CUtensorMap *m, const void *base, int cols, long long T, int BH, int rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc || cols > 256 || rows > 256) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 4u, (cuuint64_t)cols * 4u * (cuuint64_t)T};
+    cuuint32_t box[3] = {(cuuint32_t)cols, (cuuint32_t)rows, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 }  // namespace
