@@ -692,8 +692,8 @@ struct GlaQkCfg {
     static constexpr int OFF_SL = OFF_SH + XT_BYTES;
     static constexpr int OFF_AS = OFF_SL + XT_BYTES;     // alpha of the segment per key dimension [64]
     static constexpr int OFF_FS = OFF_AS + 64 * 4;       // the final-state dot, per column half [2][64]
-    static constexpr int OFF_BAR = OFF_FS + 2 * 64 * 4;  // two mbarriers
-    static constexpr int SMEM = OFF_BAR + 16 + 1024;     // + alignment slack of the 1024-byte base
+    static constexpr int OFF_BAR = OFF_FS + 2 * 64 * 4;  // four mbarriers: two products, two stage loads
+    static constexpr int SMEM = OFF_BAR + 32 + 1024;     // + alignment slack of the 1024-byte base
     // tensor memory: D, masked D parts, O, U (DV columns)
     static constexpr uint32_t C_D = 0, C_DB = 64, C_O = 128, C_U = 192, TMEM_COLS = 512;
     static constexpr int SC = DV / 4;  // state columns per thread
@@ -703,8 +703,18 @@ struct GlaQkCfg {
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-template <int DV>
-__global__ void __launch_bounds__(kGlaTcThreads, 1) gla_tc_qk_kernel(const GlaBArgs p) {
+// Tensor maps of the forward traversal's operands: X and Y ([BH][T][DV] bf16) and Z ([BH][T][d_k]
+// bf16, a 64-column box) in 128-byte-swizzled boxes of 64 tokens x 64 columns, the log decays
+// ([BH][T][d_k] fp32) in plain boxes of 64 tokens x 64 dimensions.
+struct GlaQkMaps {
+    CUtensorMap x, y, z, g;
+};
+
+// TMA: stages filled by the tensor memory accelerator (forward traversal: dQ); otherwise by
+// cp.async from every thread (the reversed dK traversal).
+template <int DV, bool TMA>
+__global__ void __launch_bounds__(kGlaTcThreads, 1)
+    gla_tc_qk_kernel(const GlaBArgs p, const __grid_constant__ GlaQkMaps maps) {
     using C = GlaQkCfg<DV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -712,7 +722,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1) gla_tc_qk_kernel(const GlaBA
     __shared__ uint32_t s_tmem;
     __shared__ unsigned int s_ticket, s_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t barA = sbase + C::OFF_BAR, barB = barA + 8;
+    const uint32_t barA = sbase + C::OFF_BAR, barB = barA + 8, barL = barA + 16;  // barL + 8 stage
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
@@ -723,6 +733,8 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1) gla_tc_qk_kernel(const GlaBA
     if (tid == 0) {
         mbar_init(barA, 1);
         mbar_init(barB, 1);
+        mbar_init(barL, 1);
+        mbar_init(barL + 8, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_ticket = atomicAdd(&p.hdr->ticket[0], 1u);
     }
@@ -750,6 +762,16 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1) gla_tc_qk_kernel(const GlaBA
         if (!mbar_wait(barB, phB)) timed_out = true;
         phB ^= 1u;
     };
+    uint32_t phL = 0u;  // bit s: parity of stage s's next load
+    auto stage_ready = [&](int stage) {
+        if constexpr (TMA) {
+            if (!mbar_wait(barL + 8u * (uint32_t)stage, (phL >> stage) & 1u)) timed_out = true;
+            phL ^= 1u << stage;
+        } else {
+            cp_async_wait<1>();
+            __syncthreads();
+        }
+    };
 
     const bf16 *Xb = p.x + (size_t)bh * p.T * DV;
     const bf16 *Yb = p.y + (size_t)bh * p.T * DV;
@@ -761,6 +783,21 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1) gla_tc_qk_kernel(const GlaBA
     auto load_stage = [&](int stage, int chunk, bool withX) {
         uint8_t *st = smem + stage * C::STAGE;
         const long long t0 = (long long)chunk * kGlaTc;
+        if constexpr (TMA) {
+            if (tid == 0) {
+                const uint32_t bar = barL + 8u * (uint32_t)stage, s0 = smem_u32(st);
+                mbar_expect_tx(bar, (uint32_t)((withX ? 2 : 1) * C::XT_BYTES + C::Z_BYTES + C::G_BYTES));
+                const int y = (int)t0;
+#pragma unroll
+                for (int kb = 0; kb < C::KB; ++kb) {
+                    tma_load_3d(s0 + C::OFF_Y + kb * 8192, &maps.y, kb * 64, y, bh, bar);
+                    if (withX) tma_load_3d(s0 + C::OFF_X + kb * 8192, &maps.x, kb * 64, y, bh, bar);
+                }
+                tma_load_3d(s0 + C::OFF_Z, &maps.z, zb * 64, y, bh, bar);
+                tma_load_3d(s0 + C::OFF_G, &maps.g, zb * 64, y, bh, bar);
+            }
+            return;
+        }
         constexpr int XC = DV / 8;
         for (int i = tid; i < kGlaTc * XC; i += kGlaTcThreads) {
             const int row = i / XC, c16 = i % XC;
@@ -992,8 +1029,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1) gla_tc_qk_kernel(const GlaBA
     cp_async_commit();
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
-        cp_async_wait<1>();
-        __syncthreads();
+        stage_ready(stage);
         la_seg += cumulate(stage);
         __syncthreads();
         scale_z(stage);
@@ -1006,6 +1042,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1) gla_tc_qk_kernel(const GlaBA
         waitA();
         tc_fence_after();
         state_finish(stage);
+        if constexpr (TMA) fence_async_smem();  // this thread's writes to the stage before its reload
         tc_fence_before();
         __syncthreads();
         if (i + 2 < nc) load_stage(stage, c_begin + i + 2, false);
@@ -1088,8 +1125,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1) gla_tc_qk_kernel(const GlaBA
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
         const long long t0 = (long long)(c_begin + i) * kGlaTc;
-        cp_async_wait<1>();
-        __syncthreads();
+        stage_ready(stage);
         cumulate(stage);
         __syncthreads();
         scale_z(stage);
@@ -1115,6 +1151,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1) gla_tc_qk_kernel(const GlaBA
         waitB();
         tc_fence_after();
         write_out(stage, t0);
+        if constexpr (TMA) fence_async_smem();
         tc_fence_before();
         __syncthreads();
         if (i + 2 < nc) load_stage(stage, c_begin + i + 2, true);
@@ -1299,14 +1336,28 @@ bool gla_bwd_supported(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, 
            gla_sizes_fit(B, H, T) && product_below({B, H, (T + kGlaDlTile - 1) / kGlaDlTile}, 2147483648.0);
 }
 
+template <int DV, bool TMA>
+int launch_gla_bwd_qk_variant(const GlaBArgs &a, const GlaQkMaps &maps, cudaStream_t s, unsigned int grid) {
+    using C = GlaQkCfg<DV>;
+    static std::atomic<unsigned long long> smem_set{0};  // per template instance
+    const int st =
+        set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_tc_qk_kernel<DV, TMA>), C::SMEM);
+    if (st) return st;
+    gla_tc_qk_kernel<DV, TMA><<<grid, kGlaTcThreads, C::SMEM, s>>>(a, maps);
+    return check_launch("gla_tc_qk_kernel");
+}
+
+// The forward traversal (dQ) loads its stages by TMA; the reversed one (dK) by cp.async.
 template <int DV>
 int launch_gla_bwd_qk(const GlaBArgs &a, cudaStream_t s, unsigned int grid) {
-    using C = GlaQkCfg<DV>;
-    static std::atomic<unsigned long long> smem_set{0};
-    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_tc_qk_kernel<DV>), C::SMEM);
-    if (st) return st;
-    gla_tc_qk_kernel<DV><<<grid, kGlaTcThreads, C::SMEM, s>>>(a);
-    return check_launch("gla_tc_qk_kernel");
+    GlaQkMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (a.rev) return launch_gla_bwd_qk_variant<DV, false>(a, maps, s, grid);
+    const bool ok = make_map(&maps.x, a.x, DV, a.T, a.BH, kGlaTc) && make_map(&maps.y, a.y, DV, a.T, a.BH, kGlaTc) &&
+                    make_map(&maps.z, a.z, a.DK, a.T, a.BH, kGlaTc) &&
+                    make_map_f32_rows(&maps.g, a.g, a.DK, a.T, a.BH, kGlaTc, 64);
+    if (!ok) return fail(CLA_ERR_CUDA, "gla_tc_qk_kernel: tensor map encoding failed");
+    return launch_gla_bwd_qk_variant<DV, true>(a, maps, s, grid);
 }
 
 template <int DK, bool TMA>
@@ -1327,7 +1378,7 @@ int launch_gla_fwd(const GlaArgs &a, cudaStream_t s, unsigned int grid) {
     if (a.rev) return launch_gla_fwd_variant<DK, false>(a, maps, s, grid);
     const bool ok = make_map(&maps.q, a.q, DK, a.T, a.BH, kGlaTc) && make_map(&maps.k, a.k, DK, a.T, a.BH, kGlaTc) &&
                     make_map(&maps.v, a.v, a.DV, a.T, a.BH, kGlaTc) &&
-                    make_map_f32_rows(&maps.g, a.g, DK, a.T, a.BH, kGlaTc);
+                    make_map_f32_rows(&maps.g, a.g, DK, a.T, a.BH, kGlaTc, DK);
     if (!ok) return fail(CLA_ERR_CUDA, "gla_tc_kernel: tensor map encoding failed");
     return launch_gla_fwd_variant<DK, true>(a, maps, s, grid);
 }

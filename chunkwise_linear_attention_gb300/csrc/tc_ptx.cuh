@@ -201,14 +201,14 @@ bool make_map(CUtensorMap *m, const void *base, int cols, long long T, int BH, i
     return r == CUDA_SUCCESS;
 }
 
-// 3-D map over a [BH][T][cols] fp32 array with plain (unswizzled) boxes {cols, rows, 1}: whole
-// rows of up to 256 elements, landing row-major in shared memory.
-bool make_map_f32_rows(CUtensorMap *m, const void *base, int cols, long long T, int BH, int rows) {
+// 3-D map over a [BH][T][cols] fp32 array with plain (unswizzled) boxes {box_cols, rows, 1}
+// (box_cols <= 256, a multiple of 4), landing row-major in shared memory.
+bool make_map_f32_rows(CUtensorMap *m, const void *base, int cols, long long T, int BH, int rows, int box_cols) {
     auto enc = tensor_map_encoder();
-    if (!enc || cols > 256 || rows > 256) return false;
+    if (!enc || box_cols > 256 || box_cols % 4 != 0 || rows > 256) return false;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)T, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)cols * 4u, (cuuint64_t)cols * 4u * (cuuint64_t)T};
-    cuuint32_t box[3] = {(cuuint32_t)cols, (cuuint32_t)rows, 1u};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)rows, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
