@@ -817,11 +817,12 @@ int launch_pass(int DX, int TC, bool REV, const LaArgs &a, cudaStream_t s, unsig
     return fail(CLA_ERR_UNSUPPORTED, "chunk_la: no kernel for head dim %d and chunk %d", DX, TC);
 }
 
-// Non-negative sizes the kernels and the plan handle: B*H <= 2^24, T <= 2^34,
-// B*H*T <= 2^40 (so no workspace offset can overflow) and every grid, at
+// Non-negative sizes the kernels and the plan handle: B*H <= 2^24, T < 2^31 (the
+// tensor-map loads take 32-bit token coordinates; one head that long would not
+// fit device memory anyway), B*H*T <= 2^40 (so no workspace offset can overflow) and every grid, at
 // most one block per chunk and 64 columns of 128, below 2^31 blocks.
 bool la_sizes_fit(int64_t B, int64_t H, int64_t T, int chunk) {
-    if (!product_below({B, H}, 16777217.0) || T > (1ll << 34)) return false;
+    if (!product_below({B, H}, 16777217.0) || T > kMaxTokens) return false;
     if (!product_below({B, H, T}, 1099511627777.0)) return false;
     const int64_t n_chunks = (T + chunk - 1) / chunk, fin_tiles = (T + kFinTile - 1) / kFinTile;
     return product_below({B, H, n_chunks, 2}, 2147483648.0) && product_below({B, H, fin_tiles}, 2147483648.0);

@@ -61,6 +61,10 @@ constexpr unsigned int kErrRange = 2u;
 // about a second before a block gives up, far beyond any legitimate wait.
 constexpr unsigned int kSpinLimit = 1u << 23;
 
+// Longest sequence of the tensor-core paths: their tensor-map loads take 32-bit token
+// coordinates, which also reach one chunk before the first token and one past the last.
+constexpr long long kMaxTokens = (1ll << 31) - 512;
+
 // ----------------------------------------------------------------- device side
 __device__ __forceinline__ unsigned int ld_acquire(const unsigned int *p) {
     unsigned int v;

@@ -89,6 +89,13 @@ struct GlaArgs {
 // the 64-row accumulators keep row 16q + i in lane 32q + i (i < 16), the DK-row
 // one (DK = 128) row r in lane r.
 //
+// Stages are filled by TMA (one thread issues, completion on a per-stage
+// mbarrier; rows past the ends of the arrays read as zeros).  A tile copy keeps
+// the array order of rows, so in the reversed traversal (token t' is array token
+// T-1-t') row j of a stage holds traversal position 63 - j: the in-chunk sums run
+// from the last row up, the midpoint and the chunk's end sit at rows 63 - m and
+// 0, and the causal mask keeps the rows at and below the diagonal row.
+//
 // Segments and look-back as before: phase 1 folds the segment's chunks into
 // (diag(alpha_seg), dS_seg) from a zero state, decoupled look-back gives the
 // incoming state, phase 2 runs the chunks from it and writes O.
@@ -122,17 +129,14 @@ struct GlaTcCfg {
 
 constexpr int kGlaTcThreads = 256;
 
-// Tensor maps of the forward traversal's operands ([BH][T][cols] arrays): q, k and v in
+// Tensor maps of a traversal's operands ([BH][T][cols] arrays): q, k and v in
 // 128-byte-swizzled boxes of 64 tokens x 64 columns (bf16), log decays in plain boxes of
 // 64 tokens x d_k (fp32).  Rows past T read as zeros (log a = 0 for the padding tokens).
 struct GlaMaps {
     CUtensorMap q, k, v, g;
 };
 
-// TMA: the stages are filled by the tensor memory accelerator (forward traversal only; one
-// thread issues, completion on a per-stage mbarrier); otherwise by cp.async from every thread
-// (the reversed traversal reads its rows in reverse order, which a tile copy cannot).
-template <int DK, bool TMA>
+template <int DK, bool REV>
 __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
     gla_tc_kernel(const GlaArgs p, const __grid_constant__ GlaMaps maps) {
     using C = GlaTcCfg<DK>;
@@ -185,88 +189,59 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
     };
     uint32_t phL = 0u;  // bit s: parity of stage s's next load
     auto stage_ready = [&](int stage) {
-        if constexpr (TMA) {
-            if (!mbar_wait(barL + 8u * (uint32_t)stage, (phL >> stage) & 1u)) timed_out = true;
-            phL ^= 1u << stage;
-        } else {
-            cp_async_wait<1>();
-            __syncthreads();
-        }
+        if (!mbar_wait(barL + 8u * (uint32_t)stage, (phL >> stage) & 1u)) timed_out = true;
+        phL ^= 1u << stage;
     };
+    // stage rows of the chunk's midpoint token and of its last token
+    constexpr int MID = REV ? kGlaTc - 1 - kGlaMid : kGlaMid;
+    constexpr int LAST = REV ? 0 : kGlaTc - 1;
 
-    const bf16 *Qb = p.q + (size_t)bh * p.T * DK;
-    const bf16 *Kb = p.k + (size_t)bh * p.T * DK;
-    const bf16 *Vb = p.v + (size_t)bh * p.T * p.DV + zb * 64;
     const float *Gb = p.g + (size_t)bh * p.T * DK;
     float *alpha_s = reinterpret_cast<float *>(smem + C::OFF_AS);
 
-    // array row of traversal token t (reversed: T-1-t), and of its decay (reversed: T-t, none at 0)
-    auto arow_of = [&](long long t) { return p.rev ? p.T - 1 - t : t; };
-    // Q, K into their K-major swizzled operand positions, V into its MN-major one, G plain.
-    auto load_stage = [&](int stage, int chunk, bool withQ) {
-        uint8_t *st = smem + stage * C::STAGE;
-        const long long t0 = (long long)chunk * kGlaTc;
-        if constexpr (TMA) {
-            if (tid == 0) {
-                const uint32_t bar = barL + 8u * (uint32_t)stage, s0 = smem_u32(st);
-                mbar_expect_tx(bar, (uint32_t)((withQ ? 2 : 1) * C::QT_BYTES + C::V_BYTES + C::G_BYTES));
-                const int y = (int)t0;
-#pragma unroll
-                for (int kb = 0; kb < C::KB; ++kb) {
-                    tma_load_3d(s0 + C::OFF_K + kb * 8192, &maps.k, kb * 64, y, bh, bar);
-                    if (withQ) tma_load_3d(s0 + C::OFF_Q + kb * 8192, &maps.q, kb * 64, y, bh, bar);
-                }
-                tma_load_3d(s0 + C::OFF_V, &maps.v, zb * 64, y, bh, bar);
-                tma_load_3d(s0 + C::OFF_G, &maps.g, 0, y, bh, bar);
-            }
-            return;
-        }
-        constexpr int QC = DK / 8;  // 16-byte chunks of a Q / K row
-        for (int i = tid; i < kGlaTc * QC; i += kGlaTcThreads) {
-            const int row = i / QC, c16 = i % QC;
-            const long long t = t0 + row;
-            const bool ok = t < p.T;
-            const size_t off = (size_t)(ok ? arow_of(t) : 0) * DK + c16 * 8;
-            const uint32_t so = (uint32_t)((c16 >> 3) * 8192) + sw128(row, (c16 & 7) * 8);
-            cp_async16(smem_u32(st + C::OFF_K) + so, Kb + off, ok ? 16u : 0u);
-            if (withQ) cp_async16(smem_u32(st + C::OFF_Q) + so, Qb + off, ok ? 16u : 0u);
-        }
-        for (int i = tid; i < kGlaTc * 8; i += kGlaTcThreads) {
-            const int row = i >> 3, c16 = i & 7;
-            const long long t = t0 + row;
-            const bool ok = t < p.T;
-            cp_async16(smem_u32(st + C::OFF_V) + sw128(row, c16 * 8), Vb + (size_t)(ok ? arow_of(t) : 0) * p.DV + c16 * 8,
-                       ok ? 16u : 0u);
-        }
-        constexpr int GC = DK / 4;
-        for (int i = tid; i < kGlaTc * GC; i += kGlaTcThreads) {  // padding tokens: log a = 0
-            const int row = i / GC, c16 = i % GC;
-            const long long t = t0 + row;
-            const bool ok = t < p.T && !(p.rev && t == 0);
-            const long long ga = p.rev ? p.T - t : t;
-            cp_async16(smem_u32(st + C::OFF_G + row * DK * 4 + c16 * 16), Gb + (size_t)(ok ? ga : 0) * DK + c16 * 4,
-                       ok ? 16u : 0u);
-        }
+    // array row of a chunk's stage row 0: the chunk's first token, or (reversed) the array
+    // token of its last traversal position (negative in a ragged last chunk)
+    auto row0_of = [&](int chunk) {
+        return REV ? p.T - (long long)kGlaTc * (chunk + 1) : (long long)kGlaTc * chunk;
     };
-
-    // In-chunk cumulative log2 decays, in place (thread i < DK scans dimension i), with the
-    // range check; returns (to thread i) the chunk's total c_L[i].
-    auto cumulate = [&](int stage) {
+    // Q, K into their K-major swizzled operand positions, V into its MN-major one, G plain.  The
+    // reversed traversal's decay of position t' is array token T - t' (none for t' = 0: the
+    // row past the end reads as zero): its G tile starts one row later.
+    auto load_stage = [&](int stage, int chunk, bool withQ) {
+        if (tid != 0) return;
+        const uint32_t bar = barL + 8u * (uint32_t)stage, s0 = smem_u32(smem + stage * C::STAGE);
+        mbar_expect_tx(bar, (uint32_t)((withQ ? 2 : 1) * C::QT_BYTES + C::V_BYTES + C::G_BYTES));
+        const int y = (int)row0_of(chunk);
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb) {
+            tma_load_3d(s0 + C::OFF_K + kb * 8192, &maps.k, kb * 64, y, bh, bar);
+            if (withQ) tma_load_3d(s0 + C::OFF_Q + kb * 8192, &maps.q, kb * 64, y, bh, bar);
+        }
+        tma_load_3d(s0 + C::OFF_V, &maps.v, zb * 64, y, bh, bar);
+        tma_load_3d(s0 + C::OFF_G, &maps.g, 0, REV ? y + 1 : y, bh, bar);
+    };
+    // In-chunk cumulative log2 decays, in place (thread i < DK scans dimension i in traversal
+    // order), with the range check; returns (to thread i) the chunk's total c_L[i].  Positions
+    // past the sequence's end decay by nothing (the reversed traversal's first one past the end
+    // would otherwise read a_0's row).
+    auto cumulate = [&](int stage, int chunk) {
         float *G = reinterpret_cast<float *>(smem + stage * C::STAGE + C::OFF_G);
         float total = 0.f;
         if (tid < DK) {
+            const long long n_tok = p.T - (long long)kGlaTc * chunk;  // positions below are tokens
             float run = 0.f, lo = 0.f, hi = 0.f;
             bool finite = true;
 #pragma unroll 8
             for (int t = 0; t < kGlaTc; ++t) {
-                const float l = G[t * DK + tid];
+                const int row = REV ? kGlaTc - 1 - t : t;
+                const float l = (REV && t >= n_tok) ? 0.f : G[row * DK + tid];
                 finite = finite && isfinite(l);
                 run += l * kGlaLog2e;
-                G[t * DK + tid] = run;
+                G[row * DK + tid] = run;
                 lo = fminf(lo, run);
                 hi = fmaxf(hi, run);
             }
-            const float cm = G[kGlaMid * DK + tid];
+            const float cm = G[MID * DK + tid];
             // the running sum starts at 0 before token 0: include it in the span as well
             if (!finite || hi - cm > kGlaSpan || cm - lo > kGlaSpan || cm > kGlaSpan)
                 atomicOr(&p.hdr->error, kErrRange);
@@ -283,7 +258,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
         for (int i = tid; i < kGlaTc * QC; i += kGlaTcThreads) {
             const int row = i / QC, c16 = i % QC;
             const float4 *crow = reinterpret_cast<const float4 *>(G + row * DK + c16 * 8);
-            const float4 *cmid = reinterpret_cast<const float4 *>(G + kGlaMid * DK + c16 * 8);
+            const float4 *cmid = reinterpret_cast<const float4 *>(G + MID * DK + c16 * 8);
             float d[8];
             {
                 const float4 a = crow[0], b = crow[1], ma = cmid[0], mb = cmid[1];
@@ -338,7 +313,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
     // S' = diag(2^c_m) S in place, and its two bf16 parts into the MN-major B tile [DK][64]
     auto state_to_mid = [&](int stage) {
         const float *G = reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G);
-        const float f = ex2(G[kGlaMid * DK + srow]);
+        const float f = ex2(G[MID * DK + srow]);
 #pragma unroll
         for (int j = 0; j < SC; ++j) S[j] *= f;
     };
@@ -356,7 +331,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
     // S_next = diag(2^(c_L - c_m)) (S' + U)
     auto state_finish = [&](int stage) {
         const float *G = reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G);
-        const float f = ex2(G[(kGlaTc - 1) * DK + srow] - G[kGlaMid * DK + srow]);
+        const float f = ex2(G[LAST * DK + srow] - G[MID * DK + srow]);
         float u[SC];
         load_u(u);
 #pragma unroll
@@ -414,9 +389,9 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
             }
     };
 
-    // Causal mask of the scores (token s <= row r), split into two bf16 parts as the A operand of
-    // P V: row r = 16 q + (lane & 15), the 32-token piece hf; threads 0..15 take tokens s0..,
-    // 16..31 tokens s0 + 16..
+    // Causal mask of the scores (stage rows s <= r; reversed, s >= r), split into two bf16 parts as
+    // the A operand of P V: row r = 16 q + (lane & 15), the 32-token piece hf; threads 0..15 take
+    // tokens s0.., 16..31 tokens s0 + 16..
     auto mask_scores = [&]() {
         const int r = 16 * q + (lane & 15);
         {
@@ -430,8 +405,8 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
             for (int j = 0; j < 8; ++j) {
                 const int s = sb + 2 * j;
                 float2 v = make_float2(__uint_as_float(pr[2 * j]), __uint_as_float(pr[2 * j + 1]));
-                if (s > r) v.x = 0.f;
-                if (s + 1 > r) v.y = 0.f;
+                if (REV ? s < r : s > r) v.x = 0.f;
+                if (REV ? s + 1 < r : s + 1 > r) v.y = 0.f;
                 split_bf16x2(v, hi[j], lo[j]);
             }
             // high parts of tokens s0.. at columns s0.., of s0 + 16.. at s0 + 8..; low parts 16 further
@@ -444,7 +419,8 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
     // + 0..15) into a [64][64] fp32 staging tile over the stage's Q~ / K~ high parts (dead once
     // the products have run; 16-byte chunks XOR-ed with the row), then whole rows to global
     // memory (a warp stores one row per instruction)
-    auto write_out = [&](int stage, long long t0) {
+    auto write_out = [&](int stage, int chunk) {
+        const long long r0 = row0_of(chunk);
         float *ot = reinterpret_cast<float *>(smem + stage * C::STAGE + C::OFF_Q);
         {
             const int r = 16 * q + (lane & 15), c0 = 32 * hf + 16 * (lane >> 4);
@@ -462,11 +438,11 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
         __syncthreads();
         for (int idx = tid; idx < kGlaTc * 32; idx += kGlaTcThreads) {
             const int r = idx >> 5, c2 = idx & 31;
-            const long long t = t0 + r;
-            if (t < p.T) {
+            const long long t = r0 + r;  // array row
+            if (t >= 0 && t < p.T) {
                 const int ch = (c2 >> 1) ^ (r & 15);
                 const float2 v = *reinterpret_cast<const float2 *>(ot + r * 64 + ch * 4 + (c2 & 1) * 2);
-                *reinterpret_cast<float2 *>(p.o + ((size_t)bh * p.T + arow_of(t)) * p.DV + zb * 64 + 2 * c2) = v;
+                *reinterpret_cast<float2 *>(p.o + ((size_t)bh * p.T + t) * p.DV + zb * 64 + 2 * c2) = v;
             }
         }
     };
@@ -484,13 +460,11 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
     for (int j = 0; j < SC; ++j) S[j] = 0.f;
     float la_seg = 0.f;  // thread i < DK: log2 of alpha_seg[i]
     load_stage(0, c_begin, false);
-    cp_async_commit();
     if (nc > 1) load_stage(1, c_begin + 1, false);
-    cp_async_commit();
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
         stage_ready(stage);
-        la_seg += cumulate(stage);
+        la_seg += cumulate(stage, c_begin + i);
         __syncthreads();
         scale_operands(stage, false);
         state_to_mid(stage);
@@ -502,14 +476,11 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
         waitA();
         tc_fence_after();
         state_finish(stage);
-        if constexpr (TMA) fence_async_smem();  // this thread's writes to the stage before its reload
+        fence_async_smem();  // this thread's writes to the stage before its reload
         tc_fence_before();
         __syncthreads();  // the stage and the state product are consumed
         if (i + 2 < nc) load_stage(stage, c_begin + i + 2, false);
-        cp_async_commit();
     }
-    cp_async_wait<0>();
-    __syncthreads();
 
     // ------------------------------------------------ look-back for the incoming state
     constexpr int TILES = SC / 4;
@@ -580,14 +551,11 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
 #pragma unroll
     for (int j = 0; j < SC; ++j) S[j] = Sin[j];
     load_stage(0, c_begin, true);
-    cp_async_commit();
     if (nc > 1) load_stage(1, c_begin + 1, true);
-    cp_async_commit();
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
-        const long long t0 = (long long)(c_begin + i) * kGlaTc;
         stage_ready(stage);
-        cumulate(stage);
+        cumulate(stage, c_begin + i);
         __syncthreads();
         scale_operands(stage, true);
         state_to_mid(stage);
@@ -611,18 +579,16 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
         state_finish(stage);
         waitB();
         tc_fence_after();
-        write_out(stage, t0);
-        if constexpr (TMA) fence_async_smem();
+        write_out(stage, c_begin + i);
+        fence_async_smem();
         tc_fence_before();
         __syncthreads();  // the stage and the accumulators are consumed
         if (i + 2 < nc) load_stage(stage, c_begin + i + 2, true);
-        cp_async_commit();
     }
-    cp_async_wait<0>();
 
     if (seg == p.n_seg - 1 && p.ST != nullptr) {
         // reversed: the state before token 0 of the arrays, decayed by a_0
-        const float f = p.rev ? __expf(__ldg(Gb + srow)) : 1.f;
+        const float f = REV ? __expf(__ldg(Gb + srow)) : 1.f;
 #pragma unroll
         for (int j = 0; j < SC; ++j) p.ST[((size_t)bh * DK + srow) * p.DV + zb * 64 + scol(j)] = f * S[j];
     }
@@ -703,16 +669,16 @@ struct GlaQkCfg {
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-// Tensor maps of the forward traversal's operands: X and Y ([BH][T][DV] bf16) and Z ([BH][T][d_k]
+// Tensor maps of the traversal operands: X and Y ([BH][T][DV] bf16) and Z ([BH][T][d_k]
 // bf16, a 64-column box) in 128-byte-swizzled boxes of 64 tokens x 64 columns, the log decays
 // ([BH][T][d_k] fp32) in plain boxes of 64 tokens x 64 dimensions.
 struct GlaQkMaps {
     CUtensorMap x, y, z, g;
 };
 
-// TMA: stages filled by the tensor memory accelerator (forward traversal: dQ); otherwise by
-// cp.async from every thread (the reversed dK traversal).
-template <int DV, bool TMA>
+// Stages filled by TMA as in gla_tc_kernel; REV (the dK traversal): row j of a stage holds
+// traversal position 63 - j.
+template <int DV, bool REV>
 __global__ void __launch_bounds__(kGlaTcThreads, 1)
     gla_tc_qk_kernel(const GlaBArgs p, const __grid_constant__ GlaQkMaps maps) {
     using C = GlaQkCfg<DV>;
@@ -764,82 +730,51 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
     };
     uint32_t phL = 0u;  // bit s: parity of stage s's next load
     auto stage_ready = [&](int stage) {
-        if constexpr (TMA) {
-            if (!mbar_wait(barL + 8u * (uint32_t)stage, (phL >> stage) & 1u)) timed_out = true;
-            phL ^= 1u << stage;
-        } else {
-            cp_async_wait<1>();
-            __syncthreads();
-        }
+        if (!mbar_wait(barL + 8u * (uint32_t)stage, (phL >> stage) & 1u)) timed_out = true;
+        phL ^= 1u << stage;
     };
-
-    const bf16 *Xb = p.x + (size_t)bh * p.T * DV;
-    const bf16 *Yb = p.y + (size_t)bh * p.T * DV;
-    const bf16 *Zb = p.z + (size_t)bh * p.T * p.DK + zb * 64;
-    const float *Gb = p.g + (size_t)bh * p.T * p.DK + zb * 64;
+    // stage rows of the chunk's midpoint token and of its last token
+    constexpr int MID = REV ? kGlaTc - 1 - kGlaMid : kGlaMid;
+    constexpr int LAST = REV ? 0 : kGlaTc - 1;
     float *alpha_s = reinterpret_cast<float *>(smem + C::OFF_AS);
 
-    auto arow_of = [&](long long t) { return p.rev ? p.T - 1 - t : t; };
-    auto load_stage = [&](int stage, int chunk, bool withX) {
-        uint8_t *st = smem + stage * C::STAGE;
-        const long long t0 = (long long)chunk * kGlaTc;
-        if constexpr (TMA) {
-            if (tid == 0) {
-                const uint32_t bar = barL + 8u * (uint32_t)stage, s0 = smem_u32(st);
-                mbar_expect_tx(bar, (uint32_t)((withX ? 2 : 1) * C::XT_BYTES + C::Z_BYTES + C::G_BYTES));
-                const int y = (int)t0;
-#pragma unroll
-                for (int kb = 0; kb < C::KB; ++kb) {
-                    tma_load_3d(s0 + C::OFF_Y + kb * 8192, &maps.y, kb * 64, y, bh, bar);
-                    if (withX) tma_load_3d(s0 + C::OFF_X + kb * 8192, &maps.x, kb * 64, y, bh, bar);
-                }
-                tma_load_3d(s0 + C::OFF_Z, &maps.z, zb * 64, y, bh, bar);
-                tma_load_3d(s0 + C::OFF_G, &maps.g, zb * 64, y, bh, bar);
-            }
-            return;
-        }
-        constexpr int XC = DV / 8;
-        for (int i = tid; i < kGlaTc * XC; i += kGlaTcThreads) {
-            const int row = i / XC, c16 = i % XC;
-            const long long t = t0 + row;
-            const bool ok = t < p.T;
-            const size_t off = (size_t)(ok ? arow_of(t) : 0) * DV + c16 * 8;
-            const uint32_t so = (uint32_t)((c16 >> 3) * 8192) + sw128(row, (c16 & 7) * 8);
-            cp_async16(smem_u32(st + C::OFF_Y) + so, Yb + off, ok ? 16u : 0u);
-            if (withX) cp_async16(smem_u32(st + C::OFF_X) + so, Xb + off, ok ? 16u : 0u);
-        }
-        for (int i = tid; i < kGlaTc * 8; i += kGlaTcThreads) {
-            const int row = i >> 3, c16 = i & 7;
-            const long long t = t0 + row;
-            const bool ok = t < p.T;
-            cp_async16(smem_u32(st + C::OFF_Z) + sw128(row, c16 * 8), Zb + (size_t)(ok ? arow_of(t) : 0) * p.DK + c16 * 8,
-                       ok ? 16u : 0u);
-        }
-        for (int i = tid; i < kGlaTc * 16; i += kGlaTcThreads) {
-            const int row = i >> 4, c16 = i & 15;
-            const long long t = t0 + row;
-            const bool ok = t < p.T && !(p.rev && t == 0);
-            const long long ga = p.rev ? p.T - t : t;
-            cp_async16(smem_u32(st + C::OFF_G + row * 256 + c16 * 16), Gb + (size_t)(ok ? ga : 0) * p.DK + c16 * 4,
-                       ok ? 16u : 0u);
-        }
+    // array row of a chunk's stage row 0 (reversed: of its last traversal position)
+    auto row0_of = [&](int chunk) {
+        return REV ? p.T - (long long)kGlaTc * (chunk + 1) : (long long)kGlaTc * chunk;
     };
-    auto cumulate = [&](int stage) {
+    // the reversed traversal's decay of position t' is array token T - t': its G tile starts a row later
+    auto load_stage = [&](int stage, int chunk, bool withX) {
+        if (tid != 0) return;
+        const uint32_t bar = barL + 8u * (uint32_t)stage, s0 = smem_u32(smem + stage * C::STAGE);
+        mbar_expect_tx(bar, (uint32_t)((withX ? 2 : 1) * C::XT_BYTES + C::Z_BYTES + C::G_BYTES));
+        const int y = (int)row0_of(chunk);
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb) {
+            tma_load_3d(s0 + C::OFF_Y + kb * 8192, &maps.y, kb * 64, y, bh, bar);
+            if (withX) tma_load_3d(s0 + C::OFF_X + kb * 8192, &maps.x, kb * 64, y, bh, bar);
+        }
+        tma_load_3d(s0 + C::OFF_Z, &maps.z, zb * 64, y, bh, bar);
+        tma_load_3d(s0 + C::OFF_G, &maps.g, zb * 64, REV ? y + 1 : y, bh, bar);
+    };
+    // in-chunk cumulative log2 decays in traversal order (positions past the end decay by nothing)
+    auto cumulate = [&](int stage, int chunk) {
         float *G = reinterpret_cast<float *>(smem + stage * C::STAGE + C::OFF_G);
         float total = 0.f;
         if (tid < 64) {
+            const long long n_tok = p.T - (long long)kGlaTc * chunk;
             float run = 0.f, lo = 0.f, hi = 0.f;
             bool finite = true;
 #pragma unroll 8
             for (int t = 0; t < kGlaTc; ++t) {
-                const float l = G[t * 64 + tid];
+                const int row = REV ? kGlaTc - 1 - t : t;
+                const float l = (REV && t >= n_tok) ? 0.f : G[row * 64 + tid];
                 finite = finite && isfinite(l);
                 run += l * kGlaLog2e;
-                G[t * 64 + tid] = run;
+                G[row * 64 + tid] = run;
                 lo = fminf(lo, run);
                 hi = fmaxf(hi, run);
             }
-            const float cm = G[kGlaMid * 64 + tid];
+            const float cm = G[MID * 64 + tid];
             if (!finite || hi - cm > kGlaSpan || cm - lo > kGlaSpan || cm > kGlaSpan)
                 atomicOr(&p.hdr->error, kErrRange);
             total = run;
@@ -853,7 +788,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
         for (int i = tid; i < kGlaTc * 8; i += kGlaTcThreads) {
             const int row = i >> 3, c16 = i & 7;
             const float4 *crow = reinterpret_cast<const float4 *>(G + row * 64 + c16 * 8);
-            const float4 *cmid = reinterpret_cast<const float4 *>(G + kGlaMid * 64 + c16 * 8);
+            const float4 *cmid = reinterpret_cast<const float4 *>(G + MID * 64 + c16 * 8);
             const float4 a = crow[0], b = crow[1], ma = cmid[0], mb = cmid[1];
             const float d[8] = {ma.x - a.x, ma.y - a.y, ma.z - a.z, ma.w - a.w,
                                 mb.x - b.x, mb.y - b.y, mb.z - b.z, mb.w - b.w};
@@ -889,7 +824,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
     };
     auto state_to_mid = [&](int stage) {
         const float *G = reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G);
-        const float f = ex2(G[kGlaMid * 64 + srow]);
+        const float f = ex2(G[MID * 64 + srow]);
 #pragma unroll
         for (int j = 0; j < SC; ++j) S[j] *= f;
     };
@@ -908,7 +843,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
     };
     auto state_finish = [&](int stage) {
         const float *G = reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G);
-        const float f = ex2(G[(kGlaTc - 1) * 64 + srow] - G[kGlaMid * 64 + srow]);
+        const float f = ex2(G[LAST * 64 + srow] - G[MID * 64 + srow]);
         float u[SC];
         load_u(u);
 #pragma unroll
@@ -972,8 +907,8 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
         for (int j = 0; j < 8; ++j) {
             const int s = sb + 2 * j;
             float2 v = make_float2(__uint_as_float(pr[2 * j]), __uint_as_float(pr[2 * j + 1]));
-            if (s > r) v.x = 0.f;
-            if (s + 1 > r) v.y = 0.f;
+            if (REV ? s < r : s > r) v.x = 0.f;  // reversed stage rows: keep s >= r
+            if (REV ? s + 1 < r : s + 1 > r) v.y = 0.f;
             split_bf16x2(v, hi[j], lo[j]);
         }
         tmem_st8x2(tmem + tlane + C::C_DB + (uint32_t)s0, hi);
@@ -982,7 +917,8 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
     };
     // OUT = 2^(c_r - c_m) O per (token r, key dimension), staged over the stage's X and Y (dead
     // once the products have run; 16-byte chunks XOR-ed with the row), written a row per warp
-    auto write_out = [&](int stage, long long t0) {
+    auto write_out = [&](int stage, int chunk) {
+        const long long r0 = row0_of(chunk);
         const float *G = reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G);
         float *ot = reinterpret_cast<float *>(smem + stage * C::STAGE + C::OFF_X);
         {
@@ -994,7 +930,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
             for (int c4 = 0; c4 < 4; ++c4) {
                 const int col = c0 + 4 * c4;
                 const float4 cr = *reinterpret_cast<const float4 *>(G + r * 64 + col);
-                const float4 cm = *reinterpret_cast<const float4 *>(G + kGlaMid * 64 + col);
+                const float4 cm = *reinterpret_cast<const float4 *>(G + MID * 64 + col);
                 const int ch = ((c0 >> 2) + c4) ^ (r & 15);
                 *reinterpret_cast<float4 *>(ot + r * 64 + ch * 4) =
                     make_float4(__uint_as_float(o[4 * c4]) * ex2(cr.x - cm.x), __uint_as_float(o[4 * c4 + 1]) * ex2(cr.y - cm.y),
@@ -1004,11 +940,11 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
         __syncthreads();
         for (int idx = tid; idx < kGlaTc * 32; idx += kGlaTcThreads) {
             const int r = idx >> 5, c2 = idx & 31;
-            const long long t = t0 + r;
-            if (t < p.T) {
+            const long long t = r0 + r;  // array row
+            if (t >= 0 && t < p.T) {
                 const int ch = (c2 >> 1) ^ (r & 15);
                 const float2 v = *reinterpret_cast<const float2 *>(ot + r * 64 + ch * 4 + (c2 & 1) * 2);
-                *reinterpret_cast<float2 *>(p.out + ((size_t)bh * p.T + arow_of(t)) * p.DK + zb * 64 + 2 * c2) = v;
+                *reinterpret_cast<float2 *>(p.out + ((size_t)bh * p.T + t) * p.DK + zb * 64 + 2 * c2) = v;
             }
         }
     };
@@ -1024,13 +960,11 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
     for (int j = 0; j < SC; ++j) S[j] = 0.f;
     float la_seg = 0.f;
     load_stage(0, c_begin, false);
-    cp_async_commit();
     if (nc > 1) load_stage(1, c_begin + 1, false);
-    cp_async_commit();
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
         stage_ready(stage);
-        la_seg += cumulate(stage);
+        la_seg += cumulate(stage, c_begin + i);
         __syncthreads();
         scale_z(stage);
         state_to_mid(stage);
@@ -1042,14 +976,11 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
         waitA();
         tc_fence_after();
         state_finish(stage);
-        if constexpr (TMA) fence_async_smem();  // this thread's writes to the stage before its reload
+        fence_async_smem();  // this thread's writes to the stage before its reload
         tc_fence_before();
         __syncthreads();
         if (i + 2 < nc) load_stage(stage, c_begin + i + 2, false);
-        cp_async_commit();
     }
-    cp_async_wait<0>();
-    __syncthreads();
 
     // ------------------------------------------------ look-back
     constexpr int TILES = SC / 4;
@@ -1119,14 +1050,11 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
 #pragma unroll
     for (int j = 0; j < SC; ++j) S[j] = Sin[j];
     load_stage(0, c_begin, true);
-    cp_async_commit();
     if (nc > 1) load_stage(1, c_begin + 1, true);
-    cp_async_commit();
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
-        const long long t0 = (long long)(c_begin + i) * kGlaTc;
         stage_ready(stage);
-        cumulate(stage);
+        cumulate(stage, c_begin + i);
         __syncthreads();
         scale_z(stage);
         state_to_mid(stage);
@@ -1150,14 +1078,12 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
         state_finish(stage);
         waitB();
         tc_fence_after();
-        write_out(stage, t0);
-        if constexpr (TMA) fence_async_smem();
+        write_out(stage, c_begin + i);
+        fence_async_smem();
         tc_fence_before();
         __syncthreads();
         if (i + 2 < nc) load_stage(stage, c_begin + i + 2, true);
-        cp_async_commit();
     }
-    cp_async_wait<0>();
 
     // the final state's rows dotted with fs_dot (the decay gradient's final-state term): the
     // paired halves of a warp, then the two column halves, summed through shared memory
@@ -1276,9 +1202,10 @@ GlaPlan gla_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv) {
     return p;
 }
 
-// Sizes the kernel handles: B*H <= 2^24, T <= 2^34, B*H*T <= 2^40, grid below 2^31 blocks.
+// Sizes the kernel handles: B*H <= 2^24, T < 2^31 (32-bit token coordinates of the tensor-map
+// loads), B*H*T <= 2^40, grid below 2^31 blocks.
 bool gla_sizes_fit(int64_t B, int64_t H, int64_t T) {
-    if (!product_below({B, H}, 16777217.0) || T > (1ll << 34)) return false;
+    if (!product_below({B, H}, 16777217.0) || T > kMaxTokens) return false;
     if (!product_below({B, H, T}, 1099511627777.0)) return false;
     const int64_t n_chunks = (T + kGlaTc - 1) / kGlaTc;
     return product_below({B, H, n_chunks, 2}, 2147483648.0);
@@ -1336,51 +1263,48 @@ bool gla_bwd_supported(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, 
            gla_sizes_fit(B, H, T) && product_below({B, H, (T + kGlaDlTile - 1) / kGlaDlTile}, 2147483648.0);
 }
 
-template <int DV, bool TMA>
+template <int DV, bool REV>
 int launch_gla_bwd_qk_variant(const GlaBArgs &a, const GlaQkMaps &maps, cudaStream_t s, unsigned int grid) {
     using C = GlaQkCfg<DV>;
     static std::atomic<unsigned long long> smem_set{0};  // per template instance
     const int st =
-        set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_tc_qk_kernel<DV, TMA>), C::SMEM);
+        set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_tc_qk_kernel<DV, REV>), C::SMEM);
     if (st) return st;
-    gla_tc_qk_kernel<DV, TMA><<<grid, kGlaTcThreads, C::SMEM, s>>>(a, maps);
+    gla_tc_qk_kernel<DV, REV><<<grid, kGlaTcThreads, C::SMEM, s>>>(a, maps);
     return check_launch("gla_tc_qk_kernel");
 }
 
-// The forward traversal (dQ) loads its stages by TMA; the reversed one (dK) by cp.async.
 template <int DV>
 int launch_gla_bwd_qk(const GlaBArgs &a, cudaStream_t s, unsigned int grid) {
     GlaQkMaps maps;
     memset(&maps, 0, sizeof(maps));
-    if (a.rev) return launch_gla_bwd_qk_variant<DV, false>(a, maps, s, grid);
     const bool ok = make_map(&maps.x, a.x, DV, a.T, a.BH, kGlaTc) && make_map(&maps.y, a.y, DV, a.T, a.BH, kGlaTc) &&
                     make_map(&maps.z, a.z, a.DK, a.T, a.BH, kGlaTc) &&
                     make_map_f32_rows(&maps.g, a.g, a.DK, a.T, a.BH, kGlaTc, 64);
     if (!ok) return fail(CLA_ERR_CUDA, "gla_tc_qk_kernel: tensor map encoding failed");
-    return launch_gla_bwd_qk_variant<DV, true>(a, maps, s, grid);
+    return a.rev ? launch_gla_bwd_qk_variant<DV, true>(a, maps, s, grid)
+                 : launch_gla_bwd_qk_variant<DV, false>(a, maps, s, grid);
 }
 
-template <int DK, bool TMA>
+template <int DK, bool REV>
 int launch_gla_fwd_variant(const GlaArgs &a, const GlaMaps &maps, cudaStream_t s, unsigned int grid) {
     using C = GlaTcCfg<DK>;
     static std::atomic<unsigned long long> smem_set{0};  // per template instance
-    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_tc_kernel<DK, TMA>), C::SMEM);
+    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(gla_tc_kernel<DK, REV>), C::SMEM);
     if (st) return st;
-    gla_tc_kernel<DK, TMA><<<grid, kGlaTcThreads, C::SMEM, s>>>(a, maps);
+    gla_tc_kernel<DK, REV><<<grid, kGlaTcThreads, C::SMEM, s>>>(a, maps);
     return check_launch("gla_tc_kernel");
 }
 
-// The forward traversal loads its stages by TMA; the reversed one by cp.async.
 template <int DK>
 int launch_gla_fwd(const GlaArgs &a, cudaStream_t s, unsigned int grid) {
     GlaMaps maps;
     memset(&maps, 0, sizeof(maps));
-    if (a.rev) return launch_gla_fwd_variant<DK, false>(a, maps, s, grid);
     const bool ok = make_map(&maps.q, a.q, DK, a.T, a.BH, kGlaTc) && make_map(&maps.k, a.k, DK, a.T, a.BH, kGlaTc) &&
                     make_map(&maps.v, a.v, a.DV, a.T, a.BH, kGlaTc) &&
                     make_map_f32_rows(&maps.g, a.g, DK, a.T, a.BH, kGlaTc, DK);
     if (!ok) return fail(CLA_ERR_CUDA, "gla_tc_kernel: tensor map encoding failed");
-    return launch_gla_fwd_variant<DK, true>(a, maps, s, grid);
+    return a.rev ? launch_gla_fwd_variant<DK, true>(a, maps, s, grid) : launch_gla_fwd_variant<DK, false>(a, maps, s, grid);
 }
 
 }  // namespace
