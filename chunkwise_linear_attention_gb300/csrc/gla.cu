@@ -459,19 +459,24 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
 #pragma unroll
     for (int j = 0; j < SC; ++j) S[j] = 0.f;
     float la_seg = 0.f;  // thread i < DK: log2 of alpha_seg[i]
+    // A chunk's in-chunk sums are formed while the tensor cores run the chunk before it.
     load_stage(0, c_begin, false);
     if (nc > 1) load_stage(1, c_begin + 1, false);
+    stage_ready(0);
+    la_seg += cumulate(0, c_begin);
+    __syncthreads();
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
-        stage_ready(stage);
-        la_seg += cumulate(stage, c_begin + i);
-        __syncthreads();
         scale_operands(stage, false);
         state_to_mid(stage);
         hand_to_tc();
         if (warp == 0) {
             issue_u(stage);
             mma_commit_w(barA);
+        }
+        if (i + 1 < nc) {
+            stage_ready(stage ^ 1);
+            la_seg += cumulate(stage ^ 1, c_begin + i + 1);
         }
         waitA();
         tc_fence_after();
@@ -552,11 +557,11 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
     for (int j = 0; j < SC; ++j) S[j] = Sin[j];
     load_stage(0, c_begin, true);
     if (nc > 1) load_stage(1, c_begin + 1, true);
+    stage_ready(0);
+    cumulate(0, c_begin);
+    __syncthreads();
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
-        stage_ready(stage);
-        cumulate(stage, c_begin + i);
-        __syncthreads();
         scale_operands(stage, true);
         state_to_mid(stage);
         write_sb();
@@ -565,6 +570,10 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
             issue_p_o(stage);
             issue_u(stage);
             mma_commit_w(barA);
+        }
+        if (i + 1 < nc) {
+            stage_ready(stage ^ 1);
+            cumulate(stage ^ 1, c_begin + i + 1);
         }
         waitA();
         tc_fence_after();
@@ -959,19 +968,24 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
 #pragma unroll
     for (int j = 0; j < SC; ++j) S[j] = 0.f;
     float la_seg = 0.f;
+    // a chunk's in-chunk sums are formed while the tensor cores run the chunk before it
     load_stage(0, c_begin, false);
     if (nc > 1) load_stage(1, c_begin + 1, false);
+    stage_ready(0);
+    la_seg += cumulate(0, c_begin);
+    __syncthreads();
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
-        stage_ready(stage);
-        la_seg += cumulate(stage, c_begin + i);
-        __syncthreads();
         scale_z(stage);
         state_to_mid(stage);
         hand_to_tc();
         if (warp == 0) {
             issue_u(stage);
             mma_commit_w(barA);
+        }
+        if (i + 1 < nc) {
+            stage_ready(stage ^ 1);
+            la_seg += cumulate(stage ^ 1, c_begin + i + 1);
         }
         waitA();
         tc_fence_after();
@@ -1051,11 +1065,11 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
     for (int j = 0; j < SC; ++j) S[j] = Sin[j];
     load_stage(0, c_begin, true);
     if (nc > 1) load_stage(1, c_begin + 1, true);
+    stage_ready(0);
+    cumulate(0, c_begin);
+    __syncthreads();
     for (int i = 0; i < nc; ++i) {
         const int stage = i & 1;
-        stage_ready(stage);
-        cumulate(stage, c_begin + i);
-        __syncthreads();
         scale_z(stage);
         state_to_mid(stage);
         write_sb();
@@ -1064,6 +1078,10 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
             issue_d_o(stage);
             issue_u(stage);
             mma_commit_w(barA);
+        }
+        if (i + 1 < nc) {
+            stage_ready(stage ^ 1);
+            cumulate(stage ^ 1, c_begin + i + 1);
         }
         waitA();
         tc_fence_after();
