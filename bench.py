@@ -318,8 +318,12 @@ def bench_scan_small(torch, cla, workloads, dev, flush, peaks, iters=20, shape=N
     ws = torch.empty(cla.scan_diag_workspace_size(B, T, D), dtype=torch.uint8, device=dev)
     h = torch.empty_like(a)
     ms = _time_calls(torch, lambda: cla.scan_diag_fwd(a, b, h=h, workspace=ws), flush, iters)
+    # the same bracket around a one-element fill kernel: what the events and a launch cost alone
+    one = torch.empty(1, device=dev)
+    floor_ms = _time_calls(torch, lambda: one.fill_(1.0), flush, iters)
     by = 12 * B * T * D
     return {"workload": f"diagonal scan fwd fp32 B={B} T={T} D={D}", "fwd_us": round(ms * 1e3, 2),
+            "timing_floor_us": round(floor_ms * 1e3, 2),
             "GBps": round(by / ms / 1e6, 1), "frac_hbm": round(by / ms / 1e6 / peaks["hbm_gbs"], 4)}
 
 

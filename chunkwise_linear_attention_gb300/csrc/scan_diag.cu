@@ -678,8 +678,9 @@ scan_diag_fwd_small_kernel(const float *__restrict__ a, const float *__restrict_
         for (int v = 0; v < VEC; ++v) carry[v] = fmaf(sA[w][cg * VEC + v], carry[v], sB[w][cg * VEC + v]);
 
     // phase 2: re-run from the true state, write h once
+    const bool one = (ch_end - ch_begin) == 1;  // the registers still hold the chunk's steps and pairs
     for (int chunk = ch_begin; chunk < ch_end; ++chunk) {
-        chunk_pairs(chunk);
+        if (!one) chunk_pairs(chunk);
         const long long t_begin = (long long)chunk * kTc + sub * kL;
         float hs[VEC];
 #pragma unroll
@@ -790,11 +791,18 @@ int scan_fwd(const char *fn, bool blelloch, const float *a, const float *b, cons
     const Plan p = make_plan(B, T, D, v4 ? 4 : 1);
     if (ws_bytes < p.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, p.total);
     if (!blelloch && p.g.n_chunks <= kSmallMaxChunks && (long long)p.g.B * p.g.n_cw <= kSmallBlocks) {
-        // short sequence, few channel groups: one block per group, no workspace traffic
-        const dim3 grid((unsigned int)p.g.n_cw, (unsigned int)p.g.B);
+        // short sequence, few channel groups: one block per group, no workspace traffic; one
+        // channel per lane while that still fits one block per SM (more blocks: more loads in
+        // flight at once, the call being bound by their latency)
         WsHeader *hdr = static_cast<WsHeader *>(ws);
-        if (v4) scan_diag_fwd_small_kernel<4><<<grid, kSmallWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, hdr);
-        else scan_diag_fwd_small_kernel<1><<<grid, kSmallWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, hdr);
+        const Plan p1 = make_plan(B, T, D, 1);
+        if (!v4 || (long long)p1.g.B * p1.g.n_cw <= kSmallBlocks) {
+            const dim3 grid((unsigned int)p1.g.n_cw, (unsigned int)p1.g.B);
+            scan_diag_fwd_small_kernel<1><<<grid, kSmallWarps * 32, 0, s>>>(a, b, h0, h, hT, p1.g, hdr);
+        } else {
+            const dim3 grid((unsigned int)p.g.n_cw, (unsigned int)p.g.B);
+            scan_diag_fwd_small_kernel<4><<<grid, kSmallWarps * 32, 0, s>>>(a, b, h0, h, hT, p.g, hdr);
+        }
         return check_launch(fn);
     }
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.total, s), fn);

@@ -47,7 +47,8 @@ def _run(cla, inp, with_h0=True, with_dhT=False, seed=0, recompute=False):
 
 
 @pytest.mark.parametrize("B,T,D", [(1, 1, 4), (2, 63, 16), (2, 64, 16), (2, 65, 20), (3, 200, 96),
-                                   (1, 1000, 7), (2, 513, 130), (1, 4097, 8), (2, 130, 3)])
+                                   (1, 1000, 7), (2, 513, 130), (1, 4097, 8), (2, 130, 3), (2, 2500, 12),
+                                   (1, 4096, 64)])
 @pytest.mark.parametrize("with_h0", [False, True])
 def test_scan_diag_small(cla, B, T, D, with_h0):
     inp = workloads.make("scan", B=B, T=T, D=D)
