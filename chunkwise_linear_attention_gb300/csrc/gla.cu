@@ -220,28 +220,29 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
         tma_load_3d(s0 + C::OFF_V, &maps.v, zb * 64, y, bh, bar);
         tma_load_3d(s0 + C::OFF_G, &maps.g, 0, REV ? y + 1 : y, bh, bar);
     };
-    // In-chunk cumulative log2 decays, in place (thread i < DK scans dimension i in traversal
-    // order), with the range check; returns (to thread i) the chunk's total c_L[i].  Positions
-    // past the sequence's end decay by nothing (the reversed traversal's first one past the end
-    // would otherwise read a_0's row).
+    // In-chunk cumulative log2 decays, in place (the last DK threads, which issue no products:
+    // thread cdim >= 0 scans dimension cdim in traversal order), with the range check; returns
+    // (to that thread) the chunk's total c_L[cdim].  Positions past the sequence's end decay by
+    // nothing (the reversed traversal's first one past the end would otherwise read a_0's row).
+    const int cdim = tid - (kGlaTcThreads - DK);
     auto cumulate = [&](int stage, int chunk) {
         float *G = reinterpret_cast<float *>(smem + stage * C::STAGE + C::OFF_G);
         float total = 0.f;
-        if (tid < DK) {
+        if (cdim >= 0) {
             const long long n_tok = p.T - (long long)kGlaTc * chunk;  // positions below are tokens
             float run = 0.f, lo = 0.f, hi = 0.f;
             bool finite = true;
 #pragma unroll 8
             for (int t = 0; t < kGlaTc; ++t) {
                 const int row = REV ? kGlaTc - 1 - t : t;
-                const float l = (REV && t >= n_tok) ? 0.f : G[row * DK + tid];
+                const float l = (REV && t >= n_tok) ? 0.f : G[row * DK + cdim];
                 finite = finite && isfinite(l);
                 run += l * kGlaLog2e;
-                G[row * DK + tid] = run;
+                G[row * DK + cdim] = run;
                 lo = fminf(lo, run);
                 hi = fmaxf(hi, run);
             }
-            const float cm = G[MID * DK + tid];
+            const float cm = G[MID * DK + cdim];
             // the running sum starts at 0 before token 0: include it in the span as well
             if (!finite || hi - cm > kGlaSpan || cm - lo > kGlaSpan || cm > kGlaSpan)
                 atomicOr(&p.hdr->error, kErrRange);
@@ -458,7 +459,7 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
     // ------------------------------------------------ phase 1: the segment's affine pair
 #pragma unroll
     for (int j = 0; j < SC; ++j) S[j] = 0.f;
-    float la_seg = 0.f;  // thread i < DK: log2 of alpha_seg[i]
+    float la_seg = 0.f;  // thread cdim >= 0: log2 of alpha_seg[cdim]
     // A chunk's in-chunk sums are formed while the tensor cores run the chunk before it.
     load_stage(0, c_begin, false);
     if (nc > 1) load_stage(1, c_begin + 1, false);
@@ -501,14 +502,14 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
         for (int j = 0; j < SC; ++j)
             Sin[j] = fmaf(scale, __ldg(p.S0 + ((size_t)bh * DK + srow) * p.DV + zb * 64 + scol(j)), Sin[j]);
     };
-    if (tid < DK) alpha_s[tid] = ex2(la_seg);
+    if (cdim >= 0) alpha_s[cdim] = ex2(la_seg);
     if (seg == 0) {
         add_state0(1.f);
     } else {
 #pragma unroll
         for (int tl = 0; tl < TILES; ++tl)
             __stcg(p.agg + ws_index(unit, tl), make_float4(S[4 * tl], S[4 * tl + 1], S[4 * tl + 2], S[4 * tl + 3]));
-        if (tid < DK) __stcg(p.alpha + unit * DK + tid, ex2(la_seg));
+        if (cdim >= 0) __stcg(p.alpha + unit * DK + cdim, ex2(la_seg));
         __threadfence();
         __syncthreads();
         if (tid == 0) st_release(p.flags + unit, 1u);
@@ -765,25 +766,27 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
         tma_load_3d(s0 + C::OFF_Z, &maps.z, zb * 64, y, bh, bar);
         tma_load_3d(s0 + C::OFF_G, &maps.g, zb * 64, REV ? y + 1 : y, bh, bar);
     };
-    // in-chunk cumulative log2 decays in traversal order (positions past the end decay by nothing)
+    // in-chunk cumulative log2 decays in traversal order (positions past the end decay by
+    // nothing), by the last 64 threads (they issue no products): thread cdim >= 0 scans cdim
+    const int cdim = tid - (kGlaTcThreads - 64);
     auto cumulate = [&](int stage, int chunk) {
         float *G = reinterpret_cast<float *>(smem + stage * C::STAGE + C::OFF_G);
         float total = 0.f;
-        if (tid < 64) {
+        if (cdim >= 0) {
             const long long n_tok = p.T - (long long)kGlaTc * chunk;
             float run = 0.f, lo = 0.f, hi = 0.f;
             bool finite = true;
 #pragma unroll 8
             for (int t = 0; t < kGlaTc; ++t) {
                 const int row = REV ? kGlaTc - 1 - t : t;
-                const float l = (REV && t >= n_tok) ? 0.f : G[row * 64 + tid];
+                const float l = (REV && t >= n_tok) ? 0.f : G[row * 64 + cdim];
                 finite = finite && isfinite(l);
                 run += l * kGlaLog2e;
-                G[row * 64 + tid] = run;
+                G[row * 64 + cdim] = run;
                 lo = fminf(lo, run);
                 hi = fmaxf(hi, run);
             }
-            const float cm = G[MID * 64 + tid];
+            const float cm = G[MID * 64 + cdim];
             if (!finite || hi - cm > kGlaSpan || cm - lo > kGlaSpan || cm > kGlaSpan)
                 atomicOr(&p.hdr->error, kErrRange);
             total = run;
@@ -1010,14 +1013,14 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
         for (int j = 0; j < SC; ++j)
             Sin[j] = fmaf(scale, __ldg(p.S0 + ((size_t)bh * p.DK + zb * 64 + srow) * DV + scol(j)), Sin[j]);
     };
-    if (tid < 64) alpha_s[tid] = ex2(la_seg);
+    if (cdim >= 0) alpha_s[cdim] = ex2(la_seg);
     if (seg == 0) {
         add_state0(1.f);
     } else {
 #pragma unroll
         for (int tl = 0; tl < TILES; ++tl)
             __stcg(p.agg + ws_index(unit, tl), make_float4(S[4 * tl], S[4 * tl + 1], S[4 * tl + 2], S[4 * tl + 3]));
-        if (tid < 64) __stcg(p.alpha + unit * 64 + tid, ex2(la_seg));
+        if (cdim >= 0) __stcg(p.alpha + unit * 64 + cdim, ex2(la_seg));
         __threadfence();
         __syncthreads();
         if (tid == 0) st_release(p.flags + unit, 1u);
