@@ -256,7 +256,10 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
         uint8_t *st = smem + stage * C::STAGE;
         const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
         constexpr int QC = DK / 8;
-        for (int i = tid; i < kGlaTc * QC; i += kGlaTcThreads) {
+        static_assert(kGlaTc * QC % kGlaTcThreads == 0, "whole rounds");
+#pragma unroll
+        for (int it = 0; it < kGlaTc * QC / kGlaTcThreads; ++it) {
+            const int i = tid + it * kGlaTcThreads;
             const int row = i / QC, c16 = i % QC;
             const float4 *crow = reinterpret_cast<const float4 *>(G + row * DK + c16 * 8);
             const float4 *cmid = reinterpret_cast<const float4 *>(G + MID * DK + c16 * 8);
@@ -437,7 +440,9 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
             }
         }
         __syncthreads();
-        for (int idx = tid; idx < kGlaTc * 32; idx += kGlaTcThreads) {
+#pragma unroll
+        for (int it = 0; it < kGlaTc * 32 / kGlaTcThreads; ++it) {
+            const int idx = tid + it * kGlaTcThreads;
             const int r = idx >> 5, c2 = idx & 31;
             const long long t = r0 + r;  // array row
             if (t >= 0 && t < p.T) {
@@ -797,7 +802,9 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
     auto scale_z = [&](int stage) {
         uint8_t *st = smem + stage * C::STAGE;
         const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
-        for (int i = tid; i < kGlaTc * 8; i += kGlaTcThreads) {
+#pragma unroll
+        for (int it = 0; it < kGlaTc * 8 / kGlaTcThreads; ++it) {
+            const int i = tid + it * kGlaTcThreads;
             const int row = i >> 3, c16 = i & 7;
             const float4 *crow = reinterpret_cast<const float4 *>(G + row * 64 + c16 * 8);
             const float4 *cmid = reinterpret_cast<const float4 *>(G + MID * 64 + c16 * 8);
@@ -950,7 +957,9 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
             }
         }
         __syncthreads();
-        for (int idx = tid; idx < kGlaTc * 32; idx += kGlaTcThreads) {
+#pragma unroll
+        for (int it = 0; it < kGlaTc * 32 / kGlaTcThreads; ++it) {
+            const int idx = tid + it * kGlaTcThreads;
             const int r = idx >> 5, c2 = idx & 31;
             const long long t = r0 + r;  // array row
             if (t >= 0 && t < p.T) {
