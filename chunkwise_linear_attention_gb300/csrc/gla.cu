@@ -255,19 +255,30 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
     auto scale_operands = [&](int stage, bool withQ) {
         uint8_t *st = smem + stage * C::STAGE;
         const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
-        constexpr int QC = DK / 8;
-        static_assert(kGlaTc * QC % kGlaTcThreads == 0, "whole rounds");
+        constexpr int QC = DK / 8;  // 8-element groups of a row
+        static_assert(kGlaTc * QC % kGlaTcThreads == 0 && kGlaTcThreads % QC == 0, "whole rounds, fixed columns");
+        // a thread keeps its 8 key dimensions (the same in every round) and steps over rows
+        const int c16 = tid % QC;
+        float2 nm[4];  // -c_m of the thread's dimensions
+        {
+            const float4 *cmid = reinterpret_cast<const float4 *>(G + MID * DK + c16 * 8);
+            const float4 ma = cmid[0], mb = cmid[1];
+            nm[0] = make_float2(-ma.x, -ma.y);
+            nm[1] = make_float2(-ma.z, -ma.w);
+            nm[2] = make_float2(-mb.x, -mb.y);
+            nm[3] = make_float2(-mb.z, -mb.w);
+        }
 #pragma unroll
         for (int it = 0; it < kGlaTc * QC / kGlaTcThreads; ++it) {
-            const int i = tid + it * kGlaTcThreads;
-            const int row = i / QC, c16 = i % QC;
+            const int row = tid / QC + it * (kGlaTcThreads / QC);
             const float4 *crow = reinterpret_cast<const float4 *>(G + row * DK + c16 * 8);
-            const float4 *cmid = reinterpret_cast<const float4 *>(G + MID * DK + c16 * 8);
-            float d[8];
+            float2 d[4];  // c - c_m
             {
-                const float4 a = crow[0], b = crow[1], ma = cmid[0], mb = cmid[1];
-                d[0] = a.x - ma.x; d[1] = a.y - ma.y; d[2] = a.z - ma.z; d[3] = a.w - ma.w;
-                d[4] = b.x - mb.x; d[5] = b.y - mb.y; d[6] = b.z - mb.z; d[7] = b.w - mb.w;
+                const float4 a = crow[0], b = crow[1];
+                d[0] = __fadd2_rn(make_float2(a.x, a.y), nm[0]);
+                d[1] = __fadd2_rn(make_float2(a.z, a.w), nm[1]);
+                d[2] = __fadd2_rn(make_float2(b.x, b.y), nm[2]);
+                d[3] = __fadd2_rn(make_float2(b.z, b.w), nm[3]);
             }
             const uint32_t off = (uint32_t)((c16 >> 3) * 8192) + sw128(row, (c16 & 7) * 8);
             {
@@ -275,10 +286,8 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
                 const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
                 uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 x = unpack_bf16(w[e]);
-                    split_bf16x2(make_float2(x.x * ex2(-d[2 * e]), x.y * ex2(-d[2 * e + 1])), hi[e], lo[e]);
-                }
+                for (int e = 0; e < 4; ++e)
+                    split_bf16x2(__fmul2_rn(unpack_bf16(w[e]), make_float2(ex2(-d[e].x), ex2(-d[e].y))), hi[e], lo[e]);
                 *reinterpret_cast<uint4 *>(st + C::OFF_K + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                 *reinterpret_cast<uint4 *>(smem + C::OFF_KL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
@@ -287,15 +296,14 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
                 const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
                 uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 x = unpack_bf16(w[e]);
-                    split_bf16x2(make_float2(x.x * ex2(d[2 * e]), x.y * ex2(d[2 * e + 1])), hi[e], lo[e]);
-                }
+                for (int e = 0; e < 4; ++e)
+                    split_bf16x2(__fmul2_rn(unpack_bf16(w[e]), make_float2(ex2(d[e].x), ex2(d[e].y))), hi[e], lo[e]);
                 *reinterpret_cast<uint4 *>(st + C::OFF_Q + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                 *reinterpret_cast<uint4 *>(smem + C::OFF_QL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
     };
+
 
     // This thread's state: one row (key dimension) srow and SC consecutive columns of half hf.
     // DK = 128: row 32 q + lane (the lane of a 128-row accumulator), columns 32 hf + {0..31}.
@@ -802,28 +810,38 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
     auto scale_z = [&](int stage) {
         uint8_t *st = smem + stage * C::STAGE;
         const float *G = reinterpret_cast<const float *>(st + C::OFF_G);
+        // a thread keeps its 8 key dimensions (the same in every round) and steps over rows
+        const int c16 = tid & 7;
+        float2 cm[4];  // c_m of the thread's dimensions
+        {
+            const float4 *cmid = reinterpret_cast<const float4 *>(G + MID * 64 + c16 * 8);
+            const float4 ma = cmid[0], mb = cmid[1];
+            cm[0] = make_float2(ma.x, ma.y);
+            cm[1] = make_float2(ma.z, ma.w);
+            cm[2] = make_float2(mb.x, mb.y);
+            cm[3] = make_float2(mb.z, mb.w);
+        }
 #pragma unroll
         for (int it = 0; it < kGlaTc * 8 / kGlaTcThreads; ++it) {
-            const int i = tid + it * kGlaTcThreads;
-            const int row = i >> 3, c16 = i & 7;
+            const int row = (tid >> 3) + it * (kGlaTcThreads / 8);
             const float4 *crow = reinterpret_cast<const float4 *>(G + row * 64 + c16 * 8);
-            const float4 *cmid = reinterpret_cast<const float4 *>(G + MID * 64 + c16 * 8);
-            const float4 a = crow[0], b = crow[1], ma = cmid[0], mb = cmid[1];
-            const float d[8] = {ma.x - a.x, ma.y - a.y, ma.z - a.z, ma.w - a.w,
-                                mb.x - b.x, mb.y - b.y, mb.z - b.z, mb.w - b.w};
+            const float4 a = crow[0], b = crow[1];
+            const float2 nc[4] = {make_float2(-a.x, -a.y), make_float2(-a.z, -a.w), make_float2(-b.x, -b.y),
+                                  make_float2(-b.z, -b.w)};
             const uint32_t off = sw128(row, c16 * 8);
             const uint4 zv = *reinterpret_cast<const uint4 *>(st + C::OFF_Z + off);
             const uint32_t w[4] = {zv.x, zv.y, zv.z, zv.w};
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float2 x = unpack_bf16(w[e]);
-                split_bf16x2(make_float2(x.x * ex2(d[2 * e]), x.y * ex2(d[2 * e + 1])), hi[e], lo[e]);
+                const float2 d = __fadd2_rn(cm[e], nc[e]);  // c_m - c
+                split_bf16x2(__fmul2_rn(unpack_bf16(w[e]), make_float2(ex2(d.x), ex2(d.y))), hi[e], lo[e]);
             }
             *reinterpret_cast<uint4 *>(st + C::OFF_Z + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             *reinterpret_cast<uint4 *>(smem + C::OFF_ZL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
     };
+
 
     // This thread's state: key dimension srow (row of the 64-row accumulator U) and SC columns of
     // the value half hf, in runs of 16: 64-row layout, paired-half shape.
