@@ -177,7 +177,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) == cudaSuccess &&
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
         return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
