@@ -952,8 +952,9 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
         tmem_st8x2(tmem + tlane + C::C_DB + (uint32_t)(s0 + 16), lo);
         tmem_st_wait();
     };
-    // OUT = 2^(c_r - c_m) O per (token r, key dimension), staged over the stage's X and Y (dead
-    // once the products have run; 16-byte chunks XOR-ed with the row), written a row per warp
+    // OUT = 2^(c_r - c_m) O per (token r, key dimension): O staged over the stage's X and Y (dead
+    // once the products have run; 16-byte chunks XOR-ed with the row), then scaled and written a
+    // row per warp (the row's decays read as one contiguous run per warp: no bank conflicts)
     auto write_out = [&](int stage, int chunk) {
         const long long r0 = row0_of(chunk);
         const float *G = reinterpret_cast<const float *>(smem + stage * C::STAGE + C::OFF_G);
@@ -965,16 +966,13 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
-                const int col = c0 + 4 * c4;
-                const float4 cr = *reinterpret_cast<const float4 *>(G + r * 64 + col);
-                const float4 cm = *reinterpret_cast<const float4 *>(G + MID * 64 + col);
                 const int ch = ((c0 >> 2) + c4) ^ (r & 15);
-                *reinterpret_cast<float4 *>(ot + r * 64 + ch * 4) =
-                    make_float4(__uint_as_float(o[4 * c4]) * ex2(cr.x - cm.x), __uint_as_float(o[4 * c4 + 1]) * ex2(cr.y - cm.y),
-                                __uint_as_float(o[4 * c4 + 2]) * ex2(cr.z - cm.z), __uint_as_float(o[4 * c4 + 3]) * ex2(cr.w - cm.w));
+                *reinterpret_cast<uint4 *>(ot + r * 64 + ch * 4) =
+                    make_uint4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
             }
         }
         __syncthreads();
+        const float2 cm = *reinterpret_cast<const float2 *>(G + MID * 64 + 2 * lane);  // the same columns every round
 #pragma unroll
         for (int it = 0; it < kGlaTc * 32 / kGlaTcThreads; ++it) {
             const int idx = tid + it * kGlaTcThreads;
@@ -983,10 +981,13 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
             if (t >= 0 && t < p.T) {
                 const int ch = (c2 >> 1) ^ (r & 15);
                 const float2 v = *reinterpret_cast<const float2 *>(ot + r * 64 + ch * 4 + (c2 & 1) * 2);
-                *reinterpret_cast<float2 *>(p.out + ((size_t)bh * p.T + t) * p.DK + zb * 64 + 2 * c2) = v;
+                const float2 cr = *reinterpret_cast<const float2 *>(G + r * 64 + 2 * c2);
+                *reinterpret_cast<float2 *>(p.out + ((size_t)bh * p.T + t) * p.DK + zb * 64 + 2 * c2) =
+                    make_float2(v.x * ex2(cr.x - cm.x), v.y * ex2(cr.y - cm.y));
             }
         }
     };
+
     auto hand_to_tc = [&]() {
         fence_async_smem();
         tc_fence_before();
