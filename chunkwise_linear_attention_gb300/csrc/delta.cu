@@ -66,6 +66,106 @@ __device__ __forceinline__ float tri_row_dot(const float *row, const float (&x)[
     return (a0 + a1) + (a2 + a3);
 }
 
+// sum_{s < r} row[s] x[s] over a 16-row block (the same loads and partial sums as tri_row_dot).
+__device__ __forceinline__ float tri_row_dot16(const float *row, const float (&x)[16], int r) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int s4 = 0; s4 + 4 <= r; s4 += 4) {
+        const float4 e = *reinterpret_cast<const float4 *>(row + s4);
+        a0 = fmaf(e.x, x[s4], a0);
+        a1 = fmaf(e.y, x[s4 + 1], a1);
+        a2 = fmaf(e.z, x[s4 + 2], a2);
+        a3 = fmaf(e.w, x[s4 + 3], a3);
+    }
+#pragma unroll
+    for (int s = r & ~3; s < r; ++s) a0 = fmaf(row[s], x[s], a0);
+    return (a0 + a1) + (a2 + a3);
+}
+
+// T = (I + A)^-1 in place, A strictly lower triangular, fp32 [64][kAS] in shared memory (zeros on
+// and above the diagonal); on return the array holds T (unit diagonal, zeros above).  Blocked by
+// 16 rows: the four diagonal blocks T_bb = (I + A_bb)^-1 by forward substitution (threads 0..63,
+// one column of one block each), then block rows i = 1, 2, 3 from
+//     T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj      (j < i),
+// the sum S_ij stored over A_ij (no longer needed) and T_ij over S_ij, every thread of the first
+// 128 taking two columns of one row.  A dependent chain of 16 rows and three block rows, instead
+// of 64 rows.  Called by the whole block (NT threads, NT >= 128); ends with a barrier.
+__device__ __forceinline__ void tri_inverse_blocked(float *Am, int tid) {
+    {  // diagonal blocks
+        const int b = (tid >> 4) & 3, c = tid & 15;
+        float x[16];
+        if (tid < 64) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const float acc = tri_row_dot16(Am + (16 * b + r) * kAS + 16 * b, x, r);
+                x[r] = (r < c) ? 0.f : (r == c ? 1.f : -acc);
+            }
+        }
+        __syncthreads();  // every diagonal block read
+        if (tid < 64) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) Am[(16 * b + r) * kAS + 16 * b + c] = x[r];
+        }
+        __syncthreads();
+    }
+    const int r = (tid >> 3) & 15, cp = 2 * (tid & 7);  // this thread's row and column pair in a block
+    const bool act = tid < 128;
+#pragma unroll
+    for (int i = 1; i < 4; ++i) {
+        float2 acc[3];
+        if (act) {
+            const float *arow = Am + (16 * i + r) * kAS;
+#pragma unroll
+            for (int j = 0; j < i; ++j) {
+                float2 a2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int s4 = 16 * j; s4 < 16 * i; s4 += 4) {
+                    const float4 av = *reinterpret_cast<const float4 *>(arow + s4);
+                    const float ae[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 tv = *reinterpret_cast<const float2 *>(Am + (s4 + e) * kAS + 16 * j + cp);
+                        a2.x = fmaf(ae[e], tv.x, a2.x);
+                        a2.y = fmaf(ae[e], tv.y, a2.y);
+                    }
+                }
+                acc[j] = a2;
+            }
+        }
+        __syncthreads();  // block row i of A read
+        if (act) {
+#pragma unroll
+            for (int j = 0; j < i; ++j) *reinterpret_cast<float2 *>(Am + (16 * i + r) * kAS + 16 * j + cp) = acc[j];
+        }
+        __syncthreads();  // S_ij in place
+        if (act) {
+            const float *trow = Am + (16 * i + r) * kAS + 16 * i;  // T_ii, zeros above its diagonal
+#pragma unroll
+            for (int j = 0; j < i; ++j) {
+                float2 a2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int s4 = 0; s4 < 16; s4 += 4) {
+                    const float4 tv4 = *reinterpret_cast<const float4 *>(trow + s4);
+                    const float te[4] = {tv4.x, tv4.y, tv4.z, tv4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 sv = *reinterpret_cast<const float2 *>(Am + (16 * i + s4 + e) * kAS + 16 * j + cp);
+                        a2.x = fmaf(te[e], sv.x, a2.x);
+                        a2.y = fmaf(te[e], sv.y, a2.y);
+                    }
+                }
+                acc[j] = make_float2(-a2.x, -a2.y);
+            }
+        }
+        __syncthreads();  // S_i* read
+        if (act) {
+#pragma unroll
+            for (int j = 0; j < i; ++j) *reinterpret_cast<float2 *>(Am + (16 * i + r) * kAS + 16 * j + cp) = acc[j];
+        }
+        __syncthreads();  // block row i of T in place
+    }
+}
+
 template <int DK>
 struct DeltaCfg {
     static constexpr int QRB = DK * 2;   // bytes per Q / K row (bf16)
@@ -273,25 +373,21 @@ __global__ void __launch_bounds__(kDlThreads, 2) delta_fwd_kernel(const DeltaArg
                 }
         }
         __syncthreads();
-        // ---- T = (I + A)^-1, unit lower triangular: thread j < 64 builds column j top-down,
-        // T[r][j] = -sum_{s<r} A[r][s] T[s][j] (T[s][j] = 0 above row j, 1 on it), in registers,
-        // then stores it as two bf16 parts (row r, column j of the [64][64] tiles)
-        if (tid < kDlTc) {
-            const int j = tid;
-            float tc[kDlTc];
+        // ---- T = (I + A)^-1 (unit lower triangular) in place, then as two bf16 parts in the
+        // [64][64] tiles: 16-byte chunks of 8 columns, four per thread
+        tri_inverse_blocked(Am, tid);
 #pragma unroll
-            for (int r = 0; r < kDlTc; ++r) {
-                const float acc = tri_row_dot(Am + r * kAS, tc, r);
-                tc[r] = (r < j) ? 0.f : (r == j ? 1.f : -acc);
-            }
-#pragma unroll
-            for (int r = 0; r < kDlTc; ++r) {
-                const uint32_t off = swz<C::VRB>(r, j >> 3) + (j & 7) * 2;
-                const uint32_t bits = __float_as_uint(tc[r]) & 0xffff0000u;
-                const float rest = tc[r] - __uint_as_float(bits);  // exact
-                *reinterpret_cast<uint16_t *>(smem + C::OFF_TH + off) = (uint16_t)(bits >> 16);
-                *reinterpret_cast<uint16_t *>(smem + C::OFF_TL + off) = (uint16_t)(__float_as_uint(rest) >> 16);
-            }
+        for (int it = 0; it < kDlTc * 8 / kDlThreads; ++it) {
+            const int task = tid + it * kDlThreads, r = task >> 3, c8 = task & 7;
+            const float4 v0 = *reinterpret_cast<const float4 *>(Am + r * kAS + 8 * c8);
+            const float4 v1 = *reinterpret_cast<const float4 *>(Am + r * kAS + 8 * c8 + 4);
+            uint32_t hi[4], lo[4];
+            split_bf16x2(make_float2(v0.x, v0.y), hi[0], lo[0]);
+            split_bf16x2(make_float2(v0.z, v0.w), hi[1], lo[1]);
+            split_bf16x2(make_float2(v1.x, v1.y), hi[2], lo[2]);
+            split_bf16x2(make_float2(v1.z, v1.w), hi[3], lo[3]);
+            *reinterpret_cast<uint4 *>(smem + C::OFF_TH + swz<C::VRB>(r, c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(smem + C::OFF_TL + swz<C::VRB>(r, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         __syncthreads();
 
