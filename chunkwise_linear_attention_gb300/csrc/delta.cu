@@ -47,26 +47,10 @@ constexpr int kDlThreads = 128;  // warp w: rows 16w..16w+15 of a chunk
 constexpr int kDlBwdThreads = 256;  // backward: warp w rows 16(w & 3).., column half w >> 2
 constexpr int kAS = kDlTc + 4;    // row stride (floats) of the fp32 [64][64] triangle: 16-byte aligned rows
 
-// sum_{s < r} row[s] x[s] for the forward substitution of a unit lower triangular system:
-// 16-byte loads of the row (broadcast: every thread reads the same row) and four partial sums,
-// so the dependent chain per row is a quarter as long.  r is a compile-time constant after
+// sum_{s < r} row[s] x[s] for the forward substitution of a unit lower triangular 16-row block:
+// 16-byte loads of the row (broadcast: the threads of a block read the same row) and four partial
+// sums, so the dependent chain per row is a quarter as long.  r is a compile-time constant after
 // unrolling; x stays in registers.
-__device__ __forceinline__ float tri_row_dot(const float *row, const float (&x)[kDlTc], int r) {
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-    for (int s4 = 0; s4 + 4 <= r; s4 += 4) {
-        const float4 e = *reinterpret_cast<const float4 *>(row + s4);
-        a0 = fmaf(e.x, x[s4], a0);
-        a1 = fmaf(e.y, x[s4 + 1], a1);
-        a2 = fmaf(e.z, x[s4 + 2], a2);
-        a3 = fmaf(e.w, x[s4 + 3], a3);
-    }
-#pragma unroll
-    for (int s = r & ~3; s < r; ++s) a0 = fmaf(row[s], x[s], a0);
-    return (a0 + a1) + (a2 + a3);
-}
-
-// sum_{s < r} row[s] x[s] over a 16-row block (the same loads and partial sums as tri_row_dot).
 __device__ __forceinline__ float tri_row_dot16(const float *row, const float (&x)[16], int r) {
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
@@ -693,6 +677,7 @@ struct DeltaBwdCfg {
     static constexpr int SMEM = OFF_RED + 64;
     static constexpr int S_MT = DK / 64;  // 16-row tiles of the state per row group
     static_assert(2 * V_BYTES <= E_BYTES, "F fits where E was");
+    static_assert(E_BYTES <= 4 * V_BYTES, "the fp32 inverse fits over U's and diag(w) U's tiles");
     static_assert(E_BYTES % 128 == 0, "tiles after E stay 128-byte aligned");
     static_assert(SMEM + 1024 <= 227 * 1024, "one block per SM");
 };
@@ -940,23 +925,32 @@ __global__ void __launch_bounds__(kDlBwdThreads, 1) delta_bwd_kernel(const Delta
                 }
         }
         __syncthreads();
-        // ---- (I + A)^-1 by forward substitution (threads 0..63, one column each), while every
-        // warp forms K S, Yv = V - diag(gamma) K S and X = diag(beta) Yv for its part
-        if (tid < kDlTc) {
-            const int j = tid;
-            float tc[kDlTc];
+        // ---- (I + A)^-1, A = diag(beta) E: A in fp32 over U's tiles (not written yet), inverted
+        // there in place by 16-row blocks, then as two bf16 parts; then every warp forms K S,
+        // Yv = V - diag(gamma) K S and X = diag(beta) Yv for its part
+        {
+            float *Aw = reinterpret_cast<float *>(smem + C::OFF_UH);
 #pragma unroll
-            for (int r = 0; r < kDlTc; ++r) {
-                const float acc = tri_row_dot(Em + r * kAS, tc, r);
-                tc[r] = (r < j) ? 0.f : (r == j ? 1.f : -bs[r] * acc);
+            for (int it = 0; it < kDlTc * 16 / kDlBwdThreads; ++it) {
+                const int task = tid + it * kDlBwdThreads, r = task >> 4, c4 = task & 15;
+                const float4 e = *reinterpret_cast<const float4 *>(Em + r * kAS + 4 * c4);
+                const float b = bs[r];
+                *reinterpret_cast<float4 *>(Aw + r * kAS + 4 * c4) = make_float4(b * e.x, b * e.y, b * e.z, b * e.w);
             }
+            __syncthreads();
+            tri_inverse_blocked(Aw, tid);
 #pragma unroll
-            for (int r = 0; r < kDlTc; ++r) {
-                const uint32_t off = swz<VRB>(r, j >> 3) + (j & 7) * 2;
-                const uint32_t bits = __float_as_uint(tc[r]) & 0xffff0000u;
-                const float rest = tc[r] - __uint_as_float(bits);  // exact
-                *reinterpret_cast<uint16_t *>(smem + C::OFF_TH + off) = (uint16_t)(bits >> 16);
-                *reinterpret_cast<uint16_t *>(smem + C::OFF_TL + off) = (uint16_t)(__float_as_uint(rest) >> 16);
+            for (int it = 0; it < kDlTc * 8 / kDlBwdThreads; ++it) {
+                const int task = tid + it * kDlBwdThreads, r = task >> 3, c8 = task & 7;
+                const float4 v0 = *reinterpret_cast<const float4 *>(Aw + r * kAS + 8 * c8);
+                const float4 v1 = *reinterpret_cast<const float4 *>(Aw + r * kAS + 8 * c8 + 4);
+                uint32_t hi[4], lo[4];
+                split_bf16x2(make_float2(v0.x, v0.y), hi[0], lo[0]);
+                split_bf16x2(make_float2(v0.z, v0.w), hi[1], lo[1]);
+                split_bf16x2(make_float2(v1.x, v1.y), hi[2], lo[2]);
+                split_bf16x2(make_float2(v1.z, v1.w), hi[3], lo[3]);
+                *reinterpret_cast<uint4 *>(smem + C::OFF_TH + swz<VRB>(r, c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(smem + C::OFF_TL + swz<VRB>(r, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
         float Yv[4][4];
