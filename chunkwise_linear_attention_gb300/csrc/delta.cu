@@ -66,15 +66,20 @@ __device__ __forceinline__ float tri_row_dot16(const float *row, const float (&x
     return (a0 + a1) + (a2 + a3);
 }
 
+// Pulls one 128-byte line of global memory into L2 (no register result, no wait).
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 // T = (I + A)^-1 in place, A strictly lower triangular, fp32 [64][kAS] in shared memory (zeros on
 // and above the diagonal); on return the array holds T (unit diagonal, zeros above).  Blocked by
 // 16 rows: the four diagonal blocks T_bb = (I + A_bb)^-1 by forward substitution (threads 0..63,
 // one column of one block each), then block rows i = 1, 2, 3 from
-//     T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj      (j < i),
-// the sum S_ij stored over A_ij (no longer needed) and T_ij over S_ij, every thread of the first
-// 128 taking two columns of one row.  A dependent chain of 16 rows and three block rows, instead
-// of 64 rows.  Called by the whole block (NT threads, NT >= 128); ends with a barrier.
-__device__ __forceinline__ void tri_inverse_blocked(float *Am, int tid) {
+//     S_ij = sum_{k=j}^{i-1} A_ik T_kj,   T_ij = -T_ii S_ij      (j < i),
+// S in the scratch Sx ([16][48] fp32) and T_ij over A_ij, every thread of the first 128 taking two
+// columns of one row.  A dependent chain of 16 rows and three block rows instead of 64 rows.
+// Called by the whole block (NT >= 128 threads); ends with a barrier.
+__device__ __forceinline__ void tri_inverse_blocked(float *Am, float *Sx, int tid) {
     {  // diagonal blocks
         const int b = (tid >> 4) & 3, c = tid & 15;
         float x[16];
@@ -92,59 +97,55 @@ __device__ __forceinline__ void tri_inverse_blocked(float *Am, int tid) {
         }
         __syncthreads();
     }
+    constexpr int SXS = 48;                             // row stride of Sx (floats)
     const int r = (tid >> 3) & 15, cp = 2 * (tid & 7);  // this thread's row and column pair in a block
     const bool act = tid < 128;
 #pragma unroll
     for (int i = 1; i < 4; ++i) {
-        float2 acc[3];
         if (act) {
             const float *arow = Am + (16 * i + r) * kAS;
 #pragma unroll
             for (int j = 0; j < i; ++j) {
-                float2 a2 = make_float2(0.f, 0.f);
+                float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);  // two chains
 #pragma unroll
                 for (int s4 = 16 * j; s4 < 16 * i; s4 += 4) {
                     const float4 av = *reinterpret_cast<const float4 *>(arow + s4);
-                    const float ae[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 tv = *reinterpret_cast<const float2 *>(Am + (s4 + e) * kAS + 16 * j + cp);
-                        a2.x = fmaf(ae[e], tv.x, a2.x);
-                        a2.y = fmaf(ae[e], tv.y, a2.y);
-                    }
+                    const float2 t0 = *reinterpret_cast<const float2 *>(Am + (s4 + 0) * kAS + 16 * j + cp);
+                    const float2 t1 = *reinterpret_cast<const float2 *>(Am + (s4 + 1) * kAS + 16 * j + cp);
+                    const float2 t2 = *reinterpret_cast<const float2 *>(Am + (s4 + 2) * kAS + 16 * j + cp);
+                    const float2 t3 = *reinterpret_cast<const float2 *>(Am + (s4 + 3) * kAS + 16 * j + cp);
+                    a0 = __ffma2_rn(make_float2(av.x, av.x), t0, a0);
+                    a1 = __ffma2_rn(make_float2(av.y, av.y), t1, a1);
+                    a0 = __ffma2_rn(make_float2(av.z, av.z), t2, a0);
+                    a1 = __ffma2_rn(make_float2(av.w, av.w), t3, a1);
                 }
-                acc[j] = a2;
+                *reinterpret_cast<float2 *>(Sx + r * SXS + 16 * j + cp) = __fadd2_rn(a0, a1);
             }
         }
-        __syncthreads();  // block row i of A read
-        if (act) {
-#pragma unroll
-            for (int j = 0; j < i; ++j) *reinterpret_cast<float2 *>(Am + (16 * i + r) * kAS + 16 * j + cp) = acc[j];
-        }
-        __syncthreads();  // S_ij in place
+        __syncthreads();  // S_i* in the scratch; block row i of A read
         if (act) {
             const float *trow = Am + (16 * i + r) * kAS + 16 * i;  // T_ii, zeros above its diagonal
+            float tr[16];
+#pragma unroll
+            for (int s4 = 0; s4 < 16; s4 += 4) {
+                const float4 tv4 = *reinterpret_cast<const float4 *>(trow + s4);
+                tr[s4] = tv4.x;
+                tr[s4 + 1] = tv4.y;
+                tr[s4 + 2] = tv4.z;
+                tr[s4 + 3] = tv4.w;
+            }
 #pragma unroll
             for (int j = 0; j < i; ++j) {
-                float2 a2 = make_float2(0.f, 0.f);
+                float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int s4 = 0; s4 < 16; s4 += 4) {
-                    const float4 tv4 = *reinterpret_cast<const float4 *>(trow + s4);
-                    const float te[4] = {tv4.x, tv4.y, tv4.z, tv4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 sv = *reinterpret_cast<const float2 *>(Am + (16 * i + s4 + e) * kAS + 16 * j + cp);
-                        a2.x = fmaf(te[e], sv.x, a2.x);
-                        a2.y = fmaf(te[e], sv.y, a2.y);
-                    }
+                for (int s = 0; s < 16; s += 2) {
+                    a0 = __ffma2_rn(make_float2(tr[s], tr[s]), *reinterpret_cast<const float2 *>(Sx + s * SXS + 16 * j + cp), a0);
+                    a1 = __ffma2_rn(make_float2(tr[s + 1], tr[s + 1]),
+                                    *reinterpret_cast<const float2 *>(Sx + (s + 1) * SXS + 16 * j + cp), a1);
                 }
-                acc[j] = make_float2(-a2.x, -a2.y);
+                const float2 t = __fadd2_rn(a0, a1);
+                *reinterpret_cast<float2 *>(Am + (16 * i + r) * kAS + 16 * j + cp) = make_float2(-t.x, -t.y);
             }
-        }
-        __syncthreads();  // S_i* read
-        if (act) {
-#pragma unroll
-            for (int j = 0; j < i; ++j) *reinterpret_cast<float2 *>(Am + (16 * i + r) * kAS + 16 * j + cp) = acc[j];
         }
         __syncthreads();  // block row i of T in place
     }
@@ -235,7 +236,6 @@ __global__ void __launch_bounds__(kDlThreads, 2) delta_fwd_kernel(const DeltaArg
             cp_async4(smem_u32(st + C::OFF_B + i * 4), Bb + (ok ? t : 0), ok ? 4u : 0u);
         }
     };
-
     // state fragments: warp w owns rows 16(w S_MT + mi) + {g, g + 8}
     constexpr int S_MT = C::S_MT;
     float S[S_MT][8][4];
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kDlThreads, 2) delta_fwd_kernel(const DeltaArg
         __syncthreads();
         // ---- T = (I + A)^-1 (unit lower triangular) in place, then as two bf16 parts in the
         // [64][64] tiles: 16-byte chunks of 8 columns, four per thread
-        tri_inverse_blocked(Am, tid);
+        tri_inverse_blocked(Am, reinterpret_cast<float *>(smem + C::OFF_TH), tid);  // scratch: T's tiles, free until below
 #pragma unroll
         for (int it = 0; it < kDlTc * 8 / kDlThreads; ++it) {
             const int task = tid + it * kDlThreads, r = task >> 3, c8 = task & 7;
@@ -677,7 +677,7 @@ struct DeltaBwdCfg {
     static constexpr int SMEM = OFF_RED + 64;
     static constexpr int S_MT = DK / 64;  // 16-row tiles of the state per row group
     static_assert(2 * V_BYTES <= E_BYTES, "F fits where E was");
-    static_assert(E_BYTES <= 4 * V_BYTES, "the fp32 inverse fits over U's and diag(w) U's tiles");
+    static_assert(E_BYTES + 16 * 48 * 4 <= 4 * V_BYTES, "the fp32 inverse and its scratch fit over U's tiles");
     static_assert(E_BYTES % 128 == 0, "tiles after E stay 128-byte aligned");
     static_assert(SMEM + 1024 <= 227 * 1024, "one block per SM");
 };
@@ -762,11 +762,19 @@ __global__ void __launch_bounds__(kDlBwdThreads, 1) delta_bwd_kernel(const Delta
             cp_async4(smem_u32(smem + C::OFF_L + i * 4), Lb + (ok ? t : 0), ok ? 4u : 0u);
             cp_async4(smem_u32(smem + C::OFF_B + i * 4), Bb + (ok ? t : 0), ok ? 4u : 0u);
         }
-        // the state entering the chunk, fp32 -> two bf16 parts (plain loads, read once)
+        // the state entering the chunk, fp32 -> two bf16 parts (plain loads, read once; all of a
+        // thread's loads issued before the first is used)
         const float *sg = p.states + ((size_t)bh * p.n_chunks + chunk) * DK * p.DV + zb * 64;
-        for (int i = tid; i < DK * 16; i += kDlBwdThreads) {
-            const int row = i >> 4, c4 = i & 15;
-            const float4 x = __ldcs(reinterpret_cast<const float4 *>(sg + (size_t)row * p.DV + c4 * 4));
+        float4 xs[DK * 16 / kDlBwdThreads];
+#pragma unroll
+        for (int it = 0; it < DK * 16 / kDlBwdThreads; ++it) {
+            const int i = tid + it * kDlBwdThreads, row = i >> 4, c4 = i & 15;
+            xs[it] = __ldcs(reinterpret_cast<const float4 *>(sg + (size_t)row * p.DV + c4 * 4));
+        }
+#pragma unroll
+        for (int it = 0; it < DK * 16 / kDlBwdThreads; ++it) {
+            const int i = tid + it * kDlBwdThreads, row = i >> 4, c4 = i & 15;
+            const float4 x = xs[it];
             uint2 hi, lo;
             split_bf16x2(make_float2(x.x, x.y), hi.x, lo.x);
             split_bf16x2(make_float2(x.z, x.w), hi.y, lo.y);
@@ -774,6 +782,27 @@ __global__ void __launch_bounds__(kDlBwdThreads, 1) delta_bwd_kernel(const Delta
             *reinterpret_cast<uint2 *>(smem + C::OFF_SH + off) = hi;
             *reinterpret_cast<uint2 *>(smem + C::OFF_SL + off) = lo;
         }
+    };
+    // the lines load_stage(chunk) reads, pulled into L2 one chunk ahead (three or so a thread)
+    auto prefetch_stage = [&](int chunk) {
+        const long long t0 = (long long)chunk * kDlTc;
+        const int nrow = (int)min((long long)kDlTc, p.T - t0);
+        constexpr int QL = C::QRB / 128;  // 128-byte lines of a Q / K row
+        for (int i = tid; i < nrow * QL; i += kDlBwdThreads) {
+            const size_t off = (size_t)(t0 + i / QL) * DK + (i % QL) * 64;
+            prefetch_l2(Qb + off);
+            prefetch_l2(Kb + off);
+        }
+        for (int i = tid; i < nrow; i += kDlBwdThreads) {
+            prefetch_l2(Vb + (size_t)(t0 + i) * p.DV);
+            prefetch_l2(dOb + (size_t)(t0 + i) * p.DV);
+        }
+        if (tid < 2 && 32 * tid < nrow) {
+            prefetch_l2(Lb + t0 + 32 * tid);
+            prefetch_l2(Bb + t0 + 32 * tid);
+        }
+        const float *sg = p.states + ((size_t)bh * p.n_chunks + chunk) * DK * p.DV + zb * 64;
+        for (int i = tid; i < DK * 2; i += kDlBwdThreads) prefetch_l2(sg + (size_t)(i >> 1) * p.DV + (i & 1) * 32);
     };
 
     // adjoint state fragments: rows 16(wr S_MT + mi) + {g, g + 8}, columns 8(4 hf + nj) + 2 tq + {0, 1}
@@ -865,6 +894,7 @@ __global__ void __launch_bounds__(kDlBwdThreads, 1) delta_bwd_kernel(const Delta
     cp_async_commit();
     for (int i = p.n_chunks - 1; i >= 0; --i) {
         const long long t0 = (long long)i * kDlTc;
+        if (i > 0) prefetch_stage(i - 1);
         // dS' (the adjoint of the state leaving chunk i) as two bf16 parts
 #pragma unroll
         for (int mi = 0; mi < S_MT; ++mi)
@@ -938,7 +968,7 @@ __global__ void __launch_bounds__(kDlBwdThreads, 1) delta_bwd_kernel(const Delta
                 *reinterpret_cast<float4 *>(Aw + r * kAS + 4 * c4) = make_float4(b * e.x, b * e.y, b * e.z, b * e.w);
             }
             __syncthreads();
-            tri_inverse_blocked(Aw, tid);
+            tri_inverse_blocked(Aw, Aw + kDlTc * kAS, tid);  // scratch: after A, still over U's tiles
 #pragma unroll
             for (int it = 0; it < kDlTc * 8 / kDlBwdThreads; ++it) {
                 const int task = tid + it * kDlBwdThreads, r = task >> 3, c8 = task & 7;
