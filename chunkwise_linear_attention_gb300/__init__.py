@@ -23,7 +23,7 @@ _lock = threading.Lock()
 _lib = None
 
 CLA_OK = 0
-SELECTIVE_CKPT_CHUNK = 64
+SELECTIVE_CKPT_CHUNK = 16
 
 
 class ClaError(RuntimeError):

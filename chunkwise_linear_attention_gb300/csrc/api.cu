@@ -36,6 +36,17 @@ int set_max_dynamic_smem(std::atomic<unsigned long long> &done, const void *func
     return CLA_OK;
 }
 
+int set_smem_carveout_max(std::atomic<unsigned long long> &done, const void *func) {
+    int dev = 0;
+    CLA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit != 0ull && (done.load(std::memory_order_acquire) & bit) != 0ull) return CLA_OK;
+    CLA_CUDA_TRY(cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, 100),
+                 "cudaFuncSetAttribute");
+    done.fetch_or(bit, std::memory_order_acq_rel);
+    return CLA_OK;
+}
+
 }  // namespace cla
 
 extern "C" const char *cla_status_string(int status) {

@@ -23,6 +23,9 @@ void clear_error();
 // Raises func's dynamic shared memory limit to `bytes` on the current device,
 // once per device: `done` (one per kernel) keeps a bit per device ordinal.
 int set_max_dynamic_smem(std::atomic<unsigned long long> &done, const void *func, int bytes);
+// Asks for the largest shared-memory carveout for func (once per device, as above), for
+// kernels whose resident blocks per SM are bounded by shared memory.
+int set_smem_carveout_max(std::atomic<unsigned long long> &done, const void *func);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -36,6 +36,7 @@
 
 #include "cla_internal.cuh"
 #include "exp2_fma.cuh"
+#include "mma_sync.cuh"
 
 namespace cla {
 namespace {
@@ -43,7 +44,9 @@ namespace {
 typedef __nv_bfloat16 bf16;
 
 constexpr int kN = 16;        // state entries per channel
-constexpr int kTc = CLA_SELECTIVE_CKPT_CHUNK;  // 64 steps per chunk
+constexpr int kTc = 64;       // steps per chunk of the chunk-parallel kernels
+constexpr int kCk = CLA_SELECTIVE_CKPT_CHUNK;  // steps between saved states (16)
+static_assert(kTc % kCk == 0, "a chunk holds whole checkpoint intervals");
 constexpr int kCh = 128;      // channels per block (forward)
 constexpr int kChB = 64;      // channels per block (backward; measured: 5% faster than 128 there,
                               // 1.4% slower in the forward)
@@ -54,6 +57,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct SelGeom {
     int B, D, n_chunks, n_cblk;
     long long T;
+    long long n_ck;  // saved states per batch row: ceil(T / kCk)
 };
 
 struct SelWs {
@@ -215,17 +219,18 @@ sel_fwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
         __syncthreads();
         if (tid == 0) st_release(ws.flags + unit, 2u);
     }
-    if (ckpt != nullptr && cok) {
-        float4 *ck = reinterpret_cast<float4 *>(ckpt + (((size_t)bi * g.n_chunks + chunk) * g.D + c) * kN);
-#pragma unroll
-        for (int q = 0; q < kN / 4; ++q) ck[q] = make_float4(hin[4 * q], hin[4 * q + 1], hin[4 * q + 2], hin[4 * q + 3]);
-    }
-
-    // phase 2: re-run from the true incoming state; write y once
+    // phase 2: re-run from the true incoming state; write y once, and the state entering
+    // every kCk-step interval for the backward
     float2 hp[kJ];
 #pragma unroll
     for (int j = 0; j < kJ; ++j) hp[j] = make_float2(hin[2 * j], hin[2 * j + 1]);
     for (int r = 0; r < L; ++r) {
+        if (ckpt != nullptr && cok && (r % kCk) == 0) {
+            float4 *ck = reinterpret_cast<float4 *>(ckpt + (((size_t)bi * g.n_ck + (t0 + r) / kCk) * g.D + c) * kN);
+#pragma unroll
+            for (int q = 0; q < kN / 4; ++q)
+                ck[q] = make_float4(hp[2 * q].x, hp[2 * q].y, hp[2 * q + 1].x, hp[2 * q + 1].y);
+        }
         const float d = s_d[r][tid];
         const float dx = d * __bfloat162float(s_x[r][tid]);
         const float2 *Br = reinterpret_cast<const float2 *>(s_B[r]);
@@ -248,6 +253,209 @@ sel_fwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
         for (int j = 0; j < kJ; ++j) {
             hT[((size_t)bi * g.D + c) * kN + 2 * j] = hp[j].x;
             hT[((size_t)bi * g.D + c) * kN + 2 * j + 1] = hp[j].y;
+        }
+    }
+}
+
+// ------------------------------------------------- forward, one walk per channel
+// With many channels (B * D) the chunk look-back is not needed to fill the GPU,
+// and it costs a second evaluation of every decay (phase 1 folds a chunk, phase 2
+// re-runs it).  This kernel walks each channel's whole sequence once.  A block
+// owns 8 channels of one batch row; LANES lanes of a warp share a channel, lane
+// LANES j + q holding state entries (16 / LANES) q.. of channel j.  Inputs are
+// staged 64 steps at a time by cp.async (two buffers); a pass over each staged
+// tile turns it into fp32 (delta, delta x) pairs per channel and fp32
+// (B_n, B_n+1, C_n, C_n+1) quadruples per entry pair.  y_t sums a channel's 16
+// entries over its lanes, LANES steps at a time: after the exchange lane q holds
+// step q's sum.
+constexpr int kSqCh = 8;                  // channels per block
+constexpr int kSqTile = 64;               // steps per staged tile
+static_assert(kSqTile % kCk == 0 && kCk % 8 == 0, "checkpoints fall on whole step groups of a tile");
+
+struct SelSeqSmem {
+    float d[2][kSqTile][kSqCh];       // staged delta
+    bf16 x[2][kSqTile][kSqCh];        // staged x
+    bf16 B[2][kSqTile][kN];           // staged B_t, C_t rows
+    bf16 C[2][kSqTile][kN];
+    float2 ddx[kSqTile][kSqCh];       // (delta, delta x) of the tile being walked
+    float4 bc[kSqTile][kN / 2];       // (B_2p, B_2p+1, C_2p, C_2p+1) of the tile being walked
+};
+
+struct SelSeqGeom {
+    int B, D;
+    long long T, n_ck;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+template <int NT>
+__device__ __forceinline__ void sel_seq_stage(SelSeqSmem &sm, int buf, const bf16 *x, const float *delta,
+                                              const bf16 *Bm, const bf16 *Cm, const SelSeqGeom &g, int bi, int c0,
+                                              long long t0, int tid) {
+    const int L = (int)min((long long)kSqTile, g.T - t0);
+    const size_t row0 = (size_t)bi * g.T + t0;
+#pragma unroll
+    for (int i = tid; i < kSqTile * 2; i += NT) {  // delta: 64 rows x two 16-byte pieces
+        const int r = i >> 1, h = i & 1;
+        if (r < L) cp_async16(smem_u32(&sm.d[buf][r][4 * h]), delta + (row0 + r) * g.D + c0 + 4 * h, 16u);
+    }
+#pragma unroll
+    for (int r = tid; r < kSqTile; r += NT)  // x: 64 rows x one 16-byte piece
+        if (r < L) cp_async16(smem_u32(&sm.x[buf][r][0]), x + (row0 + r) * g.D + c0, 16u);
+#pragma unroll
+    for (int i = tid; i < kSqTile * 2; i += NT) {  // B_t, C_t: 64 rows x two 16-byte pieces each
+        const int r = i >> 1, h = i & 1;
+        if (r < L) {
+            cp_async16(smem_u32(&sm.B[buf][r][8 * h]), Bm + (row0 + r) * kN + 8 * h, 16u);
+            cp_async16(smem_u32(&sm.C[buf][r][8 * h]), Cm + (row0 + r) * kN + 8 * h, 16u);
+        }
+    }
+    cp_async_commit();
+}
+
+// Converts staged tile `buf` (rows past the sequence's end become delta = 0, which
+// makes the step the identity: a = 1, b = 0) and returns whether every step of it
+// satisfies |delta| * amax <= 126 (then 2^x needs no clamp).
+template <int NT>
+__device__ __forceinline__ bool sel_seq_convert(SelSeqSmem &sm, int buf, int L, float amax, int tid) {
+    bool ok = true;
+#pragma unroll
+    for (int i = tid; i < kSqTile * kSqCh; i += NT) {
+        const int r = i / kSqCh, cc = i % kSqCh;
+        const float d = r < L ? sm.d[buf][r][cc] : 0.f;
+        const float xv = r < L ? __bfloat162float(sm.x[buf][r][cc]) : 0.f;
+        sm.ddx[r][cc] = make_float2(d, d * xv);
+        ok = ok && (fabsf(d) * amax <= 126.f);
+    }
+    const uint32_t *Bw = reinterpret_cast<const uint32_t *>(sm.B[buf]);
+    const uint32_t *Cw = reinterpret_cast<const uint32_t *>(sm.C[buf]);
+    float4 *bc = &sm.bc[0][0];
+#pragma unroll
+    for (int i = tid; i < kSqTile * kN / 2; i += NT) {
+        const int r = i / (kN / 2);
+        const uint32_t bw = r < L ? Bw[i] : 0u, cw = r < L ? Cw[i] : 0u;
+        bc[i] = make_float4(bf16_lo(bw), bf16_hi(bw), bf16_lo(cw), bf16_hi(cw));
+    }
+    return __syncthreads_and(ok) != 0;
+}
+
+template <int LANES>
+__global__ void __launch_bounds__(kSqCh * LANES)
+sel_fwd_seq_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, const float *__restrict__ A,
+                   const bf16 *__restrict__ Bm, const bf16 *__restrict__ Cm, const float *__restrict__ h0,
+                   float *__restrict__ y, float *__restrict__ hT, float *__restrict__ ckpt, SelSeqGeom g) {
+    constexpr int NT = kSqCh * LANES;
+    constexpr int NP = kN / LANES / 2;  // entry pairs per lane
+    constexpr int G = LANES;            // steps per output exchange
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SelSeqSmem &sm = *reinterpret_cast<SelSeqSmem *>(smem_raw);
+    const int tid = threadIdx.x;
+    const int bpr = g.D / kSqCh;  // blocks per batch row
+    const int bi = (int)(blockIdx.x / bpr);
+    const int c0 = (int)(blockIdx.x % bpr) * kSqCh;
+    const int j = tid / LANES, q = tid % LANES;
+    const int c = c0 + j, p0 = q * NP;  // this lane's first entry pair
+
+    float2 A2p[NP];
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        A2p[k] = make_float2(A[(size_t)c * kN + 2 * (p0 + k)] * kLog2e, A[(size_t)c * kN + 2 * (p0 + k) + 1] * kLog2e);
+        amax = fmaxf(amax, fmaxf(fabsf(A2p[k].x), fabsf(A2p[k].y)));
+    }
+    {  // the block's largest |A| log2(e): the clamp test of a tile covers every channel of the block
+        __shared__ float s_amax[NT / 32];
+        s_amax[tid / 32] = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < NT / 32; ++w) amax = fmaxf(amax, s_amax[w]);
+    }
+    float2 h[NP];
+#pragma unroll
+    for (int k = 0; k < NP; ++k)
+        h[k] = h0 != nullptr ? make_float2(h0[((size_t)bi * g.D + c) * kN + 2 * (p0 + k)],
+                                           h0[((size_t)bi * g.D + c) * kN + 2 * (p0 + k) + 1])
+                             : f2(0.f);
+
+    const int n_tiles = (int)((g.T + kSqTile - 1) / kSqTile);
+    sel_seq_stage<NT>(sm, 0, x, delta, Bm, Cm, g, bi, c0, 0, tid);
+    for (int tile = 0; tile < n_tiles; ++tile) {
+        const int buf = tile & 1;
+        const long long t0 = (long long)tile * kSqTile;
+        if (tile + 1 < n_tiles) {
+            sel_seq_stage<NT>(sm, buf ^ 1, x, delta, Bm, Cm, g, bi, c0, t0 + kSqTile, tid);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();  // this tile's copies from every thread; the previous walk's reads done
+        const int L = (int)min((long long)kSqTile, g.T - t0);
+        const bool noclamp = sel_seq_convert<NT>(sm, buf, L, amax, tid);  // ends with a barrier
+        auto walk = [&](auto clamp) {
+            constexpr bool CL = decltype(clamp)::value;
+#pragma unroll 2
+            for (int s16 = 0; s16 < kSqTile; s16 += kCk) {
+                if (ckpt != nullptr && t0 + s16 < g.T) {
+                    float *ck = ckpt + (((size_t)bi * g.n_ck + (t0 + s16) / kCk) * g.D + c) * kN + 2 * p0;
+                    if constexpr (NP == 2) {
+                        *reinterpret_cast<float4 *>(ck) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+                    } else {
+                        *reinterpret_cast<float2 *>(ck) = h[0];
+                    }
+                }
+#pragma unroll
+                for (int sg = 0; sg < kCk; sg += G) {
+                    // the group's decays and inputs first (independent of the state), then
+                    // the state recurrence through them
+                    float2 a[G][NP], bx[G][NP], cc[G][NP];
+#pragma unroll
+                    for (int u = 0; u < G; ++u) {
+                        const int r = s16 + sg + u;
+                        const float2 dd = sm.ddx[r][j];
+#pragma unroll
+                        for (int k = 0; k < NP; ++k) {
+                            const float4 bcv = sm.bc[r][p0 + k];
+                            a[u][k] = exp2_fma2<CL>(__fmul2_rn(f2(dd.x), A2p[k]));
+                            bx[u][k] = __fmul2_rn(f2(dd.y), make_float2(bcv.x, bcv.y));
+                            cc[u][k] = make_float2(bcv.z, bcv.w);
+                        }
+                    }
+                    float v[G];
+#pragma unroll
+                    for (int u = 0; u < G; ++u) {
+                        float2 acc = f2(0.f);
+#pragma unroll
+                        for (int k = 0; k < NP; ++k) {
+                            h[k] = __ffma2_rn(a[u][k], h[k], bx[u][k]);
+                            acc = __ffma2_rn(cc[u][k], h[k], acc);
+                        }
+                        v[u] = acc.x + acc.y;
+                    }
+                    // sum over the channel's lanes; lane q ends with step q's total
+#pragma unroll
+                    for (int m = G / 2; m >= 1; m >>= 1) {
+                        const bool up = q & m;
+#pragma unroll
+                        for (int i = 0; i < m; ++i) {
+                            const float keep = up ? v[i + m] : v[i];
+                            const float send = up ? v[i] : v[i + m];
+                            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                        }
+                    }
+                    const long long t = t0 + s16 + sg + q;
+                    if (t < g.T) __stcs(y + ((size_t)bi * g.T + t) * g.D + c, v[0]);
+                }
+            }
+        };
+        if (noclamp) walk(std::false_type{});
+        else walk(std::true_type{});
+    }
+    if (hT != nullptr) {
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+            hT[((size_t)bi * g.D + c) * kN + 2 * (p0 + k)] = h[k].x;
+            hT[((size_t)bi * g.D + c) * kN + 2 * (p0 + k) + 1] = h[k].y;
         }
     }
 }
@@ -355,7 +563,7 @@ sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
     // pass A: states (every 8th kept) and the adjoint pair of the chunk
     float h[kNh], P[kNh], Bg[kNh];
     {
-        const float *ck = ckpt + (((size_t)bi * g.n_chunks + chunk) * g.D + (cok ? c : 0)) * kN + n0;
+        const float *ck = ckpt + (((size_t)bi * g.n_ck + (long long)chunk * (kTc / kCk)) * g.D + (cok ? c : 0)) * kN + n0;
         float2 hq[kJh], Pq[kJh], Bq[kJh];
 #pragma unroll
         for (int j = 0; j < kJh; ++j) {
@@ -643,6 +851,7 @@ SelPlan sel_plan(int64_t B, int64_t T, int64_t D) {
     p.g.D = (int)D;
     p.g.T = T;
     p.g.n_chunks = (int)((T + kTc - 1) / kTc);
+    p.g.n_ck = (T + kCk - 1) / kCk;
     p.g.n_cblk = (int)((D + kCh - 1) / kCh);
     p.gb = p.g;
     p.gb.n_cblk = (int)((D + kChB - 1) / kChB);
@@ -679,6 +888,21 @@ bool sel_sizes_fit(int64_t B, int64_t T, int64_t D) {
     return product_below({(T + kTc - 1) / kTc, B, (D + kChB - 1) / kChB}, 2147483648.0);
 }
 
+// The one-walk-per-channel forward is taken when its warps (one per 4 channels of a
+// batch row) give every SM at least four, so that a walk's dependent steps overlap
+// other warps' work; it needs 16-byte aligned rows for its staged copies.
+constexpr int kSqLanes = 8;  // lanes per channel (2 entries each): two warps per block
+bool sel_use_seq(int64_t B, int64_t D, const void *x, const void *delta, const void *Bm, const void *Cm) {
+    if (D % kSqCh != 0 || !aligned16(x) || !aligned16(delta) || !aligned16(Bm) || !aligned16(Cm)) return false;
+    const double blocks = (double)B * (double)(D / kSqCh);
+    if (blocks >= 2147483648.0) return false;
+    const double warps = blocks * kSqCh * kSqLanes / 32;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    return warps >= 4.0 * sms;
+}
+
 int sel_validate(const char *fn, int64_t B, int64_t T, int64_t D, int64_t N) {
     if (B < 0 || T < 0 || D < 0 || N < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
     if (N != kN) return fail(CLA_ERR_UNSUPPORTED, "%s: N must be %d (got %lld)", fn, kN, (long long)N);
@@ -698,7 +922,7 @@ extern "C" size_t cla_selective_scan_workspace_size(int64_t B, int64_t T, int64_
 
 extern "C" size_t cla_selective_scan_ckpt_elems(int64_t B, int64_t T, int64_t D, int64_t N) {
     if (B < 0 || T < 0 || D < 0 || N != kN || !sel_sizes_fit(B, T, D)) return 0;
-    return (size_t)B * (size_t)((T + kTc - 1) / kTc) * (size_t)D * (size_t)N;
+    return (size_t)B * (size_t)((T + kCk - 1) / kCk) * (size_t)D * (size_t)N;
 }
 
 extern "C" int cla_selective_scan_fwd(const uint16_t *x, const float *delta, const float *A, const uint16_t *Bm,
@@ -727,6 +951,18 @@ extern "C" int cla_selective_scan_fwd(const uint16_t *x, const float *delta, con
     const SelPlan p = sel_plan(B, T, D);
     if (ws_bytes < p.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, p.total);
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.off_agg, s), fn);
+    if (sel_use_seq(B, D, x, delta, Bm, Cm)) {
+        // one-warp blocks: as many per SM as shared memory holds (all of it as shared memory)
+        static std::atomic<unsigned long long> carve_set{0};
+        st = set_smem_carveout_max(carve_set, reinterpret_cast<const void *>(sel_fwd_seq_kernel<kSqLanes>));
+        if (st) return st;
+        const SelSeqGeom sg{(int)B, (int)D, T, p.g.n_ck};
+        const unsigned int grid = (unsigned int)(B * (D / kSqCh));
+        sel_fwd_seq_kernel<kSqLanes><<<grid, kSqCh * kSqLanes, sizeof(SelSeqSmem), s>>>(
+            reinterpret_cast<const bf16 *>(x), delta, A, reinterpret_cast<const bf16 *>(Bm),
+            reinterpret_cast<const bf16 *>(Cm), h0, y, hT, ckpt, sg);
+        return check_launch(fn);
+    }
     const SelWs w = sel_bind(p, ws);
     static std::atomic<unsigned long long> smem_set{0};
     st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(sel_fwd_kernel), (int)sizeof(SelFwdSmem));

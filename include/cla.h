@@ -177,12 +177,12 @@ int cla_scan_diag_noalloc_check_status(void *stream);
 /* ======================================================================== */
 
 /* Time steps between the states saved by the forward for the backward. */
-#define CLA_SELECTIVE_CKPT_CHUNK 64
+#define CLA_SELECTIVE_CKPT_CHUNK 16
 
 /* Bytes of workspace for cla_selective_scan_fwd / _bwd. */
 size_t cla_selective_scan_workspace_size(int64_t B, int64_t T, int64_t D, int64_t N);
 
-/* Elements of the checkpoint tensor [B, ceil(T/64), D, N] (fp32). */
+/* Elements of the checkpoint tensor [B, ceil(T/16), D, N] (fp32). */
 size_t cla_selective_scan_ckpt_elems(int64_t B, int64_t T, int64_t D, int64_t N);
 
 /* Forward: per channel d and state entry n, h_{t,d,n} = a h_{t-1,d,n} + b with
@@ -194,8 +194,8 @@ size_t cla_selective_scan_ckpt_elems(int64_t B, int64_t T, int64_t D, int64_t N)
  *   Bm, Cm [B, T, N] bf16,  h0 [B, D, N] fp32 [opt]
  *   y      [B, T, D] fp32   out
  *   hT     [B, D, N] fp32   [opt] out
- *   ckpt   [B, ceil(T/64), D, N] fp32 [opt] out: the state entering every
- *          64-step chunk, consumed by the backward
+ *   ckpt   [B, ceil(T/16), D, N] fp32 [opt] out: the state entering every
+ *          16-step interval, consumed by the backward
  * N must be 16 in this build. */
 int cla_selective_scan_fwd(const uint16_t *x, const float *delta, const float *A,
                            const uint16_t *Bm, const uint16_t *Cm, const float *h0,

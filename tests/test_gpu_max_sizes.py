@@ -75,12 +75,16 @@ def test_chunk_la_beyond_int32_elements(cla):
         assert_bf16(f"dlog_a[head {hd}]", tail(dl)[..., 1:], rdl[..., 1:])
 
 
-def test_selective_beyond_int32_elements(cla):
-    """B=1, T = 2^20 + 37, D = 2048, N = 16: 2^31 + 75776 (t, d) elements (and 16 times as many
-    state entries).  Channels are independent in y, dx, dDelta and dA, so three whole channels
+# B = 1: the chunk look-back forward; B = 3 (6144 channels): the forward walking each
+# channel's whole sequence once
+@pytest.mark.parametrize("B,T", [(1, (1 << 20) + 37), (3, 350021)])
+def test_selective_beyond_int32_elements(cla, B, T):
+    """D = 2048, N = 16: B T D above 2^31 (t, d) elements (and 16 times as many state
+    entries).  Channels are independent in y, dx, dDelta and dA, so three whole channels
     are checked; dB and dC sum over every channel and are left to the full-workload test."""
     dev = torch.device("cuda")
-    B, T, D, N = 1, (1 << 20) + 37, 2048, 16
+    D, N = 2048, 16
+    assert B * T * D > (1 << 31)
     t = workloads.selective_inputs_device(B, T, D, N, seed=23, device=dev)
     y, hT, ck = cla.selective_scan_fwd(t["x"], t["delta"], t["A"], t["Bm"], t["Cm"], None)
     dx, dd, dA, dB, dC, dh0 = cla.selective_scan_bwd(t["x"], t["delta"], t["A"], t["Bm"], t["Cm"], None, ck, t["dy"])
