@@ -47,6 +47,12 @@ __device__ __forceinline__ float exp2_fma(float x) {
 // (add / mul / fma on float2) round each lane exactly as the scalar ones, so
 // the results equal exp2_fma's; the instruction count is about halved.
 // CLAMP = false: the caller guarantees |x| <= 126 (then the clamp changes nothing).
+__device__ __forceinline__ uint32_t mad_u32(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 template <bool CLAMP = true>
 __device__ __forceinline__ float2 exp2_fma2(float2 x) {
     constexpr float kMagic = 12582912.0f;
@@ -69,8 +75,9 @@ __device__ __forceinline__ float2 exp2_fma2(float2 x) {
         // km hold k; shifted left by 23 the rest of km's bits leave the word.  Exact, as the
         // multiply by 2^k below is, except that results under 2^-126 come out as subnormals
         // read from the wrong field (absolute error below 2^-126).
-        return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(km.x) << 23)),
-                           __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(km.y) << 23)));
+        // One integer multiply-add per lane: km * 2^23 + p (the same bits as the shift and add).
+        return make_float2(__uint_as_float(mad_u32(__float_as_uint(km.x), 1u << 23, __float_as_uint(p.x))),
+                           __uint_as_float(mad_u32(__float_as_uint(km.y), 1u << 23, __float_as_uint(p.y))));
     }
     const int ex = (__float_as_int(km.x) - __float_as_int(kMagic)) + 127;
     const int ey = (__float_as_int(km.y) - __float_as_int(kMagic)) + 127;

@@ -786,6 +786,228 @@ sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
     }
 }
 
+// ------------------------------------------------ backward, one walk per channel
+// The counterpart of sel_fwd_seq_kernel: with many channels each block walks its 8
+// channels of one batch row from the last step to the first, so no look-back over
+// later chunks is needed, and the saved states (one every kCk = 16 steps) let every
+// 16-step interval be recomputed forward once -- decays and states kept in registers
+// -- before the adjoint runs back through it: one decay evaluation per state update
+// (the chunk-parallel backward needs two).  Inputs are staged 32 steps at a time by
+// cp.async (two buffers) and converted to fp32 (delta, delta x, x, dy) per channel and
+// (B, C) per entry pair.  The sums over a channel's entries (dx, ddelta) and over the
+// block's channels (dB, dC) go through shared memory every 8 steps, in a fixed order;
+// the block's dB, dC partials are summed over blocks by sel_reduce_bc_kernel.
+constexpr int kSbTile = 32;  // steps per staged tile
+constexpr int kSbGrp = 8;    // steps per exchange of the sums
+static_assert(kSbTile % kCk == 0 && kCk % kSbGrp == 0, "tiles hold whole recompute intervals");
+
+struct SelSeqBwdSmem {
+    float d[2][kSbTile][kSqCh];      // staged delta, x, dy, B_t, C_t
+    bf16 x[2][kSbTile][kSqCh];
+    float dy[2][kSbTile][kSqCh];
+    bf16 B[2][kSbTile][kN];
+    bf16 C[2][kSbTile][kN];
+    float4 dxy[kSbTile][kSqCh];      // (delta, delta x, x, dy) of the tile being walked
+    float4 bc[kSbTile][kN / 2];      // (B_2p, B_2p+1, C_2p, C_2p+1)
+    float4 rbc[kSbGrp][kSqCh][kN / 2];  // per step: dB, dC terms of channel j, entry pair p
+    float2 rxd[kSbGrp][kSqCh][8 + 1];   // per step: channel j's lane q terms of dx / delta, ddelta
+                                        // (rows padded: the channel sums read them across rows)
+};
+
+__device__ __forceinline__ void sel_seqb_stage(SelSeqBwdSmem &sm, int buf, const bf16 *x, const float *delta,
+                                               const float *dy, const bf16 *Bm, const bf16 *Cm,
+                                               const SelSeqGeom &g, int bi, int c0, long long t0, int tid) {
+    constexpr int NT = kSqCh * 8;
+    const int L = (int)min((long long)kSbTile, g.T - t0);
+    const size_t row0 = (size_t)bi * g.T + t0;
+#pragma unroll
+    for (int i = tid; i < kSbTile * 2; i += NT) {  // delta, dy: 32 rows x two 16-byte pieces
+        const int r = i >> 1, h = i & 1;
+        if (r < L) {
+            cp_async16(smem_u32(&sm.d[buf][r][4 * h]), delta + (row0 + r) * g.D + c0 + 4 * h, 16u);
+            cp_async16(smem_u32(&sm.dy[buf][r][4 * h]), dy + (row0 + r) * g.D + c0 + 4 * h, 16u);
+        }
+    }
+#pragma unroll
+    for (int r = tid; r < kSbTile; r += NT)  // x: one 16-byte piece per row
+        if (r < L) cp_async16(smem_u32(&sm.x[buf][r][0]), x + (row0 + r) * g.D + c0, 16u);
+#pragma unroll
+    for (int i = tid; i < kSbTile * 2; i += NT) {  // B_t, C_t: two 16-byte pieces each per row
+        const int r = i >> 1, h = i & 1;
+        if (r < L) {
+            cp_async16(smem_u32(&sm.B[buf][r][8 * h]), Bm + (row0 + r) * kN + 8 * h, 16u);
+            cp_async16(smem_u32(&sm.C[buf][r][8 * h]), Cm + (row0 + r) * kN + 8 * h, 16u);
+        }
+    }
+    cp_async_commit();
+}
+
+// As sel_seq_convert: rows past the end become delta = dy = x = 0 and B = C = 0, which
+// leaves the adjoint unchanged through them and adds nothing to any gradient.
+__device__ __forceinline__ bool sel_seqb_convert(SelSeqBwdSmem &sm, int buf, int L, float amax, int tid) {
+    constexpr int NT = kSqCh * 8;
+    bool ok = true;
+#pragma unroll
+    for (int i = tid; i < kSbTile * kSqCh; i += NT) {
+        const int r = i / kSqCh, cc = i % kSqCh;
+        const float d = r < L ? sm.d[buf][r][cc] : 0.f;
+        const float xv = r < L ? __bfloat162float(sm.x[buf][r][cc]) : 0.f;
+        const float g = r < L ? sm.dy[buf][r][cc] : 0.f;
+        sm.dxy[r][cc] = make_float4(d, d * xv, xv, g);
+        ok = ok && (fabsf(d) * amax <= 126.f);
+    }
+    const uint32_t *Bw = reinterpret_cast<const uint32_t *>(sm.B[buf]);
+    const uint32_t *Cw = reinterpret_cast<const uint32_t *>(sm.C[buf]);
+    float4 *bc = &sm.bc[0][0];
+#pragma unroll
+    for (int i = tid; i < kSbTile * kN / 2; i += NT) {
+        const int r = i / (kN / 2);
+        const uint32_t bw = r < L ? Bw[i] : 0u, cw = r < L ? Cw[i] : 0u;
+        bc[i] = make_float4(bf16_lo(bw), bf16_hi(bw), bf16_lo(cw), bf16_hi(cw));
+    }
+    return __syncthreads_and(ok) != 0;
+}
+
+// 8 lanes per channel (entries 2q, 2q + 1 on lane q), 8 channels per block.
+__global__ void __launch_bounds__(kSqCh * 8, 7)
+sel_bwd_seq_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, const float *__restrict__ A,
+                   const bf16 *__restrict__ Bm, const bf16 *__restrict__ Cm, const float *__restrict__ ckpt,
+                   const float *__restrict__ dy, const float *__restrict__ dhT, float *__restrict__ dx,
+                   float *__restrict__ ddelta, float *__restrict__ dh0, float *__restrict__ partB,
+                   float *__restrict__ partC, float *__restrict__ partA, SelSeqGeom g) {
+    constexpr int NT = kSqCh * 8;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SelSeqBwdSmem &sm = *reinterpret_cast<SelSeqBwdSmem *>(smem_raw);
+    const int tid = threadIdx.x;
+    const int bpr = g.D / kSqCh;  // blocks per batch row
+    const int bi = (int)(blockIdx.x / bpr), blk = (int)(blockIdx.x % bpr);
+    const int c0 = blk * kSqCh;
+    const int j = tid >> 3, q = tid & 7;
+    const int c = c0 + j;
+
+    const float2 Ar = make_float2(A[(size_t)c * kN + 2 * q], A[(size_t)c * kN + 2 * q + 1]);
+    const float2 A2 = make_float2(Ar.x * kLog2e, Ar.y * kLog2e);
+    float amax = fmaxf(fabsf(A2.x), fabsf(A2.y));
+    {  // the block's largest |A| log2(e), as in the forward
+        __shared__ float s_amax[NT / 32];
+        s_amax[tid / 32] = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < NT / 32; ++w) amax = fmaxf(amax, s_amax[w]);
+    }
+    const size_t sidx = ((size_t)bi * g.D + c) * kN + 2 * q;  // this lane's entries in [B, D, N]
+    float2 hb = dhT != nullptr ? make_float2(dhT[sidx], dhT[sidx + 1]) : f2(0.f);
+    // dA over the whole walk: summed per 16-step interval, the interval sums added with
+    // compensation (a plain running fp32 sum over thousands of steps drifts past 1e-5)
+    float2 anext = f2(1.f), dA_acc = f2(0.f), dA_cmp = f2(0.f);
+
+    const int n_tiles = (int)((g.T + kSbTile - 1) / kSbTile);
+    // the saved state entering the interval walked next, loaded one interval ahead
+    const float *ckc = ckpt + ((size_t)bi * g.n_ck * g.D + c) * kN + 2 * q;
+    const size_t ck_stride = (size_t)g.D * kN;
+    long long ck_next = g.n_ck - 1;
+    float2 hin_next = *reinterpret_cast<const float2 *>(ckc + ck_next * ck_stride);
+    sel_seqb_stage(sm, (n_tiles - 1) & 1, x, delta, dy, Bm, Cm, g, bi, c0, (long long)(n_tiles - 1) * kSbTile, tid);
+    for (int tile = n_tiles - 1; tile >= 0; --tile) {
+        const int buf = tile & 1;
+        const long long t0 = (long long)tile * kSbTile;
+        if (tile > 0) {
+            sel_seqb_stage(sm, buf ^ 1, x, delta, dy, Bm, Cm, g, bi, c0, t0 - kSbTile, tid);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();  // this tile's copies from every thread; the previous tile's reads done
+        const int L = (int)min((long long)kSbTile, g.T - t0);
+        const bool noclamp = sel_seqb_convert(sm, buf, L, amax, tid);  // ends with a barrier
+        auto walk = [&](auto clamp) {
+            constexpr bool CL = decltype(clamp)::value;
+#pragma unroll 1
+            for (int s = kSbTile - kCk; s >= 0; s -= kCk) {
+                if (t0 + s >= g.T) continue;  // an interval wholly past the end (uniform)
+                // recompute the interval's decays and states from the saved state
+                const float2 hin = hin_next;  // intervals are walked in order: this is (t0 + s) / kCk
+                if (--ck_next >= 0) hin_next = *reinterpret_cast<const float2 *>(ckc + ck_next * ck_stride);
+                float2 as[kCk], hs[kCk];
+                {
+                    float2 h = hin;
+#pragma unroll
+                    for (int u = 0; u < kCk; ++u) {
+                        const float4 v = sm.dxy[s + u][j];
+                        const float4 b = sm.bc[s + u][q];
+                        as[u] = exp2_fma2<CL>(__fmul2_rn(f2(v.x), A2));
+                        h = __ffma2_rn(as[u], h, __fmul2_rn(f2(v.y), make_float2(b.x, b.y)));
+                        hs[u] = h;
+                    }
+                }
+                // the adjoint back through the interval, 8 steps per exchange of the sums
+                float2 dA_loc = f2(0.f);
+#pragma unroll
+                for (int gi = kCk / kSbGrp - 1; gi >= 0; --gi) {
+#pragma unroll
+                    for (int uu = kSbGrp - 1; uu >= 0; --uu) {
+                        const int u = gi * kSbGrp + uu, r = s + u;
+                        const float4 v = sm.dxy[r][j];  // (delta, delta x, x, dy)
+                        const float4 b = sm.bc[r][q];   // (B, B', C, C')
+                        const float2 Bp = make_float2(b.x, b.y);
+                        hb = __ffma2_rn(anext, hb, __fmul2_rn(make_float2(b.z, b.w), f2(v.w)));
+                        const float2 a = as[u];
+                        const float2 hp = u > 0 ? hs[u - 1] : hin;
+                        const float2 ga = __fmul2_rn(__fmul2_rn(hb, hp), a);  // dL/da * a
+                        const float2 sb = __fmul2_rn(hb, Bp);
+                        const float sx = sb.x + sb.y;                        // sum_n hbar B
+                        const float2 sd2 = __ffma2_rn(ga, Ar, __fmul2_rn(sb, f2(v.z)));
+                        dA_loc = __ffma2_rn(ga, f2(v.x), dA_loc);
+                        const float2 vb = __fmul2_rn(hb, f2(v.y));             // hbar delta x
+                        const float2 vc = __fmul2_rn(hs[u], f2(v.w));          // dy h
+                        anext = a;
+                        sm.rbc[uu][j][q] = make_float4(vb.x, vb.y, vc.x, vc.y);
+                        sm.rxd[uu][j][q] = make_float2(sx, sd2.x + sd2.y);
+                        if (t0 + r == 0 && dh0 != nullptr) {
+                            const float2 v0 = __fmul2_rn(anext, hb);
+                            dh0[sidx] = v0.x;
+                            dh0[sidx + 1] = v0.y;
+                        }
+                    }
+                    __syncthreads();
+                    {  // thread (step uu, index k): sums in channel / entry order
+                        const int uu = tid >> 3, k = tid & 7;
+                        const long long t = t0 + s + gi * kSbGrp + uu;
+                        const float4 w0 = sm.rbc[uu][0][k];
+                        float2 sb2 = make_float2(w0.x, w0.y), sc2 = make_float2(w0.z, w0.w);
+                        float2 sxd = sm.rxd[uu][k][0];
+#pragma unroll
+                        for (int i = 1; i < kSqCh; ++i) {
+                            const float4 w = sm.rbc[uu][i][k];
+                            sb2 = __fadd2_rn(sb2, make_float2(w.x, w.y));
+                            sc2 = __fadd2_rn(sc2, make_float2(w.z, w.w));
+                            sxd = __fadd2_rn(sxd, sm.rxd[uu][k][i]);
+                        }
+                        if (t < g.T) {
+                            const size_t pidx = (((size_t)bi * g.T + t) * bpr + blk) * kN + 2 * k;
+                            *reinterpret_cast<float2 *>(partB + pidx) = sb2;
+                            *reinterpret_cast<float2 *>(partC + pidx) = sc2;
+                            const size_t oidx = ((size_t)bi * g.T + t) * g.D + c0 + k;
+                            __stcs(dx + oidx, sxd.x * sm.dxy[s + gi * kSbGrp + uu][k].x);
+                            __stcs(ddelta + oidx, sxd.y);
+                        }
+                    }
+                    __syncthreads();
+                }
+                {  // Kahan step: dA_acc + dA_loc, the rounding error kept in dA_cmp
+                    const float2 yv = __fadd2_rn(dA_loc, make_float2(-dA_cmp.x, -dA_cmp.y));
+                    const float2 tv = __fadd2_rn(dA_acc, yv);
+                    dA_cmp = __fadd2_rn(__fadd2_rn(tv, make_float2(-dA_acc.x, -dA_acc.y)), make_float2(-yv.x, -yv.y));
+                    dA_acc = tv;
+                }
+            }
+        };
+        if (noclamp) walk(std::false_type{});
+        else walk(std::true_type{});
+    }
+    if (partA != nullptr) *reinterpret_cast<float2 *>(partA + sidx) = dA_acc;
+}
+
 // dB, dC: sums of the per-block partials, in block order.
 __global__ void sel_reduce_bc_kernel(const float *__restrict__ partB, const float *__restrict__ partC,
                                      float *__restrict__ dB, float *__restrict__ dC, long long rows, int n_cblk) {
@@ -839,8 +1061,31 @@ sel_reduce_a_kernel(const float *__restrict__ partA, float *__restrict__ dA, int
 }
 
 // ------------------------------------------------------------------ host side
+constexpr int kSqLanes = 8;  // lanes per channel (2 entries each): two warps per block
+// The per-channel walks (sel_fwd_seq_kernel, sel_bwd_seq_kernel) are taken when their
+// warps (one per 4 channels of a batch row) give every SM at least four, so that a
+// walk's dependent steps overlap other warps' work; they need D a multiple of 8 and
+// 16-byte aligned rows for their staged copies.
+bool sel_walk_sizes(int64_t B, int64_t D) {
+    if (D % kSqCh != 0 || D == 0) return false;
+    const double blocks = (double)B * (double)(D / kSqCh);
+    if (blocks >= 2147483648.0) return false;
+    const double warps = blocks * kSqCh * kSqLanes / 32;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    return warps >= 4.0 * sms;
+}
+bool sel_use_seq(bool walk_sizes, std::initializer_list<const void *> rows) {
+    if (!walk_sizes) return false;
+    for (const void *r : rows)
+        if (!aligned16(r)) return false;
+    return true;
+}
+
 struct SelPlan {
     SelGeom g, gb;  // forward and backward geometry (their channel blocks differ)
+    bool walk;      // sizes for which the per-channel walks run (with aligned rows)
     size_t units;
     size_t off_flags, off_agg, off_incl, off_pB, off_pC, off_pA, total;
 };
@@ -855,6 +1100,9 @@ SelPlan sel_plan(int64_t B, int64_t T, int64_t D) {
     p.g.n_cblk = (int)((D + kCh - 1) / kCh);
     p.gb = p.g;
     p.gb.n_cblk = (int)((D + kChB - 1) / kChB);
+    p.walk = sel_walk_sizes(B, D);
+    // dB, dC partials: one per channel block of the backward that runs
+    const size_t n_part = std::max((size_t)p.gb.n_cblk, p.walk ? (size_t)(D / kSqCh) : (size_t)0);
     const size_t units_f = (size_t)p.g.n_chunks * B * p.g.n_cblk, units_b = (size_t)p.g.n_chunks * B * p.gb.n_cblk;
     p.units = units_f > units_b ? units_f : units_b;
     const size_t lanes = std::max(units_f * kCh, units_b * kChB);  // channel slots over all units
@@ -862,8 +1110,8 @@ SelPlan sel_plan(int64_t B, int64_t T, int64_t D) {
     p.off_agg = align_up(p.off_flags + p.units * 4, 256);
     p.off_incl = align_up(p.off_agg + lanes * 32 * 4, 256);
     p.off_pB = align_up(p.off_incl + lanes * kN * 4, 256);
-    p.off_pC = align_up(p.off_pB + (size_t)B * T * p.gb.n_cblk * kN * 4, 256);
-    p.off_pA = align_up(p.off_pC + (size_t)B * T * p.gb.n_cblk * kN * 4, 256);
+    p.off_pC = align_up(p.off_pB + (size_t)B * T * n_part * kN * 4, 256);
+    p.off_pA = align_up(p.off_pC + (size_t)B * T * n_part * kN * 4, 256);
     p.total = align_up(p.off_pA + (size_t)B * p.g.n_chunks * D * kN * 4, 256);
     return p;
 }
@@ -891,18 +1139,6 @@ bool sel_sizes_fit(int64_t B, int64_t T, int64_t D) {
 // The one-walk-per-channel forward is taken when its warps (one per 4 channels of a
 // batch row) give every SM at least four, so that a walk's dependent steps overlap
 // other warps' work; it needs 16-byte aligned rows for its staged copies.
-constexpr int kSqLanes = 8;  // lanes per channel (2 entries each): two warps per block
-bool sel_use_seq(int64_t B, int64_t D, const void *x, const void *delta, const void *Bm, const void *Cm) {
-    if (D % kSqCh != 0 || !aligned16(x) || !aligned16(delta) || !aligned16(Bm) || !aligned16(Cm)) return false;
-    const double blocks = (double)B * (double)(D / kSqCh);
-    if (blocks >= 2147483648.0) return false;
-    const double warps = blocks * kSqCh * kSqLanes / 32;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-    return warps >= 4.0 * sms;
-}
-
 int sel_validate(const char *fn, int64_t B, int64_t T, int64_t D, int64_t N) {
     if (B < 0 || T < 0 || D < 0 || N < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
     if (N != kN) return fail(CLA_ERR_UNSUPPORTED, "%s: N must be %d (got %lld)", fn, kN, (long long)N);
@@ -951,7 +1187,7 @@ extern "C" int cla_selective_scan_fwd(const uint16_t *x, const float *delta, con
     const SelPlan p = sel_plan(B, T, D);
     if (ws_bytes < p.total) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, p.total);
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.off_agg, s), fn);
-    if (sel_use_seq(B, D, x, delta, Bm, Cm)) {
+    if (sel_use_seq(p.walk, {x, delta, Bm, Cm})) {
         // one-warp blocks: as many per SM as shared memory holds (all of it as shared memory)
         static std::atomic<unsigned long long> carve_set{0};
         st = set_smem_carveout_max(carve_set, reinterpret_cast<const void *>(sel_fwd_seq_kernel<kSqLanes>));
@@ -1008,6 +1244,29 @@ extern "C" int cla_selective_scan_bwd(const uint16_t *x, const float *delta, con
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, p.off_agg, s), fn);
     SelWs w = sel_bind(p, ws);
     if (!dA) w.partA = nullptr;
+    const long long rows = B * T;
+    if (sel_use_seq(p.walk, {x, delta, dy, Bm, Cm})) {
+        static std::atomic<unsigned long long> carve_set{0};
+        st = set_smem_carveout_max(carve_set, reinterpret_cast<const void *>(sel_bwd_seq_kernel));
+        if (st) return st;
+        const SelSeqGeom sg{(int)B, (int)D, T, p.g.n_ck};
+        const unsigned int grid = (unsigned int)(B * (D / kSqCh));
+        sel_bwd_seq_kernel<<<grid, kSqCh * 8, sizeof(SelSeqBwdSmem), s>>>(
+            reinterpret_cast<const bf16 *>(x), delta, A, reinterpret_cast<const bf16 *>(Bm),
+            reinterpret_cast<const bf16 *>(Cm), ckpt, dy, dhT, dx, ddelta, dh0, w.partB, w.partC, w.partA, sg);
+        st = check_launch(fn);
+        if (st) return st;
+        sel_reduce_bc_kernel<<<(unsigned int)((rows * kN + 255) / 256), 256, 0, s>>>(w.partB, w.partC, dB, dC, rows,
+                                                                                    (int)(D / kSqCh));
+        st = check_launch(fn);
+        if (st) return st;
+        if (dA) {
+            sel_reduce_a_kernel<<<(unsigned int)((D * kN + 31) / 32), kRedAWarps * 32, 0, s>>>(w.partA, dA, (int)B, 1,
+                                                                                             (int)D);
+            st = check_launch(fn);
+        }
+        return st;
+    }
     static std::atomic<unsigned long long> smem_set{0};
     st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(sel_bwd_kernel), (int)sizeof(SelBwdSmem));
     if (st) return st;
@@ -1017,7 +1276,6 @@ extern "C" int cla_selective_scan_bwd(const uint16_t *x, const float *delta, con
         reinterpret_cast<const bf16 *>(Cm), ckpt, dy, dhT, dx, ddelta, dh0, p.gb, w);
     st = check_launch(fn);
     if (st) return st;
-    const long long rows = B * T;
     sel_reduce_bc_kernel<<<(unsigned int)((rows * kN + 255) / 256), 256, 0, s>>>(w.partB, w.partC, dB, dC, rows,
                                                                                 p.gb.n_cblk);
     st = check_launch(fn);
