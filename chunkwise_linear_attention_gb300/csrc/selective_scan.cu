@@ -561,7 +561,7 @@ sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
         Arp[j] = make_float2(Ar[2 * j], Ar[2 * j + 1]);
     }
     // pass A: states (every 8th kept) and the adjoint pair of the chunk
-    float h[kNh], P[kNh], Bg[kNh];
+    float P[kNh], Bg[kNh];
     {
         const float *ck = ckpt + (((size_t)bi * g.n_ck + (long long)chunk * (kTc / kCk)) * g.D + (cok ? c : 0)) * kN + n0;
         float2 hq[kJh], Pq[kJh], Bq[kJh];
@@ -592,8 +592,6 @@ sel_bwd_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, cons
         }
 #pragma unroll
         for (int j = 0; j < kJh; ++j) {
-            h[2 * j] = hq[j].x;
-            h[2 * j + 1] = hq[j].y;
             P[2 * j] = Pq[j].x;
             P[2 * j + 1] = Pq[j].y;
             Bg[2 * j] = Bq[j].x;
@@ -801,36 +799,41 @@ constexpr int kSbTile = 32;  // steps per staged tile
 constexpr int kSbGrp = 8;    // steps per exchange of the sums
 static_assert(kSbTile % kCk == 0 && kCk % kSbGrp == 0, "tiles hold whole recompute intervals");
 
+template <int CH>  // channels per block
 struct SelSeqBwdSmem {
-    float d[2][kSbTile][kSqCh];      // staged delta, x, dy, B_t, C_t
-    bf16 x[2][kSbTile][kSqCh];
-    float dy[2][kSbTile][kSqCh];
+    float d[2][kSbTile][CH];      // staged delta, x, dy, B_t, C_t
+    bf16 x[2][kSbTile][CH];
+    float dy[2][kSbTile][CH];
     bf16 B[2][kSbTile][kN];
     bf16 C[2][kSbTile][kN];
-    float4 dxy[kSbTile][kSqCh];      // (delta, delta x, x, dy) of the tile being walked
-    float4 bc[kSbTile][kN / 2];      // (B_2p, B_2p+1, C_2p, C_2p+1)
-    float4 rbc[kSbGrp][kSqCh][kN / 2];  // per step: dB, dC terms of channel j, entry pair p
-    float2 rxd[kSbGrp][kSqCh][8 + 1];   // per step: channel j's lane q terms of dx / delta, ddelta
-                                        // (rows padded: the channel sums read them across rows)
+    float4 dxy[kSbTile][CH];      // (delta, delta x, x, dy) of the tile being walked
+    float4 bc[kSbTile][kN / 2];   // (B_2p, B_2p+1, C_2p, C_2p+1)
+    float4 rbc[kSbGrp][CH][kN / 2];  // per step: dB, dC terms of channel j, entry pair p
+    float2 rxd[kSbGrp][CH][8 + 1];   // per step: channel j's lane q terms of dx / delta, ddelta
+                                     // (rows padded: the channel sums read them across rows)
 };
 
-__device__ __forceinline__ void sel_seqb_stage(SelSeqBwdSmem &sm, int buf, const bf16 *x, const float *delta,
+template <int CH>
+__device__ __forceinline__ void sel_seqb_stage(SelSeqBwdSmem<CH> &sm, int buf, const bf16 *x, const float *delta,
                                                const float *dy, const bf16 *Bm, const bf16 *Cm,
                                                const SelSeqGeom &g, int bi, int c0, long long t0, int tid) {
-    constexpr int NT = kSqCh * 8;
+    constexpr int NT = CH * 8;
+    constexpr int PF = CH / 4, PX = CH / 8;  // 16-byte pieces per row of delta / dy and of x
     const int L = (int)min((long long)kSbTile, g.T - t0);
     const size_t row0 = (size_t)bi * g.T + t0;
 #pragma unroll
-    for (int i = tid; i < kSbTile * 2; i += NT) {  // delta, dy: 32 rows x two 16-byte pieces
-        const int r = i >> 1, h = i & 1;
+    for (int i = tid; i < kSbTile * PF; i += NT) {  // delta, dy
+        const int r = i / PF, h = i % PF;
         if (r < L) {
             cp_async16(smem_u32(&sm.d[buf][r][4 * h]), delta + (row0 + r) * g.D + c0 + 4 * h, 16u);
             cp_async16(smem_u32(&sm.dy[buf][r][4 * h]), dy + (row0 + r) * g.D + c0 + 4 * h, 16u);
         }
     }
 #pragma unroll
-    for (int r = tid; r < kSbTile; r += NT)  // x: one 16-byte piece per row
-        if (r < L) cp_async16(smem_u32(&sm.x[buf][r][0]), x + (row0 + r) * g.D + c0, 16u);
+    for (int i = tid; i < kSbTile * PX; i += NT) {  // x
+        const int r = i / PX, h = i % PX;
+        if (r < L) cp_async16(smem_u32(&sm.x[buf][r][8 * h]), x + (row0 + r) * g.D + c0 + 8 * h, 16u);
+    }
 #pragma unroll
     for (int i = tid; i < kSbTile * 2; i += NT) {  // B_t, C_t: two 16-byte pieces each per row
         const int r = i >> 1, h = i & 1;
@@ -844,12 +847,13 @@ __device__ __forceinline__ void sel_seqb_stage(SelSeqBwdSmem &sm, int buf, const
 
 // As sel_seq_convert: rows past the end become delta = dy = x = 0 and B = C = 0, which
 // leaves the adjoint unchanged through them and adds nothing to any gradient.
-__device__ __forceinline__ bool sel_seqb_convert(SelSeqBwdSmem &sm, int buf, int L, float amax, int tid) {
-    constexpr int NT = kSqCh * 8;
+template <int CH>
+__device__ __forceinline__ bool sel_seqb_convert(SelSeqBwdSmem<CH> &sm, int buf, int L, float amax, int tid) {
+    constexpr int NT = CH * 8;
     bool ok = true;
 #pragma unroll
-    for (int i = tid; i < kSbTile * kSqCh; i += NT) {
-        const int r = i / kSqCh, cc = i % kSqCh;
+    for (int i = tid; i < kSbTile * CH; i += NT) {
+        const int r = i / CH, cc = i % CH;
         const float d = r < L ? sm.d[buf][r][cc] : 0.f;
         const float xv = r < L ? __bfloat162float(sm.x[buf][r][cc]) : 0.f;
         const float g = r < L ? sm.dy[buf][r][cc] : 0.f;
@@ -868,20 +872,25 @@ __device__ __forceinline__ bool sel_seqb_convert(SelSeqBwdSmem &sm, int buf, int
     return __syncthreads_and(ok) != 0;
 }
 
-// 8 lanes per channel (entries 2q, 2q + 1 on lane q), 8 channels per block.
-__global__ void __launch_bounds__(kSqCh * 8, 7)
+// 8 lanes per channel (entries 2q, 2q + 1 on lane q), CH channels per block (more
+// channels per block: fewer dB, dC partials to write and sum over blocks).
+// Blocks per SM: 7 of 8 channels or 4 of 16 (shared memory allows 7 and 4; registers
+// are capped at 128 per thread for them), so that every block of the workload's grid is
+// resident at once.
+template <int CH>
+__global__ void __launch_bounds__(CH * 8, CH == 8 ? 7 : 4)
 sel_bwd_seq_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, const float *__restrict__ A,
                    const bf16 *__restrict__ Bm, const bf16 *__restrict__ Cm, const float *__restrict__ ckpt,
                    const float *__restrict__ dy, const float *__restrict__ dhT, float *__restrict__ dx,
                    float *__restrict__ ddelta, float *__restrict__ dh0, float *__restrict__ partB,
                    float *__restrict__ partC, float *__restrict__ partA, SelSeqGeom g) {
-    constexpr int NT = kSqCh * 8;
+    constexpr int NT = CH * 8;
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    SelSeqBwdSmem &sm = *reinterpret_cast<SelSeqBwdSmem *>(smem_raw);
+    SelSeqBwdSmem<CH> &sm = *reinterpret_cast<SelSeqBwdSmem<CH> *>(smem_raw);
     const int tid = threadIdx.x;
-    const int bpr = g.D / kSqCh;  // blocks per batch row
+    const int bpr = g.D / CH;  // blocks per batch row
     const int bi = (int)(blockIdx.x / bpr), blk = (int)(blockIdx.x % bpr);
-    const int c0 = blk * kSqCh;
+    const int c0 = blk * CH;
     const int j = tid >> 3, q = tid & 7;
     const int c = c0 + j;
 
@@ -963,33 +972,40 @@ sel_bwd_seq_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, 
                         anext = a;
                         sm.rbc[uu][j][q] = make_float4(vb.x, vb.y, vc.x, vc.y);
                         sm.rxd[uu][j][q] = make_float2(sx, sd2.x + sd2.y);
-                        if (t0 + r == 0 && dh0 != nullptr) {
+                        if (u == 0 && t0 + s == 0 && dh0 != nullptr) {  // step 0 of the sequence
                             const float2 v0 = __fmul2_rn(anext, hb);
                             dh0[sidx] = v0.x;
                             dh0[sidx + 1] = v0.y;
                         }
                     }
                     __syncthreads();
-                    {  // thread (step uu, index k): sums in channel / entry order
+                    {  // thread (step uu, channel k): dx, ddelta summed over the channel's lanes
+                        const int uu = tid / CH, k = tid % CH;
+                        const long long t = t0 + s + gi * kSbGrp + uu;
+                        float2 sxd = sm.rxd[uu][k][0];
+#pragma unroll
+                        for (int i = 1; i < 8; ++i) sxd = __fadd2_rn(sxd, sm.rxd[uu][k][i]);
+                        if (t < g.T) {
+                            const size_t oidx = ((size_t)bi * g.T + t) * g.D + c0 + k;
+                            __stcs(dx + oidx, sxd.x * sm.dxy[s + gi * kSbGrp + uu][k].x);
+                            __stcs(ddelta + oidx, sxd.y);
+                        }
+                    }
+                    if (tid < kSbGrp * kN / 2) {  // thread (step uu, entry pair k): dB, dC in channel order
                         const int uu = tid >> 3, k = tid & 7;
                         const long long t = t0 + s + gi * kSbGrp + uu;
                         const float4 w0 = sm.rbc[uu][0][k];
                         float2 sb2 = make_float2(w0.x, w0.y), sc2 = make_float2(w0.z, w0.w);
-                        float2 sxd = sm.rxd[uu][k][0];
 #pragma unroll
-                        for (int i = 1; i < kSqCh; ++i) {
+                        for (int i = 1; i < CH; ++i) {
                             const float4 w = sm.rbc[uu][i][k];
                             sb2 = __fadd2_rn(sb2, make_float2(w.x, w.y));
                             sc2 = __fadd2_rn(sc2, make_float2(w.z, w.w));
-                            sxd = __fadd2_rn(sxd, sm.rxd[uu][k][i]);
                         }
                         if (t < g.T) {
                             const size_t pidx = (((size_t)bi * g.T + t) * bpr + blk) * kN + 2 * k;
                             *reinterpret_cast<float2 *>(partB + pidx) = sb2;
                             *reinterpret_cast<float2 *>(partC + pidx) = sc2;
-                            const size_t oidx = ((size_t)bi * g.T + t) * g.D + c0 + k;
-                            __stcs(dx + oidx, sxd.x * sm.dxy[s + gi * kSbGrp + uu][k].x);
-                            __stcs(ddelta + oidx, sxd.y);
                         }
                     }
                     __syncthreads();
@@ -1076,6 +1092,10 @@ bool sel_walk_sizes(int64_t B, int64_t D) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
     return warps >= 4.0 * sms;
 }
+// Channels per block of the backward walk.  16 (half the dB, dC partials to write and sum)
+// measured slower on the 4 x 8192 x 2048 workload: 2300 against 2192 us (4 blocks of 4 warps
+// per SM against 7 of 2).
+constexpr int kSbCh = 8;
 bool sel_use_seq(bool walk_sizes, std::initializer_list<const void *> rows) {
     if (!walk_sizes) return false;
     for (const void *r : rows)
@@ -1102,7 +1122,7 @@ SelPlan sel_plan(int64_t B, int64_t T, int64_t D) {
     p.gb.n_cblk = (int)((D + kChB - 1) / kChB);
     p.walk = sel_walk_sizes(B, D);
     // dB, dC partials: one per channel block of the backward that runs
-    const size_t n_part = std::max((size_t)p.gb.n_cblk, p.walk ? (size_t)(D / kSqCh) : (size_t)0);
+    const size_t n_part = std::max((size_t)p.gb.n_cblk, p.walk ? (size_t)(D / kSbCh) : (size_t)0);
     const size_t units_f = (size_t)p.g.n_chunks * B * p.g.n_cblk, units_b = (size_t)p.g.n_chunks * B * p.gb.n_cblk;
     p.units = units_f > units_b ? units_f : units_b;
     const size_t lanes = std::max(units_f * kCh, units_b * kChB);  // channel slots over all units
@@ -1246,18 +1266,22 @@ extern "C" int cla_selective_scan_bwd(const uint16_t *x, const float *delta, con
     if (!dA) w.partA = nullptr;
     const long long rows = B * T;
     if (sel_use_seq(p.walk, {x, delta, dy, Bm, Cm})) {
-        static std::atomic<unsigned long long> carve_set{0};
-        st = set_smem_carveout_max(carve_set, reinterpret_cast<const void *>(sel_bwd_seq_kernel));
-        if (st) return st;
+        constexpr int CH = kSbCh;
         const SelSeqGeom sg{(int)B, (int)D, T, p.g.n_ck};
-        const unsigned int grid = (unsigned int)(B * (D / kSqCh));
-        sel_bwd_seq_kernel<<<grid, kSqCh * 8, sizeof(SelSeqBwdSmem), s>>>(
+        const unsigned int grid = (unsigned int)(B * (D / CH));
+        const void *fnp = reinterpret_cast<const void *>(sel_bwd_seq_kernel<CH>);
+        static std::atomic<unsigned long long> smem_set{0}, carve_set{0};
+        st = set_max_dynamic_smem(smem_set, fnp, (int)sizeof(SelSeqBwdSmem<CH>));
+        if (st) return st;
+        st = set_smem_carveout_max(carve_set, fnp);
+        if (st) return st;
+        sel_bwd_seq_kernel<CH><<<grid, CH * 8, sizeof(SelSeqBwdSmem<CH>), s>>>(
             reinterpret_cast<const bf16 *>(x), delta, A, reinterpret_cast<const bf16 *>(Bm),
             reinterpret_cast<const bf16 *>(Cm), ckpt, dy, dhT, dx, ddelta, dh0, w.partB, w.partC, w.partA, sg);
         st = check_launch(fn);
         if (st) return st;
         sel_reduce_bc_kernel<<<(unsigned int)((rows * kN + 255) / 256), 256, 0, s>>>(w.partB, w.partC, dB, dC, rows,
-                                                                                    (int)(D / kSqCh));
+                                                                                    (int)(D / CH));
         st = check_launch(fn);
         if (st) return st;
         if (dA) {
