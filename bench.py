@@ -587,7 +587,10 @@ def bench_selective(torch, cla, workloads, dev, flush, peaks, iters=20, shape=No
             "frac_hbm": round((by_f + by_b) / tot / (peaks["hbm_gbs"] * 1e9), 4),
             "frac_binding_roofline": round(max(floor_alu, floor_hbm) / tot, 4),
             "binding": "alu (exp2 on the special-function unit)" if floor_alu >= floor_hbm else "hbm",
-            "state_updates_per_s": round(2 * upd / tot, 1)}
+            "state_updates_per_s": round(2 * upd / tot, 1),
+            "kernels": "sel_fwd_seq_kernel, sel_bwd_seq_kernel (one walk per channel, each decay evaluated once; "
+                       "taken when B*D >= 16 x SMs) + sel_reduce_bc_kernel, sel_reduce_a_kernel; "
+                       "sel_fwd_kernel / sel_bwd_kernel (chunk look-back) for fewer channels"}
 
 
 # ------------------------------------------------------------------ CPU oracle
