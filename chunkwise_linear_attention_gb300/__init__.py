@@ -145,11 +145,14 @@ def _nbytes(t):
     return t.numel() * t.element_size()
 
 
-def _ws(nbytes, device, workspace):
+def _ws(nbytes, device, workspace, minimum=None):
+    """A workspace of nbytes (allocated when not given); a given one needs at least `minimum`
+    bytes (default nbytes) -- the entry points that take less than their size query's amount."""
     if workspace is None:
         workspace = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
-    if _nbytes(workspace) < nbytes:
-        raise ValueError(f"workspace of {_nbytes(workspace)} bytes < {nbytes} needed")
+    need = nbytes if minimum is None else minimum
+    if _nbytes(workspace) < need:
+        raise ValueError(f"workspace of {_nbytes(workspace)} bytes < {need} needed")
     return workspace
 
 
@@ -502,14 +505,15 @@ def delta_fwd(q, k, v, log_decay, beta, S0=None, *, chunk=64, o=None, ST=None, c
               stream=None):
     """Delta rule with a decay per head: S_t = a_t (I - beta_t k_t^T k_t) S_{t-1} + beta_t k_t^T v_t,
     o_t = q_t S_t; log_decay, beta [B, H, T].  Returns (o, ST).  With ckpt (see delta_ckpt) it also
-    saves the state entering every chunk for delta_bwd."""
+    saves the state entering every chunk for delta_bwd.  A given workspace needs 256 bytes; the
+    size query's amount lets the chunks' (I + A)^-1 be formed beforehand, all at once."""
     B, H, T, dk = _dims(q, 4, "q")
     dv = _dims(v, 4, "v")[3]
     dev = q.device
     f32, bf16 = torch.float32, torch.bfloat16
     o = _out(o, (B, H, T, dv), f32, dev)
     ST = _out(ST, (B, H, dk, dv), f32, dev)
-    ws = _ws(delta_workspace_size(B, H, T, dk, dv, chunk), dev, workspace)
+    ws = _ws(delta_workspace_size(B, H, T, dk, dv, chunk), dev, workspace, minimum=256)
     tk, tv, st, bht = (B, H, T, dk), (B, H, T, dv), (B, H, dk, dv), (B, H, T)
     args = (_T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
             _T(log_decay, f32, "log_decay", bht), _T(beta, f32, "beta", bht), _T(S0, f32, "S0", st),

@@ -190,10 +190,130 @@ struct DeltaArgs {
     const float *S0;        // [BH][DK][DV] or NULL
     float *o, *ST;          // o NULL: the output is not formed (the backward's states pass)
     float *states;          // [BH][n_chunks][DK][DV], the state entering every chunk, or NULL
+    // [BH][n_chunks] images of (I + A)^-1 as its two bf16 parts in the swizzled [64][64] tile
+    // layout (16 KB per chunk), formed beforehand by delta_wy_kernel; NULL: formed in the chunk loop
+    uint8_t *wy;
     int BH, DV, nzb, n_chunks;
     long long T;
     WsHeader *hdr;
 };
+
+// In-chunk log2 decays c_r (cumulative from the chunk start, one warp) with the range check of
+// the chunk's log decays and gate strengths.
+__device__ __forceinline__ void delta_chunk_decays(const float *ls, const float *bs, float *cs, int lane,
+                                                   WsHeader *hdr) {
+    float v0 = ls[2 * lane], v1 = ls[2 * lane + 1];
+    const float b0 = bs[2 * lane], b1 = bs[2 * lane + 1];
+    if (!isfinite(v0) || !isfinite(v1) || !isfinite(b0) || !isfinite(b1)) atomicOr(&hdr->error, kErrRange);
+    v0 *= kDlLog2e;
+    v1 = v0 + v1 * kDlLog2e;
+    float tot = v1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, tot, off);
+        if (lane >= off) tot += o;
+    }
+    const float ex = tot - v1;  // sum over the earlier lanes' pairs
+    cs[2 * lane] = ex + v0;
+    cs[2 * lane + 1] = ex + v1;
+}
+
+// A = strictly lower (beta_r 2^(c_r - c_s) k_r . k_s) into Am (fp32, row stride kAS): rows
+// 16 warp.. of it, K Kt on mma.sync from the swizzled K tile (QRB bytes per row).
+template <int DK, int QRB>
+__device__ __forceinline__ void delta_build_A(const uint8_t *Kt, const float *bs, const float *cs, float *Am,
+                                              int warp, int lane) {
+    const int g = lane >> 2, tq = lane & 3;
+    const int arow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    float F[8][4];
+#pragma unroll
+    for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) F[nj][e] = 0.f;
+#pragma unroll 2
+    for (int kk = 0; kk < DK / 16; ++kk) {
+        uint32_t a[4];
+        ldsm_x4(smem_u32(Kt + swz<QRB>(arow, 2 * kk + (lane >> 4))), a);
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+            uint32_t b[4];
+            const int brow = 16 * pp + (lane & 7) + (lane >> 4) * 8;
+            ldsm_x4(smem_u32(Kt + swz<QRB>(brow, 2 * kk + ((lane >> 3) & 1))), b);
+            mma16816(F[2 * pp], a, b[0], b[1]);
+            mma16816(F[2 * pp + 1], a, b[2], b[3]);
+        }
+    }
+#pragma unroll
+    for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int r = warp * 16 + g + 8 * (e >> 1), s = nj * 8 + 2 * tq + (e & 1);
+            Am[r * kAS + s] = (s < r) ? bs[r] * ex2(cs[r] - cs[s]) * F[nj][e] : 0.f;
+        }
+}
+
+// T (fp32 in Am, row stride kAS) as two bf16 parts in [64][64] tiles of 128-byte swizzled rows at
+// hi and lo (shared or global memory): 16-byte chunks of 8 columns, four per thread.
+__device__ __forceinline__ void delta_T_parts(const float *Am, uint8_t *hi_tile, uint8_t *lo_tile, int tid) {
+#pragma unroll
+    for (int it = 0; it < kDlTc * 8 / kDlThreads; ++it) {
+        const int task = tid + it * kDlThreads, r = task >> 3, c8 = task & 7;
+        const float4 v0 = *reinterpret_cast<const float4 *>(Am + r * kAS + 8 * c8);
+        const float4 v1 = *reinterpret_cast<const float4 *>(Am + r * kAS + 8 * c8 + 4);
+        uint32_t hi[4], lo[4];
+        split_bf16x2(make_float2(v0.x, v0.y), hi[0], lo[0]);
+        split_bf16x2(make_float2(v0.z, v0.w), hi[1], lo[1]);
+        split_bf16x2(make_float2(v1.x, v1.y), hi[2], lo[2]);
+        split_bf16x2(make_float2(v1.z, v1.w), hi[3], lo[3]);
+        *reinterpret_cast<uint4 *>(hi_tile + swz<128>(r, c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(lo_tile + swz<128>(r, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+// The chunks' (I + A)^-1, which do not depend on the state, all at once before the chunk loop:
+// one block per (head, chunk), writing the two bf16 parts of each in the tile layout the loop
+// copies straight into shared memory.  This takes the K K^T product and the inverse -- about
+// half of a chunk's work -- off the loop's sequential path, and forms them once per chunk
+// instead of once per 64-column value block.
+template <int DK>
+__global__ void __launch_bounds__(kDlThreads) delta_wy_kernel(const DeltaArgs p) {
+    constexpr int QRB = DK * 2;
+    constexpr int OFF_K = 0, OFF_L = kDlTc * QRB, OFF_B = OFF_L + kDlTc * 4, OFF_C = OFF_B + kDlTc * 4;
+    constexpr int OFF_A = OFF_C + kDlTc * 4, OFF_S = OFF_A + kDlTc * kAS * 4;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.x / p.n_chunks, chunk = blockIdx.x % p.n_chunks;
+    const long long t0 = (long long)chunk * kDlTc;
+    const bf16 *Kb = p.k + (size_t)bh * p.T * DK;
+    constexpr int QC = QRB / 16;
+    for (int i = tid; i < kDlTc * QC; i += kDlThreads) {
+        const int row = i / QC, c16 = i % QC;
+        const long long t = t0 + row;
+        const bool ok = t < p.T;
+        cp_async16(smem_u32(smem + OFF_K + swz<QRB>(row, c16)), Kb + (size_t)(ok ? t : 0) * DK + c16 * 8,
+                   ok ? 16u : 0u);
+    }
+    for (int i = tid; i < kDlTc; i += kDlThreads) {  // padding tokens: no decay, no write
+        const long long t = t0 + i;
+        const bool ok = t < p.T;
+        cp_async4(smem_u32(smem + OFF_L + i * 4), p.g + (size_t)bh * p.T + (ok ? t : 0), ok ? 4u : 0u);
+        cp_async4(smem_u32(smem + OFF_B + i * 4), p.beta + (size_t)bh * p.T + (ok ? t : 0), ok ? 4u : 0u);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    const float *bs = reinterpret_cast<const float *>(smem + OFF_B);
+    float *cs = reinterpret_cast<float *>(smem + OFF_C);
+    float *Am = reinterpret_cast<float *>(smem + OFF_A);
+    if (warp == 0) delta_chunk_decays(reinterpret_cast<const float *>(smem + OFF_L), bs, cs, lane, p.hdr);
+    __syncthreads();
+    delta_build_A<DK, QRB>(smem + OFF_K, bs, cs, Am, warp, lane);
+    __syncthreads();
+    tri_inverse_blocked(Am, reinterpret_cast<float *>(smem + OFF_S), tid);
+    uint8_t *out = p.wy + ((size_t)bh * p.n_chunks + chunk) * (2 * kDlTc * 128);
+    delta_T_parts(Am, out, out + kDlTc * 128, tid);
+}
+constexpr int delta_wy_smem(int DK) { return kDlTc * DK * 2 + 3 * kDlTc * 4 + kDlTc * kAS * 4 + 16 * 48 * 4; }
 
 template <int DK>
 __global__ void __launch_bounds__(kDlThreads, 2) delta_fwd_kernel(const DeltaArgs p) {
@@ -234,6 +354,11 @@ __global__ void __launch_bounds__(kDlThreads, 2) delta_fwd_kernel(const DeltaArg
             const bool ok = t < p.T;
             cp_async4(smem_u32(st + C::OFF_L + i * 4), Lb + (ok ? t : 0), ok ? 4u : 0u);
             cp_async4(smem_u32(st + C::OFF_B + i * 4), Bb + (ok ? t : 0), ok ? 4u : 0u);
+        }
+        if (p.wy != nullptr) {  // the chunk's (I + A)^-1 parts: 16 KB copied as they lie
+            const uint8_t *src = p.wy + ((size_t)bh * p.n_chunks + chunk) * (2 * kDlTc * 128);
+            for (int i = tid; i < 2 * kDlTc * 8; i += kDlThreads)
+                cp_async16(smem_u32(smem + C::OFF_TH + 16 * i), src + 16 * i, 16u);
         }
     };
     // state fragments: warp w owns rows 16(w S_MT + mi) + {g, g + 8}
@@ -311,69 +436,21 @@ __global__ void __launch_bounds__(kDlThreads, 2) delta_fwd_kernel(const DeltaArg
         cp_async_wait<0>();
         __syncthreads();
         // ---- in-chunk log2 decays (warp 0) and the state's bf16 parts (everyone)
-        if (warp == 0) {
-            float v0 = ls[2 * lane], v1 = ls[2 * lane + 1];
-            const float b0 = bs[2 * lane], b1 = bs[2 * lane + 1];
-            if (!isfinite(v0) || !isfinite(v1) || !isfinite(b0) || !isfinite(b1)) atomicOr(&p.hdr->error, kErrRange);
-            v0 *= kDlLog2e;
-            v1 = v0 + v1 * kDlLog2e;
-            float tot = v1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float o = __shfl_up_sync(0xffffffffu, tot, off);
-                if (lane >= off) tot += o;
-            }
-            const float ex = tot - v1;  // sum over the earlier lanes' pairs
-            cs[2 * lane] = ex + v0;
-            cs[2 * lane + 1] = ex + v1;
-        }
+        if (warp == 0) delta_chunk_decays(ls, bs, cs, lane, p.hdr);
         write_state_parts();
         __syncthreads();
         const float cL = cs[kDlTc - 1];
 
-        // ---- A = strictly lower (beta_r 2^(c_r - c_s) k_r . k_s), this warp's 16 rows
-        {
-            float F[8][4];
-            zero8(F);
-#pragma unroll 2
-            for (int kk = 0; kk < DK / 16; ++kk) {
-                uint32_t a[4];
-                ldsm_x4(smem_u32(st + C::OFF_K + swz<C::QRB>(arow, 2 * kk + (lane >> 4))), a);
-#pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
-                    uint32_t b[4];
-                    const int brow = 16 * pp + (lane & 7) + (lane >> 4) * 8;
-                    ldsm_x4(smem_u32(st + C::OFF_K + swz<C::QRB>(brow, 2 * kk + ((lane >> 3) & 1))), b);
-                    mma16816(F[2 * pp], a, b[0], b[1]);
-                    mma16816(F[2 * pp + 1], a, b[2], b[3]);
-                }
-            }
-#pragma unroll
-            for (int nj = 0; nj < 8; ++nj)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = warp * 16 + g + 8 * (e >> 1), s = nj * 8 + 2 * tq + (e & 1);
-                    Am[r * kAS + s] = (s < r) ? bs[r] * ex2(cs[r] - cs[s]) * F[nj][e] : 0.f;
-                }
+        if (p.wy == nullptr) {
+            // ---- A = strictly lower (beta_r 2^(c_r - c_s) k_r . k_s), this warp's 16 rows
+            delta_build_A<DK, C::QRB>(st + C::OFF_K, bs, cs, Am, warp, lane);
+            __syncthreads();
+            // ---- T = (I + A)^-1 (unit lower triangular) in place (scratch: T's tiles, free until
+            // below), then as two bf16 parts in the [64][64] tiles
+            tri_inverse_blocked(Am, reinterpret_cast<float *>(smem + C::OFF_TH), tid);
+            delta_T_parts(Am, smem + C::OFF_TH, smem + C::OFF_TL, tid);
+            __syncthreads();
         }
-        __syncthreads();
-        // ---- T = (I + A)^-1 (unit lower triangular) in place, then as two bf16 parts in the
-        // [64][64] tiles: 16-byte chunks of 8 columns, four per thread
-        tri_inverse_blocked(Am, reinterpret_cast<float *>(smem + C::OFF_TH), tid);  // scratch: T's tiles, free until below
-#pragma unroll
-        for (int it = 0; it < kDlTc * 8 / kDlThreads; ++it) {
-            const int task = tid + it * kDlThreads, r = task >> 3, c8 = task & 7;
-            const float4 v0 = *reinterpret_cast<const float4 *>(Am + r * kAS + 8 * c8);
-            const float4 v1 = *reinterpret_cast<const float4 *>(Am + r * kAS + 8 * c8 + 4);
-            uint32_t hi[4], lo[4];
-            split_bf16x2(make_float2(v0.x, v0.y), hi[0], lo[0]);
-            split_bf16x2(make_float2(v0.z, v0.w), hi[1], lo[1]);
-            split_bf16x2(make_float2(v1.x, v1.y), hi[2], lo[2]);
-            split_bf16x2(make_float2(v1.z, v1.w), hi[3], lo[3]);
-            *reinterpret_cast<uint4 *>(smem + C::OFF_TH + swz<C::VRB>(r, c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4 *>(smem + C::OFF_TL + swz<C::VRB>(r, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-        __syncthreads();
 
         // ---- X = diag(beta) (V - diag(gamma) K S) for this warp's rows (K S: two products)
         {
@@ -568,6 +645,17 @@ __global__ void __launch_bounds__(kDlThreads, 2) delta_fwd_kernel(const DeltaArg
                     p.ST[((size_t)bh * DK + s_row(mi, e >> 1)) * p.DV + zb * 64 + nj * 8 + 2 * tq + (e & 1)] =
                         S[mi][nj][e];
     }
+}
+
+template <int DK>
+int launch_delta_wy(const DeltaArgs &a, cudaStream_t s) {
+    const size_t blocks = (size_t)a.BH * a.n_chunks;
+    if (blocks >= 2147483648ull) return fail(CLA_ERR_UNSUPPORTED, "delta_wy_kernel: too many chunks for one launch");
+    static std::atomic<unsigned long long> smem_set{0};
+    const int st = set_max_dynamic_smem(smem_set, reinterpret_cast<const void *>(delta_wy_kernel<DK>), delta_wy_smem(DK));
+    if (st) return st;
+    delta_wy_kernel<DK><<<(unsigned int)blocks, kDlThreads, delta_wy_smem(DK), s>>>(a);
+    return check_launch("delta_wy_kernel");
 }
 
 template <int DK>
@@ -1499,6 +1587,11 @@ size_t delta_bwd_ws_bytes(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t d
     return sizeof(WsHeader) + align_up((size_t)states, 16) + (size_t)parts;
 }
 
+// Bytes of the chunks' precomputed (I + A)^-1 parts (forward workspace after its header).
+size_t delta_wy_bytes(int64_t B, int64_t H, int64_t T) {
+    return (size_t)B * (size_t)H * (size_t)((T + kDlTc - 1) / kDlTc) * (2 * kDlTc * 128);
+}
+
 bool delta_supported(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chunk) {
     return B >= 0 && H >= 0 && T >= 0 && (dk == 64 || dk == 128) && dv > 0 && dv % 64 == 0 && dv <= 1024 &&
            chunk == kDlTc && product_below({B, H}, 16777217.0) && T <= (1ll << 34) &&
@@ -1513,7 +1606,7 @@ using namespace cla;
 extern "C" size_t cla_delta_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
                                            int chunk) {
     if (!delta_supported(B, H, T, dim_k, dim_v, chunk)) return 0;
-    return sizeof(WsHeader);
+    return sizeof(WsHeader) + delta_wy_bytes(B, H, T);
 }
 
 namespace {
@@ -1546,6 +1639,10 @@ int delta_fwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
     if (ws_bytes < sizeof(WsHeader))
         return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, sizeof(WsHeader));
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), s), fn);
+    // with room for them (the size query's workspace), the chunks' (I + A)^-1 are formed first, all
+    // chunks in parallel; with a header-only workspace the chunk loop forms them itself
+    const size_t wy_bytes = delta_wy_bytes(B, H, T);
+    uint8_t *wy = ws_bytes >= sizeof(WsHeader) + wy_bytes ? static_cast<uint8_t *>(ws) + sizeof(WsHeader) : nullptr;
     DeltaArgs a;
     memset(&a, 0, sizeof(a));
     a.q = reinterpret_cast<const bf16 *>(q);
@@ -1563,6 +1660,11 @@ int delta_fwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
     a.T = T;
     a.hdr = static_cast<WsHeader *>(ws);
     a.states = ckpt;
+    a.wy = wy;
+    if (wy != nullptr) {
+        const int st = dim_k == 64 ? launch_delta_wy<64>(a, s) : launch_delta_wy<128>(a, s);
+        if (st) return st;
+    }
     const unsigned int grid = (unsigned int)(BH * (dim_v / 64));
     return dim_k == 64 ? launch_delta_fwd<64>(a, s, grid) : launch_delta_fwd<128>(a, s, grid);
 }

@@ -392,8 +392,13 @@ int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 /* Delta rule with a decay per head (Gated DeltaNet)                         */
 /* ======================================================================== */
 
-/* Bytes of workspace for cla_delta_fwd (its header: the error flag); 0 for
- * sizes, head dims or chunks that call refuses. */
+/* Bytes of workspace for cla_delta_fwd: its 256-byte header (the error flag)
+ * and room for every chunk's (I + A)^-1 (B H ceil(T / 64) x 16 KB: two bf16
+ * parts of the 64 x 64 matrix), which the call then forms for all chunks at
+ * once before the chunk loop; 0 for sizes, head dims or chunks that call
+ * refuses.  cla_delta_fwd also accepts a header-only workspace (256 bytes):
+ * the chunk loop then forms each (I + A)^-1 itself, with the same result
+ * bits, more slowly. */
 size_t cla_delta_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
                                 int64_t dim_v, int chunk);
 

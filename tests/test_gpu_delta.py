@@ -58,15 +58,34 @@ def test_delta_full_writes_and_strong_decay(cla):
     _run(cla, inp)
 
 
-def test_delta_nonfinite_decay_is_reported(cla):
+# a header-only workspace: (I + A)^-1 formed inside the chunk loop; the size query's: formed
+# for all chunks beforehand
+@pytest.mark.parametrize("full_ws", [False, True])
+def test_delta_nonfinite_decay_is_reported(cla, full_ws):
     inp = workloads.make("delta", B=1, H=1, T=200, dk=64, dv=64)
     inp["log_a"][0, 0, 77] = -float("inf")
     t = {k: v.cuda() for k, v in inp.items()}
-    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    n = cla.delta_workspace_size(1, 1, 200, 64, 64, 64) if full_ws else 256
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
     cla.delta_fwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], t["S0"], workspace=ws)
     with pytest.raises(cla.ClaError, match="outside the kernel's range") as ei:
         cla.check_status(ws)
     assert ei.value.status == 2
+
+
+@pytest.mark.parametrize("dk,dv,T", [(64, 64, 300), (128, 192, 1000)])
+def test_delta_precomputed_inverse_matches_in_loop(cla, dk, dv, T):
+    """The chunks' (I + A)^-1 formed beforehand (the size query's workspace) and inside the chunk
+    loop (a header-only workspace) are the same computation: bit-identical outputs."""
+    inp = workloads.make("delta", B=2, H=2, T=T, dk=dk, dv=dv)
+    t = {k: v.cuda() for k, v in inp.items()}
+    outs = []
+    for n in (256, cla.delta_workspace_size(2, 2, T, dk, dv, 64)):
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        outs.append(cla.delta_fwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], t["S0"], workspace=ws))
+        cla.check_status(ws)
+    assert n > 256
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
 def test_delta_workload_full_sampled_heads(cla):
