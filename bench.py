@@ -544,9 +544,11 @@ def bench_delta(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
             "fwd_TFLOPs": round(fl / sec / 1e12, 2), "bwd_TFLOPs": round(flb / secb / 1e12, 2),
             "frac_bf16_peak": round((fl + flb) / (sec + secb) / (peaks["bf16_tflops"] * 1e12), 4),
             "frac_hbm_min_bytes": round(by_min / sec / (peaks["hbm_gbs"] * 1e9), 4),
-            "kernels": "delta_fwd_kernel (mma.sync m16n8k16; chunks of a head in order, no look-back; saves the "
-                       "checkpoint); backward: delta_bwd_kernel (chunks in reverse, from the checkpoint; without "
-                       "one a states pass of delta_fwd_kernel runs first), delta_bwd_reduce_kernel"}
+            "kernels": "delta_wy_kernel (every chunk's (I + A)^-1, all chunks in parallel, into the checkpoint), "
+                       "delta_fwd_kernel (mma.sync m16n8k16; chunks of a head in order, no look-back; saves the "
+                       "checkpoint); backward: delta_bwd_kernel (chunks in reverse, from the checkpoint's states "
+                       "and inverses; without one delta_wy_kernel and a states pass of delta_fwd_kernel run "
+                       "first), delta_bwd_reduce_kernel"}
 
 
 def bench_selective(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):

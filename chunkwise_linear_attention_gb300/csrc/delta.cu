@@ -775,6 +775,7 @@ struct DeltaBwdArgs {
     const float *g, *beta;  // [BH][T]
     const float *dST;       // [BH][DK][DV] or NULL
     const float *states;    // [BH][n_chunks][DK][DV]
+    const uint8_t *wy;      // [BH][n_chunks] (I + A)^-1 parts, as delta_wy_kernel writes them
     float *dq, *dk, *dv, *dlog, *dbeta, *dS0;
     float *part;            // partials of the column blocks 1.. (NULL when DV == 64)
     long long part_stride;  // floats per column block: BH T (2 DK + 2)
@@ -850,6 +851,11 @@ __global__ void __launch_bounds__(kDlBwdThreads, 1) delta_bwd_kernel(const Delta
             cp_async4(smem_u32(smem + C::OFF_L + i * 4), Lb + (ok ? t : 0), ok ? 4u : 0u);
             cp_async4(smem_u32(smem + C::OFF_B + i * 4), Bb + (ok ? t : 0), ok ? 4u : 0u);
         }
+        {  // the chunk's (I + A)^-1 parts, formed by delta_wy_kernel: 16 KB copied as they lie
+            const uint8_t *src = p.wy + ((size_t)bh * p.n_chunks + chunk) * (2 * kDlTc * 128);
+            for (int i = tid; i < 2 * kDlTc * 8; i += kDlBwdThreads)
+                cp_async16(smem_u32(smem + C::OFF_TH + 16 * i), src + 16 * i, 16u);
+        }
         // the state entering the chunk, fp32 -> two bf16 parts (plain loads, read once; all of a
         // thread's loads issued before the first is used)
         const float *sg = p.states + ((size_t)bh * p.n_chunks + chunk) * DK * p.DV + zb * 64;
@@ -891,6 +897,8 @@ __global__ void __launch_bounds__(kDlBwdThreads, 1) delta_bwd_kernel(const Delta
         }
         const float *sg = p.states + ((size_t)bh * p.n_chunks + chunk) * DK * p.DV + zb * 64;
         for (int i = tid; i < DK * 2; i += kDlBwdThreads) prefetch_l2(sg + (size_t)(i >> 1) * p.DV + (i & 1) * 32);
+        const uint8_t *wy = p.wy + ((size_t)bh * p.n_chunks + chunk) * (2 * kDlTc * 128);
+        for (int i = tid; i < 2 * kDlTc; i += kDlBwdThreads) prefetch_l2(wy + 128 * i);
     };
 
     // adjoint state fragments: rows 16(wr S_MT + mi) + {g, g + 8}, columns 8(4 hf + nj) + 2 tq + {0, 1}
@@ -1043,34 +1051,8 @@ __global__ void __launch_bounds__(kDlBwdThreads, 1) delta_bwd_kernel(const Delta
                 }
         }
         __syncthreads();
-        // ---- (I + A)^-1, A = diag(beta) E: A in fp32 over U's tiles (not written yet), inverted
-        // there in place by 16-row blocks, then as two bf16 parts; then every warp forms K S,
-        // Yv = V - diag(gamma) K S and X = diag(beta) Yv for its part
-        {
-            float *Aw = reinterpret_cast<float *>(smem + C::OFF_UH);
-#pragma unroll
-            for (int it = 0; it < kDlTc * 16 / kDlBwdThreads; ++it) {
-                const int task = tid + it * kDlBwdThreads, r = task >> 4, c4 = task & 15;
-                const float4 e = *reinterpret_cast<const float4 *>(Em + r * kAS + 4 * c4);
-                const float b = bs[r];
-                *reinterpret_cast<float4 *>(Aw + r * kAS + 4 * c4) = make_float4(b * e.x, b * e.y, b * e.z, b * e.w);
-            }
-            __syncthreads();
-            tri_inverse_blocked(Aw, Aw + kDlTc * kAS, tid);  // scratch: after A, still over U's tiles
-#pragma unroll
-            for (int it = 0; it < kDlTc * 8 / kDlBwdThreads; ++it) {
-                const int task = tid + it * kDlBwdThreads, r = task >> 3, c8 = task & 7;
-                const float4 v0 = *reinterpret_cast<const float4 *>(Aw + r * kAS + 8 * c8);
-                const float4 v1 = *reinterpret_cast<const float4 *>(Aw + r * kAS + 8 * c8 + 4);
-                uint32_t hi[4], lo[4];
-                split_bf16x2(make_float2(v0.x, v0.y), hi[0], lo[0]);
-                split_bf16x2(make_float2(v0.z, v0.w), hi[1], lo[1]);
-                split_bf16x2(make_float2(v1.x, v1.y), hi[2], lo[2]);
-                split_bf16x2(make_float2(v1.z, v1.w), hi[3], lo[3]);
-                *reinterpret_cast<uint4 *>(smem + C::OFF_TH + swz<VRB>(r, c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(smem + C::OFF_TL + swz<VRB>(r, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-        }
+        // ---- (I + A)^-1 (A = diag(beta) E) arrived with the chunk's inputs, as two bf16 parts;
+        // every warp forms K S, Yv = V - diag(gamma) K S and X = diag(beta) Yv for its part
         float Yv[4][4];
         {
             zero4(Yv);
@@ -1576,20 +1558,23 @@ size_t delta_states_bytes(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t d
     return align_up(sizeof(float) * (size_t)(B * H) * (size_t)((T + kDlTc - 1) / kDlTc) * (size_t)dk * (size_t)dv, 16);
 }
 
-// Workspace of the backward: the header, the state entering every chunk, and the partials of the
-// value-column blocks after the first.  0 when the shape is unsupported or the size overflows.
+// Bytes of the chunks' precomputed (I + A)^-1 parts (16 KB a chunk).
+size_t delta_wy_bytes(int64_t B, int64_t H, int64_t T) {
+    return (size_t)B * (size_t)H * (size_t)((T + kDlTc - 1) / kDlTc) * (2 * kDlTc * 128);
+}
+
+// Workspace of the backward: the header, the state entering every chunk, every chunk's (I + A)^-1
+// parts, and the partials of the value-column blocks after the first (with a checkpoint, which
+// holds the states and the inverses, only the header and the partials).  0 when the shape is
+// unsupported or the size overflows.
 size_t delta_bwd_ws_bytes(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv) {
     const double BH = (double)B * H, nc = (double)((T + kDlTc - 1) / kDlTc);
     const double states = BH * nc * dk * dv * 4.0;
+    const double wy = BH * nc * (2.0 * kDlTc * 128);
     const double parts = (double)(dv / 64 - 1) * BH * T * (2.0 * dk + 2.0) * 4.0;
-    const double total = sizeof(WsHeader) + states + 16.0 + parts;
+    const double total = sizeof(WsHeader) + states + 16.0 + wy + parts;
     if (total > 9.0e18) return 0;
-    return sizeof(WsHeader) + align_up((size_t)states, 16) + (size_t)parts;
-}
-
-// Bytes of the chunks' precomputed (I + A)^-1 parts (forward workspace after its header).
-size_t delta_wy_bytes(int64_t B, int64_t H, int64_t T) {
-    return (size_t)B * (size_t)H * (size_t)((T + kDlTc - 1) / kDlTc) * (2 * kDlTc * 128);
+    return sizeof(WsHeader) + align_up((size_t)states, 16) + (size_t)wy + (size_t)parts;
 }
 
 bool delta_supported(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chunk) {
@@ -1641,8 +1626,11 @@ int delta_fwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), s), fn);
     // with room for them (the size query's workspace), the chunks' (I + A)^-1 are formed first, all
     // chunks in parallel; with a header-only workspace the chunk loop forms them itself
+    // (a checkpoint holds them after the states, for the backward to reuse)
     const size_t wy_bytes = delta_wy_bytes(B, H, T);
-    uint8_t *wy = ws_bytes >= sizeof(WsHeader) + wy_bytes ? static_cast<uint8_t *>(ws) + sizeof(WsHeader) : nullptr;
+    uint8_t *wy = ckpt != nullptr ? reinterpret_cast<uint8_t *>(ckpt) + delta_states_bytes(B, H, T, dim_k, dim_v)
+                  : ws_bytes >= sizeof(WsHeader) + wy_bytes ? static_cast<uint8_t *>(ws) + sizeof(WsHeader)
+                                                            : nullptr;
     DeltaArgs a;
     memset(&a, 0, sizeof(a));
     a.q = reinterpret_cast<const bf16 *>(q);
@@ -1672,8 +1660,9 @@ int delta_fwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
 
 extern "C" size_t cla_delta_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk) {
     if (!delta_supported(B, H, T, dim_k, dim_v, chunk)) return 0;
-    const double bytes = (double)B * H * (double)((T + kDlTc - 1) / kDlTc) * dim_k * dim_v * 4.0;
-    return bytes > 9.0e18 ? 0 : (size_t)bytes;
+    const double nc = (double)((T + kDlTc - 1) / kDlTc);
+    const double bytes = (double)B * H * nc * (dim_k * dim_v * 4.0 + 2.0 * kDlTc * 128) + 16.0;
+    return bytes > 9.0e18 ? 0 : delta_states_bytes(B, H, T, dim_k, dim_v) + delta_wy_bytes(B, H, T);
 }
 
 extern "C" int cla_delta_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
@@ -1733,15 +1722,19 @@ int delta_bwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
     // with a checkpoint the states pass is skipped and the workspace holds the header and the partials only
     const size_t full = delta_bwd_ws_bytes(B, H, T, dim_k, dim_v);
     if (full == 0) return fail(CLA_ERR_UNSUPPORTED, "%s: workspace size overflows", fn);
-    const size_t need = ckpt ? full - delta_states_bytes(B, H, T, dim_k, dim_v) : full;
+    const size_t states_b = delta_states_bytes(B, H, T, dim_k, dim_v), wy_b = delta_wy_bytes(B, H, T);
+    const size_t need = ckpt ? full - states_b - wy_b : full;
     if (!ws || !aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace NULL or unaligned", fn);
     if (ws_bytes < need) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, need);
     CLA_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(WsHeader), s), fn);
     const int n_chunks = (int)((T + kDlTc - 1) / kDlTc);
     float *ws_states = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + sizeof(WsHeader));
-    const size_t states_bytes = ckpt ? 0 : delta_states_bytes(B, H, T, dim_k, dim_v);
+    uint8_t *ws_wy = reinterpret_cast<uint8_t *>(ws_states) + states_b;
     const unsigned int grid = (unsigned int)(BH * (dim_v / 64));
     const float *states = ckpt ? ckpt : ws_states;
+    // every chunk's (I + A)^-1: from the checkpoint, else formed here (before the states pass, which
+    // uses them too)
+    const uint8_t *wy = ckpt ? reinterpret_cast<const uint8_t *>(ckpt) + states_b : ws_wy;
     // the states pass (no checkpoint): the forward kernel writes the state entering every chunk, no output
     if (!ckpt) {
         DeltaArgs f;
@@ -1759,7 +1752,10 @@ int delta_bwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
         f.n_chunks = n_chunks;
         f.T = T;
         f.hdr = static_cast<WsHeader *>(ws);
-        const int st = dim_k == 64 ? launch_delta_fwd<64>(f, s, grid) : launch_delta_fwd<128>(f, s, grid);
+        f.wy = ws_wy;
+        int st = dim_k == 64 ? launch_delta_wy<64>(f, s) : launch_delta_wy<128>(f, s);
+        if (st) return st;
+        st = dim_k == 64 ? launch_delta_fwd<64>(f, s, grid) : launch_delta_fwd<128>(f, s, grid);
         if (st) return st;
     }
     DeltaBwdArgs a;
@@ -1772,13 +1768,15 @@ int delta_bwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
     a.beta = beta;
     a.dST = dST;
     a.states = states;
+    a.wy = wy;
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
     a.dlog = dlog_decay;
     a.dbeta = dbeta;
     a.dS0 = dS0;
-    a.part = dim_v > 64 ? reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws_states) + states_bytes) : nullptr;
+    a.part = dim_v > 64 ? reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws_states) + (ckpt ? 0 : states_b + wy_b))
+                        : nullptr;
     a.part_stride = (long long)BH * T * (2 * dim_k + 2);
     a.BH = (int)BH;
     a.DV = (int)dim_v;
