@@ -279,6 +279,9 @@ struct SelSeqSmem {
     bf16 C[2][kSqTile][kN];
     float2 ddx[kSqTile][kSqCh];       // (delta, delta x) of the tile being walked
     float4 bc[kSqTile][kN / 2];       // (B_2p, B_2p+1, C_2p, C_2p+1) of the tile being walked
+    // per channel j: lane q's y terms of 8 steps at [j][12 q + u] (rows of 104 floats: the
+    // column sums read 8 lanes' rows without bank conflicts)
+    float yx[kSqCh][104];
 };
 
 struct SelSeqGeom {
@@ -432,19 +435,33 @@ sel_fwd_seq_kernel(const bf16 *__restrict__ x, const float *__restrict__ delta, 
                         }
                         v[u] = acc.x + acc.y;
                     }
-                    // sum over the channel's lanes; lane q ends with step q's total
+                    // sum over the channel's lanes through shared memory: lane q adds step q's
+                    // terms of the channel's 8 lanes, in lane order
+                    float yv;
+                    if constexpr (G == 8) {
+                        float *yr = sm.yx[j];
+                        *reinterpret_cast<float4 *>(yr + 12 * q) = make_float4(v[0], v[1], v[2], v[3]);
+                        *reinterpret_cast<float4 *>(yr + 12 * q + 4) = make_float4(v[4], v[5], v[6], v[7]);
+                        __syncwarp();
+                        yv = yr[q];
 #pragma unroll
-                    for (int m = G / 2; m >= 1; m >>= 1) {
-                        const bool up = q & m;
+                        for (int i = 1; i < 8; ++i) yv += yr[12 * i + q];
+                        __syncwarp();  // read before the next group's terms overwrite them
+                    } else {  // 4 lanes: exchange by shuffles, lane q ends with step q's total
 #pragma unroll
-                        for (int i = 0; i < m; ++i) {
-                            const float keep = up ? v[i + m] : v[i];
-                            const float send = up ? v[i] : v[i + m];
-                            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                        for (int m = G / 2; m >= 1; m >>= 1) {
+                            const bool up = q & m;
+#pragma unroll
+                            for (int i = 0; i < m; ++i) {
+                                const float keep = up ? v[i + m] : v[i];
+                                const float send = up ? v[i] : v[i + m];
+                                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                            }
                         }
+                        yv = v[0];
                     }
                     const long long t = t0 + s16 + sg + q;
-                    if (t < g.T) __stcs(y + ((size_t)bi * g.T + t) * g.D + c, v[0]);
+                    if (t < g.T) __stcs(y + ((size_t)bi * g.T + t) * g.D + c, yv);
                 }
             }
         };
