@@ -68,6 +68,7 @@ struct GlaArgs {
     unsigned int *flags;  // [unit]
     float *alpha;         // [unit][DK]
     float4 *agg, *incl;   // [unit][tiles][threads]
+    float *seg_out;       // [n_seg][BH][DK][DV] or NULL: the state entering each segment, saved
 };
 
 // ----------------------------------------------------------------- forward on tcgen05
@@ -565,6 +566,13 @@ __global__ void __launch_bounds__(kGlaTcThreads, GlaTcCfg<DK>::MIN_BLOCKS)
         __syncthreads();
         if (tid == 0) st_release(p.flags + unit, 2u);
     }
+    if (p.seg_out != nullptr) {  // this segment's incoming state, for a later traversal
+        float4 *dst = reinterpret_cast<float4 *>(p.seg_out + (((size_t)seg * p.BH + bh) * DK + srow) * p.DV +
+                                                 zb * 64 + scol(0));
+#pragma unroll
+        for (int tl = 0; tl < TILES; ++tl)
+            __stcg(dst + tl, make_float4(Sin[4 * tl], Sin[4 * tl + 1], Sin[4 * tl + 2], Sin[4 * tl + 3]));
+    }
 
     // ------------------------------------------------ phase 2: outputs from the true state
 #pragma unroll
@@ -651,6 +659,9 @@ struct GlaBArgs {
     unsigned int *flags;
     float *alpha;  // [unit][64]
     float4 *agg, *incl;
+    // [n_seg][BH][DK][DV] or NULL: the state entering each segment (in traversal order), saved
+    // by an earlier traversal with the same segments; phase 1 and the look-back are then skipped
+    const float *seg_in;
 };
 
 // ----------------------------------------------------------------- dQ / dK traversal on tcgen05
@@ -995,101 +1006,108 @@ __global__ void __launch_bounds__(kGlaTcThreads, 1)
         tc_fence_after();
     };
 
-    // ------------------------------------------------ phase 1
-#pragma unroll
-    for (int j = 0; j < SC; ++j) S[j] = 0.f;
-    float la_seg = 0.f;
-    // a chunk's in-chunk sums are formed while the tensor cores run the chunk before it
-    load_stage(0, c_begin, false);
-    if (nc > 1) load_stage(1, c_begin + 1, false);
-    stage_ready(0);
-    la_seg += cumulate(0, c_begin);
-    __syncthreads();
-    for (int i = 0; i < nc; ++i) {
-        const int stage = i & 1;
-        scale_z(stage);
-        state_to_mid(stage);
-        hand_to_tc();
-        if (warp == 0) {
-            issue_u(stage);
-            mma_commit_w(barA);
-        }
-        if (i + 1 < nc) {
-            stage_ready(stage ^ 1);
-            la_seg += cumulate(stage ^ 1, c_begin + i + 1);
-        }
-        waitA();
-        tc_fence_after();
-        state_finish(stage);
-        fence_async_smem();  // this thread's writes to the stage before its reload
-        tc_fence_before();
-        __syncthreads();
-        if (i + 2 < nc) load_stage(stage, c_begin + i + 2, false);
-    }
-
-    // ------------------------------------------------ look-back
     constexpr int TILES = SC / 4;
-    auto ws_index = [&](size_t u, int tile) {
-        return u * (size_t)(TILES * kGlaTcThreads) + (size_t)tile * kGlaTcThreads + tid;
-    };
     float Sin[SC];
+    if (p.seg_in != nullptr) {
+        // the incoming state saved by an earlier traversal: no phase 1, no look-back
+        const float *src = p.seg_in + (((size_t)seg * p.BH + bh) * p.DK + zb * 64 + srow) * DV;
 #pragma unroll
-    for (int j = 0; j < SC; ++j) Sin[j] = 0.f;
-    auto add_state0 = [&](float scale) {
-        if (p.S0 == nullptr) return;
-#pragma unroll
-        for (int j = 0; j < SC; ++j)
-            Sin[j] = fmaf(scale, __ldg(p.S0 + ((size_t)bh * p.DK + zb * 64 + srow) * DV + scol(j)), Sin[j]);
-    };
-    if (cdim >= 0) alpha_s[cdim] = ex2(la_seg);
-    if (seg == 0) {
-        add_state0(1.f);
+        for (int j = 0; j < SC; ++j) Sin[j] = __ldg(src + scol(j));
     } else {
+        // ------------------------------------------------ phase 1
 #pragma unroll
-        for (int tl = 0; tl < TILES; ++tl)
-            __stcg(p.agg + ws_index(unit, tl), make_float4(S[4 * tl], S[4 * tl + 1], S[4 * tl + 2], S[4 * tl + 3]));
-        if (cdim >= 0) __stcg(p.alpha + unit * 64 + cdim, ex2(la_seg));
-        __threadfence();
+        for (int j = 0; j < SC; ++j) S[j] = 0.f;
+        float la_seg = 0.f;
+        // a chunk's in-chunk sums are formed while the tensor cores run the chunk before it
+        load_stage(0, c_begin, false);
+        if (nc > 1) load_stage(1, c_begin + 1, false);
+        stage_ready(0);
+        la_seg += cumulate(0, c_begin);
         __syncthreads();
-        if (tid == 0) st_release(p.flags + unit, 1u);
-        float accA = 1.f;
-        int j = seg - 1;
-        while (true) {
-            const size_t up = ((size_t)j * p.BH + bh) * p.nzb + zb;
-            if (tid == 0) s_flag = wait_flag(p.flags + up, p.hdr, 64u);
-            __syncthreads();
-            const unsigned int f = s_flag;
-            __syncthreads();
-            if (f != 1u && f != 2u) break;
-            const float4 *src = (f == 2u) ? p.incl : p.agg;
-#pragma unroll
-            for (int tl = 0; tl < TILES; ++tl) {
-                const float4 v = ld_cg4(src + ws_index(up, tl));
-                Sin[4 * tl] = fmaf(accA, v.x, Sin[4 * tl]);
-                Sin[4 * tl + 1] = fmaf(accA, v.y, Sin[4 * tl + 1]);
-                Sin[4 * tl + 2] = fmaf(accA, v.z, Sin[4 * tl + 2]);
-                Sin[4 * tl + 3] = fmaf(accA, v.w, Sin[4 * tl + 3]);
+        for (int i = 0; i < nc; ++i) {
+            const int stage = i & 1;
+            scale_z(stage);
+            state_to_mid(stage);
+            hand_to_tc();
+            if (warp == 0) {
+                issue_u(stage);
+                mma_commit_w(barA);
             }
-            if (f == 2u) break;
-            accA *= ld_cg(p.alpha + up * 64 + srow);
-            if (--j < 0) {
-                add_state0(accA);
-                break;
+            if (i + 1 < nc) {
+                stage_ready(stage ^ 1);
+                la_seg += cumulate(stage ^ 1, c_begin + i + 1);
+            }
+            waitA();
+            tc_fence_after();
+            state_finish(stage);
+            fence_async_smem();  // this thread's writes to the stage before its reload
+            tc_fence_before();
+            __syncthreads();
+            if (i + 2 < nc) load_stage(stage, c_begin + i + 2, false);
+        }
+
+        // ------------------------------------------------ look-back
+        auto ws_index = [&](size_t u, int tile) {
+            return u * (size_t)(TILES * kGlaTcThreads) + (size_t)tile * kGlaTcThreads + tid;
+        };
+#pragma unroll
+        for (int j = 0; j < SC; ++j) Sin[j] = 0.f;
+        auto add_state0 = [&](float scale) {
+            if (p.S0 == nullptr) return;
+#pragma unroll
+            for (int j = 0; j < SC; ++j)
+                Sin[j] = fmaf(scale, __ldg(p.S0 + ((size_t)bh * p.DK + zb * 64 + srow) * DV + scol(j)), Sin[j]);
+        };
+        if (cdim >= 0) alpha_s[cdim] = ex2(la_seg);
+        if (seg == 0) {
+            add_state0(1.f);
+        } else {
+#pragma unroll
+            for (int tl = 0; tl < TILES; ++tl)
+                __stcg(p.agg + ws_index(unit, tl), make_float4(S[4 * tl], S[4 * tl + 1], S[4 * tl + 2], S[4 * tl + 3]));
+            if (cdim >= 0) __stcg(p.alpha + unit * 64 + cdim, ex2(la_seg));
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) st_release(p.flags + unit, 1u);
+            float accA = 1.f;
+            int j = seg - 1;
+            while (true) {
+                const size_t up = ((size_t)j * p.BH + bh) * p.nzb + zb;
+                if (tid == 0) s_flag = wait_flag(p.flags + up, p.hdr, 64u);
+                __syncthreads();
+                const unsigned int f = s_flag;
+                __syncthreads();
+                if (f != 1u && f != 2u) break;
+                const float4 *src = (f == 2u) ? p.incl : p.agg;
+#pragma unroll
+                for (int tl = 0; tl < TILES; ++tl) {
+                    const float4 v = ld_cg4(src + ws_index(up, tl));
+                    Sin[4 * tl] = fmaf(accA, v.x, Sin[4 * tl]);
+                    Sin[4 * tl + 1] = fmaf(accA, v.y, Sin[4 * tl + 1]);
+                    Sin[4 * tl + 2] = fmaf(accA, v.z, Sin[4 * tl + 2]);
+                    Sin[4 * tl + 3] = fmaf(accA, v.w, Sin[4 * tl + 3]);
+                }
+                if (f == 2u) break;
+                accA *= ld_cg(p.alpha + up * 64 + srow);
+                if (--j < 0) {
+                    add_state0(accA);
+                    break;
+                }
             }
         }
-    }
-    __syncthreads();
-    if (seg != p.n_seg - 1) {
-        const float a = alpha_s[srow];
-#pragma unroll
-        for (int tl = 0; tl < TILES; ++tl)
-            __stcg(p.incl + ws_index(unit, tl),
-                   make_float4(fmaf(a, Sin[4 * tl], S[4 * tl]), fmaf(a, Sin[4 * tl + 1], S[4 * tl + 1]),
-                               fmaf(a, Sin[4 * tl + 2], S[4 * tl + 2]), fmaf(a, Sin[4 * tl + 3], S[4 * tl + 3])));
-        __threadfence();
         __syncthreads();
-        if (tid == 0) st_release(p.flags + unit, 2u);
-    }
+        if (seg != p.n_seg - 1) {
+            const float a = alpha_s[srow];
+#pragma unroll
+            for (int tl = 0; tl < TILES; ++tl)
+                __stcg(p.incl + ws_index(unit, tl),
+                       make_float4(fmaf(a, Sin[4 * tl], S[4 * tl]), fmaf(a, Sin[4 * tl + 1], S[4 * tl + 1]),
+                                   fmaf(a, Sin[4 * tl + 2], S[4 * tl + 2]), fmaf(a, Sin[4 * tl + 3], S[4 * tl + 3])));
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) st_release(p.flags + unit, 2u);
+        }
+    }  // phase 1 and look-back
 
     // ------------------------------------------------ phase 2
 #pragma unroll
@@ -1282,7 +1300,8 @@ void gla_segments(int64_t BH, int n_chunks, int nzb, int &seg_chunks, int &n_seg
 // turn), the final-state term per key dimension and the decay gradient's tile sums.
 struct GlaBwdPlan {
     int n_chunks, segA, nsegA, segB, nsegB, tiles;
-    size_t off_flags, off_alpha, off_agg, off_incl, off_fs, off_tsum, total;
+    bool reuse;  // the dV and dK traversals have the same segments: dK starts from dV's states
+    size_t off_flags, off_alpha, off_agg, off_incl, off_fs, off_tsum, off_seg, total;
 };
 
 GlaBwdPlan gla_bwd_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv) {
@@ -1303,7 +1322,9 @@ GlaBwdPlan gla_bwd_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv)
     p.off_incl = align_up(p.off_agg + state_floats * 4, 256);
     p.off_fs = align_up(p.off_incl + state_floats * 4, 256);
     p.off_tsum = align_up(p.off_fs + (size_t)BH * dk * 4, 256);
-    p.total = align_up(p.off_tsum + (size_t)BH * p.tiles * dk * 4, 256);
+    p.off_seg = align_up(p.off_tsum + (size_t)BH * p.tiles * dk * 4, 256);
+    p.reuse = p.segA == p.segB;
+    p.total = p.off_seg + (p.reuse ? align_up((size_t)p.nsegA * BH * dk * dv * 4, 256) : 0);
     return p;
 }
 
@@ -1524,6 +1545,9 @@ extern "C" int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t 
     a.alpha = reinterpret_cast<float *>(w + pl.off_alpha);
     a.agg = reinterpret_cast<float4 *>(w + pl.off_agg);
     a.incl = reinterpret_cast<float4 *>(w + pl.off_incl);
+    // the adjoint state entering each segment, which the dK traversal (same segments, same
+    // state) then starts from instead of running its phase 1 and look-back
+    if (pl.reuse) a.seg_out = reinterpret_cast<float *>(w + pl.off_seg);
     const unsigned int gridA = (unsigned int)((size_t)pl.nsegA * BH * (dim_v / 64));
     st = dim_k == 64 ? launch_gla_fwd<64>(a, s, gridA) : launch_gla_fwd<128>(a, s, gridA);
     if (st) return st;
@@ -1535,6 +1559,7 @@ extern "C" int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t 
     b.y = DO;
     b.z = Q;
     b.out = dk;
+    if (pl.reuse) b.seg_in = reinterpret_cast<const float *>(w + pl.off_seg);
     st = dim_v == 64 ? launch_gla_bwd_qk<64>(b, s, gridB) : launch_gla_bwd_qk<128>(b, s, gridB);
     if (st) return st;
 

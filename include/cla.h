@@ -357,8 +357,11 @@ int cla_gla_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                 int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
                 int chunk, void *ws, size_t ws_bytes, void *stream);
 
-/* Bytes of workspace for cla_gla_bwd; 0 for sizes, head dims or chunks that
- * call refuses. */
+/* Bytes of workspace for cla_gla_bwd (look-back arrays, the decay
+ * gradient's partial sums and, when the dV and dK traversals get the same
+ * segments of chunks, the adjoint state entering each segment, which the dV
+ * traversal saves and the dK traversal starts from); 0 for sizes, head dims
+ * or chunks that call refuses. */
 size_t cla_gla_bwd_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
                                   int64_t dim_v, int chunk);
 

@@ -134,6 +134,14 @@ def test_gla_bwd_strong_decay_within_range(cla):
     _run(cla, inp, bwd=True, dST=dST)
 
 
+def test_gla_bwd_unequal_segments_sampled_heads(cla):
+    """d_k = 128, d_v = 64 on 32 heads of 16384 tokens: the dV traversal (one column block) and
+    the dK traversal (two key blocks) pick different segment lengths, so dK runs its own phase 1
+    and look-back instead of starting from dV's segment states; two heads checked."""
+    inp = workloads.make("gla", B=2, H=16, T=16384, dk=128, dv=64)
+    _run(cla, inp, heads=[0, 13], bwd=True)
+
+
 def test_gla_bwd_workload_full_sampled_heads(cla):
     """The full gla workload, backward, every output of two heads."""
     inp = workloads.make("gla")
