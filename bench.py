@@ -473,10 +473,15 @@ def bench_gla(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
     grads = dict(dq=torch.empty(B, H, T, dk, device=dev), dk=torch.empty(B, H, T, dk, device=dev),
                  dv=torch.empty(B, H, T, dv, device=dev), dlog_decay=torch.empty(B, H, T, dk, device=dev),
                  dS0=torch.empty(B, H, dk, dv, device=dev))
-    fwd = lambda: cla.gla_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], o=o, ST=ST, workspace=ws)
-    bwd = lambda: cla.gla_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"], workspace=wb, **grads)
+    # the training step's path: the forward saves the state entering every segment, the
+    # backward's dq traversal starts from it
+    ck = cla.gla_ckpt(t["q"], t["v"])
+    fwd = lambda: cla.gla_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], o=o, ST=ST, ckpt=ck, workspace=ws)
+    bwd = lambda ckpt: cla.gla_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"], ckpt=ckpt, workspace=wb,
+                                   **grads)
     tf = _time_calls(torch, fwd, flush, iters)
-    tb = _time_calls(torch, bwd, flush, iters)
+    tb = _time_calls(torch, lambda: bwd(ck), flush, iters)
+    tb_plain = _time_calls(torch, lambda: bwd(None), flush, iters)
     cla.check_status(ws)
     cla.check_status(wb)
     ntok = B * H * T
@@ -491,7 +496,10 @@ def bench_gla(torch, cla, workloads, dev, flush, peaks, iters=20, shape=None):
     bf = peaks["bf16_tflops"] * 1e12
     sec, secb = tf / 1e3, tb / 1e3
     res = {"workload": f"gated linear attention fwd+bwd B={B} H={H} T={T} dk={dk} dv={dv} chunk=64",
-           "fwd_us": round(tf * 1e3, 1), "bwd_us": round(tb * 1e3, 1), "tokens_per_s": round(B * T / (sec + secb), 1),
+           "fwd_us": round(tf * 1e3, 1), "bwd_us": round(tb * 1e3, 1),
+           "bwd_us_without_checkpoint": round(tb_plain * 1e3, 1),
+           "checkpoint": "the forward saves the state entering every segment; the backward's dq traversal starts from it",
+           "tokens_per_s": round(B * T / (sec + secb), 1),
            "fwd_TFLOPs": round(fl / sec / 1e12, 2), "bwd_TFLOPs": round(fl_b / secb / 1e12, 2),
            "fwd_GBps": round(by / sec / 1e9, 1),
            "frac_bf16_peak": round((fl + fl_b) / (sec + secb) / bf, 4),

@@ -68,6 +68,9 @@ def lib():
                 "cla_gla_fwd": ([P] * 7 + [I64] * 5 + [INT, P, SZ, P], INT),
                 "cla_gla_bwd_workspace_size": ([I64] * 5 + [INT], SZ),
                 "cla_gla_bwd": ([P] * 12 + [I64] * 5 + [INT, P, SZ, P], INT),
+                "cla_gla_ckpt_size": ([I64] * 5 + [INT], SZ),
+                "cla_gla_fwd_ckpt": ([P] * 8 + [I64] * 5 + [INT, P, SZ, P], INT),
+                "cla_gla_bwd_ckpt": ([P] * 13 + [I64] * 5 + [INT, P, SZ, P], INT),
                 "cla_decay_total": ([P, P, I64, I64, I64, P], INT),
                 "cla_delta_workspace_size": ([I64] * 5 + [INT], SZ),
                 "cla_delta_fwd": ([P] * 8 + [I64] * 5 + [INT, P, SZ, P], INT),
@@ -399,9 +402,29 @@ def gla_workspace_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
     return int(lib().cla_gla_workspace_size(B, H, T, dim_k, dim_v, int(chunk)))
 
 
-def gla_fwd(q, k, v, log_decay, S0=None, *, chunk=64, o=None, ST=None, workspace=None, stream=None):
+def gla_ckpt_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
+    """Bytes of the segment-state checkpoint the GLA forward can save for the backward."""
+    return int(lib().cla_gla_ckpt_size(B, H, T, dim_k, dim_v, int(chunk)))
+
+
+def gla_ckpt(q, v, *, chunk=64):
+    """A device buffer (fp32) for the checkpoint of a gla_fwd on q [B, H, T, dk], v [.., dv]."""
+    B, H, T, dk = _dims(q, 4, "q")
+    n = gla_ckpt_size(B, H, T, dk, v.shape[-1], chunk) // 4
+    return torch.empty(max(n, 1), dtype=torch.float32, device=q.device)
+
+
+def _gla_ckpt_arg(ckpt, B, H, T, dk, dv, chunk):
+    need = gla_ckpt_size(B, H, T, dk, dv, chunk)
+    if _nbytes(ckpt) < need:
+        raise ValueError(f"ckpt: need at least {need} bytes, got {_nbytes(ckpt)}")
+    return _T(ckpt, torch.float32, "ckpt")
+
+
+def gla_fwd(q, k, v, log_decay, S0=None, *, chunk=64, o=None, ST=None, ckpt=None, workspace=None, stream=None):
     """Gated linear attention forward (one decay per key dimension: log_decay [B, H, T, dk]);
-    returns (o, ST).  check_status(workspace) reports decays outside the kernel's range."""
+    returns (o, ST).  check_status(workspace) reports decays outside the kernel's range.  With
+    ckpt (see gla_ckpt) it also saves the state entering every segment for gla_bwd."""
     B, H, T, dk = _dims(q, 4, "q")
     dv = _dims(v, 4, "v")[3]
     dev = q.device
@@ -410,11 +433,14 @@ def gla_fwd(q, k, v, log_decay, S0=None, *, chunk=64, o=None, ST=None, workspace
     ST = _out(ST, (B, H, dk, dv), f32, dev)
     ws = _ws(gla_workspace_size(B, H, T, dk, dv, chunk), dev, workspace)
     tk, tv, st = (B, H, T, dk), (B, H, T, dv), (B, H, dk, dv)
-    _launch("cla_gla_fwd", dev, (
-        _T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
-        _T(log_decay, f32, "log_decay", tk), _T(S0, f32, "S0", st),
-        _T(o, f32, "o", tv), _T(ST, f32, "ST", st),
-        B, H, T, dk, dv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws)), stream)
+    args = (_T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
+            _T(log_decay, f32, "log_decay", tk), _T(S0, f32, "S0", st),
+            _T(o, f32, "o", tv), _T(ST, f32, "ST", st))
+    tail = (B, H, T, dk, dv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws))
+    if ckpt is None:
+        _launch("cla_gla_fwd", dev, args + tail, stream)
+    else:
+        _launch("cla_gla_fwd_ckpt", dev, args + (_gla_ckpt_arg(ckpt, B, H, T, dk, dv, chunk),) + tail, stream)
     return o, ST
 
 
@@ -423,8 +449,10 @@ def gla_bwd_workspace_size(B, H, T, dim_k, dim_v, chunk=64) -> int:
 
 
 def gla_bwd(q, k, v, log_decay, S0, dO, dST=None, *, chunk=64, dq=None, dk=None, dv=None, dlog_decay=None,
-            dS0=None, workspace=None, stream=None):
-    """Gated linear attention backward; returns (dq, dk, dv, dlog_decay [B, H, T, dk], dS0)."""
+            dS0=None, ckpt=None, workspace=None, stream=None):
+    """Gated linear attention backward; returns (dq, dk, dv, dlog_decay [B, H, T, dk], dS0).  ckpt:
+    the checkpoint a gla_fwd(..., ckpt=) on the same inputs saved (its dq traversal then starts
+    from it)."""
     B, H, T, dkk = _dims(q, 4, "q")
     dvv = _dims(v, 4, "v")[3]
     dev = q.device
@@ -436,12 +464,15 @@ def gla_bwd(q, k, v, log_decay, S0, dO, dST=None, *, chunk=64, dq=None, dk=None,
     dS0 = _out(dS0, (B, H, dkk, dvv), f32, dev)
     ws = _ws(gla_bwd_workspace_size(B, H, T, dkk, dvv, chunk), dev, workspace)
     tk, tv, st = (B, H, T, dkk), (B, H, T, dvv), (B, H, dkk, dvv)
-    _launch("cla_gla_bwd", dev, (
-        _T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
-        _T(log_decay, f32, "log_decay", tk), _T(S0, f32, "S0", st), _T(dO, bf16, "dO", tv),
-        _T(dST, f32, "dST", st), _T(dq, f32, "dq", tk), _T(dk, f32, "dk", tk), _T(dv, f32, "dv", tv),
-        _T(dlog_decay, f32, "dlog_decay", tk), _T(dS0, f32, "dS0", st),
-        B, H, T, dkk, dvv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws)), stream)
+    args = (_T(q, bf16, "q", tk), _T(k, bf16, "k", tk), _T(v, bf16, "v", tv),
+            _T(log_decay, f32, "log_decay", tk), _T(S0, f32, "S0", st), _T(dO, bf16, "dO", tv),
+            _T(dST, f32, "dST", st), _T(dq, f32, "dq", tk), _T(dk, f32, "dk", tk), _T(dv, f32, "dv", tv),
+            _T(dlog_decay, f32, "dlog_decay", tk), _T(dS0, f32, "dS0", st))
+    tail = (B, H, T, dkk, dvv, int(chunk), _T(ws, None, "workspace"), _nbytes(ws))
+    if ckpt is None:
+        _launch("cla_gla_bwd", dev, args + tail, stream)
+    else:
+        _launch("cla_gla_bwd_ckpt", dev, args + (_gla_ckpt_arg(ckpt, B, H, T, dkk, dvv, chunk),) + tail, stream)
     return dq, dk, dv, dlog_decay, dS0
 
 

@@ -1244,21 +1244,29 @@ struct GlaPlan {
     size_t units, off_flags, off_alpha, off_agg, off_incl, total;
 };
 
+// Segments of chunks, the same for every traversal of one head's sequence (the forward, dQ, dV,
+// dK), so that a state one traversal forms at a segment's start can start another: the largest
+// of kGlaSegChoices that still gives kGlaMinBlocks blocks to the traversal with the most column
+// blocks (max(d_k, d_v) / 64 per head).
+void gla_segments(int64_t BH, int n_chunks, int64_t dk, int64_t dv, int &seg_chunks, int &n_seg) {
+    const int64_t nzb = (dk > dv ? dk : dv) / 64;
+    seg_chunks = kGlaSegChoices[3];
+    for (int c : kGlaSegChoices) {
+        if ((long long)((n_chunks + c - 1) / c) * BH * nzb >= kGlaMinBlocks) {
+            seg_chunks = c;
+            break;
+        }
+    }
+    n_seg = (n_chunks + seg_chunks - 1) / seg_chunks;
+    if (n_seg < 1) n_seg = 1;
+}
+
 GlaPlan gla_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv) {
     GlaPlan p;
     p.n_chunks = (int)((T + kGlaTc - 1) / kGlaTc);
     p.nzb = (int)(dv / 64);
     const size_t BH = (size_t)B * H;
-    p.seg_chunks = kGlaSegChoices[3];
-    for (int c : kGlaSegChoices) {
-        const long long nseg = (p.n_chunks + c - 1) / c;
-        if (nseg * (long long)BH * p.nzb >= kGlaMinBlocks) {
-            p.seg_chunks = c;
-            break;
-        }
-    }
-    p.n_seg = (p.n_chunks + p.seg_chunks - 1) / p.seg_chunks;
-    if (p.n_seg < 1) p.n_seg = 1;
+    gla_segments((int64_t)BH, p.n_chunks, dk, dv, p.seg_chunks, p.n_seg);
     p.units = (size_t)p.n_seg * BH * p.nzb;
     p.off_flags = sizeof(WsHeader);
     p.off_alpha = align_up(p.off_flags + p.units * 4, 256);
@@ -1283,24 +1291,11 @@ bool gla_supported(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int 
            chunk == kGlaTc && gla_sizes_fit(B, H, T);
 }
 
-// Segments for a traversal with nzb column blocks per head (the forward's rule).
-void gla_segments(int64_t BH, int n_chunks, int nzb, int &seg_chunks, int &n_seg) {
-    seg_chunks = kGlaSegChoices[3];
-    for (int c : kGlaSegChoices) {
-        if ((long long)((n_chunks + c - 1) / c) * BH * nzb >= kGlaMinBlocks) {
-            seg_chunks = c;
-            break;
-        }
-    }
-    n_seg = (n_chunks + seg_chunks - 1) / seg_chunks;
-    if (n_seg < 1) n_seg = 1;
-}
 
 // Backward workspace: the look-back arrays of the largest traversal (reused by the three in
 // turn), the final-state term per key dimension and the decay gradient's tile sums.
 struct GlaBwdPlan {
-    int n_chunks, segA, nsegA, segB, nsegB, tiles;
-    bool reuse;  // the dV and dK traversals have the same segments: dK starts from dV's states
+    int n_chunks, seg_chunks, n_seg, tiles;
     size_t off_flags, off_alpha, off_agg, off_incl, off_fs, off_tsum, off_seg, total;
 };
 
@@ -1308,9 +1303,8 @@ GlaBwdPlan gla_bwd_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv)
     GlaBwdPlan p;
     const int64_t BH = B * H;
     p.n_chunks = (int)((T + kGlaTc - 1) / kGlaTc);
-    gla_segments(BH, p.n_chunks, (int)(dv / 64), p.segA, p.nsegA);
-    gla_segments(BH, p.n_chunks, (int)(dk / 64), p.segB, p.nsegB);
-    const size_t unitsA = (size_t)p.nsegA * BH * (dv / 64), unitsB = (size_t)p.nsegB * BH * (dk / 64);
+    gla_segments(BH, p.n_chunks, dk, dv, p.seg_chunks, p.n_seg);
+    const size_t unitsA = (size_t)p.n_seg * BH * (dv / 64), unitsB = (size_t)p.n_seg * BH * (dk / 64);
     const size_t units = unitsA > unitsB ? unitsA : unitsB;
     const size_t alpha_floats = unitsA * dk > unitsB * 64 ? unitsA * dk : unitsB * 64;
     const size_t state_floats = unitsA * dk * 64 > unitsB * 64 * dv ? unitsA * dk * 64 : unitsB * 64 * dv;
@@ -1322,9 +1316,9 @@ GlaBwdPlan gla_bwd_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv)
     p.off_incl = align_up(p.off_agg + state_floats * 4, 256);
     p.off_fs = align_up(p.off_incl + state_floats * 4, 256);
     p.off_tsum = align_up(p.off_fs + (size_t)BH * dk * 4, 256);
+    // the adjoint state entering each segment: saved by the dV traversal, read by the dK one
     p.off_seg = align_up(p.off_tsum + (size_t)BH * p.tiles * dk * 4, 256);
-    p.reuse = p.segA == p.segB;
-    p.total = p.off_seg + (p.reuse ? align_up((size_t)p.nsegA * BH * dk * dv * 4, 256) : 0);
+    p.total = p.off_seg + align_up((size_t)p.n_seg * BH * dk * dv * 4, 256);
     return p;
 }
 
@@ -1387,11 +1381,11 @@ extern "C" size_t cla_gla_workspace_size(int64_t B, int64_t H, int64_t T, int64_
     return gla_plan(B, H, T, dim_k, dim_v).total;
 }
 
-extern "C" int cla_gla_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
-                           const float *S0, float *o, float *ST, int64_t B, int64_t H, int64_t T, int64_t dim_k,
-                           int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
+namespace {
+int gla_fwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                 const float *S0, float *o, float *ST, float *ckpt, int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                 int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
     clear_error();
-    const char *fn = "cla_gla_fwd";
     if (B < 0 || H < 0 || T < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
     if (!gla_supported(B, H, T, dim_k, dim_v, chunk))
         return fail(CLA_ERR_UNSUPPORTED, "%s: needs dim_k 64 or 128, dim_v a multiple of 64 up to 1024, chunk 64 "
@@ -1440,8 +1434,35 @@ extern "C" int cla_gla_fwd(const uint16_t *q, const uint16_t *k, const uint16_t 
     a.alpha = reinterpret_cast<float *>(w + pl.off_alpha);
     a.agg = reinterpret_cast<float4 *>(w + pl.off_agg);
     a.incl = reinterpret_cast<float4 *>(w + pl.off_incl);
+    a.seg_out = ckpt;  // [n_seg][BH][dim_k][dim_v]: the state entering each segment
     const unsigned int grid = (unsigned int)(pl.units);
     return dim_k == 64 ? launch_gla_fwd<64>(a, s, grid) : launch_gla_fwd<128>(a, s, grid);
+}
+}  // namespace
+
+extern "C" int cla_gla_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                           const float *S0, float *o, float *ST, int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                           int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
+    return gla_fwd_impl("cla_gla_fwd", q, k, v, log_decay, S0, o, ST, nullptr, B, H, T, dim_k, dim_v, chunk, ws,
+                        ws_bytes, stream);
+}
+
+extern "C" size_t cla_gla_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk) {
+    if (!gla_supported(B, H, T, dim_k, dim_v, chunk) || !gla_bwd_supported(B, H, T, dim_k, dim_v, chunk)) return 0;
+    const GlaPlan pl = gla_plan(B, H, T, dim_k, dim_v);
+    return (size_t)pl.n_seg * (size_t)(B * H) * (size_t)dim_k * (size_t)dim_v * sizeof(float);
+}
+
+extern "C" int cla_gla_fwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                                const float *S0, float *o, float *ST, float *ckpt, int64_t B, int64_t H, int64_t T,
+                                int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
+    if (ckpt != nullptr && !aligned16(ckpt))
+        return fail(CLA_ERR_INVALID_ARG, "cla_gla_fwd_ckpt: ckpt must be 16-byte aligned");
+    if (ckpt != nullptr && !gla_bwd_supported(B, H, T, dim_k, dim_v, chunk))
+        return fail(CLA_ERR_UNSUPPORTED, "cla_gla_fwd_ckpt: a checkpoint needs sizes the backward takes "
+                    "(dim_k and dim_v 64 or 128)");
+    return gla_fwd_impl("cla_gla_fwd_ckpt", q, k, v, log_decay, S0, o, ST, ckpt, B, H, T, dim_k, dim_v, chunk, ws,
+                        ws_bytes, stream);
 }
 
 extern "C" size_t cla_gla_bwd_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
@@ -1450,12 +1471,12 @@ extern "C" size_t cla_gla_bwd_workspace_size(int64_t B, int64_t H, int64_t T, in
     return gla_bwd_plan(B, H, T, dim_k, dim_v).total;
 }
 
-extern "C" int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
-                           const float *S0, const uint16_t *dO, const float *dST, float *dq, float *dk, float *dv,
-                           float *dlog_decay, float *dS0, int64_t B, int64_t H, int64_t T, int64_t dim_k,
-                           int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
+namespace {
+int gla_bwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                 const float *S0, const uint16_t *dO, const float *dST, float *dq, float *dk, float *dv,
+                 float *dlog_decay, float *dS0, const float *ckpt, int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                 int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
     clear_error();
-    const char *fn = "cla_gla_bwd";
     if (B < 0 || H < 0 || T < 0) return fail(CLA_ERR_INVALID_ARG, "%s: negative size", fn);
     if (!gla_bwd_supported(B, H, T, dim_k, dim_v, chunk))
         return fail(CLA_ERR_UNSUPPORTED, "%s: needs dim_k and dim_v 64 or 128, chunk 64 and sizes within one launch "
@@ -1495,8 +1516,8 @@ extern "C" int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t 
         b.DK = (int)dim_k;
         b.nzb = (int)(dim_k / 64);
         b.n_chunks = pl.n_chunks;
-        b.seg_chunks = pl.segB;
-        b.n_seg = pl.nsegB;
+        b.seg_chunks = pl.seg_chunks;
+        b.n_seg = pl.n_seg;
         b.T = T;
         b.hdr = reinterpret_cast<WsHeader *>(w);
         b.flags = reinterpret_cast<unsigned int *>(w + pl.off_flags);
@@ -1505,7 +1526,7 @@ extern "C" int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t 
         b.incl = reinterpret_cast<float4 *>(w + pl.off_incl);
         return b;
     };
-    const unsigned int gridB = (unsigned int)((size_t)pl.nsegB * BH * (dim_k / 64));
+    const unsigned int gridB = (unsigned int)((size_t)pl.n_seg * BH * (dim_k / 64));
     int st;
     // dQ: forward traversal, X = dO, Y = V, Z = K, the state from S0; its final state dotted
     // with dST gives the decay gradient's final-state term
@@ -1518,6 +1539,7 @@ extern "C" int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t 
     b.out = dq;
     b.fs_dot = dST;
     b.fs_part = fs;
+    b.seg_in = ckpt;  // the forward's state entering each segment (the same segments), if saved
     st = dim_v == 64 ? launch_gla_bwd_qk<64>(b, s, gridB) : launch_gla_bwd_qk<128>(b, s, gridB);
     if (st) return st;
 
@@ -1537,8 +1559,8 @@ extern "C" int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t 
     a.DV = (int)dim_v;
     a.nzb = (int)(dim_v / 64);
     a.n_chunks = pl.n_chunks;
-    a.seg_chunks = pl.segA;
-    a.n_seg = pl.nsegA;
+    a.seg_chunks = pl.seg_chunks;
+    a.n_seg = pl.n_seg;
     a.T = T;
     a.hdr = reinterpret_cast<WsHeader *>(w);
     a.flags = reinterpret_cast<unsigned int *>(w + pl.off_flags);
@@ -1547,8 +1569,8 @@ extern "C" int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t 
     a.incl = reinterpret_cast<float4 *>(w + pl.off_incl);
     // the adjoint state entering each segment, which the dK traversal (same segments, same
     // state) then starts from instead of running its phase 1 and look-back
-    if (pl.reuse) a.seg_out = reinterpret_cast<float *>(w + pl.off_seg);
-    const unsigned int gridA = (unsigned int)((size_t)pl.nsegA * BH * (dim_v / 64));
+    a.seg_out = reinterpret_cast<float *>(w + pl.off_seg);
+    const unsigned int gridA = (unsigned int)((size_t)pl.n_seg * BH * (dim_v / 64));
     st = dim_k == 64 ? launch_gla_fwd<64>(a, s, gridA) : launch_gla_fwd<128>(a, s, gridA);
     if (st) return st;
 
@@ -1559,7 +1581,7 @@ extern "C" int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t 
     b.y = DO;
     b.z = Q;
     b.out = dk;
-    if (pl.reuse) b.seg_in = reinterpret_cast<const float *>(w + pl.off_seg);
+    b.seg_in = reinterpret_cast<const float *>(w + pl.off_seg);
     st = dim_v == 64 ? launch_gla_bwd_qk<64>(b, s, gridB) : launch_gla_bwd_qk<128>(b, s, gridB);
     if (st) return st;
 
@@ -1577,4 +1599,24 @@ extern "C" int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t 
         st = check_launch("gla_dlog_finalize_kernel");
     }
     return st;
+}
+}  // namespace
+
+extern "C" int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                           const float *S0, const uint16_t *dO, const float *dST, float *dq, float *dk, float *dv,
+                           float *dlog_decay, float *dS0, int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                           int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream) {
+    return gla_bwd_impl("cla_gla_bwd", q, k, v, log_decay, S0, dO, dST, dq, dk, dv, dlog_decay, dS0, nullptr, B, H,
+                        T, dim_k, dim_v, chunk, ws, ws_bytes, stream);
+}
+
+extern "C" int cla_gla_bwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
+                                const float *S0, const uint16_t *dO, const float *dST, float *dq, float *dk,
+                                float *dv, float *dlog_decay, float *dS0, const float *ckpt, int64_t B, int64_t H,
+                                int64_t T, int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes,
+                                void *stream) {
+    if (ckpt != nullptr && !aligned16(ckpt))
+        return fail(CLA_ERR_INVALID_ARG, "cla_gla_bwd_ckpt: ckpt must be 16-byte aligned");
+    return gla_bwd_impl("cla_gla_bwd_ckpt", q, k, v, log_decay, S0, dO, dST, dq, dk, dv, dlog_decay, dS0, ckpt, B,
+                        H, T, dim_k, dim_v, chunk, ws, ws_bytes, stream);
 }

@@ -391,6 +391,38 @@ int cla_gla_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                 int64_t dim_k, int64_t dim_v, int chunk, void *ws, size_t ws_bytes,
                 void *stream);
 
+/* The GLA checkpoint ("Parallel Scan", "The backward pass is a scan in
+ * reverse": store the states or recompute them).  Every traversal of a head's
+ * sequence splits it into the same segments of chunks; the forward forms the
+ * state entering every segment, and the backward's forward-order traversal
+ * (the one that gives dq) needs exactly those states.  Bytes of the
+ * checkpoint: n_seg * B * H * dim_k * dim_v fp32 values, n_seg fixed by the
+ * sizes; 0 for sizes, head dims or chunks the fwd / bwd calls refuse. */
+size_t cla_gla_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                         int64_t dim_v, int chunk);
+
+/* cla_gla_fwd that also writes the checkpoint: ckpt (device,
+ * cla_gla_ckpt_size bytes, 16-byte aligned, owned by the caller) gets the
+ * state entering each segment, [n_seg][B * H][dim_k][dim_v].  ckpt = NULL is
+ * the plain forward; a checkpoint needs dim_k and dim_v of 64 or 128 (what
+ * the backward takes). */
+int cla_gla_fwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const float *log_decay, const float *S0, float *o, float *ST,
+                     float *ckpt, int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                     int64_t dim_v, int chunk, void *ws, size_t ws_bytes, void *stream);
+
+/* cla_gla_bwd whose dq traversal starts every segment from the checkpoint a
+ * cla_gla_fwd_ckpt call on the same q, k, v, log_decay, S0, sizes and chunk
+ * wrote (read only), instead of re-forming those states; the results are
+ * those of cla_gla_bwd up to fp32 rounding.  ckpt = NULL is cla_gla_bwd.  A
+ * checkpoint from other inputs gives wrong gradients; nothing checks it. */
+int cla_gla_bwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const float *log_decay, const float *S0, const uint16_t *dO,
+                     const float *dST, float *dq, float *dk, float *dv,
+                     float *dlog_decay, float *dS0, const float *ckpt, int64_t B,
+                     int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk,
+                     void *ws, size_t ws_bytes, void *stream);
+
 /* ======================================================================== */
 /* Delta rule with a decay per head (Gated DeltaNet)                         */
 /* ======================================================================== */

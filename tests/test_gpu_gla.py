@@ -146,3 +146,44 @@ def test_gla_bwd_workload_full_sampled_heads(cla):
     """The full gla workload, backward, every output of two heads."""
     inp = workloads.make("gla")
     _run(cla, inp, heads=[3, 12], bwd=True)
+
+
+# ---------------------------------------------------------------- checkpoint
+def _gla_seg_chunks(n_chunks, n_seg):
+    """The segment length of a checkpoint with n_seg segments (the largest of 64, 32, 16, 8 that
+    gives that count)."""
+    for c in (64, 32, 16, 8):
+        if -(-n_chunks // c) == n_seg:
+            return c
+    raise AssertionError((n_chunks, n_seg))
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv", [(1, 2, 1000, 64, 64), (1, 1, 2500, 128, 64), (2, 2, 3000, 128, 128)])
+def test_gla_checkpoint(cla, B, H, T, dk, dv):
+    """The forward saving the state entering every segment: the same o and S_T bit for bit; each
+    saved state equals the oracle's state after the tokens before its segment; the backward
+    from the checkpoint (no state rebuilding in its dq traversal) matches the oracle."""
+    inp = workloads.make("gla", B=B, H=H, T=T, dk=dk, dv=dv)
+    t = {k: _dev(v) for k, v in inp.items()}
+    dST = torch.from_numpy(np.random.default_rng(T).normal(0, 0.1, (B, H, dk, dv)).astype(np.float32))
+    ck = cla.gla_ckpt(t["q"], t["v"])
+    o1, ST1 = cla.gla_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"])
+    o2, ST2 = cla.gla_fwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], ckpt=ck)
+    assert torch.equal(o1, o2) and torch.equal(ST1, ST2)
+    n_chunks = -(-T // 64)
+    n_seg = ck.numel() // (B * H * dk * dv)
+    assert n_seg >= 2
+    seg_chunks = _gla_seg_chunks(n_chunks, n_seg)
+    ckv = ck[: n_seg * B * H * dk * dv].view(n_seg, B, H, dk, dv)
+    for sg in (0, 1, n_seg - 1):
+        t0 = sg * seg_chunks * 64
+        if t0 == 0:
+            ref = inp["S0"] if inp["S0"] is not None else torch.zeros(B, H, dk, dv)
+        else:
+            _, ref = oracle.gla_fwd(inp["q"][:, :, :t0], inp["k"][:, :, :t0], inp["v"][:, :, :t0],
+                                    inp["log_a"][:, :, :t0], inp["S0"])
+        assert_bf16(f"ckpt[{sg}]", ckv[sg], ref)
+    g = cla.gla_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"], dST.cuda(), ckpt=ck)
+    ref = oracle.gla_bwd(inp["q"], inp["k"], inp["v"], inp["log_a"], inp["S0"], inp["dO"], dST)
+    for name, x, r in zip(("dq", "dk", "dv", "dlog_a", "dS0"), g, ref):
+        assert_bf16(name, x, r)
