@@ -193,6 +193,9 @@ struct DeltaArgs {
     // [BH][n_chunks] images of (I + A)^-1 as its two bf16 parts in the swizzled [64][64] tile
     // layout (16 KB per chunk), formed beforehand by delta_wy_kernel; NULL: formed in the chunk loop
     uint8_t *wy;
+    // [BH][n_chunks][64][64] fp32 or NULL: E = strictly lower (2^(c_r - c_s) k_r . k_s) of every
+    // chunk (A without the gate strengths), written by delta_wy_kernel for the backward
+    float *E;
     int BH, DV, nzb, n_chunks;
     long long T;
     WsHeader *hdr;
@@ -222,7 +225,7 @@ __device__ __forceinline__ void delta_chunk_decays(const float *ls, const float 
 // 16 warp.. of it, K Kt on mma.sync from the swizzled K tile (QRB bytes per row).
 template <int DK, int QRB>
 __device__ __forceinline__ void delta_build_A(const uint8_t *Kt, const float *bs, const float *cs, float *Am,
-                                              int warp, int lane) {
+                                              int warp, int lane, float *Eg = nullptr) {
     const int g = lane >> 2, tq = lane & 3;
     const int arow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
     float F[8][4];
@@ -250,6 +253,17 @@ __device__ __forceinline__ void delta_build_A(const uint8_t *Kt, const float *bs
             const int r = warp * 16 + g + 8 * (e >> 1), s = nj * 8 + 2 * tq + (e & 1);
             Am[r * kAS + s] = (s < r) ? bs[r] * ex2(cs[r] - cs[s]) * F[nj][e] : 0.f;
         }
+    if (Eg != nullptr) {  // E = A without the gate strengths: the two columns of a pair in one store
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = warp * 16 + g + 8 * h, s = nj * 8 + 2 * tq;
+                const float e0 = (s < r) ? ex2(cs[r] - cs[s]) * F[nj][2 * h] : 0.f;
+                const float e1 = (s + 1 < r) ? ex2(cs[r] - cs[s + 1]) * F[nj][2 * h + 1] : 0.f;
+                __stcg(reinterpret_cast<float2 *>(Eg + r * kDlTc + s), make_float2(e0, e1));
+            }
+    }
 }
 
 // T (fp32 in Am, row stride kAS) as two bf16 parts in [64][64] tiles of 128-byte swizzled rows at
@@ -307,7 +321,8 @@ __global__ void __launch_bounds__(kDlThreads) delta_wy_kernel(const DeltaArgs p)
     float *Am = reinterpret_cast<float *>(smem + OFF_A);
     if (warp == 0) delta_chunk_decays(reinterpret_cast<const float *>(smem + OFF_L), bs, cs, lane, p.hdr);
     __syncthreads();
-    delta_build_A<DK, QRB>(smem + OFF_K, bs, cs, Am, warp, lane);
+    delta_build_A<DK, QRB>(smem + OFF_K, bs, cs, Am, warp, lane,
+                           p.E != nullptr ? p.E + ((size_t)bh * p.n_chunks + chunk) * (kDlTc * kDlTc) : nullptr);
     __syncthreads();
     tri_inverse_blocked(Am, reinterpret_cast<float *>(smem + OFF_S), tid);
     uint8_t *out = p.wy + ((size_t)bh * p.n_chunks + chunk) * (2 * kDlTc * 128);
@@ -776,6 +791,7 @@ struct DeltaBwdArgs {
     const float *dST;       // [BH][DK][DV] or NULL
     const float *states;    // [BH][n_chunks][DK][DV]
     const uint8_t *wy;      // [BH][n_chunks] (I + A)^-1 parts, as delta_wy_kernel writes them
+    const float *E;         // [BH][n_chunks][64][64]: the chunks' E, as delta_wy_kernel writes it
     float *dq, *dk, *dv, *dlog, *dbeta, *dS0;
     float *part;            // partials of the column blocks 1.. (NULL when DV == 64)
     long long part_stride;  // floats per column block: BH T (2 DK + 2)
@@ -851,10 +867,15 @@ __global__ void __launch_bounds__(kDlBwdThreads, 1) delta_bwd_kernel(const Delta
             cp_async4(smem_u32(smem + C::OFF_L + i * 4), Lb + (ok ? t : 0), ok ? 4u : 0u);
             cp_async4(smem_u32(smem + C::OFF_B + i * 4), Bb + (ok ? t : 0), ok ? 4u : 0u);
         }
-        {  // the chunk's (I + A)^-1 parts, formed by delta_wy_kernel: 16 KB copied as they lie
+        {  // the chunk's (I + A)^-1 parts and E, formed by delta_wy_kernel (E into rows of kAS floats)
             const uint8_t *src = p.wy + ((size_t)bh * p.n_chunks + chunk) * (2 * kDlTc * 128);
             for (int i = tid; i < 2 * kDlTc * 8; i += kDlBwdThreads)
                 cp_async16(smem_u32(smem + C::OFF_TH + 16 * i), src + 16 * i, 16u);
+            const float *esrc = p.E + ((size_t)bh * p.n_chunks + chunk) * (kDlTc * kDlTc);
+            for (int i = tid; i < kDlTc * 16; i += kDlBwdThreads) {
+                const int r = i >> 4, c4 = i & 15;
+                cp_async16(smem_u32(smem + C::OFF_E + (r * kAS + 4 * c4) * 4), esrc + r * kDlTc + 4 * c4, 16u);
+            }
         }
         // the state entering the chunk, fp32 -> two bf16 parts (plain loads, read once; all of a
         // thread's loads issued before the first is used)
@@ -899,6 +920,8 @@ __global__ void __launch_bounds__(kDlBwdThreads, 1) delta_bwd_kernel(const Delta
         for (int i = tid; i < DK * 2; i += kDlBwdThreads) prefetch_l2(sg + (size_t)(i >> 1) * p.DV + (i & 1) * 32);
         const uint8_t *wy = p.wy + ((size_t)bh * p.n_chunks + chunk) * (2 * kDlTc * 128);
         for (int i = tid; i < 2 * kDlTc; i += kDlBwdThreads) prefetch_l2(wy + 128 * i);
+        const float *eg = p.E + ((size_t)bh * p.n_chunks + chunk) * (kDlTc * kDlTc);
+        for (int i = tid; i < kDlTc * 2; i += kDlBwdThreads) prefetch_l2(eg + 32 * i);
     };
 
     // adjoint state fragments: rows 16(wr S_MT + mi) + {g, g + 8}, columns 8(4 hf + nj) + 2 tq + {0, 1}
@@ -1037,21 +1060,8 @@ __global__ void __launch_bounds__(kDlBwdThreads, 1) delta_bwd_kernel(const Delta
         float dbr[2] = {0.f, 0.f};  // this warp's parts of dbeta (quad sums)
         float esum = 0.f;           // sum of e over this thread's rows (counted once per quad)
 
-        // ---- E = strictly lower (2^(c_r - c_s) k_r . k_s): rows of this warp, its column half
-        {
-            float F[4][4];
-            zero4(F);
-            mma_half_nk(F, sK, sK, IQ{}, IQ{}, KD{});
-#pragma unroll
-            for (int nj = 0; nj < 4; ++nj)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = rr[e >> 1], s = colof(nj) + (e & 1);
-                    Em[r * kAS + s] = (s < r) ? ex2(cs[r] - cs[s]) * F[nj][e] : 0.f;
-                }
-        }
-        __syncthreads();
-        // ---- (I + A)^-1 (A = diag(beta) E) arrived with the chunk's inputs, as two bf16 parts;
+        // ---- E = strictly lower (2^(c_r - c_s) k_r . k_s), fp32, and (I + A)^-1 (A = diag(beta) E)
+        // as two bf16 parts arrived with the chunk's inputs;
         // every warp forms K S, Yv = V - diag(gamma) K S and X = diag(beta) Yv for its part
         float Yv[4][4];
         {
@@ -1562,6 +1572,10 @@ size_t delta_states_bytes(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t d
 size_t delta_wy_bytes(int64_t B, int64_t H, int64_t T) {
     return (size_t)B * (size_t)H * (size_t)((T + kDlTc - 1) / kDlTc) * (2 * kDlTc * 128);
 }
+// Bytes of the chunks' E, fp32 [64][64] (16 KB a chunk).
+size_t delta_e_bytes(int64_t B, int64_t H, int64_t T) {
+    return (size_t)B * (size_t)H * (size_t)((T + kDlTc - 1) / kDlTc) * (kDlTc * kDlTc * 4);
+}
 
 // Workspace of the backward: the header, the state entering every chunk, every chunk's (I + A)^-1
 // parts, and the partials of the value-column blocks after the first (with a checkpoint, which
@@ -1570,7 +1584,7 @@ size_t delta_wy_bytes(int64_t B, int64_t H, int64_t T) {
 size_t delta_bwd_ws_bytes(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv) {
     const double BH = (double)B * H, nc = (double)((T + kDlTc - 1) / kDlTc);
     const double states = BH * nc * dk * dv * 4.0;
-    const double wy = BH * nc * (2.0 * kDlTc * 128);
+    const double wy = BH * nc * (2.0 * kDlTc * 128 + kDlTc * kDlTc * 4.0);  // inverse parts and E
     const double parts = (double)(dv / 64 - 1) * BH * T * (2.0 * dk + 2.0) * 4.0;
     const double total = sizeof(WsHeader) + states + 16.0 + wy + parts;
     if (total > 9.0e18) return 0;
@@ -1631,6 +1645,8 @@ int delta_fwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
     uint8_t *wy = ckpt != nullptr ? reinterpret_cast<uint8_t *>(ckpt) + delta_states_bytes(B, H, T, dim_k, dim_v)
                   : ws_bytes >= sizeof(WsHeader) + wy_bytes ? static_cast<uint8_t *>(ws) + sizeof(WsHeader)
                                                             : nullptr;
+    // with a checkpoint the backward's E too (after the inverse parts)
+    float *E = ckpt != nullptr ? reinterpret_cast<float *>(wy + wy_bytes) : nullptr;
     DeltaArgs a;
     memset(&a, 0, sizeof(a));
     a.q = reinterpret_cast<const bf16 *>(q);
@@ -1649,6 +1665,7 @@ int delta_fwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
     a.hdr = static_cast<WsHeader *>(ws);
     a.states = ckpt;
     a.wy = wy;
+    a.E = E;
     if (wy != nullptr) {
         const int st = dim_k == 64 ? launch_delta_wy<64>(a, s) : launch_delta_wy<128>(a, s);
         if (st) return st;
@@ -1661,8 +1678,9 @@ int delta_fwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
 extern "C" size_t cla_delta_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk) {
     if (!delta_supported(B, H, T, dim_k, dim_v, chunk)) return 0;
     const double nc = (double)((T + kDlTc - 1) / kDlTc);
-    const double bytes = (double)B * H * nc * (dim_k * dim_v * 4.0 + 2.0 * kDlTc * 128) + 16.0;
-    return bytes > 9.0e18 ? 0 : delta_states_bytes(B, H, T, dim_k, dim_v) + delta_wy_bytes(B, H, T);
+    const double bytes = (double)B * H * nc * (dim_k * dim_v * 4.0 + 2.0 * kDlTc * 128 + kDlTc * kDlTc * 4.0) + 16.0;
+    return bytes > 9.0e18 ? 0
+                          : delta_states_bytes(B, H, T, dim_k, dim_v) + delta_wy_bytes(B, H, T) + delta_e_bytes(B, H, T);
 }
 
 extern "C" int cla_delta_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *log_decay,
@@ -1722,7 +1740,8 @@ int delta_bwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
     // with a checkpoint the states pass is skipped and the workspace holds the header and the partials only
     const size_t full = delta_bwd_ws_bytes(B, H, T, dim_k, dim_v);
     if (full == 0) return fail(CLA_ERR_UNSUPPORTED, "%s: workspace size overflows", fn);
-    const size_t states_b = delta_states_bytes(B, H, T, dim_k, dim_v), wy_b = delta_wy_bytes(B, H, T);
+    const size_t states_b = delta_states_bytes(B, H, T, dim_k, dim_v);
+    const size_t wy_b = delta_wy_bytes(B, H, T) + delta_e_bytes(B, H, T);  // inverse parts, then E
     const size_t need = ckpt ? full - states_b - wy_b : full;
     if (!ws || !aligned16(ws)) return fail(CLA_ERR_WORKSPACE, "%s: workspace NULL or unaligned", fn);
     if (ws_bytes < need) return fail(CLA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, ws_bytes, need);
@@ -1735,6 +1754,7 @@ int delta_bwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
     // every chunk's (I + A)^-1: from the checkpoint, else formed here (before the states pass, which
     // uses them too)
     const uint8_t *wy = ckpt ? reinterpret_cast<const uint8_t *>(ckpt) + states_b : ws_wy;
+    const float *Ech = reinterpret_cast<const float *>(wy + delta_wy_bytes(B, H, T));
     // the states pass (no checkpoint): the forward kernel writes the state entering every chunk, no output
     if (!ckpt) {
         DeltaArgs f;
@@ -1753,6 +1773,7 @@ int delta_bwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
         f.T = T;
         f.hdr = static_cast<WsHeader *>(ws);
         f.wy = ws_wy;
+        f.E = reinterpret_cast<float *>(ws_wy + delta_wy_bytes(B, H, T));
         int st = dim_k == 64 ? launch_delta_wy<64>(f, s) : launch_delta_wy<128>(f, s);
         if (st) return st;
         st = dim_k == 64 ? launch_delta_fwd<64>(f, s, grid) : launch_delta_fwd<128>(f, s, grid);
@@ -1769,6 +1790,7 @@ int delta_bwd_impl(const char *fn, const uint16_t *q, const uint16_t *k, const u
     a.dST = dST;
     a.states = states;
     a.wy = wy;
+    a.E = Ech;
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;

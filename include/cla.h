@@ -467,11 +467,12 @@ int cla_delta_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 
 /* Bytes of workspace for cla_delta_bwd: the header, the state entering every
  * chunk (B H ceil(T / 64) dim_k dim_v fp32), every chunk's (I + A)^-1 as two
- * bf16 parts (B H ceil(T / 64) x 16 KB) and, for dim_v > 64, partial
+ * bf16 parts and its E = A without the gate strengths (fp32), together
+ * B H ceil(T / 64) x 32 KB, and, for dim_v > 64, partial
  * key-side gradients of the value-column blocks after the first
  * ((dim_v / 64 - 1) B H T (2 dim_k + 2) fp32); 0 for sizes, head dims or
  * chunks that call refuses.  cla_delta_bwd_ckpt needs this less
- * cla_delta_ckpt_size (the checkpoint holds the states and the inverses). */
+ * cla_delta_ckpt_size (the checkpoint holds the states, the inverses and E). */
 size_t cla_delta_bwd_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
                                     int64_t dim_v, int chunk);
 
@@ -507,10 +508,11 @@ int cla_delta_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
  * is a scan in reverse": store the states or recompute them).  The backward
  * works from the state entering every chunk; the forward computes exactly
  * those states, so it can save them instead of the backward re-running it.
- * The checkpoint also keeps every chunk's (I + A)^-1 (which depends on k,
- * log_decay and beta only), so the backward reads it instead of re-forming
- * it.  Bytes of the checkpoint: B H ceil(T / 64) dim_k dim_v fp32 values
- * (rounded up to 16 bytes), then B H ceil(T / 64) x 16 KB of inverse parts;
+ * The checkpoint also keeps every chunk's (I + A)^-1 and E (A without the
+ * gate strengths; both depend on k, log_decay and beta only), so the backward
+ * reads them instead of re-forming them.  Bytes of the checkpoint:
+ * B H ceil(T / 64) dim_k dim_v fp32 values (rounded up to 16 bytes), then
+ * B H ceil(T / 64) x 16 KB of inverse parts and B H ceil(T / 64) x 16 KB of E;
  * 0 for sizes, head dims or chunks the fwd / bwd calls refuse. */
 size_t cla_delta_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
                            int64_t dim_v, int chunk);
@@ -518,8 +520,8 @@ size_t cla_delta_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
 /* cla_delta_fwd that also writes the checkpoint: ckpt (device,
  * cla_delta_ckpt_size bytes, 16-byte aligned, owned by the caller) gets the
  * state entering each 64-token chunk, [B, H, ceil(T / 64), dim_k, dim_v],
- * followed by each chunk's (I + A)^-1 parts (the forward then needs only the
- * workspace's header).
+ * followed by each chunk's (I + A)^-1 parts and E (the forward then needs
+ * only the workspace's header).
  * ckpt = NULL is the plain forward. */
 int cla_delta_fwd_ckpt(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                        const float *log_decay, const float *beta, const float *S0,
