@@ -97,3 +97,5 @@ extern "C" int cla_check_status(const void *ws, void *stream) {
                          "rule: a non-finite log decay or beta); the results of that call are not valid");
     return CLA_OK;
 }
+
+extern "C" int cla_check_device_status(const void *ws, void *stream) { return cla_check_status(ws, stream); }

@@ -885,6 +885,10 @@ extern "C" size_t cla_chunk_la_workspace_size(int64_t B, int64_t H, int64_t T, i
     return la_plan(B, H, T, dim_k, dim_v, chunk).total;
 }
 
+extern "C" size_t cla_chunk_la_workspace(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v, int chunk) {
+    return cla_chunk_la_workspace_size(B, H, T, dim_k, dim_v, chunk);
+}
+
 extern "C" size_t cla_chunk_la_ckpt_size(int64_t B, int64_t H, int64_t T, int64_t dim_k, int64_t dim_v,
                                          int chunk) {
     if (!la_supported(B, H, T, dim_k, dim_v, chunk)) return 0;

@@ -767,6 +767,10 @@ extern "C" size_t cla_scan_diag_workspace_size(int64_t B, int64_t T, int64_t D) 
     return p1.total_recomp > p4.total_recomp ? p1.total_recomp : p4.total_recomp;
 }
 
+extern "C" size_t cla_scan_diag_workspace(int64_t B, int64_t T, int64_t D) {
+    return cla_scan_diag_workspace_size(B, T, D);
+}
+
 namespace {
 int scan_fwd(const char *fn, bool blelloch, const float *a, const float *b, const float *h0, float *h, float *hT,
              int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes, void *stream) {

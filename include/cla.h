@@ -67,6 +67,8 @@ const char *cla_last_error_message(void);
  * stream holds an error, else CLA_OK.  `ws` must be the workspace of that
  * call. */
 int cla_check_status(const void *ws, void *stream);
+/* The same call under the name the boundary's plan gives it. */
+int cla_check_device_status(const void *ws, void *stream);
 
 /* Self-test of the failure path: launches one warp that polls a workspace
  * word nothing ever sets.  Its bounded wait gives up after about a second,
@@ -82,6 +84,8 @@ int cla_selftest_wait_timeout(void *ws, size_t ws_bytes, void *stream);
 
 /* Bytes of workspace needed by cla_scan_diag_fwd / _bwd for [B, T, D]. */
 size_t cla_scan_diag_workspace_size(int64_t B, int64_t T, int64_t D);
+/* The same query under the name the boundary's plan gives it. */
+size_t cla_scan_diag_workspace(int64_t B, int64_t T, int64_t D);
 
 /* Forward: h_t = a_t * h_{t-1} + b_t elementwise over D channels, for
  * t = 1..T, from h_0 = h0 ("Parallel Scan", "The scan for one number of
@@ -232,6 +236,9 @@ int cla_selective_scan_bwd(const uint16_t *x, const float *delta, const float *A
  * or chunks those calls refuse. */
 size_t cla_chunk_la_workspace_size(int64_t B, int64_t H, int64_t T, int64_t dim_k,
                                    int64_t dim_v, int chunk);
+/* The same query under the name the boundary's plan gives it. */
+size_t cla_chunk_la_workspace(int64_t B, int64_t H, int64_t T, int64_t dim_k,
+                              int64_t dim_v, int chunk);
 
 /* Forward of S_t = a_t S_{t-1} + k_t v_t^T (S is [dim_k, dim_v], rows indexed
  * by keys), o_t = S_t^T q_t, with a_t = exp(log_decay_t), computed chunkwise

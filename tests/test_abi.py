@@ -63,6 +63,20 @@ def test_host_validation_without_gpu(lib):
     assert lib.cla_scan_diag_workspace_size(-1, 1, 1) == 0
 
 
+def test_plan_named_aliases(lib):
+    """The boundary plan's names for the workspace queries and the status call are the same
+    functions as the library's own."""
+    lib.cla_scan_diag_workspace.restype = ctypes.c_size_t
+    lib.cla_scan_diag_workspace.argtypes = [ctypes.c_int64] * 3
+    lib.cla_chunk_la_workspace.restype = ctypes.c_size_t
+    lib.cla_chunk_la_workspace.argtypes = [ctypes.c_int64] * 5 + [ctypes.c_int]
+    for shape in ((8, 4096, 1024), (1, 1024, 64), (3, 77, 6), (-1, 1, 1)):
+        assert lib.cla_scan_diag_workspace(*shape) == lib.cla_scan_diag_workspace_size(*shape)
+    for shape in ((4, 16, 8192, 64, 64, 64), (1, 32, 65536, 128, 128, 128), (1, 2, 1000, 96, 64, 64)):
+        assert lib.cla_chunk_la_workspace(*shape) == lib.cla_chunk_la_workspace_size(*shape)
+    assert hasattr(lib, "cla_check_device_status")
+
+
 def test_chunk_la_ckpt_size_follows_the_segment_rule(lib):
     """The checkpoint holds one d_k x d_v fp32 state per segment and head; segments are the
     largest of 64/32/16/8 chunks that still leave at least 1024 blocks (heads x 64-column
