@@ -75,6 +75,65 @@ def test_chunk_la_beyond_int32_elements(cla):
         assert_bf16(f"dlog_a[head {hd}]", tail(dl)[..., 1:], rdl[..., 1:])
 
 
+# Gated linear attention and the delta rule take no zero gates, so a tail independent of the earlier
+# tokens is made by strong decay instead of a reset: log a = -2 for the tail's first 192 tokens
+# scales whatever the state held before the tail by at most e^-384 (0 in fp32, far below the
+# tolerance in fp64), so from token 192 of the tail on the outputs, and everywhere in the tail the
+# gradients that look only forward in time, equal the oracle's on the tail from a zero state.
+_TAIL, _WARM = 2500, 192
+
+
+def _tail_check(inp, heads, fwd_out, bwd_out, oracle_fwd, oracle_bwd, names_bwd, t_r, extra=(), look_back=()):
+    for hd in heads:
+        tail = lambda x: x[:, hd:hd + 1, t_r:].contiguous().cpu()
+        args = [tail(inp[n]) for n in ("q", "k", "v", "log_a") + extra]
+        dO = tail(inp["dO"])
+        ro, _ = oracle_fwd(*args, None)
+        assert_bf16(f"o[head {hd}]", tail(fwd_out)[:, :, _WARM:], ro[:, :, _WARM:])
+        ref = oracle_bwd(*args, None, dO)
+        for name, x, r in zip(names_bwd, bwd_out, ref):
+            # the gradients that read the state entering a step (look back): from token _WARM on
+            lo = _WARM if name in look_back else 0
+            assert_bf16(f"{name}[head {hd}]", tail(x)[:, :, lo:], r[:, :, lo:])
+
+
+def test_gla_beyond_int32_elements(cla):
+    """B=1, H=64, T = 262,200, d = 128: 2^31 + 6.6 M elements per q/k/dq/dk/log-decay tensor;
+    forward saving its checkpoint and the backward from it, checked on the tail of the first and
+    last head (the highest element indices)."""
+    dev = torch.device("cuda")
+    B, H, T, d = 1, 64, 262200, 128
+    assert B * H * T * d > (1 << 31)
+    t = workloads.gla_inputs_device(B, H, T, d, d, seed=24, device=dev)
+    t_r = T - _TAIL
+    t["log_a"][:, :, t_r:t_r + _WARM] = -2.0
+    ck = cla.gla_ckpt(t["q"], t["v"])
+    o, ST = cla.gla_fwd(t["q"], t["k"], t["v"], t["log_a"], None, ckpt=ck)
+    g = cla.gla_bwd(t["q"], t["k"], t["v"], t["log_a"], None, t["dO"], ckpt=ck)
+    torch.cuda.synchronize()
+    _tail_check(t, (0, H - 1), o, g[:4], oracle.gla_fwd, oracle.gla_bwd, ("dq", "dk", "dv", "dlog_a"), t_r,
+                look_back=("dq", "dlog_a"))
+
+
+def test_delta_beyond_int32_elements(cla):
+    """B=1, H=64, T = 262,200, d = 128: 2^31 + 6.6 M elements per q/k/v/dO tensor; forward
+    saving its checkpoint and the backward from it, checked on the tail of the first and last
+    head."""
+    dev = torch.device("cuda")
+    B, H, T, d = 1, 64, 262200, 128
+    assert B * H * T * d > (1 << 31)
+    t = workloads.delta_inputs_device(B, H, T, d, d, seed=25, device=dev)
+    t_r = T - _TAIL
+    t["log_a"][:, :, t_r:t_r + _WARM] = -2.0
+    ck = cla.delta_ckpt(t["q"], t["v"])
+    o, ST = cla.delta_fwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], None, ckpt=ck)
+    g = cla.delta_bwd(t["q"], t["k"], t["v"], t["log_a"], t["beta"], None, t["dO"], ckpt=ck)
+    torch.cuda.synchronize()
+    # the key, its gate strength and the decay enter the transition applied to the incoming state
+    _tail_check(t, (0, H - 1), o, g[:5], oracle.delta_fwd, oracle.delta_bwd, ("dq", "dk", "dv", "dlog_a", "dbeta"),
+                t_r, extra=("beta",), look_back=("dq", "dk", "dlog_a", "dbeta"))
+
+
 # B = 1: the chunk look-back forward; B = 3 (6144 channels): the forward walking each
 # channel's whole sequence once
 @pytest.mark.parametrize("B,T", [(1, (1 << 20) + 37), (3, 350021)])

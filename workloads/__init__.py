@@ -214,6 +214,30 @@ def la_long_inputs_device(B, H, T, dk, dv, seed, device):
                 dO=_dev_normal(seed, 5, (B, H, T, dv), device, 1.0, bf))
 
 
+def gla_inputs_device(B, H, T, dk, dv, seed, device):
+    """The ``gla`` recipe drawn on the device (S0 = 0)."""
+    s = 1.0 / math.sqrt(dk)
+    bf = torch.bfloat16
+    log_a = -torch.nn.functional.softplus(_dev_normal(seed, 3, (B, H, T, dk), device)) / 16.0
+    return dict(q=_dev_normal(seed, 0, (B, H, T, dk), device, s, bf), k=_dev_normal(seed, 1, (B, H, T, dk), device, s, bf),
+                v=_dev_normal(seed, 2, (B, H, T, dv), device, s, bf), log_a=log_a, S0=None,
+                dO=_dev_normal(seed, 5, (B, H, T, dv), device, 1.0, bf))
+
+
+def delta_inputs_device(B, H, T, dk, dv, seed, device):
+    """The ``delta`` recipe drawn on the device (S0 = 0): unit-norm keys, beta = sigmoid(N(0, 1))."""
+    s = 1.0 / math.sqrt(dk)
+    bf = torch.bfloat16
+    kr = _dev_normal(seed, 1, (B, H, T, dk), device)
+    k = (kr / torch.linalg.vector_norm(kr, dim=-1, keepdim=True)).to(bf)
+    del kr
+    log_a = -torch.nn.functional.softplus(_dev_normal(seed, 3, (B, H, T), device)) / 16.0
+    beta = torch.sigmoid(_dev_normal(seed, 4, (B, H, T), device))
+    return dict(q=_dev_normal(seed, 0, (B, H, T, dk), device, s, bf), k=k,
+                v=_dev_normal(seed, 2, (B, H, T, dv), device, s, bf), log_a=log_a, beta=beta, S0=None,
+                dO=_dev_normal(seed, 6, (B, H, T, dv), device, 1.0, bf))
+
+
 def selective_inputs_device(B, T, D, N, seed, device):
     """The ``selective`` recipe drawn on the device."""
     bf = torch.bfloat16
