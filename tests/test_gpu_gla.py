@@ -187,3 +187,20 @@ def test_gla_checkpoint(cla, B, H, T, dk, dv):
     ref = oracle.gla_bwd(inp["q"], inp["k"], inp["v"], inp["log_a"], inp["S0"], inp["dO"], dST)
     for name, x, r in zip(("dq", "dk", "dv", "dlog_a", "dS0"), g, ref):
         assert_bf16(name, x, r)
+
+
+def test_gla_bwd_decay_gradient_unaligned_output(cla):
+    """A dlog_decay buffer only 4-byte aligned takes the scalar decay-gradient kernels (the
+    aligned one the 8-dimension ones): both match the oracle and each other."""
+    B, H, T, dk, dv = 1, 2, 700, 128, 64
+    inp = workloads.make("gla", B=B, H=H, T=T, dk=dk, dv=dv)
+    t = {k: _dev(v) for k, v in inp.items()}
+    buf = torch.empty(B * H * T * dk + 1, device="cuda")
+    odd = buf[1:].view(B, H, T, dk)
+    assert odd.data_ptr() % 16 != 0
+    g_al = cla.gla_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"])
+    g_un = cla.gla_bwd(t["q"], t["k"], t["v"], t["log_a"], t["S0"], t["dO"], dlog_decay=odd)
+    ref = oracle.gla_bwd(inp["q"], inp["k"], inp["v"], inp["log_a"], inp["S0"], inp["dO"])
+    assert_bf16("dlog_a (8 dimensions a thread)", g_al[3], ref[3])
+    assert_bf16("dlog_a (scalar)", g_un[3], ref[3])
+    assert_bf16("dlog_a (two paths)", g_un[3], g_al[3], tol_max=1e-5, tol_mean=1e-6)
