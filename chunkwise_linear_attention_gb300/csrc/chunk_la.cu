@@ -61,6 +61,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 // grid's size allows; the smallest choice otherwise.
 constexpr int kSegChoices[4] = {64, 32, 16, 8};
 constexpr long long kMinBlocks = 1024;
+// The compact layout (d_k = d_v = chunk = 64, two blocks per SM) has short chunk visits (about
+// 3k cycles), so a block's fixed cost weighs more there: it takes the rule with half the blocks
+// (measured on 4 x 16 x 8192: 8-chunk segments 155 / 395 us forward / backward, 16-chunk
+// segments 144 / 382 us, 4-chunk segments 181 / 434 us).
+constexpr long long kMinBlocksCompact = 512;
 
 // ----------------------------------------------------------------- configuration
 template <int DX, int TC>
@@ -767,9 +772,10 @@ LaPlan la_plan(int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int chun
     p.nzb_max = (int)((dk > dv ? dk : dv) / 64);
     const size_t BH = (size_t)B * H;
     p.seg_chunks = kSegChoices[3];
+    const long long min_blocks = (dk == 64 && dv == 64 && chunk == 64) ? kMinBlocksCompact : kMinBlocks;
     for (int c : kSegChoices) {
         const long long nseg = (p.n_chunks + c - 1) / c;
-        if (nseg * (long long)BH * p.nzb_max >= kMinBlocks) {
+        if (nseg * (long long)BH * p.nzb_max >= min_blocks) {
             p.seg_chunks = c;
             break;
         }
