@@ -62,10 +62,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kSegChoices[4] = {64, 32, 16, 8};
 constexpr long long kMinBlocks = 1024;
 // The compact layout (d_k = d_v = chunk = 64, two blocks per SM) has short chunk visits (about
-// 3k cycles), so a block's fixed cost weighs more there: it takes the rule with half the blocks
-// (measured on 4 x 16 x 8192: 8-chunk segments 155 / 395 us forward / backward, 16-chunk
-// segments 144 / 382 us, 4-chunk segments 181 / 434 us).
-constexpr long long kMinBlocksCompact = 512;
+// 3k cycles), so a block's fixed cost weighs more there: it takes the rule with a quarter of the
+// blocks, about one wave of two blocks per SM (measured on 4 x 16 x 8192: 4-chunk segments
+// 181 / 434 us forward / backward, 8-chunk 155 / 395 us, 16-chunk 143 / 382 us, 32-chunk
+// 133 / 360 us, 64-chunk (128 blocks, fewer than the SMs) 192 / 514 us).
+constexpr long long kMinBlocksCompact = 256;
 
 // ----------------------------------------------------------------- configuration
 template <int DX, int TC>

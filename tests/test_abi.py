@@ -80,7 +80,7 @@ def test_plan_named_aliases(lib):
 def test_chunk_la_ckpt_size_follows_the_segment_rule(lib):
     """The checkpoint holds one d_k x d_v fp32 state per segment and head; segments are the
     largest of 64/32/16/8 chunks that still leave at least 1024 blocks (heads x 64-column
-    blocks x segments; 512 in the compact layout, d_k = d_v = chunk = 64).  Long-context workload, chunk 128: 512 chunks per head, 32 heads,
+    blocks x segments; 256 in the compact layout, d_k = d_v = chunk = 64).  Long-context workload, chunk 128: 512 chunks per head, 32 heads,
     2 column blocks -> segments of 32 chunks, 16 of them."""
     f = lib.cla_chunk_la_ckpt_size
     f.restype = ctypes.c_size_t
@@ -88,9 +88,9 @@ def test_chunk_la_ckpt_size_follows_the_segment_rule(lib):
     assert f(1, 32, 65536, 128, 128, 128) == 16 * 32 * 128 * 128 * 4
     # chunk 64: 1024 chunks, segments of 64 chunks (16 x 32 x 2 = 1024 blocks)
     assert f(1, 32, 65536, 128, 128, 64) == 16 * 32 * 128 * 128 * 4
-    # constant-decay workload (the compact layout, d = chunk = 64: at least 512 blocks): 128
-    # chunks per head, 64 heads, one column block -> segments of 16
-    assert f(4, 16, 8192, 64, 64, 64) == 8 * 64 * 64 * 64 * 4
+    # constant-decay workload (the compact layout, d = chunk = 64: at least 256 blocks): 128
+    # chunks per head, 64 heads, one column block -> segments of 32, 4 of them
+    assert f(4, 16, 8192, 64, 64, 64) == 4 * 64 * 64 * 64 * 4
     assert f(-1, 1, 1, 64, 64, 64) == 0 and f(1, 1, 1, 64, 64, 0) == 0
 
 
