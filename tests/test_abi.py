@@ -91,6 +91,14 @@ def test_chunk_la_ckpt_size_follows_the_segment_rule(lib):
     # constant-decay workload (the compact layout, d = chunk = 64: at least 256 blocks): 128
     # chunks per head, 64 heads, one column block -> segments of 32, 4 of them
     assert f(4, 16, 8192, 64, 64, 64) == 4 * 64 * 64 * 64 * 4
+    # compact layout, one head of 1024 chunks: no choice reaches 256 blocks -> the smallest
+    # (8 chunks), 128 segments
+    assert f(1, 1, 65536, 64, 64, 64) == 128 * 1 * 64 * 64 * 4
+    # compact layout, 256 heads: 64-chunk segments already give 512 blocks
+    assert f(8, 32, 8192, 64, 64, 64) == 2 * 256 * 64 * 64 * 4
+    # d = 64 at chunk 128 is not the compact layout: the 1024-block rule, 64 chunks per head and
+    # 64 heads -> even 8-chunk segments give 512 blocks, so the smallest choice, 8 segments
+    assert f(4, 16, 8192, 64, 64, 128) == 8 * 64 * 64 * 64 * 4
     assert f(-1, 1, 1, 64, 64, 64) == 0 and f(1, 1, 1, 64, 64, 0) == 0
 
 
