@@ -102,6 +102,25 @@ def test_chunk_la_ckpt_size_follows_the_segment_rule(lib):
     assert f(-1, 1, 1, 64, 64, 64) == 0 and f(1, 1, 1, 64, 64, 0) == 0
 
 
+def test_gla_and_delta_ckpt_sizes(lib):
+    """GLA: one d_k x d_v fp32 state per segment and head, segments the largest of 64/32/16/8
+    chunks that leave at least 1024 blocks (heads x max(d_k, d_v)/64 column blocks x segments).
+    The workload (2 x 16 heads, 16384 tokens = 256 chunks, d = 128): 16-chunk segments, 16 of
+    them.  Delta rule: per 64-token chunk the state (d_k x d_v fp32), the (I + A)^-1 parts
+    (16 KB) and E (16 KB).  Both 0 for what the calls refuse."""
+    for n in ("cla_gla_ckpt_size", "cla_delta_ckpt_size"):
+        f = getattr(lib, n)
+        f.restype = ctypes.c_size_t
+        f.argtypes = [ctypes.c_int64] * 5 + [ctypes.c_int]
+    g, d = lib.cla_gla_ckpt_size, lib.cla_delta_ckpt_size
+    assert g(2, 16, 16384, 128, 128, 64) == 16 * 32 * 128 * 128 * 4
+    assert g(2, 16, 16384, 64, 128, 64) == 16 * 32 * 64 * 128 * 4  # column blocks from max(d_k, d_v)
+    assert g(1, 1, 1000, 96, 128, 64) == 0 and g(1, 1, 1000, 128, 128, 128) == 0
+    assert d(4, 32, 4096, 128, 128, 64) == 4 * 32 * 64 * (128 * 128 * 4 + 16384 + 16384)
+    assert d(1, 1, 100, 64, 192, 64) == 2 * (64 * 192 * 4 + 16384 + 16384)  # ragged: 2 chunks
+    assert d(1, 1, 100, 64, 64, 128) == 0
+
+
 def test_chunk_la_size_queries_refuse_what_the_calls_refuse(lib):
     """The workspace and checkpoint size queries return 0 for head dims or chunks the fwd / bwd
     calls reject (CLA_ERR_UNSUPPORTED), so no caller sizes a buffer for a call that cannot run."""
