@@ -25,8 +25,8 @@
 //   5. every lane re-runs its L steps from its true starting state and
 //      writes h once.
 // HBM traffic is the algorithmic 12 B per element forward (read a, b; write
-// h) and 20 B backward (read a, h, dh; write da, db), plus 24 B of look-back
-// payload per chunk and channel (about 0.4 B per element, L2-resident).
+// h) and 20 B backward (read a, h, dh; write da, db), plus 12 B of look-back
+// payload per chunk and channel (about 0.2 B per element, L2-resident).
 #include "cla_internal.cuh"
 
 namespace cla {
@@ -64,36 +64,51 @@ struct VecIO<1> {
 };
 
 // Look-back payload: per (chunk, batch row, warp column, channel group) and
-// per channel, three 64-bit words -- the chunk's decay product A, its
-// composed input B, and the state at its far edge (inclusive) -- each holding
-// the float value in its low half and its status in its high half (0 not yet
-// written, 1 aggregate, 2 inclusive).  A word is written and read with one
-// relaxed 64-bit access, which is single-copy atomic, so a reader that sees
-// the status also sees the value: no memory fence is on the critical path.
+// per channel, three 32-bit words -- the chunk's decay product A, its
+// composed input B, and the state at its far edge (inclusive).  A word is 0
+// until it is written (the launch clears them) and a written word is never 0:
+// a value of +0.0f is stored as -0.0f, which every later use treats alike
+// (a * (-0) + b and a * (+0) + b differ at most in the sign of a zero sum).
+// A word is written and read with one relaxed 32-bit access, which is
+// single-copy atomic, so a reader that sees a nonzero word sees the value: no
+// memory fence is on the critical path.  (Each element of the 16-byte vector
+// accesses below is such an access.)
 struct ScanWs {
     WsHeader *hdr;
-    unsigned long long *words;  // [unit][3][4]
+    unsigned int *words;  // [unit][3][4]
 };
 
 constexpr unsigned int kWordA = 0, kWordB = 1, kWordIncl = 2;
 
-__device__ __forceinline__ void pub_word(unsigned long long *p, float v, unsigned int status) {
-    const unsigned long long w = ((unsigned long long)status << 32) | __float_as_uint(v);
-    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+__device__ __forceinline__ unsigned int pub_bits(float v) {
+    const unsigned int b = __float_as_uint(v);
+    return b != 0u ? b : 0x80000000u;
 }
-__device__ __forceinline__ unsigned long long peek_word(const unsigned long long *p) {
-    unsigned long long w;
-    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
-    return w;
-}
-__device__ __forceinline__ unsigned int word_status(unsigned long long w) { return (unsigned int)(w >> 32); }
-__device__ __forceinline__ float word_value(unsigned long long w) { return __uint_as_float((unsigned int)w); }
 
 template <int VEC>
-__device__ __forceinline__ void publish(const ScanWs &ws, size_t u, unsigned int kind, const float (&v)[VEC],
-                                        unsigned int status) {
+__device__ __forceinline__ void publish(const ScanWs &ws, size_t u, unsigned int kind, const float (&v)[VEC]) {
+    unsigned int *p = ws.words + (u * 3 + kind) * 4;
+    if constexpr (VEC == 4)
+        asm volatile("st.relaxed.gpu.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(pub_bits(v[0])),
+                     "r"(pub_bits(v[1])), "r"(pub_bits(v[2])), "r"(pub_bits(v[3]))
+                     : "memory");
+    else
+        asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(pub_bits(v[0])) : "memory");
+}
+
+template <int VEC>
+__device__ __forceinline__ bool peek_words(const unsigned int *p, unsigned int (&w)[VEC]) {
+    if constexpr (VEC == 4)
+        asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "l"(p)
+                     : "memory");
+    else
+        asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(w[0]) : "l"(p) : "memory");
+    bool all = true;
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) pub_word(ws.words + (u * 3 + kind) * 4 + i, v[i], status);
+    for (int i = 0; i < VEC; ++i) all = all && w[i] != 0u;
+    return all;
 }
 
 // One step of the look-back walk at unit `up`: returns 2 when the unit's
@@ -102,33 +117,22 @@ __device__ __forceinline__ void publish(const ScanWs &ws, size_t u, unsigned int
 template <int VEC>
 __device__ __forceinline__ unsigned int look_at(const ScanWs &ws, size_t up, float (&accA)[VEC], float (&accB)[VEC],
                                                 float (&res)[VEC], unsigned int where) {
-    const unsigned long long *base = ws.words + up * 12;
+    const unsigned int *base = ws.words + up * 12;
     for (unsigned int it = 0; it < kSpinLimit; ++it) {
-        unsigned long long wi[VEC];
-        bool all2 = true;
+        unsigned int wi[VEC];
+        if (peek_words<VEC>(base + kWordIncl * 4, wi)) {
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) {
-            wi[i] = peek_word(base + kWordIncl * 4 + i);
-            all2 = all2 && word_status(wi[i]) == 2u;
-        }
-        if (all2) {
-#pragma unroll
-            for (int i = 0; i < VEC; ++i) res[i] = fmaf(accA[i], word_value(wi[i]), accB[i]);
+            for (int i = 0; i < VEC; ++i) res[i] = fmaf(accA[i], __uint_as_float(wi[i]), accB[i]);
             return 2u;
         }
-        unsigned long long wa[VEC], wb[VEC];
-        bool all1 = true;
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) {
-            wa[i] = peek_word(base + kWordA * 4 + i);
-            wb[i] = peek_word(base + kWordB * 4 + i);
-            all1 = all1 && word_status(wa[i]) == 1u && word_status(wb[i]) == 1u;
-        }
-        if (all1) {
+        unsigned int wa[VEC], wb[VEC];
+        const bool ra = peek_words<VEC>(base + kWordA * 4, wa);
+        const bool rb = peek_words<VEC>(base + kWordB * 4, wb);
+        if (ra && rb) {
 #pragma unroll
             for (int i = 0; i < VEC; ++i) {  // the unit's chunk happened before acc
-                accB[i] = fmaf(accA[i], word_value(wb[i]), accB[i]);
-                accA[i] *= word_value(wa[i]);
+                accB[i] = fmaf(accA[i], __uint_as_float(wb[i]), accB[i]);
+                accA[i] *= __uint_as_float(wa[i]);
             }
             return 1u;
         }
@@ -276,8 +280,8 @@ scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
             for (int v = 0; v < VEC; ++v)
                 hin[v] = (h0 != nullptr && cok) ? h0[(size_t)bi * g.D + c0 + v] : 0.f;
         } else {
-            publish<VEC>(ws, u, kWordA, A, 1u);
-            publish<VEC>(ws, u, kWordB, Bc, 1u);
+            publish<VEC>(ws, u, kWordA, A);
+            publish<VEC>(ws, u, kWordB, Bc);
             float accA[VEC], accB[VEC];
 #pragma unroll
             for (int v = 0; v < VEC; ++v) { accA[v] = 1.f; accB[v] = 0.f; hin[v] = 0.f; }
@@ -297,7 +301,7 @@ scan_diag_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
         float inc[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { inc[v] = fmaf(A[v], hin[v], Bc[v]); carry[v] = hin[v]; }
-        publish<VEC>(ws, u, kWordIncl, inc, 2u);
+        publish<VEC>(ws, u, kWordIncl, inc);
     }
 #pragma unroll
     for (int v = 0; v < VEC; ++v) carry[v] = __shfl_sync(0xffffffffu, carry[v], (kSub - 1) * kCg + cg);
@@ -507,8 +511,8 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
 #pragma unroll
         for (int v = 0; v < VEC; ++v) hin[v] = 0.f;
         if (chunk != g.n_chunks - 1) {
-            publish<VEC>(ws, u, kWordA, A, 1u);
-            publish<VEC>(ws, u, kWordB, Bc, 1u);
+            publish<VEC>(ws, u, kWordA, A);
+            publish<VEC>(ws, u, kWordB, Bc);
             float accA[VEC], accB[VEC];
 #pragma unroll
             for (int v = 0; v < VEC; ++v) { accA[v] = 1.f; accB[v] = 0.f; }
@@ -525,7 +529,7 @@ scan_diag_bwd_kernel(const float *__restrict__ a, const float *__restrict__ b,
         float inc[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { inc[v] = fmaf(A[v], hin[v], Bc[v]); carry[v] = hin[v]; }
-        publish<VEC>(ws, u, kWordIncl, inc, 2u);
+        publish<VEC>(ws, u, kWordIncl, inc);
     }
 #pragma unroll
     for (int v = 0; v < VEC; ++v) carry[v] = __shfl_sync(0xffffffffu, carry[v], cg);
@@ -724,7 +728,7 @@ Plan make_plan(int64_t B, int64_t T, int64_t D, int vec) {
     p.g.n_cw = (int)((D + per_warp - 1) / per_warp);
     p.g.n_cblk = (p.g.n_cw + kWarps - 1) / kWarps;
     p.words_off = sizeof(WsHeader);
-    p.total = p.words_off + scan_units(p.g) * 12 * sizeof(unsigned long long);
+    p.total = p.words_off + scan_units(p.g) * 12 * sizeof(unsigned int);
     p.states_off = align_up(p.total, 256);
     p.total_recomp = p.states_off + (size_t)p.g.n_chunks * (size_t)B * (size_t)D * sizeof(float);
     return p;
@@ -734,7 +738,7 @@ ScanWs bind_ws(const Plan &p, void *ws) {
     char *base = static_cast<char *>(ws);
     ScanWs w;
     w.hdr = reinterpret_cast<WsHeader *>(base);
-    w.words = reinterpret_cast<unsigned long long *>(base + p.words_off);
+    w.words = reinterpret_cast<unsigned int *>(base + p.words_off);
     return w;
 }
 

@@ -151,8 +151,8 @@ int cla_scan_diag_bwd(const float *a, const float *b, const float *h0, const flo
  *    library (one per GPU that loads it, held until the process exits).  No
  *    cudaMalloc, cudaFree or other allocating call is made.
  *  - Limit: sizes whose scratch exceeds 16 MiB are rejected with
- *    CLA_ERR_UNSUPPORTED and nothing is enqueued: about 44 million elements
- *    of B*T*D when D is a multiple of 4 (8 x 4096 x 1024 fits), about 11
+ *    CLA_ERR_UNSUPPORTED and nothing is enqueued: about 89 million elements
+ *    of B*T*D when D is a multiple of 4 (8 x 4096 x 1024 fits), about 22
  *    million otherwise.
  *  - Every call looks up the array's device address (cudaGetSymbolAddress)
  *    in the current device's context; the first lookup on a device may load

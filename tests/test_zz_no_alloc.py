@@ -92,7 +92,7 @@ def test_noalloc_rejects_oversize():
         pytest.skip("no CUDA device")
     cla, f = _fn()
     x = torch.empty(4, device="cuda")
-    # 16 x 8192 x 1024 needs about 50 MB of look-back scratch
+    # 16 x 8192 x 1024 needs about 25 MB of look-back scratch
     st = f(_p(x), _p(x), None, _p(x), None, 16, 8192, 1024, None)
     assert st == 2  # CLA_ERR_UNSUPPORTED, nothing launched
     assert "static array" in cla.last_error_message()
